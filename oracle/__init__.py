@@ -1,0 +1,251 @@
+"""fp64 CPU oracle of one speculation round and of tree-masked branch attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline / reference leg may import this package.  The product
+path (the CUDA library and its Python binding) never imports it.
+
+The arithmetic lives in ``ssd_oracle.c`` (plain C99, double precision, no
+fast-math); this module compiles it with gcc and marshals numpy arrays through
+ctypes.  See the C file's header for the definitions it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libssd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+FLAG_BAD_TOKEN = 1
+FLAG_ZERO_RESIDUAL = 2
+FLAG_BAD_OUTCOME = 8
+FLAG_BAD_TREE = 16
+FLAG_BAD_BLOCK = 32
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libssd_oracle.so`` (gcc -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _L():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = ctypes.CDLL(_LIB_PATH)
+            _declare(_lib)
+    return _lib
+
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_d = ctypes.c_double
+
+
+def _declare(lib):
+    lib.oracle_fanout_split.argtypes = [_i, _i, _d, _p]
+    lib.oracle_fanout_split.restype = _i
+    lib.oracle_softmax.argtypes = [_p, _i, _d, _p]
+    lib.oracle_softmax.restype = None
+    lib.oracle_topf.argtypes = [_p, _i, _i, _p]
+    lib.oracle_topf.restype = None
+    lib.oracle_saguaro_dist.argtypes = [_p, _i, _i, _d, _d, _p, _p]
+    lib.oracle_saguaro_dist.restype = None
+    lib.oracle_inv_cdf.argtypes = [_p, _i, _d, _p]
+    lib.oracle_inv_cdf.restype = _i
+    lib.oracle_saguaro_sample.argtypes = [_p, _i, _i64, _i64, _i, _i, _i, _p, _d, _d, _p, _p, _p, _p]
+    lib.oracle_saguaro_sample.restype = _i
+    lib.oracle_verify.argtypes = ([_p, _p, _i, _i64, _i64, _i, _i, _i, _p, _d, _d, _p, _p, _p]
+                                  + [_p] * 9)
+    lib.oracle_verify.restype = _i
+    lib.oracle_predict.argtypes = [_p, _i, _i64, _i64, _i, _i, _i, _p, _d, _p, _p]
+    lib.oracle_predict.restype = _i
+    lib.oracle_lookup.argtypes = [_p, _p, _i, _i, _p, _p, _p, _p, _p, _p]
+    lib.oracle_lookup.restype = _i
+    lib.oracle_branch_attention.argtypes = [_p, _p, _p, _p, _i, _i64, _p, _p, _i, _i, _i, _i, _i,
+                                            _i, _d, _p, _p, _p]
+    lib.oracle_branch_attention.restype = _i
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _dtype_code(arr):
+    if arr.dtype == np.float32:
+        return F32
+    if arr.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"logits must be float32 or uint16 (bf16 bits), got {arr.dtype}")
+
+
+def _F(F):
+    return _c(np.asarray(F, dtype=np.int32), np.int32)
+
+
+# ---------------------------------------------------------------------------
+def fanout_split(budget: int, K: int, r: float = 0.5):
+    F = np.zeros(K + 1, np.int32)
+    rc = _L().oracle_fanout_split(int(budget), int(K), float(r), _ptr(F))
+    if rc != 0:
+        raise ValueError("invalid fan-out arguments")
+    return tuple(int(x) for x in F)
+
+
+def softmax(z, T: float):
+    z = _c(z, np.float64)
+    p = np.zeros_like(z)
+    _L().oracle_softmax(_ptr(z), z.size, float(T), _ptr(p))
+    return p
+
+
+def topf(z, F: int):
+    z = _c(z, np.float64)
+    out = np.zeros(F, np.int32)
+    _L().oracle_topf(_ptr(z), z.size, int(F), _ptr(out))
+    return out
+
+
+def saguaro_dist(z, F: int, C: float, T: float):
+    z = _c(z, np.float64)
+    qp = np.zeros_like(z)
+    ins = np.zeros(z.size, np.uint8)
+    _L().oracle_saguaro_dist(_ptr(z), z.size, int(F), float(C), float(T), _ptr(qp), _ptr(ins))
+    return qp, ins.astype(bool)
+
+
+def inv_cdf(w, u: float):
+    w = _c(w, np.float64)
+    m = np.zeros(1, np.float64)
+    i = _L().oracle_inv_cdf(_ptr(w), w.size, float(u), _ptr(m))
+    return int(i), float(m[0])
+
+
+def _strides(logits, V):
+    B, K1, W = logits.shape
+    return K1 * W, W
+
+
+def saguaro_sample(draft, V, F, C, T, u_draft):
+    """Returns (d [B,K] int32, qd [B,K] float64, margin [B,K] float64)."""
+    draft = np.ascontiguousarray(draft)
+    B, K1, _ = draft.shape
+    K = K1 - 1
+    ss, rs = _strides(draft, V)
+    d = np.zeros((B, K), np.int32)
+    qd = np.zeros((B, K), np.float64)
+    mg = np.zeros((B, K), np.float64)
+    u = _c(u_draft, np.float32)
+    _L().oracle_saguaro_sample(_ptr(draft), _dtype_code(draft), ss, rs, B, K, int(V), _ptr(_F(F)),
+                               float(C), float(T), _ptr(u), _ptr(d), _ptr(qd), _ptr(mg))
+    return d, qd, mg
+
+
+def verify(target, draft, V, F, C, T, d, u_acc, u_bonus):
+    """Returns a dict of every verification output and diagnostic."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    assert target.shape == draft.shape and target.dtype == draft.dtype
+    B, K1, _ = target.shape
+    K = K1 - 1
+    ss, rs = _strides(target, V)
+    out = dict(
+        accept_len=np.zeros(B, np.int32),
+        out_tokens=np.zeros((B, K + 1), np.int32),
+        bonus=np.zeros(B, np.int32),
+        accept_prob=np.zeros((B, K), np.float64),
+        resid_mass=np.zeros(B, np.float64),
+        flags=np.zeros(B, np.uint32),
+        acc_margin=np.zeros((B, K), np.float64),
+        bonus_margin=np.zeros(B, np.float64),
+        alpha=np.zeros((B, K), np.float64),
+    )
+    dd = _c(d, np.int32)
+    ua = _c(u_acc, np.float32)
+    ub = _c(u_bonus, np.float32)
+    _L().oracle_verify(_ptr(target), _ptr(draft), _dtype_code(target), ss, rs, B, K, int(V),
+                       _ptr(_F(F)), float(C), float(T), _ptr(dd), _ptr(ua), _ptr(ub),
+                       *[_ptr(out[k]) for k in ("accept_len", "out_tokens", "bonus", "accept_prob",
+                                                "resid_mass", "flags", "acc_margin",
+                                                "bonus_margin", "alpha")])
+    return out
+
+
+def predict(draft, V, F, T):
+    draft = np.ascontiguousarray(draft)
+    B, K1, _ = draft.shape
+    K = K1 - 1
+    ss, rs = _strides(draft, V)
+    sumF = int(sum(F))
+    guess = np.zeros((B, sumF), np.int32)
+    gq = np.zeros((B, sumF), np.float64)
+    _L().oracle_predict(_ptr(draft), _dtype_code(draft), ss, rs, B, K, int(V), _ptr(_F(F)),
+                        float(T), _ptr(guess), _ptr(gq))
+    return guess, gq
+
+
+def lookup(guess, payload, K, F, accept_len, bonus):
+    guess = _c(guess, np.int32)
+    B = guess.shape[0]
+    slot = np.zeros(B, np.int32)
+    nxt = np.zeros((B, K), np.int32)
+    flags = np.zeros(B, np.uint32)
+    pl = None if payload is None else _c(payload, np.int32)
+    hits = _L().oracle_lookup(_ptr(guess), _ptr(pl), B, int(K), _ptr(_F(F)),
+                              _ptr(_c(accept_len, np.int32)), _ptr(_c(bonus, np.int32)),
+                              _ptr(slot), _ptr(nxt), _ptr(flags))
+    return dict(slot=slot, next_tokens=nxt, hits=int(hits), flags=flags)
+
+
+def branch_attention(q, k_cache, v_cache, block_table, prefix_len, parent, Hkv, scale=None):
+    """Returns (out [B,Nq,Hq,d] float64, lse [B,Nq,Hq] float64, flags [B])."""
+    q = _c(q, np.uint16)
+    k_cache = _c(k_cache, np.uint16)
+    v_cache = _c(v_cache, np.uint16)
+    block_table = _c(block_table, np.int32)
+    parent = _c(parent, np.int32)
+    B, Nq, Hq, d = q.shape
+    N = parent.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((B, Nq, Hq, d), np.float64)
+    lse = np.zeros((B, Nq, Hq), np.float64)
+    flags = np.zeros(B, np.uint32)
+    _L().oracle_branch_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                 block_table.shape[1], k_cache.shape[0],
+                                 _ptr(_c(prefix_len, np.int32)), _ptr(parent), B, N, Nq, Hq,
+                                 int(Hkv), d, float(scale), _ptr(out), _ptr(lse), _ptr(flags))
+    return out, lse, flags
+
+
+def run_round(inp, T=None, C=None):
+    """The whole round on the oracle: sample -> verify -> predict -> lookup."""
+    spec = inp.spec
+    T = spec.T if T is None else T
+    C = spec.C if C is None else C
+    d, qd, dm = saguaro_sample(inp.draft, spec.V, spec.F, C, T, inp.u_draft)
+    v = verify(inp.target, inp.draft, spec.V, spec.F, C, T, d, inp.u_acc, inp.u_bonus)
+    guess, gq = predict(inp.draft, spec.V, spec.F, T)
+    lk = lookup(guess, inp.payload, spec.K, spec.F, v["accept_len"], v["bonus"])
+    v.update(d=d, qd=qd, draft_margin=dm, guess=guess, guess_q=gq, slot=lk["slot"],
+             next_tokens=lk["next_tokens"], hits=lk["hits"])
+    return v

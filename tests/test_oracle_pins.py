@@ -1,0 +1,559 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Every check here is independent of the oracle's own code path: known-answer
+vectors, hand-worked rational examples, closed forms, exhaustive enumeration,
+brute force on tiny inputs, and chi-squared tests of the losslessness the pages
+state (机器之心 article "全球最強推理引擎還快2倍…", section "SSD 如何實現草擬與驗證并行？":
+the scheme samples exactly from the target distribution).
+"""
+import os
+from fractions import Fraction
+from itertools import product
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_vocab_gb300 import workloads as w
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# input generator pins
+# ---------------------------------------------------------------------------
+def test_philox_known_answers():
+    for row in _golden_rows("philox4x32_10_kat.txt"):
+        v = [int(x, 16) for x in row]
+        out = w.philox4x32_10(np.array(v[:4], np.uint32), (v[4], v[5]))
+        assert [int(x) for x in out] == v[6:10]
+
+
+def test_uniforms_are_24_bit_and_in_range():
+    ud, ua, ub = w.round_uniforms(0, 0, 64, 5)
+    for u in (ud, ua, ub):
+        assert u.dtype == np.float32
+        assert np.all(u >= 0) and np.all(u < 1)
+        assert np.all((u.astype(np.float64) * 2 ** 24) == np.floor(u.astype(np.float64) * 2 ** 24))
+    # distinct slots draw distinct numbers
+    assert not np.array_equal(ud, ua)
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(1).standard_normal(100000).astype(np.float32) * 7
+    x[:4] = [1.00390625, 1.01171875, -1.00390625, 3.0]  # exact ties to even
+    mine = w.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(mine, ref)
+
+
+# ---------------------------------------------------------------------------
+# fan-out split
+# ---------------------------------------------------------------------------
+def test_fanout_golden():
+    for row in _golden_rows("fanout_split.txt"):
+        budget, K, r = int(row[0]), int(row[1]), float(row[2])
+        assert oracle.fanout_split(budget, K, r) == tuple(int(x) for x in row[3:])
+
+
+@pytest.mark.parametrize("budget,K", [(9, 4), (32, 5), (64, 4), (16, 4), (7, 6), (1000, 3), (5, 0)])
+def test_fanout_invariants(budget, K):
+    F = oracle.fanout_split(budget, K, 0.5)
+    assert len(F) == K + 1 and sum(F) == budget and min(F) >= 1
+    assert all(F[k] >= F[k + 1] for k in range(K))  # more branches at shallow depths
+    if budget >= 100 * 2 ** K:  # far from rounding, the ratio approaches 1/r
+        for k in range(K):
+            assert abs(F[k] / F[k + 1] - 2.0) < 0.05
+
+
+def test_fanout_rejects_bad_args():
+    with pytest.raises(ValueError):
+        oracle.fanout_split(3, 4, 0.5)
+    with pytest.raises(ValueError):
+        oracle.fanout_split(9, 4, 0.0)
+
+
+# ---------------------------------------------------------------------------
+# softmax / top-F / sigma_{F,C} / inverse CDF
+# ---------------------------------------------------------------------------
+def test_softmax_two_token_closed_form():
+    for T in (0.3, 1.0, 2.5):
+        for a, b in ((0.0, 1.0), (3.0, -2.0), (5.5, 5.5)):
+            p = oracle.softmax([a, b], T)
+            assert abs(p[0] - 1.0 / (1.0 + np.exp((b - a) / T))) < 1e-15
+
+
+def test_softmax_T0_is_onehot_lowest_index():
+    p = oracle.softmax([1.0, 3.0, 3.0, -1.0], 0.0)
+    assert list(p) == [0.0, 1.0, 0.0, 0.0]
+
+
+def test_topf_bruteforce_with_ties():
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        V = int(rng.integers(1, 40))
+        z = rng.integers(-3, 4, size=V).astype(np.float64)  # many ties
+        F = int(rng.integers(1, V + 1))
+        ref = sorted(range(V), key=lambda i: (-z[i], i))[:F]
+        assert list(oracle.topf(z, F)) == ref
+
+
+def test_saguaro_worked_example():
+    g = {r[0]: float(Fraction(r[1])) for r in _golden_rows("saguaro_worked_example.txt")}
+    q = np.array([g["q0"], g["q1"], g["q2"]])
+    qp, ins = oracle.saguaro_dist(np.log(q), 1, 0.5, 1.0)
+    assert list(ins) == [True, False, False]
+    assert np.allclose(qp, [g["qprime0"], g["qprime1"], g["qprime2"]], rtol=0, atol=1e-14)
+
+
+def test_saguaro_invariants():
+    rng = np.random.default_rng(7)
+    for _ in range(40):
+        V = int(rng.integers(2, 300))
+        z = rng.standard_normal(V) * 2
+        F = int(rng.integers(1, V + 1))
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        C = float(rng.choice([1.0, 0.5, 0.25, 0.01]))
+        q = oracle.softmax(z, T)
+        qp, ins = oracle.saguaro_dist(z, F, C, T)
+        assert abs(qp.sum() - 1.0) < 1e-12
+        assert ins.sum() == F
+        if C == 1.0:
+            assert np.array_equal(qp, q)
+        # ratios: inside S scaled by C relative to outside, preserved within each side
+        i_in = np.flatnonzero(ins)[0]
+        out = np.flatnonzero(~ins)
+        if out.size:
+            k = out[0]
+            assert abs((qp[i_in] / qp[k]) / (q[i_in] / q[k]) - C) < 1e-10
+        # mass on S in closed form C*s / (1 - (1-C)*s)
+        s = q[ins].sum()
+        assert abs(qp[ins].sum() - C * s / (1 - (1 - C) * s)) < 1e-12
+
+
+def test_inv_cdf_exact_frequencies():
+    wts = np.array([0, 3, 0, 5, 8, 0, 16, 32], np.float64) / 64.0
+    counts = np.zeros(8, int)
+    n = 4096
+    for k in range(n):
+        i, m = oracle.inv_cdf(wts, k / n)
+        c = np.cumsum(wts)
+        lo = c[i - 1] if i else 0.0
+        assert lo <= (k / n) * wts.sum() < c[i]
+        counts[i] += 1
+    assert np.array_equal(counts, (wts / wts.sum() * n).astype(int))
+
+
+# ---------------------------------------------------------------------------
+# verification: greedy chain, worked example, residual identity
+# ---------------------------------------------------------------------------
+def _int_logits(rng, B, K1, V):
+    return rng.integers(-4, 5, size=(B, K1, V)).astype(np.float32)
+
+
+def test_greedy_chain_at_T0():
+    rng = np.random.default_rng(11)
+    B, K, V = 200, 5, 12
+    F = (3, 2, 1, 1, 1, 1)
+    zt = _int_logits(rng, B, K + 1, V)
+    zd = zt.copy()
+    # perturb the draft on a random subset of rows so the chain breaks at random depths
+    flip = rng.random((B, K + 1)) < 0.3
+    zd[flip] = _int_logits(rng, B, K + 1, V)[flip]
+    ud, ua, ub = w.round_uniforms(3, 0, B, K)
+    d, _, _ = oracle.saguaro_sample(zd, V, F, 0.5, 0.0, ud)
+    assert np.array_equal(d, np.argmax(zd[:, :K], axis=-1))
+    v = oracle.verify(zt, zd, V, F, 0.5, 0.0, d, ua, ub)
+    tgt = np.argmax(zt, axis=-1)
+    for b in range(B):
+        a = 0
+        while a < K and d[b, a] == tgt[b, a]:
+            a += 1
+        assert v["accept_len"][b] == a
+        expect = list(d[b, :a]) + [tgt[b, a]] + [-1] * (K - a)
+        assert list(v["out_tokens"][b]) == expect
+
+
+def test_verify_worked_example():
+    g = {r[0]: float(Fraction(r[1])) for r in _golden_rows("saguaro_worked_example.txt")}
+    p = np.array([g["p0"], g["p1"], g["p2"]])
+    q = np.array([g["q0"], g["q1"], g["q2"]])
+    # K = 1: rows = positions 1 and 2; position 2 rows are irrelevant here
+    zt = np.stack([np.log(p), np.log(p)]).astype(np.float32)[None]
+    zd = np.stack([np.log(q), np.log(q)]).astype(np.float32)[None]
+    # d_1 = 1: p/q' = (1/5)/(2/5) = 1/2; u = 0.75 rejects, u = 0.25 accepts
+    rej = oracle.verify(zt, zd, 3, (1, 1), 0.5, 1.0, np.array([[1]]), np.array([[0.75]], np.float32),
+                        np.array([0.5], np.float32))
+    assert rej["accept_len"][0] == 0
+    assert abs(rej["resid_mass"][0] - g["resid_mass"]) < 1e-6  # fp32-rounded logits
+    assert rej["bonus"][0] == 2  # the residual's only mass
+    assert abs(rej["alpha"][0, 0] - g["alpha"]) < 1e-6
+    assert abs(rej["accept_prob"][0, 0] - 0.5) < 1e-6
+    acc = oracle.verify(zt, zd, 3, (1, 1), 0.5, 1.0, np.array([[1]]), np.array([[0.25]], np.float32),
+                        np.array([0.5], np.float32))
+    assert acc["accept_len"][0] == 1 and acc["out_tokens"][0, 0] == 1
+
+
+def test_residual_identity():
+    """sum max(0, p - q') = sum max(0, q' - p) = 1 - alpha at the rejected row."""
+    spec = w.RoundSpec(B=300, K=4, V=64, dtype="f32", recipe="gauss", T=0.8, C=0.5,
+                       F=(5, 3, 2, 1, 1), target_sigma=1.5, draft_noise=1.0)
+    inp = w.make_round(spec, seed=2)
+    r = oracle.run_round(inp)
+    seen = 0
+    for b in range(spec.B):
+        a = r["accept_len"][b]
+        if a == spec.K:
+            continue
+        p = oracle.softmax(inp.target[b, a].astype(np.float64), spec.T)
+        qp, _ = oracle.saguaro_dist(inp.draft[b, a].astype(np.float64), spec.F[a], spec.C, spec.T)
+        W = r["resid_mass"][b]
+        assert abs(W - np.maximum(qp - p, 0).sum()) < 1e-12
+        assert abs(W - (1 - r["alpha"][b, a])) < 1e-12
+        seen += 1
+    assert seen > 50
+
+
+def test_zero_residual_flag_when_p_equals_q():
+    spec = w.RoundSpec(B=20, K=3, V=16, dtype="f32", recipe="gauss", T=1.0, C=1.0,
+                       F=(2, 1, 1, 1), target_sigma=1.0, draft_noise=0.0)
+    inp = w.make_round(spec, seed=4)
+    d = np.zeros((spec.B, spec.K), np.int32)  # p == q', every test accepts since u < 1 = p/q'
+    v = oracle.verify(inp.target, inp.draft, spec.V, spec.F, 1.0, 1.0, d, inp.u_acc, inp.u_bonus)
+    assert np.all(v["accept_len"] == spec.K)
+    # force a rejection with an invalid draft token: the residual p - p has no mass
+    d[:, 1] = spec.V + 3
+    v = oracle.verify(inp.target, inp.draft, spec.V, spec.F, 1.0, 1.0, d, inp.u_acc, inp.u_bonus)
+    assert np.all(v["accept_len"] == 1)
+    assert np.all(v["flags"] & oracle.FLAG_ZERO_RESIDUAL)
+    assert np.all(v["flags"] & oracle.FLAG_BAD_TOKEN)
+
+
+# ---------------------------------------------------------------------------
+# losslessness (chi-squared) and exhaustive enumeration at V = 8
+# ---------------------------------------------------------------------------
+def _chi2_pvalue(counts, probs):
+    from scipy.stats import chi2
+    n = counts.sum()
+    exp = probs * n
+    keep = exp >= 5
+    c = np.append(counts[keep], counts[~keep].sum())
+    e = np.append(exp[keep], exp[~keep].sum())
+    if e[-1] < 5:
+        c, e = c[:-1], e[:-1]
+        # fold the tiny remainder into the largest cell
+        c[np.argmax(e)] += counts[~keep].sum()
+        e[np.argmax(e)] += exp[~keep].sum()
+    stat = ((c - e) ** 2 / e).sum()
+    return chi2.sf(stat, len(c) - 1)
+
+
+def _v8_rows(seed, K):
+    rng = np.random.default_rng(seed)
+    zt = (rng.standard_normal((K + 1, 8)) * 1.5).astype(np.float32)
+    zd = (zt + rng.standard_normal((K + 1, 8)) * 0.9).astype(np.float32)
+    return zt, zd
+
+
+def _broadcast_round(zt, zd, n):
+    return (np.broadcast_to(zt, (n,) + zt.shape).copy(), np.broadcast_to(zd, (n,) + zd.shape).copy())
+
+
+P_THRESHOLD = 1e-4  # pre-registered
+
+
+@pytest.mark.parametrize("C", [1.0, 0.5, 0.25])
+@pytest.mark.parametrize("T", [0.6, 1.0])
+def test_chi2_lossless_V8(C, T):
+    K, n = 3, 200_000
+    F = (3, 2, 1, 1)
+    zt, zd = _v8_rows(100, K)
+    tgt, dft = _broadcast_round(zt, zd, n)
+    ud, ua, ub = w.round_uniforms(17, int(C * 100 + T * 10), n, K)
+    d, _, _ = oracle.saguaro_sample(dft, 8, F, C, T, ud)
+    v = oracle.verify(tgt, dft, 8, F, C, T, d, ua, ub)
+    for j in range(K + 1):
+        mask = v["accept_len"] >= j
+        counts = np.bincount(v["out_tokens"][mask, j], minlength=8)
+        p = oracle.softmax(zt[j].astype(np.float64), T)
+        assert _chi2_pvalue(counts, p) > P_THRESHOLD, (j, counts, p * mask.sum())
+
+
+def test_chi2_detects_mismatched_residual():
+    """Verifying with the raw draft q (C = 1) while the draft sampled from
+    sigma_{F,1/4} must break losslessness visibly: the test has power."""
+    K, n = 3, 200_000
+    F = (3, 2, 1, 1)
+    zt, zd = _v8_rows(100, K)
+    tgt, dft = _broadcast_round(zt, zd, n)
+    ud, ua, ub = w.round_uniforms(17, 999, n, K)
+    d, _, _ = oracle.saguaro_sample(dft, 8, F, 0.25, 1.0, ud)
+    v = oracle.verify(tgt, dft, 8, F, 1.0, 1.0, d, ua, ub)
+    counts = np.bincount(v["out_tokens"][:, 0], minlength=8)
+    p = oracle.softmax(zt[0].astype(np.float64), 1.0)
+    assert _chi2_pvalue(counts, p) < 1e-12
+
+
+def _exact_outcomes(zt, zd, F, C, T):
+    """P(a, b) by enumerating all V^K draft sequences (V = 8, K = 3)."""
+    K = zt.shape[0] - 1
+    V = zt.shape[1]
+    p = [oracle.softmax(zt[j].astype(np.float64), T) for j in range(K + 1)]
+    qp = [oracle.saguaro_dist(zd[j].astype(np.float64), F[j], C, T)[0] for j in range(K)]
+    resid = []
+    for j in range(K):
+        r = np.maximum(p[j] - qp[j], 0)
+        resid.append(r / r.sum())
+    acc = [np.where(qp[j] > 0, np.minimum(1, p[j] / np.where(qp[j] > 0, qp[j], 1)), 1.0)
+           for j in range(K)]
+    Pa = np.zeros(K + 1)
+    for ds in product(range(V), repeat=K):
+        pr = np.prod([qp[j][ds[j]] for j in range(K)])
+        run = pr
+        for k in range(K):
+            Pa[k] += run * (1 - acc[k][ds[k]])
+            run *= acc[k][ds[k]]
+        Pa[K] += run
+    Pab = np.zeros((K + 1, V))
+    for k in range(K):
+        Pab[k] = Pa[k] * resid[k]
+    Pab[K] = Pa[K] * p[K]
+    alpha = [np.minimum(p[j], qp[j]).sum() for j in range(K)]
+    return Pab, Pa, alpha, p
+
+
+@pytest.mark.parametrize("C", [1.0, 0.5, 0.25])
+def test_enumeration_V8_K3(C):
+    K, n, T = 3, 200_000, 1.0
+    F = (3, 2, 1, 1)
+    zt, zd = _v8_rows(200, K)
+    Pab, Pa, alpha, p = _exact_outcomes(zt, zd, F, C, T)
+    # closed form P(a = k) = prod_{j<=k} alpha_j (1 - alpha_{k+1})
+    run = 1.0
+    for k in range(K + 1):
+        cf = run * ((1 - alpha[k]) if k < K else 1.0)
+        assert abs(Pa[k] - cf) < 1e-12
+        if k < K:
+            run *= alpha[k]
+    # the first emitted token is exactly p_1: y_1 = d_1 when a >= 1 (probability
+    # min(p, q') per token), else the residual draw
+    qp1 = oracle.saguaro_dist(zd[0].astype(np.float64), F[0], C, T)[0]
+    emitted1 = np.minimum(p[0], qp1) + Pab[0]
+    assert np.allclose(emitted1, p[0], atol=1e-12)
+    # Monte Carlo through the oracle's sample -> verify -> predict -> lookup
+    tgt, dft = _broadcast_round(zt, zd, n)
+    ud, ua, ub = w.round_uniforms(23, int(C * 100), n, K)
+    inp = w.RoundInputs(w.RoundSpec(B=n, K=K, V=8, dtype="f32", recipe="gauss", T=T, C=C, F=F),
+                        tgt, dft, ud, ua, ub, None)
+    r = oracle.run_round(inp)
+    cells = r["accept_len"] * 8 + r["bonus"]
+    counts = np.bincount(cells, minlength=(K + 1) * 8)
+    assert _chi2_pvalue(counts, Pab.reshape(-1)) > P_THRESHOLD
+    # exact hit rate: the bonus lies among the F_a guesses of depth a
+    guess = [oracle.topf(zd[k].astype(np.float64), F[k]) for k in range(K + 1)]
+    hit = sum(Pab[a, b] for a in range(K + 1) for b in guess[a])
+    mc = r["hits"] / n
+    assert abs(mc - hit) < 5 * np.sqrt(hit * (1 - hit) / n)
+
+
+# ---------------------------------------------------------------------------
+# outcome prediction and cache lookup
+# ---------------------------------------------------------------------------
+def test_predict_bruteforce():
+    rng = np.random.default_rng(9)
+    B, K, V = 6, 3, 30
+    F = (5, 3, 2, 1)
+    z = rng.integers(-3, 3, size=(B, K + 1, V)).astype(np.float32)
+    guess, gq = oracle.predict(z, V, F, 1.0)
+    for b in range(B):
+        off = 0
+        for k in range(K + 1):
+            ref = sorted(range(V), key=lambda i: (-z[b, k, i], i))[:F[k]]
+            assert list(guess[b, off:off + F[k]]) == ref
+            e = np.exp(z[b, k].astype(np.float64) - z[b, k].max())
+            assert np.allclose(gq[b, off:off + F[k]], e[ref] / e.sum(), rtol=1e-13)
+            off += F[k]
+
+
+def test_lookup_bruteforce():
+    rng = np.random.default_rng(10)
+    B, K, V = 500, 4, 10
+    F = (4, 2, 1, 1, 1)
+    sumF = sum(F)
+    guess = rng.integers(0, V, size=(B, sumF)).astype(np.int32)
+    payload = rng.integers(0, 1000, size=(B, sumF, K)).astype(np.int32)
+    a = rng.integers(-1, K + 2, size=B).astype(np.int32)  # includes out-of-range outcomes
+    bon = rng.integers(0, V, size=B).astype(np.int32)
+    r = oracle.lookup(guess, payload, K, F, a, bon)
+    offs = np.concatenate([[0], np.cumsum(F)])
+    hits = 0
+    for b in range(B):
+        if a[b] < 0 or a[b] > K:
+            assert r["slot"][b] == -1 and r["flags"][b] & oracle.FLAG_BAD_OUTCOME
+            continue
+        cand = [offs[a[b]] + i for i in range(F[a[b]]) if guess[b, offs[a[b]] + i] == bon[b]]
+        s = cand[0] if cand else -1
+        assert r["slot"][b] == s
+        if s >= 0:
+            hits += 1
+            assert list(r["next_tokens"][b]) == list(payload[b, s])
+        else:
+            assert list(r["next_tokens"][b]) == [-1] * K
+    assert r["hits"] == hits
+
+
+# ---------------------------------------------------------------------------
+# branch attention
+# ---------------------------------------------------------------------------
+def _bf(x):
+    return w.bf16_bits_to_f32(x).astype(np.float64)
+
+
+def _dense_reference(inp, mask_fn):
+    """Dense attention over contiguous K/V gathered through the block table,
+    with an explicit boolean mask from ``mask_fn(b, query_node)``."""
+    s = inp.spec
+    B, Nq, Hq, d = inp.q.shape
+    group = Hq // s.Hkv
+    out = np.zeros((B, Nq, Hq, d))
+    lse = np.zeros((B, Nq, Hq))
+    for b in range(B):
+        L = int(inp.prefix_len[b])
+        npos = L + inp.N
+        blk = inp.block_table[b, np.arange(npos) // w.PAGE]
+        Kc = _bf(inp.k_cache[blk, :, np.arange(npos) % w.PAGE, :])  # [npos, Hkv, d]
+        Vc = _bf(inp.v_cache[blk, :, np.arange(npos) % w.PAGE, :])
+        for qi in range(Nq):
+            node = inp.N - Nq + qi
+            mask = mask_fn(b, node)  # [npos] bool
+            for h in range(Hq):
+                qv = _bf(inp.q[b, qi, h])
+                sc = Kc[:, h // group, :] @ qv / np.sqrt(d)
+                sc = np.where(mask, sc, -np.inf)
+                m = sc.max()
+                e = np.exp(sc - m)
+                out[b, qi, h] = e @ Vc[:, h // group, :] / e.sum()
+                lse[b, qi, h] = m + np.log(e.sum())
+    return out, lse
+
+
+def test_attention_single_key_returns_v():
+    spec = w.AttnSpec(B=2, Hq=4, Hkv=2, d=16, L=0, tree="chain", n_chain=1)
+    inp = w.make_attention(spec, seed=1)
+    out, lse, fl = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                           inp.prefix_len, inp.parent, spec.Hkv)
+    for b in range(2):
+        blk = inp.block_table[b, 0]
+        for h in range(4):
+            assert np.array_equal(out[b, 0, h], _bf(inp.v_cache[blk, h // 2, 0]))
+            qk = _bf(inp.q[b, 0, h]) @ _bf(inp.k_cache[blk, h // 2, 0])
+            assert abs(lse[b, 0, h] - qk / 4.0) < 1e-12
+
+
+def test_attention_equal_keys_average_visible_values():
+    spec = w.AttnSpec(B=2, Hq=2, Hkv=1, d=8, L=37, tree="fanout", K=2, F=(2, 1, 1), chain_len=3)
+    inp = w.make_attention(spec, seed=2)
+    inp.k_cache[...] = inp.k_cache[0, 0, 0]  # every key identical -> uniform weights
+    out, lse, _ = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                          inp.prefix_len, inp.parent, spec.Hkv)
+    parent = inp.parent[0]
+    for b in range(2):
+        L = int(inp.prefix_len[b])
+        for qi in range(inp.Nq):
+            node = inp.N - inp.Nq + qi
+            vis = list(range(L))
+            m = node
+            path = []
+            while m >= 0:
+                path.append(m)
+                m = parent[m]
+            vis += [L + n for n in sorted(path)]
+            blk = inp.block_table[b, np.array(vis) // 16]
+            vals = _bf(inp.v_cache[blk, 0, np.array(vis) % 16])
+            assert np.allclose(out[b, qi, 0], vals.mean(axis=0), atol=1e-12)
+            sc = _bf(inp.q[b, qi, 0]) @ _bf(inp.k_cache[0, 0, 0]) / np.sqrt(8)
+            assert abs(lse[b, qi, 0] - (sc + np.log(len(vis)))) < 1e-10
+
+
+def test_attention_chain_is_causal():
+    spec = w.AttnSpec(B=3, Hq=4, Hkv=2, d=32, L=45, tree="chain", n_chain=6, ragged_prefix=True)
+    inp = w.make_attention(spec, seed=3)
+    out, lse, fl = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                           inp.prefix_len, inp.parent, spec.Hkv)
+
+    def causal(b, node):
+        L = int(inp.prefix_len[b])
+        return np.arange(L + inp.N) <= L + node
+
+    ref, rlse = _dense_reference(inp, causal)
+    assert np.allclose(out, ref, atol=1e-12) and np.allclose(lse, rlse, atol=1e-12)
+    assert not fl.any()
+
+
+def test_attention_tree_matches_transitive_closure_mask():
+    spec = w.AttnSpec(B=2, Hq=8, Hkv=2, d=16, L=21, tree="fanout", K=3, F=(3, 2, 1, 1),
+                      chain_len=3, ragged_chains=True, ragged_prefix=True)
+    inp = w.make_attention(spec, seed=4)
+    out, lse, _ = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                          inp.prefix_len, inp.parent, spec.Hkv)
+    N = inp.N
+    A = np.zeros((N, N), bool)  # A[i, j]: j is the parent of i
+    for i, pi in enumerate(inp.parent[0]):
+        if pi >= 0:
+            A[i, pi] = True
+    R = np.eye(N, dtype=bool)
+    for _ in range(N):
+        R = R | (R.astype(int) @ A.astype(int) > 0)
+
+    def closure(b, node):
+        L = int(inp.prefix_len[b])
+        m = np.zeros(L + N, bool)
+        m[:L] = True
+        m[L:] = R[node]
+        return m
+
+    ref, rlse = _dense_reference(inp, closure)
+    assert np.allclose(out, ref, atol=1e-12) and np.allclose(lse, rlse, atol=1e-12)
+
+
+def test_attention_independent_of_block_placement():
+    spec = w.AttnSpec(B=2, Hq=4, Hkv=4, d=16, L=50, tree="fanout", K=2, F=(2, 1, 1), chain_len=2)
+    inp = w.make_attention(spec, seed=5)
+    o1, l1, _ = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                        inp.prefix_len, inp.parent, spec.Hkv)
+    # move every block to a new physical slot
+    nb = inp.k_cache.shape[0]
+    perm = np.random.default_rng(0).permutation(nb)
+    k2 = np.empty_like(inp.k_cache)
+    v2 = np.empty_like(inp.v_cache)
+    k2[perm] = inp.k_cache
+    v2[perm] = inp.v_cache
+    t2 = np.where(inp.block_table >= 0, perm[np.maximum(inp.block_table, 0)], -1).astype(np.int32)
+    o2, l2, _ = oracle.branch_attention(inp.q, k2, v2, t2, inp.prefix_len, inp.parent, spec.Hkv)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_attention_flags_bad_tree_and_block():
+    spec = w.AttnSpec(B=1, Hq=2, Hkv=1, d=8, L=20, tree="chain", n_chain=4)
+    inp = w.make_attention(spec, seed=6)
+    par = inp.parent.copy()
+    par[0, 2] = 3  # a parent after the node: invalid
+    _, _, fl = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                       inp.prefix_len, par, spec.Hkv)
+    assert fl[0] & oracle.FLAG_BAD_TREE
+    tab = inp.block_table.copy()
+    tab[0, 0] = 10 ** 6
+    _, _, fl = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, tab, inp.prefix_len,
+                                       inp.parent, spec.Hkv)
+    assert fl[0] & oracle.FLAG_BAD_BLOCK
