@@ -1,0 +1,215 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) speculation-round library.
+ *
+ * One batched round of speculative-speculative decoding with the Saguaro
+ * algorithm, as the following web pages describe it:
+ *   [A] 機器之心 article "全球最強推理引擎還快2倍，斯坦福、普林斯頓破解大模型串行魔咒",
+ *       section "SSD 如何實現草擬與驗證并行？".
+ *   [B] technical summary "超越传统SD：SSD框架全异步解码实现4.7倍平均加速",
+ *       sections "投机解码的瓶颈与 SSD 的核心机制", "Saguaro 算法：解决异步推测的三大挑战"
+ *       (part 1 "验证结果预测与缓存拓扑优化", part 2 "操纵残差分布") and
+ *       "工程优化与系统表现".
+ * The pages' formulas did not survive extraction; where a call fills a gap
+ * the reading is stated at the call.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.   Every pointer is caller-owned DEVICE memory unless marked "host".
+ *           The library allocates nothing: calls that need scratch take a
+ *           caller-provided workspace `ws` of at least the size the matching
+ *           *_workspace_size() call returns.
+ * Streams.  Every call only enqueues work on stream `s` (0 = legacy default)
+ *           and returns without synchronising.
+ * Errors.   Arguments that can be checked on the host are checked before any
+ *           launch; a failed check returns SSD_ERR_INVALID_ARG (meaningless
+ *           argument), SSD_ERR_UNSUPPORTED (valid but outside the supported
+ *           shapes/alignments) or SSD_ERR_WORKSPACE (workspace too small) and
+ *           launches nothing.  A launch failure returns SSD_ERR_CUDA.  Data
+ *           problems only the device can see set bits (SSD_FLAG_*) in the
+ *           caller's `status` word with an atomic OR and take the documented
+ *           path; no kernel traps or asserts.  The library never clears
+ *           `status`: the caller zeroes it before the calls it wants to watch.
+ * Logits.   [B, K+1, V] per tensor, element (b, r, i) at
+ *           base + b*seq_stride + r*row_stride + i (strides in elements);
+ *           row r holds position j = r + 1.  dtype fp32 or bf16.  The base
+ *           address and both strides (in bytes) must be multiples of 16;
+ *           V may be any positive size.  Supported: 0 <= K <= 16,
+ *           0 <= F_k <= min(V, 256), 1 <= V, and a per-row candidate budget
+ *           (ceil(V*elem / 32 KiB) * max F_k <= 8192).
+ * Temperature T >= 0; T = 0 is the greedy limit (one-hot distributions at the
+ *           argmax, lowest index on ties).  Saguaro's C must lie in (0, 1].
+ * Uniforms  are inputs (the caller draws them, e.g. from a counter-based
+ *           generator); each must lie in [0, 1).
+ * Draws     use the inverse CDF in vocabulary order: the smallest i with
+ *           sum_{k<=i} w_k > u * sum_k w_k.
+ * Ties      between equal logits rank the lower index first (argmax, top-F).
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssd_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1,
+  SSD_ERR_UNSUPPORTED = 2,
+  SSD_ERR_WORKSPACE = 3,
+  SSD_ERR_CUDA = 4
+} ssd_status_t;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
+
+/* status-word bits (device uint32[1], OR-ed by kernels) */
+#define SSD_FLAG_BAD_TOKEN 1u     /* a draft token outside [0, V): that test rejects       */
+#define SSD_FLAG_ZERO_RESIDUAL 2u /* residual without mass: the bonus is drawn from p_{a+1} */
+#define SSD_FLAG_WAIT_TIMEOUT 4u  /* a bounded on-device wait gave up; outputs are invalid  */
+#define SSD_FLAG_BAD_OUTCOME 8u   /* lookup: accept count outside [0, K]: treated as a miss */
+#define SSD_FLAG_BAD_TREE 16u     /* attention: parent[m] outside [-1, m-1]: path ends there */
+#define SSD_FLAG_BAD_BLOCK 32u    /* attention: block id outside [0, num_blocks): keys hidden */
+
+/* Human-readable name of a status code (static string). */
+const char *ssd_status_string(ssd_status_t st);
+
+/*
+ * Fan-out split of a speculation budget over depths k = 0..K [B, part 1: the
+ * optimal F_k follows a truncated geometric series; more branches at shallow
+ * depths].  Reading: weights r^k, F_k = max(1, floor(budget r^k / sum_j r^j));
+ * a shortfall is handed out one unit at a time by descending fractional part
+ * (ties: smaller k), an excess taken from the largest F_k > 1 (ties: larger k).
+ * budget >= K+1, 0 < r <= 1, 0 <= K <= 16.  F_out: host int32[K+1].
+ * Host-only; returns SSD_ERR_INVALID_ARG on bad arguments.
+ */
+ssd_status_t ssd_fanout_split(int budget, int K, double r, int32_t *F_out);
+
+/*
+ * Workspace bytes the vocabulary calls (ssd_saguaro_sample, ssd_verify,
+ * ssd_predict_outcomes, ssd_round) need for B sequences of K+1 rows of V
+ * logits of type dt with fan-out F (host int32[K+1]).  Returns 0 for
+ * unsupported arguments.
+ */
+size_t ssd_workspace_size(int B, int K, int V, ssd_dtype_t dt, const int32_t *F);
+
+/*
+ * Saguaro draft sampling sigma_{F,C} [B, part 2 "操纵残差分布": the draft's
+ * most likely tokens are down-weighted by C so that, when C shrinks, the
+ * residual puts more mass on them and the bonus token tends to land in the
+ * cache].  Reading: for position j = 1..K, S_j = the top-F_{j-1} tokens of
+ * draft row j by raw logit; q_j = softmax(z^d_j / T);
+ *   q'_j(i) = q_j(i) c_i / (1 - (1 - C) sum_{k in S_j} q_j(k)),  c_i = C on S_j, 1 off it;
+ *   d_j = inverse-CDF draw from q'_j with u_draft[b, j-1].
+ * draft: logits as above (rows 0..K-1 are read).  u_draft: [B, K] fp32.
+ * d_out: [B, K] int32.  qd_out: [B, K] fp32 = q'_j(d_j), or NULL.
+ */
+ssd_status_t ssd_saguaro_sample(const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                                int64_t row_stride, int B, int K, int V, const int32_t *F,
+                                float C, float T, const float *u_draft, int32_t *d_out,
+                                float *qd_out, uint32_t *status, void *ws, size_t ws_bytes,
+                                ssd_stream_t s);
+
+/*
+ * Lossless verification of K draft tokens per sequence [A: the target checks
+ * the K draft tokens in one parallel pass, accepts a prefix of them and
+ * samples one bonus token after the accepted ones, so the output follows the
+ * target distribution exactly; B: the residual distribution "p_target -
+ * p_draft"].  Reading: p_j = softmax(z^t_j / T); q'_j = sigma_{F_{j-1},C}(q_j)
+ * (the distribution the draft sampled from, see ssd_saguaro_sample);
+ *   for j = 1..K: accept d_j iff u_acc[b, j-1] * q'_j(d_j) < p_j(d_j);
+ *   stop at the first rejection; a = number accepted;
+ *   a < K: bonus ~ max(0, p_{a+1} - q'_{a+1}) renormalised (u_bonus[b]); a
+ *          residual without mass draws from p_{a+1} and sets ZERO_RESIDUAL;
+ *   a = K: bonus ~ p_{K+1}.
+ * target, draft: logits (same dtype and strides).  d: [B, K] int32 (an id
+ * outside [0, V) sets BAD_TOKEN and rejects).  u_acc: [B, K]; u_bonus: [B].
+ * Outputs: accept_len [B]; out_tokens [B, K+1] = d_1..d_a, bonus, then -1;
+ * bonus [B]; accept_prob [B, K] = P(u q' < p) = min(1, p/q') for every j (1
+ * when q' = 0 < p, 0 when p = q' = 0 or d_j is invalid), or NULL; resid_mass
+ * [B] = total mass of the residual used (1 after full acceptance), or NULL.
+ */
+ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                        int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                        const int32_t *d, const float *u_acc, const float *u_bonus,
+                        int32_t *accept_len, int32_t *out_tokens, int32_t *bonus,
+                        float *accept_prob, float *resid_mass, uint32_t *status, void *ws,
+                        size_t ws_bytes, ssd_stream_t s);
+
+/*
+ * Verification-outcome prediction [A: the draft predicts the bonus token from
+ * its most likely logits; B part 1: the outcome space has ~V^K points, so a
+ * budget is spread as fan-out F_k over depths].  For depth k = 0..K the guesses
+ * are the top-F_k tokens of draft row k+1 (value descending, index ascending):
+ * guess[b, off_k + i], off_k = F_0 + ... + F_{k-1}; guess_q = q_{k+1} of each
+ * guess (softmax(z / T); one-hot at T = 0), or NULL.
+ */
+ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                                  int64_t row_stride, int B, int K, int V, const int32_t *F,
+                                  float T, int32_t *guess, float *guess_q, uint32_t *status,
+                                  void *ws, size_t ws_bytes, ssd_stream_t s);
+
+/*
+ * Speculation-cache lookup keyed by the verification outcome (a, b) [B,
+ * "投机解码的瓶颈与 SSD 的核心机制": once verification returns, one cache lookup
+ * decides whether pre-speculated tokens are ready].  Hit iff bonus b is among
+ * the F_a guesses of depth a: slot[b] = off_a + rank, else -1.  next_tokens
+ * [B, K] = payload[b, slot, 0..K-1] on a hit and -1 on a miss (NULL to skip;
+ * payload [B, sumF, K] may then be NULL).  hits[0] = number of hits (written,
+ * not accumulated).  An accept count outside [0, K] is a miss (BAD_OUTCOME).
+ */
+ssd_status_t ssd_cache_lookup(const int32_t *guess, const int32_t *payload, int B, int K,
+                              const int32_t *F, const int32_t *accept_len, const int32_t *bonus,
+                              int32_t *slot, int32_t *next_tokens, uint32_t *hits,
+                              uint32_t *status, ssd_stream_t s);
+
+/*
+ * The whole round in one call: Saguaro sampling of d_1..d_K, verification,
+ * outcome prediction and cache lookup, with every logit row read from HBM
+ * once.  Equivalent to ssd_saguaro_sample -> ssd_verify ->
+ * ssd_predict_outcomes -> ssd_cache_lookup on the same arguments; every
+ * output pointer except the required d_out, accept_len, out_tokens, bonus may
+ * be NULL (guess is needed when slot, next_tokens or hits is given).
+ */
+ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                       int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                       const float *u_draft, const float *u_acc, const float *u_bonus,
+                       const int32_t *payload, int32_t *d_out, float *qd_out, int32_t *accept_len,
+                       int32_t *out_tokens, int32_t *bonus, float *accept_prob, float *resid_mass,
+                       int32_t *guess, float *guess_q, int32_t *slot, int32_t *next_tokens,
+                       uint32_t *hits, uint32_t *status, void *ws, size_t ws_bytes,
+                       ssd_stream_t s);
+
+/*
+ * Tree-masked decode attention over a paged bf16 KV cache, so that the draft
+ * decodes every branch of the speculation tree in one forward pass [B,
+ * "工程优化与系统表现": a custom sparse attention mask].
+ *   q [B, Nq, Hq, d] bf16; k_cache, v_cache [num_blocks, Hkv, 16, d] bf16
+ *   (a block holds 16 consecutive positions of one KV head); block_table
+ *   [B, maxb] int32; prefix_len [B] int32; parent [B, N] int32 (-1 = the
+ *   prefix end).  Node m of sequence b sits at logical position
+ *   prefix_len[b] + m (its K/V already in the cache); query row i is node
+ *   N - Nq + i.  Row i of head h attends to every prefix position and to the
+ *   nodes on its ancestor-or-self path, reading KV head h / (Hq / Hkv):
+ *     out = softmax(scale * q k^T + mask) v   (fp32 accumulation, bf16 out),
+ *     lse = natural log-sum-exp of the visible scores (fp32 [B, Nq, Hq], or NULL).
+ * Supported: d in {64, 128}, Hq % Hkv == 0, Hq / Hkv <= 16, 1 <= Nq <= N <= 128,
+ * prefix_len[b] + N <= 16 * maxb.  parent[m] outside [-1, m-1] ends the path
+ * (BAD_TREE); a block id outside [0, num_blocks) hides its keys (BAD_BLOCK).
+ */
+size_t ssd_attention_workspace_size(int B, int Nq, int Hq, int Hkv, int d, int max_prefix);
+ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_table, int maxb, int64_t num_blocks,
+                                  const int32_t *prefix_len, const int32_t *parent, int B, int N,
+                                  int Nq, int Hq, int Hkv, int d, float scale, void *out,
+                                  float *lse, uint32_t *status, void *ws, size_t ws_bytes,
+                                  ssd_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

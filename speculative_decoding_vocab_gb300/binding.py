@@ -1,0 +1,236 @@
+"""Thin Python binding of the C ABI in include/ssd.h (argument marshalling only).
+
+Each function has the name of the C call it wraps and takes torch CUDA
+tensors; it checks dtypes, derives sizes and strides, passes raw device
+pointers and the current (or given) CUDA stream, and turns a non-zero status
+into an exception.  Every step of the round runs in the library's kernels:
+there is no fallback path, and a missing library raises at load time.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA = range(5)
+SSD_F32, SSD_BF16 = 0, 1
+FLAG_BAD_TOKEN = 1
+FLAG_ZERO_RESIDUAL = 2
+FLAG_WAIT_TIMEOUT = 4
+FLAG_BAD_OUTCOME = 8
+FLAG_BAD_TREE = 16
+FLAG_BAD_BLOCK = 32
+
+EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_saguaro_sample",
+           "ssd_verify", "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round",
+           "ssd_attention_workspace_size", "ssd_branch_attention")
+
+_lib = None
+
+
+class SSDError(RuntimeError):
+    def __init__(self, call, code, msg):
+        super().__init__(f"{call} failed: {msg} (status {code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libssd_gb300.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"the CUDA library {p} is not built; run __graft_entry__.build() "
+                           "(or python -m speculative_decoding_vocab_gb300.build) first")
+    lib = ctypes.CDLL(p)
+    _declare(lib)
+    if path is None:
+        _lib = lib
+    return lib
+
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+_d = ctypes.c_double
+_sz = ctypes.c_size_t
+
+
+def _declare(lib):
+    lib.ssd_status_string.argtypes = [_i]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_fanout_split.argtypes = [_i, _i, _d, _vp]
+    lib.ssd_fanout_split.restype = _i
+    lib.ssd_workspace_size.argtypes = [_i, _i, _i, _i, _vp]
+    lib.ssd_workspace_size.restype = _sz
+    lib.ssd_saguaro_sample.argtypes = [_vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp,
+                                       _vp, _vp, _sz, _vp]
+    lib.ssd_saguaro_sample.restype = _i
+    lib.ssd_verify.argtypes = [_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.ssd_verify.restype = _i
+    lib.ssd_predict_outcomes.argtypes = [_vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _vp, _vp, _vp,
+                                         _vp, _sz, _vp]
+    lib.ssd_predict_outcomes.restype = _i
+    lib.ssd_cache_lookup.argtypes = [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.ssd_cache_lookup.restype = _i
+    lib.ssd_round.argtypes = ([_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp, _vp]
+                              + [_vp] * 13 + [_vp, _sz, _vp])
+    lib.ssd_round.restype = _i
+    lib.ssd_attention_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+    lib.ssd_attention_workspace_size.restype = _sz
+    lib.ssd_branch_attention.argtypes = [_vp, _vp, _vp, _vp, _i, _i64, _vp, _vp, _i, _i, _i, _i, _i,
+                                         _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.ssd_branch_attention.restype = _i
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must live on a CUDA device")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(call, code):
+    if code != SSD_OK:
+        msg = load().ssd_status_string(code).decode()
+        raise SSDError(call, code, msg)
+
+
+def _host_F(F):
+    arr = (ctypes.c_int32 * len(F))(*[int(x) for x in F])
+    return arr
+
+
+def _logit_meta(x: torch.Tensor):
+    if x.dim() != 3 or x.stride(2) != 1:
+        raise ValueError("logits must be [B, K+1, V'] with unit stride on the last dim")
+    if x.dtype == torch.float32:
+        dt = SSD_F32
+    elif x.dtype == torch.bfloat16:
+        dt = SSD_BF16
+    else:
+        raise ValueError(f"logits must be float32 or bfloat16, got {x.dtype}")
+    return dt, x.stride(0), x.stride(1)
+
+
+def _dtype_code(dtype) -> int:
+    return SSD_F32 if dtype in (torch.float32, "f32") else SSD_BF16
+
+
+# ---------------------------------------------------------------------------
+# the calls
+# ---------------------------------------------------------------------------
+def ssd_fanout_split(budget: int, K: int, r: float = 0.5):
+    F = (ctypes.c_int32 * (K + 1))()
+    _check("ssd_fanout_split", load().ssd_fanout_split(int(budget), int(K), float(r), F))
+    return tuple(int(x) for x in F)
+
+
+def ssd_workspace_size(B: int, K: int, V: int, dtype, F) -> int:
+    return int(load().ssd_workspace_size(int(B), int(K), int(V), _dtype_code(dtype), _host_F(F)))
+
+
+def workspace(B, K, V, dtype, F, device="cuda") -> torch.Tensor:
+    n = ssd_workspace_size(B, K, V, dtype, F)
+    if n == 0 and B > 0:
+        raise SSDError("ssd_workspace_size", SSD_ERR_UNSUPPORTED, "unsupported shape")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def ssd_saguaro_sample(draft, V, F, C, T, u_draft, d_out, qd_out=None, status=None, ws=None,
+                       stream=None):
+    dt, ss, rs = _logit_meta(draft)
+    B, K1 = draft.shape[0], draft.shape[1]
+    _check("ssd_saguaro_sample", load().ssd_saguaro_sample(
+        _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T), _ptr(u_draft),
+        _ptr(d_out), _ptr(qd_out), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
+
+
+def ssd_verify(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tokens, bonus,
+               accept_prob=None, resid_mass=None, status=None, ws=None, stream=None):
+    dt, ss, rs = _logit_meta(target)
+    if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
+        raise ValueError("target and draft logits must share dtype, shape and strides")
+    B, K1 = target.shape[0], target.shape[1]
+    _check("ssd_verify", load().ssd_verify(
+        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
+        _ptr(accept_prob), _ptr(resid_mass), _ptr(status), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_predict_outcomes(draft, V, F, T, guess, guess_q=None, status=None, ws=None, stream=None):
+    dt, ss, rs = _logit_meta(draft)
+    B, K1 = draft.shape[0], draft.shape[1]
+    _check("ssd_predict_outcomes", load().ssd_predict_outcomes(
+        _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(T), _ptr(guess),
+        _ptr(guess_q), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_cache_lookup(guess, payload, K, F, accept_len, bonus, slot, next_tokens=None, hits=None,
+                     status=None, stream=None):
+    B = guess.shape[0]
+    _check("ssd_cache_lookup", load().ssd_cache_lookup(
+        _ptr(guess), _ptr(payload), B, int(K), _host_F(F), _ptr(accept_len), _ptr(bonus),
+        _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(status), _stream(stream)))
+
+
+def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_len, out_tokens,
+              bonus, payload=None, qd_out=None, accept_prob=None, resid_mass=None, guess=None,
+              guess_q=None, slot=None, next_tokens=None, hits=None, status=None, ws=None,
+              stream=None):
+    dt, ss, rs = _logit_meta(target)
+    if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
+        raise ValueError("target and draft logits must share dtype, shape and strides")
+    B, K1 = target.shape[0], target.shape[1]
+    _check("ssd_round", load().ssd_round(
+        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(u_draft), _ptr(u_acc), _ptr(u_bonus), _ptr(payload), _ptr(d_out), _ptr(qd_out),
+        _ptr(accept_len), _ptr(out_tokens), _ptr(bonus), _ptr(accept_prob), _ptr(resid_mass),
+        _ptr(guess), _ptr(guess_q), _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(status),
+        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_attention_workspace_size(B, Nq, Hq, Hkv, d, max_prefix) -> int:
+    return int(load().ssd_attention_workspace_size(int(B), int(Nq), int(Hq), int(Hkv), int(d),
+                                                   int(max_prefix)))
+
+
+def ssd_branch_attention(q, k_cache, v_cache, block_table, prefix_len, parent, out, lse=None,
+                         scale=None, status=None, ws=None, stream=None):
+    if q.dtype != torch.bfloat16 or k_cache.dtype != torch.bfloat16 or v_cache.dtype != torch.bfloat16:
+        raise ValueError("q, k_cache and v_cache must be bfloat16")
+    for t in (q, k_cache, v_cache, out):
+        if not t.is_contiguous():
+            raise ValueError("q, k_cache, v_cache and out must be contiguous")
+    B, Nq, Hq, d = q.shape
+    nb, Hkv, page, d2 = k_cache.shape
+    if page != 16 or d2 != d:
+        raise ValueError("k_cache must be [num_blocks, Hkv, 16, d]")
+    N = parent.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    _check("ssd_branch_attention", load().ssd_branch_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], nb,
+        _ptr(prefix_len), _ptr(parent), B, N, Nq, Hq, Hkv, d, float(scale), _ptr(out), _ptr(lse),
+        _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))

@@ -102,10 +102,27 @@ def round_uniforms(seed: int, rnd: int, B: int, K: int):
 # bf16 helpers (bit-level, round-to-nearest-even)
 # ---------------------------------------------------------------------------
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bfloat16 (nearest, ties to even); returns the uint16 bits."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    return rounded.astype(np.uint16)
+    """Round finite float32 to bfloat16 (nearest, ties to even); returns the uint16 bits.
+
+    +-inf map to +-inf; NaN inputs are not supported.
+    """
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    inf = (b & np.uint32(0x7FFFFFFF)) == np.uint32(0x7F800000)
+    rounded = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    out = rounded.astype(np.uint16)
+    if inf.any():
+        out[inf] = (b[inf] >> np.uint32(16)).astype(np.uint16)
+    return out
+
+
+def _bf16_normals(rng, shape, chunk=1 << 24) -> np.ndarray:
+    """bf16 bits of N(0, 1) draws, generated in bounded chunks."""
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+    for o in range(0, n, chunk):
+        m = min(chunk, n - o)
+        out[o:o + m] = f32_to_bf16_bits(rng.standard_normal(m, dtype=np.float32))
+    return out.reshape(shape)
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
@@ -343,9 +360,9 @@ def make_attention(spec: AttnSpec, seed: int = 0, values: str = "normal") -> Att
         o += nblk[b]
     shape_kv = (nb, spec.Hkv, PAGE, spec.d)
     if values == "normal":
-        q = f32_to_bf16_bits(rng.standard_normal((B, Nq, spec.Hq, spec.d), dtype=np.float32))
-        kc = f32_to_bf16_bits(rng.standard_normal(shape_kv, dtype=np.float32))
-        vc = f32_to_bf16_bits(rng.standard_normal(shape_kv, dtype=np.float32))
+        q = _bf16_normals(rng, (B, Nq, spec.Hq, spec.d))
+        kc = _bf16_normals(rng, shape_kv)
+        vc = _bf16_normals(rng, shape_kv)
     else:
         raise ValueError(values)
     parent = np.broadcast_to(parent1, (B, N)).copy()

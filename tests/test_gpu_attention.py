@@ -1,0 +1,95 @@
+"""GPU parity of tree-masked branch attention against the fp64 oracle
+(outputs within 2e-2 absolute in bf16, log-sum-exp within 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_vocab_gb300 import binding as ssd
+from speculative_decoding_vocab_gb300 import workloads as w
+
+from parity import gpu_attention, to_dev
+
+pytestmark = pytest.mark.gpu
+ATOL = 2e-2
+LSE_ATOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from speculative_decoding_vocab_gb300 import build
+    build.build()
+    ssd.load()
+
+
+def _check(ai, seqs=None):
+    out, lse, st = gpu_attention(ai)
+    idx = np.arange(ai.spec.B) if seqs is None else np.asarray(seqs)
+    ref, rlse, fl = oracle.branch_attention(ai.q[idx], ai.k_cache, ai.v_cache, ai.block_table[idx],
+                                            ai.prefix_len[idx], ai.parent[idx], ai.spec.Hkv)
+    err = np.abs(out[idx] - ref).max()
+    lerr = np.abs(lse[idx] - rlse).max()
+    assert err <= ATOL, f"max abs error {err}"
+    assert lerr <= LSE_ATOL, f"lse max abs error {lerr}"
+    assert st == 0
+    return err
+
+
+@pytest.mark.parametrize("spec", [
+    w.AttnSpec(B=3, Hq=8, Hkv=2, d=64, L=100, tree="fanout", K=3, F=(3, 2, 1, 1), chain_len=4),
+    w.AttnSpec(B=3, Hq=16, Hkv=1, d=128, L=77, tree="chain", n_chain=6, ragged_prefix=True),
+    w.AttnSpec(B=2, Hq=4, Hkv=4, d=64, L=33, tree="fanout", K=4, F=(8, 4, 2, 1, 1), chain_len=4,
+               ragged_chains=True, ragged_prefix=True),
+    w.AttnSpec(B=2, Hq=8, Hkv=8, d=128, L=1, tree="fanout", K=2, F=(2, 1, 1), chain_len=2),
+    w.AttnSpec(B=1, Hq=32, Hkv=2, d=64, L=0, tree="chain", n_chain=1),   # no prefix, one node
+    w.AttnSpec(B=2, Hq=8, Hkv=1, d=128, L=500, tree="fanout", K=4, F=(20, 4, 2, 1, 1),
+               chain_len=4),                                              # N = 116 nodes
+], ids=["gqa4-d64", "gqa16-d128-chain", "ragged", "mha-d128", "single-node", "wide-tree"])
+def test_small_shapes(spec):
+    _check(w.make_attention(spec, seed=11))
+
+
+def test_draft_branch_attention_full():
+    ai = w.make_attention(w.draft_branch_attention(), seed=0)
+    _check(ai, seqs=[0, 5, 15])
+
+
+def test_verify_attention_at_scale_sampled():
+    """Full-size verify-shaped attention (B=64, L=8192, d=128); the oracle checks
+    a sample of sequences."""
+    spec = w.verify_attention_at_scale()
+    ai = w.make_attention(spec, seed=0)
+    _check(ai, seqs=[0, 63])
+
+
+def test_flags_bad_tree_and_block():
+    spec = w.AttnSpec(B=1, Hq=4, Hkv=2, d=64, L=40, tree="chain", n_chain=4)
+    ai = w.make_attention(spec, seed=3)
+    ai.parent[0, 2] = 3
+    _, _, st = gpu_attention(ai)
+    assert st & ssd.FLAG_BAD_TREE
+    ai = w.make_attention(spec, seed=3)
+    ai.block_table[0, 1] = 10 ** 6
+    out, _, st = gpu_attention(ai)
+    assert st & ssd.FLAG_BAD_BLOCK
+    ref, _, _ = oracle.branch_attention(ai.q, ai.k_cache, ai.v_cache, ai.block_table, ai.prefix_len,
+                                        ai.parent, spec.Hkv)
+    assert np.abs(out - ref).max() <= ATOL
+
+
+def test_attention_argument_errors():
+    spec = w.AttnSpec(B=1, Hq=4, Hkv=2, d=64, L=40, tree="chain", n_chain=4)
+    ai = w.make_attention(spec, seed=3)
+    q = to_dev(ai.q)
+    out = torch.empty_like(q)
+    kc, vc = to_dev(ai.k_cache), to_dev(ai.v_cache)
+    args = (to_dev(ai.block_table), to_dev(ai.prefix_len), to_dev(ai.parent))
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_branch_attention(q[..., :32].contiguous(), kc[..., :32].contiguous(),
+                                 vc[..., :32].contiguous(), *args, out[..., :32].contiguous())
+    assert e.value.code == ssd.SSD_ERR_UNSUPPORTED
+    with pytest.raises(ssd.SSDError) as e:
+        ssd.ssd_branch_attention(q[:, :, :3].contiguous(), kc, vc, *args,
+                                 out[:, :, :3].contiguous())
+    assert e.value.code == ssd.SSD_ERR_INVALID_ARG
