@@ -1,0 +1,565 @@
+"""Benchmark of one batched speculation round on GB300.
+
+Step = one pass of the whole round over one batch: Saguaro draft sampling,
+lossless verification with the residual / bonus draw, outcome prediction
+(top-F_k guesses) and the speculation-cache lookup, through the fused
+``ssd_round`` call of the C ABI.  Workload: the Llama-3-vocabulary round
+(B=32 sequences, K=5 draft tokens, V=128256, bf16 logits, Zipf-shaped target,
+draft = target + N(0,1), T=1, C=1, fan-out (16,8,4,2,1,1) from budget 32).
+Metric: seq-rounds/s (sequences verified+predicted per second).
+
+Prints one JSON line.  Also reported on the same line: the roofline of the
+dominant kernel (the HBM statistics pass), tree-masked branch attention on
+its two workloads (GB/s against the HBM peak), the end-to-end figure through
+host buffers, the CPU oracle on a bounded sample, and SM clocks sampled while
+the GPU was under load.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm) on the same
+workload and metric; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verify+predict seq-rounds/s at V=128k"
+UNIT = "seq-rounds/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; sequences are independent units)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank verifies its own batch of sequences (weak scaling)."""
+    return base + 1000003 * rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed work
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, tag):
+        self.marks.append((tag, time.time()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            if t0 <= ts <= t1:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def round_spec():
+    from speculative_decoding_vocab_gb300 import workloads as w
+    return w.llama3_round(T=1.0, B=32)
+
+
+class RoundBuffers:
+    """Inputs and outputs of one round resident on the device."""
+
+    def __init__(self, spec, inp, device):
+        import torch
+        from speculative_decoding_vocab_gb300.binding import tensor
+        self.spec = spec
+        self.target = tensor(inp.target, device)
+        self.draft = tensor(inp.draft, device)
+        self.u_draft = torch.from_numpy(inp.u_draft).to(device)
+        self.u_acc = torch.from_numpy(inp.u_acc).to(device)
+        self.u_bonus = torch.from_numpy(inp.u_bonus).to(device)
+        self.payload = torch.from_numpy(inp.payload).to(device)
+
+
+def make_outputs(spec, device):
+    import torch
+    B, K = spec.B, spec.K
+    sumF = int(sum(spec.F))
+    i32 = dict(dtype=torch.int32, device=device)
+    f32 = dict(dtype=torch.float32, device=device)
+    return dict(d=torch.empty(B, K, **i32), qd=torch.empty(B, K, **f32),
+                accept_len=torch.empty(B, **i32), out_tokens=torch.empty(B, K + 1, **i32),
+                bonus=torch.empty(B, **i32), accept_prob=torch.empty(B, K, **f32),
+                resid_mass=torch.empty(B, **f32), guess=torch.empty(B, sumF, **i32),
+                guess_q=torch.empty(B, sumF, **f32), slot=torch.empty(B, **i32),
+                next_tokens=torch.empty(B, K, **i32), hits=torch.zeros(1, **i32),
+                status=torch.zeros(1, **i32))
+
+
+def run_round(ssd, spec, buf, out, ws):
+    ssd.ssd_round(buf.target, buf.draft, spec.V, spec.F, spec.C, spec.T, buf.u_draft, buf.u_acc,
+                  buf.u_bonus, out["d"], out["accept_len"], out["out_tokens"], out["bonus"],
+                  payload=buf.payload, qd_out=out["qd"], accept_prob=out["accept_prob"],
+                  resid_mass=out["resid_mass"], guess=out["guess"], guess_q=out["guess_q"],
+                  slot=out["slot"], next_tokens=out["next_tokens"], hits=out["hits"],
+                  status=out["status"], ws=ws)
+
+
+KERNELS_PER_ROUND = 3  # statistics pass, Saguaro sampling, verification+prediction+lookup
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def bench_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from speculative_decoding_vocab_gb300 import build
+    build.build()
+    from speculative_decoding_vocab_gb300 import binding as ssd
+    from speculative_decoding_vocab_gb300 import workloads as w
+
+    spec = round_spec()
+    inp = w.make_round(spec, seed=rank_seed(0, rank))
+    # rotating input sets whose total exceeds L2 several times over
+    per_set = w.round_bytes(spec)
+    nsets = max(2, int(np.ceil(3 * L2_BYTES / per_set)) + 1)
+    sets = [RoundBuffers(spec, inp, device) for _ in range(nsets)]
+    out = make_outputs(spec, device)
+    ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
+    stream = torch.cuda.current_stream(device)
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        run_round(ssd, spec, sets[i % nsets], out, ws)
+    torch.cuda.synchronize()
+
+    # clocks: sample while the GPU runs untimed rounds, the timed region, untimed rounds
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else local)
+    sampler.start()
+    t_load0 = time.time()
+    settle = time.time() + 0.6
+    i = 0
+    while time.time() < settle:
+        for _ in range(200):
+            run_round(ssd, spec, sets[i % nsets], out, ws)
+            i += 1
+        torch.cuda.synchronize()
+
+    # timed region: K rounds; the statistics pass of up to 512 of them timed individually
+    nev = min(K, 512)
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+    for e in ev_b + ev_a:  # torch creates the CUDA event on its first record
+        e.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(K):
+        if s < nev:
+            ssd.ssd_set_timing_events(ev_b[s], ev_a[s])
+        elif s == nev:
+            ssd.ssd_set_timing_events(None, None)
+        run_round(ssd, spec, sets[s % nsets], out, ws)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(device)
+    ssd.ssd_set_timing_events(None, None)
+    ms = start.elapsed_time(stop) / K
+    ms = max_over_ranks(ms, device)
+    stats_ms = statistics.mean(b.elapsed_time(a) for b, a in zip(ev_b, ev_a))
+
+    settle = time.time() + 0.6
+    while time.time() < settle:
+        for _ in range(200):
+            run_round(ssd, spec, sets[i % nsets], out, ws)
+            i += 1
+        torch.cuda.synchronize()
+    t_load1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_load0, t_load1)
+    status = int(out["status"].item())
+
+    peaks = load_peaks()
+    hbm_peak = peaks.get("hbm_gbs") or 6800.0
+    alg_bytes = w.round_bytes(spec)
+    achieved = alg_bytes / (stats_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("k_row_stats", spec.name)
+
+    value = spec.B * world / (ms * 1e-3)
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded Zipf-shaped bf16 logits (-1.1 ln rank over a permutation + "
+                "N(0,0.3^2)), draft = target + N(0,1); Philox4x32-10 uniforms",
+        "config": {"workload": spec.name, "B": spec.B, "K": spec.K, "V": spec.V,
+                   "input_dtype": "bf16", "T": spec.T, "C": spec.C, "F": list(spec.F),
+                   "call": "ssd_round (sample + verify + predict + lookup)",
+                   "l2": f"rotating {nsets} input sets, {nsets * per_set / 1e6:.0f} MB > 129 MB L2",
+                   "parallelism": f"replicas x{world} (independent sequences per GPU)"},
+        "roofline": {"kernel": "k_row_stats (HBM statistics pass)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": alg_bytes, "kernel_ms": round(stats_ms, 5),
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+        "gpu_launches": KERNELS_PER_ROUND * K,
+        "clocks": clocks,
+        "status_flags": status,
+    }
+    result["step_roofline_frac"] = round(alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4)
+    if not args.no_extras:
+        result["e2e"] = bench_e2e(ssd, spec, inp, device, K, W)
+        result["branch_attention"] = bench_attention(ssd, device, hbm_peak)
+        result["other_rounds"] = bench_other_rounds(ssd, w, device, hbm_peak)
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(spec, inp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_e2e(ssd, spec, inp, device, K, W):
+    """The same metric through the public call with HOST buffers: every step
+    copies that step's logits and uniforms from pinned host memory to the
+    device, runs the round and reads the emitted tokens, accept lengths,
+    bonus tokens and cache slots back."""
+    import torch
+    from speculative_decoding_vocab_gb300.binding import pinned
+    hin = dict(target=pinned(inp.target), draft=pinned(inp.draft),
+               u_draft=torch.from_numpy(inp.u_draft).pin_memory(),
+               u_acc=torch.from_numpy(inp.u_acc).pin_memory(),
+               u_bonus=torch.from_numpy(inp.u_bonus).pin_memory(),
+               payload=torch.from_numpy(inp.payload).pin_memory())
+    buf = RoundBuffers(spec, inp, device)
+    out = make_outputs(spec, device)
+    ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
+    hout = {k: torch.empty_like(out[k], device="cpu").pin_memory()
+            for k in ("out_tokens", "accept_len", "bonus", "slot", "next_tokens")}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        for k in ("target", "draft", "u_draft", "u_acc", "u_bonus", "payload"):
+            getattr(buf, k).copy_(hin[k], non_blocking=True)
+        run_round(ssd, spec, buf, out, ws)
+        for k, t in hout.items():
+            t.copy_(out[k], non_blocking=True)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    n = max(K // 4, 20)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": round(spec.B / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def _time_calls(fn, n, stream):
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(n):
+        fn(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def device_attention_inputs(spec, device, seed):
+    """Seeded attention inputs generated directly on the device (bench only)."""
+    import torch
+    from speculative_decoding_vocab_gb300 import workloads as w
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0xA77E]))
+    parent1 = w.attn_tree(spec, rng)
+    N = int(parent1.shape[0])
+    Nq = N - spec.K if spec.tree == "fanout" else N
+    nblk = (spec.L + N + w.PAGE - 1) // w.PAGE
+    nb = spec.B * nblk
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    table = torch.randperm(nb, generator=g, device=device).to(torch.int32).view(spec.B, nblk)
+    q = torch.randn(spec.B, Nq, spec.Hq, spec.d, generator=g, device=device).to(torch.bfloat16)
+    kc = torch.randn(nb, spec.Hkv, w.PAGE, spec.d, generator=g, device=device).to(torch.bfloat16)
+    vc = torch.randn(nb, spec.Hkv, w.PAGE, spec.d, generator=g, device=device).to(torch.bfloat16)
+    prefix = torch.full((spec.B,), spec.L, dtype=torch.int32, device=device)
+    parent = torch.from_numpy(np.broadcast_to(parent1, (spec.B, N)).copy()).to(device)
+    return q, kc, vc, table, prefix, parent, N, Nq
+
+
+def bench_attention(ssd, device, hbm_peak):
+    import torch
+    from speculative_decoding_vocab_gb300 import workloads as w
+    res = {}
+    stream = torch.cuda.current_stream(device)
+    for spec in (w.draft_branch_attention(), w.verify_attention_at_scale()):
+        q, kc, vc, table, prefix, parent, N, Nq = device_attention_inputs(spec, device, 7)
+        # two copies of the caches so consecutive calls do not hit in L2 (config 4 is ~70 MB)
+        kc2, vc2 = kc.clone(), vc.clone()
+        out = torch.empty_like(q)
+        st = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def call(i):
+            ssd.ssd_branch_attention(q, kc if i % 2 == 0 else kc2, vc if i % 2 == 0 else vc2,
+                                     table, prefix, parent, out, status=st)
+
+        for i in range(3):
+            call(i)
+        n = 20 if spec.L > 4096 else 100
+        ms = _time_calls(call, n, stream)
+        alg = w.attention_bytes(spec, N, Nq, [spec.L] * spec.B)
+        vis_pairs = spec.B * spec.Hq * Nq * spec.L  # prefix keys
+        par = parent[0].cpu().numpy()
+        depth = 0
+        for m in range(N - Nq, N):
+            x = m
+            while x >= 0:
+                depth += 1
+                x = par[x]
+        vis_pairs += spec.B * spec.Hq * depth
+        flops = 4 * spec.d * vis_pairs
+        gbs = alg / (ms * 1e-3) / 1e9
+        res[spec.name] = {"ms": round(ms, 4), "algorithmic_bytes": alg, "GB/s": round(gbs, 1),
+                          "frac_of_hbm_peak": round(gbs / hbm_peak, 4),
+                          "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 2),
+                          "kernel": "k_branch_attn_simt (CUDA cores)",
+                          "status_flags": int(st.item())}
+        del q, kc, vc, kc2, vc2, out
+        torch.cuda.empty_cache()
+    return res
+
+
+def bench_other_rounds(ssd, w, device, hbm_peak):
+    """The large-batch Qwen-3 round and the at-scale Llama-3 round (seq-rounds/s)."""
+    import torch
+    res = {}
+    stream = torch.cuda.current_stream(device)
+    for spec in (w.qwen3_round(C=0.5), w.llama3_round_at_scale(), w.llama3_round(T=0.0)):
+        g = torch.Generator(device=device)
+        g.manual_seed(11)
+        shape = (spec.B, spec.K + 1, spec.V)
+        rank = torch.argsort(torch.rand(shape, generator=g, device=device), dim=-1).float() + 1
+        zt = -spec.zipf_slope * torch.log(rank) + spec.target_noise * torch.randn(
+            shape, generator=g, device=device)
+        del rank
+        zd = zt + spec.draft_noise * torch.randn(shape, generator=g, device=device)
+        sets = []
+        per = w.round_bytes(spec)
+        nsets = max(2, int(np.ceil(3 * L2_BYTES / per)) + 1) if per < 2 * L2_BYTES else 1
+        for _ in range(nsets):
+            sets.append((zt.to(torch.bfloat16), zd.to(torch.bfloat16)))
+        del zt, zd
+        u = torch.rand(3, spec.B, spec.K + 1, generator=g, device=device)
+        ud, ua, ub = u[0, :, :spec.K].contiguous(), u[1, :, :spec.K].contiguous(), u[2, :, 0].contiguous()
+        out = make_outputs(spec, device)
+        ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
+
+        def call(i):
+            t, d = sets[i % nsets]
+            ssd.ssd_round(t, d, spec.V, spec.F, spec.C, spec.T, ud, ua, ub, out["d"],
+                          out["accept_len"], out["out_tokens"], out["bonus"], guess=out["guess"],
+                          slot=out["slot"], hits=out["hits"], status=out["status"], ws=ws)
+
+        for i in range(3):
+            call(i)
+        ms = _time_calls(call, 50, stream)
+        res[spec.name] = {"ms": round(ms, 4), "seq_rounds_per_s": round(spec.B / (ms * 1e-3), 1),
+                          "algorithmic_bytes": per,
+                          "frac_of_hbm_peak": round(per / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "hit_rate": round(int(out["hits"].item()) / spec.B, 4)}
+        del sets, out, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def cpu_sample(spec, inp, nseq):
+    from speculative_decoding_vocab_gb300 import workloads as w
+    idx = np.arange(nseq) % spec.B
+    sub = w.RoundSpec(**{**spec.__dict__, "B": nseq})
+    return w.RoundInputs(sub, inp.target[idx], inp.draft[idx], inp.u_draft[idx], inp.u_acc[idx],
+                         inp.u_bonus[idx], inp.payload[idx])
+
+
+def cpu_baseline(spec, inp, seconds):
+    import oracle
+    oracle.build()
+    # calibrate on 2 sequences, then time a sample sized to about `seconds`
+    t0 = time.perf_counter()
+    oracle.run_round(cpu_sample(spec, inp, 2))
+    per_seq = (time.perf_counter() - t0) / 2
+    nseq = int(max(2, min(256, seconds / max(per_seq, 1e-6))))
+    sub = cpu_sample(spec, inp, nseq)
+    t0 = time.perf_counter()
+    oracle.run_round(sub)
+    dt = time.perf_counter() - t0
+    return {"value": round(nseq / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{nseq} sequences of the {spec.name} round (full V, all K+1 rows; "
+                      f"sample + verify + predict + lookup in fp64), {dt:.1f} s",
+            "host_cpus": os.cpu_count()}
+
+
+def bench_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_vocab_gb300 import workloads as w
+    import oracle
+    oracle.build()
+    spec = round_spec()
+    inp = w.make_round(spec, seed=0)
+    nseq = args.ref_seqs
+    sub = cpu_sample(spec, inp, nseq)
+    for _ in range(args.warmup):
+        oracle.run_round(cpu_sample(spec, inp, 1))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_round(sub)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nseq / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same workload as our arm)",
+        "config": {"workload": spec.name, "B": spec.B, "K": spec.K, "V": spec.V,
+                   "input_dtype": "bf16", "T": spec.T, "C": spec.C, "F": list(spec.F),
+                   "reference": "fp64 CPU oracle (oracle/ssd_oracle.c), one host core"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{nseq} sequences per step of the {spec.name} round"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on this
+    workload, or None when no summary for the current kernel exists."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d.get(kernel, {}).get(workload)
+    except (OSError, ValueError):
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seqs", type=int, default=2)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extras", action="store_true", help="skip e2e / attention / other rounds")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -184,6 +184,16 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
                        ssd_stream_t s);
 
 /*
+ * Timing hook for profiling: while set (both non-NULL cudaEvent_t handles),
+ * every vocabulary call records `before` and `after` on its stream around its
+ * HBM statistics pass (the dominant kernel), so a caller can time that kernel
+ * inside a real round with cudaEventElapsedTime.  Process-wide, not
+ * thread-safe; pass NULL, NULL to clear.  Returns SSD_ERR_INVALID_ARG when
+ * exactly one handle is NULL.  Not part of the method: diagnostics only.
+ */
+ssd_status_t ssd_set_timing_events(void *before, void *after);
+
+/*
  * Tree-masked decode attention over a paged bf16 KV cache, so that the draft
  * decodes every branch of the speculation tree in one forward pass [B,
  * "工程优化与系统表现": a custom sparse attention mask].

@@ -24,7 +24,8 @@ FLAG_BAD_OUTCOME = 8
 FLAG_BAD_TREE = 16
 FLAG_BAD_BLOCK = 32
 
-EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_saguaro_sample",
+EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events",
+           "ssd_saguaro_sample",
            "ssd_verify", "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round",
            "ssd_attention_workspace_size", "ssd_branch_attention")
 
@@ -72,6 +73,8 @@ def _declare(lib):
     lib.ssd_fanout_split.restype = _i
     lib.ssd_workspace_size.argtypes = [_i, _i, _i, _i, _vp]
     lib.ssd_workspace_size.restype = _sz
+    lib.ssd_set_timing_events.argtypes = [_vp, _vp]
+    lib.ssd_set_timing_events.restype = _i
     lib.ssd_saguaro_sample.argtypes = [_vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp,
                                        _vp, _vp, _sz, _vp]
     lib.ssd_saguaro_sample.restype = _i
@@ -121,8 +124,13 @@ def _host_F(F):
 
 
 def _logit_meta(x: torch.Tensor):
-    if x.dim() != 3 or x.stride(2) != 1:
-        raise ValueError("logits must be [B, K+1, V'] with unit stride on the last dim")
+    if x.dim() != 3:
+        raise ValueError("logits must be [B, K+1, V']")
+    if x.numel() == 0:  # empty batch: nothing is read
+        dt = SSD_F32 if x.dtype == torch.float32 else SSD_BF16
+        return dt, x.shape[1] * x.shape[2], x.shape[2]
+    if x.stride(2) != 1:
+        raise ValueError("logits must have unit stride on the last dim")
     if x.dtype == torch.float32:
         dt = SSD_F32
     elif x.dtype == torch.bfloat16:
@@ -130,6 +138,24 @@ def _logit_meta(x: torch.Tensor):
     else:
         raise ValueError(f"logits must be float32 or bfloat16, got {x.dtype}")
     return dt, x.stride(0), x.stride(1)
+
+
+def tensor(arr, device="cuda"):
+    """numpy -> torch on ``device``; uint16 arrays are taken as bf16 bit patterns."""
+    import numpy as np
+    arr = np.ascontiguousarray(arr)
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(arr).to(device)
+
+
+def pinned(arr):
+    """numpy -> page-locked host tensor (uint16 arrays as bf16)."""
+    import numpy as np
+    arr = np.ascontiguousarray(arr)
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).pin_memory()
+    return torch.from_numpy(arr).pin_memory()
 
 
 def _dtype_code(dtype) -> int:
@@ -143,6 +169,17 @@ def ssd_fanout_split(budget: int, K: int, r: float = 0.5):
     F = (ctypes.c_int32 * (K + 1))()
     _check("ssd_fanout_split", load().ssd_fanout_split(int(budget), int(K), float(r), F))
     return tuple(int(x) for x in F)
+
+
+def ssd_set_timing_events(before=None, after=None):
+    """Record torch.cuda.Event ``before``/``after`` around the statistics pass of
+    every following vocabulary call (None, None clears)."""
+    if before is not None and (not before.cuda_event or not after.cuda_event):
+        raise ValueError("record both events once before handing them to the library "
+                         "(torch creates the CUDA event lazily)")
+    b = None if before is None else ctypes.c_void_p(before.cuda_event)
+    a = None if after is None else ctypes.c_void_p(after.cuda_event)
+    _check("ssd_set_timing_events", load().ssd_set_timing_events(b, a))
 
 
 def ssd_workspace_size(B: int, K: int, V: int, dtype, F) -> int:

@@ -938,8 +938,24 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   return a;
 }
 
+// Optional timing hook (ssd_set_timing_events): events recorded around the
+// statistics pass of every vocabulary call while set.
+cudaEvent_t g_ev_before = nullptr;
+cudaEvent_t g_ev_after = nullptr;
+
+template <class E>
+cudaError_t launch_stats_raw(const VocabArgs &a, cudaStream_t s);
+
 template <class E>
 cudaError_t launch_stats(const VocabArgs &a, cudaStream_t s) {
+  if (g_ev_before) cudaEventRecord(g_ev_before, s);
+  cudaError_t e = launch_stats_raw<E>(a, s);
+  if (g_ev_after) cudaEventRecord(g_ev_after, s);
+  return e;
+}
+
+template <class E>
+cudaError_t launch_stats_raw(const VocabArgs &a, cudaStream_t s) {
   const size_t smem = kStages * kChunkBytes + kCandCap * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(k_row_stats<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -1046,6 +1062,13 @@ ssd_status_t ssd_fanout_split(int budget, int K, double r, int32_t *F_out) {
     --F_out[best];
     --total;
   }
+  return SSD_OK;
+}
+
+ssd_status_t ssd_set_timing_events(void *before, void *after) {
+  if ((before == nullptr) != (after == nullptr)) return SSD_ERR_INVALID_ARG;
+  g_ev_before = static_cast<cudaEvent_t>(before);
+  g_ev_after = static_cast<cudaEvent_t>(after);
   return SSD_OK;
 }
 

@@ -27,9 +27,7 @@ PROB_RTOL = 1e-5
 
 
 def to_dev(arr, dev="cuda"):
-    if arr.dtype == np.uint16:
-        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16).to(dev)
-    return torch.from_numpy(np.ascontiguousarray(arr)).to(dev)
+    return ssd.tensor(arr, dev)
 
 
 def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True):
