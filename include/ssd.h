@@ -153,6 +153,37 @@ ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq
                                   void *ws, size_t ws_bytes, ssd_stream_t s);
 
 /*
+ * ssd_verify without a caller workspace.  For callers that cannot allocate
+ * device memory themselves -- for example a plugin running inside another
+ * framework that owns every device allocation and forbids new ones in its
+ * execution path, or a plain C program linked only against this library with
+ * no allocator of its own -- this entry point takes its scratch from a fixed
+ * array compiled into the library (ssd_verify_noalloc_max_bytes() bytes,
+ * 8 MiB; one copy on every GPU that loads the library, kept until the process
+ * exits).  The pages describe no such variant; it exists only for those
+ * callers.  Arguments, outputs and semantics are those of ssd_verify; the
+ * caller still provides every input and output buffer.
+ *   - Allocates nothing: no cudaMalloc / cudaFree / allocating library call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - A batch whose scratch (ssd_workspace_size) exceeds the array returns
+ *     SSD_ERR_WORKSPACE and launches nothing.
+ *   - Every call shares the one array, and it keeps the previous call's
+ *     contents (nothing in it needs to start at zero: each call writes every
+ *     scratch record before reading it).  Calls whose work overlaps on the GPU
+ *     (different streams, or different host threads) race on it: serialise
+ *     them, e.g. on one stream.
+ */
+size_t ssd_verify_noalloc_max_bytes(void);
+ssd_status_t ssd_verify_noalloc(const void *target, const void *draft, ssd_dtype_t dt,
+                                int64_t seq_stride, int64_t row_stride, int B, int K, int V,
+                                const int32_t *F, float C, float T, const int32_t *d,
+                                const float *u_acc, const float *u_bonus, int32_t *accept_len,
+                                int32_t *out_tokens, int32_t *bonus, float *accept_prob,
+                                float *resid_mass, uint32_t *status, ssd_stream_t s);
+
+/*
  * Speculation-cache lookup keyed by the verification outcome (a, b) [B,
  * "投机解码的瓶颈与 SSD 的核心机制": once verification returns, one cache lookup
  * decides whether pre-speculated tokens are ready].  Hit iff bonus b is among

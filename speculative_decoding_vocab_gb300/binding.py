@@ -26,7 +26,8 @@ FLAG_BAD_BLOCK = 32
 
 EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events",
            "ssd_saguaro_sample",
-           "ssd_verify", "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round",
+           "ssd_verify", "ssd_verify_noalloc", "ssd_verify_noalloc_max_bytes",
+           "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round",
            "ssd_attention_workspace_size", "ssd_branch_attention")
 
 _lib = None
@@ -81,6 +82,11 @@ def _declare(lib):
     lib.ssd_verify.argtypes = [_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp,
                                _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.ssd_verify.restype = _i
+    lib.ssd_verify_noalloc.argtypes = [_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp,
+                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.ssd_verify_noalloc.restype = _i
+    lib.ssd_verify_noalloc_max_bytes.argtypes = []
+    lib.ssd_verify_noalloc_max_bytes.restype = _sz
     lib.ssd_predict_outcomes.argtypes = [_vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _vp, _vp, _vp,
                                          _vp, _sz, _vp]
     lib.ssd_predict_outcomes.restype = _i
@@ -214,6 +220,24 @@ def ssd_verify(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tok
         _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
         _ptr(accept_prob), _ptr(resid_mass), _ptr(status), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_verify_noalloc(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tokens, bonus,
+                       accept_prob=None, resid_mass=None, status=None, stream=None):
+    """ssd_verify with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory)."""
+    dt, ss, rs = _logit_meta(target)
+    if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
+        raise ValueError("target and draft logits must share dtype, shape and strides")
+    B, K1 = target.shape[0], target.shape[1]
+    _check("ssd_verify_noalloc", load().ssd_verify_noalloc(
+        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
+        _ptr(accept_prob), _ptr(resid_mass), _ptr(status), _stream(stream)))
+
+
+def ssd_verify_noalloc_max_bytes() -> int:
+    return int(load().ssd_verify_noalloc_max_bytes())
 
 
 def ssd_predict_outcomes(draft, V, F, T, guess, guess_q=None, status=None, ws=None, stream=None):

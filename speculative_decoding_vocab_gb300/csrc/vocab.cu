@@ -24,6 +24,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/ssd.h"
 #include "common.cuh"
 
@@ -1007,6 +1009,33 @@ void set_slots_verify(VocabArgs &a) {
   }
 }
 
+// Fixed device scratch for ssd_verify_noalloc: one array per GPU that loads
+// the library, held until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void *g_static_scratch_addr[kMaxDevices] = {nullptr};
+std::mutex g_static_scratch_mu;
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the array's name in host code is only a stand-in for it).
+cudaError_t static_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1276,6 +1305,25 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
     if (e == cudaSuccess) e = launch_verify_finish<EBF16>(a, o, cs);
   }
   return cuda_status(e);
+}
+
+size_t ssd_verify_noalloc_max_bytes(void) { return kStaticScratchBytes; }
+
+ssd_status_t ssd_verify_noalloc(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                                int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                                const int32_t *d, const float *u_acc, const float *u_bonus,
+                                int32_t *accept_len, int32_t *out_tokens, int32_t *bonus, float *accept_prob,
+                                float *resid_mass, uint32_t *status, ssd_stream_t s) {
+  Layout L;
+  if (!F || !make_layout(B, K, V, dt, F, &L))
+    return (F && B >= 0 && K >= 0 && V >= 1) ? SSD_ERR_UNSUPPORTED : SSD_ERR_INVALID_ARG;
+  if (L.total > kStaticScratchBytes) return SSD_ERR_WORKSPACE;  // the batch needs more scratch than the array holds
+  if (B == 0) return ssd_verify(target, draft, dt, seq_stride, row_stride, B, K, V, F, C, T, d, u_acc, u_bonus,
+                                accept_len, out_tokens, bonus, accept_prob, resid_mass, status, nullptr, 0, s);
+  void *ws = nullptr;
+  if (static_scratch(&ws) != cudaSuccess) return SSD_ERR_CUDA;
+  return ssd_verify(target, draft, dt, seq_stride, row_stride, B, K, V, F, C, T, d, u_acc, u_bonus, accept_len,
+                    out_tokens, bonus, accept_prob, resid_mass, status, ws, kStaticScratchBytes, s);
 }
 
 }  // extern "C"
