@@ -225,6 +225,17 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
 ssd_status_t ssd_set_timing_events(void *before, void *after);
 
 /*
+ * Work trace for profiling: while set, every vocabulary call writes, for each
+ * entry of its work queue, four 64-bit words into `buf` (device memory):
+ * (CTA << 48 | kind << 40 | sequence << 20 | index), the %globaltimer (ns) at
+ * the entry's start, after its dependency wait, and at its end.  kind: 0 row
+ * statistics, 1 row merge / Saguaro draw, 2 residual chunk, 3 final draw and
+ * lookup.  Calls whose queue does not fit in `bytes` write nothing.
+ * Process-wide, not thread-safe; NULL clears.  Diagnostics only.
+ */
+ssd_status_t ssd_set_trace(void *buf, size_t bytes);
+
+/*
  * Tree-masked decode attention over a paged bf16 KV cache, so that the draft
  * decodes every branch of the speculation tree in one forward pass [B,
  * "工程优化与系统表现": a custom sparse attention mask].

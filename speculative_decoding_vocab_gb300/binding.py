@@ -24,7 +24,7 @@ FLAG_BAD_OUTCOME = 8
 FLAG_BAD_TREE = 16
 FLAG_BAD_BLOCK = 32
 
-EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events",
+EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events", "ssd_set_trace",
            "ssd_saguaro_sample",
            "ssd_verify", "ssd_verify_noalloc", "ssd_verify_noalloc_max_bytes",
            "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round",
@@ -76,6 +76,8 @@ def _declare(lib):
     lib.ssd_workspace_size.restype = _sz
     lib.ssd_set_timing_events.argtypes = [_vp, _vp]
     lib.ssd_set_timing_events.restype = _i
+    lib.ssd_set_trace.argtypes = [_vp, _sz]
+    lib.ssd_set_trace.restype = _i
     lib.ssd_saguaro_sample.argtypes = [_vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp,
                                        _vp, _vp, _sz, _vp]
     lib.ssd_saguaro_sample.restype = _i
@@ -186,6 +188,15 @@ def ssd_set_timing_events(before=None, after=None):
     b = None if before is None else ctypes.c_void_p(before.cuda_event)
     a = None if after is None else ctypes.c_void_p(after.cuda_event)
     _check("ssd_set_timing_events", load().ssd_set_timing_events(b, a))
+
+
+def ssd_set_trace(buf=None):
+    """Record a per-entry work trace of the following vocabulary calls into the
+    uint8/int64 CUDA tensor ``buf`` (None clears)."""
+    if buf is None:
+        _check("ssd_set_trace", load().ssd_set_trace(None, 0))
+    else:
+        _check("ssd_set_trace", load().ssd_set_trace(_ptr(buf), buf.numel() * buf.element_size()))
 
 
 def ssd_workspace_size(B: int, K: int, V: int, dtype, F) -> int:

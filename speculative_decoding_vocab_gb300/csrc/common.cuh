@@ -150,7 +150,39 @@ SSD_DEV void load_vec(const void *row, int i0, int V, float *f, bool *valid) {
 }
 
 // ---------------------------------------------------------------------------
-// deterministic warp / block reductions (fixed association order)
+// barrier of a group of NT threads (named barrier 1): the first NT threads of a
+// CTA synchronise without the CTA's other warps
+// ---------------------------------------------------------------------------
+template <int NT>
+SSD_DEV void group_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+template <int NT>
+SSD_DEV int group_sync_count(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, 1, %2, p;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred), "n"(NT)
+      : "memory");
+  return r;
+}
+template <int NT>
+SSD_DEV int group_sync_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred), "n"(NT)
+      : "memory");
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// deterministic warp / block reductions (fixed association order); "block"
+// here is the group of the first NT threads (named barrier 1)
 // ---------------------------------------------------------------------------
 SSD_DEV float warp_max(float v) {
 #pragma unroll
@@ -176,11 +208,11 @@ template <int NT>
 SSD_DEV float block_max(float v, float *red) {
   v = warp_max(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
+  group_sync<NT>();
   float r = red[0];
 #pragma unroll
   for (int w = 1; w < NT / 32; ++w) r = fmaxf(r, red[w]);
-  __syncthreads();
+  group_sync<NT>();
   return r;
 }
 // Every thread receives the same block sum (lane 0 of each warp, warps in order).
@@ -188,22 +220,22 @@ template <int NT>
 SSD_DEV float block_sum(float v, float *red) {
   v = warp_sum(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
+  group_sync<NT>();
   float r = red[0];
 #pragma unroll
   for (int w = 1; w < NT / 32; ++w) r = __fadd_rn(r, red[w]);
-  __syncthreads();
+  group_sync<NT>();
   return r;
 }
 template <int NT>
 SSD_DEV uint64_t block_max_u64(uint64_t v, uint64_t *red) {
   v = warp_max_u64(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
+  group_sync<NT>();
   uint64_t r = red[0];
 #pragma unroll
   for (int w = 1; w < NT / 32; ++w) r = (red[w] > r) ? red[w] : r;
-  __syncthreads();
+  group_sync<NT>();
   return r;
 }
 
@@ -222,7 +254,7 @@ SSD_DEV float block_excl_scan(float v, float *red) {
   float excl_lane = __shfl_up_sync(0xffffffffu, inc, 1);
   if (lane == 0) excl_lane = 0.f;
   if (lane == 31) red[warp] = inc;
-  __syncthreads();
+  group_sync<NT>();
   if (threadIdx.x == 0) {
     float run = 0.f;
     for (int w = 0; w < NT / 32; ++w) {
@@ -232,9 +264,9 @@ SSD_DEV float block_excl_scan(float v, float *red) {
     }
     red[NT / 32] = run;
   }
-  __syncthreads();
+  group_sync<NT>();
   float r = __fadd_rn(red[warp], excl_lane);
-  __syncthreads();
+  group_sync<NT>();
   return r;
 }
 
