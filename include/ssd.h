@@ -226,12 +226,16 @@ ssd_status_t ssd_set_timing_events(void *before, void *after);
 
 /*
  * Work trace for profiling: while set, every vocabulary call writes, for each
- * entry of its work queue, four 64-bit words into `buf` (device memory):
- * (CTA << 48 | kind << 40 | sequence << 20 | index), the %globaltimer (ns) at
- * the entry's start, after its dependency wait, and at its end.  kind: 0 row
- * statistics, 1 row merge / Saguaro draw, 2 residual chunk, 3 final draw and
- * lookup.  Calls whose queue does not fit in `bytes` write nothing.
- * Process-wide, not thread-safe; NULL clears.  Diagnostics only.
+ * CTA of its kernels, eight 64-bit words into `buf` (device memory), the
+ * statistics kernel's CTAs first (in launch order), then the residual
+ * kernel's: (SM << 48 | kind << 40 | sequence << 20 | index) and seven
+ * %globaltimer marks in ns (0 = not reached).  kind: 0 chunk statistics,
+ * 1 + pair merge, 2 residual chunk, 3 + final steps.  Statistics CTA marks:
+ * start, chunk landed, record published, pair merged, Saguaro draw done,
+ * sequence finished, end.  Residual CTA marks: start, chunks landed, chunk mass
+ * done, last arrival, chain and chunk located, bonus drawn, end.  Calls whose
+ * CTAs do not fit in `bytes` write nothing.  Process-wide, not thread-safe;
+ * NULL clears.  Diagnostics only.
  */
 ssd_status_t ssd_set_trace(void *buf, size_t bytes);
 

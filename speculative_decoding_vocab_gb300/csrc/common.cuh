@@ -94,6 +94,32 @@ SSD_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 }
 
 // ---------------------------------------------------------------------------
+// packed arithmetic: two fp32 lanes in a 64-bit register (Blackwell FMA2 /
+// ADD2), two bf16 lanes in a 32-bit register
+// ---------------------------------------------------------------------------
+SSD_DEV uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+SSD_DEV void unpack2(uint64_t v, float &lo, float &hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
+SSD_DEV uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {  // a * b + c per lane, round to nearest
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+SSD_DEV uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+SSD_DEV uint32_t bmax2(uint32_t a, uint32_t b) {  // lane-wise maximum of two bf16 pairs
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
 // element types of the logits
 // ---------------------------------------------------------------------------
 struct EF32 {
@@ -108,6 +134,10 @@ struct EF32 {
   }
   SSD_DEV static float ld(const void *base, int64_t i) {
     return __ldg(reinterpret_cast<const float *>(base) + i);
+  }
+  static constexpr int kPairs = 2;  // packed fp32 pairs per vector
+  SSD_DEV static uint64_t pair(const uint4 &w, int h) {
+    return h == 0 ? pack2(__uint_as_float(w.x), __uint_as_float(w.y)) : pack2(__uint_as_float(w.z), __uint_as_float(w.w));
   }
 };
 struct EBF16 {
@@ -127,6 +157,11 @@ struct EBF16 {
   SSD_DEV static float ld(const void *base, int64_t i) {
     uint16_t h = __ldg(reinterpret_cast<const unsigned short *>(base) + i);
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  static constexpr int kPairs = 4;
+  SSD_DEV static uint64_t pair(const uint4 &w, int h) {
+    const uint32_t x = h == 0 ? w.x : (h == 1 ? w.y : (h == 2 ? w.z : w.w));
+    return pack2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
   }
 };
 

@@ -9,30 +9,32 @@
 // 核心机制" and "Saguaro 算法" parts 1-2) describe it; the readings of the
 // missing formulas are stated in include/ssd.h at each call.
 //
-// Structure: every vocabulary call is ONE persistent kernel, k_vocab, fed by a
-// global work queue (an atomic counter).  Work items, in queue order:
-//   STATS(b, slot, chunk)  the HBM pass: a 32 KiB chunk of one logit row is
-//                          staged in shared memory by a TMA bulk copy and
-//                          reduced to (max, sum of 2^(z log2e/T - max), argmax,
-//                          sorted top-F candidates).  >= 95% of the bytes.
-//   ROW(b, r)              merges row r's chunk records (target and draft),
-//                          Saguaro-samples d_{r+1} (locate the chunk from the
-//                          chunk masses, rescan only that chunk), gathers
-//                          p(d), q'(d), writes the guesses of depth r.
-//   RES(b, c)              acceptance chain, then the residual mass of chunk c
-//                          of row a (the rejected position).
-//   FIN(b)                 residual / bonus draw (locate the chunk, rescan it),
-//                          outputs, cache lookup.
-// Each group of sequence b is queued a few sequences after its inputs, and an
-// item only ever waits (bounded, on a per-sequence counter) for items EARLIER
-// in the queue.  Items are dequeued in index order by running CTAs, so every
-// awaited item is held by a running CTA: the schedule cannot deadlock, with or
-// without co-residency of the grid.
+// Structure: a vocabulary call is at most two kernels.
+//   k_stats  one CTA per 32 KiB chunk of one logit row: the HBM pass, which
+//            carries nearly all of the call's bytes.  A TMA bulk copy stages
+//            the chunk in shared memory; the CTA reduces it to (max, sum of
+//            2^(z log2e/T - max), argmax, sorted top-F candidates) and
+//            publishes that record.  Chunks are numbered sequence-major and,
+//            within a sequence, by row pair r = (target row r, draft row r), so
+//            pairs complete in launch order.  The CTA that publishes the last
+//            chunk of a pair (an atomic count per pair) merges the pair: row
+//            statistics, the top-F_r list (the guesses of depth r), the Saguaro
+//            draw of d_{r+1} (its chunk is located from the chunk masses; only
+//            that chunk is staged again), p(d) and q'(d).  The CTA that merges
+//            the last pair of a sequence runs the acceptance chain and, unless
+//            a residual draw is needed, the bonus draw and the outputs.  No CTA
+//            ever waits for another: the last to arrive does the work.
+//   k_resid  (verification at T > 0) one CTA per chunk of each sequence's
+//            rejected row pair: residual chunk masses; the last CTA of a
+//            sequence draws the bonus token from them and writes the outputs.
+//            It is a programmatic dependent launch of k_stats, so its launch
+//            overlaps k_stats' last wave.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/ssd.h"
@@ -41,16 +43,18 @@
 namespace ssd {
 
 constexpr int kThreads = 256;
-constexpr int kChunkBytes = 24576;  // = kThreads * kSegVec * 16 B
-constexpr int kStages = 3;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSegVec = 8;                             // 16-byte vectors per thread and chunk
+constexpr int kChunkBytes = kThreads * kSegVec * 16;  // 32 KiB
 constexpr int kCandCap = 512;
 constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
 constexpr int kMaxChunks = 128;  // per row: 4 lists per lane in the warp merge
-constexpr uint32_t kMaxSpins = 1u << 24;  // bounded dependency waits (x ~100 ns sleeps)
-
-enum ItemKind { IT_STATS = 0, IT_ROW = 1, IT_RES = 2, IT_FIN = 3, IT_NONE = 4 };
+constexpr int kWarpF = 32;       // top-F sizes selected warp by warp (larger F: block threshold)
+constexpr int kWarpCand = kCandCap / kWarps;  // candidate slots per warp (64)
+constexpr int kRankMax = 1024;   // lists merged by rank selection up to this many keys
+constexpr int kNone = 0x7fffffff;
 
 struct ChunkStat {
   float m;   // chunk maximum
@@ -81,11 +85,6 @@ struct ResInfo {
   int last;  // last index of the chunk with positive residual (-1: none)
 };
 
-struct Sched {
-  int B, ns, nr, nc, nf;  // items per sequence: stats, row, residual, final
-  int L1, L2, L3;         // lags of the row / residual / final groups (in sequences)
-};
-
 struct VocabArgs {
   const void *target, *draft;
   int64_t seq_stride, row_stride;  // elements
@@ -94,21 +93,24 @@ struct VocabArgs {
   float kT;    // log2(e) / T
   int greedy;  // T == 0
   float C;
-  int tslot0, dslot0;  // slot of target row 0 (-1: no target rows) and draft row 0
+  int npairs;  // row pairs per sequence, r = 0 .. npairs-1
   int do_sample, do_verify, do_predict, do_lookup;
-  RowSlot slot[kMaxSlots];
-  int F[kMaxK + 1];
+  RowSlot slot[kMaxSlots];                   // ordered by pair: target r, then draft r
+  int tsl[kMaxK + 1], dsl[kMaxK + 1];        // slot of target / draft row r (-1: none)
+  int pair_chunks[kMaxK + 1];                // chunks of pair r (both rows)
+  int F[kMaxK + 1];                          // fan-out F_r
+  int Fs[kMaxK + 1];                         // top-F list kept for draft row r (F_r or 0)
   int foff[kMaxK + 2];
-  Sched fs;   // finish queue: super-slot t holds ROW(t), RES(t-1), FIN(t-2); fs.ns = statistics per sequence
-  long nst;   // statistics items in total (B * fs.ns)
   // workspace
-  uint32_t *ctr;  // [0] queue head, [1] abort, [2] finished sequences, [3] hits; 3 per sequence after
+  uint32_t *ctr;  // [0] finished sequences, [1] hits, [2+b] pairs done, [2+B+b] residual
+                  // chunks done, [2+2B + b(K+1) + r] chunks done of pair (b, r)
   ChunkStat *stats;
   uint64_t *cands;  // [B][nslots][nchunks][Fcap]
   RowInfo *rows;    // [B][K+1]
   uint64_t *S;      // [B][K+1][Fcap] merged top-F lists
   PosInfo *pos;     // [B][K]
   ResInfo *res;     // [B][nchunks]
+  int32_t *accs;    // [B] accept count of a sequence left to k_resid, else -1
   // inputs / outputs
   const float *u_draft, *u_acc, *u_bonus;
   const int32_t *d_in;
@@ -122,12 +124,14 @@ struct VocabArgs {
   int32_t *slot_out, *next_tokens;
   uint32_t *hits;
   uint32_t *status;
-  unsigned long long *trace;  // optional: 4 words per queue entry (see ssd_set_trace)
+  unsigned long long *trace;  // optional: 4 words per CTA (see ssd_set_trace)
 };
 
-SSD_DEV uint32_t *stats_done(const VocabArgs &a, int b) { return a.ctr + 4 + 3 * b; }
-SSD_DEV uint32_t *row_done(const VocabArgs &a, int b) { return a.ctr + 5 + 3 * b; }
-SSD_DEV uint32_t *res_done(const VocabArgs &a, int b) { return a.ctr + 6 + 3 * b; }
+SSD_DEV uint32_t *seq_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + b; }
+SSD_DEV uint32_t *res_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + a.B + b; }
+SSD_DEV uint32_t *pair_ctr(const VocabArgs &a, int b, int r) {
+  return a.ctr + 2 + 2 * a.B + static_cast<size_t>(b) * (a.K + 1) + r;
+}
 
 __host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
   return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
@@ -138,344 +142,433 @@ SSD_DEV const char *row_ptr(const VocabArgs &a, int tensor, int b, int row, int 
 }
 
 // ---------------------------------------------------------------------------
-// finish queue: super-slot t holds ROW(t - L1), RES(t - L2), FIN(t - L3)
+// loads of records other CTAs published (L2, never a stale L1 line)
 // ---------------------------------------------------------------------------
-__host__ __device__ inline long clampi(long x, long lo, long hi) { return x < lo ? lo : (x > hi ? hi : x); }
-__host__ __device__ inline long sched_start(const Sched &s, long t) {
-  return s.nr * clampi(t - s.L1, 0, s.B) + s.nc * clampi(t - s.L2, 0, s.B) + s.nf * clampi(t - s.L3, 0, s.B);
+SSD_DEV ChunkStat ldcg_stat(const ChunkStat *p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  return ChunkStat{__int_as_float(v.x), __int_as_float(v.y), v.z, v.w};
 }
-__host__ __device__ inline long sched_total(const Sched &s) { return sched_start(s, s.B + s.L3); }
-
-SSD_DEV void sched_decode(const Sched &s, long q, int &kind, int &b, int &idx) {
-  long lo = 0, hi = s.B + s.L3;  // the super-slot t with start(t) <= q < start(t+1)
-  while (hi - lo > 1) {
-    const long mid = (lo + hi) >> 1;
-    if (sched_start(s, mid) <= q) lo = mid;
-    else hi = mid;
-  }
-  const long t = lo;
-  long off = q - sched_start(s, t);
-  if (t - s.L1 >= 0 && t - s.L1 < s.B) {
-    if (off < s.nr) {
-      kind = IT_ROW;
-      b = static_cast<int>(t - s.L1);
-      idx = static_cast<int>(off);
-      return;
-    }
-    off -= s.nr;
-  }
-  if (t - s.L2 >= 0 && t - s.L2 < s.B) {
-    if (off < s.nc) {
-      kind = IT_RES;
-      b = static_cast<int>(t - s.L2);
-      idx = static_cast<int>(off);
-      return;
-    }
-    off -= s.nc;
-  }
-  kind = IT_FIN;
-  b = static_cast<int>(t - s.L3);
-  idx = 0;
+SSD_DEV RowInfo ldcg_row(const RowInfo *p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  const int4 w = __ldcg(reinterpret_cast<const int4 *>(p) + 1);
+  return RowInfo{__int_as_float(v.x), __int_as_float(v.y), v.z,    v.w,
+                 __int_as_float(w.x), __int_as_float(w.y), w.z, __int_as_float(w.w)};
 }
+SSD_DEV PosInfo ldcg_pos(const PosInfo *p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  return PosInfo{v.x, __int_as_float(v.y), __int_as_float(v.z), v.w};
+}
+SSD_DEV ResInfo ldcg_res(const ResInfo *p) {
+  const int2 v = __ldcg(reinterpret_cast<const int2 *>(p));
+  return ResInfo{__int_as_float(v.x), v.y};
+}
+SSD_DEV uint64_t ldcg_key(const uint64_t *p) { return __ldcg(reinterpret_cast<const unsigned long long *>(p)); }
 
-// ---------------------------------------------------------------------------
-// dependency counters
-// ---------------------------------------------------------------------------
+SSD_DEV unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 SSD_DEV uint32_t ld_acquire(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Trace mark k of this CTA (ssd_set_trace): %globaltimer by thread 0.
+SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
+  if (a.trace && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    mk[k] = t;
+  }
+}
+SSD_DEV uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 // ---------------------------------------------------------------------------
-// shared memory of the persistent CTA
+// shared memory of a CTA (after the staged chunk buffers)
 // ---------------------------------------------------------------------------
 struct Smem {
-  float wm[kThreads / 32], ws[kThreads / 32];
-  int wa[kThreads / 32];
-  float red[kThreads / 32 + 1];
-  uint64_t redk[kThreads / 32];
-  int ncand;
-  int item_kind[2], item_b[2], item_idx[2], item_stage[2];
-  long item_q[2];
-  int ok;
-  int found, last_pos;
+  uint64_t bar;    // completion of the TMA copies
+  uint32_t phase;  // completions of `bar` so far
+  int flag, ncand, found, last_pos;
+  float wm[kWarps], ws[kWarps];
+  int wa[kWarps];
+  int wcnt[kWarps];
+  uint64_t redk[kWarps];
+  float wtot[kWarps][kSegVec];  // per-round scan: warp totals, then warp offsets
+  float rtot[kSegVec];          // per-round totals
   float scal[8];
   int ival[8];
   RowInfo ri;
-  float cmass[kMaxChunks];
+  uint64_t cand[kCandCap];
   ChunkStat cs[2][kMaxChunks];
+  float cmass[kMaxChunks];
+  int clast[kMaxChunks];
   uint64_t S[kMaxF];
   float cp[kMaxK], cq[kMaxK], cu[kMaxK];
+  int cd[kMaxK];
+  RowInfo rows[kMaxK + 1];
+  uint64_t keyF[kMaxK + 1];
+  unsigned long long mk[7];  // trace marks (thread 0)
 };
 
-// All threads call after writing an item's results; thread 0 publishes.
-SSD_DEV void signal_done(uint32_t *ctr) {
-  group_sync<kThreads>();  // every thread's writes of the item precede thread 0's release
-  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+// Every thread calls after writing its part of a published result.  True, in
+// every thread of the CTA, for the arrival that completes `total` arrivals on
+// *ctr; the results published before the earlier arrivals are then visible
+// (release / acquire through the counter, ordered with the CTA's own writes by
+// the barrier).
+SSD_DEV bool arrive_last(uint32_t *ctr, uint32_t total, Smem &sh) {
+  __syncthreads();
+  if (threadIdx.x == 0) sh.flag = (atom_add_acq_rel(ctr, 1u) + 1 == total) ? 1 : 0;
+  __syncthreads();
+  return sh.flag != 0;
 }
 
-// ===========================================================================
-// STATS item
-// ===========================================================================
+// Wait for the next completion of sh.bar (bounded; WAIT_TIMEOUT on expiry,
+// then a second bounded wait so no copy is still landing when the buffer is
+// reused).  Every thread calls.
+SSD_DEV void wait_copies(uint32_t *status, Smem &sh) {
+  const uint32_t ph = sh.phase;
+  if (!mbar_wait(&sh.bar, ph & 1u)) {
+    if (threadIdx.x == 0) atomicOr(status, kFlagWaitTimeout);
+    (void)mbar_wait(&sh.bar, ph & 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sh.phase = ph + 1;
+  __syncthreads();
+}
+
+// Stage chunk c of one or two rows (their whole 16-byte vectors; nullptr rows
+// are skipped) in shared memory with TMA bulk copies, and wait for them.
+// Every thread calls.
 template <class E>
-SSD_DEV void issue_stats(const VocabArgs &a, int b, int idx, uint8_t *dst, uint64_t *bar) {
-  const int slot = idx / a.nchunks, c = idx % a.nchunks;
-  const RowSlot rs = a.slot[slot];
+SSD_DEV void issue_rows(const VocabArgs &a, const char *r0, uint8_t *b0, const char *r1, uint8_t *b1, int c,
+                        Smem &sh) {
   const int e0 = c * a.chunk_elems;
   const int n = min(a.chunk_elems, a.V - e0);
   const uint32_t bulk = static_cast<uint32_t>((n * E::kSize) & ~15);
-  const char *src = row_ptr(a, rs.tensor, b, rs.row, E::kSize) + static_cast<int64_t>(e0) * E::kSize;
-  mbar_arrive_expect_tx(bar, bulk);
-  if (bulk) bulk_g2s(dst, src, bulk, bar);
-}
-
-// A thread's running state over its groups (16-byte vectors, or the one tail
-// element): maximum m1 and the group holding it, the second-largest group
-// maximum m2, and the sum of 2^(z kT - mk) with mk = fl(m1 kT).
-struct Stream {
-  float m1, m2, s, mk;
-  int g1;
-};
-
-template <int N>
-SSD_DEV void stream_update(Stream &st, const float *f, int g, float kT, bool greedy) {
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  float vm = f[0];
-#pragma unroll
-  for (int e = 1; e < N; ++e) vm = fmaxf(vm, f[e]);
-  if (vm > st.m2) {
-    if (vm > st.m1) {
-      st.m2 = st.m1;
-      if (!greedy) {
-        const float nk = __fmul_rn(vm, kT);
-        if (st.m1 != NEG_INF) st.s = __fmul_rn(st.s, ex2(__fsub_rn(st.mk, nk)));
-        st.mk = nk;
-      }
-      st.m1 = vm;
-      st.g1 = g;
-    } else {
-      st.m2 = vm;
-    }
-  }
-  if (!greedy && st.m1 != NEG_INF) {
-#pragma unroll
-    for (int e = 0; e < N; ++e) st.s = __fadd_rn(st.s, ex2(__fmaf_rn(f[e], kT, -st.mk)));
+  __syncthreads();  // earlier reads and writes of the buffers are done
+  if (threadIdx.x == 0) {
+    fence_proxy_async();  // ... and ordered before the copies that overwrite them
+    mbar_arrive_expect_tx(&sh.bar, (r0 ? bulk : 0u) + (r1 ? bulk : 0u));
+    if (bulk && r0) bulk_g2s(b0, r0 + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
+    if (bulk && r1) bulk_g2s(b1, r1 + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
   }
 }
-
 template <class E>
-SSD_DEV void stats_item(const VocabArgs &a, int b, int idx, const uint8_t *buf, uint64_t *cand, Smem &sh) {
-  constexpr int NT = kThreads;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = idx / a.nchunks, c = idx % a.nchunks;
-  const RowSlot rs = a.slot[slot];
-  const int e0 = c * a.chunk_elems;
-  const int n = min(a.chunk_elems, a.V - e0);
-  const int nvec = (n * E::kSize) >> 4;
-  const int nbulk = nvec * E::kVec;
-  const int ntail = n - nbulk;  // < kVec elements, only in a row's last chunk
-  const char *row = row_ptr(a, rs.tensor, b, rs.row, E::kSize);
-  const uint4 *v4 = reinterpret_cast<const uint4 *>(buf);
-  const float kT = a.kT;
-  const bool greedy = a.greedy != 0;
-  const float NEG_INF = -__int_as_float(0x7f800000);
-
-  // ---- stream: thread t owns vectors t, t+NT, ...; tail element i belongs to thread i
-  Stream st{NEG_INF, NEG_INF, 0.f, 0.f, -1};
-  for (int v = tid; v < nvec; v += NT) {
-    float f[E::kVec];
-    E::unpack(v4[v], f);
-    stream_update<E::kVec>(st, f, v, kT, greedy);
-  }
-  const float zt = (tid < ntail) ? E::ld(row, e0 + nbulk + tid) : NEG_INF;
-  if (tid < ntail) stream_update<1>(st, &zt, nvec, kT, greedy);
-  // chunk-local index of the thread's first maximum (within group g1)
-  int tidx = 0x7fffffff;
-  if (st.g1 >= 0) {
-    if (st.g1 < nvec) {
-      float f[E::kVec];
-      E::unpack(v4[st.g1], f);
-#pragma unroll
-      for (int e = E::kVec - 1; e >= 0; --e)
-        if (f[e] == st.m1) tidx = st.g1 * E::kVec + e;
-    } else {
-      tidx = nbulk + tid;
-    }
-  }
-  // ---- per warp: max, sum rescaled to it, lowest argmax
-  float wm = st.m1;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-  float sr = 0.f;
-  if (!greedy && st.m1 != NEG_INF) sr = __fmul_rn(st.s, ex2(__fsub_rn(st.mk, __fmul_rn(wm, kT))));
-  sr = warp_sum(sr);
-  int wi = (st.m1 == wm) ? tidx : 0x7fffffff;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) wi = min(wi, __shfl_xor_sync(0xffffffffu, wi, o));
-  if (lane == 0) {
-    sh.wm[warp] = wm;
-    sh.ws[warp] = sr;
-    sh.wa[warp] = wi;
-  }
-  const int F = rs.F;
-  const uint32_t mykey = (st.g1 >= 0) ? f2ord(st.m1) : 0u;
-  uint32_t tau = 0;
-  if (F > 1) {
-    // tau: the F-th largest per-thread maximum; at least F elements reach it
-    for (int bit = 31; bit >= E::kLowBit; --bit) {
-      const uint32_t t = tau | (1u << bit);
-      if (group_sync_count<kThreads>(mykey >= t) >= F) tau = t;
-    }
-    if (tid == 0) sh.ncand = 0;
-  }
-  group_sync<kThreads>();
-  float M = sh.wm[0];
-  for (int w = 1; w < NT / 32; ++w) M = fmaxf(M, sh.wm[w]);
-  int amax = 0x7fffffff;
-  for (int w = 0; w < NT / 32; ++w)
-    if (sh.wm[w] == M) amax = min(amax, sh.wa[w]);
-  uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
-  if (F > 1) {
-    // candidates: a thread whose second group maximum is below tau holds every
-    // element >= tau in group g1; otherwise it rescans all of its groups
-    if (mykey >= tau && st.g1 >= 0) {
-      const bool one = (st.m2 == NEG_INF) || f2ord(st.m2) < tau;
-      if (one) {
-        if (st.g1 < nvec) {
-          float f[E::kVec];
-          E::unpack(v4[st.g1], f);
-#pragma unroll
-          for (int e = 0; e < E::kVec; ++e)
-            if (f2ord(f[e]) >= tau) {
-              const int p = atomicAdd(&sh.ncand, 1);
-              if (p < kCandCap) cand[p] = cand_key(f[e], e0 + st.g1 * E::kVec + e);
-            }
-        } else {
-          const int p = atomicAdd(&sh.ncand, 1);
-          if (p < kCandCap) cand[p] = cand_key(zt, e0 + nbulk + tid);
-        }
-      } else {
-        for (int g = tid; g < nvec; g += NT) {
-          float f[E::kVec];
-          E::unpack(v4[g], f);
-#pragma unroll
-          for (int e = 0; e < E::kVec; ++e)
-            if (f2ord(f[e]) >= tau) {
-              const int p = atomicAdd(&sh.ncand, 1);
-              if (p < kCandCap) cand[p] = cand_key(f[e], e0 + g * E::kVec + e);
-            }
-        }
-        if (tid < ntail && f2ord(zt) >= tau) {
-          const int p = atomicAdd(&sh.ncand, 1);
-          if (p < kCandCap) cand[p] = cand_key(zt, e0 + nbulk + tid);
-        }
-      }
-    }
-    group_sync<kThreads>();
-    const int nc = sh.ncand;
-    if (nc <= kCandCap) {
-      int P = 1;
-      while (P < nc || P < F) P <<= 1;
-      for (int i = nc + tid; i < P; i += NT) cand[i] = 0ull;
-      group_sync<kThreads>();
-      if (P <= 64) {
-        // one warp sorts in registers, descending: key i lives in lane i & 31, half i >> 5
-        if (warp == 0) {
-          uint64_t x[2];
-          x[0] = (lane < P) ? cand[lane] : 0ull;
-          x[1] = (lane + 32 < P) ? cand[lane + 32] : 0ull;
-          for (int k = 2; k <= 64; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-              if (j == 32) {
-                // partner of i is i + 32 in the same lane; k == 64: descending
-                if (x[0] < x[1]) {
-                  const uint64_t t = x[0];
-                  x[0] = x[1];
-                  x[1] = t;
-                }
-              } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int i = lane + 32 * h;
-                  const uint64_t y = __shfl_xor_sync(0xffffffffu, x[h], j);
-                  const bool desc = ((i & k) == 0);
-                  const bool lower = ((i & j) == 0);
-                  const bool keep_max = (desc == lower);
-                  x[h] = keep_max ? (x[h] > y ? x[h] : y) : (x[h] < y ? x[h] : y);
-                }
-              }
-            }
-          }
-          if (lane < F) out[lane] = x[0];
-          if (lane + 32 < F) out[lane + 32] = x[1];
-        }
-      } else {
-        for (int k = 2; k <= P; k <<= 1) {
-          for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < P; i += NT) {
-              const int ixj = i ^ j;
-              if (ixj > i) {
-                const uint64_t x = cand[i], y = cand[ixj];
-                const bool desc = (i & k) == 0;
-                if (desc ? (x < y) : (x > y)) {
-                  cand[i] = y;
-                  cand[ixj] = x;
-                }
-              }
-            }
-            group_sync<kThreads>();
-          }
-        }
-        for (int i = tid; i < F; i += NT) out[i] = cand[i];
-      }
-    } else {
-      // too many ties at the threshold: exact selection, one winner per sweep
-      uint64_t prev = ~0ull;
-      for (int r = 0; r < F; ++r) {
-        uint64_t best = 0;
-        for (int g = tid; g < nvec; g += NT) {
-          float f[E::kVec];
-          E::unpack(v4[g], f);
-#pragma unroll
-          for (int e = 0; e < E::kVec; ++e) {
-            const uint64_t key = cand_key(f[e], e0 + g * E::kVec + e);
-            if (key < prev && key > best) best = key;
-          }
-        }
-        if (tid < ntail) {
-          const uint64_t key = cand_key(zt, e0 + nbulk + tid);
-          if (key < prev && key > best) best = key;
-        }
-        best = block_max_u64<NT>(best, sh.redk);
-        if (tid == 0) out[r] = best;
-        prev = best;
-      }
-    }
-  } else if (F == 1 && tid == 0) {
-    out[0] = cand_key(M, e0 + (amax == 0x7fffffff ? 0 : amax));
-  }
-  if (tid == 0) {
-    float S = 0.f;
-    if (!greedy && M != NEG_INF) {
-      const float Mk = __fmul_rn(M, kT);
-      for (int w = 0; w < NT / 32; ++w)
-        if (sh.wm[w] != NEG_INF)
-          S = __fadd_rn(S, __fmul_rn(sh.ws[w], ex2(__fsub_rn(__fmul_rn(sh.wm[w], kT), Mk))));
-    }
-    ChunkStat cs;
-    cs.m = M;
-    cs.s = S;
-    cs.amax = e0 + (amax == 0x7fffffff ? 0 : amax);  // an all -inf chunk: its first index
-    cs.pad = 0;
-    a.stats[chunk_index(a, b, slot, c)] = cs;
-  }
-  signal_done(stats_done(a, b));
+SSD_DEV void stage_rows(const VocabArgs &a, const char *r0, uint8_t *b0, const char *r1, uint8_t *b1, int c,
+                        Smem &sh) {
+  issue_rows<E>(a, r0, b0, r1, b1, c, sh);
+  wait_copies(a.status, sh);
 }
 
 // ===========================================================================
-// merges (records are first copied to shared memory by all threads at once,
-// so no thread walks a chain of dependent global loads)
+// k_stats: statistics of one staged chunk
+// ===========================================================================
+// Thread t owns the chunk's 16-byte vectors t, t + 256, ... and, in a row's
+// last chunk, tail element t (the < 16 bytes past the last whole vector).
+template <class E>
+struct ChunkView {
+  const uint4 *v4;
+  int e0, nvec, nbulk, ntail;
+  float zt;  // this thread's tail element (-inf if none)
+};
+
+// Candidates of this warp's elements for the top-F (F <= 32): every element
+// whose key reaches tau, the F-th largest lane maximum (ballot radix select),
+// so at least F of them and with them the warp's top-F.  They go to the warp's
+// kWarpCand slots of sh.cand, the count to sh.wcnt[warp]; when they do not fit
+// (ties at tau), the warp's exact top-F instead.
+template <class E>
+SSD_DEV void warp_candidates(const ChunkView<E> &cv, int F, float m1, bool has, Smem &sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t mykey = has ? f2ord(m1) : 0u;
+  uint32_t tau = 0;
+  for (int bit = 31; bit >= E::kLowBit; --bit) {
+    const uint32_t t = tau | (1u << bit);
+    if (__popc(__ballot_sync(0xffffffffu, mykey >= t)) >= F) tau = t;
+  }
+  if (lane == 0) sh.wcnt[warp] = 0;
+  __syncwarp();
+  uint64_t *wc = sh.cand + warp * kWarpCand;
+  if (has && mykey >= tau) {
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j) {
+      const int v = tid + j * kThreads;
+      if (v < cv.nvec) {
+        float f[E::kVec];
+        E::unpack(cv.v4[v], f);
+#pragma unroll
+        for (int e = 0; e < E::kVec; ++e)
+          if (f2ord(f[e]) >= tau) {
+            const int p = atomicAdd(&sh.wcnt[warp], 1);
+            if (p < kWarpCand) wc[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
+          }
+      }
+    }
+    if (tid < cv.ntail && f2ord(cv.zt) >= tau) {
+      const int p = atomicAdd(&sh.wcnt[warp], 1);
+      if (p < kWarpCand) wc[p] = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
+    }
+  }
+  __syncwarp();
+  if (sh.wcnt[warp] > kWarpCand) {
+    // too many ties at the threshold: exact selection, one winner per sweep
+    uint64_t prev = ~0ull;
+    for (int r = 0; r < F; ++r) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int j = 0; j < kSegVec; ++j) {
+        const int v = tid + j * kThreads;
+        if (v < cv.nvec) {
+          float f[E::kVec];
+          E::unpack(cv.v4[v], f);
+#pragma unroll
+          for (int e = 0; e < E::kVec; ++e) {
+            const uint64_t key = cand_key(f[e], cv.e0 + v * E::kVec + e);
+            if (key < prev && key > best) best = key;
+          }
+        }
+      }
+      if (tid < cv.ntail) {
+        const uint64_t key = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
+        if (key < prev && key > best) best = key;
+      }
+      best = warp_max_u64(best);
+      if (lane == 0) wc[r] = best;
+      prev = best;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int k = 0;
+      while (k < F && wc[k] != 0ull) ++k;  // winners are descending; 0 = none left
+      sh.wcnt[warp] = k;
+    }
+  }
+  __syncwarp();
+}
+
+// Candidates of the whole chunk (F > 32): every element whose key reaches the
+// F-th largest per-thread maximum (CTA-wide radix select), into sh.cand[0..
+// sh.ncand); when they do not fit, the chunk's exact top-F.  Every thread calls.
+template <class E>
+SSD_DEV void block_candidates(const ChunkView<E> &cv, int F, float m1, bool has, Smem &sh) {
+  const int tid = threadIdx.x;
+  const uint32_t mykey = has ? f2ord(m1) : 0u;
+  uint32_t tau = 0;
+  for (int bit = 31; bit >= E::kLowBit; --bit) {
+    const uint32_t t = tau | (1u << bit);
+    if (__syncthreads_count(mykey >= t) >= F) tau = t;
+  }
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+  if (has && mykey >= tau) {
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j) {
+      const int v = tid + j * kThreads;
+      if (v < cv.nvec) {
+        float f[E::kVec];
+        E::unpack(cv.v4[v], f);
+#pragma unroll
+        for (int e = 0; e < E::kVec; ++e)
+          if (f2ord(f[e]) >= tau) {
+            const int p = atomicAdd(&sh.ncand, 1);
+            if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
+          }
+      }
+    }
+    if (tid < cv.ntail && f2ord(cv.zt) >= tau) {
+      const int p = atomicAdd(&sh.ncand, 1);
+      if (p < kCandCap) sh.cand[p] = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
+    }
+  }
+  __syncthreads();
+  if (sh.ncand > kCandCap) {
+    uint64_t prev = ~0ull;
+    for (int r = 0; r < F; ++r) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int j = 0; j < kSegVec; ++j) {
+        const int v = tid + j * kThreads;
+        if (v < cv.nvec) {
+          float f[E::kVec];
+          E::unpack(cv.v4[v], f);
+#pragma unroll
+          for (int e = 0; e < E::kVec; ++e) {
+            const uint64_t key = cand_key(f[e], cv.e0 + v * E::kVec + e);
+            if (key < prev && key > best) best = key;
+          }
+        }
+      }
+      if (tid < cv.ntail) {
+        const uint64_t key = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
+        if (key < prev && key > best) best = key;
+      }
+      best = block_max_u64<kThreads>(best, sh.redk);
+      if (tid == 0) sh.cand[r] = best;
+      prev = best;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int k = 0;
+      while (k < F && sh.cand[k] != 0ull) ++k;
+      sh.ncand = k;
+    }
+  }
+  __syncthreads();
+}
+
+// Top-F by rank over candidate groups (group g: n[g] distinct nonzero keys
+// at keys + g * stride, ngroups <= kWarps): the key with r larger keys goes to
+// dst[r] when r < F; dst slots no key fills are set to 0.  Every thread calls;
+// no barrier inside.  Candidate i of the flattened groups is thread i's.
+SSD_DEV void rank_select(const uint64_t *keys, const int *n, int ngroups, int stride, int F, uint64_t *dst) {
+  int off[kWarps + 1];
+  off[0] = 0;
+#pragma unroll
+  for (int g = 0; g < kWarps; ++g) off[g + 1] = off[g] + (g < ngroups ? n[g] : 0);
+  const int total = off[kWarps];
+  for (int i = threadIdx.x; i < F; i += kThreads)
+    if (i >= total) dst[i] = 0ull;
+  for (int i = threadIdx.x; i < total; i += kThreads) {
+    int g = 0;
+#pragma unroll
+    for (int h = 1; h < kWarps; ++h) g += (i >= off[h]) ? 1 : 0;
+    const uint64_t k = keys[g * stride + (i - off[g])];
+    int rank = 0;
+    for (int h = 0; h < ngroups; ++h) {
+      const uint64_t *kh = keys + h * stride;
+      for (int j = 0; j < n[h]; ++j) rank += (kh[j] > k) ? 1 : 0;
+    }
+    if (rank < F) dst[rank] = k;
+  }
+}
+
+// The chunk's record (ChunkStat) and sorted top-F candidate list.
+template <class E>
+SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8_t *buf, Smem &sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const RowSlot rs = a.slot[slot];
+  const float kT = a.kT;
+  const bool greedy = a.greedy != 0;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  ChunkView<E> cv;
+  cv.v4 = reinterpret_cast<const uint4 *>(buf);
+  cv.e0 = c * a.chunk_elems;
+  const int n = min(a.chunk_elems, a.V - cv.e0);
+  cv.nvec = (n * E::kSize) >> 4;
+  cv.nbulk = cv.nvec * E::kVec;
+  cv.ntail = n - cv.nbulk;
+  cv.zt = (tid < cv.ntail) ? E::ld(row_ptr(a, rs.tensor, b, rs.row, E::kSize), cv.e0 + cv.nbulk + tid) : NEG_INF;
+  const bool has = tid < cv.nvec || tid < cv.ntail;
+
+  // pass 1: the thread's maximum (packed bf16 maxima for bf16 rows)
+  float m1;
+  if constexpr (E::kSize == 2) {
+    uint32_t mx = 0xFF80FF80u;  // two bf16 -inf
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j) {
+      const int v = tid + j * kThreads;
+      if (v < cv.nvec) {
+        const uint4 w = cv.v4[v];
+        mx = bmax2(mx, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+      }
+    }
+    m1 = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+  } else {
+    float mx = NEG_INF;
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j) {
+      const int v = tid + j * kThreads;
+      if (v < cv.nvec) {
+        const uint4 w = cv.v4[v];
+        mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                             fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
+      }
+    }
+    m1 = mx;
+  }
+  m1 = fmaxf(m1, cv.zt);
+  const float wm = warp_max(m1);
+  // a lane holding the warp maximum finds its lowest index (elements in index order)
+  int i1 = kNone;
+  if (m1 == wm) {
+#pragma unroll 1
+    for (int j = 0; j < kSegVec && i1 == kNone; ++j) {
+      const int v = tid + j * kThreads;
+      if (v >= cv.nvec) break;
+      float f[E::kVec];
+      E::unpack(cv.v4[v], f);
+#pragma unroll
+      for (int e = E::kVec - 1; e >= 0; --e)
+        if (f[e] == wm) i1 = v * E::kVec + e;
+    }
+    if (i1 == kNone && tid < cv.ntail && cv.zt == wm) i1 = cv.nbulk + tid;
+  }
+  int wi = i1;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) wi = min(wi, __shfl_xor_sync(0xffffffffu, wi, o));
+  // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed FMA / ADD
+  float s = 0.f;
+  if (!greedy && wm != NEG_INF) {
+    const float Mk = __fmul_rn(wm, kT);
+    const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
+    uint64_t acc = pack2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j) {
+      const int v = tid + j * kThreads;
+      if (v < cv.nvec) {
+        const uint4 w = cv.v4[v];
+#pragma unroll
+        for (int h = 0; h < E::kPairs; ++h) {
+          float x0, x1;
+          unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
+          acc = add2(acc, pack2(ex2(x0), ex2(x1)));
+        }
+      }
+    }
+    float lo, hi;
+    unpack2(acc, lo, hi);
+    s = __fadd_rn(lo, hi);
+    if (tid < cv.ntail) s = __fadd_rn(s, ex2(__fmaf_rn(cv.zt, kT, -Mk)));
+  }
+  s = warp_sum(s);
+  if (lane == 0) {
+    sh.wm[warp] = wm;
+    sh.ws[warp] = s;
+    sh.wa[warp] = wi;
+  }
+  const int F = rs.F;
+  if (F > 1 && F <= kWarpF) warp_candidates<E>(cv, F, m1, has, sh);
+  else if (F > kWarpF) block_candidates<E>(cv, F, m1, has, sh);
+  __syncthreads();
+  uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
+  if (F > 1 && F <= kWarpF) rank_select(sh.cand, sh.wcnt, kWarps, kWarpCand, F, out);
+  else if (F > kWarpF) rank_select(sh.cand, &sh.ncand, 1, 0, F, out);
+  if (tid == 0) {
+    float M = sh.wm[0];
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sh.wm[w]);
+    int amax = kNone;
+    for (int w = 0; w < kWarps; ++w)
+      if (sh.wm[w] == M) amax = min(amax, sh.wa[w]);
+    float S = 0.f;
+    if (!greedy && M != NEG_INF) {
+      const float Mk = __fmul_rn(M, kT);
+      for (int w = 0; w < kWarps; ++w)
+        if (sh.wm[w] != NEG_INF) S = __fadd_rn(S, __fmul_rn(sh.ws[w], ex2(__fsub_rn(__fmul_rn(sh.wm[w], kT), Mk))));
+    }
+    if (amax == kNone) amax = 0;  // an all -inf chunk: its first index
+    if (F == 1) out[0] = cand_key(M, cv.e0 + amax);
+    a.stats[chunk_index(a, b, slot, c)] = ChunkStat{M, S, cv.e0 + amax, 0};
+  }
+}
+
+// ===========================================================================
+// merges
 // ===========================================================================
 struct RowStat {
   float m, s;
@@ -498,9 +591,10 @@ SSD_DEV RowStat merge_row_smem(const VocabArgs &a, const ChunkStat *cs) {
   return r;
 }
 
-// Warp-cooperative k-way merge of the sorted per-chunk candidate lists
-// (list c at lists[c * stride], F keys each) into the top-F list `dst`
-// (descending keys; sentinel 0 past the end).
+// Warp-cooperative k-way merge of the sorted per-chunk candidate lists (list
+// c at lists[c * stride], F keys each, published by other CTAs) into the
+// top-F list `dst` (descending keys; sentinel 0 past the end).  Used when the
+// lists hold more than kRankMax keys.
 SSD_DEV void merge_topf(const uint64_t *lists, size_t stride, int nchunks, int F, uint64_t *dst) {
   constexpr int L = kMaxChunks / 32;
   const int lane = threadIdx.x & 31;
@@ -510,7 +604,7 @@ SSD_DEV void merge_topf(const uint64_t *lists, size_t stride, int nchunks, int F
   for (int l = 0; l < L; ++l) {
     const int c = lane + 32 * l;
     ptr[l] = 0;
-    head[l] = (c < nchunks && F > 0) ? lists[c * stride] : 0ull;
+    head[l] = (c < nchunks && F > 0) ? ldcg_key(lists + c * stride) : 0ull;
   }
   for (int r = 0; r < F; ++r) {
     uint64_t best = 0;
@@ -529,7 +623,7 @@ SSD_DEV void merge_topf(const uint64_t *lists, size_t stride, int nchunks, int F
         if (l == bl) {
           const int c = lane + 32 * l;
           ++ptr[l];
-          head[l] = (ptr[l] < F) ? lists[c * stride + ptr[l]] : 0ull;
+          head[l] = (ptr[l] < F) ? ldcg_key(lists + c * stride + ptr[l]) : 0ull;
         }
     }
   }
@@ -537,7 +631,7 @@ SSD_DEV void merge_topf(const uint64_t *lists, size_t stride, int nchunks, int F
 }
 
 // ===========================================================================
-// inverse-CDF draws over one chunk of a row (one CTA)
+// inverse-CDF draws over one staged chunk (one CTA)
 // ===========================================================================
 // Weight functors: operator()(zt, zd, idx) -> weight >= 0 with a fixed sequence
 // of correctly rounded operations, so every pass over the same elements agrees.
@@ -567,131 +661,194 @@ struct WResidual {  // max(0, p_i - q'_i)
   }
 };
 
-// A chunk is split into kThreads contiguous segments of kSegVec vectors; thread
-// t owns elements [start + t*SEG, start + (t+1)*SEG).  Its segment sum is taken
-// in index order, the segments are combined by one block-wide exclusive scan:
-// that fixed order defines the chunk's running weights for both range_total
-// and range_find.
-constexpr int kSegVec = 6;
-static_assert(kChunkBytes == kThreads * kSegVec * 16, "a chunk is one segment per thread");
-
-// 16 raw bytes of a row at element i0; lanes at or past `end` are left zero
-// (callers mask them by index).
+// One chunk of the target and / or draft row staged in shared memory (whole
+// vectors); its < 16 tail bytes are read from global memory.
 template <class E>
-SSD_DEV uint4 ld_raw(const char *row, int i0, int end) {
-  if (i0 + E::kVec <= end) return __ldg(reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(i0) * E::kSize));
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  for (int e = 0; e < E::kVec && i0 + e < end; ++e) {
-    if (E::kSize == 4) {
-      w[e] = __ldg(reinterpret_cast<const uint32_t *>(row) + i0 + e);
-    } else {
-      const uint32_t h = __ldg(reinterpret_cast<const unsigned short *>(row) + i0 + e);
-      w[e >> 1] |= h << ((e & 1) * 16);
-    }
+struct Staged {
+  const uint8_t *t, *d;  // staged chunks (unused rows: nullptr)
+  const char *rt, *rd;   // the rows in global memory
+  int e0, n, nbulk;      // first element, elements, elements in whole vectors
+};
+template <class E>
+SSD_DEV Staged<E> staged(const VocabArgs &a, const uint8_t *bt, const char *rt, const uint8_t *bd, const char *rd,
+                         int c) {
+  Staged<E> S;
+  S.t = bt;
+  S.d = bd;
+  S.rt = rt;
+  S.rd = rd;
+  S.e0 = c * a.chunk_elems;
+  S.n = min(a.chunk_elems, a.V - S.e0);
+  S.nbulk = ((S.n * E::kSize) >> 4) * E::kVec;
+  return S;
+}
+template <class E>
+SSD_DEV void staged_vec(const uint8_t *buf, const char *row, int e0, int n, int nbulk, int i0, float *f) {
+  if (i0 < nbulk) {
+    E::unpack(*reinterpret_cast<const uint4 *>(buf + static_cast<size_t>(i0) * E::kSize), f);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e) f[e] = (i0 + e < n) ? E::ld(row, e0 + i0 + e) : 0.f;
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// This thread's segment of one or two rows, loaded in one round of 16-byte loads.
-template <class E>
-struct Segment {
-  uint4 t[kSegVec], d[kSegVec];
-  SSD_DEV void load(const char *rowT, const char *rowD, int s0, int end) {
+// Rounds: the chunk's vectors in kSegVec rounds of kThreads, thread t owning
+// vector j * kThreads + t of round j (vocabulary order: round, thread,
+// element).  p[j] = the thread's weight sum of its round-j vector, in element
+// order; *last = its last index with positive weight.
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV void round_partials(const Staged<E> &S, const WF &wf, float *p, int *last) {
 #pragma unroll
-    for (int v = 0; v < kSegVec; ++v) {
-      t[v] = rowT ? ld_raw<E>(rowT, s0 + v * E::kVec, end) : make_uint4(0, 0, 0, 0);
-      d[v] = rowD ? ld_raw<E>(rowD, s0 + v * E::kVec, end) : make_uint4(0, 0, 0, 0);
-    }
-  }
-  // sum of weights in index order; *last = last index with w > 0
-  template <class WF>
-  SSD_DEV float sum(int s0, int end, const WF &wf, int *last) const {
+  for (int j = 0; j < kSegVec; ++j) {
+    const int i0 = (j * kThreads + static_cast<int>(threadIdx.x)) * E::kVec;
     float acc = 0.f;
-#pragma unroll
-    for (int v = 0; v < kSegVec; ++v) {
+    if (i0 < S.n) {
       float ft[E::kVec], fd[E::kVec];
-      E::unpack(t[v], ft);
-      E::unpack(d[v], fd);
+      if constexpr (HT) staged_vec<E>(S.t, S.rt, S.e0, S.n, S.nbulk, i0, ft);
+      if constexpr (HD) staged_vec<E>(S.d, S.rd, S.e0, S.n, S.nbulk, i0, fd);
 #pragma unroll
       for (int e = 0; e < E::kVec; ++e) {
-        const int i = s0 + v * E::kVec + e;
-        const float x = (i < end) ? wf(ft[e], fd[e], i) : 0.f;
+        const float x = (i0 + e < S.n) ? wf(HT ? ft[e] : 0.f, HD ? fd[e] : 0.f, S.e0 + i0 + e) : 0.f;
         acc = __fadd_rn(acc, x);
-        if (x > 0.f) *last = i;
+        if (x > 0.f) *last = S.e0 + i0 + e;
       }
     }
-    return acc;
+    p[j] = acc;
   }
-  // first index whose running weight (offset by `base`) exceeds `target`, with w > 0; -1 if none
-  template <class WF>
-  SSD_DEV int find(int s0, int end, const WF &wf, float base, float target) const {
-    float run = 0.f;
-    int hit = -1;
-#pragma unroll
-    for (int v = 0; v < kSegVec; ++v) {
-      float ft[E::kVec], fd[E::kVec];
-      E::unpack(t[v], ft);
-      E::unpack(d[v], fd);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e) {
-        const int i = s0 + v * E::kVec + e;
-        const float x = (i < end) ? wf(ft[e], fd[e], i) : 0.f;
-        run = __fadd_rn(run, x);
-        if (hit < 0 && x > 0.f && __fadd_rn(base, run) > target) hit = i;
-      }
-    }
-    return hit;
-  }
-};
+}
 
-// Total weight of [start, end) (end - start <= one chunk) in the segment order;
-// *last = last index with w > 0 (-1 if none).
-template <class E, class WF>
-SSD_DEV float range_total(const char *rowT, const char *rowD, int start, int end, const WF &wf, int *last,
-                          Smem &sh) {
-  constexpr int SEG = kSegVec * E::kVec;
-  const int tid = threadIdx.x;
-  const int s0 = start + tid * SEG;
-  Segment<E> seg;
-  seg.load(rowT, rowD, s0, end);
-  int lp = -1;
-  const float t = seg.sum(s0, end, wf, &lp);
-  if (tid == 0) sh.last_pos = -1;
-  const float ex = block_excl_scan<kThreads>(t, sh.red);  // (contains barriers)
-  if (tid == kThreads - 1) sh.scal[0] = __fadd_rn(ex, t);
-  atomicMax(&sh.last_pos, lp);
+// Per round j: ex[j] = exclusive prefix of p[j] over the threads (warp
+// Hillis-Steele scan, warp offsets summed in warp order), sh.rtot[j] = the
+// round total.  Contains barriers.
+SSD_DEV void round_scan(const float *p, float *ex, Smem &sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float inc[kSegVec];
+#pragma unroll
+  for (int j = 0; j < kSegVec; ++j) inc[j] = p[j];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j) {
+      const float t = __shfl_up_sync(0xffffffffu, inc[j], o);
+      if (lane >= o) inc[j] = __fadd_rn(inc[j], t);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kSegVec; ++j) {
+    const float t = __shfl_up_sync(0xffffffffu, inc[j], 1);
+    ex[j] = (lane == 0) ? 0.f : t;
+    if (lane == 31) sh.wtot[warp][j] = inc[j];
+  }
   group_sync<kThreads>();
-  const float tot = sh.scal[0];
+  if (threadIdx.x < kSegVec) {
+    const int j = threadIdx.x;
+    float run = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float t = sh.wtot[w][j];
+      sh.wtot[w][j] = run;
+      run = __fadd_rn(run, t);
+    }
+    sh.rtot[j] = run;
+  }
+  group_sync<kThreads>();
+#pragma unroll
+  for (int j = 0; j < kSegVec; ++j) ex[j] = __fadd_rn(sh.wtot[warp][j], ex[j]);
+  group_sync<kThreads>();
+}
+
+// Total weight of the staged chunk (rounds summed in order); *last = its last
+// index with positive weight (-1 if none).
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV float range_total(const Staged<E> &S, const WF &wf, int *last, Smem &sh) {
+  float p[kSegVec], ex[kSegVec];
+  int lp = -1;
+  round_partials<E, HT, HD>(S, wf, p, &lp);
+  if (threadIdx.x == 0) sh.last_pos = -1;
+  round_scan(p, ex, sh);
+  atomicMax(&sh.last_pos, lp);
+  if (threadIdx.x == 0) {
+    float W = 0.f;
+    for (int j = 0; j < kSegVec; ++j) W = __fadd_rn(W, sh.rtot[j]);
+    sh.scal[0] = W;
+  }
+  group_sync<kThreads>();
+  const float W = sh.scal[0];
   *last = sh.last_pos;
   group_sync<kThreads>();
-  return tot;
+  return W;
 }
 
-// First i in [start, end) whose running weight from `start` (segment order as in
-// range_total) exceeds `target` and whose weight is positive; -1 when none.
-template <class E, class WF>
-SSD_DEV int range_find(const char *rowT, const char *rowD, int start, int end, float target, const WF &wf,
-                       Smem &sh) {
-  constexpr int SEG = kSegVec * E::kVec;
-  const int tid = threadIdx.x;
-  const int s0 = start + tid * SEG;
-  Segment<E> seg;
-  seg.load(rowT, rowD, s0, end);
+// First index of the staged chunk whose running weight (the order of
+// range_total) exceeds `target` and whose weight is positive; where rounding
+// leaves no such index in the round that holds the target, that round's last
+// positive index; -1 when the chunk has no weight.
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV int range_find(const Staged<E> &S, float target, const WF &wf, Smem &sh) {
+  float p[kSegVec], ex[kSegVec];
   int lp = -1;
-  const float t = seg.sum(s0, end, wf, &lp);
-  const float ex = block_excl_scan<kThreads>(t, sh.red);
-  if (tid == 0) sh.found = 0x7fffffff;
-  group_sync<kThreads>();
-  // the segment where the running weight first exceeds the target (the earliest wins)
-  if (t > 0.f && __fadd_rn(ex, t) > target) {
-    int hit = seg.find(s0, end, wf, ex, target);
-    if (hit < 0) hit = lp;  // rounding inside the segment: its last positive element
-    atomicMin(&sh.found, hit);
+  round_partials<E, HT, HD>(S, wf, p, &lp);
+  round_scan(p, ex, sh);
+  if (threadIdx.x == 0) {
+    // the round holding the target: cumulative round totals in order
+    int js = -1, jl = -1;
+    float base = 0.f, bs = 0.f, bl = 0.f;
+    for (int j = 0; j < kSegVec; ++j) {
+      const float R = sh.rtot[j];
+      const float nb = __fadd_rn(base, R);
+      if (R > 0.f) {
+        jl = j;
+        bl = base;
+        if (js < 0 && nb > target) {
+          js = j;
+          bs = base;
+        }
+      }
+      base = nb;
+    }
+    if (js < 0) {  // rounding left the target past the end: the last round with weight
+      js = jl;
+      bs = bl;
+    }
+    sh.ival[5] = js;
+    sh.scal[5] = bs;
+    sh.found = kNone;
+    sh.last_pos = -1;
   }
   group_sync<kThreads>();
-  const int r = sh.found;
+  const int js = sh.ival[5];
+  if (js >= 0) {
+    float pj = 0.f, ej = 0.f;
+#pragma unroll
+    for (int j = 0; j < kSegVec; ++j)
+      if (j == js) {
+        pj = p[j];
+        ej = ex[j];
+      }
+    if (pj > 0.f) {
+      const float b0 = __fadd_rn(sh.scal[5], ej);
+      const int i0 = (js * kThreads + static_cast<int>(threadIdx.x)) * E::kVec;
+      float ft[E::kVec], fd[E::kVec];
+      if constexpr (HT) staged_vec<E>(S.t, S.rt, S.e0, S.n, S.nbulk, i0, ft);
+      if constexpr (HD) staged_vec<E>(S.d, S.rd, S.e0, S.n, S.nbulk, i0, fd);
+      float run = 0.f;
+      int hit = -1, lpos = -1;
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e) {
+        const float x = (i0 + e < S.n) ? wf(HT ? ft[e] : 0.f, HD ? fd[e] : 0.f, S.e0 + i0 + e) : 0.f;
+        run = __fadd_rn(run, x);
+        if (x > 0.f) {
+          lpos = S.e0 + i0 + e;
+          if (hit < 0 && __fadd_rn(b0, run) > target) hit = lpos;
+        }
+      }
+      atomicMax(&sh.last_pos, lpos);
+      if (__fadd_rn(b0, pj) > target) atomicMin(&sh.found, hit >= 0 ? hit : lpos);
+    }
+  }
   group_sync<kThreads>();
-  return r == 0x7fffffff ? -1 : r;
+  const int r = (js < 0) ? -1 : (sh.found != kNone ? sh.found : sh.last_pos);
+  group_sync<kThreads>();
+  return r;
 }
 
 // Locate the chunk holding u * W among per-chunk masses sh.cmass[0..nchunks)
@@ -726,37 +883,29 @@ SSD_DEV void locate_chunk(int nchunks, float u, Smem &sh) {
   group_sync<kThreads>();
 }
 
-// Draw by the chunk masses in sh.cmass, then one pass over that chunk.  -1 when
-// the masses sum to zero.  When the chunk's own running weight falls short of
-// the located target (the masses were rounded differently), its last index
-// with positive weight is taken.
-template <class E, class WF>
-SSD_DEV int chunked_draw(const VocabArgs &a, const char *rowT, const char *rowD, float u, const WF &wf,
-                         float *W_out, Smem &sh) {
+// Draw by the chunk masses in sh.cmass: locate the chunk, stage it (the rows
+// given: target rowT into bt, draft rowD into bd), one pass over it.  -1 when
+// the masses sum to zero or the staged chunk has no weight.
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV int chunked_draw(const VocabArgs &a, const char *rowT, uint8_t *bt, const char *rowD, uint8_t *bd, float u,
+                         const WF &wf, float *W_out, Smem &sh) {
   locate_chunk(a.nchunks, u, sh);
   const int cs = sh.ival[0];
   const float local = sh.scal[1];
   *W_out = sh.scal[2];
-  group_sync<kThreads>();
   if (cs < 0) return -1;
-  const int start = cs * a.chunk_elems, end = min(a.V, start + a.chunk_elems);
-  int d = range_find<E>(rowT, rowD, start, end, local, wf, sh);
-  if (d < 0) {
-    int last;
-    (void)range_total<E>(rowT, rowD, start, end, wf, &last, sh);
-    d = last;
-  }
-  return d;
+  stage_rows<E>(a, HT ? rowT : nullptr, bt, HD ? rowD : nullptr, bd, cs, sh);
+  return range_find<E, HT, HD>(staged<E>(a, bt, rowT, bd, rowD, cs), local, wf, sh);
 }
 
 // Exact chunk masses by one pass over every chunk of the row (used for Saguaro
 // sampling when the down-weighted mass makes the statistics' masses inexact).
 template <class E, class WF>
-SSD_DEV void exact_chunk_masses(const VocabArgs &a, const char *rowT, const char *rowD, const WF &wf,
-                                Smem &sh) {
+SSD_DEV void exact_chunk_masses_draft(const VocabArgs &a, const char *rowD, uint8_t *bd, const WF &wf, Smem &sh) {
   for (int c = 0; c < a.nchunks; ++c) {
+    stage_rows<E>(a, nullptr, nullptr, rowD, bd, c, sh);
     int last;
-    const float t = range_total<E>(rowT, rowD, c * a.chunk_elems, min(a.V, (c + 1) * a.chunk_elems), wf, &last, sh);
+    const float t = range_total<E, false, true>(staged<E>(a, nullptr, nullptr, bd, rowD, c), wf, &last, sh);
     if (threadIdx.x == 0) sh.cmass[c] = t;
   }
   group_sync<kThreads>();
@@ -764,71 +913,100 @@ SSD_DEV void exact_chunk_masses(const VocabArgs &a, const char *rowT, const char
 
 SSD_DEV float norm_N(float C, float sq) { return __fsub_rn(1.f, __fmul_rn(__fsub_rn(1.f, C), sq)); }
 
-// Acceptance chain of sequence b: PosInfo and uniforms staged in shared memory
-// by K threads, walked by thread 0.  Every thread returns the accept count.
-SSD_DEV int chain(const VocabArgs &a, int b, Smem &sh) {
-  for (int t = threadIdx.x; t < a.K; t += kThreads) {
-    const PosInfo pi = a.pos[static_cast<size_t>(b) * a.K + t];
-    sh.cp[t] = pi.p;
-    sh.cq[t] = pi.q;
-    sh.cu[t] = a.u_acc[static_cast<size_t>(b) * a.K + t];
+// p_{r+1} (target row r) drawn by its chunk masses from the published chunk
+// records; the row's argmax if they are all zero.
+template <class E>
+SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, float u, uint8_t *buf, Smem &sh) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float mtk = __fmul_rn(row.mt, a.kT);
+  for (int c = threadIdx.x; c < a.nchunks; c += kThreads) {
+    const ChunkStat cs = ldcg_stat(a.stats + chunk_index(a, b, a.tsl[r], c));
+    sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), mtk)));
   }
   group_sync<kThreads>();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int t = 0; t < a.K; ++t) {
-      if (sh.cp[t] >= 0.f && __fmul_rn(sh.cu[t], sh.cq[t]) < sh.cp[t]) ++acc;
-      else break;
-    }
-    sh.ival[1] = acc;
-  }
-  group_sync<kThreads>();
-  const int acc = sh.ival[1];
-  group_sync<kThreads>();
-  return acc;
+  const WTarget wp{mtk, a.kT};
+  float Wp;
+  const int d = chunked_draw<E, true, false>(a, row_ptr(a, 0, b, r, E::kSize), buf, nullptr, nullptr, u, wp, &Wp, sh);
+  return (d >= 0) ? d : row.at;
+}
+
+SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64_t keyF, int F) {
+  WResidual wf;
+  wf.mtk = __fmul_rn(ri.mt, a.kT);
+  wf.kT = a.kT;
+  wf.inv_st = __frcp_rn(ri.st);
+  wf.mdk = __fmul_rn(ri.md, a.kT);
+  const float sN = __fmul_rn(ri.sd, norm_N(a.C, ri.sq));
+  wf.f1 = __frcp_rn(sN);
+  wf.fC = __fdiv_rn(a.C, sN);
+  wf.hasS = F > 0;
+  wf.keyF = keyF;
+  return wf;
 }
 
 // ===========================================================================
-// ROW item: merge row r, sample d_{r+1}, gather p(d), q'(d), write guesses
+// pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
 // ===========================================================================
 template <class E>
-__device__ __noinline__ void row_item(const VocabArgs &a, int b, int r, uint64_t *lists, Smem &sh) {
-  const int tid = threadIdx.x, warp = tid >> 5;
+SSD_DEV void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh) {
+  const int tid = threadIdx.x;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  const int F = a.F[r];
-  uint64_t *S = a.S + (static_cast<size_t>(b) * (a.K + 1) + r) * a.Fcap;
-  // stage the chunk records of (target row r, draft row r) and the draft's candidate lists
+  const int ts = a.tsl[r], ds = a.dsl[r];
+  const int F = (ds >= 0) ? a.Fs[r] : 0;
+  const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
+  // stage the chunk records of the pair and the draft's candidate lists
   for (int c = tid; c < a.nchunks; c += kThreads) {
-    if (a.tslot0 >= 0) sh.cs[0][c] = a.stats[chunk_index(a, b, a.tslot0 + r, c)];
-    sh.cs[1][c] = a.stats[chunk_index(a, b, a.dslot0 + r, c)];
+    if (ts >= 0) sh.cs[0][c] = ldcg_stat(a.stats + chunk_index(a, b, ts, c));
+    if (ds >= 0) sh.cs[1][c] = ldcg_stat(a.stats + chunk_index(a, b, ds, c));
   }
-  const bool lists_smem = a.nchunks * F <= kCandCap;
-  if (lists_smem) {
-    const uint64_t *src = a.cands + chunk_index(a, b, a.dslot0 + r, 0) * a.Fcap;
-    for (int i = tid; i < a.nchunks * F; i += kThreads) lists[i] = src[(i / F) * a.Fcap + (i % F)];
+  uint64_t *lists = reinterpret_cast<uint64_t *>(buf);
+  const int nl = a.nchunks * F;
+  const bool by_rank = nl <= kRankMax;
+  if (F > 0 && by_rank) {
+    const uint64_t *src = a.cands + chunk_index(a, b, ds, 0) * a.Fcap;
+    for (int i = tid; i < nl; i += kThreads) {
+      const uint64_t k = ldcg_key(src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
+      lists[i] = k;
+    }
   }
-  group_sync<kThreads>();
+  __syncthreads();
   if (tid == 0) {
     RowInfo ri;
     memset(&ri, 0, sizeof(ri));
-    if (a.tslot0 >= 0) {
+    if (ts >= 0) {
       const RowStat t = merge_row_smem(a, sh.cs[0]);
       ri.mt = t.m;
       ri.st = t.s;
       ri.at = t.amax;
     }
-    const RowStat d = merge_row_smem(a, sh.cs[1]);
-    ri.md = d.m;
-    ri.sd = d.s;
-    ri.ad = d.amax;
+    if (ds >= 0) {
+      const RowStat d = merge_row_smem(a, sh.cs[1]);
+      ri.md = d.m;
+      ri.sd = d.s;
+      ri.ad = d.amax;
+    }
     sh.ri = ri;
   }
-  if (warp == 1) {
-    if (lists_smem) merge_topf(lists, F, a.nchunks, F, sh.S);
-    else merge_topf(a.cands + chunk_index(a, b, a.dslot0 + r, 0) * a.Fcap, a.Fcap, a.nchunks, F, sh.S);
+  if (F > 0) {
+    if (by_rank) {
+      // zero keys (a chunk with fewer than F elements) take no rank
+      for (int i = tid; i < nl; i += kThreads) {
+        const uint64_t k = lists[i];
+        if (k == 0ull) continue;
+        int rank = 0;
+        for (int j = 0; j < nl && rank < F; ++j) rank += (lists[j] > k) ? 1 : 0;
+        if (rank < F) sh.S[rank] = k;
+      }
+      int nz = 0;
+      for (int i0 = 0; i0 < nl; i0 += kThreads) nz += __syncthreads_count(i0 + tid < nl && lists[i0 + tid] != 0ull);
+      for (int i = nz + tid; i < F; i += kThreads) sh.S[i] = 0ull;
+    } else if (tid < 32) {
+      merge_topf(a.cands + chunk_index(a, b, ds, 0) * a.Fcap, a.Fcap, a.nchunks, F, sh.S);
+    }
   }
-  group_sync<kThreads>();
-  for (int i = tid; i < F; i += kThreads) S[i] = sh.S[i];  // for the residual and lookup items
+  __syncthreads();
+  if (a.do_verify || a.do_lookup)
+    for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
   const float mdk = __fmul_rn(sh.ri.md, a.kT);
   if (tid == 0) {
     float sq = 0.f;
@@ -839,12 +1017,12 @@ __device__ __noinline__ void row_item(const VocabArgs &a, int b, int r, uint64_t
     }
     sh.ri.sq = sq;
   }
-  group_sync<kThreads>();
+  __syncthreads();
   const RowInfo ri = sh.ri;
   const uint64_t keyF = F > 0 ? sh.S[F - 1] : 0ull;
-  if (a.do_predict) {
+  if (a.do_predict && ds >= 0) {
     const int sumF = a.foff[a.K + 1];
-    for (int i = tid; i < F; i += kThreads) {
+    for (int i = tid; i < a.F[r]; i += kThreads) {
       const uint64_t key = sh.S[i];
       a.guess[static_cast<size_t>(b) * sumF + a.foff[r] + i] = cand_idx(key);
       if (a.guess_q) {
@@ -855,6 +1033,7 @@ __device__ __noinline__ void row_item(const VocabArgs &a, int b, int r, uint64_t
       }
     }
   }
+  mark(a, sh.mk, 3);
   const char *rowD = row_ptr(a, 1, b, r, E::kSize);
   if (r < a.K && (a.do_sample || a.do_verify)) {
     int d;
@@ -867,14 +1046,14 @@ __device__ __noinline__ void row_item(const VocabArgs &a, int b, int r, uint64_t
         const WSaguaro wf{mdk, a.kT, a.C, keyF, F > 0};
         const float u = a.u_draft[static_cast<size_t>(b) * a.K + r];
         if (__fmul_rn(__fsub_rn(1.f, a.C), ri.sq) > 0.875f) {
-          exact_chunk_masses<E>(a, nullptr, rowD, wf, sh);
+          exact_chunk_masses_draft<E>(a, rowD, buf, wf, sh);
         } else {
           // chunk masses of q' (unnormalised): s_c 2^(Mk_c - mdk) - (1 - C) sum_{i in S, in c} e_i
           for (int c = tid; c < a.nchunks; c += kThreads) {
             const ChunkStat cs = sh.cs[1][c];
             sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), mdk)));
           }
-          group_sync<kThreads>();
+          __syncthreads();
           if (tid == 0 && a.C < 1.f) {
             for (int i = 0; i < F; ++i) {
               if (!sh.S[i]) continue;
@@ -884,10 +1063,10 @@ __device__ __noinline__ void row_item(const VocabArgs &a, int b, int r, uint64_t
             }
             for (int c = 0; c < a.nchunks; ++c) sh.cmass[c] = fmaxf(sh.cmass[c], 0.f);
           }
-          group_sync<kThreads>();
+          __syncthreads();
         }
         float W;
-        d = chunked_draw<E>(a, nullptr, rowD, u, wf, &W, sh);
+        d = chunked_draw<E, false, true>(a, nullptr, nullptr, rowD, buf, u, wf, &W, sh);
         if (d < 0) d = ri.ad;
         const float zd = E::ld(rowD, d);
         const bool ins = F > 0 && cand_key(zd, d) >= keyF;
@@ -929,116 +1108,74 @@ __device__ __noinline__ void row_item(const VocabArgs &a, int b, int r, uint64_t
       }
     }
   }
-  if (tid == 0) a.rows[static_cast<size_t>(b) * (a.K + 1) + r] = ri;
-  signal_done(row_done(a, b));
-}
-
-SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64_t keyF, int F) {
-  WResidual wf;
-  wf.mtk = __fmul_rn(ri.mt, a.kT);
-  wf.kT = a.kT;
-  wf.inv_st = __frcp_rn(ri.st);
-  wf.mdk = __fmul_rn(ri.md, a.kT);
-  const float sN = __fmul_rn(ri.sd, norm_N(a.C, ri.sq));
-  wf.f1 = __frcp_rn(sN);
-  wf.fC = __fdiv_rn(a.C, sN);
-  wf.hasS = F > 0;
-  wf.keyF = keyF;
-  return wf;
+  if (tid == 0) a.rows[rr] = ri;
 }
 
 // ===========================================================================
-// RES item: acceptance chain, residual mass of chunk c of row a
+// sequence finish: acceptance chain, bonus draw, outputs, cache lookup
 // ===========================================================================
-template <class E>
-__device__ __noinline__ void res_item(const VocabArgs &a, int b, int c, Smem &sh) {
-  const int acc = chain(a, b, sh);
-  ResInfo ri{0.f, -1};
-  if (acc < a.K && !a.greedy) {
-    const RowInfo row = a.rows[static_cast<size_t>(b) * (a.K + 1) + acc];
-    const int F = a.F[acc];
-    const uint64_t keyF = F > 0 ? a.S[(static_cast<size_t>(b) * (a.K + 1) + acc) * a.Fcap + F - 1] : 0ull;
-    const WResidual wf = residual_weights(a, row, keyF, F);
-    const int start = c * a.chunk_elems, end = min(a.V, start + a.chunk_elems);
-    int last;
-    ri.w = range_total<E>(row_ptr(a, 0, b, acc, E::kSize), row_ptr(a, 1, b, acc, E::kSize), start, end, wf,
-                          &last, sh);
-    ri.last = last;
-  }
-  if (threadIdx.x == 0) a.res[static_cast<size_t>(b) * a.nchunks + c] = ri;
-  signal_done(res_done(a, b));
-}
-
-// ===========================================================================
-// FIN item: bonus draw, outputs, cache lookup
-// ===========================================================================
-template <class E>
-__device__ __noinline__ void fin_item(const VocabArgs &a, int b, Smem &sh) {
+// Stage in shared memory, in one round of loads, what the final steps of
+// sequence b need whatever the accept count: draft tokens, p(d), q'(d), the
+// uniforms, every row's merged statistics and S threshold key and (with_res)
+// the residual chunk records.  Then the acceptance chain (thread 0).  Every
+// thread returns the accept count.
+SSD_DEV int stage_chain(const VocabArgs &a, int b, bool with_res, Smem &sh) {
   const int tid = threadIdx.x;
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  const int acc = chain(a, b, sh);
-  const RowInfo row = a.rows[static_cast<size_t>(b) * (a.K + 1) + acc];
-  const uint64_t *S = a.S + (static_cast<size_t>(b) * (a.K + 1) + acc) * a.Fcap;
-  const int Fa = a.F[acc];
-  const char *rowT = row_ptr(a, 0, b, acc, E::kSize);
-  const char *rowD = row_ptr(a, 1, b, acc, E::kSize);
-  const float ub = a.u_bonus[b];
-  int bt = row.at;
-  float W = 1.f;
-  bool zero = false, draw_p = false;
-  if (a.greedy) {
-    if (acc < a.K) {
-      W = (row.at != row.ad) ? 1.f : 0.f;
-      zero = !(W > 0.f);
-    }
-  } else if (acc < a.K) {
-    const ResInfo *res = a.res + static_cast<size_t>(b) * a.nchunks;
-    for (int c = tid; c < a.nchunks; c += kThreads) sh.cmass[c] = res[c].w;
-    group_sync<kThreads>();
-    const WResidual wf = residual_weights(a, row, Fa > 0 ? S[Fa - 1] : 0ull, Fa);
-    const int d = chunked_draw<E>(a, rowT, rowD, ub, wf, &W, sh);
-    if (d >= 0) {
-      bt = d;
-    } else {
-      zero = true;
-      draw_p = true;
-    }
-  } else {
-    draw_p = true;
+  for (int t = tid; t < a.K; t += kThreads) {
+    const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + t);
+    sh.cp[t] = pi.p;
+    sh.cq[t] = pi.q;
+    sh.cd[t] = pi.d;
+    sh.cu[t] = a.u_acc[static_cast<size_t>(b) * a.K + t];
   }
-  if (draw_p && !a.greedy) {
-    // p_{acc+1} drawn by its chunk masses from the statistics pass
-    const float mtk = __fmul_rn(row.mt, a.kT);
+  for (int r = tid; r <= a.K; r += kThreads) {
+    const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
+    sh.rows[r] = ldcg_row(a.rows + rr);
+    const int F = a.Fs[r];
+    sh.keyF[r] = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
+  }
+  if (with_res)
     for (int c = tid; c < a.nchunks; c += kThreads) {
-      const ChunkStat cs = a.stats[chunk_index(a, b, a.tslot0 + acc, c)];
-      sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), mtk)));
+      const ResInfo ri = ldcg_res(a.res + static_cast<size_t>(b) * a.nchunks + c);
+      sh.cmass[c] = ri.w;
+      sh.clast[c] = ri.last;
     }
-    group_sync<kThreads>();
-    const WTarget wp{mtk, a.kT};
-    float Wp;
-    const int d = chunked_draw<E>(a, rowT, nullptr, ub, wp, &Wp, sh);
-    bt = (d >= 0) ? d : row.at;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int t = 0; t < a.K; ++t) {
+      if (sh.cp[t] >= 0.f && __fmul_rn(sh.cu[t], sh.cq[t]) < sh.cp[t]) ++acc;
+      else break;
+    }
+    sh.ival[1] = acc;
   }
-  // lookup: the bonus among the F_a guesses of depth a
+  __syncthreads();
+  return sh.ival[1];
+}
+
+// Outputs of sequence b once its bonus token bt is known (sh.cd: draft tokens).
+SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, Smem &sh) {
+  const int tid = threadIdx.x;
+  const int Fa = a.F[acc];
+  if (tid == 0) sh.ival[3] = kNone;
+  __syncthreads();
   if (a.do_lookup) {
-    if (tid == 0) sh.ival[3] = 0x7fffffff;
-    group_sync<kThreads>();
+    const uint64_t *S = a.S + (static_cast<size_t>(b) * (a.K + 1) + acc) * a.Fcap;
     for (int i = tid; i < Fa; i += kThreads)
-      if (cand_idx(S[i]) == bt) atomicMin(&sh.ival[3], i);
-    group_sync<kThreads>();
+      if (cand_idx(ldcg_key(S + i)) == bt) atomicMin(&sh.ival[3], i);
+    __syncthreads();
   }
-  const int s_hit = (a.do_lookup && sh.ival[3] != 0x7fffffff) ? a.foff[acc] + sh.ival[3] : -1;
-  // outputs, one element per thread
+  const int s_hit = (a.do_lookup && sh.ival[3] != kNone) ? a.foff[acc] + sh.ival[3] : -1;
   if (tid <= a.K) {
     int v = -1;
-    if (tid < acc) v = a.pos[static_cast<size_t>(b) * a.K + tid].d;
+    if (tid < acc) v = sh.cd[tid];
     if (tid == acc) v = bt;
     a.out_tokens[static_cast<size_t>(b) * (a.K + 1) + tid] = v;
   }
   if (a.do_lookup && a.next_tokens && tid < a.K)
     a.next_tokens[static_cast<size_t>(b) * a.K + tid] =
         (s_hit >= 0 && a.payload) ? a.payload[(static_cast<size_t>(b) * a.foff[a.K + 1] + s_hit) * a.K + tid] : -1;
-  group_sync<kThreads>();
+  __syncthreads();
   if (tid == 0) {
     if (zero) atomicOr(a.status, kFlagZeroResidual);
     a.accept_len[b] = acc;
@@ -1046,248 +1183,162 @@ __device__ __noinline__ void fin_item(const VocabArgs &a, int b, Smem &sh) {
     if (a.resid_mass) a.resid_mass[b] = W;
     if (a.do_lookup) {
       if (a.slot_out) a.slot_out[b] = s_hit;
-      if (s_hit >= 0) atomicAdd(a.ctr + 3, 1u);
+      if (s_hit >= 0) atomicAdd(a.ctr + 1, 1u);
     }
-    __threadfence();
-    const uint32_t done = atomicAdd(a.ctr + 2, 1u);
-    if (done + 1 == static_cast<uint32_t>(a.B) && a.hits) {
-      __threadfence();
-      *a.hits = ld_acquire(a.ctr + 3);
-    }
-  }
-  group_sync<kThreads>();
-}
-
-// ===========================================================================
-// the persistent kernel
-// ===========================================================================
-SSD_DEV unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-SSD_DEV uint32_t ld_relaxed(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-SSD_DEV void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Work tickets passed from the scheduler warp to the compute warps.
-constexpr int kTickets = 4;
-struct Ticket {
-  int kind, b, idx, stage;
-  long q;  // queue position (trace)
-};
-struct Ring {
-  Ticket t[kTickets];
-  uint64_t tfull[kTickets], tempty[kTickets];  // ticket written / consumed
-  uint64_t full[kStages], sempty[kStages];     // chunk landed / stage released
-};
-
-SSD_DEV bool mbar_test(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Are the inputs of finish item f complete?  (Acquire: what its producers
-// published is visible to this CTA once the ticket is handed over.)
-SSD_DEV bool finish_ready(const VocabArgs &a, long f, Ticket &t) {
-  int kind, b, idx;
-  sched_decode(a.fs, f, kind, b, idx);
-  const uint32_t *dep;
-  uint32_t need;
-  if (kind == IT_ROW) {
-    dep = stats_done(a, b);
-    need = a.fs.ns;
-  } else if (kind == IT_RES) {
-    dep = row_done(a, b);
-    need = a.fs.nr;
-  } else {
-    dep = res_done(a, b);
-    need = a.fs.nc;
-  }
-  t.kind = kind;
-  t.b = b;
-  t.idx = idx;
-  t.stage = -1;
-  t.q = a.nst + f;
-  return ld_acquire(dep) >= need;
-}
-
-// The scheduler warp's lane 0.  Work is assigned round robin over the grid:
-// statistics chunk q to CTA q mod G, finish item f to CTA f mod G.  Each pass
-// it (1) keeps the copy ring full -- a chunk copy is issued as soon as a stage
-// and a ticket slot are free (non-blocking tests) -- and (2) hands over any of
-// its pending finish items whose inputs are complete, in any order.  No item
-// waits once handed over, so nothing can deadlock on the compute side; the
-// pending finish items of this CTA only wait for other CTAs' published work.
-constexpr int kWindow = 64;  // pending finish items scanned per pass
-constexpr int kChecksPerPass = 4;
-template <class E>
-SSD_DEV void scheduler(const VocabArgs &a, uint8_t *buf, Ring &R) {
-  const long G = gridDim.x;
-  const long fin_total = sched_total(a.fs);
-  const long my_stats = (a.nst > blockIdx.x) ? (a.nst - blockIdx.x + G - 1) / G : 0;
-  const long my_fin = (fin_total > blockIdx.x) ? (fin_total - blockIdx.x + G - 1) / G : 0;
-  long k = 0;       // statistics chunks issued
-  long w = 0;       // tickets written
-  long j_lo = 0;    // finish items below j_lo are all handed over
-  uint64_t done_mask = 0;  // handed-over items in [j_lo, j_lo + 64)
-  long fin_left = my_fin;
-  uint32_t idle = 0;
-  for (;;) {
-    bool progress = false;
-    // (1) statistics copies
-    while (k < my_stats) {
-      const int slot = static_cast<int>(w % kTickets);
-      if (w >= kTickets && !mbar_test(&R.tempty[slot], static_cast<uint32_t>((w / kTickets - 1) & 1))) break;
-      const int st = static_cast<int>(k % kStages);
-      if (k >= kStages && !mbar_test(&R.sempty[st], static_cast<uint32_t>((k / kStages - 1) & 1))) break;
-      const long q = blockIdx.x + k * G;
-      Ticket t;
-      t.kind = IT_STATS;
-      t.b = static_cast<int>(q / a.fs.ns);
-      t.idx = static_cast<int>(q % a.fs.ns);
-      t.stage = st;
-      t.q = q;
-      fence_proxy_async();
-      issue_stats<E>(a, t.b, t.idx, buf + st * kChunkBytes, &R.full[st]);
-      R.t[slot] = t;
-      mbar_arrive(&R.tfull[slot]);
-      ++w;
-      ++k;
-      progress = true;
-    }
-    // (2) finish items whose inputs are complete
-    int checks = 0;
-    for (int jj = 0; jj < kWindow && fin_left > 0 && checks < kChecksPerPass; ++jj) {
-      const long j = j_lo + jj;
-      const long f = blockIdx.x + j * G;
-      if (f >= fin_total) break;
-      if ((done_mask >> jj) & 1ull) continue;
-      const int slot = static_cast<int>(w % kTickets);
-      if (w >= kTickets && !mbar_test(&R.tempty[slot], static_cast<uint32_t>((w / kTickets - 1) & 1))) break;
-      Ticket t;
-      ++checks;
-      if (!finish_ready(a, f, t)) continue;
-      R.t[slot] = t;
-      mbar_arrive(&R.tfull[slot]);
-      ++w;
-      --fin_left;
-      done_mask |= 1ull << jj;
-      progress = true;
-    }
-    while (done_mask & 1ull) {  // slide the window past a handed-over prefix
-      done_mask >>= 1;
-      ++j_lo;
-    }
-    if (k == my_stats && fin_left == 0) break;
-    if (!progress) {
-      if (ld_relaxed(a.ctr + 1) != 0 || ++idle > kMaxSpins) {
-        atomicOr(a.status, kFlagWaitTimeout);
-        atomicExch(a.ctr + 1, 1u);
-        break;
-      }
-      __nanosleep(64);
-    } else {
-      idle = 0;
-    }
-  }
-  // end of work for the compute warps
-  const int slot = static_cast<int>(w % kTickets);
-  if (w >= kTickets) (void)mbar_wait(&R.tempty[slot], static_cast<uint32_t>((w / kTickets - 1) & 1));
-  R.t[slot].kind = IT_NONE;
-  mbar_arrive(&R.tfull[slot]);
-}
-
-template <class E>
-__global__ void __maxnreg__(112) k_vocab(const VocabArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *buf = smem;
-  uint64_t *cand = reinterpret_cast<uint64_t *>(smem + kStages * kChunkBytes);
-  Smem &sh = *reinterpret_cast<Smem *>(smem + kStages * kChunkBytes + kCandCap * sizeof(uint64_t));
-  __shared__ __align__(8) Ring R;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int i = 0; i < kTickets; ++i) {
-      mbar_init(&R.tfull[i], 1);
-      mbar_init(&R.tempty[i], 1);
-    }
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&R.full[s], 1);
-      mbar_init(&R.sempty[s], 1);
-    }
-    fence_mbar_init();
+    const uint32_t done = atom_add_acq_rel(a.ctr, 1u);
+    if (done + 1 == static_cast<uint32_t>(a.B) && a.hits) *a.hits = ld_acquire(a.ctr + 1);
   }
   __syncthreads();
-  if (tid >= kThreads) {
-    if (tid == kThreads) scheduler<E>(a, buf, R);
+}
+
+// The last pair of sequence b merged: chain, then (greedy, or every token
+// accepted) the bonus draw and the outputs; a residual draw is left to k_resid.
+template <class E>
+SSD_DEV void seq_finish(const VocabArgs &a, int b, uint8_t *buf, Smem &sh) {
+  const int acc = stage_chain(a, b, false, sh);
+  if (!a.greedy && acc < a.K) {
+    if (threadIdx.x == 0) a.accs[b] = acc;
     return;
   }
-  // compute warps: take tickets in order
-  long r = 0;
-  for (;;) {
-    const int slot = static_cast<int>(r % kTickets);
-    const bool got = mbar_wait(&R.tfull[slot], static_cast<uint32_t>((r / kTickets) & 1));
-    if (group_sync_or<kThreads>(!got)) {
-      if (tid == 0) {
-        atomicOr(a.status, kFlagWaitTimeout);
-        atomicExch(a.ctr + 1, 1u);
-      }
-      break;
+  if (threadIdx.x == 0) a.accs[b] = -1;
+  const RowInfo row = sh.rows[acc];
+  int bt = row.at;
+  float W = 1.f;
+  bool zero = false;
+  if (a.greedy) {
+    if (acc < a.K) {
+      W = (row.at != row.ad) ? 1.f : 0.f;
+      zero = !(W > 0.f);
     }
-    const Ticket t = R.t[slot];
-    if (t.kind == IT_NONE) break;
-    const unsigned long long t0 = (a.trace && tid == 0) ? globaltimer() : 0ull;
-    if (t.kind == IT_STATS) {
-      const long n = t.q / gridDim.x;  // this CTA's ordinal of the item
-      const bool ok = mbar_wait(&R.full[t.stage], static_cast<uint32_t>((n / kStages) & 1));
-      if (group_sync_or<kThreads>(!ok)) {
-        if (tid == 0) {
-          atomicOr(a.status, kFlagWaitTimeout);
-          atomicExch(a.ctr + 1, 1u);
-        }
-        // the copy may still land: a last bounded wait before leaving
-        if (tid == 0) (void)mbar_wait(&R.full[t.stage], static_cast<uint32_t>((n / kStages) & 1));
-        break;
-      }
-      stats_item<E>(a, t.b, t.idx, buf + t.stage * kChunkBytes, cand, sh);
-      if (tid == 0) mbar_arrive(&R.sempty[t.stage]);
-    } else if (t.kind == IT_ROW) {
-      row_item<E>(a, t.b, t.idx, cand, sh);
-    } else if (t.kind == IT_RES) {
-      res_item<E>(a, t.b, t.idx, sh);
+  } else {
+    bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], buf, sh);
+  }
+  emit(a, b, acc, bt, W, zero, sh);
+}
+
+// The CTA's trace entry: (SM << 48 | kind << 40 | sequence << 20 | index),
+// then its seven marks (0 = not reached).
+SSD_DEV void trace_entry(unsigned long long *tr, int kind, int b, int idx, const unsigned long long *mk) {
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  tr[0] = (static_cast<unsigned long long>(smid) << 48) | (static_cast<unsigned long long>(kind) << 40) |
+          (static_cast<unsigned long long>(b & 0xFFFFF) << 20) | static_cast<unsigned long long>(idx & 0xFFFFF);
+#pragma unroll
+  for (int k = 0; k < 7; ++k) tr[1 + k] = mk[k];
+}
+
+// ===========================================================================
+// the kernels
+// ===========================================================================
+template <class E>
+__global__ void __launch_bounds__(kThreads, 4) k_stats(const VocabArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t *buf = smem_raw;
+  Smem &sh = *reinterpret_cast<Smem *>(smem_raw + kChunkBytes);
+  // k_resid (if any) may start launching once every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x;
+  const int per_seq = a.nslots * a.nchunks;
+  const int b = static_cast<int>(blockIdx.x / per_seq);
+  const int rem = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * per_seq);
+  const int slot = rem / a.nchunks, c = rem - slot * a.nchunks;
+  const RowSlot rs = a.slot[slot];
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_mbar_init();
+    sh.phase = 0;
+    for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
+  }
+  mark(a, sh.mk, 0);
+  stage_rows<E>(a, row_ptr(a, rs.tensor, b, rs.row, E::kSize), buf, nullptr, nullptr, c, sh);
+  mark(a, sh.mk, 1);
+  stats_chunk<E>(a, b, slot, c, buf, sh);
+  int kind = 0;
+  const int r = rs.row;
+  const bool last_of_pair = arrive_last(pair_ctr(a, b, r), static_cast<uint32_t>(a.pair_chunks[r]), sh);
+  mark(a, sh.mk, 2);
+  if (last_of_pair) {
+    kind = 1;
+    row_finish<E>(a, b, r, buf, sh);
+    mark(a, sh.mk, 4);
+    if (a.do_verify && arrive_last(seq_ctr(a, b), static_cast<uint32_t>(a.npairs), sh)) {
+      kind = 3;
+      seq_finish<E>(a, b, buf, sh);
+      mark(a, sh.mk, 5);
+    }
+  }
+  mark(a, sh.mk, 6);
+  if (a.trace && tid == 0) trace_entry(a.trace + 8 * static_cast<size_t>(blockIdx.x), kind, b, rem, sh.mk);
+}
+
+template <class E>
+__global__ void __launch_bounds__(kThreads, 2) k_resid(const VocabArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t *bufT = smem_raw;
+  uint8_t *bufD = smem_raw + kChunkBytes;
+  Smem &sh = *reinterpret_cast<Smem *>(smem_raw + 2 * kChunkBytes);
+  // everything k_stats wrote is visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tid = threadIdx.x;
+  const int b = static_cast<int>(blockIdx.x / a.nchunks);
+  const int c = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * a.nchunks);
+  const int acc = __ldcg(a.accs + b);
+  if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_mbar_init();
+    sh.phase = 0;
+    for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
+  }
+  mark(a, sh.mk, 0);
+  const char *rowT = row_ptr(a, 0, b, acc, E::kSize);
+  const char *rowD = row_ptr(a, 1, b, acc, E::kSize);
+  issue_rows<E>(a, rowT, bufT, rowD, bufD, c, sh);
+  // the row's merged statistics while the chunk lands
+  const size_t rr = static_cast<size_t>(b) * (a.K + 1) + acc;
+  const RowInfo row = ldcg_row(a.rows + rr);
+  const int F = a.Fs[acc];
+  const uint64_t keyF = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
+  const WResidual wf = residual_weights(a, row, keyF, F);
+  wait_copies(a.status, sh);
+  mark(a, sh.mk, 1);
+  int last;
+  const float w = range_total<E, true, true>(staged<E>(a, bufT, rowT, bufD, rowD, c), wf, &last, sh);
+  if (tid == 0) a.res[static_cast<size_t>(b) * a.nchunks + c] = ResInfo{w, last};
+  mark(a, sh.mk, 2);
+  int kind = 2;
+  if (arrive_last(res_ctr(a, b), static_cast<uint32_t>(a.nchunks), sh)) {
+    kind = 3;
+    mark(a, sh.mk, 3);
+    const int acc2 = stage_chain(a, b, true, sh);  // the same chain: acc2 == acc
+    const RowInfo ra = sh.rows[acc2];
+    const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
+    const float ub = a.u_bonus[b];
+    locate_chunk(a.nchunks, ub, sh);
+    mark(a, sh.mk, 4);
+    const int cs = sh.ival[0];
+    const float local = sh.scal[1];
+    const float W = sh.scal[2];
+    int bt;
+    bool zero = false;
+    if (cs >= 0) {
+      if (cs != c) stage_rows<E>(a, rowT, bufT, rowD, bufD, cs, sh);
+      const int d = range_find<E, true, true>(staged<E>(a, bufT, rowT, bufD, rowD, cs), local, wa, sh);
+      bt = (d >= 0) ? d : sh.clast[cs];
     } else {
-      fin_item<E>(a, t.b, sh);
+      zero = true;  // no residual mass: p_{a+1} instead
+      bt = draw_target<E>(a, b, acc2, ra, ub, bufT, sh);
     }
-    group_sync<kThreads>();
-    if (tid == 0) {
-      mbar_arrive(&R.tempty[slot]);
-      if (a.trace) {
-        unsigned long long *tr = a.trace + 4 * t.q;
-        tr[0] = (static_cast<unsigned long long>(blockIdx.x) << 48) |
-                (static_cast<unsigned long long>(t.kind) << 40) | (static_cast<unsigned long long>(t.b) << 20) |
-                static_cast<unsigned long long>(t.idx);
-        tr[1] = t0;
-        tr[2] = t0;
-        tr[3] = globaltimer();
-      }
-    }
-    ++r;
+    mark(a, sh.mk, 5);
+    emit(a, b, acc2, bt, W, zero, sh);
+  }
+  mark(a, sh.mk, 6);
+  if (a.trace && tid == 0) {
+    const size_t base = static_cast<size_t>(a.B) * a.nslots * a.nchunks;
+    trace_entry(a.trace + 8 * (base + blockIdx.x), kind, b, c, sh.mk);
   }
 }
 
-// Cache lookup alone (one CTA; hits written, not accumulated).
 struct LookupArgs {
   const int32_t *guess, *payload, *accept_len, *bonus;
   int32_t *slot, *next_tokens;
@@ -1300,7 +1351,7 @@ struct LookupArgs {
 __global__ void __launch_bounds__(256) k_lookup(const LookupArgs l) {
   __shared__ uint32_t tot;
   if (threadIdx.x == 0) tot = 0;
-  group_sync<kThreads>();
+  __syncthreads();
   uint32_t h = 0;
   const int sumF = l.foff[l.K + 1];
   for (int b = threadIdx.x; b < l.B; b += blockDim.x) {
@@ -1324,7 +1375,7 @@ __global__ void __launch_bounds__(256) k_lookup(const LookupArgs l) {
     h += (s >= 0);
   }
   atomicAdd(&tot, h);
-  group_sync<kThreads>();
+  __syncthreads();
   if (threadIdx.x == 0 && l.hits) *l.hits = tot;
 }
 
@@ -1339,7 +1390,8 @@ namespace {
 
 struct Layout {
   int nslots, nchunks, chunk_elems, Fcap;
-  size_t ctr_off, stats_off, cands_off, rows_off, S_off, pos_off, res_off, total;
+  size_t ctr_words;
+  size_t ctr_off, stats_off, cands_off, rows_off, S_off, pos_off, res_off, accs_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1360,9 +1412,10 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   L->Fcap = fmax > 0 ? fmax : 1;
   const size_t Bn = static_cast<size_t>(B > 0 ? B : 1);
   const size_t nrec = Bn * L->nslots * L->nchunks;
+  L->ctr_words = 2 + 2 * Bn + Bn * (K + 1);
   size_t o = 0;
   L->ctr_off = o;
-  o = align_up(o + (4 + 3 * Bn) * sizeof(uint32_t), 256);
+  o = align_up(o + L->ctr_words * sizeof(uint32_t), 256);
   L->stats_off = o;
   o = align_up(o + nrec * sizeof(ChunkStat), 256);
   L->cands_off = o;
@@ -1375,15 +1428,10 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + Bn * (K > 0 ? K : 1) * sizeof(PosInfo), 256);
   L->res_off = o;
   o = align_up(o + Bn * L->nchunks * sizeof(ResInfo), 256);
+  L->accs_off = o;
+  o = align_up(o + Bn * sizeof(int32_t), 256);
   L->total = o;
   return true;
-}
-
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1447,85 +1495,113 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.S = reinterpret_cast<uint64_t *>(w + L.S_off);
   a.pos = reinterpret_cast<PosInfo *>(w + L.pos_off);
   a.res = reinterpret_cast<ResInfo *>(w + L.res_off);
+  a.accs = reinterpret_cast<int32_t *>(w + L.accs_off);
   a.status = status;
-  a.tslot0 = -1;
   return a;
 }
 
-void set_slots(VocabArgs &a, bool target_rows, int ndraft) {
+// Rows read by a call: target rows 0..ntarget-1 and draft rows 0..ndraft-1,
+// slots ordered by pair (target r, then draft r).  `topf`: draft rows keep
+// their top-F_r lists.
+void set_slots(VocabArgs &a, int ntarget, int ndraft, bool topf) {
   int n = 0;
-  if (target_rows) {
-    a.tslot0 = 0;
-    for (int r = 0; r <= a.K; ++r) a.slot[n++] = RowSlot{0, static_cast<int16_t>(r), 0, 0};
+  a.npairs = ntarget > ndraft ? ntarget : ndraft;
+  for (int r = 0; r <= a.K; ++r) {
+    a.tsl[r] = a.dsl[r] = -1;
+    a.pair_chunks[r] = 0;
+    a.Fs[r] = (topf && r < ndraft) ? a.F[r] : 0;
   }
-  a.dslot0 = n;
-  for (int r = 0; r < ndraft; ++r)
-    a.slot[n++] = RowSlot{1, static_cast<int16_t>(r), static_cast<int16_t>(a.F[r]), 0};
+  for (int r = 0; r < a.npairs; ++r) {
+    int rows = 0;
+    if (r < ntarget) {
+      a.tsl[r] = n;
+      a.slot[n++] = RowSlot{0, static_cast<int16_t>(r), 0, 0};
+      ++rows;
+    }
+    if (r < ndraft) {
+      a.dsl[r] = n;
+      a.slot[n++] = RowSlot{1, static_cast<int16_t>(r), static_cast<int16_t>(a.Fs[r]), 0};
+      ++rows;
+    }
+    a.pair_chunks[r] = rows * a.nchunks;
+  }
   a.nslots = n;
 }
 
 // Optional timing hook (ssd_set_timing_events): events recorded around the
-// persistent kernel of every vocabulary call while set.
+// statistics kernel of every vocabulary call while set.
 cudaEvent_t g_ev_before = nullptr;
 cudaEvent_t g_ev_after = nullptr;
-// Optional per-entry trace (ssd_set_trace).
+// Optional per-CTA trace (ssd_set_trace).
 void *g_trace = nullptr;
 size_t g_trace_bytes = 0;
 
-constexpr size_t kVocabSmem = kStages * kChunkBytes + kCandCap * sizeof(uint64_t) + sizeof(Smem);
-// two resident CTAs per SM: 2 x (dynamic + static + 1 KiB reserved) <= 228 KiB
-static_assert(2 * (kVocabSmem + 1024 + 512) <= 228 * 1024, "shared memory of k_vocab too large for 2 CTAs/SM");
+constexpr size_t kStatsSmem = kChunkBytes + sizeof(Smem);
+constexpr size_t kResidSmem = 2 * kChunkBytes + sizeof(Smem);
+
+ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_smem_attr_set[2][kMaxDevices / 64 + 1];
 
 template <class E>
-cudaError_t launch_vocab(VocabArgs &a, int nr, int nc, int nf, cudaStream_t s) {
-  constexpr int kBlock = kThreads + 32;  // 8 compute warps + the scheduler warp
-  cudaError_t e = cudaFuncSetAttribute(k_vocab<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kVocabSmem));
+cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
+  constexpr int ti = E::kSize == 4 ? 0 : 1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_vocab<E>, kBlock, kVocabSmem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  Sched fs;
-  fs.B = a.B;
-  fs.ns = a.nslots * a.nchunks;
-  fs.nr = nr;
-  fs.nc = nc;
-  fs.nf = nf;
-  fs.L1 = 0;
-  fs.L2 = 1;
-  fs.L3 = 2;
-  a.fs = fs;
-  a.nst = static_cast<long>(a.B) * fs.ns;
-  const long fin_total = sched_total(fs);
-  long grid = static_cast<long>(num_sms()) * per_sm;
-  if (grid > a.nst + fin_total) grid = a.nst + fin_total;
-  if (grid < 1) return cudaSuccess;
-  a.trace = (g_trace && g_trace_bytes >= static_cast<size_t>(a.nst + fin_total) * 32)
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << (dev % 64);
+  if (!(g_smem_attr_set[ti][dev / 64].load() & bit)) {
+    e = cudaFuncSetAttribute(k_stats<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_resid<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kResidSmem));
+    if (e != cudaSuccess) return e;
+    g_smem_attr_set[ti][dev / 64].fetch_or(bit);
+  }
+  const long n1 = static_cast<long>(a.B) * a.nslots * a.nchunks;
+  const long n2 = (a.do_verify && !a.greedy && a.K > 0) ? static_cast<long>(a.B) * a.nchunks : 0;
+  if (n1 < 1) return cudaSuccess;
+  if (n1 > 0x7fffffffL) return cudaErrorInvalidValue;
+  a.trace = (g_trace && g_trace_bytes >= static_cast<size_t>(n1 + n2) * 64)
                 ? static_cast<unsigned long long *>(g_trace)
                 : nullptr;
-  // the finish-queue head, abort flag, counters start at zero
-  e = cudaMemsetAsync(a.ctr, 0, (4 + 3 * static_cast<size_t>(a.B)) * sizeof(uint32_t), s);
+  // counters start at zero
+  e = cudaMemsetAsync(a.ctr, 0, (2 + 2 * static_cast<size_t>(a.B) + static_cast<size_t>(a.B) * (a.K + 1)) *
+                                    sizeof(uint32_t),
+                      s);
   if (e != cudaSuccess) return e;
   if (g_ev_before) cudaEventRecord(g_ev_before, s);
-  k_vocab<E><<<static_cast<unsigned>(grid), kBlock, kVocabSmem, s>>>(a);
+  k_stats<E><<<static_cast<unsigned>(n1), kThreads, kStatsSmem, s>>>(a);
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   if (g_ev_after) cudaEventRecord(g_ev_after, s);
+  if (n2 > 0) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(n2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kResidSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_resid<E>, a);
+  }
   return e;
 }
 
-cudaError_t launch_any(ssd_dtype_t dt, VocabArgs &a, int nr, int nc, int nf, cudaStream_t s) {
-  return dt == SSD_F32 ? launch_vocab<EF32>(a, nr, nc, nf, s) : launch_vocab<EBF16>(a, nr, nc, nf, s);
+cudaError_t launch_any(ssd_dtype_t dt, VocabArgs &a, cudaStream_t s) {
+  return dt == SSD_F32 ? launch_vocab<EF32>(a, s) : launch_vocab<EBF16>(a, s);
 }
-
-ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
 // Fixed device scratch for ssd_verify_noalloc: one array per GPU that loads
 // the library, held until the process exits.
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
 void *g_static_scratch_addr[kMaxDevices] = {nullptr};
 std::mutex g_static_scratch_mu;
 
@@ -1638,12 +1714,12 @@ ssd_status_t ssd_saguaro_sample(const void *draft, ssd_dtype_t dt, int64_t seq_s
   if (B == 0 || K == 0) return SSD_OK;
   if (!u_draft || !d_out || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(draft, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
-  set_slots(a, false, K);
+  set_slots(a, 0, K, C < 1.f);
   a.do_sample = 1;
   a.u_draft = u_draft;
   a.d_out = d_out;
   a.qd_out = qd_out;
-  return cuda_status(launch_any(dt, a, K, 0, 0, reinterpret_cast<cudaStream_t>(s)));
+  return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
 }
 
 ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
@@ -1663,7 +1739,7 @@ ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, i
   if ((K > 0 && (!d || !u_acc)) || !u_bonus || !accept_len || !out_tokens || !bonus || !status)
     return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(target, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
-  set_slots(a, true, K + 1);
+  set_slots(a, K + 1, K, C < 1.f);
   a.do_verify = 1;
   a.d_in = d;
   a.u_acc = u_acc;
@@ -1673,7 +1749,7 @@ ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, i
   a.bonus = bonus;
   a.accept_prob = accept_prob;
   a.resid_mass = resid_mass;
-  return cuda_status(launch_any(dt, a, K + 1, L.nchunks, 1, reinterpret_cast<cudaStream_t>(s)));
+  return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
 }
 
 ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq_stride, int64_t row_stride,
@@ -1689,11 +1765,11 @@ ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq
   if (B == 0) return SSD_OK;
   if (!guess || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(draft, draft, seq_stride, row_stride, B, K, V, F, 1.f, T, L, ws, status);
-  set_slots(a, false, K + 1);
+  set_slots(a, 0, K + 1, true);
   a.do_predict = 1;
   a.guess = guess;
   a.guess_q = guess_q;
-  return cuda_status(launch_any(dt, a, K + 1, 0, 0, reinterpret_cast<cudaStream_t>(s)));
+  return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
 }
 
 ssd_status_t ssd_cache_lookup(const int32_t *guess, const int32_t *payload, int B, int K, const int32_t *F,
@@ -1754,11 +1830,11 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
     return SSD_ERR_INVALID_ARG;
   if ((slot || next_tokens || hits) && !guess) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(target, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
-  set_slots(a, true, K + 1);
   a.do_sample = 1;
   a.do_verify = 1;
   a.do_predict = guess != nullptr;
   a.do_lookup = guess != nullptr;
+  set_slots(a, K + 1, a.do_predict ? K + 1 : K, a.do_predict || C < 1.f);
   a.u_draft = u_draft;
   a.u_acc = u_acc;
   a.u_bonus = u_bonus;
@@ -1776,7 +1852,7 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
   a.slot_out = slot;
   a.next_tokens = next_tokens;
   a.hits = hits;
-  return cuda_status(launch_any(dt, a, K + 1, L.nchunks, 1, cs));
+  return cuda_status(launch_any(dt, a, cs));
 }
 
 size_t ssd_verify_noalloc_max_bytes(void) { return kStaticScratchBytes; }
