@@ -8,20 +8,20 @@
 // the tree nodes on m's ancestor-or-self path; node n's K/V sits at logical
 // position prefix_len + n.  GQA: head h reads KV head h / (Hq / Hkv), and all
 // the query heads of one KV head share a CTA's rows, so each K/V page is read
-// once per (sequence, KV head, row tile).
+// once per (sequence, KV head, group of row tiles).
 //
-// One CTA = (sequence b, KV head, tile of 128 query rows, range of keys):
-//   * Q tile (128 x d) staged once in shared memory, 128-byte swizzled;
-//   * K and V pages (16 positions x d) fetched by TMA through the block table
-//     into a two-stage ring of 128-key tiles (mbarrier completion);
-//   * S = Q K^T by tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in TMEM);
-//   * one thread per row reads its S row from TMEM, applies the tree mask and
-//     an online softmax in the log2 domain (the running max is only moved,
-//     and O rescaled in TMEM, when it grows by more than 2^8), writes P (bf16)
-//     to shared memory;
-//   * O += P V by tcgen05.mma with V as an MN-major operand, in TMEM;
-//   * the epilogue normalises O, or writes (O, m, l) partials that a combine
-//     kernel merges when the keys are split across CTAs.
+// One CTA (one per SM) = (sequence b, KV head, group of MT tiles of 128 query
+// rows, range of keys), warp-specialised:
+//   * a producer warp fetches the K and V pages of each 64-key tile by TMA
+//     through the block table into a ring of stages (mbarrier completion);
+//   * an MMA warp (one thread) issues S = Q K^T for tile t + 1 into a second
+//     TMEM buffer while the softmax works on tile t, then O += P V for tile t;
+//   * one softmax warpgroup per row tile (one thread per row) reads its S row
+//     from TMEM, applies the tree mask and an online softmax in the log2 domain
+//     (the running maximum only moves, and O is rescaled in TMEM, when it grows
+//     by more than 2^8), writes P (bf16) to shared memory;
+//   * the softmax threads end by normalising O, or write (O, m, l) partials that
+//     a combine kernel merges when the keys are split across CTAs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -37,16 +37,10 @@ namespace ssd {
 
 constexpr int kPage = 16;
 constexpr int kMaxNodes = 128;
-constexpr int kRows = 128;        // query rows per CTA (MMA M)
-constexpr int kTiles = 2;         // K/V ring stages
-// keys per tile (MMA N of S, K of P V): 128 at d = 64, 64 at d = 128, so that
-// two CTAs (2 x 112 KiB of shared memory, 2 x 256 TMEM columns) share an SM
-template <int D>
-struct KeysPerTile {
-  static constexpr int value = D == 64 ? 128 : 64;
-};
-constexpr int kAttnThreads = 128;  // one thread per query row
-constexpr uint32_t kTmemCols = 256;  // S: keys-per-tile columns, O: d columns
+constexpr int kRows = 128;                  // query rows per row tile (MMA M)
+constexpr int kKeys = 64;                   // keys per tile (MMA N of S, K of P V)
+constexpr int kTilePages = kKeys / kPage;   // 4
+constexpr uint32_t kTmemCols = 512;         // S: MT x 2 x 64 columns, O: MT x d columns
 
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
@@ -159,6 +153,28 @@ SSD_DEV float bf16_round(float x) {
   return __uint_as_float(a & 0xFFFF0000u);
 }
 
+SSD_DEV void mbar_arrive1(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// two fp32 -> bf16x2 (round to nearest even): lo in the low half
+SSD_DEV uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 64 bits of the 128-bit node mask starting at bit `off` (bits below 0 read 0)
+SSD_DEV uint64_t mask_bits(const uint32_t *w, int off) {
+  uint64_t r = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int sh = 32 * k - off;  // position of word k relative to the window
+    const uint64_t x = w[k];
+    if (sh >= 0 && sh < 64) r |= x << sh;
+    else if (sh < 0 && sh > -32) r |= x >> (-sh);
+  }
+  return r;
+}
+
 struct AttnArgs {
   const uint16_t *q;
   const int32_t *table;
@@ -170,69 +186,78 @@ struct AttnArgs {
   uint16_t *out;
   float *lse;
   float *part_o;   // [B*Hkv][mtiles][splits][128][d] fp32 (splits > 1)
-  float *part_ml;  // [B*Hkv][mtiles][splits][128][2]
+  float *part_ml;  // [B*Hkv][mtiles][splits][128][3]
   uint32_t *status;
 };
 
-template <int D>
-struct AttnSmem {
-  static constexpr int kKeys = KeysPerTile<D>::value;
-  static constexpr int kQBytes = kRows * D * 2;
-  static constexpr int kKVBytes = kKeys * D * 2;  // one of K or V for a tile
-  static constexpr int kPBytes = kRows * kKeys * 2;
+// Shared-memory plan of a CTA with MT row tiles at head dimension D.
+template <int D, int MT>
+struct AttnCfg {
+  static constexpr int kQBytes = kRows * D * 2;      // one row tile of Q
+  static constexpr int kKVBytes = kKeys * D * 2;     // K or V of one key tile
+  static constexpr int kPBytes = kRows * kKeys * 2;  // one P buffer of one row tile
+  static constexpr int kFixed = MT * kQBytes + MT * 2 * kPBytes;
+  static constexpr int kStagesFit = (216 * 1024 - kFixed) / (2 * kKVBytes);
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;
-  static constexpr int kV = kK + kTiles * kKVBytes;
-  static constexpr int kP = kV + kTiles * kKVBytes;
-  static constexpr int kTable = kP + kPBytes;  // block-table entries of the CTA's key range
-  static constexpr int kTotal = kTable;        // all tile offsets multiples of 1024
+  static constexpr int kP = kQ + MT * kQBytes;
+  static constexpr int kKV = kP + MT * 2 * kPBytes;
+  static constexpr int kTable = kKV + kStages * 2 * kKVBytes;  // block-table entries of the key range
+  static constexpr int kWarps = 4 * MT + 2;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kTmaWarp = 4 * MT, kMmaWarp = 4 * MT + 1;
+  static_assert(kStages >= 2, "at least two K/V stages");
 };
 
-template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 2)
+template <int D, int MT>
+__global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
     k_branch_attn_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                     const AttnArgs a) {
-  using SL = AttnSmem<D>;
-  constexpr int kKeys = SL::kKeys;
-  constexpr int kPages = kKeys / kPage;
+                     const __grid_constant__ AttnArgs a) {
+  using CF = AttnCfg<D, MT>;
+  constexpr int NS = CF::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kTiles];
-  __shared__ __align__(8) uint64_t sdone, odone;
+  __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
+  __shared__ __align__(8) uint64_t s_full[MT][2], s_free[MT][2], p_full[MT][2], pv_done[MT][2];
   __shared__ uint32_t tmem_base;
   __shared__ uint32_t anc[kMaxNodes][kMaxNodes / 32];
-  __shared__ uint8_t page_ok[kTiles][1];
-  __shared__ int s_abort;
+  __shared__ volatile int s_abort;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, b = bh / a.Hkv, hk = bh % a.Hkv;
-  const int mt = blockIdx.y, split = blockIdx.z;
+  const int mg = blockIdx.y, split = blockIdx.z;
   const int N = a.N;
   const int L = max(0, a.prefix_len[b]);
   const int nkeys = L + N;
   const int ntiles_all = (nkeys + kKeys - 1) / kKeys;
   const int t_begin = split * a.tiles_per_split;
   const int t_end = min(ntiles_all, t_begin + a.tiles_per_split);
-  const int row = mt * kRows + tid;  // this thread's query row within (b, hk)
-  const bool row_valid = row < a.nrows;
-  const int qi = row_valid ? row / a.group : 0;
-  const int head = hk * a.group + (row_valid ? row % a.group : 0);
+  const int nt = max(0, t_end - t_begin);
+  const int mt_here = min(MT, a.mtiles - mg * MT);  // row tiles of this CTA
   const float NEG_INF = -__int_as_float(0x7f800000);
 
   if (tid == 0) {
-    for (int s = 0; s < kTiles; ++s) mbar_init(&full[s], 1);
-    mbar_init(&sdone, 1);
-    mbar_init(&odone, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int m = 0; m < MT; ++m)
+      for (int u = 0; u < 2; ++u) {
+        mbar_init(&s_full[m][u], 1);
+        mbar_init(&s_free[m][u], 4);
+        mbar_init(&p_full[m][u], 4);
+        mbar_init(&pv_done[m][u], 1);
+      }
     fence_mbar_init();
     s_abort = 0;
   }
-  if (warp == 0) {
+  if (warp == CF::kMmaWarp) {
     tmem_alloc(&tmem_base, kTmemCols);
     tmem_relinquish();
   }
   // ancestor-or-self masks of the tree nodes
-  for (int m = tid; m < N; m += kAttnThreads) {
+  for (int m = tid; m < N; m += CF::kThreads) {
     uint32_t bits[kMaxNodes / 32] = {0, 0, 0, 0};
     int x = m;
     bool bad = false;
@@ -249,22 +274,38 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll
     for (int w = 0; w < kMaxNodes / 32; ++w) anc[m][w] = bits[w];
   }
-  // block-table entries of this CTA's key range, staged once
-  int *tab = reinterpret_cast<int *>(smem + SL::kTable);
-  const int page0 = t_begin * kPages;
-  const int npages_here = max(0, (t_end - t_begin) * kPages);
-  for (int i = tid; i < npages_here; i += kAttnThreads) {
+  // block-table entries of this CTA's key range (-1: past the table or the keys, or a bad id)
+  int *tab = reinterpret_cast<int *>(smem + CF::kTable);
+  const int page0 = t_begin * kTilePages;
+  const int npages = nt * kTilePages;
+  for (int i = tid; i < npages; i += CF::kThreads) {
     const int lp = page0 + i;
-    tab[i] = (lp < a.maxb) ? a.table[static_cast<int64_t>(b) * a.maxb + lp] : -1;
+    int blk = -1;
+    if (lp < a.maxb && lp * kPage < nkeys) {
+      blk = a.table[static_cast<int64_t>(b) * a.maxb + lp];
+      if (blk < 0 || blk >= a.num_blocks) {
+        atomicOr(a.status, kFlagBadBlock);
+        blk = -1;
+      }
+    }
+    tab[i] = blk;
   }
-  // Q tile: this thread's row, 128-byte swizzled, in d/64 column blocks
-  {
+  // Q tiles: each softmax thread stages its row, 128-byte swizzled, in d/64 column blocks
+  const int m_own = warp >> 2;                        // softmax warps: row tile
+  const int r_own = (warp & 3) * 32 + lane;           // row within the tile (= TMEM lane)
+  const int row = (mg * MT + m_own) * kRows + r_own;  // row within (b, hk)
+  const bool softmax_thread = warp < 4 * MT;
+  const bool row_valid = softmax_thread && m_own < mt_here && row < a.nrows;
+  const int qi = row_valid ? row / a.group : 0;
+  const int head = hk * a.group + (row_valid ? row % a.group : 0);
+  if (softmax_thread) {
     const uint16_t *qrow = a.q + ((static_cast<int64_t>(b) * a.Nq + qi) * a.Hq + head) * D;
+    uint8_t *qt = smem + CF::kQ + m_own * CF::kQBytes;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       uint4 v = make_uint4(0, 0, 0, 0);
       if (row_valid) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
-      *reinterpret_cast<uint4 *>(smem + SL::kQ + (c >> 3) * (kRows * 128) + sw128(tid, c & 7)) = v;
+      *reinterpret_cast<uint4 *>(qt + (c >> 3) * (kRows * 128) + sw128(r_own, c & 7)) = v;
     }
   }
   fence_proxy_async();  // generic-proxy writes of Q -> visible to the tensor cores
@@ -272,240 +313,276 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t tS = tmem;          // columns [0, 128)
-  const uint32_t tO = tmem + kKeys;  // columns [kKeys, kKeys + D)
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  int issued = 0;  // producer: tiles whose copies were issued
 
-  // producer (thread 0): fetch the K and V pages of tile t into stage s
-  auto issue_tile = [&](int t, int s) {
-    uint8_t ok = 0;
-    const int expect = 2 * kPages * (D / 64) * (kPage * 128);
-    mbar_arrive_expect_tx(&full[s], expect);
-    for (int p = 0; p < kPages; ++p) {
-      const int lp = t * kPages + p;  // logical page
-      int blk = -1;
-      if (lp * kPage < nkeys) {
-        blk = tab[lp - page0];
-        if (blk >= 0 && blk < a.num_blocks) ok |= static_cast<uint8_t>(1u << p);
-        else atomicOr(a.status, kFlagBadBlock);
-      }
-      // pages past the end or with a bad id load block 0 (finite values, masked out)
-      const int use = (ok >> p) & 1 ? blk : 0;
-      const int y = (use * a.Hkv + hk) * kPage;
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_2d(smem + SL::kK + s * SL::kKVBytes + h * (kKeys * 128) + p * (kPage * 128), &kmap, h * 64, y,
-                    &full[s]);
-        tma_load_2d(smem + SL::kV + s * SL::kKVBytes + h * (kKeys * 128) + p * (kPage * 128), &vmap, h * 64, y,
-                    &full[s]);
-      }
-    }
-    page_ok[s][0] = ok;
-  };
-
-  uint32_t full_ph = 0, s_ph = 0, o_ph = 0;
-  if (tid == 0) {
-    for (int i = 0; i < kTiles && t_begin + i < t_end; ++i) issue_tile(t_begin + i, i);
-  }
-  __syncthreads();
-
-  // this row's node mask
-  uint32_t my_anc[kMaxNodes / 32] = {0, 0, 0, 0};
-  if (row_valid) {
-    const int node = N - a.Nq + qi;
-#pragma unroll
-    for (int w = 0; w < kMaxNodes / 32; ++w) my_anc[w] = anc[node][w];
-  }
-  float m_used = NEG_INF, l = 0.f, lx = 0.f;  // l: sum of the bf16 P (normalises O); lx: exact (lse)
-  const uint32_t idesc_s = idesc_bf16(kKeys, 0);
-  const uint32_t idesc_o = idesc_bf16(D, 1);
-  const uint32_t q_base = smem_u32(smem + SL::kQ);
-  const uint32_t p_base = smem_u32(smem + SL::kP);
-  bool issued_pv = false;
-
-  for (int t = t_begin; t < t_end; ++t) {
-    const int i = t - t_begin;
-    const int s = i & 1;
-    // ---- S = Q K^T
-    if (tid == 0) {
-      bool ok = mbar_wait(&full[s], (full_ph >> s) & 1u);
-      full_ph ^= 1u << s;
-      if (!ok) s_abort = 1;
-      else {
-        tc_fence_after();
-        const uint32_t k_base = smem_u32(smem + SL::kK + s * SL::kKVBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (kKeys * 128) + (kk & 3) * 32;
-          umma_bf16(tS, smem_desc_sw128(q_base + off, 16), smem_desc_sw128(k_base + koff, 16), idesc_s, kk > 0);
+  if (warp == CF::kTmaWarp) {
+    // ---------------- producer: K and V pages of each tile into the ring
+    if (lane == 0) {
+      for (int i = 0; i < nt && !s_abort; ++i) {
+        const int st = i % NS;
+        if (i >= NS && !mbar_wait(&kv_empty[st], ((i / NS) - 1) & 1)) {
+          s_abort = 1;
+          break;
         }
-        umma_commit(&sdone);
-      }
-    }
-    __syncthreads();
-    if (s_abort) break;
-    if (!mbar_wait(&sdone, s_ph)) s_abort = 1;
-    s_ph ^= 1;
-    tc_fence_after();
-    __syncthreads();
-    if (s_abort) break;
-    const uint8_t pok = page_ok[s][0];
-    // ---- pass 1: masked, scaled tile maximum of this row
-    const int kbase = t * kKeys;
-    float tmax = NEG_INF;
-    float v[32];
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kTilePages * (D / 64) * (kPage * 128));
+        uint8_t *kdst = smem + CF::kKV + st * 2 * CF::kKVBytes;
+        uint8_t *vdst = kdst + CF::kKVBytes;
+        for (int p = 0; p < kTilePages; ++p) {
+          const int blk = tab[i * kTilePages + p];
+          // pages past the keys or with a bad id load block 0 (finite values, masked out)
+          const int y = ((blk >= 0 ? blk : 0) * a.Hkv + hk) * kPage;
 #pragma unroll
-    for (int c = 0; c < kKeys / 32; ++c) {
-      tmem_ld32(tS + lane_off + c * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int kj = c * 32 + j;
-        const int pos = kbase + kj;
-        bool vis = row_valid && ((pok >> (kj >> 4)) & 1) && pos < nkeys;
-        if (vis && pos >= L) {
-          const int n = pos - L;
-          vis = (my_anc[n >> 5] >> (n & 31)) & 1u;
-        }
-        if (vis) tmax = fmaxf(tmax, v[j] * a.scale_log2);
-      }
-    }
-    float m_new = m_used;
-    bool need = false;
-    if (tmax != NEG_INF && (m_used == NEG_INF || tmax > m_used + 8.f)) {
-      m_new = tmax;
-      need = true;
-    }
-    // ---- PV of the previous tile must be done before O and P are touched
-    if (i > 0) {
-      if (!mbar_wait(&odone, o_ph)) s_abort = 1;
-      o_ph ^= 1;
-      tc_fence_after();
-    }
-    if (tid == 0 && i > 0 && t + 1 < t_end && !s_abort) issue_tile(t + 1, s ^ 1);
-    // ---- rescale O rows whose running maximum moved (never before the first P V)
-    if (i > 0 && __any_sync(0xffffffffu, need)) {
-      const float f = need ? ex2(m_used - m_new) : 1.f;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tO + lane_off + c * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= f;
-        tmem_st32(tO + lane_off + c * 32, v);
-      }
-    }
-    if (need) {
-      const float f = (m_used == NEG_INF) ? 0.f : ex2(m_used - m_new);
-      l *= f;
-      lx *= f;
-      m_used = m_new;
-    }
-    // ---- pass 2: P = 2^(s - m) (bf16) into shared memory, row sum
-    uint8_t *prow = smem + SL::kP;
-#pragma unroll
-    for (int c = 0; c < kKeys / 32; ++c) {
-      tmem_ld32(tS + lane_off + c * 32, v);
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float pr[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int kj = c * 32 + j + h;
-          const int pos = kbase + kj;
-          bool vis = row_valid && ((pok >> (kj >> 4)) & 1) && pos < nkeys;
-          if (vis && pos >= L) {
-            const int n = pos - L;
-            vis = (my_anc[n >> 5] >> (n & 31)) & 1u;
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_2d(kdst + h * (kKeys * 128) + p * (kPage * 128), &kmap, h * 64, y, &kv_full[st]);
+            tma_load_2d(vdst + h * (kKeys * 128) + p * (kPage * 128), &vmap, h * 64, y, &kv_full[st]);
           }
-          float p = 0.f;
-          if (vis && m_used != NEG_INF) p = ex2(v[j + h] * a.scale_log2 - m_used);
-          lx += p;
-          p = bf16_round(p);
-          l += p;
-          pr[h] = p;
         }
-        pk[j >> 1] = pack_bf16x2(pr[0], pr[1]);
-      }
-      // 32 keys = 64 bytes = 4 chunks of 16 B in key block (c >> 1)
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int chunk = (c & 1) * 4 + q4;
-        *reinterpret_cast<uint4 *>(prow + (c >> 1) * (kRows * 128) + sw128(tid, chunk)) =
-            make_uint4(pk[q4 * 4 + 0], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+        issued = i + 1;
       }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (s_abort) break;
-    // ---- O += P V
-    if (tid == 0) {
+  } else if (warp == CF::kMmaWarp) {
+    // ---------------- MMA issue (one thread): S(t) then O += P(t-1) V(t-1)
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(kKeys, 0);
+      const uint32_t idesc_o = idesc_bf16(D, 1);
+      auto issue_pv = [&](int u) {
+        const int st = u % NS;
+        const uint32_t v_base = smem_u32(smem + CF::kKV + st * 2 * CF::kKVBytes + CF::kKVBytes);
+        for (int m = 0; m < mt_here; ++m) {
+          if (!mbar_wait(&p_full[m][u & 1], (u >> 1) & 1)) {
+            s_abort = 1;
+            return;
+          }
+          tc_fence_after();
+          const uint32_t p_base = smem_u32(smem + CF::kP + (m * 2 + (u & 1)) * CF::kPBytes);
+          const uint32_t tO = tmem + 4 * kKeys + m * D;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            // P: 16 keys = 32 bytes of each 128-byte row; V: 16 keys = two 8-key groups of 1024 B,
+            // d blocks of 64 columns kKeys * 128 B apart
+            umma_bf16(tO, smem_desc_sw128(p_base + kk * 32, 16), smem_desc_sw128(v_base + kk * 2048, kKeys * 128),
+                      idesc_o, (u > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&pv_done[m][u & 1]);
+        }
+        umma_commit(&kv_empty[st]);
+      };
+      for (int i = 0; i < nt && !s_abort; ++i) {
+        const int st = i % NS;
+        if (!mbar_wait(&kv_full[st], (i / NS) & 1)) {
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(smem + CF::kKV + st * 2 * CF::kKVBytes);
+        for (int m = 0; m < mt_here; ++m) {
+          if (i >= 2 && !mbar_wait(&s_free[m][i & 1], ((i - 2) >> 1) & 1)) {
+            s_abort = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t q_base = smem_u32(smem + CF::kQ + m * CF::kQBytes);
+          const uint32_t tS = tmem + (m * 2 + (i & 1)) * kKeys;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qoff = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * (kKeys * 128) + (kk & 3) * 32;
+            umma_bf16(tS, smem_desc_sw128(q_base + qoff, 16), smem_desc_sw128(k_base + koff, 16), idesc_s,
+                      kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[m][i & 1]);
+        }
+        if (s_abort) break;
+        if (i >= 1) issue_pv(i - 1);
+      }
+      if (nt >= 1 && !s_abort) issue_pv(nt - 1);
+    }
+  } else if (m_own < mt_here) {
+    // ---------------- softmax: one thread per row of row tile m_own
+    const int m = m_own;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool warp_valid = __any_sync(0xffffffffu, row_valid);
+    uint32_t my_anc[kMaxNodes / 32] = {0, 0, 0, 0};
+    if (row_valid) {
+      const int node = N - a.Nq + qi;
+#pragma unroll
+      for (int w = 0; w < kMaxNodes / 32; ++w) my_anc[w] = anc[node][w];
+    }
+    const float c = a.scale_log2;
+    float m_used = NEG_INF;
+    uint64_t l2 = pack2(0.f, 0.f), lx2 = pack2(0.f, 0.f);  // sums of the bf16 P (normalises O) and exact (lse)
+    for (int i = 0; i < nt; ++i) {
+      const int t = t_begin + i, u = i & 1;
+      if (!__all_sync(0xffffffffu, !s_abort && mbar_wait(&s_full[m][u], (i >> 1) & 1))) {
+        s_abort = 1;
+        break;
+      }
       tc_fence_after();
-      const uint32_t v_base = smem_u32(smem + SL::kV + s * SL::kKVBytes);
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
-        const uint32_t poff = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-        // V: 16 keys = two 8-key groups of 1024 B; d blocks of 64 at kKeys*128 B
-        const uint32_t voff = kk * 2048;
-        umma_bf16(tO, smem_desc_sw128(p_base + poff, 16), smem_desc_sw128(v_base + voff, kKeys * 128), idesc_o,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+      float s[kKeys];
+      if (warp_valid) {
+        tmem_ld32(tmem + (m * 2 + u) * kKeys + lane_off, s);
+        tmem_ld32(tmem + (m * 2 + u) * kKeys + 32 + lane_off, s + 32);
       }
-      umma_commit(&odone);
-    }
-    issued_pv = true;
-  }
-  // ---- epilogue
-  if (issued_pv) {
-    if (!mbar_wait(&odone, o_ph)) s_abort = 1;
-    o_ph ^= 1;
-    tc_fence_after();
-  }
-  __syncthreads();
-  const bool abort_all = s_abort != 0;
-  if (abort_all && tid == 0) atomicOr(a.status, kFlagWaitTimeout);
-  if (!abort_all && issued_pv) {
-    float o[32];
-    const int64_t orow = (static_cast<int64_t>(b) * a.Nq + qi) * a.Hq + head;
-    if (a.splits == 1) {
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&s_free[m][u]);
+      // visibility of the tile's 64 keys for this row
+      const int kbase = t * kKeys;
+      uint64_t vis = ~0ull;
+      bool full = kbase + kKeys <= L;
+      uint32_t pmask = 0;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tO + lane_off + c * 32, o);
-        if (row_valid) {
-          uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * D + c * 32);
+      for (int p = 0; p < kTilePages; ++p) pmask |= (tab[i * kTilePages + p] >= 0 ? 1u : 0u) << p;
+      full = full && pmask == 0xFu;
+      if (!full) {
+        const uint64_t pre = (L - kbase >= kKeys) ? ~0ull : (L > kbase ? ((1ull << (L - kbase)) - 1ull) : 0ull);
+        const uint64_t tree = mask_bits(my_anc, kbase - L) & ~pre;
+        uint64_t pg = 0;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv),
-                                 pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv),
-                                 pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv),
-                                 pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv));
+        for (int p = 0; p < kTilePages; ++p)
+          if ((pmask >> p) & 1u) pg |= 0xFFFFull << (16 * p);
+        const uint64_t inr = (nkeys - kbase >= kKeys) ? ~0ull : ((1ull << (nkeys - kbase)) - 1ull);
+        vis = (pre | tree) & pg & inr;
+      }
+      if (!row_valid) vis = 0;
+      // masked tile maximum (scores scaled to log2 units)
+      float tmax = NEG_INF;
+      if (warp_valid) {
+        if (full && row_valid) {
+#pragma unroll
+          for (int j = 0; j < kKeys; ++j) tmax = fmaxf(tmax, s[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kKeys; ++j)
+            if ((vis >> j) & 1ull) tmax = fmaxf(tmax, s[j]);
         }
+        tmax = (tmax == NEG_INF) ? NEG_INF : __fmul_rn(tmax, c);
       }
-      if (row_valid && a.lse) a.lse[orow] = (lx > 0.f) ? (m_used + log2f(lx)) * 0.69314718055994531f : NEG_INF;
-    } else {
-      const size_t pidx = ((static_cast<size_t>(bh) * a.mtiles + mt) * a.splits + split) * kRows + tid;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tO + lane_off + c * 32, o);
-        float4 *dst = reinterpret_cast<float4 *>(a.part_o + pidx * D + c * 32);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) dst[q4] = make_float4(o[q4 * 4], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+      const bool grow = tmax != NEG_INF && (m_used == NEG_INF || tmax > m_used + 8.f);
+      // P buffer u is free once P V of tile i - 2 completed
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[m][u], ((i - 2) >> 1) & 1))) {
+        s_abort = 1;
+        break;
       }
-      a.part_ml[pidx * 3 + 0] = m_used;
-      a.part_ml[pidx * 3 + 1] = l;
-      a.part_ml[pidx * 3 + 2] = lx;
+      // O is rescaled in TMEM (after P V of tile i - 1) when a row's maximum moved
+      if (i >= 1 && __any_sync(0xffffffffu, grow && m_used != NEG_INF)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[m][u ^ 1], ((i - 1) >> 1) & 1))) {
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const float f = (grow && m_used != NEG_INF) ? ex2(m_used - tmax) : 1.f;
+        float o[32];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          const uint32_t ta = tmem + 4 * kKeys + m * D + cc * 32 + lane_off;
+          tmem_ld32(ta, o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __fmul_rn(o[j], f);
+          tmem_st32(ta, o);
+        }
+        tc_fence_before();
+      }
+      if (grow) {
+        if (m_used != NEG_INF) {
+          const float f = ex2(m_used - tmax);
+          l2 = fma2(l2, pack2(f, f), pack2(0.f, 0.f));
+          lx2 = fma2(lx2, pack2(f, f), pack2(0.f, 0.f));
+        }
+        m_used = tmax;
+      }
+      // P = 2^(s c - m) in bf16, 128 bytes of this row in the swizzled K-major tile
+      uint8_t *prow = smem + CF::kP + (m * 2 + u) * CF::kPBytes;
+      const uint64_t c2 = pack2(c, c), nm2 = pack2(-m_used, -m_used);
+      const bool any = row_valid && m_used != NEG_INF;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int j = q4 * 8 + 2 * h;
+          float p0 = 0.f, p1 = 0.f;
+          if (any) {
+            float x0, x1;
+            unpack2(fma2(pack2(s[j], s[j + 1]), c2, nm2), x0, x1);
+            p0 = ((vis >> j) & 1ull) ? ex2(x0) : 0.f;
+            p1 = ((vis >> (j + 1)) & 1ull) ? ex2(x1) : 0.f;
+          }
+          const uint32_t pb = cvt_bf16x2(p0, p1);
+          lx2 = add2(lx2, pack2(p0, p1));
+          l2 = add2(l2, pack2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
+          pk[h] = pb;
+        }
+        *reinterpret_cast<uint4 *>(prow + sw128(r_own, q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      fence_proxy_async();  // P (generic writes) -> visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&p_full[m][u]);
     }
-  } else if (!abort_all && a.splits > 1) {
-    // no key of this split: an empty partial
-    const size_t pidx = ((static_cast<size_t>(bh) * a.mtiles + mt) * a.splits + split) * kRows + tid;
-    a.part_ml[pidx * 3 + 0] = NEG_INF;
-    a.part_ml[pidx * 3 + 1] = 0.f;
-    a.part_ml[pidx * 3 + 2] = 0.f;
+    // ---------------- epilogue: O after the last P V
+    float lo, hi;
+    unpack2(l2, lo, hi);
+    const float l = __fadd_rn(lo, hi);
+    unpack2(lx2, lo, hi);
+    const float lx = __fadd_rn(lo, hi);
+    bool have = false;
+    if (nt > 0 && !s_abort) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[m][(nt - 1) & 1], ((nt - 1) >> 1) & 1))) s_abort = 1;
+      else have = true;
+      tc_fence_after();
+    }
+    const int64_t orow = (static_cast<int64_t>(b) * a.Nq + qi) * a.Hq + head;
+    const int mtile = mg * MT + m;
+    if (have) {
+      float o[32];
+      if (a.splits == 1) {
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          tmem_ld32(tmem + 4 * kKeys + m * D + cc * 32 + lane_off, o);
+          if (row_valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * D + cc * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(pack_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv),
+                                   pack_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv),
+                                   pack_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv),
+                                   pack_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv));
+          }
+        }
+        if (row_valid && a.lse) a.lse[orow] = (lx > 0.f) ? (m_used + log2f(lx)) * 0.69314718055994531f : NEG_INF;
+      } else {
+        const size_t pidx = ((static_cast<size_t>(bh) * a.mtiles + mtile) * a.splits + split) * kRows + r_own;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          tmem_ld32(tmem + 4 * kKeys + m * D + cc * 32 + lane_off, o);
+          float4 *dst = reinterpret_cast<float4 *>(a.part_o + pidx * D + cc * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) dst[q4] = make_float4(o[q4 * 4], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+        }
+        a.part_ml[pidx * 3 + 0] = m_used;
+        a.part_ml[pidx * 3 + 1] = l;
+        a.part_ml[pidx * 3 + 2] = lx;
+      }
+    } else if (!s_abort && a.splits > 1) {
+      // no key of this split: an empty partial
+      const size_t pidx = ((static_cast<size_t>(bh) * a.mtiles + mtile) * a.splits + split) * kRows + r_own;
+      a.part_ml[pidx * 3 + 0] = NEG_INF;
+      a.part_ml[pidx * 3 + 1] = 0.f;
+      a.part_ml[pidx * 3 + 2] = 0.f;
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (s_abort && tid == 0) atomicOr(a.status, kFlagWaitTimeout);
+  if (warp == CF::kTmaWarp && lane == 0 && s_abort) {
+    // copies still in flight land before the CTA's shared memory is released
+    for (int i = max(0, issued - NS); i < issued; ++i) (void)mbar_wait(&kv_full[i % NS], (i / NS) & 1);
+  }
+  if (warp == CF::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // Merge the key-split partials of every (sequence, query row, head).
@@ -594,24 +671,26 @@ int attn_num_sms() {
 }
 
 struct AttnPlan {
-  int nrows, mtiles, splits, tiles_per_split;
+  int nrows, mtiles, mt_per_cta, mgroups, splits, tiles_per_split;
   size_t part_o_bytes, part_ml_bytes;
 };
 
-// Split the keys of every (sequence, KV head, row tile) so that the CTAs fill
-// whole waves of the GPU (2 resident per SM), with at least 2 tiles per split.
+// Row tiles per CTA: two at d = 64 (when there are two), one at d = 128.  Keys
+// are split so that the CTAs (one per SM) fill whole waves, with at least 4
+// tiles per split.
 AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   AttnPlan p;
-  const int kt = d == 64 ? KeysPerTile<64>::value : KeysPerTile<128>::value;
   p.nrows = (Hq / Hkv) * Nq;
   p.mtiles = (p.nrows + kRows - 1) / kRows;
-  const int ntiles = (max_keys + kt - 1) / kt;
-  const long base = static_cast<long>(B) * Hkv * p.mtiles;
-  const long slots = 2L * attn_num_sms();
+  p.mt_per_cta = (d == 64 && p.mtiles >= 2) ? 2 : 1;
+  p.mgroups = (p.mtiles + p.mt_per_cta - 1) / p.mt_per_cta;
+  const int ntiles = (max_keys + kKeys - 1) / kKeys;
+  const long base = static_cast<long>(B) * Hkv * p.mgroups;
+  const long slots = attn_num_sms();
   int best = 1;
   double best_eff = 0.0;
-  for (int s = 1; s <= 8; ++s) {
-    if (s > 1 && ntiles / s < 2) break;
+  for (int s = 1; s <= 16; ++s) {
+    if (s > 1 && ntiles / s < 4) break;
     const long ctas = base * s;
     const double waves = static_cast<double>(ctas) / slots;
     const double eff = waves / std::ceil(waves);
@@ -623,13 +702,30 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   p.splits = best;
   p.tiles_per_split = (ntiles + best - 1) / best;
   if (p.tiles_per_split < 1) p.tiles_per_split = 1;
-  const size_t nparts = best > 1 ? static_cast<size_t>(base) * best * kRows : 0;
+  const size_t nparts = best > 1 ? static_cast<size_t>(B) * Hkv * p.mtiles * best * kRows : 0;
   p.part_o_bytes = nparts * d * sizeof(float);
   p.part_ml_bytes = nparts * 3 * sizeof(float);
   return p;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+template <int D, int MT>
+cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a, dim3 grid,
+                             cudaStream_t cs) {
+  using CF = AttnCfg<D, MT>;
+  const int smem = CF::kTable + a.tiles_per_split * kTilePages * 4 + 1024;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(k_branch_attn_tc<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_branch_attn_tc<D, MT><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
+  e = cudaGetLastError();
+  if (e == cudaSuccess && a.splits > 1) {
+    k_attn_combine<D><<<dim3(grid.x, a.mtiles), 128, 0, cs>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
+}
 
 }  // namespace
 
@@ -682,8 +778,7 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   a.mtiles = p.mtiles;
   const bool split_ok = p.splits > 1 && ws && ws_bytes >= need && !(reinterpret_cast<uintptr_t>(ws) & 255u);
   a.splits = split_ok ? p.splits : 1;
-  const int kt = d == 64 ? KeysPerTile<64>::value : KeysPerTile<128>::value;
-  a.tiles_per_split = split_ok ? p.tiles_per_split : (max_keys + kt - 1) / kt;
+  a.tiles_per_split = split_ok ? p.tiles_per_split : (max_keys + kKeys - 1) / kKeys;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = static_cast<uint16_t *>(out);
   a.lse = lse;
@@ -694,31 +789,11 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   if (!make_kv_map(&kmap, k_cache, num_blocks, Hkv, d) || !make_kv_map(&vmap, v_cache, num_blocks, Hkv, d))
     return SSD_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  dim3 grid(B * Hkv, a.mtiles, a.splits);
+  const dim3 grid(B * Hkv, p.mgroups, a.splits);
   cudaError_t e;
-  if (d == 64) {
-    const int smem = AttnSmem<64>::kTotal + a.tiles_per_split * (KeysPerTile<64>::value / kPage) * 4 + 1024;
-    e = cudaFuncSetAttribute(k_branch_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) {
-      k_branch_attn_tc<64><<<grid, kAttnThreads, smem, cs>>>(kmap, vmap, a);
-      e = cudaGetLastError();
-    }
-    if (e == cudaSuccess && a.splits > 1) {
-      k_attn_combine<64><<<dim3(B * Hkv, a.mtiles), 128, 0, cs>>>(a);
-      e = cudaGetLastError();
-    }
-  } else {
-    const int smem = AttnSmem<128>::kTotal + a.tiles_per_split * (KeysPerTile<128>::value / kPage) * 4 + 1024;
-    e = cudaFuncSetAttribute(k_branch_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) {
-      k_branch_attn_tc<128><<<grid, kAttnThreads, smem, cs>>>(kmap, vmap, a);
-      e = cudaGetLastError();
-    }
-    if (e == cudaSuccess && a.splits > 1) {
-      k_attn_combine<128><<<dim3(B * Hkv, a.mtiles), 128, 0, cs>>>(a);
-      e = cudaGetLastError();
-    }
-  }
+  if (d == 64 && p.mt_per_cta == 2) e = launch_attention<64, 2>(kmap, vmap, a, grid, cs);
+  else if (d == 64) e = launch_attention<64, 1>(kmap, vmap, a, grid, cs);
+  else e = launch_attention<128, 1>(kmap, vmap, a, grid, cs);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -77,10 +77,30 @@ SSD_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// One poll that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (no busy spinning).
+SSD_DEV bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase with the given parity; false on timeout.
 SSD_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
   for (uint32_t it = 0; it < kMaxPolls; ++it)
     if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// The same wait for a single thread that may sleep between polls (at most
+// kMaxPolls polls of at most 1 us each).
+SSD_DEV bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kMaxPolls; ++it)
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
   return false;
 }
 // One bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)

@@ -12,23 +12,26 @@
 // Structure: a vocabulary call is at most two kernels.
 //   k_stats  one CTA per 32 KiB chunk of one logit row: the HBM pass, which
 //            carries nearly all of the call's bytes.  A TMA bulk copy stages
-//            the chunk in shared memory; the CTA reduces it to (max, sum of
-//            2^(z log2e/T - max), argmax, sorted top-F candidates) and
-//            publishes that record.  Chunks are numbered sequence-major and,
-//            within a sequence, by row pair r = (target row r, draft row r), so
-//            pairs complete in launch order.  The CTA that publishes the last
-//            chunk of a pair (an atomic count per pair) merges the pair: row
-//            statistics, the top-F_r list (the guesses of depth r), the Saguaro
-//            draw of d_{r+1} (its chunk is located from the chunk masses; only
-//            that chunk is staged again), p(d) and q'(d).  The CTA that merges
-//            the last pair of a sequence runs the acceptance chain and, unless
-//            a residual draw is needed, the bonus draw and the outputs.  No CTA
-//            ever waits for another: the last to arrive does the work.
-//   k_resid  (verification at T > 0) one CTA per chunk of each sequence's
-//            rejected row pair: residual chunk masses; the last CTA of a
-//            sequence draws the bonus token from them and writes the outputs.
-//            It is a programmatic dependent launch of k_stats, so its launch
-//            overlaps k_stats' last wave.
+//            the chunk in shared memory; the CTA reduces it to a record (max,
+//            sum of 2^(z log2e/T - max), argmax), the sorted top-F candidates
+//            and, for rows that are drawn from, per-block partial sums (a block
+//            = the 32 vectors one warp reads in one round).  Chunks are
+//            numbered sequence-major and, within a sequence, by row pair r =
+//            (target row r, draft row r), so pairs complete in launch order.
+//            The CTA that publishes the last chunk of a pair (an atomic count
+//            per pair) merges the pair: row statistics, the top-F_r list (the
+//            guesses of depth r), the Saguaro draw of d_{r+1}, p(d) and q'(d).
+//            A draw locates its chunk from the chunk masses and its block from
+//            the block sums; one warp then reads that block's 32 vectors again.
+//            The CTA that merges the last pair of a sequence runs the
+//            acceptance chain and, unless a residual draw is needed, the bonus
+//            draw and the outputs.  No CTA ever waits for another: the last to
+//            arrive does the work.
+//   k_resid  (verification at T > 0) one CTA per quarter chunk of each
+//            sequence's rejected row pair: residual block sums; the last CTA of
+//            a sequence draws the bonus token from them and writes the
+//            outputs.  It is a programmatic dependent launch of k_stats, so its
+//            launch overlaps k_stats' last wave.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -44,15 +47,16 @@ namespace ssd {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSegVec = 8;                             // 16-byte vectors per thread and chunk
-constexpr int kChunkBytes = kThreads * kSegVec * 16;  // 32 KiB
+constexpr int kRounds = 8;                             // 16-byte vectors per thread and chunk
+constexpr int kChunkBytes = kThreads * kRounds * 16;  // 32 KiB
+constexpr int kBlocks = kRounds * kWarps;              // blocks per chunk (round j, warp w)
+constexpr int kQuarters = 4;                           // k_resid units per chunk (2 rounds each)
 constexpr int kCandCap = 512;
 constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
 constexpr int kMaxChunks = 128;  // per row: 4 lists per lane in the warp merge
-constexpr int kWarpF = 32;       // top-F sizes selected warp by warp (larger F: block threshold)
-constexpr int kWarpCand = kCandCap / kWarps;  // candidate slots per warp (64)
+constexpr int kWarpF = 32;       // top-F sizes with per-warp thresholds (larger F: CTA-wide)
 constexpr int kRankMax = 1024;   // lists merged by rank selection up to this many keys
 constexpr int kNone = 0x7fffffff;
 
@@ -62,11 +66,18 @@ struct ChunkStat {
   int amax;  // lowest index holding m
   int pad;
 };
+// Per chunk of a row that is drawn from: each warp's maximum and, per block
+// (round j, warp w), the sum of 2^(z kT - fl(wm[w] kT)) over the block's
+// elements (0 when greedy or for a warp without finite elements).
+struct BlockRec {
+  float wm[kWarps];
+  float bs[kRounds][kWarps];
+};
 struct RowSlot {
   int16_t tensor;  // 0 = target, 1 = draft
   int16_t row;
-  int16_t F;  // top-F candidates wanted (0 = none)
-  int16_t pad;
+  int16_t F;       // top-F candidates wanted (0 = none)
+  int16_t blocks;  // block sums wanted (the row is drawn from)
 };
 struct RowInfo {  // merged statistics of row r of a sequence
   float mt, st;   // target max, sum relative to fl(mt kT)
@@ -79,10 +90,6 @@ struct PosInfo {  // draft token d_j and its probabilities
   int d;
   float p, q;  // p_j(d), q'_j(d); p < 0 marks an invalid token
   int pad;
-};
-struct ResInfo {
-  float w;   // residual mass of a chunk of row a
-  int last;  // last index of the chunk with positive residual (-1: none)
 };
 
 struct VocabArgs {
@@ -103,14 +110,16 @@ struct VocabArgs {
   int foff[kMaxK + 2];
   // workspace
   uint32_t *ctr;  // [0] finished sequences, [1] hits, [2+b] pairs done, [2+B+b] residual
-                  // chunks done, [2+2B + b(K+1) + r] chunks done of pair (b, r)
-  ChunkStat *stats;
-  uint64_t *cands;  // [B][nslots][nchunks][Fcap]
-  RowInfo *rows;    // [B][K+1]
-  uint64_t *S;      // [B][K+1][Fcap] merged top-F lists
-  PosInfo *pos;     // [B][K]
-  ResInfo *res;     // [B][nchunks]
-  int32_t *accs;    // [B] accept count of a sequence left to k_resid, else -1
+                  // units done, [2+2B + b(K+1) + r] chunks done of pair (b, r)
+  ChunkStat *stats;  // [B][nslots][nchunks]
+  BlockRec *blk;     // [B][nslots][nchunks]
+  uint64_t *cands;   // [B][nslots][nchunks][Fcap]
+  RowInfo *rows;     // [B][K+1]
+  uint64_t *S;       // [B][K+1][Fcap] merged top-F lists
+  PosInfo *pos;      // [B][K]
+  float *rmass;      // [B][nchunks * kQuarters] residual mass per unit
+  float *rbs;        // [B][nchunks][kBlocks] residual block sums
+  int32_t *accs;     // [B] accept count of a sequence left to k_resid, else -1
   // inputs / outputs
   const float *u_draft, *u_acc, *u_bonus;
   const int32_t *d_in;
@@ -124,7 +133,7 @@ struct VocabArgs {
   int32_t *slot_out, *next_tokens;
   uint32_t *hits;
   uint32_t *status;
-  unsigned long long *trace;  // optional: 4 words per CTA (see ssd_set_trace)
+  unsigned long long *trace;  // optional: 8 words per CTA (see ssd_set_trace)
 };
 
 SSD_DEV uint32_t *seq_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + b; }
@@ -158,21 +167,17 @@ SSD_DEV PosInfo ldcg_pos(const PosInfo *p) {
   const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
   return PosInfo{v.x, __int_as_float(v.y), __int_as_float(v.z), v.w};
 }
-SSD_DEV ResInfo ldcg_res(const ResInfo *p) {
-  const int2 v = __ldcg(reinterpret_cast<const int2 *>(p));
-  return ResInfo{__int_as_float(v.x), v.y};
-}
 SSD_DEV uint64_t ldcg_key(const uint64_t *p) { return __ldcg(reinterpret_cast<const unsigned long long *>(p)); }
 
-SSD_DEV unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
 SSD_DEV uint32_t ld_acquire(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+SSD_DEV uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 // Trace mark k of this CTA (ssd_set_trace): %globaltimer by thread 0.
 SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
@@ -182,32 +187,24 @@ SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
     mk[k] = t;
   }
 }
-SSD_DEV uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
 // ---------------------------------------------------------------------------
-// shared memory of a CTA (after the staged chunk buffers)
+// shared memory of a CTA (k_stats: after the staged chunk)
 // ---------------------------------------------------------------------------
 struct Smem {
-  uint64_t bar;    // completion of the TMA copies
-  uint32_t phase;  // completions of `bar` so far
-  int flag, ncand, found, last_pos;
+  uint64_t bar;  // completion of the chunk's TMA copy
+  int flag, ncand;
   float wm[kWarps], ws[kWarps];
   int wa[kWarps];
-  int wcnt[kWarps];
+  uint32_t tau[kWarps];
   uint64_t redk[kWarps];
-  float wtot[kWarps][kSegVec];  // per-round scan: warp totals, then warp offsets
-  float rtot[kSegVec];          // per-round totals
   float scal[8];
   int ival[8];
   RowInfo ri;
   uint64_t cand[kCandCap];
   ChunkStat cs[2][kMaxChunks];
-  float cmass[kMaxChunks];
-  int clast[kMaxChunks];
+  float cmass[kMaxChunks * kQuarters];
+  float bw[kBlocks];
   uint64_t S[kMaxF];
   float cp[kMaxK], cq[kMaxK], cu[kMaxK];
   int cd[kMaxK];
@@ -228,185 +225,232 @@ SSD_DEV bool arrive_last(uint32_t *ctr, uint32_t total, Smem &sh) {
   return sh.flag != 0;
 }
 
-// Wait for the next completion of sh.bar (bounded; WAIT_TIMEOUT on expiry,
-// then a second bounded wait so no copy is still landing when the buffer is
-// reused).  Every thread calls.
-SSD_DEV void wait_copies(uint32_t *status, Smem &sh) {
-  const uint32_t ph = sh.phase;
-  if (!mbar_wait(&sh.bar, ph & 1u)) {
-    if (threadIdx.x == 0) atomicOr(status, kFlagWaitTimeout);
-    (void)mbar_wait(&sh.bar, ph & 1u);
+// ===========================================================================
+// element access and weights
+// ===========================================================================
+// The 16-byte vector at chunk-local element i0 of a row chunk starting at e0
+// with n elements, from global memory; elements at or past n read as `fill`.
+template <class E>
+SSD_DEV void ld_vec(const char *row, int e0, int n, int i0, float fill, float *f) {
+  if (i0 + E::kVec <= n) {
+    E::unpack(__ldg(reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(e0 + i0) * E::kSize)), f);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e) f[e] = (i0 + e < n) ? E::ld(row, e0 + i0 + e) : fill;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) sh.phase = ph + 1;
-  __syncthreads();
 }
 
-// Stage chunk c of one or two rows (their whole 16-byte vectors; nullptr rows
-// are skipped) in shared memory with TMA bulk copies, and wait for them.
-// Every thread calls.
-template <class E>
-SSD_DEV void issue_rows(const VocabArgs &a, const char *r0, uint8_t *b0, const char *r1, uint8_t *b1, int c,
-                        Smem &sh) {
+// Weight functors: operator()(zt, zd, idx) -> weight >= 0 with a fixed sequence
+// of correctly rounded operations, so every pass over the same elements agrees.
+struct WSaguaro {  // unnormalised q'_i
+  float mdk, kT, C;
+  uint64_t keyF;
+  bool hasS;
+  SSD_DEV float operator()(float, float zd, int idx) const {
+    const float e = ex2(__fmaf_rn(zd, kT, -mdk));
+    return (hasS && cand_key(zd, idx) >= keyF) ? __fmul_rn(e, C) : e;
+  }
+};
+struct WTarget {  // unnormalised p_i
+  float mtk, kT;
+  SSD_DEV float operator()(float zt, float, int) const { return ex2(__fmaf_rn(zt, kT, -mtk)); }
+};
+struct WResidual {  // max(0, p_i - q'_i)
+  float mtk, kT, inv_st, mdk, fC, f1;
+  uint64_t keyF;
+  bool hasS;
+  SSD_DEV float operator()(float zt, float zd, int idx) const {
+    const float p = __fmul_rn(ex2(__fmaf_rn(zt, kT, -mtk)), inv_st);
+    const float f = (hasS && cand_key(zd, idx) >= keyF) ? fC : f1;
+    const float q = __fmul_rn(ex2(__fmaf_rn(zd, kT, -mdk)), f);
+    const float r = __fsub_rn(p, q);
+    return r > 0.f ? r : 0.f;
+  }
+};
+
+// A block is the 32 consecutive vectors (256 j + 32 w + lane) warp w reads in
+// round j.  Within a block the running weight has a fixed order: each lane
+// sums its vector's weights in element order, the lanes are combined by a
+// Hillis-Steele inclusive scan; the block's sum is the scan's last value.
+SSD_DEV float warp_incl_scan(float x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = __fadd_rn(x, t);
+  }
+  return x;
+}
+
+// This lane's weights of its vector of block (round j, warp w) of chunk c; the
+// return value is their sum in element order.
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV float lane_weights(const VocabArgs &a, const char *rowT, const char *rowD, int c, int j, int w, const WF &wf,
+                           float *x) {
+  const int lane = threadIdx.x & 31;
   const int e0 = c * a.chunk_elems;
   const int n = min(a.chunk_elems, a.V - e0);
-  const uint32_t bulk = static_cast<uint32_t>((n * E::kSize) & ~15);
-  __syncthreads();  // earlier reads and writes of the buffers are done
-  if (threadIdx.x == 0) {
-    fence_proxy_async();  // ... and ordered before the copies that overwrite them
-    mbar_arrive_expect_tx(&sh.bar, (r0 ? bulk : 0u) + (r1 ? bulk : 0u));
-    if (bulk && r0) bulk_g2s(b0, r0 + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
-    if (bulk && r1) bulk_g2s(b1, r1 + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
+  const int i0 = (j * kThreads + w * 32 + lane) * E::kVec;
+  float ft[E::kVec], fd[E::kVec];
+  if constexpr (HT) ld_vec<E>(rowT, e0, n, i0, 0.f, ft);
+  if constexpr (HD) ld_vec<E>(rowD, e0, n, i0, 0.f, fd);
+  float p = 0.f;
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) {
+    x[e] = (i0 + e < n) ? wf(HT ? ft[e] : 0.f, HD ? fd[e] : 0.f, e0 + i0 + e) : 0.f;
+    p = __fadd_rn(p, x[e]);
   }
+  return p;
 }
-template <class E>
-SSD_DEV void stage_rows(const VocabArgs &a, const char *r0, uint8_t *b0, const char *r1, uint8_t *b1, int c,
-                        Smem &sh) {
-  issue_rows<E>(a, r0, b0, r1, b1, c, sh);
-  wait_copies(a.status, sh);
+
+// One warp: the first element of block (c, j, w) whose running weight exceeds
+// `target` with positive weight; when rounding leaves the target in a lane that
+// has no such element, that lane's last positive element; when no lane holds
+// it, the block's last positive element; -1 for a block without weight.  All
+// 32 lanes call; all return the result.
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, int c, int j, int w, float target,
+                      const WF &wf) {
+  const int lane = threadIdx.x & 31;
+  float x[E::kVec];
+  const float p = lane_weights<E, HT, HD>(a, rowT, rowD, c, j, w, wf, x);
+  const float incl = warp_incl_scan(p);
+  float ex = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) ex = 0.f;
+  const int i0 = c * a.chunk_elems + (j * kThreads + w * 32 + lane) * E::kVec;
+  float run = 0.f;
+  int hit = -1, lpos = -1;
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) {
+    run = __fadd_rn(run, x[e]);
+    if (x[e] > 0.f) {
+      lpos = i0 + e;
+      if (hit < 0 && __fadd_rn(ex, run) > target) hit = lpos;
+    }
+  }
+  const bool cross = p > 0.f && __fadd_rn(ex, p) > target;
+  const uint32_t mc = __ballot_sync(0xffffffffu, cross);
+  if (mc) return __shfl_sync(0xffffffffu, hit >= 0 ? hit : lpos, __ffs(mc) - 1);
+  int best = lpos;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  return best;
+}
+
+// Thread 0: the first of n masses (summed in order) whose cumulative sum
+// exceeds the target (u * total, or u itself when u_is_target), with positive
+// mass; rounding past the end takes the last positive one.  sh.ival[0] = its
+// index (-1 when the total is 0), sh.scal[1] = the target minus the mass
+// before it, sh.scal[2] = the total.  The caller synchronises.
+SSD_DEV void locate(const float *mass, int n, float u, bool u_is_target, Smem &sh) {
+  float W = 0.f;
+  for (int c = 0; c < n; ++c) W = __fadd_rn(W, mass[c]);
+  const float target = u_is_target ? u : __fmul_rn(u, W);
+  int cs = -1;
+  float before = 0.f, cum = 0.f;
+  for (int c = 0; c < n; ++c) {
+    const float nc = __fadd_rn(cum, mass[c]);
+    if (nc > target && mass[c] > 0.f) {
+      cs = c;
+      before = cum;
+      break;
+    }
+    cum = nc;
+  }
+  if (cs < 0 && W > 0.f) {  // rounding left the target past the end: the last positive mass
+    float b2 = 0.f;
+    for (int c = 0; c < n; ++c) {
+      if (mass[c] > 0.f) {
+        cs = c;
+        before = b2;
+      }
+      b2 = __fadd_rn(b2, mass[c]);
+    }
+  }
+  sh.ival[0] = (W > 0.f) ? cs : -1;
+  sh.scal[1] = __fsub_rn(target, before);
+  sh.scal[2] = W;
 }
 
 // ===========================================================================
 // k_stats: statistics of one staged chunk
 // ===========================================================================
-// Thread t owns the chunk's 16-byte vectors t, t + 256, ... and, in a row's
-// last chunk, tail element t (the < 16 bytes past the last whole vector).
+// Thread t owns the chunk's vectors t + 256 j (round j); vector nvec, when the
+// row's last chunk ends inside it, is read from global memory (-inf past the
+// end).
 template <class E>
 struct ChunkView {
   const uint4 *v4;
-  int e0, nvec, nbulk, ntail;
-  float zt;  // this thread's tail element (-inf if none)
-};
-
-// Candidates of this warp's elements for the top-F (F <= 32): every element
-// whose key reaches tau, the F-th largest lane maximum (ballot radix select),
-// so at least F of them and with them the warp's top-F.  They go to the warp's
-// kWarpCand slots of sh.cand, the count to sh.wcnt[warp]; when they do not fit
-// (ties at tau), the warp's exact top-F instead.
-template <class E>
-SSD_DEV void warp_candidates(const ChunkView<E> &cv, int F, float m1, bool has, Smem &sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t mykey = has ? f2ord(m1) : 0u;
-  uint32_t tau = 0;
-  for (int bit = 31; bit >= E::kLowBit; --bit) {
-    const uint32_t t = tau | (1u << bit);
-    if (__popc(__ballot_sync(0xffffffffu, mykey >= t)) >= F) tau = t;
+  const char *row;
+  int e0, n, nvec, ntail;
+  SSD_DEV bool has(int v) const { return v < nvec || (v == nvec && ntail > 0); }
+  SSD_DEV void get(int v, float *f) const {
+    if (v < nvec) E::unpack(v4[v], f);
+    else ld_vec<E>(row, e0, n, v * E::kVec, -__int_as_float(0x7f800000), f);
   }
-  if (lane == 0) sh.wcnt[warp] = 0;
-  __syncwarp();
-  uint64_t *wc = sh.cand + warp * kWarpCand;
-  if (has && mykey >= tau) {
-#pragma unroll
-    for (int j = 0; j < kSegVec; ++j) {
-      const int v = tid + j * kThreads;
-      if (v < cv.nvec) {
-        float f[E::kVec];
-        E::unpack(cv.v4[v], f);
-#pragma unroll
-        for (int e = 0; e < E::kVec; ++e)
-          if (f2ord(f[e]) >= tau) {
-            const int p = atomicAdd(&sh.wcnt[warp], 1);
-            if (p < kWarpCand) wc[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
-          }
+  // maximum of vector v (-inf if absent)
+  SSD_DEV float vmax(int v) const {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    if (v < nvec) {
+      const uint4 w = v4[v];
+      if constexpr (E::kSize == 2) {
+        const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+        return fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
+      } else {
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
       }
     }
-    if (tid < cv.ntail && f2ord(cv.zt) >= tau) {
-      const int p = atomicAdd(&sh.wcnt[warp], 1);
-      if (p < kWarpCand) wc[p] = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
+    float m = NEG_INF;
+    if (has(v)) {
+      float f[E::kVec];
+      get(v, f);
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e) m = fmaxf(m, f[e]);
+    }
+    return m;
+  }
+};
+
+// Candidates for the top-F: every element whose key reaches tau goes to
+// sh.cand (count sh.ncand); past kCandCap (ties at tau), the chunk's exact
+// top-F instead.  `mine`: this thread may hold candidates.  Every thread calls.
+template <class E>
+SSD_DEV void collect(const ChunkView<E> &cv, bool mine, uint32_t tau, int F, Smem &sh) {
+  const int tid = threadIdx.x;
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const int v = tid + j * kThreads;
+    if (mine && cv.has(v) && f2ord(cv.vmax(v)) >= tau) {
+      float f[E::kVec];
+      cv.get(v, f);
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e)
+        if (v * E::kVec + e < cv.n && f2ord(f[e]) >= tau) {
+          const int p = atomicAdd(&sh.ncand, 1);
+          if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
+        }
     }
   }
-  __syncwarp();
-  if (sh.wcnt[warp] > kWarpCand) {
+  __syncthreads();
+  if (sh.ncand > kCandCap) {
     // too many ties at the threshold: exact selection, one winner per sweep
     uint64_t prev = ~0ull;
     for (int r = 0; r < F; ++r) {
       uint64_t best = 0;
 #pragma unroll
-      for (int j = 0; j < kSegVec; ++j) {
+      for (int j = 0; j < kRounds; ++j) {
         const int v = tid + j * kThreads;
-        if (v < cv.nvec) {
+        if (cv.has(v)) {
           float f[E::kVec];
-          E::unpack(cv.v4[v], f);
+          cv.get(v, f);
 #pragma unroll
           for (int e = 0; e < E::kVec; ++e) {
-            const uint64_t key = cand_key(f[e], cv.e0 + v * E::kVec + e);
+            const uint64_t key = (v * E::kVec + e < cv.n) ? cand_key(f[e], cv.e0 + v * E::kVec + e) : 0ull;
             if (key < prev && key > best) best = key;
           }
         }
-      }
-      if (tid < cv.ntail) {
-        const uint64_t key = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
-        if (key < prev && key > best) best = key;
-      }
-      best = warp_max_u64(best);
-      if (lane == 0) wc[r] = best;
-      prev = best;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      int k = 0;
-      while (k < F && wc[k] != 0ull) ++k;  // winners are descending; 0 = none left
-      sh.wcnt[warp] = k;
-    }
-  }
-  __syncwarp();
-}
-
-// Candidates of the whole chunk (F > 32): every element whose key reaches the
-// F-th largest per-thread maximum (CTA-wide radix select), into sh.cand[0..
-// sh.ncand); when they do not fit, the chunk's exact top-F.  Every thread calls.
-template <class E>
-SSD_DEV void block_candidates(const ChunkView<E> &cv, int F, float m1, bool has, Smem &sh) {
-  const int tid = threadIdx.x;
-  const uint32_t mykey = has ? f2ord(m1) : 0u;
-  uint32_t tau = 0;
-  for (int bit = 31; bit >= E::kLowBit; --bit) {
-    const uint32_t t = tau | (1u << bit);
-    if (__syncthreads_count(mykey >= t) >= F) tau = t;
-  }
-  if (tid == 0) sh.ncand = 0;
-  __syncthreads();
-  if (has && mykey >= tau) {
-#pragma unroll
-    for (int j = 0; j < kSegVec; ++j) {
-      const int v = tid + j * kThreads;
-      if (v < cv.nvec) {
-        float f[E::kVec];
-        E::unpack(cv.v4[v], f);
-#pragma unroll
-        for (int e = 0; e < E::kVec; ++e)
-          if (f2ord(f[e]) >= tau) {
-            const int p = atomicAdd(&sh.ncand, 1);
-            if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
-          }
-      }
-    }
-    if (tid < cv.ntail && f2ord(cv.zt) >= tau) {
-      const int p = atomicAdd(&sh.ncand, 1);
-      if (p < kCandCap) sh.cand[p] = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
-    }
-  }
-  __syncthreads();
-  if (sh.ncand > kCandCap) {
-    uint64_t prev = ~0ull;
-    for (int r = 0; r < F; ++r) {
-      uint64_t best = 0;
-#pragma unroll
-      for (int j = 0; j < kSegVec; ++j) {
-        const int v = tid + j * kThreads;
-        if (v < cv.nvec) {
-          float f[E::kVec];
-          E::unpack(cv.v4[v], f);
-#pragma unroll
-          for (int e = 0; e < E::kVec; ++e) {
-            const uint64_t key = cand_key(f[e], cv.e0 + v * E::kVec + e);
-            if (key < prev && key > best) best = key;
-          }
-        }
-      }
-      if (tid < cv.ntail) {
-        const uint64_t key = cand_key(cv.zt, cv.e0 + cv.nbulk + tid);
-        if (key < prev && key > best) best = key;
       }
       best = block_max_u64<kThreads>(best, sh.redk);
       if (tid == 0) sh.cand[r] = best;
@@ -418,37 +462,24 @@ SSD_DEV void block_candidates(const ChunkView<E> &cv, int F, float m1, bool has,
       while (k < F && sh.cand[k] != 0ull) ++k;
       sh.ncand = k;
     }
+    __syncthreads();
   }
-  __syncthreads();
 }
 
-// Top-F by rank over candidate groups (group g: n[g] distinct nonzero keys
-// at keys + g * stride, ngroups <= kWarps): the key with r larger keys goes to
-// dst[r] when r < F; dst slots no key fills are set to 0.  Every thread calls;
-// no barrier inside.  Candidate i of the flattened groups is thread i's.
-SSD_DEV void rank_select(const uint64_t *keys, const int *n, int ngroups, int stride, int F, uint64_t *dst) {
-  int off[kWarps + 1];
-  off[0] = 0;
-#pragma unroll
-  for (int g = 0; g < kWarps; ++g) off[g + 1] = off[g] + (g < ngroups ? n[g] : 0);
-  const int total = off[kWarps];
+// Top-F of n distinct nonzero keys by rank (the key with r larger keys goes
+// to dst[r] when r < F); slots past n are set to 0.  No barrier inside.
+SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
   for (int i = threadIdx.x; i < F; i += kThreads)
-    if (i >= total) dst[i] = 0ull;
-  for (int i = threadIdx.x; i < total; i += kThreads) {
-    int g = 0;
-#pragma unroll
-    for (int h = 1; h < kWarps; ++h) g += (i >= off[h]) ? 1 : 0;
-    const uint64_t k = keys[g * stride + (i - off[g])];
+    if (i >= n) dst[i] = 0ull;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint64_t k = keys[i];
     int rank = 0;
-    for (int h = 0; h < ngroups; ++h) {
-      const uint64_t *kh = keys + h * stride;
-      for (int j = 0; j < n[h]; ++j) rank += (kh[j] > k) ? 1 : 0;
-    }
+    for (int j = 0; j < n; ++j) rank += (keys[j] > k) ? 1 : 0;
     if (rank < F) dst[rank] = k;
   }
 }
 
-// The chunk's record (ChunkStat) and sorted top-F candidate list.
+// The chunk's record, block sums and sorted top-F candidate list.
 template <class E>
 SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8_t *buf, Smem &sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -458,112 +489,175 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
   const float NEG_INF = -__int_as_float(0x7f800000);
   ChunkView<E> cv;
   cv.v4 = reinterpret_cast<const uint4 *>(buf);
+  cv.row = row_ptr(a, rs.tensor, b, rs.row, E::kSize);
   cv.e0 = c * a.chunk_elems;
-  const int n = min(a.chunk_elems, a.V - cv.e0);
-  cv.nvec = (n * E::kSize) >> 4;
-  cv.nbulk = cv.nvec * E::kVec;
-  cv.ntail = n - cv.nbulk;
-  cv.zt = (tid < cv.ntail) ? E::ld(row_ptr(a, rs.tensor, b, rs.row, E::kSize), cv.e0 + cv.nbulk + tid) : NEG_INF;
-  const bool has = tid < cv.nvec || tid < cv.ntail;
+  cv.n = min(a.chunk_elems, a.V - cv.e0);
+  cv.nvec = (cv.n * E::kSize) >> 4;
+  cv.ntail = cv.n - cv.nvec * E::kVec;
+  const bool tail_mine = cv.ntail > 0 && tid == (cv.nvec & (kThreads - 1));  // the partial vector
 
-  // pass 1: the thread's maximum (packed bf16 maxima for bf16 rows)
-  float m1;
-  if constexpr (E::kSize == 2) {
-    uint32_t mx = 0xFF80FF80u;  // two bf16 -inf
+  // pass 1: the thread's maximum and the first of its vectors holding it
+  // (packed bf16 maxima for bf16 rows)
+  float m1 = NEG_INF;
+  int j1 = -1;
 #pragma unroll
-    for (int j = 0; j < kSegVec; ++j) {
-      const int v = tid + j * kThreads;
-      if (v < cv.nvec) {
-        const uint4 w = cv.v4[v];
-        mx = bmax2(mx, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+  for (int j = 0; j < kRounds; ++j) {
+    const int v = tid + j * kThreads;
+    if (v < cv.nvec) {
+      const uint4 w = cv.v4[v];
+      float vm;
+      if constexpr (E::kSize == 2) {
+        const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+        vm = fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
+      } else {
+        vm = fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+      }
+      if (vm > m1 || j1 < 0) {  // strictly larger: the first vector among equal maxima
+        m1 = fmaxf(m1, vm);
+        j1 = j;
       }
     }
-    m1 = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
-  } else {
-    float mx = NEG_INF;
-#pragma unroll
-    for (int j = 0; j < kSegVec; ++j) {
-      const int v = tid + j * kThreads;
-      if (v < cv.nvec) {
-        const uint4 w = cv.v4[v];
-        mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                             fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
-      }
-    }
-    m1 = mx;
   }
-  m1 = fmaxf(m1, cv.zt);
-  const float wm = warp_max(m1);
-  // a lane holding the warp maximum finds its lowest index (elements in index order)
-  int i1 = kNone;
-  if (m1 == wm) {
-#pragma unroll 1
-    for (int j = 0; j < kSegVec && i1 == kNone; ++j) {
-      const int v = tid + j * kThreads;
-      if (v >= cv.nvec) break;
-      float f[E::kVec];
-      E::unpack(cv.v4[v], f);
-#pragma unroll
-      for (int e = E::kVec - 1; e >= 0; --e)
-        if (f[e] == wm) i1 = v * E::kVec + e;
+  if (tail_mine) {
+    const float vm = cv.vmax(cv.nvec);
+    if (vm > m1 || j1 < 0) {
+      m1 = fmaxf(m1, vm);
+      j1 = cv.nvec / kThreads;
     }
-    if (i1 == kNone && tid < cv.ntail && cv.zt == wm) i1 = cv.nbulk + tid;
+  }
+  const float wm = warp_max(m1);
+  // the lane holding the warp maximum: its first element there
+  int i1 = kNone;
+  if (m1 == wm && j1 >= 0) {
+    const int v = tid + j1 * kThreads;
+    float f[E::kVec];
+    cv.get(v, f);
+#pragma unroll
+    for (int e = E::kVec - 1; e >= 0; --e)
+      if (f[e] == wm && v * E::kVec + e < cv.n) i1 = v * E::kVec + e;
   }
   int wi = i1;
 #pragma unroll
   for (int o = 16; o; o >>= 1) wi = min(wi, __shfl_xor_sync(0xffffffffu, wi, o));
-  // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed FMA / ADD
+  // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed
+  // FMA / ADD (the same arithmetic whether or not block sums are kept); rows
+  // that are drawn from also keep their block sums
   float s = 0.f;
+  BlockRec *br = a.blk + chunk_index(a, b, slot, c);
   if (!greedy && wm != NEG_INF) {
     const float Mk = __fmul_rn(wm, kT);
     const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
+    float tail = 0.f;  // the partial vector's sum, element order
+    if (tail_mine) {
+      float f[E::kVec];
+      cv.get(cv.nvec, f);
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
+    }
     uint64_t acc = pack2(0.f, 0.f);
+    if (rs.blocks) {
 #pragma unroll
-    for (int j = 0; j < kSegVec; ++j) {
-      const int v = tid + j * kThreads;
-      if (v < cv.nvec) {
-        const uint4 w = cv.v4[v];
+      for (int j = 0; j < kRounds; ++j) {
+        const int v = tid + j * kThreads;
+        float pj = 0.f;
+        if (v < cv.nvec) {
+          const uint4 w = cv.v4[v];
+          uint64_t accj = pack2(0.f, 0.f);
 #pragma unroll
-        for (int h = 0; h < E::kPairs; ++h) {
-          float x0, x1;
-          unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
-          acc = add2(acc, pack2(ex2(x0), ex2(x1)));
+          for (int h = 0; h < E::kPairs; ++h) {
+            float x0, x1;
+            unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
+            const uint64_t e2 = pack2(ex2(x0), ex2(x1));
+            acc = add2(acc, e2);
+            accj = add2(accj, e2);
+          }
+          float lo, hi;
+          unpack2(accj, lo, hi);
+          pj = __fadd_rn(lo, hi);
+        } else if (tail_mine && v == cv.nvec) {
+          pj = tail;
+        }
+        const float bsum = warp_sum(pj);
+        if (lane == 0) br->bs[j][warp] = bsum;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRounds; ++j) {
+        const int v = tid + j * kThreads;
+        if (v < cv.nvec) {
+          const uint4 w = cv.v4[v];
+#pragma unroll
+          for (int h = 0; h < E::kPairs; ++h) {
+            float x0, x1;
+            unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
+            acc = add2(acc, pack2(ex2(x0), ex2(x1)));
+          }
         }
       }
     }
     float lo, hi;
     unpack2(acc, lo, hi);
-    s = __fadd_rn(lo, hi);
-    if (tid < cv.ntail) s = __fadd_rn(s, ex2(__fmaf_rn(cv.zt, kT, -Mk)));
+    s = __fadd_rn(__fadd_rn(lo, hi), tail);
+    s = warp_sum(s);
+  } else if (rs.blocks && lane == 0) {
+#pragma unroll
+    for (int j = 0; j < kRounds; ++j) br->bs[j][warp] = 0.f;  // every block record of a drawn row is written
   }
-  s = warp_sum(s);
   if (lane == 0) {
+    if (rs.blocks) br->wm[warp] = wm;
     sh.wm[warp] = wm;
     sh.ws[warp] = s;
     sh.wa[warp] = wi;
   }
+  // top-F candidates: threshold tau with at least F elements reaching it
   const int F = rs.F;
-  if (F > 1 && F <= kWarpF) warp_candidates<E>(cv, F, m1, has, sh);
-  else if (F > kWarpF) block_candidates<E>(cv, F, m1, has, sh);
-  __syncthreads();
   uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
-  if (F > 1 && F <= kWarpF) rank_select(sh.cand, sh.wcnt, kWarps, kWarpCand, F, out);
-  else if (F > kWarpF) rank_select(sh.cand, &sh.ncand, 1, 0, F, out);
-  if (tid == 0) {
-    float M = sh.wm[0];
-    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sh.wm[w]);
-    int amax = kNone;
-    for (int w = 0; w < kWarps; ++w)
-      if (sh.wm[w] == M) amax = min(amax, sh.wa[w]);
-    float S = 0.f;
-    if (!greedy && M != NEG_INF) {
-      const float Mk = __fmul_rn(M, kT);
-      for (int w = 0; w < kWarps; ++w)
-        if (sh.wm[w] != NEG_INF) S = __fadd_rn(S, __fmul_rn(sh.ws[w], ex2(__fsub_rn(__fmul_rn(sh.wm[w], kT), Mk))));
+  if (F > 1) {
+    const uint32_t mykey = cv.has(tid) ? f2ord(m1) : 0u;
+    uint32_t tau = 0;
+    if (F <= kWarpF) {
+      // per warp: the F-th largest lane maximum (ballot radix select); the
+      // chunk's top-F all reach the largest of the warps' thresholds
+      for (int bit = 31; bit >= E::kLowBit; --bit) {
+        const uint32_t t = tau | (1u << bit);
+        if (__popc(__ballot_sync(0xffffffffu, mykey >= t)) >= F) tau = t;
+      }
+      if (lane == 0) sh.tau[warp] = tau;
+      __syncthreads();
+      tau = sh.tau[0];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) tau = max(tau, sh.tau[w]);
+    } else {
+      // CTA-wide: the F-th largest thread maximum
+      for (int bit = 31; bit >= E::kLowBit; --bit) {
+        const uint32_t t = tau | (1u << bit);
+        if (__syncthreads_count(mykey >= t) >= F) tau = t;
+      }
     }
-    if (amax == kNone) amax = 0;  // an all -inf chunk: its first index
-    if (F == 1) out[0] = cand_key(M, cv.e0 + amax);
-    a.stats[chunk_index(a, b, slot, c)] = ChunkStat{M, S, cv.e0 + amax, 0};
+    collect<E>(cv, cv.has(tid) && mykey >= tau, tau, F, sh);
+    rank_select(sh.cand, sh.ncand, F, out);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // lanes 0..7 hold the warps' records; reduced within groups of 8 lanes
+    const int w = lane & (kWarps - 1);
+    const float wmw = sh.wm[w];
+    float M = wmw;
+#pragma unroll
+    for (int o = kWarps / 2; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    int amax = (wmw == M) ? sh.wa[w] : kNone;
+#pragma unroll
+    for (int o = kWarps / 2; o; o >>= 1) amax = min(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float S = 0.f;
+    if (!greedy && M != NEG_INF && wmw != NEG_INF)
+      S = __fmul_rn(sh.ws[w], ex2(__fsub_rn(__fmul_rn(wmw, kT), __fmul_rn(M, kT))));
+#pragma unroll
+    for (int o = kWarps / 2; o; o >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
+    if (lane == 0) {
+      if (amax == kNone) amax = 0;  // an all -inf chunk: its first index
+      if (F == 1) out[0] = cand_key(M, cv.e0 + amax);
+      a.stats[chunk_index(a, b, slot, c)] = ChunkStat{M, S, cv.e0 + amax, 0};
+    }
   }
 }
 
@@ -630,303 +724,140 @@ SSD_DEV void merge_topf(const uint64_t *lists, size_t stride, int nchunks, int F
   __syncwarp();
 }
 
-// ===========================================================================
-// inverse-CDF draws over one staged chunk (one CTA)
-// ===========================================================================
-// Weight functors: operator()(zt, zd, idx) -> weight >= 0 with a fixed sequence
-// of correctly rounded operations, so every pass over the same elements agrees.
-struct WSaguaro {  // unnormalised q'_i
-  float mdk, kT, C;
-  uint64_t keyF;
-  bool hasS;
-  SSD_DEV float operator()(float, float zd, int idx) const {
-    const float e = ex2(__fmaf_rn(zd, kT, -mdk));
-    return (hasS && cand_key(zd, idx) >= keyF) ? __fmul_rn(e, C) : e;
-  }
-};
-struct WTarget {  // unnormalised p_i
-  float mtk, kT;
-  SSD_DEV float operator()(float zt, float, int) const { return ex2(__fmaf_rn(zt, kT, -mtk)); }
-};
-struct WResidual {  // max(0, p_i - q'_i)
-  float mtk, kT, inv_st, mdk, fC, f1;
-  uint64_t keyF;
-  bool hasS;
-  SSD_DEV float operator()(float zt, float zd, int idx) const {
-    const float p = __fmul_rn(ex2(__fmaf_rn(zt, kT, -mtk)), inv_st);
-    const float f = (hasS && cand_key(zd, idx) >= keyF) ? fC : f1;
-    const float q = __fmul_rn(ex2(__fmaf_rn(zd, kT, -mdk)), f);
-    const float r = __fsub_rn(p, q);
-    return r > 0.f ? r : 0.f;
-  }
-};
-
-// One chunk of the target and / or draft row staged in shared memory (whole
-// vectors); its < 16 tail bytes are read from global memory.
-template <class E>
-struct Staged {
-  const uint8_t *t, *d;  // staged chunks (unused rows: nullptr)
-  const char *rt, *rd;   // the rows in global memory
-  int e0, n, nbulk;      // first element, elements, elements in whole vectors
-};
-template <class E>
-SSD_DEV Staged<E> staged(const VocabArgs &a, const uint8_t *bt, const char *rt, const uint8_t *bd, const char *rd,
-                         int c) {
-  Staged<E> S;
-  S.t = bt;
-  S.d = bd;
-  S.rt = rt;
-  S.rd = rd;
-  S.e0 = c * a.chunk_elems;
-  S.n = min(a.chunk_elems, a.V - S.e0);
-  S.nbulk = ((S.n * E::kSize) >> 4) * E::kVec;
-  return S;
-}
-template <class E>
-SSD_DEV void staged_vec(const uint8_t *buf, const char *row, int e0, int n, int nbulk, int i0, float *f) {
-  if (i0 < nbulk) {
-    E::unpack(*reinterpret_cast<const uint4 *>(buf + static_cast<size_t>(i0) * E::kSize), f);
-  } else {
-#pragma unroll
-    for (int e = 0; e < E::kVec; ++e) f[e] = (i0 + e < n) ? E::ld(row, e0 + i0 + e) : 0.f;
-  }
-}
-
-// Rounds: the chunk's vectors in kSegVec rounds of kThreads, thread t owning
-// vector j * kThreads + t of round j (vocabulary order: round, thread,
-// element).  p[j] = the thread's weight sum of its round-j vector, in element
-// order; *last = its last index with positive weight.
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV void round_partials(const Staged<E> &S, const WF &wf, float *p, int *last) {
-#pragma unroll
-  for (int j = 0; j < kSegVec; ++j) {
-    const int i0 = (j * kThreads + static_cast<int>(threadIdx.x)) * E::kVec;
-    float acc = 0.f;
-    if (i0 < S.n) {
-      float ft[E::kVec], fd[E::kVec];
-      if constexpr (HT) staged_vec<E>(S.t, S.rt, S.e0, S.n, S.nbulk, i0, ft);
-      if constexpr (HD) staged_vec<E>(S.d, S.rd, S.e0, S.n, S.nbulk, i0, fd);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e) {
-        const float x = (i0 + e < S.n) ? wf(HT ? ft[e] : 0.f, HD ? fd[e] : 0.f, S.e0 + i0 + e) : 0.f;
-        acc = __fadd_rn(acc, x);
-        if (x > 0.f) *last = S.e0 + i0 + e;
-      }
-    }
-    p[j] = acc;
-  }
-}
-
-// Per round j: ex[j] = exclusive prefix of p[j] over the threads (warp
-// Hillis-Steele scan, warp offsets summed in warp order), sh.rtot[j] = the
-// round total.  Contains barriers.
-SSD_DEV void round_scan(const float *p, float *ex, Smem &sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float inc[kSegVec];
-#pragma unroll
-  for (int j = 0; j < kSegVec; ++j) inc[j] = p[j];
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-    for (int j = 0; j < kSegVec; ++j) {
-      const float t = __shfl_up_sync(0xffffffffu, inc[j], o);
-      if (lane >= o) inc[j] = __fadd_rn(inc[j], t);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kSegVec; ++j) {
-    const float t = __shfl_up_sync(0xffffffffu, inc[j], 1);
-    ex[j] = (lane == 0) ? 0.f : t;
-    if (lane == 31) sh.wtot[warp][j] = inc[j];
-  }
-  group_sync<kThreads>();
-  if (threadIdx.x < kSegVec) {
-    const int j = threadIdx.x;
-    float run = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float t = sh.wtot[w][j];
-      sh.wtot[w][j] = run;
-      run = __fadd_rn(run, t);
-    }
-    sh.rtot[j] = run;
-  }
-  group_sync<kThreads>();
-#pragma unroll
-  for (int j = 0; j < kSegVec; ++j) ex[j] = __fadd_rn(sh.wtot[warp][j], ex[j]);
-  group_sync<kThreads>();
-}
-
-// Total weight of the staged chunk (rounds summed in order); *last = its last
-// index with positive weight (-1 if none).
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV float range_total(const Staged<E> &S, const WF &wf, int *last, Smem &sh) {
-  float p[kSegVec], ex[kSegVec];
-  int lp = -1;
-  round_partials<E, HT, HD>(S, wf, p, &lp);
-  if (threadIdx.x == 0) sh.last_pos = -1;
-  round_scan(p, ex, sh);
-  atomicMax(&sh.last_pos, lp);
-  if (threadIdx.x == 0) {
-    float W = 0.f;
-    for (int j = 0; j < kSegVec; ++j) W = __fadd_rn(W, sh.rtot[j]);
-    sh.scal[0] = W;
-  }
-  group_sync<kThreads>();
-  const float W = sh.scal[0];
-  *last = sh.last_pos;
-  group_sync<kThreads>();
-  return W;
-}
-
-// First index of the staged chunk whose running weight (the order of
-// range_total) exceeds `target` and whose weight is positive; where rounding
-// leaves no such index in the round that holds the target, that round's last
-// positive index; -1 when the chunk has no weight.
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV int range_find(const Staged<E> &S, float target, const WF &wf, Smem &sh) {
-  float p[kSegVec], ex[kSegVec];
-  int lp = -1;
-  round_partials<E, HT, HD>(S, wf, p, &lp);
-  round_scan(p, ex, sh);
-  if (threadIdx.x == 0) {
-    // the round holding the target: cumulative round totals in order
-    int js = -1, jl = -1;
-    float base = 0.f, bs = 0.f, bl = 0.f;
-    for (int j = 0; j < kSegVec; ++j) {
-      const float R = sh.rtot[j];
-      const float nb = __fadd_rn(base, R);
-      if (R > 0.f) {
-        jl = j;
-        bl = base;
-        if (js < 0 && nb > target) {
-          js = j;
-          bs = base;
-        }
-      }
-      base = nb;
-    }
-    if (js < 0) {  // rounding left the target past the end: the last round with weight
-      js = jl;
-      bs = bl;
-    }
-    sh.ival[5] = js;
-    sh.scal[5] = bs;
-    sh.found = kNone;
-    sh.last_pos = -1;
-  }
-  group_sync<kThreads>();
-  const int js = sh.ival[5];
-  if (js >= 0) {
-    float pj = 0.f, ej = 0.f;
-#pragma unroll
-    for (int j = 0; j < kSegVec; ++j)
-      if (j == js) {
-        pj = p[j];
-        ej = ex[j];
-      }
-    if (pj > 0.f) {
-      const float b0 = __fadd_rn(sh.scal[5], ej);
-      const int i0 = (js * kThreads + static_cast<int>(threadIdx.x)) * E::kVec;
-      float ft[E::kVec], fd[E::kVec];
-      if constexpr (HT) staged_vec<E>(S.t, S.rt, S.e0, S.n, S.nbulk, i0, ft);
-      if constexpr (HD) staged_vec<E>(S.d, S.rd, S.e0, S.n, S.nbulk, i0, fd);
-      float run = 0.f;
-      int hit = -1, lpos = -1;
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e) {
-        const float x = (i0 + e < S.n) ? wf(HT ? ft[e] : 0.f, HD ? fd[e] : 0.f, S.e0 + i0 + e) : 0.f;
-        run = __fadd_rn(run, x);
-        if (x > 0.f) {
-          lpos = S.e0 + i0 + e;
-          if (hit < 0 && __fadd_rn(b0, run) > target) hit = lpos;
-        }
-      }
-      atomicMax(&sh.last_pos, lpos);
-      if (__fadd_rn(b0, pj) > target) atomicMin(&sh.found, hit >= 0 ? hit : lpos);
-    }
-  }
-  group_sync<kThreads>();
-  const int r = (js < 0) ? -1 : (sh.found != kNone ? sh.found : sh.last_pos);
-  group_sync<kThreads>();
-  return r;
-}
-
-// Locate the chunk holding u * W among per-chunk masses sh.cmass[0..nchunks)
-// (summed in chunk order) -- thread 0 -- with the target inside that chunk.
-SSD_DEV void locate_chunk(int nchunks, float u, Smem &sh) {
-  if (threadIdx.x == 0) {
-    float W = 0.f;
-    for (int c = 0; c < nchunks; ++c) W = __fadd_rn(W, sh.cmass[c]);
-    const float target = __fmul_rn(u, W);
-    int cs = -1;
-    float before = 0.f, cum = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-      const float nc = __fadd_rn(cum, sh.cmass[c]);
-      if (nc > target && sh.cmass[c] > 0.f) {
-        cs = c;
-        before = cum;
-        break;
-      }
-      cum = nc;
-    }
-    if (cs < 0 && W > 0.f)  // rounding left u * W past the end: the last chunk with mass
-      for (int c = nchunks - 1; c >= 0; --c)
-        if (sh.cmass[c] > 0.f) {
-          cs = c;
-          before = __fsub_rn(W, sh.cmass[c]);
-          break;
-        }
-    sh.ival[0] = (W > 0.f) ? cs : -1;
-    sh.scal[1] = __fsub_rn(target, before);
-    sh.scal[2] = W;
-  }
-  group_sync<kThreads>();
-}
-
-// Draw by the chunk masses in sh.cmass: locate the chunk, stage it (the rows
-// given: target rowT into bt, draft rowD into bd), one pass over it.  -1 when
-// the masses sum to zero or the staged chunk has no weight.
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV int chunked_draw(const VocabArgs &a, const char *rowT, uint8_t *bt, const char *rowD, uint8_t *bd, float u,
-                         const WF &wf, float *W_out, Smem &sh) {
-  locate_chunk(a.nchunks, u, sh);
-  const int cs = sh.ival[0];
-  const float local = sh.scal[1];
-  *W_out = sh.scal[2];
-  if (cs < 0) return -1;
-  stage_rows<E>(a, HT ? rowT : nullptr, bt, HD ? rowD : nullptr, bd, cs, sh);
-  return range_find<E, HT, HD>(staged<E>(a, bt, rowT, bd, rowD, cs), local, wf, sh);
-}
-
-// Exact chunk masses by one pass over every chunk of the row (used for Saguaro
-// sampling when the down-weighted mass makes the statistics' masses inexact).
-template <class E, class WF>
-SSD_DEV void exact_chunk_masses_draft(const VocabArgs &a, const char *rowD, uint8_t *bd, const WF &wf, Smem &sh) {
-  for (int c = 0; c < a.nchunks; ++c) {
-    stage_rows<E>(a, nullptr, nullptr, rowD, bd, c, sh);
-    int last;
-    const float t = range_total<E, false, true>(staged<E>(a, nullptr, nullptr, bd, rowD, c), wf, &last, sh);
-    if (threadIdx.x == 0) sh.cmass[c] = t;
-  }
-  group_sync<kThreads>();
-}
-
 SSD_DEV float norm_N(float C, float sq) { return __fsub_rn(1.f, __fmul_rn(__fsub_rn(1.f, C), sq)); }
 
-// p_{r+1} (target row r) drawn by its chunk masses from the published chunk
-// records; the row's argmax if they are all zero.
-template <class E>
-SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, float u, uint8_t *buf, Smem &sh) {
+// ===========================================================================
+// draws by the statistics of a row: chunk (chunk masses), block (block sums),
+// then one warp over the block
+// ===========================================================================
+// Chunk masses of 2^(z kT - rk) (rk = fl(row max kT)) from the row's chunk
+// records, into sh.cmass.  Caller synchronises.
+SSD_DEV void chunk_masses(const VocabArgs &a, int b, int slot, float rk, Smem &sh) {
   const float NEG_INF = -__int_as_float(0x7f800000);
-  const float mtk = __fmul_rn(row.mt, a.kT);
   for (int c = threadIdx.x; c < a.nchunks; c += kThreads) {
-    const ChunkStat cs = ldcg_stat(a.stats + chunk_index(a, b, a.tsl[r], c));
-    sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), mtk)));
+    const ChunkStat cs = ldcg_stat(a.stats + chunk_index(a, b, slot, c));
+    sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), rk)));
   }
-  group_sync<kThreads>();
+}
+
+// Draw from row `slot` of sequence b (its elements in `row`) with weights wf =
+// 2^(z kT - rk), scaled by C on the set S (the Fn keys of Slist) when C < 1.
+// sh.cmass holds the chunk masses with the down-weighting applied.  Every
+// thread calls; returns the token (-1 if the masses are all 0).
+template <class E, bool HT, class WF>
+SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, float rk, float u, const WF &wf,
+                       const uint64_t *Slist, int Fn, float C, Smem &sh) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) locate(sh.cmass, a.nchunks, u, false, sh);
+  __syncthreads();
+  const int cs = sh.ival[0];
+  const float local = sh.scal[1];
+  if (cs < 0) return -1;
+  // block weights of chunk cs
+  if (tid < kBlocks) {
+    const BlockRec *br = a.blk + chunk_index(a, b, slot, cs);
+    const int j = tid / kWarps, w = tid % kWarps;
+    const float wmw = __ldcg(&br->wm[w]);
+    const float bs = __ldcg(&br->bs[j][w]);
+    sh.bw[tid] = (wmw == -__int_as_float(0x7f800000) || !(bs > 0.f))
+                     ? 0.f
+                     : __fmul_rn(bs, ex2(__fsub_rn(__fmul_rn(wmw, a.kT), rk)));
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (C < 1.f) {  // the set S inside this chunk: down-weight its elements
+      const int e0 = cs * a.chunk_elems;
+      for (int i = 0; i < Fn; ++i) {
+        const uint64_t k = Slist[i];
+        if (!k) continue;
+        const int idx = cand_idx(k) - e0;
+        if (idx < 0 || idx >= a.chunk_elems) continue;
+        const int v = idx / E::kVec;
+        const int blk = (v / kThreads) * kWarps + (v % kThreads) / 32;
+        const float e = ex2(__fmaf_rn(cand_val(k), a.kT, -rk));
+        sh.bw[blk] = fmaxf(__fsub_rn(sh.bw[blk], __fmul_rn(__fsub_rn(1.f, C), e)), 0.f);
+      }
+    }
+    locate(sh.bw, kBlocks, local, true, sh);
+    if (sh.ival[0] < 0) {  // no block weight (the masses rounded differently): the last block
+      sh.ival[0] = kBlocks - 1;
+      sh.scal[1] = local;
+    }
+  }
+  __syncthreads();
+  const int blk = sh.ival[0];
+  const float local2 = sh.scal[1];
+  int d = -1;
+  if (warp == 0)
+    d = warp_find<E, HT, !HT>(a, HT ? row : nullptr, HT ? nullptr : row, cs, blk / kWarps, blk % kWarps, local2,
+                              wf);
+  __syncthreads();  // everyone read sh.ival / sh.scal
+  if (tid == 0) sh.ival[4] = d;
+  __syncthreads();
+  return sh.ival[4];
+}
+
+// A draw from a row without usable block sums (rows whose statistics kept
+// none, or Saguaro weights whose down-weighting makes the statistics' masses
+// inexact): exact block sums by one warp per block (the arithmetic of
+// warp_find), chunk masses from them, then the located chunk's block sums
+// again and one warp over the located block.  Every thread calls; returns the
+// token (-1 when the row has no weight).
+template <class E, bool HT, bool HD, class WF>
+SSD_DEV int exact_draw(const VocabArgs &a, const char *rowT, const char *rowD, float u, const WF &wf, Smem &sh) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto block_sums = [&](int c) {  // sh.bw[0..kBlocks) of chunk c
+    for (int k = warp; k < kBlocks; k += kWarps) {
+      float x[E::kVec];
+      const float p = lane_weights<E, HT, HD>(a, rowT, rowD, c, k / kWarps, k % kWarps, wf, x);
+      const float incl = warp_incl_scan(p);
+      if (lane == 31) sh.bw[k] = incl;
+    }
+    __syncthreads();
+  };
+  for (int c = 0; c < a.nchunks; ++c) {
+    block_sums(c);
+    if (tid == 0) {
+      float m = 0.f;
+      for (int k = 0; k < kBlocks; ++k) m = __fadd_rn(m, sh.bw[k]);
+      sh.cmass[c] = m;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) locate(sh.cmass, a.nchunks, u, false, sh);
+  __syncthreads();
+  const int cs = sh.ival[0];
+  const float local = sh.scal[1];
+  if (cs < 0) return -1;
+  __syncthreads();
+  block_sums(cs);
+  if (tid == 0) locate(sh.bw, kBlocks, local, true, sh);
+  __syncthreads();
+  const int blk = sh.ival[0];
+  const float local2 = sh.scal[1];
+  int d = -1;
+  if (warp == 0 && blk >= 0) d = warp_find<E, HT, HD>(a, rowT, rowD, cs, blk / kWarps, blk % kWarps, local2, wf);
+  __syncthreads();
+  if (tid == 0) sh.ival[4] = d;
+  __syncthreads();
+  return sh.ival[4];
+}
+
+// p_{r+1} (target row r) drawn by its statistics; the row's argmax if the
+// masses are all zero.
+template <class E>
+SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, float u, Smem &sh) {
+  const float mtk = __fmul_rn(row.mt, a.kT);
   const WTarget wp{mtk, a.kT};
-  float Wp;
-  const int d = chunked_draw<E, true, false>(a, row_ptr(a, 0, b, r, E::kSize), buf, nullptr, nullptr, u, wp, &Wp, sh);
+  const char *rowT = row_ptr(a, 0, b, r, E::kSize);
+  int d;
+  if (a.slot[a.tsl[r]].blocks) {
+    chunk_masses(a, b, a.tsl[r], mtk, sh);
+    __syncthreads();
+    d = stats_draw<E, true>(a, b, a.tsl[r], rowT, mtk, u, wp, nullptr, 0, 1.f, sh);
+  } else {
+    d = exact_draw<E, true, false>(a, rowT, nullptr, u, wp, sh);
+  }
   return (d >= 0) ? d : row.at;
 }
 
@@ -948,7 +879,7 @@ SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64
 // pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
 // ===========================================================================
 template <class E>
-SSD_DEV void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh) {
+__device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh) {
   const int tid = threadIdx.x;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int ts = a.tsl[r], ds = a.dsl[r];
@@ -964,10 +895,7 @@ SSD_DEV void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh
   const bool by_rank = nl <= kRankMax;
   if (F > 0 && by_rank) {
     const uint64_t *src = a.cands + chunk_index(a, b, ds, 0) * a.Fcap;
-    for (int i = tid; i < nl; i += kThreads) {
-      const uint64_t k = ldcg_key(src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
-      lists[i] = k;
-    }
+    for (int i = tid; i < nl; i += kThreads) lists[i] = ldcg_key(src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
   }
   __syncthreads();
   if (tid == 0) {
@@ -1045,8 +973,8 @@ SSD_DEV void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh
       } else {
         const WSaguaro wf{mdk, a.kT, a.C, keyF, F > 0};
         const float u = a.u_draft[static_cast<size_t>(b) * a.K + r];
-        if (__fmul_rn(__fsub_rn(1.f, a.C), ri.sq) > 0.875f) {
-          exact_chunk_masses_draft<E>(a, rowD, buf, wf, sh);
+        if (__fmul_rn(__fsub_rn(1.f, a.C), ri.sq) > 0.875f || !a.slot[ds].blocks) {
+          d = exact_draw<E, false, true>(a, nullptr, rowD, u, wf, sh);
         } else {
           // chunk masses of q' (unnormalised): s_c 2^(Mk_c - mdk) - (1 - C) sum_{i in S, in c} e_i
           for (int c = tid; c < a.nchunks; c += kThreads) {
@@ -1064,9 +992,8 @@ SSD_DEV void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh
             for (int c = 0; c < a.nchunks; ++c) sh.cmass[c] = fmaxf(sh.cmass[c], 0.f);
           }
           __syncthreads();
+          d = stats_draw<E, false>(a, b, ds, rowD, mdk, u, wf, sh.S, F, a.C, sh);
         }
-        float W;
-        d = chunked_draw<E, false, true>(a, nullptr, nullptr, rowD, buf, u, wf, &W, sh);
         if (d < 0) d = ri.ad;
         const float zd = E::ld(rowD, d);
         const bool ins = F > 0 && cand_key(zd, d) >= keyF;
@@ -1117,7 +1044,7 @@ SSD_DEV void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh
 // Stage in shared memory, in one round of loads, what the final steps of
 // sequence b need whatever the accept count: draft tokens, p(d), q'(d), the
 // uniforms, every row's merged statistics and S threshold key and (with_res)
-// the residual chunk records.  Then the acceptance chain (thread 0).  Every
+// the residual unit masses.  Then the acceptance chain (thread 0).  Every
 // thread returns the accept count.
 SSD_DEV int stage_chain(const VocabArgs &a, int b, bool with_res, Smem &sh) {
   const int tid = threadIdx.x;
@@ -1134,12 +1061,10 @@ SSD_DEV int stage_chain(const VocabArgs &a, int b, bool with_res, Smem &sh) {
     const int F = a.Fs[r];
     sh.keyF[r] = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
   }
-  if (with_res)
-    for (int c = tid; c < a.nchunks; c += kThreads) {
-      const ResInfo ri = ldcg_res(a.res + static_cast<size_t>(b) * a.nchunks + c);
-      sh.cmass[c] = ri.w;
-      sh.clast[c] = ri.last;
-    }
+  if (with_res) {
+    const int nu = a.nchunks * kQuarters;
+    for (int q = tid; q < nu; q += kThreads) sh.cmass[q] = __ldcg(a.rmass + static_cast<size_t>(b) * nu + q);
+  }
   __syncthreads();
   if (tid == 0) {
     int acc = 0;
@@ -1194,7 +1119,7 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
 // The last pair of sequence b merged: chain, then (greedy, or every token
 // accepted) the bonus draw and the outputs; a residual draw is left to k_resid.
 template <class E>
-SSD_DEV void seq_finish(const VocabArgs &a, int b, uint8_t *buf, Smem &sh) {
+__device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Smem &sh) {
   const int acc = stage_chain(a, b, false, sh);
   if (!a.greedy && acc < a.K) {
     if (threadIdx.x == 0) a.accs[b] = acc;
@@ -1211,7 +1136,7 @@ SSD_DEV void seq_finish(const VocabArgs &a, int b, uint8_t *buf, Smem &sh) {
       zero = !(W > 0.f);
     }
   } else {
-    bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], buf, sh);
+    bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], sh);
   }
   emit(a, b, acc, bt, W, zero, sh);
 }
@@ -1231,7 +1156,7 @@ SSD_DEV void trace_entry(unsigned long long *tr, int kind, int b, int idx, const
 // the kernels
 // ===========================================================================
 template <class E>
-__global__ void __launch_bounds__(kThreads, 4) k_stats(const VocabArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ VocabArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t *buf = smem_raw;
   Smem &sh = *reinterpret_cast<Smem *>(smem_raw + kChunkBytes);
@@ -1243,15 +1168,27 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const VocabArgs a) {
   const int rem = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * per_seq);
   const int slot = rem / a.nchunks, c = rem - slot * a.nchunks;
   const RowSlot rs = a.slot[slot];
+  // the chunk's whole vectors: one TMA bulk copy; thread 0 waits (bounded,
+  // sleeping between polls), the other threads at the barrier
   if (tid == 0) {
+    if (a.trace)
+      for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
+    mark(a, sh.mk, 0);
+    const int e0 = c * a.chunk_elems;
+    const int n = min(a.chunk_elems, a.V - e0);
+    const uint32_t bulk = static_cast<uint32_t>((n * E::kSize) & ~15);
     mbar_init(&sh.bar, 1);
     fence_mbar_init();
-    sh.phase = 0;
-    for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
+    mbar_arrive_expect_tx(&sh.bar, bulk);
+    if (bulk)
+      bulk_g2s(buf, row_ptr(a, rs.tensor, b, rs.row, E::kSize) + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
+    if (!mbar_wait_sleep(&sh.bar, 0)) {
+      atomicOr(a.status, kFlagWaitTimeout);
+      (void)mbar_wait_sleep(&sh.bar, 0);  // the copy still in flight: a second bounded wait before the buffer is read
+    }
+    mark(a, sh.mk, 1);
   }
-  mark(a, sh.mk, 0);
-  stage_rows<E>(a, row_ptr(a, rs.tensor, b, rs.row, E::kSize), buf, nullptr, nullptr, c, sh);
-  mark(a, sh.mk, 1);
+  __syncthreads();
   stats_chunk<E>(a, b, slot, c, buf, sh);
   int kind = 0;
   const int r = rs.row;
@@ -1263,7 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const VocabArgs a) {
     mark(a, sh.mk, 4);
     if (a.do_verify && arrive_last(seq_ctr(a, b), static_cast<uint32_t>(a.npairs), sh)) {
       kind = 3;
-      seq_finish<E>(a, b, buf, sh);
+      seq_finish<E>(a, b, sh);
       mark(a, sh.mk, 5);
     }
   }
@@ -1271,71 +1208,101 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const VocabArgs a) {
   if (a.trace && tid == 0) trace_entry(a.trace + 8 * static_cast<size_t>(blockIdx.x), kind, b, rem, sh.mk);
 }
 
+// Residual unit (sequence b, chunk c, quarter g = rounds 2g, 2g+1): its block
+// sums of max(0, p - q') over target and draft row a, read straight from
+// global memory; the last unit of the sequence draws the bonus.
 template <class E>
-__global__ void __launch_bounds__(kThreads, 2) k_resid(const VocabArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t *bufT = smem_raw;
-  uint8_t *bufD = smem_raw + kChunkBytes;
-  Smem &sh = *reinterpret_cast<Smem *>(smem_raw + 2 * kChunkBytes);
+__global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ VocabArgs a) {
+  __shared__ Smem sh;
   // everything k_stats wrote is visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int tid = threadIdx.x;
-  const int b = static_cast<int>(blockIdx.x / a.nchunks);
-  const int c = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * a.nchunks);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nu = a.nchunks * kQuarters;
+  const int b = static_cast<int>(blockIdx.x / nu);
+  const int u = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * nu);
+  const int c = u / kQuarters, g = u % kQuarters;
   const int acc = __ldcg(a.accs + b);
   if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
-  if (tid == 0) {
-    mbar_init(&sh.bar, 1);
-    fence_mbar_init();
-    sh.phase = 0;
+  if (tid == 0 && a.trace)
     for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
-  }
   mark(a, sh.mk, 0);
   const char *rowT = row_ptr(a, 0, b, acc, E::kSize);
   const char *rowD = row_ptr(a, 1, b, acc, E::kSize);
-  issue_rows<E>(a, rowT, bufT, rowD, bufD, c, sh);
-  // the row's merged statistics while the chunk lands
   const size_t rr = static_cast<size_t>(b) * (a.K + 1) + acc;
   const RowInfo row = ldcg_row(a.rows + rr);
   const int F = a.Fs[acc];
   const uint64_t keyF = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
   const WResidual wf = residual_weights(a, row, keyF, F);
-  wait_copies(a.status, sh);
-  mark(a, sh.mk, 1);
-  int last;
-  const float w = range_total<E, true, true>(staged<E>(a, bufT, rowT, bufD, rowD, c), wf, &last, sh);
-  if (tid == 0) a.res[static_cast<size_t>(b) * a.nchunks + c] = ResInfo{w, last};
+  float *rbs = a.rbs + (static_cast<size_t>(b) * a.nchunks + c) * kBlocks;
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const int j = 2 * g + jj;
+    float x[E::kVec];
+    const float p = lane_weights<E, true, true>(a, rowT, rowD, c, j, warp, wf, x);
+    const float incl = warp_incl_scan(p);
+    if (lane == 31) {
+      rbs[j * kWarps + warp] = incl;
+      sh.bw[jj * kWarps + warp] = incl;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float m = 0.f;
+    for (int k = 0; k < 2 * kWarps; ++k) m = __fadd_rn(m, sh.bw[k]);
+    a.rmass[static_cast<size_t>(b) * nu + u] = m;
+  }
   mark(a, sh.mk, 2);
   int kind = 2;
-  if (arrive_last(res_ctr(a, b), static_cast<uint32_t>(a.nchunks), sh)) {
+  if (arrive_last(res_ctr(a, b), static_cast<uint32_t>(nu), sh)) {
     kind = 3;
     mark(a, sh.mk, 3);
     const int acc2 = stage_chain(a, b, true, sh);  // the same chain: acc2 == acc
     const RowInfo ra = sh.rows[acc2];
     const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
     const float ub = a.u_bonus[b];
-    locate_chunk(a.nchunks, ub, sh);
-    mark(a, sh.mk, 4);
-    const int cs = sh.ival[0];
-    const float local = sh.scal[1];
-    const float W = sh.scal[2];
-    int bt;
-    bool zero = false;
-    if (cs >= 0) {
-      if (cs != c) stage_rows<E>(a, rowT, bufT, rowD, bufD, cs, sh);
-      const int d = range_find<E, true, true>(staged<E>(a, bufT, rowT, bufD, rowD, cs), local, wa, sh);
-      bt = (d >= 0) ? d : sh.clast[cs];
-    } else {
-      zero = true;  // no residual mass: p_{a+1} instead
-      bt = draw_target<E>(a, b, acc2, ra, ub, bufT, sh);
+    if (tid == 0) {
+      locate(sh.cmass, nu, ub, false, sh);
+      const int uq = sh.ival[0];
+      sh.ival[6] = uq;
+      sh.scal[6] = sh.scal[2];  // the residual's total mass
+      if (uq >= 0) {
+        const float *src = a.rbs + (static_cast<size_t>(b) * a.nchunks + uq / kQuarters) * kBlocks +
+                           2 * (uq % kQuarters) * kWarps;
+        for (int k = 0; k < 2 * kWarps; ++k) sh.bw[k] = __ldcg(src + k);
+        const float local = sh.scal[1];
+        locate(sh.bw, 2 * kWarps, local, true, sh);
+        if (sh.ival[0] < 0) {  // a unit of positive mass has a positive block; kept for safety
+          sh.ival[0] = 2 * kWarps - 1;
+          sh.scal[1] = local;
+        }
+      }
     }
+    __syncthreads();
+    mark(a, sh.mk, 4);
+    const int uq = sh.ival[6];
+    const float W = sh.scal[6];
+    int bt = -1;
+    if (uq >= 0) {
+      const int k = sh.ival[0];
+      const float local2 = sh.scal[1];
+      int d = -1;
+      if (warp == 0)
+        d = warp_find<E, true, true>(a, rowT, rowD, uq / kQuarters, 2 * (uq % kQuarters) + k / kWarps, k % kWarps,
+                                     local2, wa);
+      __syncthreads();
+      if (tid == 0) sh.ival[4] = d;
+      __syncthreads();
+      bt = sh.ival[4];
+    }
+    const bool zero = uq < 0;  // no residual mass: p_{a+1} instead
+    if (bt < 0) bt = draw_target<E>(a, b, acc2, ra, ub, sh);
     mark(a, sh.mk, 5);
     emit(a, b, acc2, bt, W, zero, sh);
   }
   mark(a, sh.mk, 6);
   if (a.trace && tid == 0) {
     const size_t base = static_cast<size_t>(a.B) * a.nslots * a.nchunks;
-    trace_entry(a.trace + 8 * (base + blockIdx.x), kind, b, c, sh.mk);
+    trace_entry(a.trace + 8 * (base + blockIdx.x), kind, b, u, sh.mk);
   }
 }
 
@@ -1391,7 +1358,7 @@ namespace {
 struct Layout {
   int nslots, nchunks, chunk_elems, Fcap;
   size_t ctr_words;
-  size_t ctr_off, stats_off, cands_off, rows_off, S_off, pos_off, res_off, accs_off, total;
+  size_t ctr_off, stats_off, blk_off, cands_off, rows_off, S_off, pos_off, rmass_off, rbs_off, accs_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1418,6 +1385,8 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + L->ctr_words * sizeof(uint32_t), 256);
   L->stats_off = o;
   o = align_up(o + nrec * sizeof(ChunkStat), 256);
+  L->blk_off = o;
+  o = align_up(o + nrec * sizeof(BlockRec), 256);
   L->cands_off = o;
   o = align_up(o + nrec * L->Fcap * sizeof(uint64_t), 256);
   L->rows_off = o;
@@ -1426,8 +1395,10 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + Bn * (K + 1) * L->Fcap * sizeof(uint64_t), 256);
   L->pos_off = o;
   o = align_up(o + Bn * (K > 0 ? K : 1) * sizeof(PosInfo), 256);
-  L->res_off = o;
-  o = align_up(o + Bn * L->nchunks * sizeof(ResInfo), 256);
+  L->rmass_off = o;
+  o = align_up(o + Bn * L->nchunks * kQuarters * sizeof(float), 256);
+  L->rbs_off = o;
+  o = align_up(o + Bn * L->nchunks * kBlocks * sizeof(float), 256);
   L->accs_off = o;
   o = align_up(o + Bn * sizeof(int32_t), 256);
   L->total = o;
@@ -1494,7 +1465,9 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.rows = reinterpret_cast<RowInfo *>(w + L.rows_off);
   a.S = reinterpret_cast<uint64_t *>(w + L.S_off);
   a.pos = reinterpret_cast<PosInfo *>(w + L.pos_off);
-  a.res = reinterpret_cast<ResInfo *>(w + L.res_off);
+  a.blk = reinterpret_cast<BlockRec *>(w + L.blk_off);
+  a.rmass = reinterpret_cast<float *>(w + L.rmass_off);
+  a.rbs = reinterpret_cast<float *>(w + L.rbs_off);
   a.accs = reinterpret_cast<int32_t *>(w + L.accs_off);
   a.status = status;
   return a;
@@ -1503,7 +1476,7 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
 // Rows read by a call: target rows 0..ntarget-1 and draft rows 0..ndraft-1,
 // slots ordered by pair (target r, then draft r).  `topf`: draft rows keep
 // their top-F_r lists.
-void set_slots(VocabArgs &a, int ntarget, int ndraft, bool topf) {
+void set_slots(VocabArgs &a, int ntarget, int ndraft, bool topf, bool draws) {
   int n = 0;
   a.npairs = ntarget > ndraft ? ntarget : ndraft;
   for (int r = 0; r <= a.K; ++r) {
@@ -1515,12 +1488,16 @@ void set_slots(VocabArgs &a, int ntarget, int ndraft, bool topf) {
     int rows = 0;
     if (r < ntarget) {
       a.tsl[r] = n;
-      a.slot[n++] = RowSlot{0, static_cast<int16_t>(r), 0, 0};
+      // block sums on the rows a draw may use: target row K (the bonus after
+      // full acceptance) and the draft rows sampled from (d_{r+1})
+      const bool blk = draws && a.do_verify && r == a.K;
+      a.slot[n++] = RowSlot{0, static_cast<int16_t>(r), 0, static_cast<int16_t>(blk)};
       ++rows;
     }
     if (r < ndraft) {
       a.dsl[r] = n;
-      a.slot[n++] = RowSlot{1, static_cast<int16_t>(r), static_cast<int16_t>(a.Fs[r]), 0};
+      const bool blk = draws && a.do_sample && r < a.K;
+      a.slot[n++] = RowSlot{1, static_cast<int16_t>(r), static_cast<int16_t>(a.Fs[r]), static_cast<int16_t>(blk)};
       ++rows;
     }
     a.pair_chunks[r] = rows * a.nchunks;
@@ -1537,7 +1514,6 @@ void *g_trace = nullptr;
 size_t g_trace_bytes = 0;
 
 constexpr size_t kStatsSmem = kChunkBytes + sizeof(Smem);
-constexpr size_t kResidSmem = 2 * kChunkBytes + sizeof(Smem);
 
 ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
@@ -1555,12 +1531,10 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   if (!(g_smem_attr_set[ti][dev / 64].load() & bit)) {
     e = cudaFuncSetAttribute(k_stats<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_resid<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kResidSmem));
-    if (e != cudaSuccess) return e;
     g_smem_attr_set[ti][dev / 64].fetch_or(bit);
   }
   const long n1 = static_cast<long>(a.B) * a.nslots * a.nchunks;
-  const long n2 = (a.do_verify && !a.greedy && a.K > 0) ? static_cast<long>(a.B) * a.nchunks : 0;
+  const long n2 = (a.do_verify && !a.greedy && a.K > 0) ? static_cast<long>(a.B) * a.nchunks * kQuarters : 0;
   if (n1 < 1) return cudaSuccess;
   if (n1 > 0x7fffffffL) return cudaErrorInvalidValue;
   a.trace = (g_trace && g_trace_bytes >= static_cast<size_t>(n1 + n2) * 64)
@@ -1581,7 +1555,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(n2));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kResidSmem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1714,8 +1688,8 @@ ssd_status_t ssd_saguaro_sample(const void *draft, ssd_dtype_t dt, int64_t seq_s
   if (B == 0 || K == 0) return SSD_OK;
   if (!u_draft || !d_out || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(draft, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
-  set_slots(a, 0, K, C < 1.f);
   a.do_sample = 1;
+  set_slots(a, 0, K, C < 1.f, !a.greedy);
   a.u_draft = u_draft;
   a.d_out = d_out;
   a.qd_out = qd_out;
@@ -1739,8 +1713,8 @@ ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, i
   if ((K > 0 && (!d || !u_acc)) || !u_bonus || !accept_len || !out_tokens || !bonus || !status)
     return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(target, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
-  set_slots(a, K + 1, K, C < 1.f);
   a.do_verify = 1;
+  set_slots(a, K + 1, K, C < 1.f, !a.greedy);
   a.d_in = d;
   a.u_acc = u_acc;
   a.u_bonus = u_bonus;
@@ -1765,8 +1739,8 @@ ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq
   if (B == 0) return SSD_OK;
   if (!guess || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(draft, draft, seq_stride, row_stride, B, K, V, F, 1.f, T, L, ws, status);
-  set_slots(a, 0, K + 1, true);
   a.do_predict = 1;
+  set_slots(a, 0, K + 1, true, false);
   a.guess = guess;
   a.guess_q = guess_q;
   return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
@@ -1834,7 +1808,7 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
   a.do_verify = 1;
   a.do_predict = guess != nullptr;
   a.do_lookup = guess != nullptr;
-  set_slots(a, K + 1, a.do_predict ? K + 1 : K, a.do_predict || C < 1.f);
+  set_slots(a, K + 1, a.do_predict ? K + 1 : K, a.do_predict || C < 1.f, !a.greedy);
   a.u_draft = u_draft;
   a.u_acc = u_acc;
   a.u_bonus = u_bonus;
