@@ -577,6 +577,38 @@ def profiled_traffic(kernel, workload):
         return None
 
 
+def probe(which):
+    """A few calls of one workload and nothing else, for a profiler to capture
+    (e.g. ncu -k regex:k_stats -s 2 -c 1 python bench.py --probe round)."""
+    import torch
+    from speculative_decoding_vocab_gb300 import build
+    build.build()
+    from speculative_decoding_vocab_gb300 import binding as ssd
+    from speculative_decoding_vocab_gb300 import workloads as w
+    device = torch.device("cuda", 0)
+    if which == "round":
+        spec = round_spec()
+        inp = w.make_round(spec, seed=0)
+        buf = RoundBuffers(spec, inp, device)
+        out = make_outputs(spec, device)
+        ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
+        for _ in range(3):
+            run_round(ssd, spec, buf, out, ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"probe": which, "workload": spec.name, "status": int(out["status"].item())}))
+        return
+    spec = w.draft_branch_attention() if which == "attn-draft" else w.verify_attention_at_scale()
+    q, kc, vc, table, prefix, parent, N, Nq = device_attention_inputs(spec, device, 7)
+    out = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    wsn = ssd.ssd_attention_workspace_size(spec.B, Nq, spec.Hq, spec.Hkv, spec.d, spec.L)
+    aws = torch.empty(max(wsn, 256), dtype=torch.uint8, device=device)
+    for _ in range(3):
+        ssd.ssd_branch_attention(q, kc, vc, table, prefix, parent, out, status=st, ws=aws)
+    torch.cuda.synchronize()
+    print(json.dumps({"probe": which, "workload": spec.name, "status": int(st.item())}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,7 +619,12 @@ def main(argv=None):
     ap.add_argument("--ref-seqs", type=int, default=2)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e / attention / other rounds")
+    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify"),
+                    help="only run a few calls of one workload (for profilers) and exit")
     args = ap.parse_args(argv)
+    if args.probe:
+        probe(args.probe)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

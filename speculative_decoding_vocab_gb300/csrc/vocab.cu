@@ -56,7 +56,6 @@ constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
 constexpr int kMaxChunks = 128;  // per row: 4 lists per lane in the warp merge
-constexpr int kWarpF = 32;       // top-F sizes with per-warp thresholds (larger F: CTA-wide)
 constexpr int kRankMax = 1024;   // lists merged by rank selection up to this many keys
 constexpr int kNone = 0x7fffffff;
 
@@ -196,7 +195,6 @@ struct Smem {
   int flag, ncand;
   float wm[kWarps], ws[kWarps];
   int wa[kWarps];
-  uint32_t tau[kWarps];
   uint64_t redk[kWarps];
   float scal[8];
   int ival[8];
@@ -411,59 +409,66 @@ struct ChunkView {
   }
 };
 
+// The chunk's exact top-F into sh.cand (one winner per sweep; used when ties at
+// the threshold overflow the candidate buffer).  Every thread calls.
+template <class E>
+__device__ __noinline__ void collect_exact(const ChunkView<E> &cv, int F, Smem &sh) {
+  const int tid = threadIdx.x;
+  uint64_t prev = ~0ull;
+  for (int r = 0; r < F; ++r) {
+    uint64_t best = 0;
+#pragma unroll 1
+    for (int j = 0; j < kRounds; ++j) {
+      const int v = tid + j * kThreads;
+      if (cv.has(v)) {
+        float f[E::kVec];
+        cv.get(v, f);
+#pragma unroll
+        for (int e = 0; e < E::kVec; ++e) {
+          const uint64_t key = (v * E::kVec + e < cv.n) ? cand_key(f[e], cv.e0 + v * E::kVec + e) : 0ull;
+          if (key < prev && key > best) best = key;
+        }
+      }
+    }
+    best = block_max_u64<kThreads>(best, sh.redk);
+    if (tid == 0) sh.cand[r] = best;
+    prev = best;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int k = 0;
+    while (k < F && sh.cand[k] != 0ull) ++k;
+    sh.ncand = k;
+  }
+  __syncthreads();
+}
+
 // Candidates for the top-F: every element whose key reaches tau goes to
-// sh.cand (count sh.ncand); past kCandCap (ties at tau), the chunk's exact
-// top-F instead.  `mine`: this thread may hold candidates.  Every thread calls.
+// sh.cand (count sh.ncand, zeroed before the call); past kCandCap (ties at
+// tau), the chunk's exact top-F instead.  `mine`: this thread may hold
+// candidates.  Every thread calls.
 template <class E>
 SSD_DEV void collect(const ChunkView<E> &cv, bool mine, uint32_t tau, int F, Smem &sh) {
   const int tid = threadIdx.x;
-  if (tid == 0) sh.ncand = 0;
-  __syncthreads();
+  if (mine) {
+#pragma unroll 1
+    for (int j = 0; j < kRounds; ++j) {
+      const int v = tid + j * kThreads;
+      if (!cv.has(v)) break;
+      if (f2ord(cv.vmax(v)) >= tau) {
+        float f[E::kVec];
+        cv.get(v, f);
 #pragma unroll
-  for (int j = 0; j < kRounds; ++j) {
-    const int v = tid + j * kThreads;
-    if (mine && cv.has(v) && f2ord(cv.vmax(v)) >= tau) {
-      float f[E::kVec];
-      cv.get(v, f);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e)
-        if (v * E::kVec + e < cv.n && f2ord(f[e]) >= tau) {
-          const int p = atomicAdd(&sh.ncand, 1);
-          if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
-        }
-    }
-  }
-  __syncthreads();
-  if (sh.ncand > kCandCap) {
-    // too many ties at the threshold: exact selection, one winner per sweep
-    uint64_t prev = ~0ull;
-    for (int r = 0; r < F; ++r) {
-      uint64_t best = 0;
-#pragma unroll
-      for (int j = 0; j < kRounds; ++j) {
-        const int v = tid + j * kThreads;
-        if (cv.has(v)) {
-          float f[E::kVec];
-          cv.get(v, f);
-#pragma unroll
-          for (int e = 0; e < E::kVec; ++e) {
-            const uint64_t key = (v * E::kVec + e < cv.n) ? cand_key(f[e], cv.e0 + v * E::kVec + e) : 0ull;
-            if (key < prev && key > best) best = key;
+        for (int e = 0; e < E::kVec; ++e)
+          if (v * E::kVec + e < cv.n && f2ord(f[e]) >= tau) {
+            const int p = atomicAdd(&sh.ncand, 1);
+            if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
           }
-        }
       }
-      best = block_max_u64<kThreads>(best, sh.redk);
-      if (tid == 0) sh.cand[r] = best;
-      prev = best;
     }
-    __syncthreads();
-    if (tid == 0) {
-      int k = 0;
-      while (k < F && sh.cand[k] != 0ull) ++k;
-      sh.ncand = k;
-    }
-    __syncthreads();
   }
+  __syncthreads();
+  if (sh.ncand > kCandCap) collect_exact<E>(cv, F, sh);
 }
 
 // Top-F of n distinct nonzero keys by rank (the key with r larger keys goes
@@ -474,7 +479,7 @@ SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
   for (int i = threadIdx.x; i < n; i += kThreads) {
     const uint64_t k = keys[i];
     int rank = 0;
-    for (int j = 0; j < n; ++j) rank += (keys[j] > k) ? 1 : 0;
+    for (int j = 0; j < n && rank < F; ++j) rank += (keys[j] > k) ? 1 : 0;
     if (rank < F) dst[rank] = k;
   }
 }
@@ -614,25 +619,13 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
   uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
   if (F > 1) {
     const uint32_t mykey = cv.has(tid) ? f2ord(m1) : 0u;
+    // tau: the F-th largest thread maximum (CTA-wide radix select on the
+    // order-preserving keys); the chunk's top-F all reach it, and typically
+    // little more than F elements do
     uint32_t tau = 0;
-    if (F <= kWarpF) {
-      // per warp: the F-th largest lane maximum (ballot radix select); the
-      // chunk's top-F all reach the largest of the warps' thresholds
-      for (int bit = 31; bit >= E::kLowBit; --bit) {
-        const uint32_t t = tau | (1u << bit);
-        if (__popc(__ballot_sync(0xffffffffu, mykey >= t)) >= F) tau = t;
-      }
-      if (lane == 0) sh.tau[warp] = tau;
-      __syncthreads();
-      tau = sh.tau[0];
-#pragma unroll
-      for (int w = 1; w < kWarps; ++w) tau = max(tau, sh.tau[w]);
-    } else {
-      // CTA-wide: the F-th largest thread maximum
-      for (int bit = 31; bit >= E::kLowBit; --bit) {
-        const uint32_t t = tau | (1u << bit);
-        if (__syncthreads_count(mykey >= t) >= F) tau = t;
-      }
+    for (int bit = 31; bit >= E::kLowBit; --bit) {
+      const uint32_t t = tau | (1u << bit);
+      if (__syncthreads_count(mykey >= t) >= F) tau = t;
     }
     collect<E>(cv, cv.has(tid) && mykey >= tau, tau, F, sh);
     rank_select(sh.cand, sh.ncand, F, out);
@@ -1177,6 +1170,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ V
     const int e0 = c * a.chunk_elems;
     const int n = min(a.chunk_elems, a.V - e0);
     const uint32_t bulk = static_cast<uint32_t>((n * E::kSize) & ~15);
+    sh.ncand = 0;
     mbar_init(&sh.bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&sh.bar, bulk);
