@@ -34,8 +34,8 @@
  *           row r holds position j = r + 1.  dtype fp32 or bf16.  The base
  *           address and both strides (in bytes) must be multiples of 16;
  *           V may be any positive size.  Supported: 0 <= K <= 16,
- *           0 <= F_k <= min(V, 256), 1 <= V, and a per-row candidate budget
- *           (ceil(V*elem / 32 KiB) * max F_k <= 8192).
+ *           0 <= F_k <= min(V, 256), 1 <= V, and rows of at most 128
+ *           chunks of 32 KiB (V*elem <= 4 MiB: V <= 2^21 in bf16).
  * Temperature T >= 0; T = 0 is the greedy limit (one-hot distributions at the
  *           argmax, lowest index on ties).  Saguaro's C must lie in (0, 1].
  * Uniforms  are inputs (the caller draws them, e.g. from a counter-based

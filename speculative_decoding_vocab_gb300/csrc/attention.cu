@@ -88,6 +88,29 @@ SSD_DEV void tmem_ld32(uint32_t taddr, float *v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// The same load without its wait: both halves of a 64-column row are issued
+// before tmem_wait32 (which orders every use of the registers after the wait).
+SSD_DEV void tmem_ld32_async(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+SSD_DEV void tmem_wait32(uint32_t *r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
 SSD_DEV void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -222,6 +245,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
   __shared__ __align__(8) uint64_t s_full[MT][2], s_free[MT][2], p_full[MT][2], pv_done[MT][2];
   __shared__ uint32_t tmem_base;
   __shared__ uint32_t anc[kMaxNodes][kMaxNodes / 32];
+  __shared__ int par[kMaxNodes];
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -242,13 +266,17 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int m = 0; m < MT; ++m)
+    for (int m = 0; m < MT; ++m) {
+      // softmax warps of row tile m that hold a valid row (the others sit out)
+      const int rows_m = a.nrows - (mg * MT + m) * kRows;
+      const int nact = rows_m <= 0 ? 1 : min(4, (min(rows_m, kRows) + 31) / 32);
       for (int u = 0; u < 2; ++u) {
         mbar_init(&s_full[m][u], 1);
-        mbar_init(&s_free[m][u], 4);
-        mbar_init(&p_full[m][u], 4);
+        mbar_init(&s_free[m][u], nact);
+        mbar_init(&p_full[m][u], nact);
         mbar_init(&pv_done[m][u], 1);
       }
+    }
     fence_mbar_init();
     s_abort = 0;
   }
@@ -256,14 +284,17 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
     tmem_alloc(&tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // ancestor-or-self masks of the tree nodes
+  // the tree's parent indices (one coalesced load), then the ancestor-or-self
+  // masks walked in shared memory
+  for (int m = tid; m < N; m += CF::kThreads) par[m] = a.parent[static_cast<int64_t>(b) * N + m];
+  __syncthreads();
   for (int m = tid; m < N; m += CF::kThreads) {
     uint32_t bits[kMaxNodes / 32] = {0, 0, 0, 0};
     int x = m;
     bool bad = false;
     while (x >= 0) {
       bits[x >> 5] |= 1u << (x & 31);
-      const int px = a.parent[static_cast<int64_t>(b) * N + x];
+      const int px = par[x];
       if (px < -1 || px >= x) {
         bad = true;
         break;
@@ -298,6 +329,16 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
   const bool row_valid = softmax_thread && m_own < mt_here && row < a.nrows;
   const int qi = row_valid ? row / a.group : 0;
   const int head = hk * a.group + (row_valid ? row % a.group : 0);
+  // a softmax warp without a valid row sits the loop out; its P rows stay zero
+  const bool warp_active = __any_sync(0xffffffffu, row_valid);
+  if (softmax_thread && !warp_active) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<uint4 *>(smem + CF::kP + (m_own * 2 + u) * CF::kPBytes + sw128(r_own, q4)) =
+            make_uint4(0, 0, 0, 0);
+  }
   if (softmax_thread) {
     const uint16_t *qrow = a.q + ((static_cast<int64_t>(b) * a.Nq + qi) * a.Hq + head) * D;
     uint8_t *qt = smem + CF::kQ + m_own * CF::kQBytes;
@@ -320,7 +361,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
     if (lane == 0) {
       for (int i = 0; i < nt && !s_abort; ++i) {
         const int st = i % NS;
-        if (i >= NS && !mbar_wait(&kv_empty[st], ((i / NS) - 1) & 1)) {
+        if (i >= NS && !mbar_wait_sleep(&kv_empty[st], ((i / NS) - 1) & 1)) {
           s_abort = 1;
           break;
         }
@@ -349,7 +390,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
         const int st = u % NS;
         const uint32_t v_base = smem_u32(smem + CF::kKV + st * 2 * CF::kKVBytes + CF::kKVBytes);
         for (int m = 0; m < mt_here; ++m) {
-          if (!mbar_wait(&p_full[m][u & 1], (u >> 1) & 1)) {
+          if (!mbar_wait_sleep(&p_full[m][u & 1], (u >> 1) & 1)) {
             s_abort = 1;
             return;
           }
@@ -369,14 +410,14 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
       };
       for (int i = 0; i < nt && !s_abort; ++i) {
         const int st = i % NS;
-        if (!mbar_wait(&kv_full[st], (i / NS) & 1)) {
+        if (!mbar_wait_sleep(&kv_full[st], (i / NS) & 1)) {
           s_abort = 1;
           break;
         }
         tc_fence_after();
         const uint32_t k_base = smem_u32(smem + CF::kKV + st * 2 * CF::kKVBytes);
         for (int m = 0; m < mt_here; ++m) {
-          if (i >= 2 && !mbar_wait(&s_free[m][i & 1], ((i - 2) >> 1) & 1)) {
+          if (i >= 2 && !mbar_wait_sleep(&s_free[m][i & 1], ((i - 2) >> 1) & 1)) {
             s_abort = 1;
             break;
           }
@@ -397,11 +438,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
       }
       if (nt >= 1 && !s_abort) issue_pv(nt - 1);
     }
-  } else if (m_own < mt_here) {
+  } else if (m_own < mt_here && warp_active) {
     // ---------------- softmax: one thread per row of row tile m_own
     const int m = m_own;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const bool warp_valid = __any_sync(0xffffffffu, row_valid);
     uint32_t my_anc[kMaxNodes / 32] = {0, 0, 0, 0};
     if (row_valid) {
       const int node = N - a.Nq + qi;
@@ -413,15 +453,20 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
     uint64_t l2 = pack2(0.f, 0.f), lx2 = pack2(0.f, 0.f);  // sums of the bf16 P (normalises O) and exact (lse)
     for (int i = 0; i < nt; ++i) {
       const int t = t_begin + i, u = i & 1;
-      if (!__all_sync(0xffffffffu, !s_abort && mbar_wait(&s_full[m][u], (i >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, !s_abort && mbar_wait_sleep(&s_full[m][u], (i >> 1) & 1))) {
         s_abort = 1;
         break;
       }
       tc_fence_after();
       float s[kKeys];
-      if (warp_valid) {
-        tmem_ld32(tmem + (m * 2 + u) * kKeys + lane_off, s);
-        tmem_ld32(tmem + (m * 2 + u) * kKeys + 32 + lane_off, s + 32);
+      {
+        uint32_t rs[kKeys];
+        tmem_ld32_async(tmem + (m * 2 + u) * kKeys + lane_off, rs);
+        tmem_ld32_async(tmem + (m * 2 + u) * kKeys + 32 + lane_off, rs + 32);
+        tmem_wait32(rs);
+        tmem_wait32(rs + 32);
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) s[j] = __uint_as_float(rs[j]);
       }
       tc_fence_before();
       __syncwarp();
@@ -444,23 +489,23 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
         const uint64_t inr = (nkeys - kbase >= kKeys) ? ~0ull : ((1ull << (nkeys - kbase)) - 1ull);
         vis = (pre | tree) & pg & inr;
       }
-      if (!row_valid) vis = 0;
-      // masked tile maximum (scores scaled to log2 units)
-      float tmax = NEG_INF;
-      if (warp_valid) {
-        if (full && row_valid) {
+      if (!full) {  // hidden keys score -inf (their P is then 0)
 #pragma unroll
-          for (int j = 0; j < kKeys; ++j) tmax = fmaxf(tmax, s[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kKeys; ++j)
-            if ((vis >> j) & 1ull) tmax = fmaxf(tmax, s[j]);
-        }
-        tmax = (tmax == NEG_INF) ? NEG_INF : __fmul_rn(tmax, c);
+        for (int j = 0; j < kKeys; ++j) s[j] = ((vis >> j) & 1ull) ? s[j] : NEG_INF;
       }
+      // tile maximum (a tree), scaled to log2 units
+      float t2[kKeys / 2];
+#pragma unroll
+      for (int j = 0; j < kKeys / 2; ++j) t2[j] = fmaxf(s[2 * j], s[2 * j + 1]);
+#pragma unroll
+      for (int w = kKeys / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t2[j] = fmaxf(t2[j], t2[j + w]);
+      float tmax = row_valid ? t2[0] : NEG_INF;
+      tmax = (tmax == NEG_INF) ? NEG_INF : __fmul_rn(tmax, c);
       const bool grow = tmax != NEG_INF && (m_used == NEG_INF || tmax > m_used + 8.f);
       // P buffer u is free once P V of tile i - 2 completed
-      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[m][u], ((i - 2) >> 1) & 1))) {
+      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[m][u], ((i - 2) >> 1) & 1))) {
         s_abort = 1;
         break;
       }
@@ -495,6 +540,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
       uint8_t *prow = smem + CF::kP + (m * 2 + u) * CF::kPBytes;
       const uint64_t c2 = pack2(c, c), nm2 = pack2(-m_used, -m_used);
       const bool any = row_valid && m_used != NEG_INF;
+      uint64_t la[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)}, lxa[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4) {
         uint32_t pk[4];
@@ -505,16 +551,18 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
           if (any) {
             float x0, x1;
             unpack2(fma2(pack2(s[j], s[j + 1]), c2, nm2), x0, x1);
-            p0 = ((vis >> j) & 1ull) ? ex2(x0) : 0.f;
-            p1 = ((vis >> (j + 1)) & 1ull) ? ex2(x1) : 0.f;
+            p0 = ex2(x0);
+            p1 = ex2(x1);
           }
           const uint32_t pb = cvt_bf16x2(p0, p1);
-          lx2 = add2(lx2, pack2(p0, p1));
-          l2 = add2(l2, pack2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
+          lxa[h & 1] = add2(lxa[h & 1], pack2(p0, p1));
+          la[h & 1] = add2(la[h & 1], pack2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
           pk[h] = pb;
         }
         *reinterpret_cast<uint4 *>(prow + sw128(r_own, q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      l2 = add2(l2, add2(la[0], la[1]));
+      lx2 = add2(lx2, add2(lxa[0], lxa[1]));
       fence_proxy_async();  // P (generic writes) -> visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive1(&p_full[m][u]);
@@ -687,15 +735,18 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   const int ntiles = (max_keys + kKeys - 1) / kKeys;
   const long base = static_cast<long>(B) * Hkv * p.mgroups;
   const long slots = attn_num_sms();
+  // estimated time in tile-steps: whole waves x (tiles per split + a CTA's
+  // set-up, about kSetupTiles tiles: masks, Q, TMEM, the first copies)
+  constexpr double kSetupTiles = 4.0;
   int best = 1;
-  double best_eff = 0.0;
+  double best_cost = 0.0;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && ntiles / s < 4) break;
     const long ctas = base * s;
-    const double waves = static_cast<double>(ctas) / slots;
-    const double eff = waves / std::ceil(waves);
-    if (eff > best_eff + 0.03) {
-      best_eff = eff;
+    const double waves = std::ceil(static_cast<double>(ctas) / slots);
+    const double cost = waves * (std::ceil(static_cast<double>(ntiles) / s) + kSetupTiles);
+    if (s == 1 || cost < best_cost * 0.97) {
+      best_cost = cost;
       best = s;
     }
   }

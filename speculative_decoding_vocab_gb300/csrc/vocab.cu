@@ -46,6 +46,7 @@
 namespace ssd {
 
 constexpr int kThreads = 256;
+constexpr int kStatsCtas = 5;  // resident k_stats CTAs per SM
 constexpr int kWarps = kThreads / 32;
 constexpr int kRounds = 8;                             // 16-byte vectors per thread and chunk
 constexpr int kChunkBytes = kThreads * kRounds * 16;  // 32 KiB
@@ -56,7 +57,7 @@ constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
 constexpr int kMaxChunks = 128;  // per row: 4 lists per lane in the warp merge
-constexpr int kRankMax = 1024;   // lists merged by rank selection up to this many keys
+constexpr int kRankMax = 512;    // lists merged by rank selection up to this many keys
 constexpr int kNone = 0x7fffffff;
 
 struct ChunkStat {
@@ -100,6 +101,7 @@ struct VocabArgs {
   int greedy;  // T == 0
   float C;
   int npairs;  // row pairs per sequence, r = 0 .. npairs-1
+  long nst;    // chunks of the call: B * nslots * nchunks
   int do_sample, do_verify, do_predict, do_lookup;
   RowSlot slot[kMaxSlots];                   // ordered by pair: target r, then draft r
   int tsl[kMaxK + 1], dsl[kMaxK + 1];        // slot of target / draft row r (-1: none)
@@ -191,7 +193,7 @@ SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
 // shared memory of a CTA (k_stats: after the staged chunk)
 // ---------------------------------------------------------------------------
 struct Smem {
-  uint64_t bar;  // completion of the chunk's TMA copy
+  uint64_t bar;  // k_stats: completion of the chunk's TMA copy
   int flag, ncand;
   float wm[kWarps], ws[kWarps];
   int wa[kWarps];
@@ -199,9 +201,8 @@ struct Smem {
   float scal[8];
   int ival[8];
   RowInfo ri;
-  uint64_t cand[kCandCap];
-  ChunkStat cs[2][kMaxChunks];
-  float cmass[kMaxChunks * kQuarters];
+  uint64_t cand[kCandCap];  // statistics: top-F candidates; pair merge: the chunk lists
+  float cmass[kMaxChunks];
   float bw[kBlocks];
   uint64_t S[kMaxF];
   float cp[kMaxK], cq[kMaxK], cu[kMaxK];
@@ -647,6 +648,7 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
 #pragma unroll
     for (int o = kWarps / 2; o; o >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
     if (lane == 0) {
+      sh.ncand = 0;  // for the next chunk's candidates
       if (amax == kNone) amax = 0;  // an all -inf chunk: its first index
       if (F == 1) out[0] = cand_key(M, cv.e0 + amax);
       a.stats[chunk_index(a, b, slot, c)] = ChunkStat{M, S, cv.e0 + amax, 0};
@@ -661,21 +663,47 @@ struct RowStat {
   float m, s;
   int amax;
 };
-// Chunks in index order: a strictly larger maximum keeps the lowest index.
-SSD_DEV RowStat merge_row_smem(const VocabArgs &a, const ChunkStat *cs) {
+// One warp merges the published chunk records of row `slot` of sequence b:
+// the maximum (a strictly larger maximum keeps the lower chunk, hence the
+// lowest index), and the sum rescaled to it (each lane sums its chunks in
+// order, the lanes by a fixed tree).  All 32 lanes call; all return it.
+SSD_DEV RowStat merge_row_warp(const VocabArgs &a, int b, int slot) {
+  constexpr int L = kMaxChunks / 32;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  RowStat r{cs[0].m, 0.f, cs[0].amax};
-  for (int c = 1; c < a.nchunks; ++c)
-    if (cs[c].m > r.m) {
-      r.m = cs[c].m;
-      r.amax = cs[c].amax;
-    }
-  if (!a.greedy && r.m != NEG_INF) {
-    const float mk = __fmul_rn(r.m, a.kT);
-    for (int c = 0; c < a.nchunks; ++c)
-      if (cs[c].m != NEG_INF) r.s = __fadd_rn(r.s, __fmul_rn(cs[c].s, ex2(__fsub_rn(__fmul_rn(cs[c].m, a.kT), mk))));
+  const int lane = threadIdx.x & 31;
+  ChunkStat cs[L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    const int c = lane + 32 * l;
+    cs[l] = (c < a.nchunks) ? ldcg_stat(a.stats + chunk_index(a, b, slot, c)) : ChunkStat{NEG_INF, 0.f, kNone, 0};
   }
-  return r;
+  float m = cs[0].m;
+  int am = cs[0].amax;
+#pragma unroll
+  for (int l = 1; l < L; ++l)
+    if (cs[l].m > m) {
+      m = cs[l].m;
+      am = cs[l].amax;
+    }
+  // across lanes: the larger maximum; equal maxima keep the lower index
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
+    if (m2 > m || (m2 == m && a2 < am)) {
+      m = m2;
+      am = a2;
+    }
+  }
+  float sum = 0.f;
+  if (!a.greedy && m != NEG_INF) {
+    const float mk = __fmul_rn(m, a.kT);
+#pragma unroll
+    for (int l = 0; l < L; ++l)
+      if (cs[l].m != NEG_INF) sum = __fadd_rn(sum, __fmul_rn(cs[l].s, ex2(__fsub_rn(__fmul_rn(cs[l].m, a.kT), mk))));
+    sum = warp_sum(sum);
+  }
+  return RowStat{m, sum, am == kNone ? 0 : am};
 }
 
 // Warp-cooperative k-way merge of the sorted per-chunk candidate lists (list
@@ -872,41 +900,37 @@ SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64
 // pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
 // ===========================================================================
 template <class E>
-__device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, uint8_t *buf, Smem &sh) {
-  const int tid = threadIdx.x;
-  const float NEG_INF = -__int_as_float(0x7f800000);
+__device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &sh) {
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int ts = a.tsl[r], ds = a.dsl[r];
   const int F = (ds >= 0) ? a.Fs[r] : 0;
   const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
-  // stage the chunk records of the pair and the draft's candidate lists
-  for (int c = tid; c < a.nchunks; c += kThreads) {
-    if (ts >= 0) sh.cs[0][c] = ldcg_stat(a.stats + chunk_index(a, b, ts, c));
-    if (ds >= 0) sh.cs[1][c] = ldcg_stat(a.stats + chunk_index(a, b, ds, c));
-  }
-  uint64_t *lists = reinterpret_cast<uint64_t *>(buf);
+  // the draft's candidate lists, staged for the rank selection
+  uint64_t *lists = sh.cand;
   const int nl = a.nchunks * F;
   const bool by_rank = nl <= kRankMax;
   if (F > 0 && by_rank) {
     const uint64_t *src = a.cands + chunk_index(a, b, ds, 0) * a.Fcap;
     for (int i = tid; i < nl; i += kThreads) lists[i] = ldcg_key(src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
   }
+  if (tid == 0) memset(&sh.ri, 0, sizeof(sh.ri));
   __syncthreads();
-  if (tid == 0) {
-    RowInfo ri;
-    memset(&ri, 0, sizeof(ri));
-    if (ts >= 0) {
-      const RowStat t = merge_row_smem(a, sh.cs[0]);
-      ri.mt = t.m;
-      ri.st = t.s;
-      ri.at = t.amax;
+  // warps 0 and 1 merge the target and draft rows' chunk records
+  if (warp == 0 && ts >= 0) {
+    const RowStat t = merge_row_warp(a, b, ts);
+    if (tid == 0) {
+      sh.ri.mt = t.m;
+      sh.ri.st = t.s;
+      sh.ri.at = t.amax;
     }
-    if (ds >= 0) {
-      const RowStat d = merge_row_smem(a, sh.cs[1]);
-      ri.md = d.m;
-      ri.sd = d.s;
-      ri.ad = d.amax;
+  }
+  if (warp == 1 && ds >= 0) {
+    const RowStat d = merge_row_warp(a, b, ds);
+    if ((tid & 31) == 0) {
+      sh.ri.md = d.m;
+      sh.ri.sd = d.s;
+      sh.ri.ad = d.amax;
     }
-    sh.ri = ri;
   }
   if (F > 0) {
     if (by_rank) {
@@ -921,13 +945,14 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, uint8_
       int nz = 0;
       for (int i0 = 0; i0 < nl; i0 += kThreads) nz += __syncthreads_count(i0 + tid < nl && lists[i0 + tid] != 0ull);
       for (int i = nz + tid; i < F; i += kThreads) sh.S[i] = 0ull;
-    } else if (tid < 32) {
+    } else if (warp == 2) {
       merge_topf(a.cands + chunk_index(a, b, ds, 0) * a.Fcap, a.Fcap, a.nchunks, F, sh.S);
     }
   }
   __syncthreads();
   if (a.do_verify || a.do_lookup)
     for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
+  const float NEG_INF = -__int_as_float(0x7f800000);
   const float mdk = __fmul_rn(sh.ri.md, a.kT);
   if (tid == 0) {
     float sq = 0.f;
@@ -970,10 +995,7 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, uint8_
           d = exact_draw<E, false, true>(a, nullptr, rowD, u, wf, sh);
         } else {
           // chunk masses of q' (unnormalised): s_c 2^(Mk_c - mdk) - (1 - C) sum_{i in S, in c} e_i
-          for (int c = tid; c < a.nchunks; c += kThreads) {
-            const ChunkStat cs = sh.cs[1][c];
-            sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), mdk)));
-          }
+          chunk_masses(a, b, ds, mdk, sh);
           __syncthreads();
           if (tid == 0 && a.C < 1.f) {
             for (int i = 0; i < F; ++i) {
@@ -1036,10 +1058,10 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, uint8_
 // ===========================================================================
 // Stage in shared memory, in one round of loads, what the final steps of
 // sequence b need whatever the accept count: draft tokens, p(d), q'(d), the
-// uniforms, every row's merged statistics and S threshold key and (with_res)
-// the residual unit masses.  Then the acceptance chain (thread 0).  Every
+// uniforms, every row's merged statistics and S threshold key and (umass
+// given) the residual unit masses.  Then the acceptance chain (thread 0).  Every
 // thread returns the accept count.
-SSD_DEV int stage_chain(const VocabArgs &a, int b, bool with_res, Smem &sh) {
+SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, Smem &sh) {
   const int tid = threadIdx.x;
   for (int t = tid; t < a.K; t += kThreads) {
     const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + t);
@@ -1054,9 +1076,9 @@ SSD_DEV int stage_chain(const VocabArgs &a, int b, bool with_res, Smem &sh) {
     const int F = a.Fs[r];
     sh.keyF[r] = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
   }
-  if (with_res) {
+  if (umass) {
     const int nu = a.nchunks * kQuarters;
-    for (int q = tid; q < nu; q += kThreads) sh.cmass[q] = __ldcg(a.rmass + static_cast<size_t>(b) * nu + q);
+    for (int q = tid; q < nu; q += kThreads) umass[q] = __ldcg(a.rmass + static_cast<size_t>(b) * nu + q);
   }
   __syncthreads();
   if (tid == 0) {
@@ -1113,7 +1135,7 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
 // accepted) the bonus draw and the outputs; a residual draw is left to k_resid.
 template <class E>
 __device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Smem &sh) {
-  const int acc = stage_chain(a, b, false, sh);
+  const int acc = stage_chain(a, b, nullptr, sh);
   if (!a.greedy && acc < a.K) {
     if (threadIdx.x == 0) a.accs[b] = acc;
     return;
@@ -1149,7 +1171,7 @@ SSD_DEV void trace_entry(unsigned long long *tr, int kind, int b, int idx, const
 // the kernels
 // ===========================================================================
 template <class E>
-__global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ VocabArgs a) {
+__global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_constant__ VocabArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t *buf = smem_raw;
   Smem &sh = *reinterpret_cast<Smem *>(smem_raw + kChunkBytes);
@@ -1190,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ V
   mark(a, sh.mk, 2);
   if (last_of_pair) {
     kind = 1;
-    row_finish<E>(a, b, r, buf, sh);
+    row_finish<E>(a, b, r, sh);
     mark(a, sh.mk, 4);
     if (a.do_verify && arrive_last(seq_ctr(a, b), static_cast<uint32_t>(a.npairs), sh)) {
       kind = 3;
@@ -1208,6 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ V
 template <class E>
 __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ VocabArgs a) {
   __shared__ Smem sh;
+  __shared__ float umass[kMaxChunks * kQuarters];  // the sequence's unit masses (final draw)
   // everything k_stats wrote is visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1250,12 +1273,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ V
   if (arrive_last(res_ctr(a, b), static_cast<uint32_t>(nu), sh)) {
     kind = 3;
     mark(a, sh.mk, 3);
-    const int acc2 = stage_chain(a, b, true, sh);  // the same chain: acc2 == acc
+    const int acc2 = stage_chain(a, b, umass, sh);  // the same chain: acc2 == acc
     const RowInfo ra = sh.rows[acc2];
     const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
     const float ub = a.u_bonus[b];
     if (tid == 0) {
-      locate(sh.cmass, nu, ub, false, sh);
+      locate(umass, nu, ub, false, sh);
       const int uq = sh.ival[0];
       sh.ival[6] = uq;
       sh.scal[6] = sh.scal[2];  // the residual's total mass
@@ -1508,6 +1531,7 @@ void *g_trace = nullptr;
 size_t g_trace_bytes = 0;
 
 constexpr size_t kStatsSmem = kChunkBytes + sizeof(Smem);
+static_assert(kStatsCtas * (kStatsSmem + 1024) <= 228 * 1024, "shared memory of k_stats too large for its CTAs/SM");
 
 ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
@@ -1531,6 +1555,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   const long n2 = (a.do_verify && !a.greedy && a.K > 0) ? static_cast<long>(a.B) * a.nchunks * kQuarters : 0;
   if (n1 < 1) return cudaSuccess;
   if (n1 > 0x7fffffffL) return cudaErrorInvalidValue;
+  a.nst = n1;
   a.trace = (g_trace && g_trace_bytes >= static_cast<size_t>(n1 + n2) * 64)
                 ? static_cast<unsigned long long *>(g_trace)
                 : nullptr;
