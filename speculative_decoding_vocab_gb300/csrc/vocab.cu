@@ -27,11 +27,14 @@
 //            acceptance chain and, unless a residual draw is needed, the bonus
 //            draw and the outputs.  No CTA ever waits for another: the last to
 //            arrive does the work.
+//            The merges stage the records they read in shared memory (over
+//            the chunk buffer) with one round of loads.
 //   k_resid  (verification at T > 0) one CTA per quarter chunk of each
 //            sequence's rejected row pair: residual block sums; the last CTA of
 //            a sequence draws the bonus token from them and writes the
-//            outputs.  It is a programmatic dependent launch of k_stats, so its
-//            launch overlaps k_stats' last wave.
+//            outputs.  It is a programmatic dependent launch of k_stats: its
+//            CTAs start once every k_stats CTA has started and each waits only
+//            for its own sequence's acceptance chain (a ready word).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -111,7 +114,9 @@ struct VocabArgs {
   int foff[kMaxK + 2];
   // workspace
   uint32_t *ctr;  // [0] finished sequences, [1] hits, [2+b] pairs done, [2+B+b] residual
-                  // units done, [2+2B + b(K+1) + r] chunks done of pair (b, r)
+                  // units done, [2+2B + b(K+1) + r] chunks done of pair (b, r), then
+                  // per sequence b its ready word (accs[b] published), then the
+                  // residual CTAs that have exited
   ChunkStat *stats;  // [B][nslots][nchunks]
   BlockRec *blk;     // [B][nslots][nchunks]
   uint64_t *cands;   // [B][nslots][nchunks][Fcap]
@@ -142,6 +147,13 @@ SSD_DEV uint32_t *res_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + a.B + 
 SSD_DEV uint32_t *pair_ctr(const VocabArgs &a, int b, int r) {
   return a.ctr + 2 + 2 * a.B + static_cast<size_t>(b) * (a.K + 1) + r;
 }
+SSD_DEV uint32_t *ready_word(const VocabArgs &a, int b) {
+  return a.ctr + 2 + 2 * a.B + static_cast<size_t>(a.B) * (a.K + 1) + b;
+}
+SSD_DEV uint32_t *resid_exit_ctr(const VocabArgs &a) {
+  return a.ctr + 2 + 3 * a.B + static_cast<size_t>(a.B) * (a.K + 1);
+}
+__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 3 + 3 * B + B * (K + 1); }
 
 __host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
   return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
@@ -170,15 +182,22 @@ SSD_DEV PosInfo ldcg_pos(const PosInfo *p) {
 }
 SSD_DEV uint64_t ldcg_key(const uint64_t *p) { return __ldcg(reinterpret_cast<const unsigned long long *>(p)); }
 
-SSD_DEV uint32_t ld_acquire(const uint32_t *p) {
+// Arrivals and polls are release / relaxed; only the CTA that goes on to read
+// what others published pays for the acquire (a fence), since an acquire
+// invalidates the SM's L1, where the other resident CTAs keep their spills.
+SSD_DEV uint32_t ld_relaxed(const uint32_t *p) {
   uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-SSD_DEV uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+SSD_DEV void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+SSD_DEV uint32_t atom_add_release(uint32_t *p, uint32_t v) {
   uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+SSD_DEV void st_release(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Trace mark k of this CTA (ssd_set_trace): %globaltimer by thread 0.
 SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
@@ -212,6 +231,19 @@ struct Smem {
   unsigned long long mk[7];  // trace marks (thread 0)
 };
 
+// What a merge reads of other CTAs' records, staged in shared memory by one
+// round of loads (k_stats: laid over the chunk buffer once the chunk's own
+// statistics are published).
+constexpr int kStageChunks = 64;  // block records staged up to this many chunks per row
+constexpr int kPayStage = 1024;   // payload words staged
+struct Stage {
+  ChunkStat cs[2][kMaxChunks];  // chunk records: target row, draft row
+  BlockRec blk[kStageChunks];   // block records of the row drawn from
+  float z[32 * 8];              // the other row's values of the block a draw located
+  int32_t pay[kPayStage];       // the sequence's cache payload
+};
+static_assert(sizeof(Stage) <= kChunkBytes, "the merge stage must fit the chunk buffer");
+
 // Every thread calls after writing its part of a published result.  True, in
 // every thread of the CTA, for the arrival that completes `total` arrivals on
 // *ctr; the results published before the earlier arrivals are then visible
@@ -219,7 +251,11 @@ struct Smem {
 // the barrier).
 SSD_DEV bool arrive_last(uint32_t *ctr, uint32_t total, Smem &sh) {
   __syncthreads();
-  if (threadIdx.x == 0) sh.flag = (atom_add_acq_rel(ctr, 1u) + 1 == total) ? 1 : 0;
+  if (threadIdx.x == 0) {
+    const bool last = atom_add_release(ctr, 1u) + 1 == total;
+    if (last) fence_acq_rel();
+    sh.flag = last ? 1 : 0;
+  }
   __syncthreads();
   return sh.flag != 0;
 }
@@ -336,39 +372,72 @@ SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, in
   return best;
 }
 
-// Thread 0: the first of n masses (summed in order) whose cumulative sum
-// exceeds the target (u * total, or u itself when u_is_target), with positive
-// mass; rounding past the end takes the last positive one.  sh.ival[0] = its
-// index (-1 when the total is 0), sh.scal[1] = the target minus the mass
-// before it, sh.scal[2] = the total.  The caller synchronises.
+// Cumulative masses, one warp: lane l sums its run of `per` consecutive
+// masses in order, the runs are combined by a Hillis-Steele inclusive scan.
+// Returns the lane's exclusive prefix; *W = the total (every lane).
+SSD_DEV float warp_runs(const float *mass, int n, int per, float *W) {
+  const int lane = threadIdx.x & 31;
+  float run = 0.f;
+  for (int k = 0, i = lane * per; k < per && i < n; ++k, ++i) run = __fadd_rn(run, mass[i]);
+  const float incl = warp_incl_scan(run);
+  *W = __shfl_sync(0xffffffffu, incl, 31);
+  const float ex = __shfl_up_sync(0xffffffffu, incl, 1);
+  return lane == 0 ? 0.f : ex;
+}
+// The total of n masses with the arithmetic of warp_runs (one warp; every
+// lane returns it).
+SSD_DEV float warp_total(const float *mass, int n) {
+  float W;
+  (void)warp_runs(mass, n, (n + 31) / 32, &W);
+  return W;
+}
+
+// One warp: the first of n masses whose cumulative sum (warp_runs) exceeds
+// the target (u * total, or u itself when u_is_target), with positive mass;
+// rounding past the end takes the last positive one.  Lane 0 sets
+// sh.ival[0] = its index (-1 when the total is 0), sh.scal[1] = the target
+// minus the mass before it, sh.scal[2] = the total.  The caller synchronises.
 SSD_DEV void locate(const float *mass, int n, float u, bool u_is_target, Smem &sh) {
-  float W = 0.f;
-  for (int c = 0; c < n; ++c) W = __fadd_rn(W, mass[c]);
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) / 32;
+  float W;
+  float cum = warp_runs(mass, n, per, &W);
   const float target = u_is_target ? u : __fmul_rn(u, W);
-  int cs = -1;
-  float before = 0.f, cum = 0.f;
-  for (int c = 0; c < n; ++c) {
-    const float nc = __fadd_rn(cum, mass[c]);
-    if (nc > target && mass[c] > 0.f) {
-      cs = c;
-      before = cum;
-      break;
+  int hit = -1, lpos = -1;
+  float hb = 0.f, lb = 0.f;
+  for (int k = 0, i = lane * per; k < per && i < n; ++k, ++i) {
+    const float m = mass[i];
+    const float nc = __fadd_rn(cum, m);
+    if (m > 0.f) {
+      if (hit < 0 && nc > target) {
+        hit = i;
+        hb = cum;
+      }
+      lpos = i;
+      lb = cum;
     }
     cum = nc;
   }
-  if (cs < 0 && W > 0.f) {  // rounding left the target past the end: the last positive mass
-    float b2 = 0.f;
-    for (int c = 0; c < n; ++c) {
-      if (mass[c] > 0.f) {
-        cs = c;
-        before = b2;
-      }
-      b2 = __fadd_rn(b2, mass[c]);
+  int idx = -1;
+  float before = 0.f;
+  const uint32_t mh = __ballot_sync(0xffffffffu, hit >= 0);
+  if (mh) {
+    const int src = __ffs(mh) - 1;
+    idx = __shfl_sync(0xffffffffu, hit, src);
+    before = __shfl_sync(0xffffffffu, hb, src);
+  } else {  // rounding left the target past the end: the last positive mass
+    const uint32_t ml = __ballot_sync(0xffffffffu, lpos >= 0);
+    if (ml) {
+      const int src = 31 - __clz(ml);
+      idx = __shfl_sync(0xffffffffu, lpos, src);
+      before = __shfl_sync(0xffffffffu, lb, src);
     }
   }
-  sh.ival[0] = (W > 0.f) ? cs : -1;
-  sh.scal[1] = __fsub_rn(target, before);
-  sh.scal[2] = W;
+  if (lane == 0) {
+    sh.ival[0] = (W > 0.f) ? idx : -1;
+    sh.scal[1] = __fsub_rn(target, before);
+    sh.scal[2] = W;
+  }
 }
 
 // ===========================================================================
@@ -663,11 +732,11 @@ struct RowStat {
   float m, s;
   int amax;
 };
-// One warp merges the published chunk records of row `slot` of sequence b:
-// the maximum (a strictly larger maximum keeps the lower chunk, hence the
-// lowest index), and the sum rescaled to it (each lane sums its chunks in
-// order, the lanes by a fixed tree).  All 32 lanes call; all return it.
-SSD_DEV RowStat merge_row_warp(const VocabArgs &a, int b, int slot) {
+// One warp merges the chunk records of a row (staged in shared memory): the
+// maximum (a strictly larger maximum keeps the lower chunk, hence the lowest
+// index), and the sum rescaled to it (each lane sums its chunks in order, the
+// lanes by a fixed tree).  All 32 lanes call; all return it.
+SSD_DEV RowStat merge_row_warp(const VocabArgs &a, const ChunkStat *rec) {
   constexpr int L = kMaxChunks / 32;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int lane = threadIdx.x & 31;
@@ -675,7 +744,7 @@ SSD_DEV RowStat merge_row_warp(const VocabArgs &a, int b, int slot) {
 #pragma unroll
   for (int l = 0; l < L; ++l) {
     const int c = lane + 32 * l;
-    cs[l] = (c < a.nchunks) ? ldcg_stat(a.stats + chunk_index(a, b, slot, c)) : ChunkStat{NEG_INF, 0.f, kNone, 0};
+    cs[l] = (c < a.nchunks) ? rec[c] : ChunkStat{NEG_INF, 0.f, kNone, 0};
   }
   float m = cs[0].m;
   int am = cs[0].amax;
@@ -753,40 +822,48 @@ SSD_DEV float norm_N(float C, float sq) { return __fsub_rn(1.f, __fmul_rn(__fsub
 // ===========================================================================
 // Chunk masses of 2^(z kT - rk) (rk = fl(row max kT)) from the row's chunk
 // records, into sh.cmass.  Caller synchronises.
+SSD_DEV float chunk_mass(const ChunkStat &cs, float kT, float rk) {
+  return (cs.m == -__int_as_float(0x7f800000)) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, kT), rk)));
+}
 SSD_DEV void chunk_masses(const VocabArgs &a, int b, int slot, float rk, Smem &sh) {
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  for (int c = threadIdx.x; c < a.nchunks; c += kThreads) {
-    const ChunkStat cs = ldcg_stat(a.stats + chunk_index(a, b, slot, c));
-    sh.cmass[c] = (cs.m == NEG_INF) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, a.kT), rk)));
-  }
+  for (int c = threadIdx.x; c < a.nchunks; c += kThreads)
+    sh.cmass[c] = chunk_mass(ldcg_stat(a.stats + chunk_index(a, b, slot, c)), a.kT, rk);
 }
 
 // Draw from row `slot` of sequence b (its elements in `row`) with weights wf =
 // 2^(z kT - rk), scaled by C on the set S (the Fn keys of Slist) when C < 1.
-// sh.cmass holds the chunk masses with the down-weighting applied.  Every
-// thread calls; returns the token (-1 if the masses are all 0).
+// sh.cmass holds the chunk masses with the down-weighting applied; `sbr`, when
+// given, the row's block records staged in shared memory (else they are read
+// from global memory).  With `rowZ`, warp 1 stages the other row's values of
+// the located block in zbuf while warp 0 scans it.  Every thread calls;
+// returns the token (-1 if the masses are all 0).
 template <class E, bool HT, class WF>
 SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, float rk, float u, const WF &wf,
-                       const uint64_t *Slist, int Fn, float C, Smem &sh) {
+                       const BlockRec *sbr, const uint64_t *Slist, int Fn, float C, const char *rowZ, float *zbuf,
+                       Smem &sh) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  if (tid == 0) locate(sh.cmass, a.nchunks, u, false, sh);
+  if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
   __syncthreads();
   const int cs = sh.ival[0];
   const float local = sh.scal[1];
   if (cs < 0) return -1;
-  // block weights of chunk cs
+  // block weights of chunk cs; the elements of S in a block down-weighted in
+  // list order
   if (tid < kBlocks) {
-    const BlockRec *br = a.blk + chunk_index(a, b, slot, cs);
     const int j = tid / kWarps, w = tid % kWarps;
-    const float wmw = __ldcg(&br->wm[w]);
-    const float bs = __ldcg(&br->bs[j][w]);
-    sh.bw[tid] = (wmw == -__int_as_float(0x7f800000) || !(bs > 0.f))
-                     ? 0.f
-                     : __fmul_rn(bs, ex2(__fsub_rn(__fmul_rn(wmw, a.kT), rk)));
-  }
-  __syncthreads();
-  if (tid == 0) {
-    if (C < 1.f) {  // the set S inside this chunk: down-weight its elements
+    float wmw, bs;
+    if (sbr) {
+      wmw = sbr[cs].wm[w];
+      bs = sbr[cs].bs[j][w];
+    } else {
+      const BlockRec *br = a.blk + chunk_index(a, b, slot, cs);
+      wmw = __ldcg(&br->wm[w]);
+      bs = __ldcg(&br->bs[j][w]);
+    }
+    float x = (wmw == -__int_as_float(0x7f800000) || !(bs > 0.f))
+                  ? 0.f
+                  : __fmul_rn(bs, ex2(__fsub_rn(__fmul_rn(wmw, a.kT), rk)));
+    if (C < 1.f) {
       const int e0 = cs * a.chunk_elems;
       for (int i = 0; i < Fn; ++i) {
         const uint64_t k = Slist[i];
@@ -794,13 +871,18 @@ SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, flo
         const int idx = cand_idx(k) - e0;
         if (idx < 0 || idx >= a.chunk_elems) continue;
         const int v = idx / E::kVec;
-        const int blk = (v / kThreads) * kWarps + (v % kThreads) / 32;
+        if ((v / kThreads) * kWarps + (v % kThreads) / 32 != tid) continue;
         const float e = ex2(__fmaf_rn(cand_val(k), a.kT, -rk));
-        sh.bw[blk] = fmaxf(__fsub_rn(sh.bw[blk], __fmul_rn(__fsub_rn(1.f, C), e)), 0.f);
+        x = fmaxf(__fsub_rn(x, __fmul_rn(__fsub_rn(1.f, C), e)), 0.f);
       }
     }
+    sh.bw[tid] = x;
+  }
+  __syncthreads();
+  if (warp == 0) {
     locate(sh.bw, kBlocks, local, true, sh);
-    if (sh.ival[0] < 0) {  // no block weight (the masses rounded differently): the last block
+    __syncwarp();
+    if (tid == 0 && sh.ival[0] < 0) {  // no block weight (the masses rounded differently): the last block
       sh.ival[0] = kBlocks - 1;
       sh.scal[1] = local;
     }
@@ -809,11 +891,24 @@ SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, flo
   const int blk = sh.ival[0];
   const float local2 = sh.scal[1];
   int d = -1;
-  if (warp == 0)
+  if (warp == 0) {
     d = warp_find<E, HT, !HT>(a, HT ? row : nullptr, HT ? nullptr : row, cs, blk / kWarps, blk % kWarps, local2,
                               wf);
+  } else if (warp == 1 && rowZ) {
+    const int lane = tid & 31;
+    const int e0 = cs * a.chunk_elems;
+    const int n = min(a.chunk_elems, a.V - e0);
+    const int i0 = ((blk / kWarps) * kThreads + (blk % kWarps) * 32 + lane) * E::kVec;
+    float f[E::kVec];
+    ld_vec<E>(rowZ, e0, n, i0, 0.f, f);
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e) zbuf[lane * E::kVec + e] = f[e];
+  }
   __syncthreads();  // everyone read sh.ival / sh.scal
-  if (tid == 0) sh.ival[4] = d;
+  if (tid == 0) {
+    sh.ival[4] = d;
+    sh.ival[5] = cs * a.chunk_elems + ((blk / kWarps) * kThreads + (blk % kWarps) * 32) * E::kVec;  // zbuf[0]
+  }
   __syncthreads();
   return sh.ival[4];
 }
@@ -838,21 +933,20 @@ SSD_DEV int exact_draw(const VocabArgs &a, const char *rowT, const char *rowD, f
   };
   for (int c = 0; c < a.nchunks; ++c) {
     block_sums(c);
-    if (tid == 0) {
-      float m = 0.f;
-      for (int k = 0; k < kBlocks; ++k) m = __fadd_rn(m, sh.bw[k]);
-      sh.cmass[c] = m;
+    if (warp == 0) {
+      const float m = warp_total(sh.bw, kBlocks);
+      if (lane == 0) sh.cmass[c] = m;
     }
     __syncthreads();
   }
-  if (tid == 0) locate(sh.cmass, a.nchunks, u, false, sh);
+  if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
   __syncthreads();
   const int cs = sh.ival[0];
   const float local = sh.scal[1];
   if (cs < 0) return -1;
   __syncthreads();
   block_sums(cs);
-  if (tid == 0) locate(sh.bw, kBlocks, local, true, sh);
+  if (warp == 0) locate(sh.bw, kBlocks, local, true, sh);
   __syncthreads();
   const int blk = sh.ival[0];
   const float local2 = sh.scal[1];
@@ -865,17 +959,24 @@ SSD_DEV int exact_draw(const VocabArgs &a, const char *rowT, const char *rowD, f
 }
 
 // p_{r+1} (target row r) drawn by its statistics; the row's argmax if the
-// masses are all zero.
+// masses are all zero.  `st`: the row's chunk (and, up to kStageChunks
+// chunks, block) records staged by stage_chain (target row K only).
 template <class E>
-SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, float u, Smem &sh) {
+SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, float u, const Stage *st, Smem &sh) {
   const float mtk = __fmul_rn(row.mt, a.kT);
   const WTarget wp{mtk, a.kT};
   const char *rowT = row_ptr(a, 0, b, r, E::kSize);
   int d;
   if (a.slot[a.tsl[r]].blocks) {
-    chunk_masses(a, b, a.tsl[r], mtk, sh);
+    const BlockRec *sbr = nullptr;
+    if (st) {
+      for (int c = threadIdx.x; c < a.nchunks; c += kThreads) sh.cmass[c] = chunk_mass(st->cs[0][c], a.kT, mtk);
+      if (a.nchunks <= kStageChunks) sbr = st->blk;
+    } else {
+      chunk_masses(a, b, a.tsl[r], mtk, sh);
+    }
     __syncthreads();
-    d = stats_draw<E, true>(a, b, a.tsl[r], rowT, mtk, u, wp, nullptr, 0, 1.f, sh);
+    d = stats_draw<E, true>(a, b, a.tsl[r], rowT, mtk, u, wp, sbr, nullptr, 0, 1.f, nullptr, nullptr, sh);
   } else {
     d = exact_draw<E, true, false>(a, rowT, nullptr, u, wp, sh);
   }
@@ -900,12 +1001,20 @@ SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64
 // pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
 // ===========================================================================
 template <class E>
-__device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &sh) {
-  const int tid = threadIdx.x, warp = tid >> 5;
+__device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage &st, Smem &sh) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ts = a.tsl[r], ds = a.dsl[r];
   const int F = (ds >= 0) ? a.Fs[r] : 0;
   const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
-  // the draft's candidate lists, staged for the rank selection
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const char *rowT = row_ptr(a, 0, b, r, E::kSize);
+  const char *rowD = row_ptr(a, 1, b, r, E::kSize);
+  const bool draws = r < a.K && a.do_sample && !a.greedy && ds >= 0;
+  const bool stage_blk = draws && a.slot[ds].blocks && a.nchunks <= kStageChunks;
+  const bool given = r < a.K && !a.do_sample && a.do_verify;  // verification of tokens the caller drew
+  // one round of loads: the draft's candidate lists, both rows' chunk records,
+  // the block records of a row drawn from and (tokens given) the token with
+  // its two logits
   uint64_t *lists = sh.cand;
   const int nl = a.nchunks * F;
   const bool by_rank = nl <= kRankMax;
@@ -913,20 +1022,40 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
     const uint64_t *src = a.cands + chunk_index(a, b, ds, 0) * a.Fcap;
     for (int i = tid; i < nl; i += kThreads) lists[i] = ldcg_key(src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
   }
-  if (tid == 0) memset(&sh.ri, 0, sizeof(sh.ri));
+  for (int c = tid; c < a.nchunks; c += kThreads) {
+    if (ts >= 0) st.cs[0][c] = ldcg_stat(a.stats + chunk_index(a, b, ts, c));
+    if (ds >= 0) st.cs[1][c] = ldcg_stat(a.stats + chunk_index(a, b, ds, c));
+  }
+  if (stage_blk) {
+    constexpr int kW = static_cast<int>(sizeof(BlockRec) / 16);
+    const int4 *src = reinterpret_cast<const int4 *>(a.blk + chunk_index(a, b, ds, 0));
+    int4 *dst = reinterpret_cast<int4 *>(st.blk);
+    for (int i = tid; i < a.nchunks * kW; i += kThreads) dst[i] = __ldcg(src + i);
+  }
+  if (tid == 0) {
+    memset(&sh.ri, 0, sizeof(sh.ri));
+    if (given) {
+      const int d = a.d_in[static_cast<size_t>(b) * a.K + r];
+      sh.ival[2] = d;
+      if (d >= 0 && d < a.V && !a.greedy) {
+        sh.scal[4] = E::ld(rowT, d);
+        sh.scal[5] = E::ld(rowD, d);
+      }
+    }
+  }
   __syncthreads();
   // warps 0 and 1 merge the target and draft rows' chunk records
   if (warp == 0 && ts >= 0) {
-    const RowStat t = merge_row_warp(a, b, ts);
-    if (tid == 0) {
+    const RowStat t = merge_row_warp(a, st.cs[0]);
+    if (lane == 0) {
       sh.ri.mt = t.m;
       sh.ri.st = t.s;
       sh.ri.at = t.amax;
     }
   }
   if (warp == 1 && ds >= 0) {
-    const RowStat d = merge_row_warp(a, b, ds);
-    if ((tid & 31) == 0) {
+    const RowStat d = merge_row_warp(a, st.cs[1]);
+    if (lane == 0) {
       sh.ri.md = d.m;
       sh.ri.sd = d.s;
       sh.ri.ad = d.amax;
@@ -934,12 +1063,25 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
   }
   if (F > 0) {
     if (by_rank) {
-      // zero keys (a chunk with fewer than F elements) take no rank
+      // a key's rank: its place in its own list (sorted descending, zeros
+      // past the end) plus, per other list, the count of larger keys (binary
+      // search); zero keys (a chunk with fewer than F elements) take no rank
       for (int i = tid; i < nl; i += kThreads) {
         const uint64_t k = lists[i];
         if (k == 0ull) continue;
-        int rank = 0;
-        for (int j = 0; j < nl && rank < F; ++j) rank += (lists[j] > k) ? 1 : 0;
+        const int own = i / F;
+        int rank = i - own * F;
+        for (int c = 0; c < a.nchunks && rank < F; ++c) {
+          if (c == own) continue;
+          const uint64_t *Lc = lists + c * F;
+          int lo = 0, hi = F;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (Lc[mid] > k) lo = mid + 1;
+            else hi = mid;
+          }
+          rank += lo;
+        }
         if (rank < F) sh.S[rank] = k;
       }
       int nz = 0;
@@ -952,16 +1094,16 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
   __syncthreads();
   if (a.do_verify || a.do_lookup)
     for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
-  const float NEG_INF = -__int_as_float(0x7f800000);
   const float mdk = __fmul_rn(sh.ri.md, a.kT);
-  if (tid == 0) {
+  // the draft's normalised mass on S: lane-strided partial sums, a fixed tree
+  if (warp == 0) {
     float sq = 0.f;
     if (!a.greedy && sh.ri.md != NEG_INF) {
-      for (int i = 0; i < F; ++i)
+      for (int i = lane; i < F; i += 32)
         if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
-      sq = __fdiv_rn(sq, sh.ri.sd);
+      sq = __fdiv_rn(warp_sum(sq), sh.ri.sd);
     }
-    sh.ri.sq = sq;
+    if (lane == 0) sh.ri.sq = sq;
   }
   __syncthreads();
   const RowInfo ri = sh.ri;
@@ -980,9 +1122,10 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
     }
   }
   mark(a, sh.mk, 3);
-  const char *rowD = row_ptr(a, 1, b, r, E::kSize);
   if (r < a.K && (a.do_sample || a.do_verify)) {
     int d;
+    bool zknown = false;  // zt / zd hold the token's logits
+    float zt = 0.f, zd = 0.f;
     if (a.do_sample) {
       float qd;
       if (a.greedy) {
@@ -994,23 +1137,35 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
         if (__fmul_rn(__fsub_rn(1.f, a.C), ri.sq) > 0.875f || !a.slot[ds].blocks) {
           d = exact_draw<E, false, true>(a, nullptr, rowD, u, wf, sh);
         } else {
-          // chunk masses of q' (unnormalised): s_c 2^(Mk_c - mdk) - (1 - C) sum_{i in S, in c} e_i
-          chunk_masses(a, b, ds, mdk, sh);
-          __syncthreads();
-          if (tid == 0 && a.C < 1.f) {
-            for (int i = 0; i < F; ++i) {
-              if (!sh.S[i]) continue;
-              const int c = cand_idx(sh.S[i]) / a.chunk_elems;
-              const float e = ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk));
-              sh.cmass[c] = __fsub_rn(sh.cmass[c], __fmul_rn(__fsub_rn(1.f, a.C), e));
+          // chunk masses of q' (unnormalised): s_c 2^(Mk_c - mdk) - (1 - C) sum_{i in S, in c} e_i,
+          // the elements of S in list order
+          for (int c = tid; c < a.nchunks; c += kThreads) {
+            float m = chunk_mass(st.cs[1][c], a.kT, mdk);
+            if (a.C < 1.f) {
+              for (int i = 0; i < F; ++i) {
+                const uint64_t k = sh.S[i];
+                if (!k || cand_idx(k) / a.chunk_elems != c) continue;
+                m = __fsub_rn(m, __fmul_rn(__fsub_rn(1.f, a.C), ex2(__fmaf_rn(cand_val(k), a.kT, -mdk))));
+              }
+              m = fmaxf(m, 0.f);
             }
-            for (int c = 0; c < a.nchunks; ++c) sh.cmass[c] = fmaxf(sh.cmass[c], 0.f);
+            sh.cmass[c] = m;
           }
           __syncthreads();
-          d = stats_draw<E, false>(a, b, ds, rowD, mdk, u, wf, sh.S, F, a.C, sh);
+          d = stats_draw<E, false>(a, b, ds, rowD, mdk, u, wf, stage_blk ? st.blk : nullptr, sh.S, F, a.C,
+                                   a.do_verify ? rowT : nullptr, st.z, sh);
+          if (a.do_verify && d >= 0) {
+            const int o = d - sh.ival[5];
+            if (o >= 0 && o < 32 * E::kVec) {
+              zt = st.z[o];
+              zknown = true;
+            }
+          }
         }
         if (d < 0) d = ri.ad;
-        const float zd = E::ld(rowD, d);
+        zd = E::ld(rowD, d);
+        if (!zknown) zt = a.do_verify ? E::ld(rowT, d) : 0.f;
+        zknown = true;
         const bool ins = F > 0 && cand_key(zd, d) >= keyF;
         const float q = __fdiv_rn(ex2(__fmaf_rn(zd, a.kT, -mdk)), ri.sd);
         qd = __fdiv_rn(ins ? __fmul_rn(q, a.C) : q, norm_N(a.C, ri.sq));
@@ -1020,17 +1175,22 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
         if (a.qd_out) a.qd_out[static_cast<size_t>(b) * a.K + r] = qd;
       }
     } else {
-      d = a.d_in[static_cast<size_t>(b) * a.K + r];
+      d = sh.ival[2];
+      zt = sh.scal[4];
+      zd = sh.scal[5];
+      zknown = true;
     }
     if (a.do_verify && tid == 0) {
       PosInfo pi{d, 0.f, 0.f, 0};
       if (d >= 0 && d < a.V) {
-        const float zt = E::ld(row_ptr(a, 0, b, r, E::kSize), d);
-        const float zd = E::ld(rowD, d);
         if (a.greedy) {
           pi.p = (d == ri.at) ? 1.f : 0.f;
           pi.q = (d == ri.ad) ? 1.f : 0.f;
         } else {
+          if (!zknown) {
+            zt = E::ld(rowT, d);
+            zd = E::ld(rowD, d);
+          }
           const bool ins = F > 0 && cand_key(zd, d) >= keyF;
           pi.p = __fdiv_rn(ex2(__fmaf_rn(zt, a.kT, -__fmul_rn(ri.mt, a.kT))), ri.st);
           const float q = __fdiv_rn(ex2(__fmaf_rn(zd, a.kT, -mdk)), ri.sd);
@@ -1056,12 +1216,21 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Smem &
 // ===========================================================================
 // sequence finish: acceptance chain, bonus draw, outputs, cache lookup
 // ===========================================================================
+// The top-F lists of a sequence (cache lookup) fit sh.cand; its payload fits
+// the payload stage.
+SSD_DEV bool lists_staged(const VocabArgs &a) { return a.do_lookup && a.foff[a.K + 1] <= kCandCap; }
+SSD_DEV bool pay_staged(const VocabArgs &a) {
+  return a.do_lookup && a.next_tokens && a.payload && a.foff[a.K + 1] * a.K <= kPayStage;
+}
+
 // Stage in shared memory, in one round of loads, what the final steps of
 // sequence b need whatever the accept count: draft tokens, p(d), q'(d), the
-// uniforms, every row's merged statistics and S threshold key and (umass
-// given) the residual unit masses.  Then the acceptance chain (thread 0).  Every
+// uniforms, every row's merged statistics and S threshold key, the top-F
+// lists (sh.cand) and payload (`pay`) of the cache lookup when they fit, the
+// residual unit masses (`umass`) and target row K's chunk and block records
+// for the bonus draw (`st`).  Then the acceptance chain (thread 0).  Every
 // thread returns the accept count.
-SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, Smem &sh) {
+SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, Stage *st, Smem &sh) {
   const int tid = threadIdx.x;
   for (int t = tid; t < a.K; t += kThreads) {
     const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + t);
@@ -1080,6 +1249,26 @@ SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, Smem &sh) {
     const int nu = a.nchunks * kQuarters;
     for (int q = tid; q < nu; q += kThreads) umass[q] = __ldcg(a.rmass + static_cast<size_t>(b) * nu + q);
   }
+  if (lists_staged(a))
+    for (int r = 0; r <= a.K; ++r) {
+      const uint64_t *src = a.S + (static_cast<size_t>(b) * (a.K + 1) + r) * a.Fcap;
+      for (int i = tid; i < a.F[r]; i += kThreads) sh.cand[a.foff[r] + i] = ldcg_key(src + i);
+    }
+  if (pay && pay_staged(a)) {
+    const int n = a.foff[a.K + 1] * a.K;
+    const int32_t *src = a.payload + static_cast<size_t>(b) * n;
+    for (int i = tid; i < n; i += kThreads) pay[i] = src[i];
+  }
+  if (st && !a.greedy && a.tsl[a.K] >= 0) {
+    const int ts = a.tsl[a.K];
+    for (int c = tid; c < a.nchunks; c += kThreads) st->cs[0][c] = ldcg_stat(a.stats + chunk_index(a, b, ts, c));
+    if (a.slot[ts].blocks && a.nchunks <= kStageChunks) {
+      constexpr int kW = static_cast<int>(sizeof(BlockRec) / 16);
+      const int4 *src = reinterpret_cast<const int4 *>(a.blk + chunk_index(a, b, ts, 0));
+      int4 *dst = reinterpret_cast<int4 *>(st->blk);
+      for (int i = tid; i < a.nchunks * kW; i += kThreads) dst[i] = __ldcg(src + i);
+    }
+  }
   __syncthreads();
   if (tid == 0) {
     int acc = 0;
@@ -1093,16 +1282,23 @@ SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, Smem &sh) {
   return sh.ival[1];
 }
 
-// Outputs of sequence b once its bonus token bt is known (sh.cd: draft tokens).
-SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, Smem &sh) {
+// Outputs of sequence b once its bonus token bt is known (sh.cd: draft tokens;
+// the lookup's lists and payload as stage_chain staged them, `pay` its
+// payload stage).
+SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, const int32_t *pay, Smem &sh) {
   const int tid = threadIdx.x;
   const int Fa = a.F[acc];
   if (tid == 0) sh.ival[3] = kNone;
   __syncthreads();
   if (a.do_lookup) {
-    const uint64_t *S = a.S + (static_cast<size_t>(b) * (a.K + 1) + acc) * a.Fcap;
-    for (int i = tid; i < Fa; i += kThreads)
-      if (cand_idx(ldcg_key(S + i)) == bt) atomicMin(&sh.ival[3], i);
+    if (lists_staged(a)) {
+      for (int i = tid; i < Fa; i += kThreads)
+        if (cand_idx(sh.cand[a.foff[acc] + i]) == bt) atomicMin(&sh.ival[3], i);
+    } else {
+      const uint64_t *S = a.S + (static_cast<size_t>(b) * (a.K + 1) + acc) * a.Fcap;
+      for (int i = tid; i < Fa; i += kThreads)
+        if (cand_idx(ldcg_key(S + i)) == bt) atomicMin(&sh.ival[3], i);
+    }
     __syncthreads();
   }
   const int s_hit = (a.do_lookup && sh.ival[3] != kNone) ? a.foff[acc] + sh.ival[3] : -1;
@@ -1112,9 +1308,13 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
     if (tid == acc) v = bt;
     a.out_tokens[static_cast<size_t>(b) * (a.K + 1) + tid] = v;
   }
-  if (a.do_lookup && a.next_tokens && tid < a.K)
-    a.next_tokens[static_cast<size_t>(b) * a.K + tid] =
-        (s_hit >= 0 && a.payload) ? a.payload[(static_cast<size_t>(b) * a.foff[a.K + 1] + s_hit) * a.K + tid] : -1;
+  if (a.do_lookup && a.next_tokens && tid < a.K) {
+    int v = -1;
+    if (s_hit >= 0 && a.payload)
+      v = (pay && pay_staged(a)) ? pay[s_hit * a.K + tid]
+                                 : a.payload[(static_cast<size_t>(b) * a.foff[a.K + 1] + s_hit) * a.K + tid];
+    a.next_tokens[static_cast<size_t>(b) * a.K + tid] = v;
+  }
   __syncthreads();
   if (tid == 0) {
     if (zero) atomicOr(a.status, kFlagZeroResidual);
@@ -1125,8 +1325,11 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
       if (a.slot_out) a.slot_out[b] = s_hit;
       if (s_hit >= 0) atomicAdd(a.ctr + 1, 1u);
     }
-    const uint32_t done = atom_add_acq_rel(a.ctr, 1u);
-    if (done + 1 == static_cast<uint32_t>(a.B) && a.hits) *a.hits = ld_acquire(a.ctr + 1);
+    const uint32_t done = atom_add_release(a.ctr, 1u);
+    if (done + 1 == static_cast<uint32_t>(a.B) && a.hits) {
+      fence_acq_rel();
+      *a.hits = ld_relaxed(a.ctr + 1);
+    }
   }
   __syncthreads();
 }
@@ -1134,13 +1337,14 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
 // The last pair of sequence b merged: chain, then (greedy, or every token
 // accepted) the bonus draw and the outputs; a residual draw is left to k_resid.
 template <class E>
-__device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Smem &sh) {
-  const int acc = stage_chain(a, b, nullptr, sh);
-  if (!a.greedy && acc < a.K) {
-    if (threadIdx.x == 0) a.accs[b] = acc;
-    return;
+__device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Stage &st, Smem &sh) {
+  const int acc = stage_chain(a, b, nullptr, st.pay, &st, sh);
+  const bool resid = !a.greedy && acc < a.K;
+  if (threadIdx.x == 0) {
+    a.accs[b] = resid ? acc : -1;
+    st_release(ready_word(a, b), 1u);  // the sequence's k_resid CTAs may go on
   }
-  if (threadIdx.x == 0) a.accs[b] = -1;
+  if (resid) return;
   const RowInfo row = sh.rows[acc];
   int bt = row.at;
   float W = 1.f;
@@ -1151,9 +1355,9 @@ __device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Smem &sh) {
       zero = !(W > 0.f);
     }
   } else {
-    bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], sh);
+    bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], acc == a.K ? &st : nullptr, sh);
   }
-  emit(a, b, acc, bt, W, zero, sh);
+  emit(a, b, acc, bt, W, zero, st.pay, sh);
 }
 
 // The CTA's trace entry: (SM << 48 | kind << 40 | sequence << 20 | index),
@@ -1212,11 +1416,12 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
   mark(a, sh.mk, 2);
   if (last_of_pair) {
     kind = 1;
-    row_finish<E>(a, b, r, sh);
+    Stage &st = *reinterpret_cast<Stage *>(buf);  // the chunk buffer is free again
+    row_finish<E>(a, b, r, st, sh);
     mark(a, sh.mk, 4);
     if (a.do_verify && arrive_last(seq_ctr(a, b), static_cast<uint32_t>(a.npairs), sh)) {
       kind = 3;
-      seq_finish<E>(a, b, sh);
+      seq_finish<E>(a, b, st, sh);
       mark(a, sh.mk, 5);
     }
   }
@@ -1224,20 +1429,39 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
   if (a.trace && tid == 0) trace_entry(a.trace + 8 * static_cast<size_t>(blockIdx.x), kind, b, rem, sh.mk);
 }
 
-// Residual unit (sequence b, chunk c, quarter g = rounds 2g, 2g+1): its block
-// sums of max(0, p - q') over target and draft row a, read straight from
-// global memory; the last unit of the sequence draws the bonus.
+// Thread 0 of a residual CTA: bounded wait (sleeping between polls) for a
+// sequence's ready word.  k_resid is a programmatic dependent launch that
+// starts once every k_stats CTA has started, so the word is set unless
+// k_stats failed.
+SSD_DEV bool wait_ready(const uint32_t *w) {
+  for (uint32_t it = 0; it < kMaxPolls; ++it) {
+    if (ld_relaxed(w)) {
+      fence_acq_rel();
+      return true;
+    }
+    __nanosleep(500);
+  }
+  return false;
+}
+
+// Residual unit (sequence b, chunk c, quarter g = rounds 2g, 2g+1): once the
+// sequence's acceptance chain has run, its block sums of max(0, p - q') over
+// target and draft row a, read straight from global memory; the last unit of
+// the sequence draws the bonus.
 template <class E>
-__global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ VocabArgs a) {
-  __shared__ Smem sh;
-  __shared__ float umass[kMaxChunks * kQuarters];  // the sequence's unit masses (final draw)
-  // everything k_stats wrote is visible after this
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+SSD_DEV void resid_unit(const VocabArgs &a, float *umass, int32_t *pay, Smem &sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nu = a.nchunks * kQuarters;
   const int b = static_cast<int>(blockIdx.x / nu);
   const int u = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * nu);
   const int c = u / kQuarters, g = u % kQuarters;
+  if (tid == 0) {
+    const bool ok = wait_ready(ready_word(a, b));
+    if (!ok) atomicOr(a.status, kFlagWaitTimeout);
+    sh.flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sh.flag) return;
   const int acc = __ldcg(a.accs + b);
   if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
   if (tid == 0 && a.trace)
@@ -1263,32 +1487,38 @@ __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ V
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    float m = 0.f;
-    for (int k = 0; k < 2 * kWarps; ++k) m = __fadd_rn(m, sh.bw[k]);
-    a.rmass[static_cast<size_t>(b) * nu + u] = m;
+  if (warp == 0) {
+    const float m = warp_total(sh.bw, 2 * kWarps);
+    if (lane == 0) a.rmass[static_cast<size_t>(b) * nu + u] = m;
   }
   mark(a, sh.mk, 2);
   int kind = 2;
   if (arrive_last(res_ctr(a, b), static_cast<uint32_t>(nu), sh)) {
     kind = 3;
     mark(a, sh.mk, 3);
-    const int acc2 = stage_chain(a, b, umass, sh);  // the same chain: acc2 == acc
+    const int acc2 = stage_chain(a, b, umass, pay, nullptr, sh);  // the same chain: acc2 == acc
     const RowInfo ra = sh.rows[acc2];
     const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
     const float ub = a.u_bonus[b];
-    if (tid == 0) {
+    if (warp == 0) {
       locate(umass, nu, ub, false, sh);
+      __syncwarp();
       const int uq = sh.ival[0];
-      sh.ival[6] = uq;
-      sh.scal[6] = sh.scal[2];  // the residual's total mass
+      const float local = sh.scal[1];
+      const float W = sh.scal[2];  // the residual's total mass
+      __syncwarp();
+      if (lane == 0) {
+        sh.ival[6] = uq;
+        sh.scal[6] = W;
+      }
       if (uq >= 0) {
         const float *src = a.rbs + (static_cast<size_t>(b) * a.nchunks + uq / kQuarters) * kBlocks +
                            2 * (uq % kQuarters) * kWarps;
-        for (int k = 0; k < 2 * kWarps; ++k) sh.bw[k] = __ldcg(src + k);
-        const float local = sh.scal[1];
+        if (lane < 2 * kWarps) sh.bw[lane] = __ldcg(src + lane);
+        __syncwarp();
         locate(sh.bw, 2 * kWarps, local, true, sh);
-        if (sh.ival[0] < 0) {  // a unit of positive mass has a positive block; kept for safety
+        __syncwarp();
+        if (lane == 0 && sh.ival[0] < 0) {  // a unit of positive mass has a positive block; kept for safety
           sh.ival[0] = 2 * kWarps - 1;
           sh.scal[1] = local;
         }
@@ -1312,15 +1542,27 @@ __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ V
       bt = sh.ival[4];
     }
     const bool zero = uq < 0;  // no residual mass: p_{a+1} instead
-    if (bt < 0) bt = draw_target<E>(a, b, acc2, ra, ub, sh);
+    if (bt < 0) bt = draw_target<E>(a, b, acc2, ra, ub, nullptr, sh);
     mark(a, sh.mk, 5);
-    emit(a, b, acc2, bt, W, zero, sh);
+    emit(a, b, acc2, bt, W, zero, pay, sh);
   }
   mark(a, sh.mk, 6);
   if (a.trace && tid == 0) {
     const size_t base = static_cast<size_t>(a.B) * a.nslots * a.nchunks;
     trace_entry(a.trace + 8 * (base + blockIdx.x), kind, b, u, sh.mk);
   }
+}
+
+template <class E>
+__global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ VocabArgs a) {
+  __shared__ Smem sh;
+  __shared__ float umass[kMaxChunks * kQuarters];  // the sequence's unit masses (final draw)
+  __shared__ int32_t pay[kPayStage];                // the sequence's cache payload (final draw)
+  resid_unit<E>(a, umass, pay, sh);
+  // the grid completes only after k_stats has: its last CTA to exit waits for it
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(resid_exit_ctr(a), 1u) + 1 == gridDim.x)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 struct LookupArgs {
@@ -1396,7 +1638,7 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   L->Fcap = fmax > 0 ? fmax : 1;
   const size_t Bn = static_cast<size_t>(B > 0 ? B : 1);
   const size_t nrec = Bn * L->nslots * L->nchunks;
-  L->ctr_words = 2 + 2 * Bn + Bn * (K + 1);
+  L->ctr_words = ctr_words(Bn, K);
   size_t o = 0;
   L->ctr_off = o;
   o = align_up(o + L->ctr_words * sizeof(uint32_t), 256);
@@ -1560,9 +1802,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
                 ? static_cast<unsigned long long *>(g_trace)
                 : nullptr;
   // counters start at zero
-  e = cudaMemsetAsync(a.ctr, 0, (2 + 2 * static_cast<size_t>(a.B) + static_cast<size_t>(a.B) * (a.K + 1)) *
-                                    sizeof(uint32_t),
-                      s);
+  e = cudaMemsetAsync(a.ctr, 0, ctr_words(static_cast<size_t>(a.B), a.K) * sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   if (g_ev_before) cudaEventRecord(g_ev_before, s);
   k_stats<E><<<static_cast<unsigned>(n1), kThreads, kStatsSmem, s>>>(a);
