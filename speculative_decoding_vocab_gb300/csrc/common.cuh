@@ -26,6 +26,19 @@ constexpr uint32_t kMaxPolls = 1u << 22;
 SSD_DEV uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Asynchronous global -> shared copies (all in flight together; one wait).
+// 16 bytes through L2 only; 8 and 4 bytes through L1 (callers order them
+// after the acquire that makes the source current).
+SSD_DEV void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+SSD_DEV void cp_async8(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+SSD_DEV void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+SSD_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // order-preserving keys: larger float -> larger unsigned key

@@ -63,7 +63,7 @@ constexpr int kMaxChunks = 128;  // per row: 4 lists per lane in the warp merge
 constexpr int kRankMax = 512;    // lists merged by rank selection up to this many keys
 constexpr int kNone = 0x7fffffff;
 
-struct ChunkStat {
+struct __align__(16) ChunkStat {
   float m;   // chunk maximum
   float s;   // sum over the chunk of 2^(z kT - fl(m kT)) (0 when greedy)
   int amax;  // lowest index holding m
@@ -72,7 +72,7 @@ struct ChunkStat {
 // Per chunk of a row that is drawn from: each warp's maximum and, per block
 // (round j, warp w), the sum of 2^(z kT - fl(wm[w] kT)) over the block's
 // elements (0 when greedy or for a warp without finite elements).
-struct BlockRec {
+struct __align__(16) BlockRec {
   float wm[kWarps];
   float bs[kRounds][kWarps];
 };
@@ -82,14 +82,14 @@ struct RowSlot {
   int16_t F;       // top-F candidates wanted (0 = none)
   int16_t blocks;  // block sums wanted (the row is drawn from)
 };
-struct RowInfo {  // merged statistics of row r of a sequence
+struct __align__(16) RowInfo {  // merged statistics of row r of a sequence
   float mt, st;   // target max, sum relative to fl(mt kT)
   int at, pad0;   // target argmax
   float md, sd;   // draft max, sum
   int ad;         // draft argmax
   float sq;       // sum of q over S (normalised)
 };
-struct PosInfo {  // draft token d_j and its probabilities
+struct __align__(16) PosInfo {  // draft token d_j and its probabilities
   int d;
   float p, q;  // p_j(d), q'_j(d); p < 0 marks an invalid token
   int pad;
@@ -105,6 +105,7 @@ struct VocabArgs {
   float C;
   int npairs;  // row pairs per sequence, r = 0 .. npairs-1
   long nst;    // chunks of the call: B * nslots * nchunks
+  int b0;      // k_stats: the first sequence of this launch (grid z = sequence - b0)
   int do_sample, do_verify, do_predict, do_lookup;
   RowSlot slot[kMaxSlots];                   // ordered by pair: target r, then draft r
   int tsl[kMaxK + 1], dsl[kMaxK + 1];        // slot of target / draft row r (-1: none)
@@ -224,8 +225,8 @@ struct Smem {
   float cmass[kMaxChunks];
   float bw[kBlocks];
   uint64_t S[kMaxF];
-  float cp[kMaxK], cq[kMaxK], cu[kMaxK];
-  int cd[kMaxK];
+  PosInfo pos[kMaxK];  // draft tokens, p(d), q'(d)
+  float cu[kMaxK];     // acceptance uniforms
   RowInfo rows[kMaxK + 1];
   uint64_t keyF[kMaxK + 1];
   unsigned long long mk[7];  // trace marks (thread 0)
@@ -239,10 +240,12 @@ constexpr int kPayStage = 1024;   // payload words staged
 struct Stage {
   ChunkStat cs[2][kMaxChunks];  // chunk records: target row, draft row
   BlockRec blk[kStageChunks];   // block records of the row drawn from
-  float z[32 * 8];              // the other row's values of the block a draw located
+  float z[2][32 * 8];           // target / draft row values of the block a draw located
   int32_t pay[kPayStage];       // the sequence's cache payload
 };
 static_assert(sizeof(Stage) <= kChunkBytes, "the merge stage must fit the chunk buffer");
+static_assert(sizeof(ChunkStat) == 16 && sizeof(BlockRec) % 16 == 0 && sizeof(RowInfo) == 32 && sizeof(PosInfo) == 16,
+              "records are copied in 16-byte pieces");
 
 // Every thread calls after writing its part of a published result.  True, in
 // every thread of the CTA, for the arrival that completes `total` arrivals on
@@ -554,6 +557,32 @@ SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
   }
 }
 
+// The 8 block sums of a warp (kRounds = 8): pr[j] is this lane's part of
+// round j's block.  Recursive halving: at each step a lane keeps half of its
+// rounds and adds its partner's part of them (partners 16, 8, 4 lanes apart),
+// then the last four lanes of a round are summed by a butterfly.  Lane l ends
+// with the sum of round l / 4.
+SSD_DEV float warp_round_sums(const float (&pr)[kRounds]) {
+  static_assert(kRounds == 8, "three halving steps");
+  const int lane = threadIdx.x & 31;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float q4[4], q2[2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float keep = b4 ? pr[4 + k] : pr[k], send = b4 ? pr[k] : pr[4 + k];
+    q4[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float keep = b3 ? q4[2 + k] : q4[k], send = b3 ? q4[k] : q4[2 + k];
+    q2[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  float q = __fadd_rn(b2 ? q2[1] : q2[0], __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 2));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 1));
+  return q;
+}
+
 // The chunk's record, block sums and sorted top-F candidate list.
 template <class E>
 SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8_t *buf, Smem &sh) {
@@ -571,52 +600,75 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
   cv.ntail = cv.n - cv.nvec * E::kVec;
   const bool tail_mine = cv.ntail > 0 && tid == (cv.nvec & (kThreads - 1));  // the partial vector
 
-  // pass 1: the thread's maximum and the first of its vectors holding it
-  // (packed bf16 maxima for bf16 rows)
+  // the chunk's argmax is kept where it is used: greedy rows and rows whose
+  // top-1 list is the argmax (F = 1).  Elsewhere the record's index is the
+  // chunk's first element, which is the argmax in the one case a T > 0 draw
+  // can fall back to it (a row without finite logits: every chunk max -inf).
+  const bool need_arg = greedy || rs.F == 1;
   float m1 = NEG_INF;
-  int j1 = -1;
+  int wi = kNone;
+  if (need_arg) {
+    // pass 1: the thread's maximum and the first of its vectors holding it
+    int j1 = -1;
 #pragma unroll
-  for (int j = 0; j < kRounds; ++j) {
-    const int v = tid + j * kThreads;
-    if (v < cv.nvec) {
-      const uint4 w = cv.v4[v];
-      float vm;
-      if constexpr (E::kSize == 2) {
-        const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-        vm = fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
-      } else {
-        vm = fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    for (int j = 0; j < kRounds; ++j) {
+      const int v = tid + j * kThreads;
+      if (v < cv.nvec) {
+        const float vm = cv.vmax(v);
+        if (vm > m1 || j1 < 0) {  // strictly larger: the first vector among equal maxima
+          m1 = fmaxf(m1, vm);
+          j1 = j;
+        }
       }
-      if (vm > m1 || j1 < 0) {  // strictly larger: the first vector among equal maxima
+    }
+    if (tail_mine) {
+      const float vm = cv.vmax(cv.nvec);
+      if (vm > m1 || j1 < 0) {
         m1 = fmaxf(m1, vm);
-        j1 = j;
+        j1 = cv.nvec / kThreads;
       }
     }
-  }
-  if (tail_mine) {
-    const float vm = cv.vmax(cv.nvec);
-    if (vm > m1 || j1 < 0) {
-      m1 = fmaxf(m1, vm);
-      j1 = cv.nvec / kThreads;
+    const float wm1 = warp_max(m1);
+    // the lane holding the warp maximum: its first element there
+    int i1 = kNone;
+    if (m1 == wm1 && j1 >= 0) {
+      const int v = tid + j1 * kThreads;
+      float f[E::kVec];
+      cv.get(v, f);
+#pragma unroll
+      for (int e = E::kVec - 1; e >= 0; --e)
+        if (f[e] == wm1 && v * E::kVec + e < cv.n) i1 = v * E::kVec + e;
     }
+    wi = i1;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wi = min(wi, __shfl_xor_sync(0xffffffffu, wi, o));
+  } else {
+    // pass 1: the thread's maximum (bf16 rows: packed maxima of all vectors)
+    if constexpr (E::kSize == 2) {
+      uint32_t mm = 0xFF80FF80u;  // (-inf, -inf)
+#pragma unroll
+      for (int j = 0; j < kRounds; ++j) {
+        const int v = tid + j * kThreads;
+        if (v < cv.nvec) {
+          const uint4 w = cv.v4[v];
+          mm = bmax2(mm, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+        }
+      }
+      m1 = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRounds; ++j) {
+        const int v = tid + j * kThreads;
+        if (v < cv.nvec) m1 = fmaxf(m1, cv.vmax(v));
+      }
+    }
+    if (tail_mine) m1 = fmaxf(m1, cv.vmax(cv.nvec));
   }
   const float wm = warp_max(m1);
-  // the lane holding the warp maximum: its first element there
-  int i1 = kNone;
-  if (m1 == wm && j1 >= 0) {
-    const int v = tid + j1 * kThreads;
-    float f[E::kVec];
-    cv.get(v, f);
-#pragma unroll
-    for (int e = E::kVec - 1; e >= 0; --e)
-      if (f[e] == wm && v * E::kVec + e < cv.n) i1 = v * E::kVec + e;
-  }
-  int wi = i1;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) wi = min(wi, __shfl_xor_sync(0xffffffffu, wi, o));
   // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed
-  // FMA / ADD (the same arithmetic whether or not block sums are kept); rows
-  // that are drawn from also keep their block sums
+  // FMA / ADD; per round the lane's four pairs first, then into the lane's
+  // total (the same arithmetic whether or not block sums are kept).  Rows
+  // that are drawn from also keep their block sums.
   float s = 0.f;
   BlockRec *br = a.blk + chunk_index(a, b, slot, c);
   if (!greedy && wm != NEG_INF) {
@@ -630,53 +682,41 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
       for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
     }
     uint64_t acc = pack2(0.f, 0.f);
-    if (rs.blocks) {
+    float pr[kRounds];  // block rows: the lane's sum of each round
 #pragma unroll
-      for (int j = 0; j < kRounds; ++j) {
-        const int v = tid + j * kThreads;
-        float pj = 0.f;
-        if (v < cv.nvec) {
-          const uint4 w = cv.v4[v];
-          uint64_t accj = pack2(0.f, 0.f);
+    for (int j = 0; j < kRounds; ++j) {
+      const int v = tid + j * kThreads;
+      pr[j] = 0.f;
+      if (v < cv.nvec) {
+        const uint4 w = cv.v4[v];
+        uint64_t accj = 0;
 #pragma unroll
-          for (int h = 0; h < E::kPairs; ++h) {
-            float x0, x1;
-            unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
-            const uint64_t e2 = pack2(ex2(x0), ex2(x1));
-            acc = add2(acc, e2);
-            accj = add2(accj, e2);
-          }
+        for (int h = 0; h < E::kPairs; ++h) {
+          float x0, x1;
+          unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
+          const uint64_t e2 = pack2(ex2(x0), ex2(x1));
+          accj = (h == 0) ? e2 : add2(accj, e2);
+        }
+        acc = add2(acc, accj);
+        if (rs.blocks) {
           float lo, hi;
           unpack2(accj, lo, hi);
-          pj = __fadd_rn(lo, hi);
-        } else if (tail_mine && v == cv.nvec) {
-          pj = tail;
+          pr[j] = __fadd_rn(lo, hi);
         }
-        const float bsum = warp_sum(pj);
-        if (lane == 0) br->bs[j][warp] = bsum;
+      } else if (tail_mine && v == cv.nvec) {
+        pr[j] = tail;
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kRounds; ++j) {
-        const int v = tid + j * kThreads;
-        if (v < cv.nvec) {
-          const uint4 w = cv.v4[v];
-#pragma unroll
-          for (int h = 0; h < E::kPairs; ++h) {
-            float x0, x1;
-            unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
-            acc = add2(acc, pack2(ex2(x0), ex2(x1)));
-          }
-        }
-      }
+    }
+    if (rs.blocks) {
+      const float bsum = warp_round_sums(pr);
+      if ((lane & 3) == 0) br->bs[lane >> 2][warp] = bsum;
     }
     float lo, hi;
     unpack2(acc, lo, hi);
     s = __fadd_rn(__fadd_rn(lo, hi), tail);
     s = warp_sum(s);
-  } else if (rs.blocks && lane == 0) {
-#pragma unroll
-    for (int j = 0; j < kRounds; ++j) br->bs[j][warp] = 0.f;  // every block record of a drawn row is written
+  } else if (rs.blocks && lane < kRounds) {
+    br->bs[lane][warp] = 0.f;  // every block record of a drawn row is written
   }
   if (lane == 0) {
     if (rs.blocks) br->wm[warp] = wm;
@@ -834,13 +874,14 @@ SSD_DEV void chunk_masses(const VocabArgs &a, int b, int slot, float rk, Smem &s
 // 2^(z kT - rk), scaled by C on the set S (the Fn keys of Slist) when C < 1.
 // sh.cmass holds the chunk masses with the down-weighting applied; `sbr`, when
 // given, the row's block records staged in shared memory (else they are read
-// from global memory).  With `rowZ`, warp 1 stages the other row's values of
-// the located block in zbuf while warp 0 scans it.  Every thread calls;
-// returns the token (-1 if the masses are all 0).
+// from global memory).  While warp 0 scans the located block, warp 1 stages
+// its values (zdrawn) and, with `rowZ`, the other row's values there
+// (zother); sh.ival[5] is then the block's first element.  Every thread
+// calls; returns the token (-1 if the masses are all 0).
 template <class E, bool HT, class WF>
 SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, float rk, float u, const WF &wf,
-                       const BlockRec *sbr, const uint64_t *Slist, int Fn, float C, const char *rowZ, float *zbuf,
-                       Smem &sh) {
+                       const BlockRec *sbr, const uint64_t *Slist, int Fn, float C, float *zdrawn, const char *rowZ,
+                       float *zother, Smem &sh) {
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
   __syncthreads();
@@ -894,15 +935,19 @@ SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, flo
   if (warp == 0) {
     d = warp_find<E, HT, !HT>(a, HT ? row : nullptr, HT ? nullptr : row, cs, blk / kWarps, blk % kWarps, local2,
                               wf);
-  } else if (warp == 1 && rowZ) {
+  } else if (warp == 1 && zdrawn) {
     const int lane = tid & 31;
     const int e0 = cs * a.chunk_elems;
     const int n = min(a.chunk_elems, a.V - e0);
     const int i0 = ((blk / kWarps) * kThreads + (blk % kWarps) * 32 + lane) * E::kVec;
-    float f[E::kVec];
-    ld_vec<E>(rowZ, e0, n, i0, 0.f, f);
+    float f[E::kVec], g[E::kVec];
+    ld_vec<E>(row, e0, n, i0, 0.f, f);
+    if (rowZ) ld_vec<E>(rowZ, e0, n, i0, 0.f, g);
 #pragma unroll
-    for (int e = 0; e < E::kVec; ++e) zbuf[lane * E::kVec + e] = f[e];
+    for (int e = 0; e < E::kVec; ++e) zdrawn[lane * E::kVec + e] = f[e];
+    if (rowZ)
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e) zother[lane * E::kVec + e] = g[e];
   }
   __syncthreads();  // everyone read sh.ival / sh.scal
   if (tid == 0) {
@@ -976,7 +1021,7 @@ SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, fl
       chunk_masses(a, b, a.tsl[r], mtk, sh);
     }
     __syncthreads();
-    d = stats_draw<E, true>(a, b, a.tsl[r], rowT, mtk, u, wp, sbr, nullptr, 0, 1.f, nullptr, nullptr, sh);
+    d = stats_draw<E, true>(a, b, a.tsl[r], rowT, mtk, u, wp, sbr, nullptr, 0, 1.f, nullptr, nullptr, nullptr, sh);
   } else {
     d = exact_draw<E, true, false>(a, rowT, nullptr, u, wp, sh);
   }
@@ -1020,17 +1065,17 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage 
   const bool by_rank = nl <= kRankMax;
   if (F > 0 && by_rank) {
     const uint64_t *src = a.cands + chunk_index(a, b, ds, 0) * a.Fcap;
-    for (int i = tid; i < nl; i += kThreads) lists[i] = ldcg_key(src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
+    for (int i = tid; i < nl; i += kThreads) cp_async8(&lists[i], src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
   }
   for (int c = tid; c < a.nchunks; c += kThreads) {
-    if (ts >= 0) st.cs[0][c] = ldcg_stat(a.stats + chunk_index(a, b, ts, c));
-    if (ds >= 0) st.cs[1][c] = ldcg_stat(a.stats + chunk_index(a, b, ds, c));
+    if (ts >= 0) cp_async16(&st.cs[0][c], a.stats + chunk_index(a, b, ts, c));
+    if (ds >= 0) cp_async16(&st.cs[1][c], a.stats + chunk_index(a, b, ds, c));
   }
   if (stage_blk) {
     constexpr int kW = static_cast<int>(sizeof(BlockRec) / 16);
     const int4 *src = reinterpret_cast<const int4 *>(a.blk + chunk_index(a, b, ds, 0));
     int4 *dst = reinterpret_cast<int4 *>(st.blk);
-    for (int i = tid; i < a.nchunks * kW; i += kThreads) dst[i] = __ldcg(src + i);
+    for (int i = tid; i < a.nchunks * kW; i += kThreads) cp_async16(dst + i, src + i);
   }
   if (tid == 0) {
     memset(&sh.ri, 0, sizeof(sh.ri));
@@ -1043,6 +1088,7 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage 
       }
     }
   }
+  cp_async_wait_all();
   __syncthreads();
   // warps 0 and 1 merge the target and draft rows' chunk records
   if (warp == 0 && ts >= 0) {
@@ -1152,20 +1198,23 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage 
             sh.cmass[c] = m;
           }
           __syncthreads();
-          d = stats_draw<E, false>(a, b, ds, rowD, mdk, u, wf, stage_blk ? st.blk : nullptr, sh.S, F, a.C,
-                                   a.do_verify ? rowT : nullptr, st.z, sh);
-          if (a.do_verify && d >= 0) {
+          d = stats_draw<E, false>(a, b, ds, rowD, mdk, u, wf, stage_blk ? st.blk : nullptr, sh.S, F, a.C, st.z[1],
+                                   a.do_verify ? rowT : nullptr, st.z[0], sh);
+          if (d >= 0) {
             const int o = d - sh.ival[5];
             if (o >= 0 && o < 32 * E::kVec) {
-              zt = st.z[o];
+              zd = st.z[1][o];
+              zt = st.z[0][o];
               zknown = true;
             }
           }
         }
         if (d < 0) d = ri.ad;
-        zd = E::ld(rowD, d);
-        if (!zknown) zt = a.do_verify ? E::ld(rowT, d) : 0.f;
-        zknown = true;
+        if (!zknown) {
+          zd = E::ld(rowD, d);
+          zt = a.do_verify ? E::ld(rowT, d) : 0.f;
+          zknown = true;
+        }
         const bool ins = F > 0 && cand_key(zd, d) >= keyF;
         const float q = __fdiv_rn(ex2(__fmaf_rn(zd, a.kT, -mdk)), ri.sd);
         qd = __fdiv_rn(ins ? __fmul_rn(q, a.C) : q, norm_N(a.C, ri.sq));
@@ -1232,48 +1281,52 @@ SSD_DEV bool pay_staged(const VocabArgs &a) {
 // thread returns the accept count.
 SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, Stage *st, Smem &sh) {
   const int tid = threadIdx.x;
+  const size_t r0 = static_cast<size_t>(b) * (a.K + 1);
   for (int t = tid; t < a.K; t += kThreads) {
-    const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + t);
-    sh.cp[t] = pi.p;
-    sh.cq[t] = pi.q;
-    sh.cd[t] = pi.d;
-    sh.cu[t] = a.u_acc[static_cast<size_t>(b) * a.K + t];
+    cp_async16(&sh.pos[t], a.pos + static_cast<size_t>(b) * a.K + t);
+    cp_async4(&sh.cu[t], a.u_acc + static_cast<size_t>(b) * a.K + t);
   }
+  for (int i = tid; i < 2 * (a.K + 1); i += kThreads)
+    cp_async16(reinterpret_cast<int4 *>(&sh.rows[i >> 1]) + (i & 1), reinterpret_cast<const int4 *>(a.rows + r0 + (i >> 1)) + (i & 1));
   for (int r = tid; r <= a.K; r += kThreads) {
-    const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
-    sh.rows[r] = ldcg_row(a.rows + rr);
     const int F = a.Fs[r];
-    sh.keyF[r] = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
+    if (F > 0) cp_async8(&sh.keyF[r], a.S + (r0 + r) * a.Fcap + F - 1);
+    else sh.keyF[r] = 0ull;
   }
   if (umass) {
     const int nu = a.nchunks * kQuarters;
-    for (int q = tid; q < nu; q += kThreads) umass[q] = __ldcg(a.rmass + static_cast<size_t>(b) * nu + q);
+    for (int q = tid; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
   }
-  if (lists_staged(a))
-    for (int r = 0; r <= a.K; ++r) {
-      const uint64_t *src = a.S + (static_cast<size_t>(b) * (a.K + 1) + r) * a.Fcap;
-      for (int i = tid; i < a.F[r]; i += kThreads) sh.cand[a.foff[r] + i] = ldcg_key(src + i);
+  if (lists_staged(a)) {
+    const int nS = a.foff[a.K + 1];
+    for (int i = tid; i < nS; i += kThreads) {
+      int r = 0;
+      while (i >= a.foff[r + 1]) ++r;
+      cp_async8(&sh.cand[i], a.S + (r0 + r) * a.Fcap + (i - a.foff[r]));
     }
+  }
   if (pay && pay_staged(a)) {
     const int n = a.foff[a.K + 1] * a.K;
     const int32_t *src = a.payload + static_cast<size_t>(b) * n;
-    for (int i = tid; i < n; i += kThreads) pay[i] = src[i];
+    for (int i = tid; i < n; i += kThreads) cp_async4(&pay[i], src + i);
   }
   if (st && !a.greedy && a.tsl[a.K] >= 0) {
     const int ts = a.tsl[a.K];
-    for (int c = tid; c < a.nchunks; c += kThreads) st->cs[0][c] = ldcg_stat(a.stats + chunk_index(a, b, ts, c));
+    for (int c = tid; c < a.nchunks; c += kThreads) cp_async16(&st->cs[0][c], a.stats + chunk_index(a, b, ts, c));
     if (a.slot[ts].blocks && a.nchunks <= kStageChunks) {
       constexpr int kW = static_cast<int>(sizeof(BlockRec) / 16);
       const int4 *src = reinterpret_cast<const int4 *>(a.blk + chunk_index(a, b, ts, 0));
       int4 *dst = reinterpret_cast<int4 *>(st->blk);
-      for (int i = tid; i < a.nchunks * kW; i += kThreads) dst[i] = __ldcg(src + i);
+      for (int i = tid; i < a.nchunks * kW; i += kThreads) cp_async16(dst + i, src + i);
     }
   }
+  cp_async_wait_all();
   __syncthreads();
   if (tid == 0) {
     int acc = 0;
     for (int t = 0; t < a.K; ++t) {
-      if (sh.cp[t] >= 0.f && __fmul_rn(sh.cu[t], sh.cq[t]) < sh.cp[t]) ++acc;
+      const PosInfo pi = sh.pos[t];
+      if (pi.p >= 0.f && __fmul_rn(sh.cu[t], pi.q) < pi.p) ++acc;
       else break;
     }
     sh.ival[1] = acc;
@@ -1304,7 +1357,7 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
   const int s_hit = (a.do_lookup && sh.ival[3] != kNone) ? a.foff[acc] + sh.ival[3] : -1;
   if (tid <= a.K) {
     int v = -1;
-    if (tid < acc) v = sh.cd[tid];
+    if (tid < acc) v = sh.pos[tid].d;
     if (tid == acc) v = bt;
     a.out_tokens[static_cast<size_t>(b) * (a.K + 1) + tid] = v;
   }
@@ -1342,7 +1395,8 @@ __device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Stage &st, Sm
   const bool resid = !a.greedy && acc < a.K;
   if (threadIdx.x == 0) {
     a.accs[b] = resid ? acc : -1;
-    st_release(ready_word(a, b), 1u);  // the sequence's k_resid CTAs may go on
+    // the sequence's k_resid CTAs may go on; the word carries accs[b] + 2
+    st_release(ready_word(a, b), static_cast<uint32_t>((resid ? acc : -1) + 2));
   }
   if (resid) return;
   const RowInfo row = sh.rows[acc];
@@ -1382,10 +1436,9 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
   // k_resid (if any) may start launching once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
-  const int per_seq = a.nslots * a.nchunks;
-  const int b = static_cast<int>(blockIdx.x / per_seq);
-  const int rem = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * per_seq);
-  const int slot = rem / a.nchunks, c = rem - slot * a.nchunks;
+  const int c = static_cast<int>(blockIdx.x), slot = static_cast<int>(blockIdx.y);
+  const int b = a.b0 + static_cast<int>(blockIdx.z);
+  const int rem = slot * a.nchunks + c;
   const RowSlot rs = a.slot[slot];
   // the chunk's whole vectors: one TMA bulk copy; thread 0 waits (bounded,
   // sleeping between polls), the other threads at the barrier
@@ -1426,22 +1479,24 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
     }
   }
   mark(a, sh.mk, 6);
-  if (a.trace && tid == 0) trace_entry(a.trace + 8 * static_cast<size_t>(blockIdx.x), kind, b, rem, sh.mk);
+  if (a.trace && tid == 0)
+    trace_entry(a.trace + 8 * (static_cast<size_t>(b) * a.nslots * a.nchunks + rem), kind, b, rem, sh.mk);
 }
 
 // Thread 0 of a residual CTA: bounded wait (sleeping between polls) for a
-// sequence's ready word.  k_resid is a programmatic dependent launch that
-// starts once every k_stats CTA has started, so the word is set unless
-// k_stats failed.
-SSD_DEV bool wait_ready(const uint32_t *w) {
+// sequence's ready word; returns it (0: the wait ran out).  k_resid is a
+// programmatic dependent launch that starts once every k_stats CTA has
+// started, so the word is set unless k_stats failed.
+SSD_DEV uint32_t wait_ready(const uint32_t *w) {
   for (uint32_t it = 0; it < kMaxPolls; ++it) {
-    if (ld_relaxed(w)) {
+    const uint32_t v = ld_relaxed(w);
+    if (v) {
       fence_acq_rel();
-      return true;
+      return v;
     }
     __nanosleep(500);
   }
-  return false;
+  return 0u;
 }
 
 // Residual unit (sequence b, chunk c, quarter g = rounds 2g, 2g+1): once the
@@ -1456,19 +1511,32 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, int32_t *pay, Smem &sh
   const int u = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * nu);
   const int c = u / kQuarters, g = u % kQuarters;
   if (tid == 0) {
-    const bool ok = wait_ready(ready_word(a, b));
-    if (!ok) atomicOr(a.status, kFlagWaitTimeout);
-    sh.flag = ok ? 1 : 0;
+    const uint32_t v = wait_ready(ready_word(a, b));
+    if (!v) atomicOr(a.status, kFlagWaitTimeout);
+    sh.flag = static_cast<int>(v);
   }
   __syncthreads();
   if (!sh.flag) return;
-  const int acc = __ldcg(a.accs + b);
+  const int acc = sh.flag - 2;
   if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
   if (tid == 0 && a.trace)
     for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
   mark(a, sh.mk, 0);
   const char *rowT = row_ptr(a, 0, b, acc, E::kSize);
   const char *rowD = row_ptr(a, 1, b, acc, E::kSize);
+  {  // this lane's vectors of the unit, on their way into L1 while the row's statistics load
+    const int e0 = c * a.chunk_elems;
+    const int n = min(a.chunk_elems, a.V - e0);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int i0 = ((2 * g + jj) * kThreads + warp * 32 + lane) * E::kVec;
+      if (i0 + E::kVec <= n) {
+        const int64_t off = static_cast<int64_t>(e0 + i0) * E::kSize;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(rowT + off));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(rowD + off));
+      }
+    }
+  }
   const size_t rr = static_cast<size_t>(b) * (a.K + 1) + acc;
   const RowInfo row = ldcg_row(a.rows + rr);
   const int F = a.Fs[acc];
@@ -1805,9 +1873,16 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   e = cudaMemsetAsync(a.ctr, 0, ctr_words(static_cast<size_t>(a.B), a.K) * sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
   if (g_ev_before) cudaEventRecord(g_ev_before, s);
-  k_stats<E><<<static_cast<unsigned>(n1), kThreads, kStatsSmem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // grid (chunk, row slot, sequence); sequences in launches of at most 65535
+  for (int b0 = 0; b0 < a.B; b0 += 65535) {
+    a.b0 = b0;
+    const unsigned nb = static_cast<unsigned>(a.B - b0 < 65535 ? a.B - b0 : 65535);
+    k_stats<E><<<dim3(static_cast<unsigned>(a.nchunks), static_cast<unsigned>(a.nslots), nb), kThreads, kStatsSmem,
+                 s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  a.b0 = 0;
   if (g_ev_after) cudaEventRecord(g_ev_after, s);
   if (n2 > 0) {
     cudaLaunchConfig_t cfg;
