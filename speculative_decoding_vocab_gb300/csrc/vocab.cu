@@ -116,8 +116,7 @@ struct VocabArgs {
   // workspace
   uint32_t *ctr;  // [0] finished sequences, [1] hits, [2+b] pairs done, [2+B+b] residual
                   // units done, [2+2B + b(K+1) + r] chunks done of pair (b, r), then
-                  // per sequence b its ready word (accs[b] published), then the
-                  // residual CTAs that have exited
+                  // per sequence b its ready word (accs[b] + 2 once published)
   ChunkStat *stats;  // [B][nslots][nchunks]
   BlockRec *blk;     // [B][nslots][nchunks]
   uint64_t *cands;   // [B][nslots][nchunks][Fcap]
@@ -151,10 +150,7 @@ SSD_DEV uint32_t *pair_ctr(const VocabArgs &a, int b, int r) {
 SSD_DEV uint32_t *ready_word(const VocabArgs &a, int b) {
   return a.ctr + 2 + 2 * a.B + static_cast<size_t>(a.B) * (a.K + 1) + b;
 }
-SSD_DEV uint32_t *resid_exit_ctr(const VocabArgs &a) {
-  return a.ctr + 2 + 3 * a.B + static_cast<size_t>(a.B) * (a.K + 1);
-}
-__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 3 + 3 * B + B * (K + 1); }
+__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 3 * B + B * (K + 1); }
 
 __host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
   return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
@@ -1046,7 +1042,7 @@ SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64
 // pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
 // ===========================================================================
 template <class E>
-__device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage &st, Smem &sh) {
+__device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Stage &st, Smem &sh) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ts = a.tsl[r], ds = a.dsl[r];
   const int F = (ds >= 0) ? a.Fs[r] : 0;
@@ -1090,8 +1086,9 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage 
   }
   cp_async_wait_all();
   __syncthreads();
-  // warps 0 and 1 merge the target and draft rows' chunk records
-  if (warp == 0 && ts >= 0) {
+  // the last two warps merge the target and draft rows' chunk records while
+  // the first ones rank the candidate lists
+  if (warp == kWarps - 2 && ts >= 0) {
     const RowStat t = merge_row_warp(a, st.cs[0]);
     if (lane == 0) {
       sh.ri.mt = t.m;
@@ -1099,7 +1096,7 @@ __device__ __noinline__ void row_finish(const VocabArgs &a, int b, int r, Stage 
       sh.ri.at = t.amax;
     }
   }
-  if (warp == 1 && ds >= 0) {
+  if (warp == kWarps - 1 && ds >= 0) {
     const RowStat d = merge_row_warp(a, st.cs[1]);
     if (lane == 0) {
       sh.ri.md = d.m;
@@ -1390,7 +1387,7 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
 // The last pair of sequence b merged: chain, then (greedy, or every token
 // accepted) the bonus draw and the outputs; a residual draw is left to k_resid.
 template <class E>
-__device__ __noinline__ void seq_finish(const VocabArgs &a, int b, Stage &st, Smem &sh) {
+__device__ __forceinline__ void seq_finish(const VocabArgs &a, int b, Stage &st, Smem &sh) {
   const int acc = stage_chain(a, b, nullptr, st.pay, &st, sh);
   const bool resid = !a.greedy && acc < a.K;
   if (threadIdx.x == 0) {
@@ -1627,10 +1624,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ V
   __shared__ float umass[kMaxChunks * kQuarters];  // the sequence's unit masses (final draw)
   __shared__ int32_t pay[kPayStage];                // the sequence's cache payload (final draw)
   resid_unit<E>(a, umass, pay, sh);
-  // the grid completes only after k_stats has: its last CTA to exit waits for it
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(resid_exit_ctr(a), 1u) + 1 == gridDim.x)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the grid completes only after k_stats has: its first CTA waits for it
+  // before exiting
+  if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 struct LookupArgs {
