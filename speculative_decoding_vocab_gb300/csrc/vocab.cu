@@ -211,6 +211,7 @@ SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
 struct Smem {
   uint64_t bar;  // k_stats: completion of the chunk's TMA copy
   int flag, ncand;
+  uint32_t hist[2][256];  // top-F threshold: counts of thread maxima by key byte
   float wm[kWarps], ws[kWarps];
   int wa[kWarps];
   uint64_t redk[kWarps];
@@ -579,6 +580,49 @@ SSD_DEV float warp_round_sums(const float (&pr)[kRounds]) {
   return q;
 }
 
+// One warp: over 256 bucket counts, the bucket where the count from the top
+// bucket down first reaches `need` (sh.ival[5]) and the count in the buckets
+// above it (sh.ival[6]); when the total stays below `need`, bucket 0 and the
+// count above bucket 0.  Lane l holds buckets 255 - 8l down to 248 - 8l.
+SSD_DEV void find_bucket(const uint32_t *hist, int need, Smem &sh) {
+  const int lane = threadIdx.x & 31;
+  const int hi = 255 - 8 * lane;
+  const uint4 x = *reinterpret_cast<const uint4 *>(hist + hi - 7);
+  const uint4 y = *reinterpret_cast<const uint4 *>(hist + hi - 3);
+  const uint32_t c[8] = {y.w, y.z, y.y, y.x, x.w, x.z, x.y, x.x};  // buckets hi, hi - 1, ..., hi - 7
+  uint32_t tot = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) tot += c[k];
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const uint32_t n = static_cast<uint32_t>(need);
+  const uint32_t m = __ballot_sync(0xffffffffu, incl >= n);
+  int bucket = 0;
+  uint32_t above = 0;
+  if (m) {
+    const int src = __ffs(m) - 1;
+    if (lane == src) {
+      uint32_t run = incl - tot;
+      int k = 0;
+      while (k < 7 && run + c[k] < n) run += c[k++];
+      bucket = hi - k;
+      above = run;
+    }
+    bucket = __shfl_sync(0xffffffffu, bucket, src);
+    above = __shfl_sync(0xffffffffu, above, src);
+  } else {
+    above = __shfl_sync(0xffffffffu, incl, 31) - __shfl_sync(0xffffffffu, c[7], 31);
+  }
+  if (lane == 0) {
+    sh.ival[5] = bucket;
+    sh.ival[6] = static_cast<int>(above);
+  }
+}
+
 // The chunk's record, block sums and sorted top-F candidate list.
 template <class E>
 SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8_t *buf, Smem &sh) {
@@ -725,11 +769,23 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
   uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
   if (F > 1) {
     const uint32_t mykey = cv.has(tid) ? f2ord(m1) : 0u;
-    // tau: the F-th largest thread maximum (CTA-wide radix select on the
-    // order-preserving keys); the chunk's top-F all reach it, and typically
-    // little more than F elements do
-    uint32_t tau = 0;
-    for (int bit = 31; bit >= E::kLowBit; --bit) {
+    // tau: the 16-bit prefix of the F-th largest thread maximum's
+    // order-preserving key (exact for bf16), by two levels of 256-bucket
+    // counts; the chunk's top-F all reach it, and typically little more than
+    // F elements do
+    const uint32_t k16 = mykey >> 16;
+    if (cv.has(tid)) atomicAdd(&sh.hist[0][k16 >> 8], 1u);
+    __syncthreads();
+    if (warp == 0) find_bucket(sh.hist[0], F, sh);
+    __syncthreads();
+    const uint32_t b1 = static_cast<uint32_t>(sh.ival[5]);
+    const int above = sh.ival[6];
+    if (cv.has(tid) && (k16 >> 8) == b1) atomicAdd(&sh.hist[1][k16 & 0xFFu], 1u);
+    __syncthreads();
+    if (warp == 0) find_bucket(sh.hist[1], F - above, sh);
+    __syncthreads();
+    uint32_t tau = ((b1 << 8) | static_cast<uint32_t>(sh.ival[5])) << 16;
+    for (int bit = 15; bit >= E::kLowBit; --bit) {  // fp32 rows: the low key bits by radix select
       const uint32_t t = tau | (1u << bit);
       if (__syncthreads_count(mykey >= t) >= F) tau = t;
     }
@@ -1437,6 +1493,9 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
   const int b = a.b0 + static_cast<int>(blockIdx.z);
   const int rem = slot * a.nchunks + c;
   const RowSlot rs = a.slot[slot];
+  if (tid == 0) sh.ncand = 0;
+  sh.hist[0][tid] = 0u;
+  sh.hist[1][tid] = 0u;
   // the chunk's whole vectors: one TMA bulk copy; thread 0 waits (bounded,
   // sleeping between polls), the other threads at the barrier
   if (tid == 0) {
@@ -1446,7 +1505,6 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
     const int e0 = c * a.chunk_elems;
     const int n = min(a.chunk_elems, a.V - e0);
     const uint32_t bulk = static_cast<uint32_t>((n * E::kSize) & ~15);
-    sh.ncand = 0;
     mbar_init(&sh.bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&sh.bar, bulk);
