@@ -114,9 +114,11 @@ struct VocabArgs {
   int Fs[kMaxK + 1];                         // top-F list kept for draft row r (F_r or 0)
   int foff[kMaxK + 2];
   // workspace
-  uint32_t *ctr;  // [0] finished sequences, [1] hits, [2+b] pairs done, [2+B+b] residual
-                  // units done, [2+2B + b(K+1) + r] chunks done of pair (b, r), then
-                  // per sequence b its ready word (accs[b] + 2 once published)
+  uint32_t *ctr;  // [0] finished sequences, [1] hits; per sequence b: [2+b] pair-merge
+                  // tickets, [2+B+b] merged pairs published, [2+2B+b] residual units
+                  // done, [2+3B+b] ready word (accs[b] + 2 once published); per pair
+                  // (b, r): [2+4B + b(K+1)+r] chunk tickets, [2+4B+B(K+1) + b(K+1)+r]
+                  // chunks published
   ChunkStat *stats;  // [B][nslots][nchunks]
   BlockRec *blk;     // [B][nslots][nchunks]
   uint64_t *cands;   // [B][nslots][nchunks][Fcap]
@@ -142,15 +144,17 @@ struct VocabArgs {
   unsigned long long *trace;  // optional: 8 words per CTA (see ssd_set_trace)
 };
 
-SSD_DEV uint32_t *seq_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + b; }
-SSD_DEV uint32_t *res_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + a.B + b; }
-SSD_DEV uint32_t *pair_ctr(const VocabArgs &a, int b, int r) {
-  return a.ctr + 2 + 2 * a.B + static_cast<size_t>(b) * (a.K + 1) + r;
+SSD_DEV uint32_t *seq_tkt(const VocabArgs &a, int b) { return a.ctr + 2 + b; }
+SSD_DEV uint32_t *seq_pub(const VocabArgs &a, int b) { return a.ctr + 2 + a.B + b; }
+SSD_DEV uint32_t *res_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + 2 * a.B + b; }
+SSD_DEV uint32_t *ready_word(const VocabArgs &a, int b) { return a.ctr + 2 + 3 * a.B + b; }
+SSD_DEV uint32_t *pair_tkt(const VocabArgs &a, int b, int r) {
+  return a.ctr + 2 + 4 * static_cast<size_t>(a.B) + static_cast<size_t>(b) * (a.K + 1) + r;
 }
-SSD_DEV uint32_t *ready_word(const VocabArgs &a, int b) {
-  return a.ctr + 2 + 2 * a.B + static_cast<size_t>(a.B) * (a.K + 1) + b;
+SSD_DEV uint32_t *pair_pub(const VocabArgs &a, int b, int r) {
+  return pair_tkt(a, b, r) + static_cast<size_t>(a.B) * (a.K + 1);
 }
-__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 3 * B + B * (K + 1); }
+__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 4 * B + 2 * B * (K + 1); }
 
 __host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
   return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
@@ -192,6 +196,9 @@ SSD_DEV uint32_t atom_add_release(uint32_t *p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+SSD_DEV void red_add_release(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 SSD_DEV void st_release(uint32_t *p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -258,6 +265,20 @@ SSD_DEV bool arrive_last(uint32_t *ctr, uint32_t total, Smem &sh) {
   }
   __syncthreads();
   return sh.flag != 0;
+}
+
+// Thread 0: bounded wait (sleeping between polls) until *ctr reaches `target`,
+// then an acquire; false when the wait ran out.  Used only for counts that
+// CTAs which started earlier raise, so the wait ends unless they failed.
+SSD_DEV bool wait_count(const uint32_t *ctr, uint32_t target) {
+  for (uint32_t it = 0; it < kMaxPolls; ++it) {
+    if (ld_relaxed(ctr) >= target) {
+      fence_acq_rel();
+      return true;
+    }
+    __nanosleep(200);
+  }
+  return false;
 }
 
 // ===========================================================================
@@ -482,7 +503,7 @@ struct ChunkView {
 // The chunk's exact top-F into sh.cand (one winner per sweep; used when ties at
 // the threshold overflow the candidate buffer).  Every thread calls.
 template <class E>
-__device__ __noinline__ void collect_exact(const ChunkView<E> &cv, int F, Smem &sh) {
+__device__ __noinline__ void collect_exact(const ChunkView<E> cv, int F, Smem &sh) {
   const int tid = threadIdx.x;
   uint64_t prev = ~0ull;
   for (int r = 0; r < F; ++r) {
@@ -521,20 +542,25 @@ template <class E>
 SSD_DEV void collect(const ChunkView<E> &cv, bool mine, uint32_t tau, int F, Smem &sh) {
   const int tid = threadIdx.x;
   if (mine) {
-#pragma unroll 1
+    // the rounds whose vector reaches tau (independent loads), then those vectors
+    uint32_t rm = 0;
+#pragma unroll
     for (int j = 0; j < kRounds; ++j) {
       const int v = tid + j * kThreads;
-      if (!cv.has(v)) break;
-      if (f2ord(cv.vmax(v)) >= tau) {
-        float f[E::kVec];
-        cv.get(v, f);
+      if (cv.has(v) && f2ord(cv.vmax(v)) >= tau) rm |= 1u << j;
+    }
+    while (rm) {
+      const int j = __ffs(rm) - 1;
+      rm &= rm - 1;
+      const int v = tid + j * kThreads;
+      float f[E::kVec];
+      cv.get(v, f);
 #pragma unroll
-        for (int e = 0; e < E::kVec; ++e)
-          if (v * E::kVec + e < cv.n && f2ord(f[e]) >= tau) {
-            const int p = atomicAdd(&sh.ncand, 1);
-            if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
-          }
-      }
+      for (int e = 0; e < E::kVec; ++e)
+        if (v * E::kVec + e < cv.n && f2ord(f[e]) >= tau) {
+          const int p = atomicAdd(&sh.ncand, 1);
+          if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
+        }
     }
   }
   __syncthreads();
@@ -542,10 +568,22 @@ SSD_DEV void collect(const ChunkView<E> &cv, bool mine, uint32_t tau, int F, Sme
 }
 
 // Top-F of n distinct nonzero keys by rank (the key with r larger keys goes
-// to dst[r] when r < F); slots past n are set to 0.  No barrier inside.
+// to dst[r] when r < F); slots past n are set to 0.  No barrier inside.  Up to
+// 64 keys: warp w ranks keys w, w + 8, ..., its lanes comparing keys l and
+// l + 32 against it (two ballots); beyond, a thread per key.
 SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
   for (int i = threadIdx.x; i < F; i += kThreads)
     if (i >= n) dst[i] = 0ull;
+  if (n <= 64) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t a0 = lane < n ? keys[lane] : 0ull, a1 = lane + 32 < n ? keys[lane + 32] : 0ull;
+    for (int i = threadIdx.x >> 5; i < n; i += kWarps) {
+      const uint64_t k = keys[i];
+      const int rank = __popc(__ballot_sync(0xffffffffu, a0 > k)) + __popc(__ballot_sync(0xffffffffu, a1 > k));
+      if (lane == 0 && rank < F) dst[rank] = k;
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < n; i += kThreads) {
     const uint64_t k = keys[i];
     int rank = 0;
@@ -580,11 +618,12 @@ SSD_DEV float warp_round_sums(const float (&pr)[kRounds]) {
   return q;
 }
 
-// One warp: over 256 bucket counts, the bucket where the count from the top
-// bucket down first reaches `need` (sh.ival[5]) and the count in the buckets
-// above it (sh.ival[6]); when the total stays below `need`, bucket 0 and the
-// count above bucket 0.  Lane l holds buckets 255 - 8l down to 248 - 8l.
-SSD_DEV void find_bucket(const uint32_t *hist, int need, Smem &sh) {
+// One warp (every lane returns the result): over 256 bucket counts, the
+// bucket where the count from the top bucket down first reaches `need` and
+// the count in the buckets above it; when the total stays below `need`,
+// bucket 0 and the count above bucket 0.  Lane l holds buckets 255 - 8l down
+// to 248 - 8l.
+SSD_DEV void find_bucket(const uint32_t *hist, int need, uint32_t &bucket_out, int &above_out) {
   const int lane = threadIdx.x & 31;
   const int hi = 255 - 8 * lane;
   const uint4 x = *reinterpret_cast<const uint4 *>(hist + hi - 7);
@@ -607,8 +646,17 @@ SSD_DEV void find_bucket(const uint32_t *hist, int need, Smem &sh) {
     const int src = __ffs(m) - 1;
     if (lane == src) {
       uint32_t run = incl - tot;
-      int k = 0;
-      while (k < 7 && run + c[k] < n) run += c[k++];
+      int k = 7;
+      bool found = false;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (!found && (q == 7 || run + c[q] >= n)) {
+          k = q;
+          found = true;
+        } else if (!found) {
+          run += c[q];
+        }
+      }
       bucket = hi - k;
       above = run;
     }
@@ -617,10 +665,8 @@ SSD_DEV void find_bucket(const uint32_t *hist, int need, Smem &sh) {
   } else {
     above = __shfl_sync(0xffffffffu, incl, 31) - __shfl_sync(0xffffffffu, c[7], 31);
   }
-  if (lane == 0) {
-    sh.ival[5] = bucket;
-    sh.ival[6] = static_cast<int>(above);
-  }
+  bucket_out = static_cast<uint32_t>(bucket);
+  above_out = static_cast<int>(above);
 }
 
 // The chunk's record, block sums and sorted top-F candidate list.
@@ -705,48 +751,70 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
     if (tail_mine) m1 = fmaxf(m1, cv.vmax(cv.nvec));
   }
   const float wm = warp_max(m1);
+  // draft rows with F > 1: the top-F threshold from the thread maxima (its
+  // two counting levels interleaved with pass 2, below)
+  const int F = rs.F;
+  const bool topf = F > 1;
+  const uint32_t mykey = cv.has(tid) ? f2ord(m1) : 0u;
+  const uint32_t k16 = mykey >> 16;
+  if (topf && cv.has(tid)) atomicAdd(&sh.hist[0][k16 >> 8], 1u);
   // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed
   // FMA / ADD; per round the lane's four pairs first, then into the lane's
   // total (the same arithmetic whether or not block sums are kept).  Rows
   // that are drawn from also keep their block sums.
   float s = 0.f;
   BlockRec *br = a.blk + chunk_index(a, b, slot, c);
-  if (!greedy && wm != NEG_INF) {
-    const float Mk = __fmul_rn(wm, kT);
-    const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
-    float tail = 0.f;  // the partial vector's sum, element order
-    if (tail_mine) {
-      float f[E::kVec];
-      cv.get(cv.nvec, f);
+  const bool sums = !greedy && wm != NEG_INF;  // warp-uniform
+  const float Mk = __fmul_rn(wm, kT);
+  const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
+  float tail = 0.f;  // the partial vector's sum, element order
+  if (sums && tail_mine) {
+    float f[E::kVec];
+    cv.get(cv.nvec, f);
 #pragma unroll
-      for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
-    }
-    uint64_t acc = pack2(0.f, 0.f);
-    float pr[kRounds];  // block rows: the lane's sum of each round
+    for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
+  }
+  uint64_t acc = pack2(0.f, 0.f);
+  float pr[kRounds];  // block rows: the lane's sum of each round
+  auto round = [&](int j) {
+    const int v = tid + j * kThreads;
+    pr[j] = 0.f;
+    if (v < cv.nvec) {
+      const uint4 w = cv.v4[v];
+      uint64_t accj = 0;
 #pragma unroll
-    for (int j = 0; j < kRounds; ++j) {
-      const int v = tid + j * kThreads;
-      pr[j] = 0.f;
-      if (v < cv.nvec) {
-        const uint4 w = cv.v4[v];
-        uint64_t accj = 0;
-#pragma unroll
-        for (int h = 0; h < E::kPairs; ++h) {
-          float x0, x1;
-          unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
-          const uint64_t e2 = pack2(ex2(x0), ex2(x1));
-          accj = (h == 0) ? e2 : add2(accj, e2);
-        }
-        acc = add2(acc, accj);
-        if (rs.blocks) {
-          float lo, hi;
-          unpack2(accj, lo, hi);
-          pr[j] = __fadd_rn(lo, hi);
-        }
-      } else if (tail_mine && v == cv.nvec) {
-        pr[j] = tail;
+      for (int h = 0; h < E::kPairs; ++h) {
+        float x0, x1;
+        unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
+        const uint64_t e2 = pack2(ex2(x0), ex2(x1));
+        accj = (h == 0) ? e2 : add2(accj, e2);
       }
+      acc = add2(acc, accj);
+      if (rs.blocks) {
+        float lo, hi;
+        unpack2(accj, lo, hi);
+        pr[j] = __fadd_rn(lo, hi);
+      }
+    } else if (tail_mine && v == cv.nvec) {
+      pr[j] = tail;
     }
+  };
+  if (sums) {
+#pragma unroll
+    for (int j = 0; j < kRounds / 2; ++j) round(j);
+  }
+  uint32_t b1 = 0;
+  int above = 0;
+  if (topf) {
+    // level 1 (every warp, the same result): the top byte of the 16-bit key
+    // prefix; then the thread maxima in that bucket counted by the next byte
+    __syncthreads();
+    find_bucket(sh.hist[0], F, b1, above);
+    if (cv.has(tid) && (k16 >> 8) == b1) atomicAdd(&sh.hist[1][k16 & 0xFFu], 1u);
+  }
+  if (sums) {
+#pragma unroll
+    for (int j = kRounds / 2; j < kRounds; ++j) round(j);
     if (rs.blocks) {
       const float bsum = warp_round_sums(pr);
       if ((lane & 3) == 0) br->bs[lane >> 2][warp] = bsum;
@@ -765,26 +833,17 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
     sh.wa[warp] = wi;
   }
   // top-F candidates: threshold tau with at least F elements reaching it
-  const int F = rs.F;
   uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
-  if (F > 1) {
-    const uint32_t mykey = cv.has(tid) ? f2ord(m1) : 0u;
+  if (topf) {
     // tau: the 16-bit prefix of the F-th largest thread maximum's
-    // order-preserving key (exact for bf16), by two levels of 256-bucket
-    // counts; the chunk's top-F all reach it, and typically little more than
-    // F elements do
-    const uint32_t k16 = mykey >> 16;
-    if (cv.has(tid)) atomicAdd(&sh.hist[0][k16 >> 8], 1u);
+    // order-preserving key (exact for bf16), from the two levels of counts;
+    // the chunk's top-F all reach it, and typically little more than F
+    // elements do
     __syncthreads();
-    if (warp == 0) find_bucket(sh.hist[0], F, sh);
-    __syncthreads();
-    const uint32_t b1 = static_cast<uint32_t>(sh.ival[5]);
-    const int above = sh.ival[6];
-    if (cv.has(tid) && (k16 >> 8) == b1) atomicAdd(&sh.hist[1][k16 & 0xFFu], 1u);
-    __syncthreads();
-    if (warp == 0) find_bucket(sh.hist[1], F - above, sh);
-    __syncthreads();
-    uint32_t tau = ((b1 << 8) | static_cast<uint32_t>(sh.ival[5])) << 16;
+    uint32_t b2 = 0;
+    int above2 = 0;
+    find_bucket(sh.hist[1], F - above, b2, above2);
+    uint32_t tau = ((b1 << 8) | b2) << 16;
     for (int bit = 15; bit >= E::kLowBit; --bit) {  // fp32 rows: the low key bits by radix select
       const uint32_t t = tau | (1u << bit);
       if (__syncthreads_count(mykey >= t) >= F) tau = t;
@@ -1510,6 +1569,15 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
     mbar_arrive_expect_tx(&sh.bar, bulk);
     if (bulk)
       bulk_g2s(buf, row_ptr(a, rs.tensor, b, rs.row, E::kSize) + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
+    // tickets, taken while the copy is in flight: the last CTA of a pair to
+    // start merges the pair, the last pair merger of a sequence to start
+    // finishes the sequence.  Each waits only for CTAs that started before it.
+    int role = 0;
+    if (atomicAdd(pair_tkt(a, b, rs.row), 1u) + 1 == static_cast<uint32_t>(a.pair_chunks[rs.row])) {
+      role = 1;
+      if (a.do_verify && atomicAdd(seq_tkt(a, b), 1u) + 1 == static_cast<uint32_t>(a.npairs)) role = 2;
+    }
+    sh.flag = role;
     if (!mbar_wait_sleep(&sh.bar, 0)) {
       atomicOr(a.status, kFlagWaitTimeout);
       (void)mbar_wait_sleep(&sh.bar, 0);  // the copy still in flight: a second bounded wait before the buffer is read
@@ -1517,22 +1585,36 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
     mark(a, sh.mk, 1);
   }
   __syncthreads();
+  const int role = sh.flag;
   stats_chunk<E>(a, b, slot, c, buf, sh);
-  int kind = 0;
   const int r = rs.row;
-  const bool last_of_pair = arrive_last(pair_ctr(a, b, r), static_cast<uint32_t>(a.pair_chunks[r]), sh);
+  __syncthreads();  // the chunk's records are written
   mark(a, sh.mk, 2);
-  if (last_of_pair) {
-    kind = 1;
+  if (role == 0) {
+    if (tid == 0) red_add_release(pair_pub(a, b, r), 1u);
+  } else {
+    // merge pair r once its other chunks are published
+    if (tid == 0 && !wait_count(pair_pub(a, b, r), static_cast<uint32_t>(a.pair_chunks[r] - 1)))
+      atomicOr(a.status, kFlagWaitTimeout);
+    __syncthreads();
+    mark(a, sh.mk, 3);
     Stage &st = *reinterpret_cast<Stage *>(buf);  // the chunk buffer is free again
     row_finish<E>(a, b, r, st, sh);
     mark(a, sh.mk, 4);
-    if (a.do_verify && arrive_last(seq_ctr(a, b), static_cast<uint32_t>(a.npairs), sh)) {
-      kind = 3;
-      seq_finish<E>(a, b, st, sh);
-      mark(a, sh.mk, 5);
+    if (a.do_verify) {
+      __syncthreads();  // the pair's results are written
+      if (role == 1) {
+        if (tid == 0) red_add_release(seq_pub(a, b), 1u);
+      } else {
+        if (tid == 0 && !wait_count(seq_pub(a, b), static_cast<uint32_t>(a.npairs - 1)))
+          atomicOr(a.status, kFlagWaitTimeout);
+        __syncthreads();
+        seq_finish<E>(a, b, st, sh);
+        mark(a, sh.mk, 5);
+      }
     }
   }
+  const int kind = role == 2 ? 3 : role;
   mark(a, sh.mk, 6);
   if (a.trace && tid == 0)
     trace_entry(a.trace + 8 * (static_cast<size_t>(b) * a.nslots * a.nchunks + rem), kind, b, rem, sh.mk);
