@@ -59,8 +59,7 @@ constexpr int kCandCap = 512;
 constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
-constexpr int kMaxChunks = 128;  // per row: 4 lists per lane in the warp merge
-constexpr int kRankMax = 512;    // lists merged by rank selection up to this many keys
+constexpr int kMaxChunks = 128;  // per row: 4 chunk records per lane in the warp merge
 constexpr int kNone = 0x7fffffff;
 
 struct __align__(16) ChunkStat {
@@ -121,7 +120,7 @@ struct VocabArgs {
                   // chunks published
   ChunkStat *stats;  // [B][nslots][nchunks]
   BlockRec *blk;     // [B][nslots][nchunks]
-  uint64_t *cands;   // [B][nslots][nchunks][Fcap]
+  uint32_t *bmk;     // [B][nslots][nchunks][kBlocks] block maximum keys of top-F rows (0: empty block)
   RowInfo *rows;     // [B][K+1]
   uint64_t *S;       // [B][K+1][Fcap] merged top-F lists
   PosInfo *pos;      // [B][K]
@@ -225,7 +224,7 @@ struct Smem {
   float scal[8];
   int ival[8];
   RowInfo ri;
-  uint64_t cand[kCandCap];  // statistics: top-F candidates; pair merge: the chunk lists
+  uint64_t cand[kCandCap];  // pair merge: candidate block list; sequence finish: the lookup's lists
   float cmass[kMaxChunks];
   float bw[kBlocks];
   uint64_t S[kMaxF];
@@ -239,13 +238,16 @@ struct Smem {
 // What a merge reads of other CTAs' records, staged in shared memory by one
 // round of loads (k_stats: laid over the chunk buffer once the chunk's own
 // statistics are published).
-constexpr int kStageChunks = 64;  // block records staged up to this many chunks per row
+constexpr int kStageChunks = 32;  // block records and block maxima staged up to this many chunks per row
 constexpr int kPayStage = 1024;   // payload words staged
+constexpr int kKeyCap = 512;      // top-F candidate keys of a row merge
 struct Stage {
-  ChunkStat cs[2][kMaxChunks];  // chunk records: target row, draft row
-  BlockRec blk[kStageChunks];   // block records of the row drawn from
-  float z[2][32 * 8];           // target / draft row values of the block a draw located
-  int32_t pay[kPayStage];       // the sequence's cache payload
+  ChunkStat cs[2][kMaxChunks];         // chunk records: target row, draft row
+  BlockRec blk[kStageChunks];          // block records of the row drawn from
+  uint32_t bmk[kStageChunks * kBlocks];  // block maximum keys of the draft row (top-F)
+  float z[2][32 * 8];                  // target / draft row values of the block a draw located
+  int32_t pay[kPayStage];              // the sequence's cache payload
+  uint64_t ck[kKeyCap];                // top-F candidate keys
 };
 static_assert(sizeof(Stage) <= kChunkBytes, "the merge stage must fit the chunk buffer");
 static_assert(sizeof(ChunkStat) == 16 && sizeof(BlockRec) % 16 == 0 && sizeof(RowInfo) == 32 && sizeof(PosInfo) == 16,
@@ -500,73 +502,6 @@ struct ChunkView {
   }
 };
 
-// The chunk's exact top-F into sh.cand (one winner per sweep; used when ties at
-// the threshold overflow the candidate buffer).  Every thread calls.
-template <class E>
-__device__ __noinline__ void collect_exact(const ChunkView<E> cv, int F, Smem &sh) {
-  const int tid = threadIdx.x;
-  uint64_t prev = ~0ull;
-  for (int r = 0; r < F; ++r) {
-    uint64_t best = 0;
-#pragma unroll 1
-    for (int j = 0; j < kRounds; ++j) {
-      const int v = tid + j * kThreads;
-      if (cv.has(v)) {
-        float f[E::kVec];
-        cv.get(v, f);
-#pragma unroll
-        for (int e = 0; e < E::kVec; ++e) {
-          const uint64_t key = (v * E::kVec + e < cv.n) ? cand_key(f[e], cv.e0 + v * E::kVec + e) : 0ull;
-          if (key < prev && key > best) best = key;
-        }
-      }
-    }
-    best = block_max_u64<kThreads>(best, sh.redk);
-    if (tid == 0) sh.cand[r] = best;
-    prev = best;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int k = 0;
-    while (k < F && sh.cand[k] != 0ull) ++k;
-    sh.ncand = k;
-  }
-  __syncthreads();
-}
-
-// Candidates for the top-F: every element whose key reaches tau goes to
-// sh.cand (count sh.ncand, zeroed before the call); past kCandCap (ties at
-// tau), the chunk's exact top-F instead.  `mine`: this thread may hold
-// candidates.  Every thread calls.
-template <class E>
-SSD_DEV void collect(const ChunkView<E> &cv, bool mine, uint32_t tau, int F, Smem &sh) {
-  const int tid = threadIdx.x;
-  if (mine) {
-    // the rounds whose vector reaches tau (independent loads), then those vectors
-    uint32_t rm = 0;
-#pragma unroll
-    for (int j = 0; j < kRounds; ++j) {
-      const int v = tid + j * kThreads;
-      if (cv.has(v) && f2ord(cv.vmax(v)) >= tau) rm |= 1u << j;
-    }
-    while (rm) {
-      const int j = __ffs(rm) - 1;
-      rm &= rm - 1;
-      const int v = tid + j * kThreads;
-      float f[E::kVec];
-      cv.get(v, f);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e)
-        if (v * E::kVec + e < cv.n && f2ord(f[e]) >= tau) {
-          const int p = atomicAdd(&sh.ncand, 1);
-          if (p < kCandCap) sh.cand[p] = cand_key(f[e], cv.e0 + v * E::kVec + e);
-        }
-    }
-  }
-  __syncthreads();
-  if (sh.ncand > kCandCap) collect_exact<E>(cv, F, sh);
-}
-
 // Top-F of n distinct nonzero keys by rank (the key with r larger keys goes
 // to dst[r] when r < F); slots past n are set to 0.  No barrier inside.  Up to
 // 64 keys: warp w ranks keys w, w + 8, ..., its lanes comparing keys l and
@@ -669,7 +604,30 @@ SSD_DEV void find_bucket(const uint32_t *hist, int need, uint32_t &bucket_out, i
   above_out = static_cast<int>(above);
 }
 
-// The chunk's record, block sums and sorted top-F candidate list.
+// The 8 block maximum keys of a warp: vk[j] is this lane's vector key of
+// round j (0: none).  The exchange pattern of warp_round_sums with max; lane
+// l ends with the maximum of round l / 4.
+SSD_DEV uint32_t warp_round_umax(const uint32_t (&vk)[kRounds]) {
+  const int lane = threadIdx.x & 31;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  uint32_t q4[4], q2[2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t keep = b4 ? vk[4 + k] : vk[k], send = b4 ? vk[k] : vk[4 + k];
+    q4[k] = max(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t keep = b3 ? q4[2 + k] : q4[k], send = b3 ? q4[k] : q4[2 + k];
+    q2[k] = max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  uint32_t q = max(b2 ? q2[1] : q2[0], __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4));
+  q = max(q, __shfl_xor_sync(0xffffffffu, q, 2));
+  q = max(q, __shfl_xor_sync(0xffffffffu, q, 1));
+  return q;
+}
+
+// The chunk's record, block sums and (top-F rows) block maximum keys.
 template <class E>
 SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8_t *buf, Smem &sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -691,6 +649,10 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
   // chunk's first element, which is the argmax in the one case a T > 0 draw
   // can fall back to it (a row without finite logits: every chunk max -inf).
   const bool need_arg = greedy || rs.F == 1;
+  // rows with a top-F list (F > 1) publish the maximum key of each block
+  // (round, warp); the pair merge selects the row's top-F from them
+  const bool topf = rs.F > 1;
+  uint32_t vk[kRounds];  // topf rows: this lane's vector key of each round (0: no vector)
   float m1 = NEG_INF;
   int wi = kNone;
   if (need_arg) {
@@ -699,19 +661,14 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
 #pragma unroll
     for (int j = 0; j < kRounds; ++j) {
       const int v = tid + j * kThreads;
-      if (v < cv.nvec) {
+      vk[j] = 0u;
+      if (cv.has(v)) {
         const float vm = cv.vmax(v);
+        if (topf) vk[j] = f2ord(vm);
         if (vm > m1 || j1 < 0) {  // strictly larger: the first vector among equal maxima
           m1 = fmaxf(m1, vm);
           j1 = j;
         }
-      }
-    }
-    if (tail_mine) {
-      const float vm = cv.vmax(cv.nvec);
-      if (vm > m1 || j1 < 0) {
-        m1 = fmaxf(m1, vm);
-        j1 = cv.nvec / kThreads;
       }
     }
     const float wm1 = warp_max(m1);
@@ -735,9 +692,12 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
 #pragma unroll
       for (int j = 0; j < kRounds; ++j) {
         const int v = tid + j * kThreads;
+        vk[j] = 0u;
         if (v < cv.nvec) {
           const uint4 w = cv.v4[v];
-          mm = bmax2(mm, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+          const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+          mm = bmax2(mm, t);
+          if (topf) vk[j] = f2ord(fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u)));
         }
       }
       m1 = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
@@ -745,76 +705,71 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
 #pragma unroll
       for (int j = 0; j < kRounds; ++j) {
         const int v = tid + j * kThreads;
-        if (v < cv.nvec) m1 = fmaxf(m1, cv.vmax(v));
+        vk[j] = 0u;
+        if (v < cv.nvec) {
+          const float vm = cv.vmax(v);
+          m1 = fmaxf(m1, vm);
+          if (topf) vk[j] = f2ord(vm);
+        }
       }
     }
-    if (tail_mine) m1 = fmaxf(m1, cv.vmax(cv.nvec));
+    if (tail_mine) {
+      const float vm = cv.vmax(cv.nvec);
+      m1 = fmaxf(m1, vm);
+      if (topf) {
+#pragma unroll
+        for (int j = 0; j < kRounds; ++j)
+          if (j == cv.nvec / kThreads) vk[j] = f2ord(vm);
+      }
+    }
+  }
+  if (topf) {
+    const uint32_t key = warp_round_umax(vk);
+    if ((lane & 3) == 0) a.bmk[chunk_index(a, b, slot, c) * kBlocks + (lane >> 2) * kWarps + warp] = key;
   }
   const float wm = warp_max(m1);
-  // draft rows with F > 1: the top-F threshold from the thread maxima (its
-  // two counting levels interleaved with pass 2, below)
-  const int F = rs.F;
-  const bool topf = F > 1;
-  const uint32_t mykey = cv.has(tid) ? f2ord(m1) : 0u;
-  const uint32_t k16 = mykey >> 16;
-  if (topf && cv.has(tid)) atomicAdd(&sh.hist[0][k16 >> 8], 1u);
   // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed
   // FMA / ADD; per round the lane's four pairs first, then into the lane's
   // total (the same arithmetic whether or not block sums are kept).  Rows
   // that are drawn from also keep their block sums.
   float s = 0.f;
   BlockRec *br = a.blk + chunk_index(a, b, slot, c);
-  const bool sums = !greedy && wm != NEG_INF;  // warp-uniform
-  const float Mk = __fmul_rn(wm, kT);
-  const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
-  float tail = 0.f;  // the partial vector's sum, element order
-  if (sums && tail_mine) {
-    float f[E::kVec];
-    cv.get(cv.nvec, f);
+  if (!greedy && wm != NEG_INF) {
+    const float Mk = __fmul_rn(wm, kT);
+    const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
+    float tail = 0.f;  // the partial vector's sum, element order
+    if (tail_mine) {
+      float f[E::kVec];
+      cv.get(cv.nvec, f);
 #pragma unroll
-    for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
-  }
-  uint64_t acc = pack2(0.f, 0.f);
-  float pr[kRounds];  // block rows: the lane's sum of each round
-  auto round = [&](int j) {
-    const int v = tid + j * kThreads;
-    pr[j] = 0.f;
-    if (v < cv.nvec) {
-      const uint4 w = cv.v4[v];
-      uint64_t accj = 0;
-#pragma unroll
-      for (int h = 0; h < E::kPairs; ++h) {
-        float x0, x1;
-        unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
-        const uint64_t e2 = pack2(ex2(x0), ex2(x1));
-        accj = (h == 0) ? e2 : add2(accj, e2);
-      }
-      acc = add2(acc, accj);
-      if (rs.blocks) {
-        float lo, hi;
-        unpack2(accj, lo, hi);
-        pr[j] = __fadd_rn(lo, hi);
-      }
-    } else if (tail_mine && v == cv.nvec) {
-      pr[j] = tail;
+      for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
     }
-  };
-  if (sums) {
+    uint64_t acc = pack2(0.f, 0.f);
+    float pr[kRounds];  // block rows: the lane's sum of each round
 #pragma unroll
-    for (int j = 0; j < kRounds / 2; ++j) round(j);
-  }
-  uint32_t b1 = 0;
-  int above = 0;
-  if (topf) {
-    // level 1 (every warp, the same result): the top byte of the 16-bit key
-    // prefix; then the thread maxima in that bucket counted by the next byte
-    __syncthreads();
-    find_bucket(sh.hist[0], F, b1, above);
-    if (cv.has(tid) && (k16 >> 8) == b1) atomicAdd(&sh.hist[1][k16 & 0xFFu], 1u);
-  }
-  if (sums) {
+    for (int j = 0; j < kRounds; ++j) {
+      const int v = tid + j * kThreads;
+      pr[j] = 0.f;
+      if (v < cv.nvec) {
+        const uint4 w = cv.v4[v];
+        uint64_t accj = 0;
 #pragma unroll
-    for (int j = kRounds / 2; j < kRounds; ++j) round(j);
+        for (int h = 0; h < E::kPairs; ++h) {
+          float x0, x1;
+          unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
+          const uint64_t e2 = pack2(ex2(x0), ex2(x1));
+          accj = (h == 0) ? e2 : add2(accj, e2);
+        }
+        acc = add2(acc, accj);
+        if (rs.blocks) {
+          float lo, hi;
+          unpack2(accj, lo, hi);
+          pr[j] = __fadd_rn(lo, hi);
+        }
+      } else if (tail_mine && v == cv.nvec) {
+        pr[j] = tail;
+      }
+    }
     if (rs.blocks) {
       const float bsum = warp_round_sums(pr);
       if ((lane & 3) == 0) br->bs[lane >> 2][warp] = bsum;
@@ -831,25 +786,6 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
     sh.wm[warp] = wm;
     sh.ws[warp] = s;
     sh.wa[warp] = wi;
-  }
-  // top-F candidates: threshold tau with at least F elements reaching it
-  uint64_t *out = a.cands + chunk_index(a, b, slot, c) * a.Fcap;
-  if (topf) {
-    // tau: the 16-bit prefix of the F-th largest thread maximum's
-    // order-preserving key (exact for bf16), from the two levels of counts;
-    // the chunk's top-F all reach it, and typically little more than F
-    // elements do
-    __syncthreads();
-    uint32_t b2 = 0;
-    int above2 = 0;
-    find_bucket(sh.hist[1], F - above, b2, above2);
-    uint32_t tau = ((b1 << 8) | b2) << 16;
-    for (int bit = 15; bit >= E::kLowBit; --bit) {  // fp32 rows: the low key bits by radix select
-      const uint32_t t = tau | (1u << bit);
-      if (__syncthreads_count(mykey >= t) >= F) tau = t;
-    }
-    collect<E>(cv, cv.has(tid) && mykey >= tau, tau, F, sh);
-    rank_select(sh.cand, sh.ncand, F, out);
   }
   __syncthreads();
   if (warp == 0) {
@@ -868,9 +804,7 @@ SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8
 #pragma unroll
     for (int o = kWarps / 2; o; o >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
     if (lane == 0) {
-      sh.ncand = 0;  // for the next chunk's candidates
       if (amax == kNone) amax = 0;  // an all -inf chunk: its first index
-      if (F == 1) out[0] = cand_key(M, cv.e0 + amax);
       a.stats[chunk_index(a, b, slot, c)] = ChunkStat{M, S, cv.e0 + amax, 0};
     }
   }
@@ -924,45 +858,6 @@ SSD_DEV RowStat merge_row_warp(const VocabArgs &a, const ChunkStat *rec) {
     sum = warp_sum(sum);
   }
   return RowStat{m, sum, am == kNone ? 0 : am};
-}
-
-// Warp-cooperative k-way merge of the sorted per-chunk candidate lists (list
-// c at lists[c * stride], F keys each, published by other CTAs) into the
-// top-F list `dst` (descending keys; sentinel 0 past the end).  Used when the
-// lists hold more than kRankMax keys.
-SSD_DEV void merge_topf(const uint64_t *lists, size_t stride, int nchunks, int F, uint64_t *dst) {
-  constexpr int L = kMaxChunks / 32;
-  const int lane = threadIdx.x & 31;
-  int ptr[L];
-  uint64_t head[L];
-#pragma unroll
-  for (int l = 0; l < L; ++l) {
-    const int c = lane + 32 * l;
-    ptr[l] = 0;
-    head[l] = (c < nchunks && F > 0) ? ldcg_key(lists + c * stride) : 0ull;
-  }
-  for (int r = 0; r < F; ++r) {
-    uint64_t best = 0;
-    int bl = -1;
-#pragma unroll
-    for (int l = 0; l < L; ++l)
-      if (head[l] > best) {
-        best = head[l];
-        bl = l;
-      }
-    const uint64_t win = warp_max_u64(best);
-    if (lane == 0) dst[r] = win;
-    if (win != 0 && best == win && bl >= 0) {
-#pragma unroll
-      for (int l = 0; l < L; ++l)
-        if (l == bl) {
-          const int c = lane + 32 * l;
-          ++ptr[l];
-          head[l] = (ptr[l] < F) ? ldcg_key(lists + c * stride + ptr[l]) : 0ull;
-        }
-    }
-  }
-  __syncwarp();
 }
 
 SSD_DEV float norm_N(float C, float sq) { return __fsub_rn(1.f, __fmul_rn(__fsub_rn(1.f, C), sq)); }
@@ -1154,6 +1049,105 @@ SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64
 }
 
 // ===========================================================================
+// the row's top-F from its block maximum keys
+// ===========================================================================
+// The elements (value descending, index ascending) of block `blk` (chunk
+// blk / kBlocks, round, warp) that this lane reads: its 16-byte vector.
+template <class E>
+SSD_DEV void block_vec(const VocabArgs &a, const char *row, int blk, float *f, int *i0, int *n) {
+  const int lane = threadIdx.x & 31;
+  const int c = blk / kBlocks, k = blk - c * kBlocks;
+  const int e0 = c * a.chunk_elems;
+  *n = min(a.chunk_elems, a.V - e0) + e0;
+  *i0 = e0 + ((k / kWarps) * kThreads + (k % kWarps) * 32 + lane) * E::kVec;
+  ld_vec<E>(row, e0, *n - e0, *i0 - e0, -__int_as_float(0x7f800000), f);
+}
+
+// The top-F (F > 1) of a draft row into sh.S (descending; zeros past the
+// row's elements).  t16 = the 16-bit key prefix of the F-th largest block
+// maximum (two levels of 256-bucket counts): at least F elements reach it,
+// so the row's top-F all lie in blocks whose maximum does.  Those blocks are
+// read again (one warp per block) and their elements reaching t16 ranked;
+// when ties overflow the buffers, F sweeps of a CTA-wide maximum instead.
+// sh.hist, sh.ncand and sh.ival[7] start at zero.  Every thread calls.
+template <class E>
+SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t *bmk, bool staged, Stage &st,
+                      Smem &sh) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nb = a.nchunks * kBlocks;
+  auto key_at = [&](int i) -> uint32_t { return staged ? bmk[i] : __ldcg(bmk + i); };
+  for (int i = tid; i < nb; i += kThreads) {
+    const uint32_t k = key_at(i);
+    if (k) atomicAdd(&sh.hist[0][k >> 24], 1u);
+  }
+  __syncthreads();
+  uint32_t b1, b2;
+  int above, above2;
+  find_bucket(sh.hist[0], F, b1, above);
+  for (int i = tid; i < nb; i += kThreads) {
+    const uint32_t k = key_at(i);
+    if (k && (k >> 24) == b1) atomicAdd(&sh.hist[1][(k >> 16) & 0xFFu], 1u);
+  }
+  __syncthreads();
+  find_bucket(sh.hist[1], F - above, b2, above2);
+  const uint32_t t16 = (b1 << 8) | b2;
+  // the candidate blocks
+  constexpr int kListCap = kCandCap * 2;
+  int *blist = reinterpret_cast<int *>(sh.cand);
+  for (int i = tid; i < nb; i += kThreads) {
+    const uint32_t k = key_at(i);
+    if (k && (k >> 16) >= t16) {
+      const int p = atomicAdd(&sh.ival[7], 1);
+      if (p < kListCap) blist[p] = i;
+    }
+  }
+  __syncthreads();
+  const int nbl = sh.ival[7];
+  const bool listed = nbl <= kListCap;
+  if (listed) {
+    for (int q = warp; q < nbl; q += kWarps) {
+      float f[E::kVec];
+      int i0, n;
+      block_vec<E>(a, row, blist[q], f, &i0, &n);
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e)
+        if (i0 + e < n && (f2ord(f[e]) >> 16) >= t16) {
+          const int p = atomicAdd(&sh.ncand, 1);
+          if (p < kKeyCap) st.ck[p] = cand_key(f[e], i0 + e);
+        }
+    }
+  }
+  __syncthreads();
+  const int nc = sh.ncand;
+  if (listed && nc <= kKeyCap) {
+    rank_select(st.ck, nc, F, sh.S);
+  } else {
+    // ties at the threshold: one winner per sweep over the candidate blocks
+    // (every block when they overflow the list)
+    const int nq = listed ? nbl : nb;
+    uint64_t prev = ~0ull;
+    for (int r = 0; r < F; ++r) {
+      uint64_t best = 0ull;
+      for (int q = warp; q < nq; q += kWarps) {
+        float f[E::kVec];
+        int i0, n;
+        block_vec<E>(a, row, listed ? blist[q] : q, f, &i0, &n);
+#pragma unroll
+        for (int e = 0; e < E::kVec; ++e) {
+          if (i0 + e >= n || (f2ord(f[e]) >> 16) < t16) continue;
+          const uint64_t key = cand_key(f[e], i0 + e);
+          if (key < prev && key > best) best = key;
+        }
+      }
+      best = block_max_u64<kThreads>(best, sh.redk);
+      if (tid == 0) sh.S[r] = best;
+      prev = best;
+    }
+  }
+  __syncthreads();
+}
+
+// ===========================================================================
 // pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
 // ===========================================================================
 template <class E>
@@ -1168,15 +1162,17 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
   const bool draws = r < a.K && a.do_sample && !a.greedy && ds >= 0;
   const bool stage_blk = draws && a.slot[ds].blocks && a.nchunks <= kStageChunks;
   const bool given = r < a.K && !a.do_sample && a.do_verify;  // verification of tokens the caller drew
-  // one round of loads: the draft's candidate lists, both rows' chunk records,
-  // the block records of a row drawn from and (tokens given) the token with
-  // its two logits
-  uint64_t *lists = sh.cand;
-  const int nl = a.nchunks * F;
-  const bool by_rank = nl <= kRankMax;
-  if (F > 0 && by_rank) {
-    const uint64_t *src = a.cands + chunk_index(a, b, ds, 0) * a.Fcap;
-    for (int i = tid; i < nl; i += kThreads) cp_async8(&lists[i], src + static_cast<size_t>(i / F) * a.Fcap + (i % F));
+  const bool stage_bmk = F > 1 && a.nchunks <= kStageChunks;
+  // one round of loads: both rows' chunk records, the draft row's block
+  // maximum keys (top-F), the block records of a row drawn from and (tokens
+  // given) the token with its two logits
+  const uint32_t *gbmk = a.bmk + chunk_index(a, b, ds, 0) * kBlocks;
+  if (stage_bmk)
+    for (int i = tid; i < a.nchunks * (kBlocks / 4); i += kThreads)
+      cp_async16(reinterpret_cast<int4 *>(st.bmk) + i, reinterpret_cast<const int4 *>(gbmk) + i);
+  if (F > 1) {
+    sh.hist[0][tid] = 0u;
+    sh.hist[1][tid] = 0u;
   }
   for (int c = tid; c < a.nchunks; c += kThreads) {
     if (ts >= 0) cp_async16(&st.cs[0][c], a.stats + chunk_index(a, b, ts, c));
@@ -1190,6 +1186,8 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
   }
   if (tid == 0) {
     memset(&sh.ri, 0, sizeof(sh.ri));
+    sh.ncand = 0;
+    sh.ival[7] = 0;
     if (given) {
       const int d = a.d_in[static_cast<size_t>(b) * a.K + r];
       sh.ival[2] = d;
@@ -1201,8 +1199,8 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
   }
   cp_async_wait_all();
   __syncthreads();
-  // the last two warps merge the target and draft rows' chunk records while
-  // the first ones rank the candidate lists
+  // the last two warps merge the target and draft rows' chunk records; all
+  // warps then select the draft row's top-F
   if (warp == kWarps - 2 && ts >= 0) {
     const RowStat t = merge_row_warp(a, st.cs[0]);
     if (lane == 0) {
@@ -1219,37 +1217,10 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
       sh.ri.ad = d.amax;
     }
   }
-  if (F > 0) {
-    if (by_rank) {
-      // a key's rank: its place in its own list (sorted descending, zeros
-      // past the end) plus, per other list, the count of larger keys (binary
-      // search); zero keys (a chunk with fewer than F elements) take no rank
-      for (int i = tid; i < nl; i += kThreads) {
-        const uint64_t k = lists[i];
-        if (k == 0ull) continue;
-        const int own = i / F;
-        int rank = i - own * F;
-        for (int c = 0; c < a.nchunks && rank < F; ++c) {
-          if (c == own) continue;
-          const uint64_t *Lc = lists + c * F;
-          int lo = 0, hi = F;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (Lc[mid] > k) lo = mid + 1;
-            else hi = mid;
-          }
-          rank += lo;
-        }
-        if (rank < F) sh.S[rank] = k;
-      }
-      int nz = 0;
-      for (int i0 = 0; i0 < nl; i0 += kThreads) nz += __syncthreads_count(i0 + tid < nl && lists[i0 + tid] != 0ull);
-      for (int i = nz + tid; i < F; i += kThreads) sh.S[i] = 0ull;
-    } else if (warp == 2) {
-      merge_topf(a.cands + chunk_index(a, b, ds, 0) * a.Fcap, a.Fcap, a.nchunks, F, sh.S);
-    }
-  }
+  if (F > 1) row_topf<E>(a, rowD, F, stage_bmk ? st.bmk : gbmk, stage_bmk, st, sh);
   __syncthreads();
+  if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.ri.md, sh.ri.ad);  // the top-1: the row's argmax
+  if (F == 1) __syncthreads();
   if (a.do_verify || a.do_lookup)
     for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
   const float mdk = __fmul_rn(sh.ri.md, a.kT);
@@ -1552,9 +1523,6 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
   const int b = a.b0 + static_cast<int>(blockIdx.z);
   const int rem = slot * a.nchunks + c;
   const RowSlot rs = a.slot[slot];
-  if (tid == 0) sh.ncand = 0;
-  sh.hist[0][tid] = 0u;
-  sh.hist[1][tid] = 0u;
   // the chunk's whole vectors: one TMA bulk copy; thread 0 waits (bounded,
   // sleeping between polls), the other threads at the barrier
   if (tid == 0) {
@@ -1821,7 +1789,7 @@ namespace {
 struct Layout {
   int nslots, nchunks, chunk_elems, Fcap;
   size_t ctr_words;
-  size_t ctr_off, stats_off, blk_off, cands_off, rows_off, S_off, pos_off, rmass_off, rbs_off, accs_off, total;
+  size_t ctr_off, stats_off, blk_off, bmk_off, rows_off, S_off, pos_off, rmass_off, rbs_off, accs_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1850,8 +1818,8 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + nrec * sizeof(ChunkStat), 256);
   L->blk_off = o;
   o = align_up(o + nrec * sizeof(BlockRec), 256);
-  L->cands_off = o;
-  o = align_up(o + nrec * L->Fcap * sizeof(uint64_t), 256);
+  L->bmk_off = o;
+  o = align_up(o + nrec * kBlocks * sizeof(uint32_t), 256);
   L->rows_off = o;
   o = align_up(o + Bn * (K + 1) * sizeof(RowInfo), 256);
   L->S_off = o;
@@ -1924,7 +1892,7 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   char *w = static_cast<char *>(ws);
   a.ctr = reinterpret_cast<uint32_t *>(w + L.ctr_off);
   a.stats = reinterpret_cast<ChunkStat *>(w + L.stats_off);
-  a.cands = reinterpret_cast<uint64_t *>(w + L.cands_off);
+  a.bmk = reinterpret_cast<uint32_t *>(w + L.bmk_off);
   a.rows = reinterpret_cast<RowInfo *>(w + L.rows_off);
   a.S = reinterpret_cast<uint64_t *>(w + L.S_off);
   a.pos = reinterpret_cast<PosInfo *>(w + L.pos_off);
