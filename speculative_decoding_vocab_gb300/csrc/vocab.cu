@@ -114,9 +114,10 @@ struct VocabArgs {
   int foff[kMaxK + 2];
   // workspace
   uint32_t *ctr;  // [0] finished sequences, [1] hits; per sequence b: [2+b] pair-merge
-                  // tickets, [2+B+b] merged pairs published, [2+2B+b] residual units
-                  // done, [2+3B+b] ready word (accs[b] + 2 once published); per pair
-                  // (b, r): [2+4B + b(K+1)+r] chunk tickets, [2+4B+B(K+1) + b(K+1)+r]
+                  // tickets, [2+B+b] merged pairs published, [2+2B+b] residual unit
+                  // tickets, [2+3B+b] ready word (accs[b] + 2 once published),
+                  // [2+4B+b] residual units published; per pair (b, r):
+                  // [2+5B + b(K+1)+r] chunk tickets, [2+5B+B(K+1) + b(K+1)+r]
                   // chunks published
   ChunkStat *stats;  // [B][nslots][nchunks]
   BlockRec *blk;     // [B][nslots][nchunks]
@@ -145,15 +146,16 @@ struct VocabArgs {
 
 SSD_DEV uint32_t *seq_tkt(const VocabArgs &a, int b) { return a.ctr + 2 + b; }
 SSD_DEV uint32_t *seq_pub(const VocabArgs &a, int b) { return a.ctr + 2 + a.B + b; }
-SSD_DEV uint32_t *res_ctr(const VocabArgs &a, int b) { return a.ctr + 2 + 2 * a.B + b; }
+SSD_DEV uint32_t *res_tkt(const VocabArgs &a, int b) { return a.ctr + 2 + 2 * a.B + b; }
 SSD_DEV uint32_t *ready_word(const VocabArgs &a, int b) { return a.ctr + 2 + 3 * a.B + b; }
+SSD_DEV uint32_t *res_pub(const VocabArgs &a, int b) { return a.ctr + 2 + 4 * a.B + b; }
 SSD_DEV uint32_t *pair_tkt(const VocabArgs &a, int b, int r) {
-  return a.ctr + 2 + 4 * static_cast<size_t>(a.B) + static_cast<size_t>(b) * (a.K + 1) + r;
+  return a.ctr + 2 + 5 * static_cast<size_t>(a.B) + static_cast<size_t>(b) * (a.K + 1) + r;
 }
 SSD_DEV uint32_t *pair_pub(const VocabArgs &a, int b, int r) {
   return pair_tkt(a, b, r) + static_cast<size_t>(a.B) * (a.K + 1);
 }
-__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 4 * B + 2 * B * (K + 1); }
+__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 5 * B + 2 * B * (K + 1); }
 
 __host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
   return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
@@ -252,22 +254,6 @@ struct Stage {
 static_assert(sizeof(Stage) <= kChunkBytes, "the merge stage must fit the chunk buffer");
 static_assert(sizeof(ChunkStat) == 16 && sizeof(BlockRec) % 16 == 0 && sizeof(RowInfo) == 32 && sizeof(PosInfo) == 16,
               "records are copied in 16-byte pieces");
-
-// Every thread calls after writing its part of a published result.  True, in
-// every thread of the CTA, for the arrival that completes `total` arrivals on
-// *ctr; the results published before the earlier arrivals are then visible
-// (release / acquire through the counter, ordered with the CTA's own writes by
-// the barrier).
-SSD_DEV bool arrive_last(uint32_t *ctr, uint32_t total, Smem &sh) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const bool last = atom_add_release(ctr, 1u) + 1 == total;
-    if (last) fence_acq_rel();
-    sh.flag = last ? 1 : 0;
-  }
-  __syncthreads();
-  return sh.flag != 0;
-}
 
 // Thread 0: bounded wait (sleeping between polls) until *ctr reaches `target`,
 // then an acquire; false when the wait ran out.  Used only for counts that
@@ -1362,7 +1348,18 @@ SSD_DEV bool pay_staged(const VocabArgs &a) {
 // residual unit masses (`umass`) and target row K's chunk and block records
 // for the bonus draw (`st`).  Then the acceptance chain (thread 0).  Every
 // thread returns the accept count.
+SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, Smem &sh);
+SSD_DEV int stage_complete(const VocabArgs &a, Smem &sh);
 SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, Stage *st, Smem &sh) {
+  stage_issue(a, b, pay, st, sh);
+  if (umass) {
+    const int nu = a.nchunks * kQuarters;
+    for (int q = threadIdx.x; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
+  }
+  return stage_complete(a, sh);
+}
+// The loads of stage_chain but the unit masses, issued (cp.async) without a wait.
+SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, Smem &sh) {
   const int tid = threadIdx.x;
   const size_t r0 = static_cast<size_t>(b) * (a.K + 1);
   for (int t = tid; t < a.K; t += kThreads) {
@@ -1375,10 +1372,6 @@ SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, S
     const int F = a.Fs[r];
     if (F > 0) cp_async8(&sh.keyF[r], a.S + (r0 + r) * a.Fcap + F - 1);
     else sh.keyF[r] = 0ull;
-  }
-  if (umass) {
-    const int nu = a.nchunks * kQuarters;
-    for (int q = tid; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
   }
   if (lists_staged(a)) {
     const int nS = a.foff[a.K + 1];
@@ -1403,6 +1396,11 @@ SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, S
       for (int i = tid; i < a.nchunks * kW; i += kThreads) cp_async16(dst + i, src + i);
     }
   }
+}
+// Waits for the staged loads, then the acceptance chain; every thread returns
+// the accept count.
+SSD_DEV int stage_complete(const VocabArgs &a, Smem &sh) {
+  const int tid = threadIdx.x;
   cp_async_wait_all();
   __syncthreads();
   if (tid == 0) {
@@ -1606,10 +1604,13 @@ SSD_DEV uint32_t wait_ready(const uint32_t *w) {
 
 // Residual unit (sequence b, chunk c, quarter g = rounds 2g, 2g+1): once the
 // sequence's acceptance chain has run, its block sums of max(0, p - q') over
-// target and draft row a, read straight from global memory; the last unit of
-// the sequence draws the bonus.
+// target and draft row a, read straight from global memory.  The unit with the
+// sequence's last ticket draws the bonus once the others are published; it
+// issues its staging loads before its own unit.  `rbst`: the sequence's
+// residual block sums, staged for up to kResidStage chunks.
+constexpr int kResidStage = 16;
 template <class E>
-SSD_DEV void resid_unit(const VocabArgs &a, float *umass, int32_t *pay, Smem &sh) {
+SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *pay, Smem &sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nu = a.nchunks * kQuarters;
   const int b = static_cast<int>(blockIdx.x / nu);
@@ -1618,12 +1619,16 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, int32_t *pay, Smem &sh
   if (tid == 0) {
     const uint32_t v = wait_ready(ready_word(a, b));
     if (!v) atomicOr(a.status, kFlagWaitTimeout);
+    const int acc0 = static_cast<int>(v) - 2;
     sh.flag = static_cast<int>(v);
+    sh.ival[2] = (v && acc0 >= 0 && acc0 < a.K && atomicAdd(res_tkt(a, b), 1u) + 1 == static_cast<uint32_t>(nu)) ? 1 : 0;
   }
   __syncthreads();
   if (!sh.flag) return;
   const int acc = sh.flag - 2;
   if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
+  const bool fin = sh.ival[2] != 0;
+  if (fin) stage_issue(a, b, pay, nullptr, sh);
   if (tid == 0 && a.trace)
     for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
   mark(a, sh.mk, 0);
@@ -1666,10 +1671,22 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, int32_t *pay, Smem &sh
   }
   mark(a, sh.mk, 2);
   int kind = 2;
-  if (arrive_last(res_ctr(a, b), static_cast<uint32_t>(nu), sh)) {
+  __syncthreads();  // the unit's sums are written
+  if (!fin) {
+    if (tid == 0) red_add_release(res_pub(a, b), 1u);
+  } else {
     kind = 3;
+    if (tid == 0 && !wait_count(res_pub(a, b), static_cast<uint32_t>(nu - 1))) atomicOr(a.status, kFlagWaitTimeout);
+    __syncthreads();
     mark(a, sh.mk, 3);
-    const int acc2 = stage_chain(a, b, umass, pay, nullptr, sh);  // the same chain: acc2 == acc
+    // the unit masses and (up to kResidStage chunks) every unit's block sums
+    for (int q = tid; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
+    const bool rbs_staged = a.nchunks <= kResidStage;
+    if (rbs_staged) {
+      const int4 *src = reinterpret_cast<const int4 *>(a.rbs + static_cast<size_t>(b) * a.nchunks * kBlocks);
+      for (int i = tid; i < a.nchunks * (kBlocks / 4); i += kThreads) cp_async16(reinterpret_cast<int4 *>(rbst) + i, src + i);
+    }
+    const int acc2 = stage_complete(a, sh);  // the same chain: acc2 == acc
     const RowInfo ra = sh.rows[acc2];
     const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
     const float ub = a.u_bonus[b];
@@ -1685,9 +1702,9 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, int32_t *pay, Smem &sh
         sh.scal[6] = W;
       }
       if (uq >= 0) {
-        const float *src = a.rbs + (static_cast<size_t>(b) * a.nchunks + uq / kQuarters) * kBlocks +
-                           2 * (uq % kQuarters) * kWarps;
-        if (lane < 2 * kWarps) sh.bw[lane] = __ldcg(src + lane);
+        const size_t o = (static_cast<size_t>(uq / kQuarters)) * kBlocks + 2 * (uq % kQuarters) * kWarps;
+        if (lane < 2 * kWarps)
+          sh.bw[lane] = rbs_staged ? rbst[o + lane] : __ldcg(a.rbs + static_cast<size_t>(b) * a.nchunks * kBlocks + o + lane);
         __syncwarp();
         locate(sh.bw, 2 * kWarps, local, true, sh);
         __syncwarp();
@@ -1731,7 +1748,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ V
   __shared__ Smem sh;
   __shared__ float umass[kMaxChunks * kQuarters];  // the sequence's unit masses (final draw)
   __shared__ int32_t pay[kPayStage];                // the sequence's cache payload (final draw)
-  resid_unit<E>(a, umass, pay, sh);
+  __shared__ __align__(16) float rbst[kResidStage * kBlocks];  // the sequence's residual block sums (final draw)
+  resid_unit<E>(a, umass, rbst, pay, sh);
   // the grid completes only after k_stats has: its first CTA waits for it
   // before exiting
   if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
