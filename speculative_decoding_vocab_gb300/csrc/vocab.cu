@@ -37,6 +37,7 @@
 //            for its own sequence's acceptance chain (a ready word).
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -219,7 +220,7 @@ SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
 struct Smem {
   uint64_t bar;  // k_stats: completion of the chunk's TMA copy
   int flag, ncand;
-  uint32_t hist[2][256];  // top-F threshold: counts of thread maxima by key byte
+  alignas(16) uint32_t hist[2][256];  // top-F threshold: block maxima counted by key byte (read as 16-byte vectors)
   float wm[kWarps], ws[kWarps];
   int wa[kWarps];
   uint64_t redk[kWarps];
@@ -252,6 +253,8 @@ struct Stage {
   uint64_t ck[kKeyCap];                // top-F candidate keys
 };
 static_assert(sizeof(Stage) <= kChunkBytes, "the merge stage must fit the chunk buffer");
+static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Stage, bmk) % 16 == 0 && offsetof(Stage, blk) % 16 == 0,
+              "shared arrays read or copied in 16-byte pieces");
 static_assert(sizeof(ChunkStat) == 16 && sizeof(BlockRec) % 16 == 0 && sizeof(RowInfo) == 32 && sizeof(PosInfo) == 16,
               "records are copied in 16-byte pieces");
 
