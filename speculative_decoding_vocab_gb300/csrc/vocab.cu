@@ -119,7 +119,7 @@ struct VocabArgs {
                   // tickets, [2+3B+b] ready word (accs[b] + 2 once published),
                   // [2+4B+b] residual units published; per pair (b, r):
                   // [2+5B + b(K+1)+r] chunk tickets, [2+5B+B(K+1) + b(K+1)+r]
-                  // chunks published
+                  // chunks published, [2+5B+2B(K+1) + b(K+1)+r] position verdict
   ChunkStat *stats;  // [B][nslots][nchunks]
   BlockRec *blk;     // [B][nslots][nchunks]
   uint32_t *bmk;     // [B][nslots][nchunks][kBlocks] block maximum keys of top-F rows (0: empty block)
@@ -156,7 +156,12 @@ SSD_DEV uint32_t *pair_tkt(const VocabArgs &a, int b, int r) {
 SSD_DEV uint32_t *pair_pub(const VocabArgs &a, int b, int r) {
   return pair_tkt(a, b, r) + static_cast<size_t>(a.B) * (a.K + 1);
 }
-__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 5 * B + 2 * B * (K + 1); }
+// Verification of position r of sequence b, once its pair is merged: 1
+// accepted, 2 rejected (0: not yet known).
+SSD_DEV uint32_t *pos_verdict(const VocabArgs &a, int b, int r) {
+  return pair_tkt(a, b, r) + 2 * static_cast<size_t>(a.B) * (a.K + 1);
+}
+__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 5 * B + 3 * B * (K + 1); }
 
 __host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
   return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
@@ -1332,6 +1337,27 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
     }
   }
   if (tid == 0) a.rows[rr] = ri;
+  if (a.do_verify && !a.greedy && r < a.K) {
+    // the position's verdict, then the frontier: once the positions before
+    // the first rejection are all accepted, the residual draw may start
+    // (ready word = rejected position + 2) without waiting for the sequence's
+    // remaining pairs
+    __syncthreads();  // the pair's results are written
+    if (tid == 0) {
+      const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + r);
+      const bool ok = pi.p >= 0.f && __fmul_rn(a.u_acc[static_cast<size_t>(b) * a.K + r], pi.q) < pi.p;
+      st_release(pos_verdict(a, b, r), ok ? 1u : 2u);
+      for (int j = 0; j < a.K; ++j) {
+        const uint32_t v = ld_relaxed(pos_verdict(a, b, j));
+        if (v == 1u) continue;
+        if (v == 2u) {
+          fence_acq_rel();  // the verdicts (and results) of positions 0..j, then the ready word
+          atomicCAS(ready_word(a, b), 0u, static_cast<uint32_t>(j + 2));
+        }
+        break;
+      }
+    }
+  }
 }
 
 // ===========================================================================
@@ -1479,8 +1505,10 @@ __device__ __forceinline__ void seq_finish(const VocabArgs &a, int b, Stage &st,
   const bool resid = !a.greedy && acc < a.K;
   if (threadIdx.x == 0) {
     a.accs[b] = resid ? acc : -1;
-    // the sequence's k_resid CTAs may go on; the word carries accs[b] + 2
-    st_release(ready_word(a, b), static_cast<uint32_t>((resid ? acc : -1) + 2));
+    // the sequence's k_resid CTAs may go on (unless a pair merge's frontier
+    // already set the word: to the same value); the word carries accs[b] + 2
+    fence_acq_rel();
+    atomicCAS(ready_word(a, b), 0u, static_cast<uint32_t>((resid ? acc : -1) + 2));
   }
   if (resid) return;
   const RowInfo row = sh.rows[acc];
