@@ -1211,39 +1211,51 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
       sh.ri.ad = d.amax;
     }
   }
-  if (F > 1) row_topf<E>(a, rowD, F, stage_bmk ? st.bmk : gbmk, stage_bmk, st, sh);
-  __syncthreads();
-  if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.ri.md, sh.ri.ad);  // the top-1: the row's argmax
-  if (F == 1) __syncthreads();
-  if (a.do_verify || a.do_lookup)
-    for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
-  const float mdk = __fmul_rn(sh.ri.md, a.kT);
-  // the draft's normalised mass on S: lane-strided partial sums, a fixed tree
-  if (warp == 0) {
-    float sq = 0.f;
-    if (!a.greedy && sh.ri.md != NEG_INF) {
-      for (int i = lane; i < F; i += 32)
-        if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
-      sq = __fdiv_rn(warp_sum(sq), sh.ri.sd);
+  // the draft row's top-F list: S (and its global copy), Σ_S q and the
+  // guesses of depth r
+  auto list_part = [&]() {
+    if (F > 1) row_topf<E>(a, rowD, F, stage_bmk ? st.bmk : gbmk, stage_bmk, st, sh);
+    __syncthreads();  // the merged statistics and the list
+    const float mdk = __fmul_rn(sh.ri.md, a.kT);
+    if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.ri.md, sh.ri.ad);  // the top-1: the row's argmax
+    if (F == 1) __syncthreads();
+    if (a.do_verify || a.do_lookup)
+      for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
+    // the draft's normalised mass on S: lane-strided partial sums, a fixed tree
+    if (warp == 0) {
+      float sq = 0.f;
+      if (!a.greedy && sh.ri.md != NEG_INF) {
+        for (int i = lane; i < F; i += 32)
+          if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
+        sq = __fdiv_rn(warp_sum(sq), sh.ri.sd);
+      }
+      if (lane == 0) sh.ri.sq = sq;
     }
-    if (lane == 0) sh.ri.sq = sq;
-  }
-  __syncthreads();
-  const RowInfo ri = sh.ri;
-  const uint64_t keyF = F > 0 ? sh.S[F - 1] : 0ull;
-  if (a.do_predict && ds >= 0) {
-    const int sumF = a.foff[a.K + 1];
-    for (int i = tid; i < a.F[r]; i += kThreads) {
-      const uint64_t key = sh.S[i];
-      a.guess[static_cast<size_t>(b) * sumF + a.foff[r] + i] = cand_idx(key);
-      if (a.guess_q) {
-        float q;
-        if (a.greedy) q = (i == 0) ? 1.f : 0.f;
-        else q = __fdiv_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), ri.sd);
-        a.guess_q[static_cast<size_t>(b) * sumF + a.foff[r] + i] = q;
+    __syncthreads();
+    if (a.do_predict && ds >= 0) {
+      const int sumF = a.foff[a.K + 1];
+      for (int i = tid; i < a.F[r]; i += kThreads) {
+        const uint64_t key = sh.S[i];
+        a.guess[static_cast<size_t>(b) * sumF + a.foff[r] + i] = cand_idx(key);
+        if (a.guess_q) {
+          float q;
+          if (a.greedy) q = (i == 0) ? 1.f : 0.f;
+          else q = __fdiv_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), sh.ri.sd);
+          a.guess_q[static_cast<size_t>(b) * sumF + a.foff[r] + i] = q;
+        }
       }
     }
-  }
+  };
+  // with C = 1 the draw, p(d), q'(d) and the residual weights do not depend
+  // on S: the list comes after the position's verdict, which may start the
+  // residual draw sooner
+  const bool verdict = a.do_verify && !a.greedy && r < a.K;
+  const bool late_list = verdict && !(a.C < 1.f);
+  if (late_list) __syncthreads();  // the merged statistics
+  else list_part();
+  const float mdk = __fmul_rn(sh.ri.md, a.kT);
+  const RowInfo ri = sh.ri;  // late_list: sq = 0 until the list is done (C = 1 makes q' not depend on it)
+  const uint64_t keyF = (F > 0 && !late_list) ? sh.S[F - 1] : 0ull;
   mark(a, sh.mk, 3);
   if (r < a.K && (a.do_sample || a.do_verify)) {
     int d;
@@ -1337,25 +1349,41 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
     }
   }
   if (tid == 0) a.rows[rr] = ri;
-  if (a.do_verify && !a.greedy && r < a.K) {
-    // the position's verdict, then the frontier: once the positions before
-    // the first rejection are all accepted, the residual draw may start
-    // (ready word = rejected position + 2) without waiting for the sequence's
-    // remaining pairs
+  if (verdict) {
+    // the position's verdict (1 accepted, 2 rejected; + 2 once the pair's
+    // list is also written), then the frontier: once the positions before the
+    // first rejection are all accepted, the residual draw may start (ready
+    // word = rejected position + 2) without waiting for the remaining pairs
     __syncthreads();  // the pair's results are written
+    uint32_t vword = 0;
     if (tid == 0) {
       const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + r);
       const bool ok = pi.p >= 0.f && __fmul_rn(a.u_acc[static_cast<size_t>(b) * a.K + r], pi.q) < pi.p;
-      st_release(pos_verdict(a, b, r), ok ? 1u : 2u);
-      for (int j = 0; j < a.K; ++j) {
-        const uint32_t v = ld_relaxed(pos_verdict(a, b, j));
-        if (v == 1u) continue;
-        if (v == 2u) {
+      vword = (ok ? 1u : 2u) + (late_list ? 0u : 2u);
+      st_release(pos_verdict(a, b, r), vword);
+      uint32_t v[kMaxK];  // every verdict load in flight at once
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) v[j] = (j < a.K) ? ld_relaxed(pos_verdict(a, b, j)) : 1u;
+      uint32_t acc_mask = 0, rej_mask = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (v[j] == 1u || v[j] == 3u) acc_mask |= 1u << j;
+        if (v[j] == 2u || v[j] == 4u) rej_mask |= 1u << j;
+      }
+      const uint32_t open = ~acc_mask;  // the first position not known to be accepted
+      if (open) {
+        const int j = __ffs(static_cast<int>(open)) - 1;
+        if ((rej_mask >> j) & 1u) {
           fence_acq_rel();  // the verdicts (and results) of positions 0..j, then the ready word
           atomicCAS(ready_word(a, b), 0u, static_cast<uint32_t>(j + 2));
         }
-        break;
       }
+    }
+    if (late_list) {
+      list_part();
+      if (tid == 0) a.rows[rr] = sh.ri;  // with Σ_S q
+      __syncthreads();                   // the list is written
+      if (tid == 0) st_release(pos_verdict(a, b, r), vword + 2u);
     }
   }
 }
@@ -1377,18 +1405,32 @@ SSD_DEV bool pay_staged(const VocabArgs &a) {
 // residual unit masses (`umass`) and target row K's chunk and block records
 // for the bonus draw (`st`).  Then the acceptance chain (thread 0).  Every
 // thread returns the accept count.
-SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, Smem &sh);
+SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, bool lists, Smem &sh);
+SSD_DEV void stage_lists(const VocabArgs &a, int b, Smem &sh);
 SSD_DEV int stage_complete(const VocabArgs &a, Smem &sh);
 SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, Stage *st, Smem &sh) {
-  stage_issue(a, b, pay, st, sh);
+  stage_issue(a, b, pay, st, true, sh);
   if (umass) {
     const int nu = a.nchunks * kQuarters;
     for (int q = threadIdx.x; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
   }
   return stage_complete(a, sh);
 }
-// The loads of stage_chain but the unit masses, issued (cp.async) without a wait.
-SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, Smem &sh) {
+// The top-F lists of the cache lookup (when they fit sh.cand), issued
+// (cp.async) without a wait.
+SSD_DEV void stage_lists(const VocabArgs &a, int b, Smem &sh) {
+  if (!lists_staged(a)) return;
+  const size_t r0 = static_cast<size_t>(b) * (a.K + 1);
+  const int nS = a.foff[a.K + 1];
+  for (int i = threadIdx.x; i < nS; i += kThreads) {
+    int r = 0;
+    while (i >= a.foff[r + 1]) ++r;
+    cp_async8(&sh.cand[i], a.S + (r0 + r) * a.Fcap + (i - a.foff[r]));
+  }
+}
+// The loads of stage_chain but the unit masses (and, unless `lists`, the
+// lookup lists), issued (cp.async) without a wait.
+SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, bool lists, Smem &sh) {
   const int tid = threadIdx.x;
   const size_t r0 = static_cast<size_t>(b) * (a.K + 1);
   for (int t = tid; t < a.K; t += kThreads) {
@@ -1402,14 +1444,7 @@ SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, Sme
     if (F > 0) cp_async8(&sh.keyF[r], a.S + (r0 + r) * a.Fcap + F - 1);
     else sh.keyF[r] = 0ull;
   }
-  if (lists_staged(a)) {
-    const int nS = a.foff[a.K + 1];
-    for (int i = tid; i < nS; i += kThreads) {
-      int r = 0;
-      while (i >= a.foff[r + 1]) ++r;
-      cp_async8(&sh.cand[i], a.S + (r0 + r) * a.Fcap + (i - a.foff[r]));
-    }
-  }
+  if (lists) stage_lists(a, b, sh);
   if (pay && pay_staged(a)) {
     const int n = a.foff[a.K + 1] * a.K;
     const int32_t *src = a.payload + static_cast<size_t>(b) * n;
@@ -1659,7 +1694,7 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
   const int acc = sh.flag - 2;
   if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
   const bool fin = sh.ival[2] != 0;
-  if (fin) stage_issue(a, b, pay, nullptr, sh);
+  if (fin) stage_issue(a, b, pay, nullptr, false, sh);
   if (tid == 0 && a.trace)
     for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
   mark(a, sh.mk, 0);
@@ -1707,8 +1742,13 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
     if (tid == 0) red_add_release(res_pub(a, b), 1u);
   } else {
     kind = 3;
-    if (tid == 0 && !wait_count(res_pub(a, b), static_cast<uint32_t>(nu - 1))) atomicOr(a.status, kFlagWaitTimeout);
+    if (tid == 0) {
+      if (!wait_count(res_pub(a, b), static_cast<uint32_t>(nu - 1))) atomicOr(a.status, kFlagWaitTimeout);
+      // the lookup lists: the pair merge of position acc also finished its list
+      if (a.do_lookup && !wait_count(pos_verdict(a, b, acc), 3u)) atomicOr(a.status, kFlagWaitTimeout);
+    }
     __syncthreads();
+    stage_lists(a, b, sh);
     mark(a, sh.mk, 3);
     // the unit masses and (up to kResidStage chunks) every unit's block sums
     for (int q = tid; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
