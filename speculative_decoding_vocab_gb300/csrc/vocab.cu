@@ -1638,10 +1638,15 @@ __global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_con
       if (role == 1) {
         if (tid == 0) red_add_release(seq_pub(a, b), 1u);
       } else {
-        if (tid == 0 && !wait_count(seq_pub(a, b), static_cast<uint32_t>(a.npairs - 1)))
-          atomicOr(a.status, kFlagWaitTimeout);
+        // a rejection the pair merges already resolved (ready word set) leaves
+        // the sequence to the residual draw: nothing is left to finish here
+        if (tid == 0) {
+          sh.flag = (!a.greedy && ld_relaxed(ready_word(a, b)) != 0u) ? 1 : 0;
+          if (!sh.flag && !wait_count(seq_pub(a, b), static_cast<uint32_t>(a.npairs - 1)))
+            atomicOr(a.status, kFlagWaitTimeout);
+        }
         __syncthreads();
-        seq_finish<E>(a, b, st, sh);
+        if (!sh.flag) seq_finish<E>(a, b, st, sh);
         mark(a, sh.mk, 5);
       }
     }
