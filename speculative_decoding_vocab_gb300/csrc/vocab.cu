@@ -1747,13 +1747,8 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
     if (tid == 0) red_add_release(res_pub(a, b), 1u);
   } else {
     kind = 3;
-    if (tid == 0) {
-      if (!wait_count(res_pub(a, b), static_cast<uint32_t>(nu - 1))) atomicOr(a.status, kFlagWaitTimeout);
-      // the lookup lists: the pair merge of position acc also finished its list
-      if (a.do_lookup && !wait_count(pos_verdict(a, b, acc), 3u)) atomicOr(a.status, kFlagWaitTimeout);
-    }
+    if (tid == 0 && !wait_count(res_pub(a, b), static_cast<uint32_t>(nu - 1))) atomicOr(a.status, kFlagWaitTimeout);
     __syncthreads();
-    stage_lists(a, b, sh);
     mark(a, sh.mk, 3);
     // the unit masses and (up to kResidStage chunks) every unit's block sums
     for (int q = tid; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
@@ -1809,6 +1804,14 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
     }
     const bool zero = uq < 0;  // no residual mass: p_{a+1} instead
     if (bt < 0) bt = draw_target<E>(a, b, acc2, ra, ub, nullptr, sh);
+    if (a.do_lookup) {
+      // the lookup lists, once the pair merge of position acc has written its list
+      if (tid == 0 && !wait_count(pos_verdict(a, b, acc), 3u)) atomicOr(a.status, kFlagWaitTimeout);
+      __syncthreads();
+      stage_lists(a, b, sh);
+      cp_async_wait_all();
+      __syncthreads();
+    }
     mark(a, sh.mk, 5);
     emit(a, b, acc2, bt, W, zero, pay, sh);
   }
