@@ -123,8 +123,9 @@ def test_zero_batch_is_a_noop():
 
 
 def test_all_equal_logits_ties():
-    """Every logit equal: top-F and argmax break ties by the lower index, the
-    chunk-level top-F takes its exact tie path."""
+    """Every logit equal: top-F and argmax break ties by the lower index; the
+    pair merge's top-F overflows its candidate buffers and takes its tie
+    fallback (one winner per sweep)."""
     spec = w.RoundSpec(B=3, K=3, V=50000, dtype="bf16", recipe="gauss", T=1.0, C=0.5,
                        F=(40, 20, 3, 1))
     inp = w.make_round(spec, seed=1)
