@@ -40,7 +40,6 @@ constexpr int kMaxNodes = 128;
 constexpr int kRows = 128;                  // query rows per row tile (MMA M)
 constexpr int kKeys = 64;                   // keys per tile (MMA N of S, K of P V)
 constexpr int kTilePages = kKeys / kPage;   // 4
-constexpr uint32_t kTmemCols = 512;         // S: MT x 2 x 64 columns, O: MT x d columns
 
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
@@ -213,15 +212,21 @@ struct AttnArgs {
   uint32_t *status;
 };
 
-// Shared-memory plan of a CTA with MT row tiles at head dimension D.
-template <int D, int MT>
+// Shared-memory plan of a CTA with MT row tiles at head dimension D, CPS
+// CTAs resident per SM.
+template <int D, int MT, int CPS>
 struct AttnCfg {
   static constexpr int kQBytes = kRows * D * 2;      // one row tile of Q
   static constexpr int kKVBytes = kKeys * D * 2;     // K or V of one key tile
   static constexpr int kPBytes = kRows * kKeys * 2;  // one P buffer of one row tile
   static constexpr int kFixed = MT * kQBytes + MT * 2 * kPBytes;
-  static constexpr int kStagesFit = (216 * 1024 - kFixed) / (2 * kKVBytes);
+  static constexpr int kStagesFit = (216 * 1024 / CPS - kFixed) / (2 * kKVBytes);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  // TMEM: S buffers (MT x 2 x 64 columns), then O (MT x D); a power of two
+  static constexpr uint32_t kOCol = MT * 2 * kKeys;
+  static constexpr uint32_t kTmemNeed = kOCol + MT * D;
+  static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128 : (kTmemNeed <= 256 ? 256 : 512);
+  static_assert(kTmemCols * CPS <= 512, "TMEM of the resident CTAs");
   static constexpr int kQ = 0;
   static constexpr int kP = kQ + MT * kQBytes;
   static constexpr int kKV = kP + MT * 2 * kPBytes;
@@ -232,11 +237,11 @@ struct AttnCfg {
   static_assert(kStages >= 2, "at least two K/V stages");
 };
 
-template <int D, int MT>
-__global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
+template <int D, int MT, int CPS>
+__global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
     k_branch_attn_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ AttnArgs a) {
-  using CF = AttnCfg<D, MT>;
+  using CF = AttnCfg<D, MT, CPS>;
   constexpr int NS = CF::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
     s_abort = 0;
   }
   if (warp == CF::kMmaWarp) {
-    tmem_alloc(&tmem_base, kTmemCols);
+    tmem_alloc(&tmem_base, CF::kTmemCols);
     tmem_relinquish();
   }
   // the tree's parent indices (one coalesced load), then the ancestor-or-self
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t p_base = smem_u32(smem + CF::kP + (m * 2 + (u & 1)) * CF::kPBytes);
-          const uint32_t tO = tmem + 4 * kKeys + m * D;
+          const uint32_t tO = tmem + CF::kOCol + m * D;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
             // P: 16 keys = 32 bytes of each 128-byte row; V: 16 keys = two 8-key groups of 1024 B,
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
         float o[32];
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          const uint32_t ta = tmem + 4 * kKeys + m * D + cc * 32 + lane_off;
+          const uint32_t ta = tmem + CF::kOCol + m * D + cc * 32 + lane_off;
           tmem_ld32(ta, o);
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = __fmul_rn(o[j], f);
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          tmem_ld32(tmem + 4 * kKeys + m * D + cc * 32 + lane_off, o);
+          tmem_ld32(tmem + CF::kOCol + m * D + cc * 32 + lane_off, o);
           if (row_valid) {
             uint4 *dst = reinterpret_cast<uint4 *>(a.out + orow * D + cc * 32);
 #pragma unroll
@@ -603,7 +608,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
         const size_t pidx = ((static_cast<size_t>(bh) * a.mtiles + mtile) * a.splits + split) * kRows + r_own;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          tmem_ld32(tmem + 4 * kKeys + m * D + cc * 32 + lane_off, o);
+          tmem_ld32(tmem + CF::kOCol + m * D + cc * 32 + lane_off, o);
           float4 *dst = reinterpret_cast<float4 *>(a.part_o + pidx * D + cc * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) dst[q4] = make_float4(o[q4 * 4], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
@@ -629,7 +634,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::kThreads, 1)
   }
   if (warp == CF::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, CF::kTmemCols);
   }
 }
 
@@ -730,11 +735,11 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   AttnPlan p;
   p.nrows = (Hq / Hkv) * Nq;
   p.mtiles = (p.nrows + kRows - 1) / kRows;
-  p.mt_per_cta = (d == 64 && p.mtiles >= 2) ? 2 : 1;
+  p.mt_per_cta = 1;  // d = 64: two CTAs per SM instead of two row tiles per CTA
   p.mgroups = (p.mtiles + p.mt_per_cta - 1) / p.mt_per_cta;
   const int ntiles = (max_keys + kKeys - 1) / kKeys;
   const long base = static_cast<long>(B) * Hkv * p.mgroups;
-  const long slots = attn_num_sms();
+  const long slots = attn_num_sms() * (d == 64 ? 2 : 1);  // resident CTAs
   // estimated time in tile-steps: whole waves x (tiles per split + a CTA's
   // set-up, about kSetupTiles tiles: masks, Q, TMEM, the first copies)
   constexpr double kSetupTiles = 4.0;
@@ -761,15 +766,16 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-template <int D, int MT>
+template <int D, int MT, int CPS>
 cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a, dim3 grid,
                              cudaStream_t cs) {
-  using CF = AttnCfg<D, MT>;
+  using CF = AttnCfg<D, MT, CPS>;
   const int smem = CF::kTable + a.tiles_per_split * kTilePages * 4 + 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(k_branch_attn_tc<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_branch_attn_tc<D, MT, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_branch_attn_tc<D, MT><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
+  k_branch_attn_tc<D, MT, CPS><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
   e = cudaGetLastError();
   if (e == cudaSuccess && a.splits > 1) {
     k_attn_combine<D><<<dim3(grid.x, a.mtiles), 128, 0, cs>>>(a);
@@ -842,9 +848,9 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
   const dim3 grid(B * Hkv, p.mgroups, a.splits);
   cudaError_t e;
-  if (d == 64 && p.mt_per_cta == 2) e = launch_attention<64, 2>(kmap, vmap, a, grid, cs);
-  else if (d == 64) e = launch_attention<64, 1>(kmap, vmap, a, grid, cs);
-  else e = launch_attention<128, 1>(kmap, vmap, a, grid, cs);
+  if (d == 64 && p.mt_per_cta == 2) e = launch_attention<64, 2, 1>(kmap, vmap, a, grid, cs);
+  else if (d == 64) e = launch_attention<64, 1, 2>(kmap, vmap, a, grid, cs);
+  else e = launch_attention<128, 1, 1>(kmap, vmap, a, grid, cs);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
