@@ -10,8 +10,9 @@
 // the query heads of one KV head share a CTA's rows, so each K/V page is read
 // once per (sequence, KV head, group of row tiles).
 //
-// One CTA (one per SM) = (sequence b, KV head, group of MT tiles of 128 query
-// rows, range of keys), warp-specialised:
+// One CTA = (sequence b, KV head, group of MT tiles of 128 query rows, range
+// of keys); two are resident per SM at d = 64 (one row tile each, 256 TMEM
+// columns), one at d = 128.  Warp-specialised:
 //   * a producer warp fetches the K and V pages of each 64-key tile by TMA
 //     through the block table into a ring of stages (mbarrier completion);
 //   * an MMA warp (one thread) issues S = Q K^T for tile t + 1 into a second
@@ -728,9 +729,8 @@ struct AttnPlan {
   size_t part_o_bytes, part_ml_bytes;
 };
 
-// Row tiles per CTA: two at d = 64 (when there are two), one at d = 128.  Keys
-// are split so that the CTAs (one per SM) fill whole waves, with at least 4
-// tiles per split.
+// One row tile per CTA.  Keys are split so that the CTAs (two per SM at
+// d = 64, one at d = 128) fill whole waves, with at least 4 tiles per split.
 AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   AttnPlan p;
   p.nrows = (Hq / Hkv) * Nq;
