@@ -231,11 +231,11 @@ ssd_status_t ssd_set_timing_events(void *before, void *after);
  * kernel's: (SM << 48 | kind << 40 | sequence << 20 | index) and seven
  * %globaltimer marks in ns (0 = not reached).  kind: 0 chunk statistics,
  * 1 + pair merge, 2 residual chunk, 3 + final steps.  Statistics CTA marks:
- * start, chunk landed, record published, pair merged, Saguaro draw done,
- * sequence finished, end.  Residual CTA marks: start, chunks landed, chunk mass
- * done, last arrival, chain and chunk located, bonus drawn, end.  Calls whose
- * CTAs do not fit in `bytes` write nothing.  Process-wide, not thread-safe;
- * NULL clears.  Diagnostics only.
+ * start, chunk landed, records published, the merge's list and draw begin,
+ * pair merged, sequence finished, end.  Residual CTA marks: start, -, unit
+ * published, the other units published, unit and block located, bonus drawn,
+ * end.  Calls whose CTAs do not fit in `bytes` write nothing.  Process-wide,
+ * not thread-safe; NULL clears.  Diagnostics only.
  */
 ssd_status_t ssd_set_trace(void *buf, size_t bytes);
 

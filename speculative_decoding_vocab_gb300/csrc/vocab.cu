@@ -13,28 +13,29 @@
 //   k_stats  one CTA per 32 KiB chunk of one logit row: the HBM pass, which
 //            carries nearly all of the call's bytes.  A TMA bulk copy stages
 //            the chunk in shared memory; the CTA reduces it to a record (max,
-//            sum of 2^(z log2e/T - max), argmax), the sorted top-F candidates
-//            and, for rows that are drawn from, per-block partial sums (a block
-//            = the 32 vectors one warp reads in one round).  Chunks are
-//            numbered sequence-major and, within a sequence, by row pair r =
-//            (target row r, draft row r), so pairs complete in launch order.
-//            The CTA that publishes the last chunk of a pair (an atomic count
-//            per pair) merges the pair: row statistics, the top-F_r list (the
-//            guesses of depth r), the Saguaro draw of d_{r+1}, p(d) and q'(d).
-//            A draw locates its chunk from the chunk masses and its block from
-//            the block sums; one warp then reads that block's 32 vectors again.
-//            The CTA that merges the last pair of a sequence runs the
-//            acceptance chain and, unless a residual draw is needed, the bonus
-//            draw and the outputs.  No CTA ever waits for another: the last to
-//            arrive does the work.
+//            sum of 2^(z log2e/T - max), argmax), per-block partial sums for
+//            rows that are drawn from (a block = the 32 vectors one warp reads
+//            in one round) and per-block maximum keys for rows with a top-F
+//            list.  Chunks are numbered sequence-major and, within a sequence,
+//            by row pair r = (target row r, draft row r).  Each CTA takes its
+//            pair's ticket while its copy is in flight: the last CTA of a pair
+//            to start merges the pair once the others are published (row
+//            statistics, the top-F_r list from the block maxima, the Saguaro
+//            draw of d_{r+1}, p(d) and q'(d), the position's verdict), and the
+//            last merger of a sequence to start runs the acceptance chain and,
+//            unless a residual draw is needed, the bonus draw and the outputs.
+//            A merger waits only for CTAs that started before it.  A draw
+//            locates its chunk from the chunk masses and its block from the
+//            block sums; one warp then reads that block's 32 vectors again.
 //            The merges stage the records they read in shared memory (over
 //            the chunk buffer) with one round of loads.
 //   k_resid  (verification at T > 0) one CTA per quarter chunk of each
-//            sequence's rejected row pair: residual block sums; the last CTA of
-//            a sequence draws the bonus token from them and writes the
-//            outputs.  It is a programmatic dependent launch of k_stats: its
-//            CTAs start once every k_stats CTA has started and each waits only
-//            for its own sequence's acceptance chain (a ready word).
+//            sequence's rejected row pair: residual block sums; the unit with
+//            the sequence's last ticket draws the bonus token from them and
+//            writes the outputs.  It is a programmatic dependent launch of
+//            k_stats: its CTAs start once every k_stats CTA has started, and
+//            each waits only for its own sequence's ready word, which the pair
+//            merges set as soon as the first rejected position is known.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
@@ -116,7 +117,7 @@ struct VocabArgs {
   // workspace
   uint32_t *ctr;  // [0] finished sequences, [1] hits; per sequence b: [2+b] pair-merge
                   // tickets, [2+B+b] merged pairs published, [2+2B+b] residual unit
-                  // tickets, [2+3B+b] ready word (accs[b] + 2 once published),
+                  // tickets, [2+3B+b] ready word (accept count + 2 once known),
                   // [2+4B+b] residual units published; per pair (b, r):
                   // [2+5B + b(K+1)+r] chunk tickets, [2+5B+B(K+1) + b(K+1)+r]
                   // chunks published, [2+5B+2B(K+1) + b(K+1)+r] position verdict
@@ -128,7 +129,6 @@ struct VocabArgs {
   PosInfo *pos;      // [B][K]
   float *rmass;      // [B][nchunks * kQuarters] residual mass per unit
   float *rbs;        // [B][nchunks][kBlocks] residual block sums
-  int32_t *accs;     // [B] accept count of a sequence left to k_resid, else -1
   // inputs / outputs
   const float *u_draft, *u_acc, *u_bonus;
   const int32_t *d_in;
@@ -1539,9 +1539,9 @@ __device__ __forceinline__ void seq_finish(const VocabArgs &a, int b, Stage &st,
   const int acc = stage_chain(a, b, nullptr, st.pay, &st, sh);
   const bool resid = !a.greedy && acc < a.K;
   if (threadIdx.x == 0) {
-    a.accs[b] = resid ? acc : -1;
     // the sequence's k_resid CTAs may go on (unless a pair merge's frontier
-    // already set the word: to the same value); the word carries accs[b] + 2
+    // already set the word: to the same value); the word carries the accept
+    // count + 2 (1: no residual draw)
     fence_acq_rel();
     atomicCAS(ready_word(a, b), 0u, static_cast<uint32_t>((resid ? acc : -1) + 2));
   }
@@ -1886,7 +1886,7 @@ namespace {
 struct Layout {
   int nslots, nchunks, chunk_elems, Fcap;
   size_t ctr_words;
-  size_t ctr_off, stats_off, blk_off, bmk_off, rows_off, S_off, pos_off, rmass_off, rbs_off, accs_off, total;
+  size_t ctr_off, stats_off, blk_off, bmk_off, rows_off, S_off, pos_off, rmass_off, rbs_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1927,8 +1927,6 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + Bn * L->nchunks * kQuarters * sizeof(float), 256);
   L->rbs_off = o;
   o = align_up(o + Bn * L->nchunks * kBlocks * sizeof(float), 256);
-  L->accs_off = o;
-  o = align_up(o + Bn * sizeof(int32_t), 256);
   L->total = o;
   return true;
 }
@@ -1996,7 +1994,6 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.blk = reinterpret_cast<BlockRec *>(w + L.blk_off);
   a.rmass = reinterpret_cast<float *>(w + L.rmass_off);
   a.rbs = reinterpret_cast<float *>(w + L.rbs_off);
-  a.accs = reinterpret_cast<int32_t *>(w + L.accs_off);
   a.status = status;
   return a;
 }
