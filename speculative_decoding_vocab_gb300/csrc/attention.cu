@@ -10,9 +10,12 @@
 // the query heads of one KV head share a CTA's rows, so each K/V page is read
 // once per (sequence, KV head, group of row tiles).
 //
-// One CTA = (sequence b, KV head, group of MT tiles of 128 query rows, range
-// of keys); two are resident per SM at d = 64 (one row tile each, 256 TMEM
-// columns), one at d = 128.  Warp-specialised:
+// A work item = (sequence b, KV head, tile of 128 query rows, range of keys).
+// A kernel that allocates TMEM is resident once per SM.  At d = 64 one CTA
+// runs two independent pipelines, each on its own work item with 256 TMEM
+// columns; at d = 128 it runs one, with all of shared memory for its K/V ring
+// (Q and P held as 64-row tiles when at most 64 query rows share a KV head).
+// Each pipeline is warp-specialised:
 //   * a producer warp fetches the K and V pages of each 64-key tile by TMA
 //     through the block table into a ring of stages (mbarrier completion);
 //   * an MMA warp (one thread) issues S = Q K^T for tile t + 1 into a second
@@ -131,6 +134,33 @@ SSD_DEV void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane (load, then store back)
+SSD_DEV void tmem_ld16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+SSD_DEV void tmem_st16(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 SSD_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -205,6 +235,7 @@ struct AttnArgs {
   int64_t num_blocks;
   const int32_t *prefix_len, *parent;
   int B, N, Nq, Hq, Hkv, group, nrows, mtiles, splits, tiles_per_split;
+  int items;     // work items: (sequence, KV head) x row-tile groups x key splits
   float scale_log2;  // scale * log2(e)
   uint16_t *out;
   float *lse;
@@ -213,58 +244,100 @@ struct AttnArgs {
   uint32_t *status;
 };
 
-// Shared-memory plan of a CTA with MT row tiles at head dimension D, CPS
-// CTAs resident per SM.
-template <int D, int MT, int CPS>
+// Shared-memory plan of a CTA at head dimension D that runs PL independent
+// pipelines (each its own work item, Q, K/V ring, barriers and TMEM columns),
+// each with MT row tiles of which RA rows of Q and P are held in shared
+// memory.  A kernel that allocates TMEM is resident once per SM, so PL = 2 is
+// how two tile streams share an SM.  RA < 128 serves problems with at most RA
+// query rows: the MMA still reads 128 rows of A, and rows RA..127 fall on the
+// next buffer (finite or not, they only feed TMEM lanes that no thread reads).
+template <int D, int MT, int PL, int RA = kRows>
 struct AttnCfg {
-  static constexpr int kQBytes = kRows * D * 2;      // one row tile of Q
+  static_assert(RA == kRows || (MT == 1 && RA % 32 == 0 && RA < kRows), "trimmed row tiles: one per pipeline");
+  static constexpr int kQBytes = RA * D * 2;         // one row tile of Q
   static constexpr int kKVBytes = kKeys * D * 2;     // K or V of one key tile
-  static constexpr int kPBytes = kRows * kKeys * 2;  // one P buffer of one row tile
+  static constexpr int kPBytes = RA * kKeys * 2;     // one P buffer of one row tile
   static constexpr int kFixed = MT * kQBytes + MT * 2 * kPBytes;
-  static constexpr int kStagesFit = (216 * 1024 / CPS - kFixed) / (2 * kKVBytes);
+  static constexpr int kStagesFit = (216 * 1024 / PL - kFixed) / (2 * kKVBytes);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   // TMEM: S buffers (MT x 2 x 64 columns), then O (MT x D); a power of two
   static constexpr uint32_t kOCol = MT * 2 * kKeys;
   static constexpr uint32_t kTmemNeed = kOCol + MT * D;
   static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128 : (kTmemNeed <= 256 ? 256 : 512);
-  static_assert(kTmemCols * CPS <= 512, "TMEM of the resident CTAs");
+  static_assert(kTmemCols * PL <= 512, "TMEM of the pipelines");
   static constexpr int kQ = 0;
   static constexpr int kP = kQ + MT * kQBytes;
   static constexpr int kKV = kP + MT * 2 * kPBytes;
-  static constexpr int kTable = kKV + kStages * 2 * kKVBytes;  // block-table entries of the key range
-  static constexpr int kWarps = 4 * MT + 2;
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kTmaWarp = 4 * MT, kMmaWarp = 4 * MT + 1;
+  static constexpr int kPipe = kKV + kStages * 2 * kKVBytes;  // one pipeline's region
+  static constexpr int kTable = PL * kPipe;  // then each pipeline's block-table entries
+  static constexpr int kPWarps = 4 * MT + 2;  // warps of one pipeline
+  static constexpr int kPThreads = kPWarps * 32;
+  static constexpr int kThreads = PL * kPThreads;
+  static constexpr int kTmaWarp = 4 * MT, kMmaWarp = 4 * MT + 1;  // within a pipeline
   static_assert(kStages >= 2, "at least two K/V stages");
+  static_assert(kPipe % 1024 == 0, "each pipeline's swizzled tiles stay 1024-byte aligned");
+  static_assert(PL == 1 || MT == 1, "two pipelines hold one row tile each");
+  // the 128 A rows the MMA reads from the last Q column block and the last P
+  // buffer stay inside the pipeline's region
+  static_assert(kQ + MT * kQBytes - RA * 128 + kRows * 128 <= kPipe, "Q rows read by the MMA");
+  static_assert(kP + (MT * 2 - 1) * kPBytes + kRows * 128 <= kPipe, "P rows read by the MMA");
 };
 
-template <int D, int MT, int CPS>
-__global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
+// int entries of one pipeline's block-table slice (16-byte multiple)
+__host__ __device__ inline int attn_tab_stride(int tiles_per_split) { return (tiles_per_split * kTilePages + 3) & ~3; }
+
+template <int D, int MT, int PL, int RA>
+__global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA>::kThreads, 1)
     k_branch_attn_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ AttnArgs a) {
-  using CF = AttnCfg<D, MT, CPS>;
+  using CF = AttnCfg<D, MT, PL, RA>;
   constexpr int NS = CF::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
-  __shared__ __align__(8) uint64_t s_full[MT][2], s_free[MT][2], p_full[MT][2], pv_done[MT][2];
+  uint8_t *const smem_all =
+      reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t kv_full_[PL][NS], kv_empty_[PL][NS];
+  __shared__ __align__(8) uint64_t s_full_[PL][MT][2], s_free_[PL][MT][2], p_full_[PL][MT][2], pv_done_[PL][MT][2];
   __shared__ uint32_t tmem_base;
-  __shared__ uint32_t anc[kMaxNodes][kMaxNodes / 32];
-  __shared__ int par[kMaxNodes];
-  __shared__ volatile int s_abort;
+  __shared__ uint32_t anc_[PL][kMaxNodes][kMaxNodes / 32];
+  __shared__ int par_[PL][kMaxNodes];
+  __shared__ volatile int s_abort_[PL];
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x, b = bh / a.Hkv, hk = bh % a.Hkv;
-  const int mg = blockIdx.y, split = blockIdx.z;
+  // This thread's pipeline, and its warp and thread numbers within it.  The
+  // softmax warpgroups come first (a warp reaches the TMEM lanes 32 (w % 4) ..
+  // + 31 by its warp number w in the CTA), then each pipeline's producer and
+  // MMA warps.
+  constexpr int kSoftWarps = 4 * MT;
+  const int gw = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool soft_w = gw < PL * kSoftWarps;
+  const int pl = soft_w ? gw / kSoftWarps : (gw - PL * kSoftWarps) / 2;
+  const int warp = soft_w ? gw % kSoftWarps : kSoftWarps + (gw - PL * kSoftWarps) % 2;
+  const int tid = warp * 32 + lane;
+  uint64_t(&kv_full)[NS] = kv_full_[pl];
+  uint64_t(&kv_empty)[NS] = kv_empty_[pl];
+  uint64_t(&s_full)[MT][2] = s_full_[pl];
+  uint64_t(&s_free)[MT][2] = s_free_[pl];
+  uint64_t(&p_full)[MT][2] = p_full_[pl];
+  uint64_t(&pv_done)[MT][2] = pv_done_[pl];
+  uint32_t(&anc)[kMaxNodes][kMaxNodes / 32] = anc_[pl];
+  int(&par)[kMaxNodes] = par_[pl];
+  volatile int &s_abort = s_abort_[pl];
+  uint8_t *const smem = smem_all + pl * CF::kPipe;
+  // the pipeline's work item: (sequence, KV head), group of row tiles, key range
+  const int mgroups = (a.mtiles + MT - 1) / MT;
+  const int item = blockIdx.x * PL + pl;
+  const bool has_item = item < a.items;
+  const int it = has_item ? item : 0;
+  const int split = it % a.splits, mg = (it / a.splits) % mgroups, bh = it / (a.splits * mgroups);
+  const int b = bh / a.Hkv, hk = bh % a.Hkv;
   const int N = a.N;
   const int L = max(0, a.prefix_len[b]);
   const int nkeys = L + N;
   const int ntiles_all = (nkeys + kKeys - 1) / kKeys;
   const int t_begin = split * a.tiles_per_split;
   const int t_end = min(ntiles_all, t_begin + a.tiles_per_split);
-  const int nt = max(0, t_end - t_begin);
-  const int mt_here = min(MT, a.mtiles - mg * MT);  // row tiles of this CTA
+  const int nt = has_item ? max(0, t_end - t_begin) : 0;
+  const int mt_here = has_item ? min(MT, a.mtiles - mg * MT) : 0;  // row tiles of this pipeline
   const float NEG_INF = -__int_as_float(0x7f800000);
 
   if (tid == 0) {
@@ -286,15 +359,15 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
     fence_mbar_init();
     s_abort = 0;
   }
-  if (warp == CF::kMmaWarp) {
-    tmem_alloc(&tmem_base, CF::kTmemCols);
+  if (pl == 0 && warp == CF::kMmaWarp) {
+    tmem_alloc(&tmem_base, PL * CF::kTmemCols);
     tmem_relinquish();
   }
   // the tree's parent indices (one coalesced load), then the ancestor-or-self
   // masks walked in shared memory
-  for (int m = tid; m < N; m += CF::kThreads) par[m] = a.parent[static_cast<int64_t>(b) * N + m];
+  for (int m = tid; m < N; m += CF::kPThreads) par[m] = a.parent[static_cast<int64_t>(b) * N + m];
   __syncthreads();
-  for (int m = tid; m < N; m += CF::kThreads) {
+  for (int m = tid; m < N; m += CF::kPThreads) {
     uint32_t bits[kMaxNodes / 32] = {0, 0, 0, 0};
     int x = m;
     bool bad = false;
@@ -312,10 +385,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
     for (int w = 0; w < kMaxNodes / 32; ++w) anc[m][w] = bits[w];
   }
   // block-table entries of this CTA's key range (-1: past the table or the keys, or a bad id)
-  int *tab = reinterpret_cast<int *>(smem + CF::kTable);
+  int *tab = reinterpret_cast<int *>(smem_all + CF::kTable) + pl * attn_tab_stride(a.tiles_per_split);
   const int page0 = t_begin * kTilePages;
   const int npages = nt * kTilePages;
-  for (int i = tid; i < npages; i += CF::kThreads) {
+  for (int i = tid; i < npages; i += CF::kPThreads) {
     const int lp = page0 + i;
     int blk = -1;
     if (lp < a.maxb && lp * kPage < nkeys) {
@@ -337,7 +410,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
   const int head = hk * a.group + (row_valid ? row % a.group : 0);
   // a softmax warp without a valid row sits the loop out; its P rows stay zero
   const bool warp_active = __any_sync(0xffffffffu, row_valid);
-  if (softmax_thread && !warp_active) {
+  if (softmax_thread && !warp_active && r_own < RA) {
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -345,21 +418,21 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
         *reinterpret_cast<uint4 *>(smem + CF::kP + (m_own * 2 + u) * CF::kPBytes + sw128(r_own, q4)) =
             make_uint4(0, 0, 0, 0);
   }
-  if (softmax_thread) {
+  if (softmax_thread && r_own < RA) {
     const uint16_t *qrow = a.q + ((static_cast<int64_t>(b) * a.Nq + qi) * a.Hq + head) * D;
     uint8_t *qt = smem + CF::kQ + m_own * CF::kQBytes;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       uint4 v = make_uint4(0, 0, 0, 0);
       if (row_valid) v = __ldg(reinterpret_cast<const uint4 *>(qrow) + c);
-      *reinterpret_cast<uint4 *>(qt + (c >> 3) * (kRows * 128) + sw128(r_own, c & 7)) = v;
+      *reinterpret_cast<uint4 *>(qt + (c >> 3) * (RA * 128) + sw128(r_own, c & 7)) = v;
     }
   }
   fence_proxy_async();  // generic-proxy writes of Q -> visible to the tensor cores
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base;
+  const uint32_t tmem = tmem_base + pl * CF::kTmemCols;  // this pipeline's columns
   int issued = 0;  // producer: tiles whose copies were issued
 
   if (warp == CF::kTmaWarp) {
@@ -432,7 +505,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
           const uint32_t tS = tmem + (m * 2 + (i & 1)) * kKeys;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qoff = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (RA * 128) + (kk & 3) * 32;
             const uint32_t koff = (kk >> 2) * (kKeys * 128) + (kk & 3) * 32;
             umma_bf16(tS, smem_desc_sw128(q_base + qoff, 16), smem_desc_sw128(k_base + koff, 16), idesc_s,
                       kk > 0 ? 1u : 0u);
@@ -499,15 +572,17 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
 #pragma unroll
         for (int j = 0; j < kKeys; ++j) s[j] = ((vis >> j) & 1ull) ? s[j] : NEG_INF;
       }
-      // tile maximum (a tree), scaled to log2 units
-      float t2[kKeys / 2];
+      // tile maximum (eight running maxima, then a tree), scaled to log2 units
+      float t8[8];
 #pragma unroll
-      for (int j = 0; j < kKeys / 2; ++j) t2[j] = fmaxf(s[2 * j], s[2 * j + 1]);
+      for (int j = 0; j < 8; ++j) t8[j] = s[j];
 #pragma unroll
-      for (int w = kKeys / 4; w >= 1; w >>= 1)
+      for (int j = 8; j < kKeys; ++j) t8[j & 7] = fmaxf(t8[j & 7], s[j]);
 #pragma unroll
-        for (int j = 0; j < w; ++j) t2[j] = fmaxf(t2[j], t2[j + w]);
-      float tmax = row_valid ? t2[0] : NEG_INF;
+      for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t8[j] = fmaxf(t8[j], t8[j + w]);
+      float tmax = row_valid ? t8[0] : NEG_INF;
       tmax = (tmax == NEG_INF) ? NEG_INF : __fmul_rn(tmax, c);
       const bool grow = tmax != NEG_INF && (m_used == NEG_INF || tmax > m_used + 8.f);
       // P buffer u is free once P V of tile i - 2 completed
@@ -523,14 +598,14 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
         }
         tc_fence_after();
         const float f = (grow && m_used != NEG_INF) ? ex2(m_used - tmax) : 1.f;
-        float o[32];
+        float o[16];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          const uint32_t ta = tmem + CF::kOCol + m * D + cc * 32 + lane_off;
-          tmem_ld32(ta, o);
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const uint32_t ta = tmem + CF::kOCol + m * D + cc * 16 + lane_off;
+          tmem_ld16(ta, o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __fmul_rn(o[j], f);
-          tmem_st32(ta, o);
+          for (int j = 0; j < 16; ++j) o[j] = __fmul_rn(o[j], f);
+          tmem_st16(ta, o);
         }
         tc_fence_before();
       }
@@ -633,9 +708,9 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, CPS>::kThreads, CPS)
     // copies still in flight land before the CTA's shared memory is released
     for (int i = max(0, issued - NS); i < issued; ++i) (void)mbar_wait(&kv_full[i % NS], (i / NS) & 1);
   }
-  if (warp == CF::kMmaWarp) {
+  if (pl == 0 && warp == CF::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, CF::kTmemCols);
+    tmem_dealloc(tmem_base, PL * CF::kTmemCols);
   }
 }
 
@@ -724,22 +799,28 @@ int attn_num_sms() {
   return n;
 }
 
+// At d = 128, problems with at most this many query rows per KV head hold
+// 64-row Q and P tiles, which leaves shared memory for a fifth K/V stage.
+constexpr int kTrimRows = 64;
+
 struct AttnPlan {
-  int nrows, mtiles, mt_per_cta, mgroups, splits, tiles_per_split;
+  int nrows, mtiles, pipes, splits, tiles_per_split;
   size_t part_o_bytes, part_ml_bytes;
 };
 
-// One row tile per CTA.  Keys are split so that the CTAs (two per SM at
-// d = 64, one at d = 128) fill whole waves, with at least 4 tiles per split.
+// One row tile per work item; two pipelines per CTA at d = 64 (the two row
+// tiles of a KV head then read its pages once from HBM), one at d = 128 (all
+// of shared memory for the K/V ring).  One CTA is resident per SM.  Keys are
+// split so that the work items fill whole waves of pipelines, with at least 4
+// tiles per split.
 AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   AttnPlan p;
   p.nrows = (Hq / Hkv) * Nq;
   p.mtiles = (p.nrows + kRows - 1) / kRows;
-  p.mt_per_cta = 1;  // d = 64: two CTAs per SM instead of two row tiles per CTA
-  p.mgroups = (p.mtiles + p.mt_per_cta - 1) / p.mt_per_cta;
+  p.pipes = d == 64 ? 2 : 1;
   const int ntiles = (max_keys + kKeys - 1) / kKeys;
-  const long base = static_cast<long>(B) * Hkv * p.mgroups;
-  const long slots = attn_num_sms() * (d == 64 ? 2 : 1);  // resident CTAs
+  const long base = static_cast<long>(B) * Hkv * p.mtiles;
+  const long slots = static_cast<long>(attn_num_sms()) * p.pipes;  // concurrent work items
   // estimated time in tile-steps: whole waves x (tiles per split + a CTA's
   // set-up, about kSetupTiles tiles: masks, Q, TMEM, the first copies)
   constexpr double kSetupTiles = 4.0;
@@ -766,19 +847,20 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-template <int D, int MT, int CPS>
-cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a, dim3 grid,
+template <int D, int MT, int PL, int RA = kRows>
+cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a,
                              cudaStream_t cs) {
-  using CF = AttnCfg<D, MT, CPS>;
-  const int smem = CF::kTable + a.tiles_per_split * kTilePages * 4 + 1024;
+  using CF = AttnCfg<D, MT, PL, RA>;
+  const int smem = CF::kTable + PL * attn_tab_stride(a.tiles_per_split) * 4 + 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e =
-      cudaFuncSetAttribute(k_branch_attn_tc<D, MT, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(k_branch_attn_tc<D, MT, PL, RA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_branch_attn_tc<D, MT, CPS><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
+  const dim3 grid((a.items + PL - 1) / PL);
+  k_branch_attn_tc<D, MT, PL, RA><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
   e = cudaGetLastError();
   if (e == cudaSuccess && a.splits > 1) {
-    k_attn_combine<D><<<dim3(grid.x, a.mtiles), 128, 0, cs>>>(a);
+    k_attn_combine<D><<<dim3(a.B * a.Hkv, a.mtiles), 128, 0, cs>>>(a);
     e = cudaGetLastError();
   }
   return e;
@@ -846,11 +928,11 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   if (!make_kv_map(&kmap, k_cache, num_blocks, Hkv, d) || !make_kv_map(&vmap, v_cache, num_blocks, Hkv, d))
     return SSD_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  const dim3 grid(B * Hkv, p.mgroups, a.splits);
+  a.items = B * Hkv * p.mtiles * a.splits;
   cudaError_t e;
-  if (d == 64 && p.mt_per_cta == 2) e = launch_attention<64, 2, 1>(kmap, vmap, a, grid, cs);
-  else if (d == 64) e = launch_attention<64, 1, 2>(kmap, vmap, a, grid, cs);
-  else e = launch_attention<128, 1, 1>(kmap, vmap, a, grid, cs);
+  if (d == 64) e = launch_attention<64, 1, 2>(kmap, vmap, a, cs);
+  else if (p.nrows <= kTrimRows) e = launch_attention<128, 1, 1, kTrimRows>(kmap, vmap, a, cs);
+  else e = launch_attention<128, 1, 1>(kmap, vmap, a, cs);
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -45,7 +45,10 @@ def _check(ai, seqs=None):
     w.AttnSpec(B=1, Hq=32, Hkv=2, d=64, L=0, tree="chain", n_chain=1),   # no prefix, one node
     w.AttnSpec(B=2, Hq=8, Hkv=1, d=128, L=500, tree="fanout", K=4, F=(20, 4, 2, 1, 1),
                chain_len=4),                                              # N = 116 nodes
-], ids=["gqa4-d64", "gqa16-d128-chain", "ragged", "mha-d128", "single-node", "wide-tree"])
+    w.AttnSpec(B=2, Hq=16, Hkv=2, d=128, L=3000, tree="chain", n_chain=8,
+               ragged_prefix=True),                     # 64 rows per KV head, keys split
+], ids=["gqa4-d64", "gqa16-d128-chain", "ragged", "mha-d128", "single-node", "wide-tree",
+        "d128-64rows-split"])
 def test_small_shapes(spec):
     _check(w.make_attention(spec, seed=11))
 
