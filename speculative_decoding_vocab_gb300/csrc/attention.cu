@@ -251,13 +251,15 @@ struct AttnArgs {
 // how two tile streams share an SM.  RA < 128 serves problems with at most RA
 // query rows: the MMA still reads 128 rows of A, and rows RA..127 fall on the
 // next buffer (finite or not, they only feed TMEM lanes that no thread reads).
-template <int D, int MT, int PL, int RA = kRows>
+// NPB P buffers per row tile: with two, the softmax writes P of tile t while
+// P V of tile t - 1 runs; with one, it first waits for that P V.
+template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
 struct AttnCfg {
   static_assert(RA == kRows || (MT == 1 && RA % 32 == 0 && RA < kRows), "trimmed row tiles: one per pipeline");
   static constexpr int kQBytes = RA * D * 2;         // one row tile of Q
   static constexpr int kKVBytes = kKeys * D * 2;     // K or V of one key tile
   static constexpr int kPBytes = RA * kKeys * 2;     // one P buffer of one row tile
-  static constexpr int kFixed = MT * kQBytes + MT * 2 * kPBytes;
+  static constexpr int kFixed = MT * kQBytes + MT * NPB * kPBytes;
   static constexpr int kStagesFit = (216 * 1024 / PL - kFixed) / (2 * kKVBytes);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   // TMEM: S buffers (MT x 2 x 64 columns), then O (MT x D); a power of two
@@ -267,7 +269,7 @@ struct AttnCfg {
   static_assert(kTmemCols * PL <= 512, "TMEM of the pipelines");
   static constexpr int kQ = 0;
   static constexpr int kP = kQ + MT * kQBytes;
-  static constexpr int kKV = kP + MT * 2 * kPBytes;
+  static constexpr int kKV = kP + MT * NPB * kPBytes;
   static constexpr int kPipe = kKV + kStages * 2 * kKVBytes;  // one pipeline's region
   static constexpr int kTable = PL * kPipe;  // then each pipeline's block-table entries
   static constexpr int kPWarps = 4 * MT + 2;  // warps of one pipeline
@@ -280,17 +282,18 @@ struct AttnCfg {
   // the 128 A rows the MMA reads from the last Q column block and the last P
   // buffer stay inside the pipeline's region
   static_assert(kQ + MT * kQBytes - RA * 128 + kRows * 128 <= kPipe, "Q rows read by the MMA");
-  static_assert(kP + (MT * 2 - 1) * kPBytes + kRows * 128 <= kPipe, "P rows read by the MMA");
+  static_assert(kP + (MT * NPB - 1) * kPBytes + kRows * 128 <= kPipe, "P rows read by the MMA");
+  static_assert(NPB == 1 || NPB == 2, "one or two P buffers");
 };
 
 // int entries of one pipeline's block-table slice (16-byte multiple)
 __host__ __device__ inline int attn_tab_stride(int tiles_per_split) { return (tiles_per_split * kTilePages + 3) & ~3; }
 
-template <int D, int MT, int PL, int RA>
-__global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA>::kThreads, 1)
+template <int D, int MT, int PL, int RA, int NPB>
+__global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
     k_branch_attn_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ AttnArgs a) {
-  using CF = AttnCfg<D, MT, PL, RA>;
+  using CF = AttnCfg<D, MT, PL, RA, NPB>;
   constexpr int NS = CF::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
@@ -412,10 +415,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA>::kThreads, 1)
   const bool warp_active = __any_sync(0xffffffffu, row_valid);
   if (softmax_thread && !warp_active && r_own < RA) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+    for (int u = 0; u < NPB; ++u)
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4)
-        *reinterpret_cast<uint4 *>(smem + CF::kP + (m_own * 2 + u) * CF::kPBytes + sw128(r_own, q4)) =
+        *reinterpret_cast<uint4 *>(smem + CF::kP + (m_own * NPB + u) * CF::kPBytes + sw128(r_own, q4)) =
             make_uint4(0, 0, 0, 0);
   }
   if (softmax_thread && r_own < RA) {
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA>::kThreads, 1)
             return;
           }
           tc_fence_after();
-          const uint32_t p_base = smem_u32(smem + CF::kP + (m * 2 + (u & 1)) * CF::kPBytes);
+          const uint32_t p_base = smem_u32(smem + CF::kP + (m * NPB + u % NPB) * CF::kPBytes);
           const uint32_t tO = tmem + CF::kOCol + m * D;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -585,8 +588,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA>::kThreads, 1)
       float tmax = row_valid ? t8[0] : NEG_INF;
       tmax = (tmax == NEG_INF) ? NEG_INF : __fmul_rn(tmax, c);
       const bool grow = tmax != NEG_INF && (m_used == NEG_INF || tmax > m_used + 8.f);
-      // P buffer u is free once P V of tile i - 2 completed
-      if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[m][u], ((i - 2) >> 1) & 1))) {
+      // the P buffer of tile i is free once P V of tile i - NPB completed
+      if (i >= NPB && !__all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[m][(i - NPB) & 1], ((i - NPB) >> 1) & 1))) {
         s_abort = 1;
         break;
       }
@@ -618,7 +621,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA>::kThreads, 1)
         m_used = tmax;
       }
       // P = 2^(s c - m) in bf16, 128 bytes of this row in the swizzled K-major tile
-      uint8_t *prow = smem + CF::kP + (m * 2 + u) * CF::kPBytes;
+      uint8_t *prow = smem + CF::kP + (m * NPB + i % NPB) * CF::kPBytes;
       const uint64_t c2 = pack2(c, c), nm2 = pack2(-m_used, -m_used);
       const bool any = row_valid && m_used != NEG_INF;
       uint64_t la[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)}, lxa[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
@@ -800,7 +803,8 @@ int attn_num_sms() {
 }
 
 // At d = 128, problems with at most this many query rows per KV head hold
-// 64-row Q and P tiles, which leaves shared memory for a fifth K/V stage.
+// 64-row Q and one 64-row P buffer, which leaves shared memory for six K/V
+// stages instead of four.
 constexpr int kTrimRows = 64;
 
 struct AttnPlan {
@@ -847,17 +851,27 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-template <int D, int MT, int PL, int RA = kRows>
+template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
 cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a,
                              cudaStream_t cs) {
-  using CF = AttnCfg<D, MT, PL, RA>;
+  using CF = AttnCfg<D, MT, PL, RA, NPB>;
   const int smem = CF::kTable + PL * attn_tab_stride(a.tiles_per_split) * 4 + 1024;
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  // dynamic + static shared memory within the per-block opt-in limit
+  static const int room = [] {
+    cudaFuncAttributes fa;
+    int dev = 0, optin = 0;
+    if (cudaFuncGetAttributes(&fa, k_branch_attn_tc<D, MT, PL, RA, NPB>) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return 227 * 1024 - 4096;
+    return optin - static_cast<int>(fa.sharedSizeBytes);
+  }();
+  if (smem > room) return cudaErrorInvalidValue;
   cudaError_t e =
-      cudaFuncSetAttribute(k_branch_attn_tc<D, MT, PL, RA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(k_branch_attn_tc<D, MT, PL, RA, NPB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.items + PL - 1) / PL);
-  k_branch_attn_tc<D, MT, PL, RA><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
+  k_branch_attn_tc<D, MT, PL, RA, NPB><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
   e = cudaGetLastError();
   if (e == cudaSuccess && a.splits > 1) {
     k_attn_combine<D><<<dim3(a.B * a.Hkv, a.mtiles), 128, 0, cs>>>(a);
@@ -931,8 +945,13 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   a.items = B * Hkv * p.mtiles * a.splits;
   cudaError_t e;
   if (d == 64) e = launch_attention<64, 1, 2>(kmap, vmap, a, cs);
-  else if (p.nrows <= kTrimRows) e = launch_attention<128, 1, 1, kTrimRows>(kmap, vmap, a, cs);
-  else e = launch_attention<128, 1, 1>(kmap, vmap, a, cs);
+  else {
+    // six stages with 64-row tiles and one P buffer, unless the key range's
+    // block-table slice leaves no room for them (then four)
+    e = cudaErrorInvalidValue;
+    if (p.nrows <= kTrimRows) e = launch_attention<128, 1, 1, kTrimRows, 1>(kmap, vmap, a, cs);
+    if (e == cudaErrorInvalidValue) e = launch_attention<128, 1, 1>(kmap, vmap, a, cs);
+  }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -148,14 +148,15 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
     return rep
 
 
-def gpu_attention(ai: w.AttnInputs, dev="cuda"):
+def gpu_attention(ai: w.AttnInputs, dev="cuda", use_ws=True):
+    """Run ssd_branch_attention; without a workspace the keys are not split."""
     q = to_dev(ai.q, dev)
     out = torch.full_like(q, float("nan"))
     lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     s = ai.spec
     ws_n = ssd.ssd_attention_workspace_size(s.B, ai.Nq, s.Hq, s.Hkv, s.d, int(ai.prefix_len.max()))
-    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev) if use_ws else None
     ssd.ssd_branch_attention(q, to_dev(ai.k_cache, dev), to_dev(ai.v_cache, dev),
                              to_dev(ai.block_table, dev), to_dev(ai.prefix_len, dev),
                              to_dev(ai.parent, dev), out, lse=lse, status=status, ws=ws)

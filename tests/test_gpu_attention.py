@@ -23,8 +23,8 @@ def _lib():
     ssd.load()
 
 
-def _check(ai, seqs=None):
-    out, lse, st = gpu_attention(ai)
+def _check(ai, seqs=None, use_ws=True):
+    out, lse, st = gpu_attention(ai, use_ws=use_ws)
     idx = np.arange(ai.spec.B) if seqs is None else np.asarray(seqs)
     ref, rlse, fl = oracle.branch_attention(ai.q[idx], ai.k_cache, ai.v_cache, ai.block_table[idx],
                                             ai.prefix_len[idx], ai.parent[idx], ai.spec.Hkv)
@@ -51,6 +51,13 @@ def _check(ai, seqs=None):
         "d128-64rows-split"])
 def test_small_shapes(spec):
     _check(w.make_attention(spec, seed=11))
+
+
+def test_long_unsplit_keys_d128():
+    """30,000 keys in one key range (no workspace): the block-table slice leaves
+    no room for the six-stage d = 128 kernel, so the four-stage one runs."""
+    spec = w.AttnSpec(B=1, Hq=8, Hkv=1, d=128, L=30000, tree="chain", n_chain=4)
+    _check(w.make_attention(spec, seed=5), use_ws=False)
 
 
 def test_draft_branch_attention_full():
