@@ -944,7 +944,7 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
   a.items = B * Hkv * p.mtiles * a.splits;
   cudaError_t e;
-  if (d == 64) e = launch_attention<64, 1, 2>(kmap, vmap, a, cs);
+  if (d == 64) e = launch_attention<64, 1, 2, kRows, 1>(kmap, vmap, a, cs);
   else {
     // six stages with 64-row tiles and one P buffer, unless the key range's
     // block-table slice leaves no room for them (then four)
