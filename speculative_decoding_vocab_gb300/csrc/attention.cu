@@ -11,10 +11,12 @@
 // once per (sequence, KV head, group of row tiles).
 //
 // A work item = (sequence b, KV head, tile of 128 query rows, range of keys).
-// A kernel that allocates TMEM is resident once per SM.  At d = 64 one CTA
-// runs two independent pipelines, each on its own work item with 256 TMEM
-// columns; at d = 128 it runs one, with all of shared memory for its K/V ring
-// (Q and P held as 64-row tiles when at most 64 query rows share a KV head).
+// At d = 64 one CTA runs two independent pipelines, each on its own work item
+// with 256 TMEM columns, so an SM carries two tile streams without relying on
+// two CTAs being co-resident (the CUDA occupancy calculator counts one for a
+// kernel that allocates TMEM).  At d = 128 it runs one, with all of shared
+// memory for its K/V ring (Q and P held as 64-row tiles when at most 64 query
+// rows share a KV head).
 // Each pipeline is warp-specialised:
 //   * a producer warp fetches the K and V pages of each 64-key tile by TMA
 //     through the block table into a ring of stages (mbarrier completion);
@@ -247,10 +249,10 @@ struct AttnArgs {
 // Shared-memory plan of a CTA at head dimension D that runs PL independent
 // pipelines (each its own work item, Q, K/V ring, barriers and TMEM columns),
 // each with MT row tiles of which RA rows of Q and P are held in shared
-// memory.  A kernel that allocates TMEM is resident once per SM, so PL = 2 is
-// how two tile streams share an SM.  RA < 128 serves problems with at most RA
-// query rows: the MMA still reads 128 rows of A, and rows RA..127 fall on the
-// next buffer (finite or not, they only feed TMEM lanes that no thread reads).
+// memory.  PL = 2 puts two tile streams on an SM within one CTA.  RA < 128
+// serves problems with at most RA query rows: the MMA still reads 128 rows of
+// A, and rows RA..127 fall on the next buffer (finite or not, they only feed
+// TMEM lanes that no thread reads).
 // NPB P buffers per row tile: with two, the softmax writes P of tile t while
 // P V of tile t - 1 runs; with one, it first waits for that P V.
 template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
@@ -814,7 +816,7 @@ struct AttnPlan {
 
 // One row tile per work item; two pipelines per CTA at d = 64 (the two row
 // tiles of a KV head then read its pages once from HBM), one at d = 128 (all
-// of shared memory for the K/V ring).  One CTA is resident per SM.  Keys are
+// of shared memory for the K/V ring), one CTA per SM.  Keys are
 // split so that the work items fill whole waves of pipelines, with at least 4
 // tiles per split.
 AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
