@@ -816,9 +816,9 @@ struct AttnPlan {
 
 // One row tile per work item; two pipelines per CTA at d = 64 (the two row
 // tiles of a KV head then read its pages once from HBM), one at d = 128 (all
-// of shared memory for the K/V ring), one CTA per SM.  Keys are
-// split so that the work items fill whole waves of pipelines, with at least 4
-// tiles per split.
+// of shared memory for the K/V ring), one CTA per SM.  Keys are split so that
+// the work items fill whole waves of pipelines, with at least 4 tiles per
+// split.
 AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   AttnPlan p;
   p.nrows = (Hq / Hkv) * Nq;
@@ -827,15 +827,15 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
   const int ntiles = (max_keys + kKeys - 1) / kKeys;
   const long base = static_cast<long>(B) * Hkv * p.mtiles;
   const long slots = static_cast<long>(attn_num_sms()) * p.pipes;  // concurrent work items
-  // estimated time in tile-steps: whole waves x (tiles per split + a CTA's
-  // set-up, about kSetupTiles tiles: masks, Q, TMEM, the first copies)
+  // estimated time in tile-steps: whole waves x (tiles per split + a work
+  // item's set-up, about kSetupTiles tiles: masks, Q, TMEM, the first copies)
   constexpr double kSetupTiles = 4.0;
   int best = 1;
   double best_cost = 0.0;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && ntiles / s < 4) break;
-    const long ctas = base * s;
-    const double waves = std::ceil(static_cast<double>(ctas) / slots);
+    const long items = base * s;
+    const double waves = std::ceil(static_cast<double>(items) / slots);
     const double cost = waves * (std::ceil(static_cast<double>(ntiles) / s) + kSetupTiles);
     if (s == 1 || cost < best_cost * 0.97) {
       best_cost = cost;
