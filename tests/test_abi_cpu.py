@@ -71,6 +71,20 @@ def test_workspace_size(lib):
     assert ssd.ssd_workspace_size(2, 1, 1000, "f32", (300, 1)) == 0          # F > 256
 
 
+def test_attention_workspace_size(lib):
+    """Key-split partials: O (d floats) and (m, l, unrounded l) per row of every
+    split, in two 256-byte aligned arrays; none when the work items already fill
+    the GPU."""
+    B, Hkv, d = 64, 8, 128
+    per_split = B * Hkv * 128 * d * 4 + B * Hkv * 128 * 3 * 4  # one row tile per KV head
+    n = ssd.ssd_attention_workspace_size(B, 6, 64, Hkv, d, 8192)
+    assert n > 0 and n % per_split == 0 and 2 <= n // per_split <= 16
+    # draft tree shape: its 256 row tiles run as pipelines without splitting the keys
+    assert ssd.ssd_attention_workspace_size(16, 64, 32, 8, 64, 2048) == 0
+    assert ssd.ssd_attention_workspace_size(2, 6, 12, 8, 128, 100) == 0    # Hq % Hkv != 0
+    assert ssd.ssd_attention_workspace_size(0, 6, 64, 8, 128, 100) == 0    # no sequences
+
+
 def _F(F):
     return (ctypes.c_int32 * len(F))(*F)
 
