@@ -7,8 +7,9 @@
 // Row i of head h (query node m = N - Nq + i) sees every prefix position and
 // the tree nodes on m's ancestor-or-self path; node n's K/V sits at logical
 // position prefix_len + n.  GQA: head h reads KV head h / (Hq / Hkv), and all
-// the query heads of one KV head share a CTA's rows, so each K/V page is read
-// once per (sequence, KV head, group of row tiles).
+// the query heads of one KV head share the rows of a row tile, so each K/V page
+// is read once per (sequence, KV head, row tile); at d = 64 the two row tiles of
+// a KV head run in one CTA, and the second read comes from L2.
 //
 // A work item = (sequence b, KV head, tile of 128 query rows, range of keys).
 // At d = 64 one CTA runs two independent pipelines, each on its own work item
@@ -27,7 +28,7 @@
 //     (the running maximum only moves, and O is rescaled in TMEM, when it grows
 //     by more than 2^8), writes P (bf16) to shared memory;
 //   * the softmax threads end by normalising O, or write (O, m, l) partials that
-//     a combine kernel merges when the keys are split across CTAs.
+//     a combine kernel merges when the keys are split across work items.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
 #pragma unroll
     for (int w = 0; w < kMaxNodes / 32; ++w) anc[m][w] = bits[w];
   }
-  // block-table entries of this CTA's key range (-1: past the table or the keys, or a bad id)
+  // block-table entries of this pipeline's key range (-1: past the table or the keys, or a bad id)
   int *tab = reinterpret_cast<int *>(smem_all + CF::kTable) + pl * attn_tab_stride(a.tiles_per_split);
   const int page0 = t_begin * kTilePages;
   const int npages = nt * kTilePages;
