@@ -2083,8 +2083,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   a.b0 = 0;
   if (g_ev_after) cudaEventRecord(g_ev_after, s);
   if (n2 > 0) {
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(n2));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
