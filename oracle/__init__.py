@@ -29,6 +29,7 @@ FLAG_ZERO_RESIDUAL = 2
 FLAG_BAD_OUTCOME = 8
 FLAG_BAD_TREE = 16
 FLAG_BAD_BLOCK = 32
+FLAG_BAD_PREFIX = 64
 
 
 def build(force: bool = False) -> str:

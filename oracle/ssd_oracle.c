@@ -55,6 +55,7 @@
 #define OR_FLAG_BAD_OUTCOME 8u
 #define OR_FLAG_BAD_TREE 16u
 #define OR_FLAG_BAD_BLOCK 32u
+#define OR_FLAG_BAD_PREFIX 64u
 
 static double load_elem(const void *base, int dtype, int64_t i) {
   if (dtype == OR_F32) return (double)((const float *)base)[i];
@@ -432,7 +433,8 @@ int oracle_lookup(const int32_t *guess, const int32_t *payload, int B, int K, co
 /* h / (Hq / Hkv).  out = softmax(scale * q k^T over the visible keys) v,   */
 /* lse = log sum exp(scale * q k^T) (natural log), both in double.          */
 /* A parent outside [-1, m-1] ends the path (BAD_TREE); a block id outside  */
-/* [0, num_blocks) hides the keys it would hold (BAD_BLOCK).                */
+/* [0, num_blocks) hides the keys it would hold (BAD_BLOCK); a negative     */
+/* prefix counts as 0 and positions past 16 * maxb are hidden (BAD_PREFIX). */
 /* ---------------------------------------------------------------------- */
 int oracle_branch_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                             const int32_t *block_table, int maxb, int64_t num_blocks,
@@ -444,6 +446,13 @@ int oracle_branch_attention(const uint16_t *q, const uint16_t *k_cache, const ui
   for (int b = 0; b < B; b++) {
     uint32_t fl = 0;
     int L = prefix_len[b];
+    /* a prefix the block table cannot hold: a negative one counts as 0, and the
+     * positions past the table's 16 * maxb are hidden */
+    if (L < 0) {
+      fl |= OR_FLAG_BAD_PREFIX;
+      L = 0;
+    }
+    if ((int64_t)L + N > (int64_t)maxb * page) fl |= OR_FLAG_BAD_PREFIX;
     int nkeys_max = L + N;
     int32_t *keys = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nkeys_max > 0 ? nkeys_max : 1));
     double *s = (double *)malloc(sizeof(double) * (size_t)(nkeys_max > 0 ? nkeys_max : 1));
@@ -473,6 +482,10 @@ int oracle_branch_attention(const uint16_t *q, const uint16_t *k_cache, const ui
         int nvis = 0;
         for (int t = 0; t < nk; t++) {
           int pos = keys[t];
+          if (pos / page >= maxb) { /* past the table: hidden */
+            s[t] = -INFINITY;
+            continue;
+          }
           int blk = block_table[(int64_t)b * maxb + pos / page];
           if (blk < 0 || blk >= num_blocks) {
             fl |= OR_FLAG_BAD_BLOCK;

@@ -6,7 +6,11 @@ brute force on tiny inputs, and chi-squared tests of the losslessness the pages
 state (机器之心 article "全球最強推理引擎還快2倍…", section "SSD 如何實現草擬與驗證并行？":
 the scheme samples exactly from the target distribution).
 """
+import contextlib
+import ctypes
 import os
+import subprocess
+import tempfile
 from fractions import Fraction
 from itertools import product
 
@@ -153,6 +157,131 @@ def test_inv_cdf_exact_frequencies():
         assert lo <= (k / n) * wts.sum() < c[i]
         counts[i] += 1
     assert np.array_equal(counts, (wts / wts.sum() * n).astype(int))
+
+
+# ---------------------------------------------------------------------------
+# near-tie margins: the oracle outputs that decide which GPU / oracle integer
+# differences the parity tests excuse (the 1e-6 near-tie window), pinned to
+# hand-computed values; the mutants below show that the pins have power
+# ---------------------------------------------------------------------------
+def _pin_inv_cdf_margin():
+    """The margin is the distance of u*W to the nearer edge of the chosen bin,
+    over W.  Unnormalised dyadic weights (W = 64) keep every edge and u*W exact
+    in fp64, so the expected value is exact too."""
+    wts = np.array([0, 3, 0, 5, 8, 0, 16, 32], np.float64)
+    edges = np.concatenate([[0.0], np.cumsum(wts)])
+    W = wts.sum()
+    for k in range(256):
+        u = k / 256
+        t = u * W
+        i, m = oracle.inv_cdf(wts, u)
+        assert edges[i] <= t < edges[i + 1]
+        expect = min(t - edges[i], edges[i + 1] - t) / W
+        assert m == expect, (u, i, m, expect)
+
+
+def _worked_rows():
+    g = {r[0]: float(Fraction(r[1])) for r in _golden_rows("saguaro_worked_example.txt")}
+    p = np.array([g["p0"], g["p1"], g["p2"]])
+    q = np.array([g["q0"], g["q1"], g["q2"]])
+    zt = np.stack([np.log(p), np.log(p)]).astype(np.float32)[None]
+    zd = np.stack([np.log(q), np.log(q)]).astype(np.float32)[None]
+    return zt, zd
+
+
+def _pin_draft_margin():
+    """q' = (1/3, 2/5, 4/15) (the worked sigma_{1,1/2} example, edges 0, 1/3,
+    11/15, 1): u = 1/2 lands in bin 1 with distances 1/6 and 7/30; u = 1/8 in
+    bin 0 (1/8, 5/24); u = 11/16 in bin 1 (17/48, 11/240).  Greedy draws have
+    no margin (inf)."""
+    zt, zd = _worked_rows()
+    for u, expect in ((0.5, 1 / 6), (0.125, 0.125), (0.6875, 11 / 240)):
+        _, _, m = oracle.saguaro_sample(zd, 3, (1, 1), 0.5, 1.0, np.array([[u]], np.float32))
+        assert abs(m[0, 0] - expect) < 1e-6, (u, m[0, 0], expect)
+    _, _, m = oracle.saguaro_sample(zd, 3, (1, 1), 0.5, 0.0, np.array([[0.5]], np.float32))
+    assert m[0, 0] == np.inf
+
+
+def _pin_verify_margins():
+    """Worked example, d_1 = 1 with p/q' = 1/2: acc_margin = |u - 1/2| = 1/4
+    for u = 3/4 (rejected) and u = 1/4 (accepted).  After the rejection the
+    residual (0, 0, 1/3) has W = 1/3 and one bin [0, 1/3): u_bonus = 1/2 is
+    1/2 of W from either edge, u_bonus = 1/8 is 1/8 from the lower one.  After
+    the acceptance the bonus comes from p_2 = (1/5, 1/5, 3/5): u_bonus = 1/2
+    falls in [2/5, 1), 1/10 above its lower edge."""
+    zt, zd = _worked_rows()
+    d = np.array([[1]], np.int32)
+
+    def run(ua, ub, T=1.0):
+        return oracle.verify(zt, zd, 3, (1, 1), 0.5, T, d, np.array([[ua]], np.float32),
+                             np.array([ub], np.float32))
+    rej = run(0.75, 0.5)
+    assert rej["accept_len"][0] == 0
+    assert abs(rej["acc_margin"][0, 0] - 0.25) < 1e-6
+    assert abs(rej["bonus_margin"][0] - 0.5) < 1e-6
+    assert abs(run(0.75, 0.125)["bonus_margin"][0] - 0.125) < 1e-6
+    acc = run(0.25, 0.5)
+    assert acc["accept_len"][0] == 1
+    assert abs(acc["acc_margin"][0, 0] - 0.25) < 1e-6
+    assert abs(acc["bonus_margin"][0] - 0.1) < 1e-6
+    greedy = run(0.75, 0.5, T=0.0)
+    assert greedy["acc_margin"][0, 0] == np.inf and greedy["bonus_margin"][0] == np.inf
+
+
+def test_inv_cdf_margin_is_distance_to_nearer_edge():
+    _pin_inv_cdf_margin()
+
+
+def test_draft_margin_worked_example():
+    _pin_draft_margin()
+
+
+def test_verify_margins_worked_example():
+    _pin_verify_margins()
+
+
+@contextlib.contextmanager
+def _mutant_oracle(old: str, new: str):
+    """The oracle with one planted mistake: its C source with ``old`` replaced
+    by ``new``, compiled into a temporary library that the ``oracle`` module
+    uses until the block ends."""
+    with open(oracle._SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, old
+    with tempfile.TemporaryDirectory() as tmp:
+        c_path = os.path.join(tmp, "mutant.c")
+        so_path = os.path.join(tmp, "libmutant.so")
+        with open(c_path, "w") as f:
+            f.write(src.replace(old, new))
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", so_path, c_path,
+                               "-lm"])
+        lib = ctypes.CDLL(so_path)
+        oracle._declare(lib)
+        saved = oracle._L()
+        oracle._lib = lib
+        try:
+            yield
+        finally:
+            oracle._lib = saved
+
+
+_MARGIN_LINE = "*margin = (lo < hi ? lo : hi) / W;"
+
+
+@pytest.mark.parametrize("old,new,pins", [
+    (_MARGIN_LINE, "*margin = 0.0;", ("inv_cdf", "draft", "verify")),         # margin left at 0
+    (_MARGIN_LINE, "*margin = (lo < hi ? hi : lo) / W;", ("inv_cdf", "draft", "verify")),  # far edge
+    (_MARGIN_LINE, "*margin = (lo < hi ? lo : hi);", ("inv_cdf", "verify")),  # not divided by W
+    ("fabs(u - pd / qd)", "0.0", ("verify",)),                                  # acceptance margin 0
+    ("fabs(u - pd / qd)", "fabs(u - qd / pd)", ("verify",)),                    # ratio inverted
+])
+def test_margin_pins_catch_planted_mistakes(old, new, pins):
+    run = {"inv_cdf": _pin_inv_cdf_margin, "draft": _pin_draft_margin, "verify": _pin_verify_margins}
+    with _mutant_oracle(old, new):
+        for name in pins:
+            with pytest.raises(AssertionError):
+                run[name]()
+    _pin_inv_cdf_margin()  # the real oracle is back
 
 
 # ---------------------------------------------------------------------------
@@ -557,3 +686,28 @@ def test_attention_flags_bad_tree_and_block():
     _, _, fl = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, tab, inp.prefix_len,
                                        inp.parent, spec.Hkv)
     assert fl[0] & oracle.FLAG_BAD_BLOCK
+
+
+def test_attention_prefix_past_the_table_is_hidden():
+    """A prefix the block table cannot hold: positions at or past 16 * maxb are
+    hidden and flagged (dense reference with those positions masked, gathered
+    through a table padded with a real block); a negative prefix counts as 0."""
+    spec = w.AttnSpec(B=2, Hq=4, Hkv=2, d=16, L=40, tree="chain", n_chain=4)
+    inp = w.make_attention(spec, seed=8)
+    maxb = inp.block_table.shape[1]
+    inp.prefix_len[0] = 16 * maxb - 2  # two nodes in the table, two past it
+    inp.prefix_len[1] = -5
+    out, lse, fl = oracle.branch_attention(inp.q, inp.k_cache, inp.v_cache, inp.block_table,
+                                           inp.prefix_len, inp.parent, spec.Hkv)
+    assert fl[0] & oracle.FLAG_BAD_PREFIX and fl[1] & oracle.FLAG_BAD_PREFIX
+    padded = w.AttnInputs(**{**inp.__dict__})
+    padded.block_table = np.concatenate([inp.block_table, inp.block_table[:, :1]], axis=1)
+    padded.prefix_len = np.maximum(inp.prefix_len, 0)
+
+    def visible(b, node):
+        L = int(padded.prefix_len[b])
+        pos = np.arange(L + inp.N)
+        return (pos <= L + node) & (pos < 16 * maxb)
+
+    ref, rlse = _dense_reference(padded, visible)
+    assert np.allclose(out, ref, atol=1e-12) and np.allclose(lse, rlse, atol=1e-12)
