@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -162,7 +163,7 @@ def make_outputs(spec, device):
                 resid_mass=torch.empty(B, **f32), guess=torch.empty(B, sumF, **i32),
                 guess_q=torch.empty(B, sumF, **f32), slot=torch.empty(B, **i32),
                 next_tokens=torch.empty(B, K, **i32), hits=torch.zeros(1, **i32),
-                status=torch.zeros(1, **i32))
+                near_ties=torch.zeros(1, **i32), status=torch.zeros(1, **i32))
 
 
 def run_round(ssd, spec, buf, out, ws):
@@ -171,7 +172,7 @@ def run_round(ssd, spec, buf, out, ws):
                   payload=buf.payload, qd_out=out["qd"], accept_prob=out["accept_prob"],
                   resid_mass=out["resid_mass"], guess=out["guess"], guess_q=out["guess_q"],
                   slot=out["slot"], next_tokens=out["next_tokens"], hits=out["hits"],
-                  status=out["status"], ws=ws)
+                  status=out["status"], ws=ws, near_ties=out["near_ties"])
 
 
 def kernels_per_round(spec) -> int:
@@ -267,6 +268,7 @@ def bench_ours(args):
 
     # timed region: K rounds, each a graph replay of one input set's round
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out["near_ties"].zero_()
     barrier(device)
     torch.cuda.synchronize()
     start.record(stream)
@@ -288,6 +290,12 @@ def bench_ours(args):
     sampler.stop()
     clocks = sampler.summary(t_load0, t_load1)
     status = int(out["status"].item())
+    # near-ties of the K timed rounds alone
+    out["near_ties"].zero_()
+    for s in range(K):
+        graphs[s % nsets].replay()
+    torch.cuda.synchronize()
+    near_k = int(out["near_ties"].item())
 
     peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs") or 6800.0
@@ -315,12 +323,16 @@ def bench_ours(args):
         "gpu_launches": kernels_per_round(spec) * K,
         "clocks": clocks,
         "status_flags": status,
+        "near_ties": {"count": near_k, "rounds": K, "sequences": K * spec.B,
+                      "what": "draws within 1e-6 W of a bin edge and acceptance tests with "
+                              "|u - p/q'| < 1e-6 (GPU fp32 count, ssd_round near_ties output)"},
     }
     result["step_roofline_frac"] = round(alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4)
     if not args.no_extras:
         result["e2e"] = bench_e2e(ssd, spec, inp, device, K, W)
         result["branch_attention"] = bench_attention(ssd, device, hbm_peak)
         result["other_rounds"] = bench_other_rounds(ssd, w, device, hbm_peak)
+        result["tiny_round"] = bench_tiny_round(ssd, w, device)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(spec, inp, args.cpu_seconds)
     if rank == 0:
@@ -453,12 +465,33 @@ def bench_attention(ssd, device, hbm_peak):
     return res
 
 
+def bench_tiny_round(ssd, w, device):
+    """The tiny round (B=1, K=4, V=4096 fp32): latency-bound, so its figure is
+    microseconds per round (graph replays over 64 seeded rounds)."""
+    import torch
+    spec = w.tiny_round()
+    nsets = 64
+    sets = [RoundBuffers(spec, w.make_round(spec, seed=0, rnd=r), device) for r in range(nsets)]
+    out = make_outputs(spec, device)
+    ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
+    for i in range(3):
+        run_round(ssd, spec, sets[i], out, ws)
+    graphs = capture_graphs([lambda b=b: run_round(ssd, spec, b, out, ws) for b in sets], device)
+    stream = torch.cuda.current_stream(device)
+    ms = _time_calls(lambda i: graphs[i % nsets].replay(), 500, stream)
+    return {"workload": spec.name, "us_per_round": round(ms * 1e3, 2),
+            "seq_rounds_per_s": round(spec.B / (ms * 1e-3), 1),
+            "note": "back-to-back graph replays of one round each (B = 1): latency, not bandwidth"}
+
+
 def bench_other_rounds(ssd, w, device, hbm_peak):
-    """The large-batch Qwen-3 round and the at-scale Llama-3 round (seq-rounds/s)."""
+    """The large-batch Qwen-3 round for each Saguaro C (with its cache hit rate),
+    the at-scale Llama-3 round and the greedy Llama-3 round (seq-rounds/s)."""
     import torch
     res = {}
     stream = torch.cuda.current_stream(device)
-    for spec in (w.qwen3_round(C=0.5), w.llama3_round_at_scale(), w.llama3_round(T=0.0)):
+    for spec in (w.qwen3_round(C=1.0), w.qwen3_round(C=0.5), w.qwen3_round(C=0.25),
+                 w.llama3_round_at_scale(), w.llama3_round(T=0.0)):
         g = torch.Generator(device=device)
         g.manual_seed(11)
         shape = (spec.B, spec.K + 1, spec.V)
@@ -489,7 +522,7 @@ def bench_other_rounds(ssd, w, device, hbm_peak):
         graphs = capture_graphs([lambda i=i: call(i) for i in range(nsets)], device)
         ms = _time_calls(lambda i: graphs[i % nsets].replay(), 50, stream)
         res[spec.name] = {"ms": round(ms, 4), "seq_rounds_per_s": round(spec.B / (ms * 1e-3), 1),
-                          "algorithmic_bytes": per,
+                          "algorithmic_bytes": per, "C": spec.C, "T": spec.T,
                           "frac_of_hbm_peak": round(per / (ms * 1e-3) / 1e9 / hbm_peak, 4),
                           "hit_rate": round(int(out["hits"].item()) / spec.B, 4)}
         del graphs, sets, out, ws
@@ -508,22 +541,67 @@ def cpu_sample(spec, inp, nseq):
                          inp.u_bonus[idx], inp.payload[idx])
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in outp.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_rounds(sub, cores: int):
+    """The oracle's whole round over the sample's sequences, split over `cores`
+    threads (its C functions release the GIL); returns the wall time."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from speculative_decoding_vocab_gb300 import workloads as w
+    B = sub.spec.B
+    step = -(-B // cores)
+    parts = []
+    for lo in range(0, B, step):
+        hi = min(B, lo + step)
+        sp = w.RoundSpec(**{**sub.spec.__dict__, "B": hi - lo})
+        parts.append(w.RoundInputs(sp, sub.target[lo:hi], sub.draft[lo:hi], sub.u_draft[lo:hi],
+                                   sub.u_acc[lo:hi], sub.u_bonus[lo:hi], sub.payload[lo:hi]))
+    t0 = time.perf_counter()
+    if cores == 1:
+        oracle.run_round(sub)
+    else:
+        with ThreadPoolExecutor(max_workers=cores) as ex:
+            list(ex.map(oracle.run_round, parts))
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(spec, inp, seconds):
+    """The oracle timed on all host cores and on one core, on bounded samples
+    of the workload (about `seconds` of one core's work for the one-core
+    figure, a full batch of B sequences over all cores)."""
     import oracle
     oracle.build()
-    # calibrate on 2 sequences, then time a sample sized to about `seconds`
-    t0 = time.perf_counter()
-    oracle.run_round(cpu_sample(spec, inp, 2))
-    per_seq = (time.perf_counter() - t0) / 2
-    nseq = int(max(2, min(256, seconds / max(per_seq, 1e-6))))
-    sub = cpu_sample(spec, inp, nseq)
-    t0 = time.perf_counter()
-    oracle.run_round(sub)
-    dt = time.perf_counter() - t0
-    return {"value": round(nseq / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{nseq} sequences of the {spec.name} round (full V, all K+1 rows; "
-                      f"sample + verify + predict + lookup in fp64), {dt:.1f} s",
-            "host_cpus": os.cpu_count()}
+    cores = max(1, os.cpu_count() or 1)
+    # calibrate on 2 sequences, then time a one-core sample sized to about `seconds`
+    per_seq = oracle_rounds(cpu_sample(spec, inp, 2), 1) / 2
+    n1 = int(max(2, min(spec.B, seconds / max(per_seq, 1e-6))))
+    dt1 = oracle_rounds(cpu_sample(spec, inp, n1), 1)
+    nall = spec.B if cores > 1 else n1
+    dtall = oracle_rounds(cpu_sample(spec, inp, nall), cores) if cores > 1 else dt1
+    return {"value": round(nall / dtall, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{nall} sequences of the {spec.name} round (full V, all K+1 rows; sample + "
+                      f"verify + predict + lookup in fp64) over {cores} threads, {dtall:.1f} s",
+            "one_core": {"value": round(n1 / dt1, 3), "unit": UNIT, "cores": 1,
+                         "sample": f"{n1} sequences, {dt1:.1f} s"},
+            "cpu_model": cpu_model(), "nproc": cores}
 
 
 def bench_reference(args):
@@ -535,14 +613,12 @@ def bench_reference(args):
     oracle.build()
     spec = round_spec()
     inp = w.make_round(spec, seed=0)
-    nseq = args.ref_seqs
+    cores = max(1, os.cpu_count() or 1)
+    nseq = min(spec.B, args.ref_seqs * cores)
     sub = cpu_sample(spec, inp, nseq)
     for _ in range(args.warmup):
-        oracle.run_round(cpu_sample(spec, inp, 1))
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.run_round(sub)
-    dt = (time.perf_counter() - t0) / args.steps
+        oracle_rounds(cpu_sample(spec, inp, min(nseq, cores)), cores)
+    dt = sum(oracle_rounds(sub, cores) for _ in range(args.steps)) / args.steps
     value = nseq / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
@@ -551,9 +627,10 @@ def bench_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same workload as our arm)",
         "config": {"workload": spec.name, "B": spec.B, "K": spec.K, "V": spec.V,
                    "input_dtype": "bf16", "T": spec.T, "C": spec.C, "F": list(spec.F),
-                   "reference": "fp64 CPU oracle (oracle/ssd_oracle.c), one host core"},
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{nseq} sequences per step of the {spec.name} round"},
+                   "reference": f"fp64 CPU oracle (oracle/ssd_oracle.c) over {cores} host threads"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{nseq} sequences per step of the {spec.name} round",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -621,7 +698,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-seqs", type=int, default=2)
+    ap.add_argument("--ref-seqs", type=int, default=2,
+                    help="reference arm: sequences per host core per step (capped at one batch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e / attention / other rounds")
     ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify"),

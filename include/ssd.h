@@ -73,6 +73,8 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
 #define SSD_FLAG_BAD_OUTCOME 8u   /* lookup: accept count outside [0, K]: treated as a miss */
 #define SSD_FLAG_BAD_TREE 16u     /* attention: parent[m] outside [-1, m-1]: path ends there */
 #define SSD_FLAG_BAD_BLOCK 32u    /* attention: block id outside [0, num_blocks): keys hidden */
+#define SSD_FLAG_BAD_PREFIX 64u   /* attention: prefix_len < 0 or prefix_len + N > 16 maxb:  */
+                                  /* keys past the block table are hidden                   */
 
 /* Human-readable name of a status code (static string). */
 const char *ssd_status_string(ssd_status_t st);
@@ -131,13 +133,20 @@ ssd_status_t ssd_saguaro_sample(const void *draft, ssd_dtype_t dt, int64_t seq_s
  * bonus [B]; accept_prob [B, K] = P(u q' < p) = min(1, p/q') for every j (1
  * when q' = 0 < p, 0 when p = q' = 0 or d_j is invalid), or NULL; resid_mass
  * [B] = total mass of the residual used (1 after full acceptance), or NULL.
+ * near_ties [1] (or NULL): the number of near-ties is ADDED to it (like
+ * status, the caller zeroes it).  A near-tie is a decision that fp32 and
+ * exact arithmetic may take differently, counted so that a caller can report
+ * how many of its outcomes rest on one: an acceptance test actually taken (positions 1..a+1) with |u - p/q'| < 1e-6, or an
+ * inverse-CDF draw whose target u*W lies within 1e-6*W of an edge of the
+ * chosen token's bin (including the draws the kernel resolves by its
+ * rounding fallback).  Greedy (T = 0) decisions are exact and never count.
  */
 ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
                         int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
                         const int32_t *d, const float *u_acc, const float *u_bonus,
                         int32_t *accept_len, int32_t *out_tokens, int32_t *bonus,
-                        float *accept_prob, float *resid_mass, uint32_t *status, void *ws,
-                        size_t ws_bytes, ssd_stream_t s);
+                        float *accept_prob, float *resid_mass, uint32_t *near_ties,
+                        uint32_t *status, void *ws, size_t ws_bytes, ssd_stream_t s);
 
 /*
  * Verification-outcome prediction [A: the draft predicts the bonus token from
@@ -167,8 +176,9 @@ ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture on the device.
- *   - A batch whose scratch (ssd_workspace_size) exceeds the array returns
- *     SSD_ERR_WORKSPACE and launches nothing.
+ *   - Argument errors map exactly as in ssd_verify; a batch whose scratch
+ *     (ssd_workspace_size) exceeds the array then returns SSD_ERR_WORKSPACE
+ *     and launches nothing.
  *   - Every call shares the one array, and it keeps the previous call's
  *     contents (nothing in it needs to start at zero: each call writes every
  *     scratch record before reading it).  Calls whose work overlaps on the GPU
@@ -181,7 +191,8 @@ ssd_status_t ssd_verify_noalloc(const void *target, const void *draft, ssd_dtype
                                 const int32_t *F, float C, float T, const int32_t *d,
                                 const float *u_acc, const float *u_bonus, int32_t *accept_len,
                                 int32_t *out_tokens, int32_t *bonus, float *accept_prob,
-                                float *resid_mass, uint32_t *status, ssd_stream_t s);
+                                float *resid_mass, uint32_t *near_ties, uint32_t *status,
+                                ssd_stream_t s);
 
 /*
  * Speculation-cache lookup keyed by the verification outcome (a, b) [B,
@@ -204,6 +215,7 @@ ssd_status_t ssd_cache_lookup(const int32_t *guess, const int32_t *payload, int 
  * ssd_predict_outcomes -> ssd_cache_lookup on the same arguments; every
  * output pointer except the required d_out, accept_len, out_tokens, bonus may
  * be NULL (guess is needed when slot, next_tokens or hits is given).
+ * near_ties counts as in ssd_verify, plus the K Saguaro draws of d_1..d_K.
  */
 ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
                        int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
@@ -211,8 +223,8 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
                        const int32_t *payload, int32_t *d_out, float *qd_out, int32_t *accept_len,
                        int32_t *out_tokens, int32_t *bonus, float *accept_prob, float *resid_mass,
                        int32_t *guess, float *guess_q, int32_t *slot, int32_t *next_tokens,
-                       uint32_t *hits, uint32_t *status, void *ws, size_t ws_bytes,
-                       ssd_stream_t s);
+                       uint32_t *hits, uint32_t *near_ties, uint32_t *status, void *ws,
+                       size_t ws_bytes, ssd_stream_t s);
 
 /*
  * Timing hook for profiling: while set (both non-NULL cudaEvent_t handles),
@@ -254,7 +266,13 @@ ssd_status_t ssd_set_trace(void *buf, size_t bytes);
  *     lse = natural log-sum-exp of the visible scores (fp32 [B, Nq, Hq], or NULL).
  * Supported: d in {64, 128}, Hq % Hkv == 0, Hq / Hkv <= 16, 1 <= Nq <= N <= 128,
  * prefix_len[b] + N <= 16 * maxb.  parent[m] outside [-1, m-1] ends the path
- * (BAD_TREE); a block id outside [0, num_blocks) hides its keys (BAD_BLOCK).
+ * (BAD_TREE); a block id outside [0, num_blocks) hides its keys (BAD_BLOCK);
+ * prefix_len[b] < 0 or prefix_len[b] + N > 16 * maxb sets BAD_PREFIX and the
+ * keys past the table stay hidden (a negative prefix counts as 0).
+ * Workspace: ssd_attention_workspace_size() bytes (256-byte aligned) let a
+ * long key range be split across CTAs and merged afterwards.  ws may be NULL
+ * or short: the keys are then not split, which gives the same result but can
+ * be many times slower when few query rows meet a long prefix.
  */
 size_t ssd_attention_workspace_size(int B, int Nq, int Hq, int Hkv, int d, int max_prefix);
 ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void *v_cache,

@@ -23,6 +23,7 @@ FLAG_WAIT_TIMEOUT = 4
 FLAG_BAD_OUTCOME = 8
 FLAG_BAD_TREE = 16
 FLAG_BAD_BLOCK = 32
+FLAG_BAD_PREFIX = 64
 
 EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events", "ssd_set_trace",
            "ssd_saguaro_sample",
@@ -82,10 +83,10 @@ def _declare(lib):
                                        _vp, _vp, _sz, _vp]
     lib.ssd_saguaro_sample.restype = _i
     lib.ssd_verify.argtypes = [_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp,
-                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+                               _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.ssd_verify.restype = _i
     lib.ssd_verify_noalloc.argtypes = [_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp,
-                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.ssd_verify_noalloc.restype = _i
     lib.ssd_verify_noalloc_max_bytes.argtypes = []
     lib.ssd_verify_noalloc_max_bytes.restype = _sz
@@ -95,7 +96,7 @@ def _declare(lib):
     lib.ssd_cache_lookup.argtypes = [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.ssd_cache_lookup.restype = _i
     lib.ssd_round.argtypes = ([_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp, _vp]
-                              + [_vp] * 13 + [_vp, _sz, _vp])
+                              + [_vp] * 14 + [_vp, _sz, _vp])
     lib.ssd_round.restype = _i
     lib.ssd_attention_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
     lib.ssd_attention_workspace_size.restype = _sz
@@ -221,7 +222,7 @@ def ssd_saguaro_sample(draft, V, F, C, T, u_draft, d_out, qd_out=None, status=No
 
 
 def ssd_verify(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tokens, bonus,
-               accept_prob=None, resid_mass=None, status=None, ws=None, stream=None):
+               accept_prob=None, resid_mass=None, status=None, ws=None, stream=None, near_ties=None):
     dt, ss, rs = _logit_meta(target)
     if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
         raise ValueError("target and draft logits must share dtype, shape and strides")
@@ -229,12 +230,12 @@ def ssd_verify(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tok
     _check("ssd_verify", load().ssd_verify(
         _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
         _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
-        _ptr(accept_prob), _ptr(resid_mass), _ptr(status), _ptr(ws),
+        _ptr(accept_prob), _ptr(resid_mass), _ptr(near_ties), _ptr(status), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def ssd_verify_noalloc(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tokens, bonus,
-                       accept_prob=None, resid_mass=None, status=None, stream=None):
+                       accept_prob=None, resid_mass=None, status=None, stream=None, near_ties=None):
     """ssd_verify with the library's fixed device scratch instead of a workspace
     (for callers that cannot allocate device memory)."""
     dt, ss, rs = _logit_meta(target)
@@ -244,7 +245,7 @@ def ssd_verify_noalloc(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len,
     _check("ssd_verify_noalloc", load().ssd_verify_noalloc(
         _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
         _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
-        _ptr(accept_prob), _ptr(resid_mass), _ptr(status), _stream(stream)))
+        _ptr(accept_prob), _ptr(resid_mass), _ptr(near_ties), _ptr(status), _stream(stream)))
 
 
 def ssd_verify_noalloc_max_bytes() -> int:
@@ -270,7 +271,7 @@ def ssd_cache_lookup(guess, payload, K, F, accept_len, bonus, slot, next_tokens=
 def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_len, out_tokens,
               bonus, payload=None, qd_out=None, accept_prob=None, resid_mass=None, guess=None,
               guess_q=None, slot=None, next_tokens=None, hits=None, status=None, ws=None,
-              stream=None):
+              stream=None, near_ties=None):
     dt, ss, rs = _logit_meta(target)
     if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
         raise ValueError("target and draft logits must share dtype, shape and strides")
@@ -279,8 +280,8 @@ def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_
         _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
         _ptr(u_draft), _ptr(u_acc), _ptr(u_bonus), _ptr(payload), _ptr(d_out), _ptr(qd_out),
         _ptr(accept_len), _ptr(out_tokens), _ptr(bonus), _ptr(accept_prob), _ptr(resid_mass),
-        _ptr(guess), _ptr(guess_q), _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(status),
-        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(guess), _ptr(guess_q), _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(near_ties),
+        _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def ssd_attention_workspace_size(B, Nq, Hq, Hkv, d, max_prefix) -> int:

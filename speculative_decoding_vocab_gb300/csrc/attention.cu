@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
   const int split = it % a.splits, mg = (it / a.splits) % mgroups, bh = it / (a.splits * mgroups);
   const int b = bh / a.Hkv, hk = bh % a.Hkv;
   const int N = a.N;
-  const int L = max(0, a.prefix_len[b]);
+  const int L_in = a.prefix_len[b];
+  const int L = max(0, L_in);
   const int nkeys = L + N;
   const int ntiles_all = (nkeys + kKeys - 1) / kKeys;
   const int t_begin = split * a.tiles_per_split;
@@ -364,6 +365,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
     }
     fence_mbar_init();
     s_abort = 0;
+    // a prefix the block table cannot hold: the keys past it stay hidden
+    if (has_item && (L_in < 0 || nkeys > a.maxb * kPage)) atomicOr(a.status, kFlagBadPrefix);
   }
   if (pl == 0 && warp == CF::kMmaWarp) {
     tmem_alloc(&tmem_base, PL * CF::kTmemCols);
@@ -855,11 +858,15 @@ AttnPlan plan_attention(int B, int Nq, int Hq, int Hkv, int d, int max_keys) {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
-cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a,
-                             cudaStream_t cs) {
+int attention_smem(const AttnArgs &a) {
   using CF = AttnCfg<D, MT, PL, RA, NPB>;
-  const int smem = CF::kTable + PL * attn_tab_stride(a.tiles_per_split) * 4 + 1024;
-  // dynamic + static shared memory within the per-block opt-in limit
+  return CF::kTable + PL * attn_tab_stride(a.tiles_per_split) * 4 + 1024;
+}
+
+// Whether the configuration's dynamic + static shared memory for this key
+// range fits the per-block opt-in limit.
+template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
+bool attention_fits(const AttnArgs &a) {
   static const int room = [] {
     cudaFuncAttributes fa;
     int dev = 0, optin = 0;
@@ -869,7 +876,15 @@ cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, c
       return 227 * 1024 - 4096;
     return optin - static_cast<int>(fa.sharedSizeBytes);
   }();
-  if (smem > room) return cudaErrorInvalidValue;
+  return attention_smem<D, MT, PL, RA, NPB>(a) <= room;
+}
+
+template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
+cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a,
+                             cudaStream_t cs) {
+  using CF = AttnCfg<D, MT, PL, RA, NPB>;
+  const int smem = attention_smem<D, MT, PL, RA, NPB>(a);
+  if (!attention_fits<D, MT, PL, RA, NPB>(a)) return cudaErrorInvalidValue;
   cudaError_t e =
       cudaFuncSetAttribute(k_branch_attn_tc<D, MT, PL, RA, NPB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -913,9 +928,6 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   const int max_keys = maxb * kPage;
   const AttnPlan p = plan_attention(B, Nq, Hq, Hkv, d, max_keys);
   const size_t need = align256(p.part_o_bytes) + align256(p.part_ml_bytes);
-  if (p.splits > 1 && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))) {
-    // not enough workspace for split partials: run unsplit
-  }
   AttnArgs a;
   memset(&a, 0, sizeof(a));
   a.q = static_cast<const uint16_t *>(q);
@@ -932,6 +944,8 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   a.group = Hq / Hkv;
   a.nrows = p.nrows;
   a.mtiles = p.mtiles;
+  // without room for the split partials the keys are not split (documented at
+  // the declaration: correct, but slower for long prefixes)
   const bool split_ok = p.splits > 1 && ws && ws_bytes >= need && !(reinterpret_cast<uintptr_t>(ws) & 255u);
   a.splits = split_ok ? p.splits : 1;
   a.tiles_per_split = split_ok ? p.tiles_per_split : (max_keys + kKeys - 1) / kKeys;
@@ -947,13 +961,15 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
   a.items = B * Hkv * p.mtiles * a.splits;
   cudaError_t e;
-  if (d == 64) e = launch_attention<64, 1, 2, kRows, 1>(kmap, vmap, a, cs);
-  else {
-    // six stages with 64-row tiles and one P buffer, unless the key range's
-    // block-table slice leaves no room for them (then four)
-    e = cudaErrorInvalidValue;
-    if (p.nrows <= kTrimRows) e = launch_attention<128, 1, 1, kTrimRows, 1>(kmap, vmap, a, cs);
-    if (e == cudaErrorInvalidValue) e = launch_attention<128, 1, 1>(kmap, vmap, a, cs);
+  if (d == 64) {
+    e = launch_attention<64, 1, 2, kRows, 1>(kmap, vmap, a, cs);
+  } else if (p.nrows <= kTrimRows && attention_fits<128, 1, 1, kTrimRows, 1>(a)) {
+    // six stages with 64-row tiles and one P buffer
+    e = launch_attention<128, 1, 1, kTrimRows, 1>(kmap, vmap, a, cs);
+  } else {
+    // more rows, or a key range whose block-table slice leaves no room for
+    // six stages: four
+    e = launch_attention<128, 1, 1>(kmap, vmap, a, cs);
   }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

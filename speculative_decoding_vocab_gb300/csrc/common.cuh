@@ -17,6 +17,7 @@ constexpr uint32_t kFlagWaitTimeout = 4u;
 constexpr uint32_t kFlagBadOutcome = 8u;
 constexpr uint32_t kFlagBadTree = 16u;
 constexpr uint32_t kFlagBadBlock = 32u;
+constexpr uint32_t kFlagBadPrefix = 64u;
 
 // Upper bound on polls of an mbarrier before a wait gives up and reports
 // SSD_FLAG_WAIT_TIMEOUT (each poll may suspend the thread for a short,

@@ -63,6 +63,11 @@ constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
 constexpr int kMaxChunks = 128;  // per row: 4 chunk records per lane in the warp merge
 constexpr int kNone = 0x7fffffff;
+// A draw whose target lies within kNearTie * W of an edge of the chosen
+// element's bin, and an acceptance test with |u - p/q'| < kNearTie, is a
+// near-tie: fp32 and exact arithmetic may decide it differently.  Such
+// events are counted (the optional near_ties output).
+constexpr float kNearTie = 1e-6f;
 
 struct __align__(16) ChunkStat {
   float m;   // chunk maximum
@@ -141,6 +146,7 @@ struct VocabArgs {
   float *guess_q;
   int32_t *slot_out, *next_tokens;
   uint32_t *hits;
+  uint32_t *near_ties;  // optional: near-tie draws and tests, added to
   uint32_t *status;
   unsigned long long *trace;  // optional: 8 words per CTA (see ssd_set_trace)
 };
@@ -241,6 +247,7 @@ struct Smem {
   RowInfo rows[kMaxK + 1];
   uint64_t keyF[kMaxK + 1];
   unsigned long long mk[7];  // trace marks (thread 0)
+  int near;                  // thread 0: the last draw was a near-tie (its target within 1e-6 W of a bin edge)
 };
 
 // What a merge reads of other CTAs' records, staged in shared memory by one
@@ -359,10 +366,12 @@ SSD_DEV float lane_weights(const VocabArgs &a, const char *rowT, const char *row
 // `target` with positive weight; when rounding leaves the target in a lane that
 // has no such element, that lane's last positive element; when no lane holds
 // it, the block's last positive element; -1 for a block without weight.  All
-// 32 lanes call; all return the result.
+// 32 lanes call; all return the result.  *dist (every lane) is the distance
+// of the target from the nearer edge of the chosen element's bin in the
+// block's running weight, 0 for the fallbacks (a near-tie by construction).
 template <class E, bool HT, bool HD, class WF>
 SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, int c, int j, int w, float target,
-                      const WF &wf) {
+                      const WF &wf, float *dist) {
   const int lane = threadIdx.x & 31;
   float x[E::kVec];
   const float p = lane_weights<E, HT, HD>(a, rowT, rowD, c, j, w, wf, x);
@@ -370,19 +379,29 @@ SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, in
   float ex = __shfl_up_sync(0xffffffffu, incl, 1);
   if (lane == 0) ex = 0.f;
   const int i0 = c * a.chunk_elems + (j * kThreads + w * 32 + lane) * E::kVec;
-  float run = 0.f;
+  float run = 0.f, edge = 0.f;
   int hit = -1, lpos = -1;
 #pragma unroll
   for (int e = 0; e < E::kVec; ++e) {
+    const float before = __fadd_rn(ex, run);
     run = __fadd_rn(run, x[e]);
     if (x[e] > 0.f) {
       lpos = i0 + e;
-      if (hit < 0 && __fadd_rn(ex, run) > target) hit = lpos;
+      const float after = __fadd_rn(ex, run);
+      if (hit < 0 && after > target) {
+        hit = lpos;
+        edge = fminf(__fsub_rn(target, before), __fsub_rn(after, target));
+      }
     }
   }
   const bool cross = p > 0.f && __fadd_rn(ex, p) > target;
   const uint32_t mc = __ballot_sync(0xffffffffu, cross);
-  if (mc) return __shfl_sync(0xffffffffu, hit >= 0 ? hit : lpos, __ffs(mc) - 1);
+  if (mc) {
+    const int src = __ffs(mc) - 1;
+    *dist = __shfl_sync(0xffffffffu, hit >= 0 ? fmaxf(edge, 0.f) : 0.f, src);
+    return __shfl_sync(0xffffffffu, hit >= 0 ? hit : lpos, src);
+  }
+  *dist = 0.f;
   int best = lpos;
 #pragma unroll
   for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
@@ -883,10 +902,12 @@ SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, flo
                        const BlockRec *sbr, const uint64_t *Slist, int Fn, float C, float *zdrawn, const char *rowZ,
                        float *zother, Smem &sh) {
   const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) sh.near = 0;
   if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
   __syncthreads();
   const int cs = sh.ival[0];
   const float local = sh.scal[1];
+  const float Wrow = sh.scal[2];  // the row's total weight
   if (cs < 0) return -1;
   // block weights of chunk cs; the elements of S in a block down-weighted in
   // list order
@@ -926,15 +947,17 @@ SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, flo
     if (tid == 0 && sh.ival[0] < 0) {  // no block weight (the masses rounded differently): the last block
       sh.ival[0] = kBlocks - 1;
       sh.scal[1] = local;
+      sh.near = 1;
     }
   }
   __syncthreads();
   const int blk = sh.ival[0];
   const float local2 = sh.scal[1];
   int d = -1;
+  float dist = 0.f;
   if (warp == 0) {
     d = warp_find<E, HT, !HT>(a, HT ? row : nullptr, HT ? nullptr : row, cs, blk / kWarps, blk % kWarps, local2,
-                              wf);
+                              wf, &dist);
   } else if (warp == 1 && zdrawn) {
     const int lane = tid & 31;
     const int e0 = cs * a.chunk_elems;
@@ -953,6 +976,7 @@ SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, flo
   if (tid == 0) {
     sh.ival[4] = d;
     sh.ival[5] = cs * a.chunk_elems + ((blk / kWarps) * kThreads + (blk % kWarps) * 32) * E::kVec;  // zbuf[0]
+    if (!(dist >= __fmul_rn(kNearTie, Wrow))) sh.near = 1;
   }
   __syncthreads();
   return sh.ival[4];
@@ -984,10 +1008,12 @@ SSD_DEV int exact_draw(const VocabArgs &a, const char *rowT, const char *rowD, f
     }
     __syncthreads();
   }
+  if (tid == 0) sh.near = 0;
   if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
   __syncthreads();
   const int cs = sh.ival[0];
   const float local = sh.scal[1];
+  const float Wrow = sh.scal[2];  // the row's total weight
   if (cs < 0) return -1;
   __syncthreads();
   block_sums(cs);
@@ -996,9 +1022,14 @@ SSD_DEV int exact_draw(const VocabArgs &a, const char *rowT, const char *rowD, f
   const int blk = sh.ival[0];
   const float local2 = sh.scal[1];
   int d = -1;
-  if (warp == 0 && blk >= 0) d = warp_find<E, HT, HD>(a, rowT, rowD, cs, blk / kWarps, blk % kWarps, local2, wf);
+  float dist = 0.f;
+  if (warp == 0 && blk >= 0)
+    d = warp_find<E, HT, HD>(a, rowT, rowD, cs, blk / kWarps, blk % kWarps, local2, wf, &dist);
   __syncthreads();
-  if (tid == 0) sh.ival[4] = d;
+  if (tid == 0) {
+    sh.ival[4] = d;
+    if (!(dist >= __fmul_rn(kNearTie, Wrow))) sh.near = 1;
+  }
   __syncthreads();
   return sh.ival[4];
 }
@@ -1298,6 +1329,7 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
             }
           }
         }
+        if (tid == 0 && sh.near && a.near_ties) atomicAdd(a.near_ties, 1u);
         if (d < 0) d = ri.ad;
         if (!zknown) {
           zd = E::ld(rowD, d);
@@ -1483,10 +1515,23 @@ SSD_DEV int stage_complete(const VocabArgs &a, Smem &sh) {
 // Outputs of sequence b once its bonus token bt is known (sh.cd: draft tokens;
 // the lookup's lists and payload as stage_chain staged them, `pay` its
 // payload stage).
-SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, const int32_t *pay, Smem &sh) {
+SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, bool near_bonus, const int32_t *pay,
+                  Smem &sh) {
   const int tid = threadIdx.x;
   const int Fa = a.F[acc];
-  if (tid == 0) sh.ival[3] = kNone;
+  if (tid == 0) {
+    sh.ival[3] = kNone;
+    if (a.near_ties && !a.greedy) {
+      // the acceptance tests actually taken (positions 1..acc+1) whose u lies
+      // within kNearTie of p/q', and the bonus draw
+      uint32_t n = near_bonus ? 1u : 0u;
+      for (int t = 0; t <= acc && t < a.K; ++t) {
+        const PosInfo pi = sh.pos[t];
+        if (pi.p >= 0.f && pi.q > 0.f && fabsf(__fsub_rn(sh.cu[t], __fdiv_rn(pi.p, pi.q))) < kNearTie) ++n;
+      }
+      if (n) atomicAdd(a.near_ties, n);
+    }
+  }
   __syncthreads();
   if (a.do_lookup) {
     if (lists_staged(a)) {
@@ -1549,7 +1594,7 @@ __device__ __forceinline__ void seq_finish(const VocabArgs &a, int b, Stage &st,
   const RowInfo row = sh.rows[acc];
   int bt = row.at;
   float W = 1.f;
-  bool zero = false;
+  bool zero = false, near = false;
   if (a.greedy) {
     if (acc < a.K) {
       W = (row.at != row.ad) ? 1.f : 0.f;
@@ -1557,8 +1602,9 @@ __device__ __forceinline__ void seq_finish(const VocabArgs &a, int b, Stage &st,
     }
   } else {
     bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], acc == a.K ? &st : nullptr, sh);
+    near = threadIdx.x == 0 && sh.near;
   }
-  emit(a, b, acc, bt, W, zero, st.pay, sh);
+  emit(a, b, acc, bt, W, zero, near, st.pay, sh);
 }
 
 // The CTA's trace entry: (SM << 48 | kind << 40 | sequence << 20 | index),
@@ -1761,6 +1807,7 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
     const RowInfo ra = sh.rows[acc2];
     const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
     const float ub = a.u_bonus[b];
+    if (tid == 0) sh.near = 0;
     if (warp == 0) {
       locate(umass, nu, ub, false, sh);
       __syncwarp();
@@ -1782,6 +1829,7 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
         if (lane == 0 && sh.ival[0] < 0) {  // a unit of positive mass has a positive block; kept for safety
           sh.ival[0] = 2 * kWarps - 1;
           sh.scal[1] = local;
+          sh.near = 1;
         }
       }
     }
@@ -1790,20 +1838,28 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
     const int uq = sh.ival[6];
     const float W = sh.scal[6];
     int bt = -1;
+    bool near = false;  // thread 0
     if (uq >= 0) {
       const int k = sh.ival[0];
       const float local2 = sh.scal[1];
       int d = -1;
+      float dist = 0.f;
       if (warp == 0)
         d = warp_find<E, true, true>(a, rowT, rowD, uq / kQuarters, 2 * (uq % kQuarters) + k / kWarps, k % kWarps,
-                                     local2, wa);
+                                     local2, wa, &dist);
       __syncthreads();
-      if (tid == 0) sh.ival[4] = d;
+      if (tid == 0) {
+        sh.ival[4] = d;
+        near = sh.near || !(dist >= __fmul_rn(kNearTie, W));
+      }
       __syncthreads();
       bt = sh.ival[4];
     }
     const bool zero = uq < 0;  // no residual mass: p_{a+1} instead
-    if (bt < 0) bt = draw_target<E>(a, b, acc2, ra, ub, nullptr, sh);
+    if (bt < 0) {
+      bt = draw_target<E>(a, b, acc2, ra, ub, nullptr, sh);
+      near = tid == 0 && sh.near;
+    }
     if (a.do_lookup) {
       // the lookup lists, once the pair merge of position acc has written its list
       if (tid == 0 && !wait_count(pos_verdict(a, b, acc), 3u)) atomicOr(a.status, kFlagWaitTimeout);
@@ -1813,7 +1869,7 @@ SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *
       __syncthreads();
     }
     mark(a, sh.mk, 5);
-    emit(a, b, acc2, bt, W, zero, pay, sh);
+    emit(a, b, acc2, bt, W, zero, near, pay, sh);
   }
   mark(a, sh.mk, 6);
   if (a.trace && tid == 0) {
@@ -2231,7 +2287,7 @@ ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, i
                         int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
                         const int32_t *d, const float *u_acc, const float *u_bonus, int32_t *accept_len,
                         int32_t *out_tokens, int32_t *bonus, float *accept_prob, float *resid_mass,
-                        uint32_t *status, void *ws, size_t ws_bytes, ssd_stream_t s) {
+                        uint32_t *near_ties, uint32_t *status, void *ws, size_t ws_bytes, ssd_stream_t s) {
   Layout L;
   ssd_status_t st = layout_or_error(B, K, V, dt, F, &L);
   if (st != SSD_OK) return st;
@@ -2254,6 +2310,7 @@ ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, i
   a.bonus = bonus;
   a.accept_prob = accept_prob;
   a.resid_mass = resid_mass;
+  a.near_ties = near_ties;
   return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
 }
 
@@ -2316,8 +2373,8 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
                        const float *u_draft, const float *u_acc, const float *u_bonus, const int32_t *payload,
                        int32_t *d_out, float *qd_out, int32_t *accept_len, int32_t *out_tokens, int32_t *bonus,
                        float *accept_prob, float *resid_mass, int32_t *guess, float *guess_q, int32_t *slot,
-                       int32_t *next_tokens, uint32_t *hits, uint32_t *status, void *ws, size_t ws_bytes,
-                       ssd_stream_t s) {
+                       int32_t *next_tokens, uint32_t *hits, uint32_t *near_ties, uint32_t *status, void *ws,
+                       size_t ws_bytes, ssd_stream_t s) {
   Layout L;
   ssd_status_t st = layout_or_error(B, K, V, dt, F, &L);
   if (st != SSD_OK) return st;
@@ -2357,6 +2414,7 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
   a.slot_out = slot;
   a.next_tokens = next_tokens;
   a.hits = hits;
+  a.near_ties = near_ties;
   return cuda_status(launch_any(dt, a, cs));
 }
 
@@ -2366,17 +2424,23 @@ ssd_status_t ssd_verify_noalloc(const void *target, const void *draft, ssd_dtype
                                 int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
                                 const int32_t *d, const float *u_acc, const float *u_bonus,
                                 int32_t *accept_len, int32_t *out_tokens, int32_t *bonus, float *accept_prob,
-                                float *resid_mass, uint32_t *status, ssd_stream_t s) {
+                                float *resid_mass, uint32_t *near_ties, uint32_t *status, ssd_stream_t s) {
+  // every argument error maps as in ssd_verify; only then the scratch size
   Layout L;
-  if (!F || !make_layout(B, K, V, dt, F, &L))
-    return (F && B >= 0 && K >= 0 && V >= 1) ? SSD_ERR_UNSUPPORTED : SSD_ERR_INVALID_ARG;
+  ssd_status_t st = layout_or_error(B, K, V, dt, F, &L);
+  if (st != SSD_OK) return st;
+  st = check_logits(target, dt, seq_stride, row_stride, B, K, V);
+  if (st == SSD_OK) st = check_logits(draft, dt, seq_stride, row_stride, B, K, V);
+  if (st != SSD_OK) return st;
+  if (!(T >= 0.f) || !isfinite(T) || !(C > 0.f && C <= 1.f)) return SSD_ERR_INVALID_ARG;
+  if (B == 0) return SSD_OK;
+  if ((K > 0 && (!d || !u_acc)) || !u_bonus || !accept_len || !out_tokens || !bonus || !status)
+    return SSD_ERR_INVALID_ARG;
   if (L.total > kStaticScratchBytes) return SSD_ERR_WORKSPACE;  // the batch needs more scratch than the array holds
-  if (B == 0) return ssd_verify(target, draft, dt, seq_stride, row_stride, B, K, V, F, C, T, d, u_acc, u_bonus,
-                                accept_len, out_tokens, bonus, accept_prob, resid_mass, status, nullptr, 0, s);
   void *ws = nullptr;
   if (static_scratch(&ws) != cudaSuccess) return SSD_ERR_CUDA;
   return ssd_verify(target, draft, dt, seq_stride, row_stride, B, K, V, F, C, T, d, u_acc, u_bonus, accept_len,
-                    out_tokens, bonus, accept_prob, resid_mass, status, ws, kStaticScratchBytes, s);
+                    out_tokens, bonus, accept_prob, resid_mass, near_ties, status, ws, kStaticScratchBytes, s);
 }
 
 }  // extern "C"

@@ -10,10 +10,21 @@ Comparison rules (the tolerances a fp32 kernel can be held to against fp64):
 * each stage is checked on the inputs the GPU actually produced upstream (the
   oracle verifies the GPU's draft tokens, looks up the GPU's outcomes), so one
   near-tie does not cascade;
-* probabilities agree within 1e-5 relative error (residual masses, which are
-  differences of probabilities, within 1e-5 absolute).
+* probabilities (q'(d), accept_prob, guess_q and the residual masses) agree
+  within 1e-5 relative error;
+* near-ties are rare by construction (a uniform lands in a 2e-6 window with
+  probability 2e-6 per draw; about 0.02 near-ties are expected over the 10^4
+  draws of the largest comparison here), so each comparison allows at most
+  NEAR_TIE_BOUND of them, both those the oracle's margins excuse and those the
+  GPU counts in its own near_ties output.
+
+The oracle runs on every host core: its C functions release the GIL, so a
+thread pool over slices of the batch runs them in parallel.
 """
 from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -24,6 +35,38 @@ from speculative_decoding_vocab_gb300 import workloads as w
 
 NEAR_TIE = 1e-6
 PROB_RTOL = 1e-5
+NEAR_TIE_BOUND = 2
+
+_pool = None
+
+
+def oracle_pool() -> ThreadPoolExecutor:
+    global _pool
+    if _pool is None:
+        _pool = ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1))
+    return _pool
+
+
+def _cat(parts):
+    if isinstance(parts[0], dict):
+        return {k: _cat([p[k] for p in parts]) for k in parts[0]}
+    if isinstance(parts[0], tuple):
+        return tuple(_cat([p[i] for p in parts]) for i in range(len(parts[0])))
+    if isinstance(parts[0], np.ndarray):
+        return np.concatenate(parts)
+    return sum(parts)
+
+
+def batched(fn, n, batch_args, *rest, **kw):
+    """fn(*[a[lo:hi] for a in batch_args], *rest, **kw) over slices of the
+    batch of n sequences, on every host core; results concatenated."""
+    workers = oracle_pool()._max_workers
+    step = max(1, -(-n // (2 * workers)))
+    spans = [(lo, min(n, lo + step)) for lo in range(0, n, step)]
+    if len(spans) <= 1:
+        return fn(*batch_args, *rest, **kw)
+    futs = [oracle_pool().submit(fn, *[a[lo:hi] for a in batch_args], *rest, **kw) for lo, hi in spans]
+    return _cat([f.result() for f in futs])
 
 
 def to_dev(arr, dev="cuda"):
@@ -46,7 +89,7 @@ def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True):
              resid_mass=torch.zeros(B, **f32), guess=torch.full((B, sumF), -7, **i32),
              guess_q=torch.zeros(B, sumF, **f32), slot=torch.full((B,), -7, **i32),
              next_tokens=torch.full((B, K), -7, **i32), hits=torch.full((1,), 12345, **i32),
-             status=torch.zeros(1, **i32))
+             near_ties=torch.zeros(1, **i32), status=torch.zeros(1, **i32))
     ws = ssd.workspace(B, K, V, spec.dtype, spec.F, dev)
     ud, ua, ub = to_dev(inp.u_draft, dev), to_dev(inp.u_acc, dev), to_dev(inp.u_bonus, dev)
     pl = to_dev(inp.payload, dev) if inp.payload is not None else None
@@ -55,12 +98,12 @@ def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True):
                       o["out_tokens"], o["bonus"], payload=pl, qd_out=o["qd"],
                       accept_prob=o["accept_prob"], resid_mass=o["resid_mass"], guess=o["guess"],
                       guess_q=o["guess_q"], slot=o["slot"], next_tokens=o["next_tokens"],
-                      hits=o["hits"], status=o["status"], ws=ws)
+                      hits=o["hits"], status=o["status"], ws=ws, near_ties=o["near_ties"])
     else:
         ssd.ssd_saguaro_sample(dft, V, spec.F, C, T, ud, o["d"], o["qd"], status=o["status"], ws=ws)
         ssd.ssd_verify(tgt, dft, V, spec.F, C, T, o["d"], ua, ub, o["accept_len"], o["out_tokens"],
                        o["bonus"], accept_prob=o["accept_prob"], resid_mass=o["resid_mass"],
-                       status=o["status"], ws=ws)
+                       status=o["status"], ws=ws, near_ties=o["near_ties"])
         ssd.ssd_predict_outcomes(dft, V, spec.F, T, o["guess"], o["guess_q"], status=o["status"],
                                  ws=ws)
         ssd.ssd_cache_lookup(o["guess"], pl, K, spec.F, o["accept_len"], o["bonus"], o["slot"],
@@ -76,12 +119,17 @@ def _rel_ok(a, b, rtol=PROB_RTOL, floor=1e-30):
 
 
 class Report:
+    """near_ties: GPU / oracle differences the oracle's margins excused;
+    gpu_near_ties: the near-ties the GPU itself counted (near_ties output)."""
+
     def __init__(self):
         self.near_ties = 0
+        self.gpu_near_ties = 0
         self.compared = 0
 
     def __repr__(self):
-        return f"Report(compared={self.compared}, near_ties={self.near_ties})"
+        return (f"Report(compared={self.compared}, near_ties={self.near_ties}, "
+                f"gpu_near_ties={self.gpu_near_ties})")
 
 
 def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report=None,
@@ -92,11 +140,17 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
     C = spec.C if C is None else C
     K, V, F = spec.K, spec.V, spec.F
     rep = report or Report()
+    excused0 = rep.near_ties
     idx = np.arange(spec.B) if seqs is None else np.asarray(seqs)
-    tgt, dft = inp.target[idx], inp.draft[idx]
-    ud, ua, ub = inp.u_draft[idx], inp.u_acc[idx], inp.u_bonus[idx]
+    if seqs is None:
+        tgt, dft = inp.target, inp.draft
+        ud, ua, ub = inp.u_draft, inp.u_acc, inp.u_bonus
+    else:
+        tgt, dft = inp.target[idx], inp.draft[idx]
+        ud, ua, ub = inp.u_draft[idx], inp.u_acc[idx], inp.u_bonus[idx]
+    n = len(idx)
     # --- Saguaro sampling
-    od, oqd, dmar = oracle.saguaro_sample(dft, V, F, C, T, ud)
+    od, oqd, dmar = batched(lambda d_, u_: oracle.saguaro_sample(d_, V, F, C, T, u_), n, (dft, ud))
     gd = g["d"][idx]
     skip = np.zeros(len(idx), bool)
     for i in range(len(idx)):
@@ -111,7 +165,8 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
     ok = ~skip
     assert np.all(_rel_ok(g["qd"][idx][ok], oqd[ok])), "q'(d) differs beyond 1e-5 relative"
     # --- verification, on the GPU's draft tokens
-    ov = oracle.verify(tgt, dft, V, F, C, T, gd, ua, ub)
+    ov = batched(lambda t_, d_, g_, a_, b_: oracle.verify(t_, d_, V, F, C, T, g_, a_, b_), n,
+                 (tgt, dft, gd, ua, ub))
     ga, gb = g["accept_len"][idx], g["bonus"][idx]
     for i in range(len(idx)):
         if ga[i] != ov["accept_len"][i]:
@@ -131,9 +186,9 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
             continue
         assert np.array_equal(g["out_tokens"][idx][i], ov["out_tokens"][i]), f"seq {idx[i]} tokens"
     assert np.all(_rel_ok(g["accept_prob"][idx], ov["accept_prob"])), "accept_prob differs"
-    assert np.all(np.abs(g["resid_mass"][idx] - ov["resid_mass"]) <= PROB_RTOL), "resid_mass"
+    assert np.all(_rel_ok(g["resid_mass"][idx][~skip], ov["resid_mass"][~skip])), "resid_mass"
     # --- prediction (exact on raw logits)
-    og, ogq = oracle.predict(dft, V, F, T)
+    og, ogq = batched(oracle.predict, n, (dft,), V, F, T)
     assert np.array_equal(g["guess"][idx], og), "guesses differ"
     assert np.all(_rel_ok(g["guess_q"][idx], ogq)), "guess_q differs"
     # --- lookup, on the GPU's outcomes
@@ -145,6 +200,10 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
         if seqs is None:
             assert int(g["hits"][0]) == ol["hits"], "hit count differs"
     rep.compared += len(idx)
+    gpu_nt = int(g["near_ties"][0]) if "near_ties" in g else 0
+    rep.gpu_near_ties += gpu_nt
+    assert rep.near_ties - excused0 <= NEAR_TIE_BOUND, f"{rep.near_ties - excused0} excused near-ties"
+    assert gpu_nt <= NEAR_TIE_BOUND, f"the GPU counted {gpu_nt} near-ties"
     return rep
 
 

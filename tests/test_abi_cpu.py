@@ -108,11 +108,25 @@ def test_validation_returns_before_any_launch(lib):
                                   good, None, good, good, ws_n, None) == ssd.SSD_ERR_INVALID_ARG
     # workspace too small or missing
     assert lib.ssd_verify(good, good, ssd.SSD_F32, 3000, 1000, 2, 2, 1000, F, 0.5, 1.0, good, good,
-                          good, good, good, good, None, None, good, good, ws_n - 256,
+                          good, good, good, good, None, None, None, good, good, ws_n - 256,
                           None) == ssd.SSD_ERR_WORKSPACE
     assert lib.ssd_round(good, good, ssd.SSD_F32, 3000, 1000, 2, 2, 1000, F, 0.5, 1.0, good, good,
                          good, None, good, None, good, good, good, None, None, None, None, None,
-                         None, None, good, None, 0, None) == ssd.SSD_ERR_WORKSPACE
+                         None, None, None, good, None, 0, None) == ssd.SSD_ERR_WORKSPACE
+    # the no-allocation entry point maps argument errors as ssd_verify does,
+    # before its scratch-size check
+    assert lib.ssd_verify_noalloc(good, good, ssd.SSD_F32, 3000, 1000, 2, 2, 1000, _F((-1, 1, 1)),
+                                  0.5, 1.0, good, good, good, good, good, good, None, None, None,
+                                  good, None) == ssd.SSD_ERR_INVALID_ARG
+    assert lib.ssd_verify_noalloc(good, good, 7, 3000, 1000, 2, 2, 1000, F, 0.5, 1.0, good, good,
+                                  good, good, good, good, None, None, None, good,
+                                  None) == ssd.SSD_ERR_INVALID_ARG
+    assert lib.ssd_verify_noalloc(good, good, ssd.SSD_F32, 3000, 1000, 2, 2, 1000, F, 1.5, 1.0, good,
+                                  good, good, good, good, good, None, None, None, good,
+                                  None) == ssd.SSD_ERR_INVALID_ARG
+    assert lib.ssd_verify_noalloc(odd, good, ssd.SSD_F32, 3000, 1000, 2, 2, 1000, F, 0.5, 1.0, good,
+                                  good, good, good, good, good, None, None, None, good,
+                                  None) == ssd.SSD_ERR_UNSUPPORTED
     # F_k > V
     assert lib.ssd_predict_outcomes(good, ssd.SSD_BF16, 3008, 1008, 2, 2, 4, _F((8, 1, 1)), 1.0,
                                     good, None, good, good, 1 << 20, None) == ssd.SSD_ERR_UNSUPPORTED

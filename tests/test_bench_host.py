@@ -62,7 +62,7 @@ def test_reference_arm_prints_json_line():
     assert line["impl"] == "reference"
     assert line["unit"] == "seq-rounds/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
-    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
 
 
 def test_reference_arm_rank_nonzero_is_silent():

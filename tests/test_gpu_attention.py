@@ -8,7 +8,7 @@ import oracle
 from speculative_decoding_vocab_gb300 import binding as ssd
 from speculative_decoding_vocab_gb300 import workloads as w
 
-from parity import gpu_attention, to_dev
+from parity import batched, gpu_attention, to_dev
 
 pytestmark = pytest.mark.gpu
 ATOL = 2e-2
@@ -26,8 +26,10 @@ def _lib():
 def _check(ai, seqs=None, use_ws=True):
     out, lse, st = gpu_attention(ai, use_ws=use_ws)
     idx = np.arange(ai.spec.B) if seqs is None else np.asarray(seqs)
-    ref, rlse, fl = oracle.branch_attention(ai.q[idx], ai.k_cache, ai.v_cache, ai.block_table[idx],
-                                            ai.prefix_len[idx], ai.parent[idx], ai.spec.Hkv)
+    ref, rlse, fl = batched(
+        lambda q_, bt_, pl_, pa_: oracle.branch_attention(q_, ai.k_cache, ai.v_cache, bt_, pl_, pa_,
+                                                          ai.spec.Hkv),
+        len(idx), (ai.q[idx], ai.block_table[idx], ai.prefix_len[idx], ai.parent[idx]))
     err = np.abs(out[idx] - ref).max()
     lerr = np.abs(lse[idx] - rlse).max()
     assert err <= ATOL, f"max abs error {err}"
@@ -61,16 +63,16 @@ def test_long_unsplit_keys_d128():
 
 
 def test_draft_branch_attention_full():
+    """The draft-shaped workload at full size: all 16 sequences."""
     ai = w.make_attention(w.draft_branch_attention(), seed=0)
-    _check(ai, seqs=[0, 5, 15])
+    _check(ai)
 
 
-def test_verify_attention_at_scale_sampled():
-    """Full-size verify-shaped attention (B=64, L=8192, d=128); the oracle checks
-    a sample of sequences."""
+def test_verify_attention_at_scale_full():
+    """Full-size verify-shaped attention (B=64, L=8192, d=128): all 64 sequences."""
     spec = w.verify_attention_at_scale()
     ai = w.make_attention(spec, seed=0)
-    _check(ai, seqs=[0, 63])
+    _check(ai)
 
 
 def test_flags_bad_tree_and_block():
@@ -86,6 +88,23 @@ def test_flags_bad_tree_and_block():
     ref, _, _ = oracle.branch_attention(ai.q, ai.k_cache, ai.v_cache, ai.block_table, ai.prefix_len,
                                         ai.parent, spec.Hkv)
     assert np.abs(out - ref).max() <= ATOL
+
+
+def test_flag_bad_prefix():
+    """A prefix the block table cannot hold: the keys past it stay hidden (as in
+    the oracle) and BAD_PREFIX is set; a negative prefix counts as 0."""
+    spec = w.AttnSpec(B=2, Hq=8, Hkv=2, d=64, L=40, tree="chain", n_chain=4)
+    ai = w.make_attention(spec, seed=4)
+    maxb = ai.block_table.shape[1]
+    ai.prefix_len[0] = 16 * maxb - 2
+    ai.prefix_len[1] = -5
+    out, lse, st = gpu_attention(ai)
+    assert st & ssd.FLAG_BAD_PREFIX
+    ref, rlse, fl = oracle.branch_attention(ai.q, ai.k_cache, ai.v_cache, ai.block_table,
+                                            ai.prefix_len, ai.parent, spec.Hkv)
+    assert np.all(fl & oracle.FLAG_BAD_PREFIX)
+    assert np.abs(out - ref).max() <= ATOL
+    assert np.abs(lse - rlse).max() <= LSE_ATOL
 
 
 def test_attention_argument_errors():

@@ -67,23 +67,23 @@ def test_llama3_round_full(T):
 
 
 @pytest.mark.parametrize("C", [1.0, 0.5, 0.25])
-def test_qwen3_round_full_sampled(C):
+def test_qwen3_round_full(C):
+    """All 256 sequences of the Qwen-3 round against the oracle, per C."""
     spec = w.qwen3_round(C=C)
     inp = w.make_round(spec, seed=0)
     g = gpu_round(inp)
-    seqs = np.random.default_rng(int(C * 100)).choice(spec.B, size=10, replace=False)
-    rep = compare_round(inp, g, seqs=seqs)
-    # the whole batch: cache hits equal a brute-force lookup of the GPU's own outcomes
-    ol = oracle.lookup(g["guess"], inp.payload, spec.K, spec.F, g["accept_len"], g["bonus"])
-    assert int(g["hits"][0]) == ol["hits"]
-    print(rep, f"C={C} hit rate {ol['hits'] / spec.B:.3f}")
+    rep = compare_round(inp, g)
+    assert rep.compared == spec.B and g["status"][0] == 0
+    print(rep, f"C={C} hit rate {int(g['hits'][0]) / spec.B:.4f}")
 
 
-def test_llama3_round_at_scale_sampled():
+def test_llama3_round_at_scale_full():
+    """All 64 sequences of the round that accompanies verify-shaped attention."""
     spec = w.llama3_round_at_scale()
     inp = w.make_round(spec, seed=0)
     g = gpu_round(inp)
-    compare_round(inp, g, seqs=[0, 17, 40, 63])
+    rep = compare_round(inp, g)
+    assert rep.compared == spec.B and g["status"][0] == 0
 
 
 def test_separate_calls_equal_fused_call():
