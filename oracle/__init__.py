@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
 bench's CPU-baseline / reference leg may import this package.  The product
 path (the CUDA library and its Python binding) never imports it.
 
-The arithmetic lives in ``ssd_oracle.c`` (plain C99, double precision, no
+The arithmetic lives in ``ssd_oracle.c`` (plain C11, double precision, no
 fast-math); this module compiles it with gcc and marshals numpy arrays through
 ctypes.  See the C file's header for the definitions it follows.
 """
@@ -36,7 +36,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/libssd_oracle.so`` (gcc -O2, no fast-math)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

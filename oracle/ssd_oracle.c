@@ -145,7 +145,9 @@ void oracle_softmax(const double *z, int V, double T, double *p) {
   for (int i = 0; i < V; i++) p[i] /= s;
 }
 
-static const double *g_sort_keys;
+/* the keys of the sort in progress, one per thread (callers may run the
+ * oracle on several threads at once) */
+static _Thread_local const double *g_sort_keys;
 static int cmp_desc_then_index(const void *a, const void *b) {
   int ia = *(const int32_t *)a, ib = *(const int32_t *)b;
   double va = g_sort_keys[ia], vb = g_sort_keys[ib];

@@ -12,11 +12,14 @@ Comparison rules (the tolerances a fp32 kernel can be held to against fp64):
   near-tie does not cascade;
 * probabilities (q'(d), accept_prob, guess_q and the residual masses) agree
   within 1e-5 relative error;
-* near-ties are rare by construction (a uniform lands in a 2e-6 window with
-  probability 2e-6 per draw; about 0.02 near-ties are expected over the 10^4
-  draws of the largest comparison here), so each comparison allows at most
-  NEAR_TIE_BOUND of them, both those the oracle's margins excuse and those the
-  GPU counts in its own near_ties output.
+* near-ties are counted on both sides and the counts must agree: the oracle's
+  (decisions whose exact margin is below 1e-6) and the GPU's own near_ties
+  output (its fp32 view of the same decisions) may differ only by decisions
+  whose margin sits within rounding of the 1e-6 line: at most
+  NEAR_TIE_SLACK + 5%.  Note that an inverse-CDF draw is a near-tie whenever
+  its token's own probability is below 2e-6 (the window covers the whole bin),
+  so on 128K-token Zipf rows several percent of the draws are near-ties; the
+  differences the margins excuse are a subset of them.
 
 The oracle runs on every host core: its C functions release the GIL, so a
 thread pool over slices of the batch runs them in parallel.
@@ -35,7 +38,7 @@ from speculative_decoding_vocab_gb300 import workloads as w
 
 NEAR_TIE = 1e-6
 PROB_RTOL = 1e-5
-NEAR_TIE_BOUND = 2
+NEAR_TIE_SLACK = 2
 
 _pool = None
 
@@ -109,7 +112,9 @@ def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True):
         ssd.ssd_cache_lookup(o["guess"], pl, K, spec.F, o["accept_len"], o["bonus"], o["slot"],
                              o["next_tokens"], o["hits"], status=o["status"])
     torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in o.items()}
+    res = {k: v.cpu().numpy() for k, v in o.items()}
+    res["near_tie_scope"] = "round" if fused else "verify"  # which decisions near_ties counts
+    return res
 
 
 def _rel_ok(a, b, rtol=PROB_RTOL, floor=1e-30):
@@ -120,15 +125,19 @@ def _rel_ok(a, b, rtol=PROB_RTOL, floor=1e-30):
 
 class Report:
     """near_ties: GPU / oracle differences the oracle's margins excused;
-    gpu_near_ties: the near-ties the GPU itself counted (near_ties output)."""
+    oracle_near_ties / gpu_near_ties: the decisions each side counts as
+    near-ties; decisions: the draws and acceptance tests compared."""
 
     def __init__(self):
         self.near_ties = 0
+        self.oracle_near_ties = 0
         self.gpu_near_ties = 0
+        self.decisions = 0
         self.compared = 0
 
     def __repr__(self):
-        return (f"Report(compared={self.compared}, near_ties={self.near_ties}, "
+        return (f"Report(compared={self.compared}, decisions={self.decisions}, "
+                f"excused={self.near_ties}, oracle_near_ties={self.oracle_near_ties}, "
                 f"gpu_near_ties={self.gpu_near_ties})")
 
 
@@ -200,10 +209,21 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
         if seqs is None:
             assert int(g["hits"][0]) == ol["hits"], "hit count differs"
     rep.compared += len(idx)
-    gpu_nt = int(g["near_ties"][0]) if "near_ties" in g else 0
-    rep.gpu_near_ties += gpu_nt
-    assert rep.near_ties - excused0 <= NEAR_TIE_BOUND, f"{rep.near_ties - excused0} excused near-ties"
-    assert gpu_nt <= NEAR_TIE_BOUND, f"the GPU counted {gpu_nt} near-ties"
+    # near-ties: the decisions actually taken whose exact margin is below 1e-6
+    draws = g.get("near_tie_scope", "round") == "round"
+    tests_taken = int(sum(min(int(a) + 1, K) for a in ga)) if T > 0 else 0
+    o_nt = int((ov["acc_margin"] < NEAR_TIE).sum() + (ov["bonus_margin"] < NEAR_TIE).sum())
+    if draws:
+        o_nt += int((dmar < NEAR_TIE).sum())
+    rep.decisions += (n * K if draws else 0) + tests_taken + n
+    rep.oracle_near_ties += o_nt
+    excused = rep.near_ties - excused0
+    assert excused <= o_nt, f"{excused} differences excused but only {o_nt} near-ties"
+    if "near_ties" in g and seqs is None:
+        gpu_nt = int(g["near_ties"][0])
+        rep.gpu_near_ties += gpu_nt
+        assert abs(gpu_nt - o_nt) <= NEAR_TIE_SLACK + 0.05 * o_nt, (
+            f"the GPU counted {gpu_nt} near-ties, the oracle {o_nt}")
     return rep
 
 

@@ -84,6 +84,7 @@ def test_llama3_round_at_scale_full():
     g = gpu_round(inp)
     rep = compare_round(inp, g)
     assert rep.compared == spec.B and g["status"][0] == 0
+    print(rep, "hits", int(g["hits"][0]))
 
 
 def test_separate_calls_equal_fused_call():

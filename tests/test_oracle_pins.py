@@ -253,7 +253,7 @@ def _mutant_oracle(old: str, new: str):
         so_path = os.path.join(tmp, "libmutant.so")
         with open(c_path, "w") as f:
             f.write(src.replace(old, new))
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", so_path, c_path,
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", so_path, c_path,
                                "-lm"])
         lib = ctypes.CDLL(so_path)
         oracle._declare(lib)
@@ -711,3 +711,19 @@ def test_attention_prefix_past_the_table_is_hidden():
 
     ref, rlse = _dense_reference(padded, visible)
     assert np.allclose(out, ref, atol=1e-12) and np.allclose(lse, rlse, atol=1e-12)
+
+
+def test_oracle_is_thread_safe():
+    """The parity tests run the oracle on every host core at once: threaded
+    calls over slices of a batch equal one call over the whole batch."""
+    from concurrent.futures import ThreadPoolExecutor
+    spec = w.RoundSpec(B=48, K=3, V=3000, dtype="f32", recipe="gauss", T=1.0, C=0.5,
+                       F=(40, 9, 3, 1), target_sigma=2.0, draft_noise=0.5)
+    inp = w.make_round(spec, seed=12)
+    whole = oracle.saguaro_sample(inp.draft, spec.V, spec.F, spec.C, spec.T, inp.u_draft)
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        parts = list(ex.map(lambda lo: oracle.saguaro_sample(inp.draft[lo:lo + 6], spec.V, spec.F,
+                                                             spec.C, spec.T, inp.u_draft[lo:lo + 6]),
+                            range(0, spec.B, 6)))
+    for k in range(3):
+        assert np.array_equal(np.concatenate([p[k] for p in parts]), whole[k])

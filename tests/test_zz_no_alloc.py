@@ -76,14 +76,16 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
             assert np.array_equal(got[k], ref[k]), (call, k)
         assert _rel_ok(got["accept_prob"], ref["accept_prob"]), call
         assert _rel_ok(got["resid_mass"], ref["resid_mass"]), call
-        # and against the oracle (no near-tie at these sizes and seeds)
+        # and against the oracle (no decision of these seeds differs within a near-tie)
         ov = oracle.verify(inp.target, inp.draft, spec.V, spec.F, spec.C, spec.T, d, inp.u_acc,
                            inp.u_bonus)
         assert np.array_equal(got["accept_len"], ov["accept_len"]), call
         assert np.array_equal(got["out_tokens"], ov["out_tokens"]), call
         assert _rel_ok(got["accept_prob"], ov["accept_prob"]), call
         assert _rel_ok(got["resid_mass"], ov["resid_mass"]), call
-        assert got["near_ties"][0] == 0, call
+        # the near-ties counted: those of the oracle's exact margins
+        o_nt = int((ov["acc_margin"] < 1e-6).sum() + (ov["bonus_margin"] < 1e-6).sum())
+        assert abs(int(got["near_ties"][0]) - o_nt) <= 2, (call, got["near_ties"][0], o_nt)
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
