@@ -78,6 +78,8 @@ def _declare(lib):
     lib.oracle_predict.restype = _i
     lib.oracle_lookup.argtypes = [_p, _p, _i, _i, _p, _p, _p, _p, _p, _p]
     lib.oracle_lookup.restype = _i
+    lib.oracle_round_analytics.argtypes = [_p, _p, _i, _i64, _i64, _i, _i, _i, _p, _d, _d] + [_p] * 6
+    lib.oracle_round_analytics.restype = _i
     lib.oracle_branch_attention.argtypes = [_p, _p, _p, _p, _i, _i64, _p, _p, _i, _i, _i, _i, _i,
                                             _i, _d, _p, _p, _p]
     lib.oracle_branch_attention.restype = _i
@@ -215,6 +217,25 @@ def lookup(guess, payload, K, F, accept_len, bonus):
                               _ptr(_c(accept_len, np.int32)), _ptr(_c(bonus, np.int32)),
                               _ptr(slot), _ptr(nxt), _ptr(flags))
     return dict(slot=slot, next_tokens=nxt, hits=int(hits), flags=flags)
+
+
+def round_analytics(target, draft, V, F, C, T):
+    """Exact analytics of the round before any draw: alpha [B,K], resid_w [B,K],
+    p_accept [B,K+1] = P(a = k), hit_mass [B,K+1] = P(bonus among the depth-k
+    guesses | a = k), hit_rate [B], exp_tokens [B]."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    assert target.shape == draft.shape and target.dtype == draft.dtype
+    B, K1, _ = target.shape
+    K = K1 - 1
+    ss, rs = _strides(target, V)
+    out = dict(alpha=np.zeros((B, K)), resid_w=np.zeros((B, K)), p_accept=np.zeros((B, K + 1)),
+               hit_mass=np.zeros((B, K + 1)), hit_rate=np.zeros(B), exp_tokens=np.zeros(B))
+    _L().oracle_round_analytics(_ptr(target), _ptr(draft), _dtype_code(target), ss, rs, B, K,
+                                int(V), _ptr(_F(F)), float(C), float(T),
+                                *[_ptr(out[k]) for k in ("alpha", "resid_w", "p_accept", "hit_mass",
+                                                         "hit_rate", "exp_tokens")])
+    return out
 
 
 def branch_attention(q, k_cache, v_cache, block_table, prefix_len, parent, Hkv, scale=None):

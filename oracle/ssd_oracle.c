@@ -425,6 +425,78 @@ int oracle_lookup(const int32_t *guess, const int32_t *payload, int B, int K, co
   return hits;
 }
 
+/* Exact analytics of one round, before any uniform is drawn (technical
+ * summary "超越传统SD：SSD框架全异步解码实现4.7倍平均加速": section "投机解码的瓶颈与
+ * SSD 的核心机制" names the acceptance rate alpha; "Saguaro 算法" part 1
+ * makes the chance that the bonus token lands among the cached guesses the
+ * objective of the fan-out).  With the logit rows fixed, d_j ~ q'_j is
+ * accepted with probability sum_i q'_j(i) min(1, p_j(i)/q'_j(i)) =
+ * sum_i min(p_j(i), q'_j(i)), so per sequence:
+ *   alpha[j-1]  = sum_i min(p_j(i), q'_j(i))                 (j = 1..K)
+ *   resid_w[j-1] = W_j = sum_i max(0, p_j(i) - q'_j(i))       (= 1 - alpha_j)
+ *   p_accept[k] = P(a = k) = prod_{j<=k} alpha_j * W_{k+1}   (k < K)
+ *   p_accept[K] = prod_{j<=K} alpha_j
+ *   hit_mass[k] = P(bonus in S_{k+1} | a = k): the bonus is drawn from the
+ *                 normalised residual r_{k+1} / W_{k+1} (from p_{k+1} when
+ *                 W_{k+1} = 0) for k < K and from p_{K+1} for k = K; S_{k+1}
+ *                 is the top-F_k list of draft row k+1 (the depth-k guesses)
+ *   hit_rate    = sum_k p_accept[k] hit_mass[k]
+ *   exp_tokens  = sum_k p_accept[k] (k + 1)   (tokens emitted per round). */
+int oracle_round_analytics(const void *target, const void *draft, int dtype, int64_t seq_stride,
+                           int64_t row_stride, int B, int K, int V, const int32_t *F, double C,
+                           double T, double *alpha, double *resid_w, double *p_accept,
+                           double *hit_mass, double *hit_rate, double *exp_tokens) {
+  double *zt = (double *)malloc(sizeof(double) * (size_t)V);
+  double *zd = (double *)malloc(sizeof(double) * (size_t)V);
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  double *qp = (double *)malloc(sizeof(double) * (size_t)V);
+  uint8_t *ins = (uint8_t *)malloc((size_t)V);
+  for (int b = 0; b < B; b++) {
+    double run = 1.0, hit = 0.0, etok = 0.0;
+    for (int k = 0; k <= K; k++) {
+      int64_t off = b * seq_stride + (int64_t)k * row_stride; /* position k + 1 */
+      load_row(target, dtype, off, V, zt);
+      load_row(draft, dtype, off, V, zd);
+      oracle_softmax(zt, V, T, p);
+      /* S_{k+1} and, for k < K, the distribution the draft samples d_{k+1} from */
+      oracle_saguaro_dist(zd, V, F[k], C, T, qp, ins);
+      double pk, hk = 0.0;
+      if (k < K) {
+        double al = 0.0, w = 0.0;
+        for (int i = 0; i < V; i++) {
+          al += (p[i] < qp[i]) ? p[i] : qp[i];
+          w += (p[i] > qp[i]) ? p[i] - qp[i] : 0.0;
+        }
+        alpha[b * K + k] = al;
+        resid_w[b * K + k] = w;
+        for (int i = 0; i < V; i++) {
+          if (!ins[i]) continue;
+          if (w > 0.0) hk += ((p[i] > qp[i]) ? p[i] - qp[i] : 0.0) / w;
+          else hk += p[i];
+        }
+        pk = run * w;
+        run *= al;
+      } else {
+        for (int i = 0; i < V; i++)
+          if (ins[i]) hk += p[i];
+        pk = run;
+      }
+      p_accept[b * (K + 1) + k] = pk;
+      hit_mass[b * (K + 1) + k] = hk;
+      hit += pk * hk;
+      etok += pk * (double)(k + 1);
+    }
+    hit_rate[b] = hit;
+    exp_tokens[b] = etok;
+  }
+  free(zt);
+  free(zd);
+  free(p);
+  free(qp);
+  free(ins);
+  return 0;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Branch attention                                                        */
 /* q [B, Nq, Hq, d] bf16; k_cache, v_cache [num_blocks, Hkv, 16, d] bf16;   */

@@ -496,6 +496,48 @@ def test_enumeration_V8_K3(C):
     assert abs(mc - hit) < 5 * np.sqrt(hit * (1 - hit) / n)
 
 
+@pytest.mark.parametrize("C,T", [(1.0, 1.0), (0.5, 1.0), (0.25, 0.6)])
+def test_round_analytics_match_enumeration(C, T):
+    """The analytics against the exhaustive enumeration of all 8^3 draft
+    sequences at V = 8, K = 3: P(a = k), the hit rate and the expected tokens
+    per round, plus alpha against the verification's own alpha."""
+    K, F = 3, (3, 2, 1, 1)
+    zt, zd = _v8_rows(300 + int(C * 10), K)
+    Pab, Pa, alpha, p = _exact_outcomes(zt, zd, F, C, T)
+    an = oracle.round_analytics(zt[None], zd[None], 8, F, C, T)
+    assert np.allclose(an["p_accept"][0], Pa, rtol=0, atol=1e-12)
+    assert abs(an["p_accept"][0].sum() - 1.0) < 1e-12
+    assert np.allclose(an["alpha"][0], alpha, rtol=0, atol=1e-12)
+    assert np.allclose(an["resid_w"][0], 1.0 - np.array(alpha), rtol=0, atol=1e-12)
+    guess = [oracle.topf(zd[k].astype(np.float64), F[k]) for k in range(K + 1)]
+    hit = sum(Pab[a, b] for a in range(K + 1) for b in guess[a])
+    assert abs(an["hit_rate"][0] - hit) < 1e-12
+    for a in range(K + 1):
+        assert abs(an["hit_mass"][0, a] * Pa[a] - sum(Pab[a, b] for b in guess[a])) < 1e-12
+    assert abs(an["exp_tokens"][0] - sum(Pa[k] * (k + 1) for k in range(K + 1))) < 1e-12
+    ud, ua, ub = w.round_uniforms(5, 0, 1, K)
+    d, _, _ = oracle.saguaro_sample(zd[None], 8, F, C, T, ud)
+    v = oracle.verify(zt[None], zd[None], 8, F, C, T, d, ua, ub)
+    assert np.allclose(v["alpha"][0], an["alpha"][0], rtol=0, atol=1e-14)
+
+
+def test_round_analytics_greedy_and_no_drafts():
+    """T = 0: alpha_j is 1 when both argmaxes agree, else 0, so the accept
+    count is the greedy chain's; K = 0: the round emits one token, drawn from
+    p_1, and hits when it is among the depth-0 guesses."""
+    zt = np.array([[[0.0, 2.0, 1.0], [3.0, 0.0, 0.0], [0.0, 0.0, 5.0]]], np.float32)
+    zd = np.array([[[0.0, 3.0, 1.0], [0.0, 4.0, 0.0], [5.0, 0.0, 0.0]]], np.float32)
+    an = oracle.round_analytics(zt, zd, 3, (1, 1, 2), 0.5, 0.0)
+    assert list(an["alpha"][0]) == [1.0, 0.0]
+    assert list(an["p_accept"][0]) == [0.0, 1.0, 0.0]
+    assert an["hit_mass"][0, 1] == 0.0 and an["hit_rate"][0] == 0.0  # argmax 0 is not draft row 2's top-1
+    assert an["exp_tokens"][0] == 2.0
+    z1 = np.log(np.array([[[0.5, 0.3, 0.2]]])).astype(np.float32)
+    an0 = oracle.round_analytics(z1, z1, 3, (2,), 1.0, 1.0)
+    assert an0["p_accept"][0, 0] == 1.0 and an0["exp_tokens"][0] == 1.0
+    assert abs(an0["hit_rate"][0] - 0.8) < 1e-6
+
+
 # ---------------------------------------------------------------------------
 # outcome prediction and cache lookup
 # ---------------------------------------------------------------------------
