@@ -227,6 +227,34 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
                        size_t ws_bytes, ssd_stream_t s);
 
 /*
+ * Exact analytics of a round, before any uniform is drawn [B,
+ * "投机解码的瓶颈与 SSD 的核心机制": the acceptance rate alpha; B, "Saguaro 算法"
+ * part 1: the chance that the bonus token lands among the cached guesses is
+ * what the fan-out is chosen for].  With the logit rows fixed, a draft token
+ * d_j ~ q'_j is accepted with probability sum_i min(p_j(i), q'_j(i)), so per
+ * sequence b (arguments as in ssd_round; F also names the guess lists):
+ *   alpha    [B, K]  = sum_i min(p_j(i), q'_j(i))                 (or NULL)
+ *   resid_w  [B, K]  = W_j = sum_i max(0, p_j(i) - q'_j(i))        (or NULL)
+ *   p_accept [B, K+1]: P(a = k) = prod_{j<=k} alpha_j * W_{k+1}, P(a = K) = prod alpha_j
+ *   hit_mass [B, K+1]: P(bonus among the F_k guesses of depth k | a = k); the
+ *            bonus follows r_{k+1} / W_{k+1} (p_{k+1} when W_{k+1} = 0) for
+ *            k < K and p_{K+1} for k = K                         (or NULL)
+ *   hit_rate [B] = sum_k P(a = k) hit_mass_k  (the exact cache hit rate)
+ *   exp_tokens [B] = sum_k P(a = k) (k + 1)  (tokens emitted per round)
+ * All fp32.  T = 0 gives the greedy limit (alpha_j = 1 when both argmaxes
+ * agree).  The statistics pass reads every row once; the sums of min and
+ * max(0, p - q') then read the K row pairs again (from L2 when the batch
+ * fits).  The fan-out may then be re-split with ssd_fanout_split(budget, K,
+ * r) at a measured ratio, e.g. the batch's mean alpha.
+ */
+ssd_status_t ssd_round_analytics(const void *target, const void *draft, ssd_dtype_t dt,
+                                 int64_t seq_stride, int64_t row_stride, int B, int K, int V,
+                                 const int32_t *F, float C, float T, float *alpha, float *resid_w,
+                                 float *p_accept, float *hit_mass, float *hit_rate,
+                                 float *exp_tokens, uint32_t *status, void *ws, size_t ws_bytes,
+                                 ssd_stream_t s);
+
+/*
  * Timing hook for profiling: while set (both non-NULL cudaEvent_t handles),
  * every vocabulary call records `before` and `after` on its stream around its
  * HBM statistics pass (the dominant kernel), so a caller can time that kernel

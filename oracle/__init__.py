@@ -78,7 +78,7 @@ def _declare(lib):
     lib.oracle_predict.restype = _i
     lib.oracle_lookup.argtypes = [_p, _p, _i, _i, _p, _p, _p, _p, _p, _p]
     lib.oracle_lookup.restype = _i
-    lib.oracle_round_analytics.argtypes = [_p, _p, _i, _i64, _i64, _i, _i, _i, _p, _d, _d] + [_p] * 6
+    lib.oracle_round_analytics.argtypes = [_p, _p, _i, _i64, _i64, _i, _i, _i, _p, _d, _d] + [_p] * 7
     lib.oracle_round_analytics.restype = _i
     lib.oracle_branch_attention.argtypes = [_p, _p, _p, _p, _i, _i64, _p, _p, _i, _i, _i, _i, _i,
                                             _i, _d, _p, _p, _p]
@@ -222,7 +222,8 @@ def lookup(guess, payload, K, F, accept_len, bonus):
 def round_analytics(target, draft, V, F, C, T):
     """Exact analytics of the round before any draw: alpha [B,K], resid_w [B,K],
     p_accept [B,K+1] = P(a = k), hit_mass [B,K+1] = P(bonus among the depth-k
-    guesses | a = k), hit_rate [B], exp_tokens [B]."""
+    guesses | a = k), hit_rate [B], exp_tokens [B], and hit_scale [B,K+1], the size of
+    the terms whose differences make up hit_mass."""
     target = np.ascontiguousarray(target)
     draft = np.ascontiguousarray(draft)
     assert target.shape == draft.shape and target.dtype == draft.dtype
@@ -230,11 +231,12 @@ def round_analytics(target, draft, V, F, C, T):
     K = K1 - 1
     ss, rs = _strides(target, V)
     out = dict(alpha=np.zeros((B, K)), resid_w=np.zeros((B, K)), p_accept=np.zeros((B, K + 1)),
-               hit_mass=np.zeros((B, K + 1)), hit_rate=np.zeros(B), exp_tokens=np.zeros(B))
+               hit_mass=np.zeros((B, K + 1)), hit_rate=np.zeros(B), exp_tokens=np.zeros(B),
+               hit_scale=np.zeros((B, K + 1)))
     _L().oracle_round_analytics(_ptr(target), _ptr(draft), _dtype_code(target), ss, rs, B, K,
                                 int(V), _ptr(_F(F)), float(C), float(T),
                                 *[_ptr(out[k]) for k in ("alpha", "resid_w", "p_accept", "hit_mass",
-                                                         "hit_rate", "exp_tokens")])
+                                                         "hit_rate", "exp_tokens", "hit_scale")])
     return out
 
 

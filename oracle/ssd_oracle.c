@@ -441,11 +441,15 @@ int oracle_lookup(const int32_t *guess, const int32_t *payload, int B, int K, co
  *                 W_{k+1} = 0) for k < K and from p_{K+1} for k = K; S_{k+1}
  *                 is the top-F_k list of draft row k+1 (the depth-k guesses)
  *   hit_rate    = sum_k p_accept[k] hit_mass[k]
- *   exp_tokens  = sum_k p_accept[k] (k + 1)   (tokens emitted per round). */
+ *   exp_tokens  = sum_k p_accept[k] (k + 1)   (tokens emitted per round)
+ *   hit_scale[k] = sum_{i in S_{k+1}} (p_{k+1}(i) + q'_{k+1}(i)) / W_{k+1} when
+ *                 the residual is used, else hit_mass[k]: the size of the terms
+ *                 whose differences make up hit_mass[k] (an error of eps in
+ *                 each probability moves hit_mass[k] by at most eps times it). */
 int oracle_round_analytics(const void *target, const void *draft, int dtype, int64_t seq_stride,
                            int64_t row_stride, int B, int K, int V, const int32_t *F, double C,
                            double T, double *alpha, double *resid_w, double *p_accept,
-                           double *hit_mass, double *hit_rate, double *exp_tokens) {
+                           double *hit_mass, double *hit_rate, double *exp_tokens, double *hit_scale) {
   double *zt = (double *)malloc(sizeof(double) * (size_t)V);
   double *zd = (double *)malloc(sizeof(double) * (size_t)V);
   double *p = (double *)malloc(sizeof(double) * (size_t)V);
@@ -460,7 +464,7 @@ int oracle_round_analytics(const void *target, const void *draft, int dtype, int
       oracle_softmax(zt, V, T, p);
       /* S_{k+1} and, for k < K, the distribution the draft samples d_{k+1} from */
       oracle_saguaro_dist(zd, V, F[k], C, T, qp, ins);
-      double pk, hk = 0.0;
+      double pk, hk = 0.0, hs = 0.0;
       if (k < K) {
         double al = 0.0, w = 0.0;
         for (int i = 0; i < V; i++) {
@@ -471,18 +475,25 @@ int oracle_round_analytics(const void *target, const void *draft, int dtype, int
         resid_w[b * K + k] = w;
         for (int i = 0; i < V; i++) {
           if (!ins[i]) continue;
-          if (w > 0.0) hk += ((p[i] > qp[i]) ? p[i] - qp[i] : 0.0) / w;
-          else hk += p[i];
+          if (w > 0.0) {
+            hk += ((p[i] > qp[i]) ? p[i] - qp[i] : 0.0) / w;
+            hs += (p[i] + qp[i]) / w;
+          } else {
+            hk += p[i];
+            hs += p[i];
+          }
         }
         pk = run * w;
         run *= al;
       } else {
         for (int i = 0; i < V; i++)
           if (ins[i]) hk += p[i];
+        hs = hk;
         pk = run;
       }
       p_accept[b * (K + 1) + k] = pk;
       hit_mass[b * (K + 1) + k] = hk;
+      if (hit_scale) hit_scale[b * (K + 1) + k] = hs;
       hit += pk * hk;
       etok += pk * (double)(k + 1);
     }

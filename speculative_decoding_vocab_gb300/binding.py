@@ -28,7 +28,7 @@ FLAG_BAD_PREFIX = 64
 EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events", "ssd_set_trace",
            "ssd_saguaro_sample",
            "ssd_verify", "ssd_verify_noalloc", "ssd_verify_noalloc_max_bytes",
-           "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round",
+           "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round", "ssd_round_analytics",
            "ssd_attention_workspace_size", "ssd_branch_attention")
 
 _lib = None
@@ -98,6 +98,9 @@ def _declare(lib):
     lib.ssd_round.argtypes = ([_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp, _vp]
                               + [_vp] * 14 + [_vp, _sz, _vp])
     lib.ssd_round.restype = _i
+    lib.ssd_round_analytics.argtypes = ([_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f]
+                                        + [_vp] * 7 + [_vp, _sz, _vp])
+    lib.ssd_round_analytics.restype = _i
     lib.ssd_attention_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
     lib.ssd_attention_workspace_size.restype = _sz
     lib.ssd_branch_attention.argtypes = [_vp, _vp, _vp, _vp, _i, _i64, _vp, _vp, _i, _i, _i, _i, _i,
@@ -282,6 +285,19 @@ def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_
         _ptr(accept_len), _ptr(out_tokens), _ptr(bonus), _ptr(accept_prob), _ptr(resid_mass),
         _ptr(guess), _ptr(guess_q), _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(near_ties),
         _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_round_analytics(target, draft, V, F, C, T, p_accept, hit_rate, exp_tokens, alpha=None,
+                        resid_w=None, hit_mass=None, status=None, ws=None, stream=None):
+    dt, ss, rs = _logit_meta(target)
+    if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
+        raise ValueError("target and draft logits must share dtype, shape and strides")
+    B, K1 = target.shape[0], target.shape[1]
+    _check("ssd_round_analytics", load().ssd_round_analytics(
+        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(alpha), _ptr(resid_w), _ptr(p_accept), _ptr(hit_mass), _ptr(hit_rate),
+        _ptr(exp_tokens), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
 
 
 def ssd_attention_workspace_size(B, Nq, Hq, Hkv, d, max_prefix) -> int:

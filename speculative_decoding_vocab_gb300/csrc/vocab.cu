@@ -112,7 +112,7 @@ struct VocabArgs {
   int npairs;  // row pairs per sequence, r = 0 .. npairs-1
   long nst;    // chunks of the call: B * nslots * nchunks
   int b0;      // k_stats: the first sequence of this launch (grid z = sequence - b0)
-  int do_sample, do_verify, do_predict, do_lookup;
+  int do_sample, do_verify, do_predict, do_lookup, do_analytics;
   RowSlot slot[kMaxSlots];                   // ordered by pair: target r, then draft r
   int tsl[kMaxK + 1], dsl[kMaxK + 1];        // slot of target / draft row r (-1: none)
   int pair_chunks[kMaxK + 1];                // chunks of pair r (both rows)
@@ -134,6 +134,9 @@ struct VocabArgs {
   PosInfo *pos;      // [B][K]
   float *rmass;      // [B][nchunks * kQuarters] residual mass per unit
   float *rbs;        // [B][nchunks][kBlocks] residual block sums
+  float *amass;      // analytics: [B][K][nchunks * kQuarters][2] unit sums of min(p, q'), max(0, p - q')
+  // analytics outputs
+  float *an_alpha, *an_resid_w, *an_p_accept, *an_hit_mass, *an_hit_rate, *an_exp_tokens;
   // inputs / outputs
   const float *u_draft, *u_acc, *u_bonus;
   const int32_t *d_in;
@@ -1100,18 +1103,26 @@ SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t
                       Smem &sh) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nb = a.nchunks * kBlocks;
+  const int lane = tid & 31;
   auto key_at = [&](int i) -> uint32_t { return staged ? bmk[i] : __ldcg(bmk + i); };
-  for (int i = tid; i < nb; i += kThreads) {
-    const uint32_t k = key_at(i);
-    if (k) atomicAdd(&sh.hist[0][k >> 24], 1u);
+  // Bucket counts, one add per distinct bucket of a warp's 32 keys (block
+  // maxima of one row crowd into a few buckets; adding key by key would
+  // serialise the shared-memory atomics on them).  The loops run whole warps.
+  auto count = [&](uint32_t *hist, bool v, uint32_t bucket) {
+    const uint32_t peers = __match_any_sync(0xffffffffu, v ? bucket : 0xFFFFFFFFu);
+    if (v && lane == __ffs(peers) - 1) atomicAdd(&hist[bucket], static_cast<uint32_t>(__popc(peers)));
+  };
+  for (int i0 = warp * 32; i0 < nb; i0 += kThreads) {
+    const uint32_t k = (i0 + lane < nb) ? key_at(i0 + lane) : 0u;
+    count(sh.hist[0], k != 0u, k >> 24);
   }
   __syncthreads();
   uint32_t b1, b2;
   int above, above2;
   find_bucket(sh.hist[0], F, b1, above);
-  for (int i = tid; i < nb; i += kThreads) {
-    const uint32_t k = key_at(i);
-    if (k && (k >> 24) == b1) atomicAdd(&sh.hist[1][(k >> 16) & 0xFFu], 1u);
+  for (int i0 = warp * 32; i0 < nb; i0 += kThreads) {
+    const uint32_t k = (i0 + lane < nb) ? key_at(i0 + lane) : 0u;
+    count(sh.hist[1], k != 0u && (k >> 24) == b1, (k >> 16) & 0xFFu);
   }
   __syncthreads();
   find_bucket(sh.hist[1], F - above, b2, above2);
@@ -1250,7 +1261,7 @@ __device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Sta
     const float mdk = __fmul_rn(sh.ri.md, a.kT);
     if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.ri.md, sh.ri.ad);  // the top-1: the row's argmax
     if (F == 1) __syncthreads();
-    if (a.do_verify || a.do_lookup)
+    if (a.do_verify || a.do_lookup || a.do_analytics)
       for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
     // the draft's normalised mass on S: lane-strided partial sums, a fixed tree
     if (warp == 0) {
@@ -1890,6 +1901,161 @@ __global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ V
   if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ===========================================================================
+// round analytics: alpha_j, W_j, P(a = k), the hit rate, expected tokens
+// ===========================================================================
+// One CTA per (sequence b, position j = r + 1, unit u = chunk u / kQuarters,
+// rounds 2 (u % kQuarters) and the next) of row pair r < K, once the
+// statistics pass has merged the rows: the unit's sums of min(p, q') and of
+// max(0, p - q') (each lane in element order, then the warps by a fixed tree).
+template <class E>
+__global__ void __launch_bounds__(kThreads) k_alpha(const __grid_constant__ VocabArgs a) {
+  __shared__ float red[2][kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nu = a.nchunks * kQuarters;
+  const long id = blockIdx.x;
+  const int u = static_cast<int>(id % nu);
+  const int r = static_cast<int>((id / nu) % a.K);
+  const int b = static_cast<int>(id / (static_cast<long>(nu) * a.K));
+  const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
+  const RowInfo ri = ldcg_row(a.rows + rr);
+  const int F = a.Fs[r];
+  const uint64_t keyF = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
+  const WResidual wf = residual_weights(a, ri, keyF, F);  // p and q' factors
+  const char *rowT = row_ptr(a, 0, b, r, E::kSize);
+  const char *rowD = row_ptr(a, 1, b, r, E::kSize);
+  const int c = u / kQuarters, g = u % kQuarters;
+  const int e0 = c * a.chunk_elems;
+  const int n = min(a.chunk_elems, a.V - e0);
+  float smin = 0.f, sres = 0.f;
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const int i0 = ((2 * g + jj) * kThreads + warp * 32 + lane) * E::kVec;
+    float ft[E::kVec], fd[E::kVec];
+    ld_vec<E>(rowT, e0, n, i0, -__int_as_float(0x7f800000), ft);
+    ld_vec<E>(rowD, e0, n, i0, -__int_as_float(0x7f800000), fd);
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e) {
+      if (i0 + e >= n) continue;
+      const float p = __fmul_rn(ex2(__fmaf_rn(ft[e], wf.kT, -wf.mtk)), wf.inv_st);
+      const float f = (wf.hasS && cand_key(fd[e], e0 + i0 + e) >= wf.keyF) ? wf.fC : wf.f1;
+      const float q = __fmul_rn(ex2(__fmaf_rn(fd[e], wf.kT, -wf.mdk)), f);
+      smin = __fadd_rn(smin, fminf(p, q));
+      sres = __fadd_rn(sres, fmaxf(__fsub_rn(p, q), 0.f));
+    }
+  }
+  smin = warp_sum(smin);
+  sres = warp_sum(sres);
+  if (lane == 0) {
+    red[0][warp] = smin;
+    red[1][warp] = sres;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float m = 0.f, w = 0.f;
+    for (int k = 0; k < kWarps; ++k) {
+      m = __fadd_rn(m, red[0][k]);
+      w = __fadd_rn(w, red[1][k]);
+    }
+    float *o = a.amass + ((static_cast<size_t>(b) * a.K + r) * nu + u) * 2;
+    o[0] = m;
+    o[1] = w;
+  }
+}
+
+// One CTA per sequence, after k_alpha (T > 0) or straight after the
+// statistics pass (T = 0, where p and q' are one-hot at the argmaxes): alpha
+// and W per position, the chance that the bonus lands among the depth-k
+// guesses given a = k, P(a = k), the hit rate and the expected tokens.
+template <class E>
+__global__ void __launch_bounds__(kThreads) k_analytics(const __grid_constant__ VocabArgs a) {
+  __shared__ float s_alpha[kMaxK + 1], s_w[kMaxK + 1], s_hit[kMaxK + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int nu = a.nchunks * kQuarters;
+  const int K = a.K;
+  // alpha_j and W_j: warp r % kWarps sums position r's units in order
+  for (int r = warp; r < K; r += kWarps) {
+    const size_t rr = static_cast<size_t>(b) * (K + 1) + r;
+    float al, w;
+    if (a.greedy) {
+      const RowInfo ri = ldcg_row(a.rows + rr);
+      al = (ri.at == ri.ad) ? 1.f : 0.f;
+      w = 1.f - al;
+    } else {
+      const float *m = a.amass + (static_cast<size_t>(b) * K + r) * nu * 2;
+      float sa = 0.f, sw = 0.f;
+      for (int u = lane; u < nu; u += 32) {
+        sa = __fadd_rn(sa, __ldcg(m + 2 * u));
+        sw = __fadd_rn(sw, __ldcg(m + 2 * u + 1));
+      }
+      al = warp_sum(sa);
+      w = warp_sum(sw);
+    }
+    if (lane == 0) {
+      s_alpha[r] = al;
+      s_w[r] = w;
+    }
+  }
+  __syncthreads();
+  // hit masses: warp k % kWarps over depth k's guesses (S_{k+1}, the top-F_k
+  // of draft row k), each weighted by the bonus distribution given a = k
+  for (int k = warp; k <= K; k += kWarps) {
+    const size_t rr = static_cast<size_t>(b) * (K + 1) + k;
+    const RowInfo ri = ldcg_row(a.rows + rr);
+    const int F = a.Fs[k];
+    const char *rowT = row_ptr(a, 0, b, k, E::kSize);
+    const bool resid = k < K && s_w[k] > 0.f;
+    float h = 0.f;
+    if (a.greedy) {
+      // the bonus is the target argmax (the residual of one-hot rows is that
+      // same one-hot whenever it has mass)
+      for (int i = lane; i < F; i += 32)
+        if (cand_idx(ldcg_key(a.S + rr * a.Fcap + i)) == ri.at) h = 1.f;
+      h = warp_max(h);
+    } else {
+      const float mtk = __fmul_rn(ri.mt, a.kT);
+      const float inv_st = __frcp_rn(ri.st);
+      const float mdk = __fmul_rn(ri.md, a.kT);
+      const float sN = __fmul_rn(ri.sd, norm_N(a.C, ri.sq));
+      const float fC = __fdiv_rn(a.C, sN);
+      for (int i = lane; i < F; i += 32) {
+        const uint64_t key = ldcg_key(a.S + rr * a.Fcap + i);
+        if (!key) continue;
+        const int d = cand_idx(key);
+        const float p = __fmul_rn(ex2(__fmaf_rn(E::ld(rowT, d), a.kT, -mtk)), inv_st);
+        float x = p;
+        if (resid) {  // every guess is in S, so q' carries the factor C
+          const float q = __fmul_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), fC);
+          x = fmaxf(__fsub_rn(p, q), 0.f);
+        }
+        h = __fadd_rn(h, x);
+      }
+      h = warp_sum(h);
+      if (resid) h = __fdiv_rn(h, s_w[k]);
+    }
+    if (lane == 0) s_hit[k] = h;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float run = 1.f, hit = 0.f, etok = 0.f;
+    for (int k = 0; k <= K; ++k) {
+      const float pk = (k < K) ? __fmul_rn(run, s_w[k]) : run;
+      if (k < K) run = __fmul_rn(run, s_alpha[k]);
+      hit = __fmaf_rn(pk, s_hit[k], hit);
+      etok = __fmaf_rn(pk, static_cast<float>(k + 1), etok);
+      a.an_p_accept[static_cast<size_t>(b) * (K + 1) + k] = pk;
+      if (a.an_hit_mass) a.an_hit_mass[static_cast<size_t>(b) * (K + 1) + k] = s_hit[k];
+      if (k < K) {
+        if (a.an_alpha) a.an_alpha[static_cast<size_t>(b) * K + k] = s_alpha[k];
+        if (a.an_resid_w) a.an_resid_w[static_cast<size_t>(b) * K + k] = s_w[k];
+      }
+    }
+    a.an_hit_rate[b] = hit;
+    a.an_exp_tokens[b] = etok;
+  }
+}
+
 struct LookupArgs {
   const int32_t *guess, *payload, *accept_len, *bonus;
   int32_t *slot, *next_tokens;
@@ -1942,7 +2108,7 @@ namespace {
 struct Layout {
   int nslots, nchunks, chunk_elems, Fcap;
   size_t ctr_words;
-  size_t ctr_off, stats_off, blk_off, bmk_off, rows_off, S_off, pos_off, rmass_off, rbs_off, total;
+  size_t ctr_off, stats_off, blk_off, bmk_off, rows_off, S_off, pos_off, rmass_off, rbs_off, amass_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1983,6 +2149,8 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + Bn * L->nchunks * kQuarters * sizeof(float), 256);
   L->rbs_off = o;
   o = align_up(o + Bn * L->nchunks * kBlocks * sizeof(float), 256);
+  L->amass_off = o;
+  o = align_up(o + Bn * (K > 0 ? K : 1) * L->nchunks * kQuarters * 2 * sizeof(float), 256);
   L->total = o;
   return true;
 }
@@ -2050,6 +2218,7 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.blk = reinterpret_cast<BlockRec *>(w + L.blk_off);
   a.rmass = reinterpret_cast<float *>(w + L.rmass_off);
   a.rbs = reinterpret_cast<float *>(w + L.rbs_off);
+  a.amass = reinterpret_cast<float *>(w + L.amass_off);
   a.status = status;
   return a;
 }
@@ -2156,6 +2325,22 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
 
 cudaError_t launch_any(ssd_dtype_t dt, VocabArgs &a, cudaStream_t s) {
   return dt == SSD_F32 ? launch_vocab<EF32>(a, s) : launch_vocab<EBF16>(a, s);
+}
+
+// The analytics kernels after the statistics pass: the unit sums of every
+// row pair r < K (T > 0), then one CTA per sequence.
+template <class E>
+cudaError_t launch_analytics(const VocabArgs &a, cudaStream_t s) {
+  if (a.B < 1) return cudaSuccess;
+  if (!a.greedy && a.K > 0) {
+    const long n = static_cast<long>(a.B) * a.K * a.nchunks * kQuarters;
+    if (n > 0x7fffffffL) return cudaErrorInvalidValue;
+    k_alpha<E><<<static_cast<unsigned>(n), kThreads, 0, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  k_analytics<E><<<static_cast<unsigned>(a.B), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 // Fixed device scratch for ssd_verify_noalloc: one array per GPU that loads
@@ -2416,6 +2601,35 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
   a.hits = hits;
   a.near_ties = near_ties;
   return cuda_status(launch_any(dt, a, cs));
+}
+
+ssd_status_t ssd_round_analytics(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                                 int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                                 float *alpha, float *resid_w, float *p_accept, float *hit_mass, float *hit_rate,
+                                 float *exp_tokens, uint32_t *status, void *ws, size_t ws_bytes, ssd_stream_t s) {
+  Layout L;
+  ssd_status_t st = layout_or_error(B, K, V, dt, F, &L);
+  if (st != SSD_OK) return st;
+  st = check_logits(target, dt, seq_stride, row_stride, B, K, V);
+  if (st == SSD_OK) st = check_logits(draft, dt, seq_stride, row_stride, B, K, V);
+  if (st != SSD_OK) return st;
+  st = check_common(B, C, T, L, ws, ws_bytes, true);
+  if (st != SSD_OK) return st;
+  if (B == 0) return SSD_OK;
+  if (!p_accept || !hit_rate || !exp_tokens || !status) return SSD_ERR_INVALID_ARG;
+  VocabArgs a = base_args(target, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
+  a.do_analytics = 1;
+  set_slots(a, K + 1, K + 1, true, false);
+  a.an_alpha = alpha;
+  a.an_resid_w = resid_w;
+  a.an_p_accept = p_accept;
+  a.an_hit_mass = hit_mass;
+  a.an_hit_rate = hit_rate;
+  a.an_exp_tokens = exp_tokens;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  cudaError_t e = launch_any(dt, a, cs);
+  if (e == cudaSuccess) e = dt == SSD_F32 ? launch_analytics<EF32>(a, cs) : launch_analytics<EBF16>(a, cs);
+  return cuda_status(e);
 }
 
 size_t ssd_verify_noalloc_max_bytes(void) { return kStaticScratchBytes; }

@@ -515,6 +515,10 @@ def test_round_analytics_match_enumeration(C, T):
     for a in range(K + 1):
         assert abs(an["hit_mass"][0, a] * Pa[a] - sum(Pab[a, b] for b in guess[a])) < 1e-12
     assert abs(an["exp_tokens"][0] - sum(Pa[k] * (k + 1) for k in range(K + 1))) < 1e-12
+    qp = [oracle.saguaro_dist(zd[j].astype(np.float64), F[j], C, T)[0] for j in range(K)]
+    for k in range(K):
+        scale = sum(p[k + 1 - 1][b] + qp[k][b] for b in guess[k]) / (1.0 - alpha[k])
+        assert abs(an["hit_scale"][0, k] - scale) < 1e-12
     ud, ua, ub = w.round_uniforms(5, 0, 1, K)
     d, _, _ = oracle.saguaro_sample(zd[None], 8, F, C, T, ud)
     v = oracle.verify(zt[None], zd[None], 8, F, C, T, d, ua, ub)
