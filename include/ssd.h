@@ -266,16 +266,18 @@ ssd_status_t ssd_set_timing_events(void *before, void *after);
 
 /*
  * Work trace for profiling: while set, every vocabulary call writes, for each
- * CTA of its kernels, eight 64-bit words into `buf` (device memory), the
- * statistics kernel's CTAs first (in launch order), then the residual
- * kernel's: (SM << 48 | kind << 40 | sequence << 20 | index) and seven
- * %globaltimer marks in ns (0 = not reached).  kind: 0 chunk statistics,
- * 1 + pair merge, 2 residual chunk, 3 + final steps.  Statistics CTA marks:
- * start, chunk landed, records published, the merge's list and draw begin,
- * pair merged, sequence finished, end.  Residual CTA marks: start, -, unit
- * published, the other units published, unit and block located, bonus drawn,
- * end.  Calls whose CTAs do not fit in `bytes` write nothing.  Process-wide,
- * not thread-safe; NULL clears.  Diagnostics only.
+ * CTA of its kernels, eight 64-bit words into `buf` (device memory): first
+ * the statistics kernel's CTAs (grid order: chunk, row slot, sequence), then
+ * the pair kernel's (sequence-major, one per row pair), then the residual
+ * kernel's.  Word 0 = (SM << 48 | kind << 40 | sequence << 20 | index), kind
+ * 0 statistics (index: row slot * chunks + chunk), 1 pair (index: position),
+ * 2 residual unit (index: unit); words 1-7 = %globaltimer marks in ns (0 =
+ * not reached): start, after the wait for the previous kernel, then per
+ * kind -- pair: records staged, rows merged, draw of d done, top-F done,
+ * end; residual: records read, unit pass done, ticket taken, bonus drawn,
+ * end (statistics CTAs mark only start and end).  Calls whose CTAs do not
+ * fit in `bytes`, or with more than 65535 sequences, write nothing.
+ * Process-wide, not thread-safe; NULL clears.  Diagnostics only.
  */
 ssd_status_t ssd_set_trace(void *buf, size_t bytes);
 

@@ -1,6 +1,7 @@
 // vocab.cu -- the vocabulary-wide kernels of one speculation round on sm_103a:
-// Saguaro draft sampling, lossless verification with residual / bonus draw,
-// outcome prediction (top-F_k guesses) and the speculation-cache lookup.
+// Saguaro draft sampling, lossless verification with the residual / bonus
+// draw, outcome prediction (top-F_k guesses), the speculation-cache lookup and
+// the exact analytics of a round.
 //
 // Method: speculative-speculative decoding with the Saguaro algorithm as the
 // 機器之心 article "全球最強推理引擎還快2倍，斯坦福、普林斯頓破解大模型串行魔咒"
@@ -9,33 +10,29 @@
 // 核心机制" and "Saguaro 算法" parts 1-2) describe it; the readings of the
 // missing formulas are stated in include/ssd.h at each call.
 //
-// Structure: a vocabulary call is at most two kernels.
-//   k_stats  one CTA per 32 KiB chunk of one logit row: the HBM pass, which
-//            carries nearly all of the call's bytes.  A TMA bulk copy stages
-//            the chunk in shared memory; the CTA reduces it to a record (max,
-//            sum of 2^(z log2e/T - max), argmax), per-block partial sums for
-//            rows that are drawn from (a block = the 32 vectors one warp reads
-//            in one round) and per-block maximum keys for rows with a top-F
-//            list.  Chunks are numbered sequence-major and, within a sequence,
-//            by row pair r = (target row r, draft row r).  Each CTA takes its
-//            pair's ticket while its copy is in flight: the last CTA of a pair
-//            to start merges the pair once the others are published (row
-//            statistics, the top-F_r list from the block maxima, the Saguaro
-//            draw of d_{r+1}, p(d) and q'(d), the position's verdict), and the
-//            last merger of a sequence to start runs the acceptance chain and,
-//            unless a residual draw is needed, the bonus draw and the outputs.
-//            A merger waits only for CTAs that started before it.  A draw
-//            locates its chunk from the chunk masses and its block from the
-//            block sums; one warp then reads that block's 32 vectors again.
-//            The merges stage the records they read in shared memory (over
-//            the chunk buffer) with one round of loads.
-//   k_resid  (verification at T > 0) one CTA per quarter chunk of each
-//            sequence's rejected row pair: residual block sums; the unit with
-//            the sequence's last ticket draws the bonus token from them and
-//            writes the outputs.  It is a programmatic dependent launch of
-//            k_stats: its CTAs start once every k_stats CTA has started, and
-//            each waits only for its own sequence's ready word, which the pair
-//            merges set as soon as the first rejected position is known.
+// Structure: a vocabulary call is up to three kernels, chained by
+// programmatic dependent launches (each may start while the previous one
+// drains and waits for its completion with griddepcontrol.wait):
+//   k_stats  the HBM pass, which carries nearly all of the call's bytes.  Each
+//            warp reduces one segment of a logit row (256 16-byte vectors,
+//            eight blocks of 32) held in registers: its maximum, the sum of
+//            2^(z log2e/T - fl(max log2e/T)), its argmax where it is used,
+//            and, for rows a draw reads, the eight block sums; for draft rows
+//            with a top-F list, the eight block maximum keys.  No barrier and
+//            no shared memory: a CTA is eight independent warps.
+//   k_pair   one CTA per row pair (target row j, draft row j) of a sequence:
+//            merges the segment records into row statistics, selects the
+//            top-F from the block maxima (re-reading the few candidate blocks,
+//            from L2), draws d_{j+1} from the Saguaro weights (segment, block,
+//            then one block read again), takes p(d), q'(d) and the position's
+//            verdict; at position K+1 it draws the bonus for full acceptance.
+//   k_resid  (verification at T > 0) units of 32 KiB per row: the sequence's
+//            first rejected pair read again (from L2) for the block sums of
+//            max(0, p - q'); the unit with the sequence's last ticket draws the
+//            bonus from them and writes the outputs and the cache lookup.  A
+//            sequence that needs no residual is finished by its first unit.
+//            The analytics call runs the units over every pair for the sums of
+//            min(p, q') and max(0, p - q').
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
@@ -51,92 +48,88 @@
 namespace ssd {
 
 constexpr int kThreads = 256;
-constexpr int kStatsCtas = 5;  // resident k_stats CTAs per SM
 constexpr int kWarps = kThreads / 32;
-constexpr int kRounds = 8;                             // 16-byte vectors per thread and chunk
-constexpr int kChunkBytes = kThreads * kRounds * 16;  // 32 KiB
-constexpr int kBlocks = kRounds * kWarps;              // blocks per chunk (round j, warp w)
-constexpr int kQuarters = 4;                           // k_resid units per chunk (2 rounds each)
-constexpr int kCandCap = 512;
+constexpr int kSegVec = 256;                   // 16-byte vectors per segment (one warp)
+constexpr int kSegBlocks = 8;                  // blocks of 32 vectors per segment
+constexpr int kUnitSeg = kWarps;               // segments per k_stats CTA and per residual unit
+constexpr int kMaxSeg = 1024;                  // rows of at most 4 MiB
+constexpr int kMaxUnits = kMaxSeg / kUnitSeg;  // 128
 constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
-constexpr int kMaxChunks = 128;  // per row: 4 chunk records per lane in the warp merge
+constexpr int kCandCap = 512;
 constexpr int kNone = 0x7fffffff;
+constexpr int kTgt = 0, kDft = 1;
 // A draw whose target lies within kNearTie * W of an edge of the chosen
 // element's bin, and an acceptance test with |u - p/q'| < kNearTie, is a
 // near-tie: fp32 and exact arithmetic may decide it differently.  Such
 // events are counted (the optional near_ties output).
 constexpr float kNearTie = 1e-6f;
 
-struct __align__(16) ChunkStat {
-  float m;   // chunk maximum
-  float s;   // sum over the chunk of 2^(z kT - fl(m kT)) (0 when greedy)
-  int amax;  // lowest index holding m
-  int pad;
+// flag bits of a position's record
+constexpr uint32_t kRecAccepted = 1u;   // the acceptance test passed
+constexpr uint32_t kRecDrawNear = 2u;   // the draw of d was a near-tie
+constexpr uint32_t kRecBonusNear = 4u;  // the bonus draw after full acceptance was a near-tie
+constexpr uint32_t kRecZero = 8u;       // greedy: the residual has no mass
+
+struct __align__(16) SegRec {
+  float m;  // segment maximum
+  float s;  // sum over the segment of 2^(z kT - fl(m kT)) (0 when greedy)
+  int a;    // lowest index holding m (argmax rows), else the segment's first index
+  float t;  // rows a draw reads: the total of the eight block sums by warp_runs' arithmetic
 };
-// Per chunk of a row that is drawn from: each warp's maximum and, per block
-// (round j, warp w), the sum of 2^(z kT - fl(wm[w] kT)) over the block's
-// elements (0 when greedy or for a warp without finite elements).
-struct __align__(16) BlockRec {
-  float wm[kWarps];
-  float bs[kRounds][kWarps];
+// What k_pair leaves for k_resid about position j+1 (row pair j).
+struct __align__(16) PairRec {
+  int d;          // draft token d_{j+1}
+  float p, q;     // p_j(d), q'_j(d) (p < 0: d outside [0, V))
+  uint32_t fl;    // kRec* bits
+  int bt;         // bonus after full acceptance (position K+1); greedy: the bonus at every position
+  float W;        // greedy: the residual's mass; analytics: W_j
+  float N;        // Saguaro normaliser 1 - (1 - C) sum_S q
+  float hp;       // analytics: the guesses' target probability
+  uint64_t keyF;  // the smallest key of S (0: S empty)
+  float hr;       // analytics: the guesses' residual probability
+  float al;       // analytics: alpha_j
+  float gm[2];    // target / draft row maximum
+  float gs[2];    // target / draft sum of 2^(z kT - fl(gm kT))
 };
+static_assert(sizeof(PairRec) == 64, "records are copied as four 16-byte pieces");
 struct RowSlot {
-  int16_t tensor;  // 0 = target, 1 = draft
+  int16_t tensor;  // 0 target, 1 draft
   int16_t row;
-  int16_t F;       // top-F candidates wanted (0 = none)
-  int16_t blocks;  // block sums wanted (the row is drawn from)
-};
-struct __align__(16) RowInfo {  // merged statistics of row r of a sequence
-  float mt, st;   // target max, sum relative to fl(mt kT)
-  int at, pad0;   // target argmax
-  float md, sd;   // draft max, sum
-  int ad;         // draft argmax
-  float sq;       // sum of q over S (normalised)
-};
-struct __align__(16) PosInfo {  // draft token d_j and its probabilities
-  int d;
-  float p, q;  // p_j(d), q'_j(d); p < 0 marks an invalid token
-  int pad;
+  uint8_t keys;    // block maximum keys (draft rows with a top-F list)
+  uint8_t blocks;  // block sums (rows a draw reads)
+  uint8_t arg;     // argmax tracked (greedy rows and top-1 lists)
+  uint8_t pad;
 };
 
 struct VocabArgs {
   const void *target, *draft;
   int64_t seq_stride, row_stride;  // elements
   int B, K, V;
-  int nslots, nchunks, chunk_elems, Fcap;
+  int nvec, nfull;  // 16-byte vectors per row (the last may be partial), whole ones
+  int nseg, nblk, nunits;
+  int nslots, npairs;
+  int b0;  // k_stats: first sequence of this launch (grid z = sequence - b0)
   float kT;    // log2(e) / T
   int greedy;  // T == 0
   float C;
-  int npairs;  // row pairs per sequence, r = 0 .. npairs-1
-  long nst;    // chunks of the call: B * nslots * nchunks
-  int b0;      // k_stats: the first sequence of this launch (grid z = sequence - b0)
   int do_sample, do_verify, do_predict, do_lookup, do_analytics;
-  RowSlot slot[kMaxSlots];                   // ordered by pair: target r, then draft r
-  int tsl[kMaxK + 1], dsl[kMaxK + 1];        // slot of target / draft row r (-1: none)
-  int pair_chunks[kMaxK + 1];                // chunks of pair r (both rows)
-  int F[kMaxK + 1];                          // fan-out F_r
-  int Fs[kMaxK + 1];                         // top-F list kept for draft row r (F_r or 0)
+  RowSlot slot[kMaxSlots];
+  int tsl[kMaxK + 1], dsl[kMaxK + 1];  // slot of target / draft row j (-1: not read)
+  int F[kMaxK + 1];                    // fan-out F_j
+  int Fs[kMaxK + 1];                   // top-F list built for draft row j (F_j or 0)
   int foff[kMaxK + 2];
   // workspace
-  uint32_t *ctr;  // [0] finished sequences, [1] hits; per sequence b: [2+b] pair-merge
-                  // tickets, [2+B+b] merged pairs published, [2+2B+b] residual unit
-                  // tickets, [2+3B+b] ready word (accept count + 2 once known),
-                  // [2+4B+b] residual units published; per pair (b, r):
-                  // [2+5B + b(K+1)+r] chunk tickets, [2+5B+B(K+1) + b(K+1)+r]
-                  // chunks published, [2+5B+2B(K+1) + b(K+1)+r] position verdict
-  ChunkStat *stats;  // [B][nslots][nchunks]
-  BlockRec *blk;     // [B][nslots][nchunks]
-  uint32_t *bmk;     // [B][nslots][nchunks][kBlocks] block maximum keys of top-F rows (0: empty block)
-  RowInfo *rows;     // [B][K+1]
-  uint64_t *S;       // [B][K+1][Fcap] merged top-F lists
-  PosInfo *pos;      // [B][K]
-  float *rmass;      // [B][nchunks * kQuarters] residual mass per unit
-  float *rbs;        // [B][nchunks][kBlocks] residual block sums
-  float *amass;      // analytics: [B][K][nchunks * kQuarters][2] unit sums of min(p, q'), max(0, p - q')
-  // analytics outputs
-  float *an_alpha, *an_resid_w, *an_p_accept, *an_hit_mass, *an_hit_rate, *an_exp_tokens;
+  uint32_t *ctr;   // [0] sequences finished, [1] hits, [2 + b] sequence tickets, [2 + B + b K + j] analytics pair tickets
+  SegRec *seg;     // [B][nslots][nseg]
+  float *bsum;     // [B][nslots][nblk]
+  uint32_t *bkey;  // [B][nslots][nblk]
+  PairRec *rec;    // [B][K+1]
+  float2 *umass;   // residual units: [B][nunits] masses of max(0, p - q') and of p
+  float2 *ublk;    // residual block sums: [B][nblk]
+  float2 *useg;    // residual segment masses: [B][nseg]
+  float2 *amass;   // analytics units: [B][K][nunits] sums of min(p, q') and max(0, p - q')
   // inputs / outputs
   const float *u_draft, *u_acc, *u_bonus;
   const int32_t *d_in;
@@ -149,191 +142,95 @@ struct VocabArgs {
   float *guess_q;
   int32_t *slot_out, *next_tokens;
   uint32_t *hits;
-  uint32_t *near_ties;  // optional: near-tie draws and tests, added to
+  uint32_t *near_ties;
+  float *an_alpha, *an_resid_w, *an_p_accept, *an_hit_mass, *an_hit_rate, *an_exp_tokens;
   uint32_t *status;
-  unsigned long long *trace;  // optional: 8 words per CTA (see ssd_set_trace)
+  unsigned long long *trace;     // optional: 8 words per CTA (see ssd_set_trace)
+  long trace_pair, trace_resid;  // first trace entry of k_pair's and of k_resid's CTAs
 };
 
-SSD_DEV uint32_t *seq_tkt(const VocabArgs &a, int b) { return a.ctr + 2 + b; }
-SSD_DEV uint32_t *seq_pub(const VocabArgs &a, int b) { return a.ctr + 2 + a.B + b; }
-SSD_DEV uint32_t *res_tkt(const VocabArgs &a, int b) { return a.ctr + 2 + 2 * a.B + b; }
-SSD_DEV uint32_t *ready_word(const VocabArgs &a, int b) { return a.ctr + 2 + 3 * a.B + b; }
-SSD_DEV uint32_t *res_pub(const VocabArgs &a, int b) { return a.ctr + 2 + 4 * a.B + b; }
-SSD_DEV uint32_t *pair_tkt(const VocabArgs &a, int b, int r) {
-  return a.ctr + 2 + 5 * static_cast<size_t>(a.B) + static_cast<size_t>(b) * (a.K + 1) + r;
-}
-SSD_DEV uint32_t *pair_pub(const VocabArgs &a, int b, int r) {
-  return pair_tkt(a, b, r) + static_cast<size_t>(a.B) * (a.K + 1);
-}
-// Verification of position r of sequence b, once its pair is merged: 1
-// accepted, 2 rejected (0: not yet known).
-SSD_DEV uint32_t *pos_verdict(const VocabArgs &a, int b, int r) {
-  return pair_tkt(a, b, r) + 2 * static_cast<size_t>(a.B) * (a.K + 1);
-}
-__host__ __device__ inline size_t ctr_words(size_t B, int K) { return 2 + 5 * B + 3 * B * (K + 1); }
-
-__host__ __device__ inline size_t chunk_index(const VocabArgs &a, int b, int slot, int c) {
-  return (static_cast<size_t>(b) * a.nslots + slot) * a.nchunks + c;
-}
 SSD_DEV const char *row_ptr(const VocabArgs &a, int tensor, int b, int row, int esize) {
   const char *base = reinterpret_cast<const char *>(tensor ? a.draft : a.target);
   return base + (static_cast<int64_t>(b) * a.seq_stride + static_cast<int64_t>(row) * a.row_stride) * esize;
 }
+SSD_DEV size_t slot_index(const VocabArgs &a, int b, int slot) { return static_cast<size_t>(b) * a.nslots + slot; }
+
+// Trace marks (ssd_set_trace): %globaltimer.
+SSD_DEV unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+SSD_DEV void trace_entry(const VocabArgs &a, long idx, int kind, int b, int j, const unsigned long long *mk) {
+  if (!a.trace || threadIdx.x != 0) return;
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  unsigned long long *tr = a.trace + 8 * idx;
+  tr[0] = (static_cast<unsigned long long>(smid) << 48) | (static_cast<unsigned long long>(kind) << 40) |
+          (static_cast<unsigned long long>(b & 0xFFFFF) << 20) | static_cast<unsigned long long>(j & 0xFFFFF);
+#pragma unroll
+  for (int k = 1; k < 8; ++k) tr[k] = mk[k];
+}
 
 // ---------------------------------------------------------------------------
-// loads of records other CTAs published (L2, never a stale L1 line)
+// vectors, weights and fixed-order sums
 // ---------------------------------------------------------------------------
-SSD_DEV ChunkStat ldcg_stat(const ChunkStat *p) {
-  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
-  return ChunkStat{__int_as_float(v.x), __int_as_float(v.y), v.z, v.w};
+template <class E>
+SSD_DEV uint4 neg_inf_vec() {
+  const uint32_t w = (E::kSize == 2) ? 0xFF80FF80u : 0xFF800000u;
+  return make_uint4(w, w, w, w);
 }
-SSD_DEV RowInfo ldcg_row(const RowInfo *p) {
-  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
-  const int4 w = __ldcg(reinterpret_cast<const int4 *>(p) + 1);
-  return RowInfo{__int_as_float(v.x), __int_as_float(v.y), v.z,    v.w,
-                 __int_as_float(w.x), __int_as_float(w.y), w.z, __int_as_float(w.w)};
-}
-SSD_DEV PosInfo ldcg_pos(const PosInfo *p) {
-  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
-  return PosInfo{v.x, __int_as_float(v.y), __int_as_float(v.z), v.w};
-}
-SSD_DEV uint64_t ldcg_key(const uint64_t *p) { return __ldcg(reinterpret_cast<const unsigned long long *>(p)); }
-
-// Arrivals and polls are release / relaxed; only the CTA that goes on to read
-// what others published pays for the acquire (a fence), since an acquire
-// invalidates the SM's L1, where the other resident CTAs keep their spills.
-SSD_DEV uint32_t ld_relaxed(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// One 16-byte vector of a row that is streamed once (no L1 allocation).
+SSD_DEV uint4 ld_stream(const char *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
-SSD_DEV void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-SSD_DEV uint32_t atom_add_release(uint32_t *p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-SSD_DEV void red_add_release(uint32_t *p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-SSD_DEV void st_release(uint32_t *p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Trace mark k of this CTA (ssd_set_trace): %globaltimer by thread 0.
-SSD_DEV void mark(const VocabArgs &a, unsigned long long *mk, int k) {
-  if (a.trace && threadIdx.x == 0) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    mk[k] = t;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// shared memory of a CTA (k_stats: after the staged chunk)
-// ---------------------------------------------------------------------------
-struct Smem {
-  uint64_t bar;  // k_stats: completion of the chunk's TMA copy
-  int flag, ncand;
-  alignas(16) uint32_t hist[2][256];  // top-F threshold: block maxima counted by key byte (read as 16-byte vectors)
-  float wm[kWarps], ws[kWarps];
-  int wa[kWarps];
-  uint64_t redk[kWarps];
-  float scal[8];
-  int ival[8];
-  RowInfo ri;
-  uint64_t cand[kCandCap];  // pair merge: candidate block list; sequence finish: the lookup's lists
-  float cmass[kMaxChunks];
-  float bw[kBlocks];
-  uint64_t S[kMaxF];
-  PosInfo pos[kMaxK];  // draft tokens, p(d), q'(d)
-  float cu[kMaxK];     // acceptance uniforms
-  RowInfo rows[kMaxK + 1];
-  uint64_t keyF[kMaxK + 1];
-  unsigned long long mk[7];  // trace marks (thread 0)
-  int near;                  // thread 0: the last draw was a near-tie (its target within 1e-6 W of a bin edge)
-};
-
-// What a merge reads of other CTAs' records, staged in shared memory by one
-// round of loads (k_stats: laid over the chunk buffer once the chunk's own
-// statistics are published).
-constexpr int kStageChunks = 32;  // block records and block maxima staged up to this many chunks per row
-constexpr int kPayStage = 1024;   // payload words staged
-constexpr int kKeyCap = 512;      // top-F candidate keys of a row merge
-struct Stage {
-  ChunkStat cs[2][kMaxChunks];         // chunk records: target row, draft row
-  BlockRec blk[kStageChunks];          // block records of the row drawn from
-  uint32_t bmk[kStageChunks * kBlocks];  // block maximum keys of the draft row (top-F)
-  float z[2][32 * 8];                  // target / draft row values of the block a draw located
-  int32_t pay[kPayStage];              // the sequence's cache payload
-  uint64_t ck[kKeyCap];                // top-F candidate keys
-};
-static_assert(sizeof(Stage) <= kChunkBytes, "the merge stage must fit the chunk buffer");
-static_assert(offsetof(Smem, hist) % 16 == 0 && offsetof(Stage, bmk) % 16 == 0 && offsetof(Stage, blk) % 16 == 0,
-              "shared arrays read or copied in 16-byte pieces");
-static_assert(sizeof(ChunkStat) == 16 && sizeof(BlockRec) % 16 == 0 && sizeof(RowInfo) == 32 && sizeof(PosInfo) == 16,
-              "records are copied in 16-byte pieces");
-
-// Thread 0: bounded wait (sleeping between polls) until *ctr reaches `target`,
-// then an acquire; false when the wait ran out.  Used only for counts that
-// CTAs which started earlier raise, so the wait ends unless they failed.
-SSD_DEV bool wait_count(const uint32_t *ctr, uint32_t target) {
-  for (uint32_t it = 0; it < kMaxPolls; ++it) {
-    if (ld_relaxed(ctr) >= target) {
-      fence_acq_rel();
-      return true;
-    }
-    __nanosleep(200);
-  }
-  return false;
-}
-
-// ===========================================================================
-// element access and weights
-// ===========================================================================
-// The 16-byte vector at chunk-local element i0 of a row chunk starting at e0
-// with n elements, from global memory; elements at or past n read as `fill`.
+// Vector v of a row: a whole vector by one load, the partial last vector by
+// element loads (-inf past V), vectors past the row as -inf.
 template <class E>
-SSD_DEV void ld_vec(const char *row, int e0, int n, int i0, float fill, float *f) {
-  if (i0 + E::kVec <= n) {
-    E::unpack(__ldg(reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(e0 + i0) * E::kSize)), f);
+SSD_DEV uint4 row_vec(const VocabArgs &a, const char *row, int v) {
+  if (v < a.nfull) return __ldg(reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v) * 16));
+  if (v >= a.nvec) return neg_inf_vec<E>();
+  float f[E::kVec];
+  const int i0 = v * E::kVec;
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) f[e] = (i0 + e < a.V) ? E::ld(row, i0 + e) : -__int_as_float(0x7f800000);
+  uint32_t w[4];
+  if constexpr (E::kSize == 2) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = (__float_as_uint(f[2 * q]) >> 16) | (__float_as_uint(f[2 * q + 1]) & 0xFFFF0000u);
   } else {
 #pragma unroll
-    for (int e = 0; e < E::kVec; ++e) f[e] = (i0 + e < n) ? E::ld(row, e0 + i0 + e) : fill;
+    for (int q = 0; q < 4; ++q) w[q] = __float_as_uint(f[q]);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <class E>
+SSD_DEV float vec_max(const uint4 &w) {
+  if constexpr (E::kSize == 2) {
+    const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+    return fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
+  } else {
+    return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
   }
 }
-
-// Weight functors: operator()(zt, zd, idx) -> weight >= 0 with a fixed sequence
-// of correctly rounded operations, so every pass over the same elements agrees.
-struct WSaguaro {  // unnormalised q'_i
-  float mdk, kT, C;
-  uint64_t keyF;
-  bool hasS;
-  SSD_DEV float operator()(float, float zd, int idx) const {
-    const float e = ex2(__fmaf_rn(zd, kT, -mdk));
-    return (hasS && cand_key(zd, idx) >= keyF) ? __fmul_rn(e, C) : e;
-  }
-};
-struct WTarget {  // unnormalised p_i
-  float mtk, kT;
-  SSD_DEV float operator()(float zt, float, int) const { return ex2(__fmaf_rn(zt, kT, -mtk)); }
-};
-struct WResidual {  // max(0, p_i - q'_i)
-  float mtk, kT, inv_st, mdk, fC, f1;
-  uint64_t keyF;
-  bool hasS;
-  SSD_DEV float operator()(float zt, float zd, int idx) const {
-    const float p = __fmul_rn(ex2(__fmaf_rn(zt, kT, -mtk)), inv_st);
-    const float f = (hasS && cand_key(zd, idx) >= keyF) ? fC : f1;
-    const float q = __fmul_rn(ex2(__fmaf_rn(zd, kT, -mdk)), f);
-    const float r = __fsub_rn(p, q);
-    return r > 0.f ? r : 0.f;
-  }
-};
-
-// A block is the 32 consecutive vectors (256 j + 32 w + lane) warp w reads in
-// round j.  Within a block the running weight has a fixed order: each lane
-// sums its vector's weights in element order, the lanes are combined by a
-// Hillis-Steele inclusive scan; the block's sum is the scan's last value.
+// The lane sum of a vector's weights, with one fixed association used by
+// every pass and every draw: even and odd elements summed separately in order
+// (a packed add), then the two.
+template <int N>
+SSD_DEV float lane_sum(const float *x) {
+  uint64_t acc = pack2(x[0], x[1]);
+#pragma unroll
+  for (int h = 1; h < N / 2; ++h) acc = add2(acc, pack2(x[2 * h], x[2 * h + 1]));
+  float lo, hi;
+  unpack2(acc, lo, hi);
+  return __fadd_rn(lo, hi);
+}
+// A block's running weight: lane sums combined by a Hillis-Steele inclusive
+// scan over the warp.
 SSD_DEV float warp_incl_scan(float x) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -343,74 +240,29 @@ SSD_DEV float warp_incl_scan(float x) {
   }
   return x;
 }
-
-// This lane's weights of its vector of block (round j, warp w) of chunk c; the
-// return value is their sum in element order.
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV float lane_weights(const VocabArgs &a, const char *rowT, const char *rowD, int c, int j, int w, const WF &wf,
-                           float *x) {
+// The eight block sums of a warp: pr[k] is this lane's part of block k.
+// Recursive halving (partners 16, 8, 4 lanes apart keep half of the blocks
+// each), then a butterfly over the last four lanes of a block.  Lane l ends
+// with the sum of block l / 4.
+SSD_DEV float warp_block_sums(const float (&pr)[kSegBlocks]) {
   const int lane = threadIdx.x & 31;
-  const int e0 = c * a.chunk_elems;
-  const int n = min(a.chunk_elems, a.V - e0);
-  const int i0 = (j * kThreads + w * 32 + lane) * E::kVec;
-  float ft[E::kVec], fd[E::kVec];
-  if constexpr (HT) ld_vec<E>(rowT, e0, n, i0, 0.f, ft);
-  if constexpr (HD) ld_vec<E>(rowD, e0, n, i0, 0.f, fd);
-  float p = 0.f;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float q4[4], q2[2];
 #pragma unroll
-  for (int e = 0; e < E::kVec; ++e) {
-    x[e] = (i0 + e < n) ? wf(HT ? ft[e] : 0.f, HD ? fd[e] : 0.f, e0 + i0 + e) : 0.f;
-    p = __fadd_rn(p, x[e]);
+  for (int k = 0; k < 4; ++k) {
+    const float keep = b4 ? pr[4 + k] : pr[k], send = b4 ? pr[k] : pr[4 + k];
+    q4[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
   }
-  return p;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float keep = b3 ? q4[2 + k] : q4[k], send = b3 ? q4[k] : q4[2 + k];
+    q2[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  float q = __fadd_rn(b2 ? q2[1] : q2[0], __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 2));
+  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 1));
+  return q;
 }
-
-// One warp: the first element of block (c, j, w) whose running weight exceeds
-// `target` with positive weight; when rounding leaves the target in a lane that
-// has no such element, that lane's last positive element; when no lane holds
-// it, the block's last positive element; -1 for a block without weight.  All
-// 32 lanes call; all return the result.  *dist (every lane) is the distance
-// of the target from the nearer edge of the chosen element's bin in the
-// block's running weight, 0 for the fallbacks (a near-tie by construction).
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, int c, int j, int w, float target,
-                      const WF &wf, float *dist) {
-  const int lane = threadIdx.x & 31;
-  float x[E::kVec];
-  const float p = lane_weights<E, HT, HD>(a, rowT, rowD, c, j, w, wf, x);
-  const float incl = warp_incl_scan(p);
-  float ex = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) ex = 0.f;
-  const int i0 = c * a.chunk_elems + (j * kThreads + w * 32 + lane) * E::kVec;
-  float run = 0.f, edge = 0.f;
-  int hit = -1, lpos = -1;
-#pragma unroll
-  for (int e = 0; e < E::kVec; ++e) {
-    const float before = __fadd_rn(ex, run);
-    run = __fadd_rn(run, x[e]);
-    if (x[e] > 0.f) {
-      lpos = i0 + e;
-      const float after = __fadd_rn(ex, run);
-      if (hit < 0 && after > target) {
-        hit = lpos;
-        edge = fminf(__fsub_rn(target, before), __fsub_rn(after, target));
-      }
-    }
-  }
-  const bool cross = p > 0.f && __fadd_rn(ex, p) > target;
-  const uint32_t mc = __ballot_sync(0xffffffffu, cross);
-  if (mc) {
-    const int src = __ffs(mc) - 1;
-    *dist = __shfl_sync(0xffffffffu, hit >= 0 ? fmaxf(edge, 0.f) : 0.f, src);
-    return __shfl_sync(0xffffffffu, hit >= 0 ? hit : lpos, src);
-  }
-  *dist = 0.f;
-  int best = lpos;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
-  return best;
-}
-
 // Cumulative masses, one warp: lane l sums its run of `per` consecutive
 // masses in order, the runs are combined by a Hillis-Steele inclusive scan.
 // Returns the lane's exclusive prefix; *W = the total (every lane).
@@ -430,13 +282,12 @@ SSD_DEV float warp_total(const float *mass, int n) {
   (void)warp_runs(mass, n, (n + 31) / 32, &W);
   return W;
 }
-
-// One warp: the first of n masses whose cumulative sum (warp_runs) exceeds
-// the target (u * total, or u itself when u_is_target), with positive mass;
-// rounding past the end takes the last positive one.  Lane 0 sets
-// sh.ival[0] = its index (-1 when the total is 0), sh.scal[1] = the target
-// minus the mass before it, sh.scal[2] = the total.  The caller synchronises.
-SSD_DEV void locate(const float *mass, int n, float u, bool u_is_target, Smem &sh) {
+// One warp: the first of n masses whose running sum (warp_runs) exceeds the
+// target (u * total, or u itself when u_is_target) with positive mass; when
+// rounding leaves the target past the end, the last positive mass (*fb set).
+// Returns its index (-1 when the total is 0) and, in every lane, *rem = the
+// target minus the mass before it and *W = the total.
+SSD_DEV int warp_locate(const float *mass, int n, float u, bool u_is_target, float *rem, float *Wout, bool *fb) {
   const int lane = threadIdx.x & 31;
   const int per = (n + 31) / 32;
   float W;
@@ -459,69 +310,380 @@ SSD_DEV void locate(const float *mass, int n, float u, bool u_is_target, Smem &s
   }
   int idx = -1;
   float before = 0.f;
+  bool f = false;
   const uint32_t mh = __ballot_sync(0xffffffffu, hit >= 0);
   if (mh) {
     const int src = __ffs(mh) - 1;
     idx = __shfl_sync(0xffffffffu, hit, src);
     before = __shfl_sync(0xffffffffu, hb, src);
-  } else {  // rounding left the target past the end: the last positive mass
+  } else {
     const uint32_t ml = __ballot_sync(0xffffffffu, lpos >= 0);
     if (ml) {
       const int src = 31 - __clz(ml);
       idx = __shfl_sync(0xffffffffu, lpos, src);
       before = __shfl_sync(0xffffffffu, lb, src);
+      f = true;
     }
   }
-  if (lane == 0) {
-    sh.ival[0] = (W > 0.f) ? idx : -1;
-    sh.scal[1] = __fsub_rn(target, before);
-    sh.scal[2] = W;
+  *rem = __fsub_rn(target, before);
+  *Wout = W;
+  *fb = f;
+  return (W > 0.f) ? idx : -1;
+}
+
+// Membership of element (z, idx) in the top-F set whose smallest key is keyF.
+SSD_DEV bool in_set(float z, int idx, float vF, uint64_t keyF) {
+  return !(z < vF) && cand_key(z, idx) >= keyF;
+}
+SSD_DEV float norm_N(float C, float sq) { return __fsub_rn(1.f, __fmul_rn(__fsub_rn(1.f, C), sq)); }
+
+// Element weights of the draws.  operator()(zt, zd, idx, Mk) -> weight >= 0,
+// with Mk = fl(segment max kT) for the weights of the statistics pass; the
+// passes and the draws compute them with the same operations.
+struct WDraft {  // unnormalised q'_i relative to the segment maximum
+  float kT, C, vF;
+  uint64_t keyF;
+  bool S;
+  SSD_DEV float operator()(float, float zd, int idx, float Mk) const {
+    const float e = ex2(__fmaf_rn(zd, kT, -Mk));
+    return (S && in_set(zd, idx, vF, keyF)) ? __fmul_rn(e, C) : e;
+  }
+};
+struct WTarget {  // unnormalised p_i relative to the segment maximum
+  float kT;
+  SSD_DEV float operator()(float zt, float, int, float Mk) const { return ex2(__fmaf_rn(zt, kT, -Mk)); }
+};
+struct WResid {  // max(0, p_i - q'_i), both normalised
+  float kT, Mtk, inv_st, Mdk, f1, fC, vF;
+  uint64_t keyF;
+  bool S;
+  SSD_DEV float p(float zt) const { return __fmul_rn(ex2(__fmaf_rn(zt, kT, -Mtk)), inv_st); }
+  SSD_DEV float q(float zd, int idx) const {
+    return __fmul_rn(ex2(__fmaf_rn(zd, kT, -Mdk)), (S && in_set(zd, idx, vF, keyF)) ? fC : f1);
+  }
+  SSD_DEV float operator()(float zt, float zd, int idx, float) const {
+    const float r = __fsub_rn(p(zt), q(zd, idx));
+    return r > 0.f ? r : 0.f;
+  }
+};
+struct WProb {  // p_i normalised (the fallback of a residual without mass)
+  float kT, Mtk, inv_st;
+  SSD_DEV float operator()(float zt, float, int, float) const { return __fmul_rn(ex2(__fmaf_rn(zt, kT, -Mtk)), inv_st); }
+};
+// The residual weights of a position from its record.
+SSD_DEV WResid resid_weights(const VocabArgs &a, const PairRec &r, int F) {
+  WResid w;
+  w.kT = a.kT;
+  w.Mtk = __fmul_rn(r.gm[kTgt], a.kT);
+  w.inv_st = __frcp_rn(r.gs[kTgt]);
+  w.Mdk = __fmul_rn(r.gm[kDft], a.kT);
+  const float sN = __fmul_rn(r.gs[kDft], r.N);
+  w.f1 = __frcp_rn(sN);
+  w.fC = __fdiv_rn(a.C, sN);
+  w.S = F > 0;
+  w.keyF = r.keyF;
+  w.vF = cand_val(r.keyF);
+  return w;
+}
+
+// One warp: the element of block g (vectors 32 g .. 32 g + 31) of the rows
+// whose running weight (lane sums by lane_sum, lanes by a scan) first exceeds
+// `target` with positive weight; when rounding leaves the target in a lane
+// without such an element, that lane's last positive element; when no lane
+// holds it, the block's last positive element.  *dist: the target's distance
+// from the nearer edge of the chosen element's bin (0 for the fallbacks).
+template <class E, class WF>
+SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, int g, float target, const WF &wf,
+                      float Mk, float *dist, float *zt_out = nullptr, float *zd_out = nullptr) {
+  const int lane = threadIdx.x & 31;
+  const int v = g * 32 + lane;
+  float zt[E::kVec], zd[E::kVec], x[E::kVec];
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) zt[e] = zd[e] = 0.f;
+  if (rowT) E::unpack(row_vec<E>(a, rowT, v), zt);
+  if (rowD) E::unpack(row_vec<E>(a, rowD, v), zd);
+  const int i0 = v * E::kVec;
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) x[e] = (i0 + e < a.V) ? wf(zt[e], zd[e], i0 + e, Mk) : 0.f;
+  const float L = lane_sum<E::kVec>(x);
+  const float incl = warp_incl_scan(L);
+  float ex = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) ex = 0.f;
+  float run = 0.f, edge = 0.f;
+  int hit = -1, lpos = -1;
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) {
+    const float before = __fadd_rn(ex, run);
+    run = __fadd_rn(run, x[e]);
+    if (x[e] > 0.f) {
+      lpos = i0 + e;
+      const float after = __fadd_rn(ex, run);
+      if (hit < 0 && after > target) {
+        hit = lpos;
+        edge = fminf(__fsub_rn(target, before), __fsub_rn(after, target));
+      }
+    }
+  }
+  const bool cross = L > 0.f && __fadd_rn(ex, L) > target;
+  const uint32_t mc = __ballot_sync(0xffffffffu, cross);
+  int d;
+  if (mc) {
+    const int src = __ffs(mc) - 1;
+    *dist = __shfl_sync(0xffffffffu, hit >= 0 ? fmaxf(edge, 0.f) : 0.f, src);
+    d = __shfl_sync(0xffffffffu, hit >= 0 ? hit : lpos, src);
+  } else {
+    *dist = 0.f;
+    d = lpos;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) d = max(d, __shfl_xor_sync(0xffffffffu, d, o));
+  }
+  if (zt_out || zd_out) {  // the element's two values, from the lane that read it
+    const int owner = (d >= 0) ? d / E::kVec - g * 32 : 0;
+    float vt = 0.f, vd = 0.f;
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e)
+      if (lane == owner && i0 + e == d) {
+        vt = zt[e];
+        vd = zd[e];
+      }
+    vt = __shfl_sync(0xffffffffu, vt, owner & 31);
+    vd = __shfl_sync(0xffffffffu, vd, owner & 31);
+    if (zt_out) *zt_out = vt;
+    if (zd_out) *zd_out = vd;
+  }
+  return d;
+}
+
+// ===========================================================================
+// k_stats: one warp per segment of a row
+// ===========================================================================
+template <class E>
+__global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ VocabArgs a) {
+  // k_pair may start launching once every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const unsigned long long t0 = (a.trace && threadIdx.x == 0) ? now_ns() : 0ull;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sg = static_cast<int>(blockIdx.x) * kWarps + warp;
+  const int slot = static_cast<int>(blockIdx.y);
+  const int b = a.b0 + static_cast<int>(blockIdx.z);
+  const RowSlot rs = a.slot[slot];
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  if (sg < a.nseg) {
+    const char *row = row_ptr(a, rs.tensor, b, rs.row, E::kSize);
+    const int v0 = sg * kSegVec;
+    // every load of the segment in flight at once
+    uint4 w[kSegBlocks];
+#pragma unroll
+    for (int k = 0; k < kSegBlocks; ++k) {
+      const int v = v0 + 32 * k + lane;
+      w[k] = (v < a.nfull) ? ld_stream(row + static_cast<int64_t>(v) * 16) : neg_inf_vec<E>();
+    }
+    if (a.nvec > a.nfull && a.nfull >= v0 && a.nfull < v0 + kSegVec && lane == ((a.nfull - v0) & 31)) {
+      const int kk = (a.nfull - v0) >> 5;  // the row's partial last vector
+      const uint4 t = row_vec<E>(a, row, a.nfull);
+#pragma unroll
+      for (int k = 0; k < kSegBlocks; ++k)
+        if (k == kk) w[k] = t;
+    }
+    // pass 1: maxima (bf16: packed), block maximum keys (lane k < 8 keeps
+    // block k's), the argmax's vector
+    uint32_t bk = 0u;
+    float m1 = NEG_INF;
+    int k1 = -1;
+    if constexpr (E::kSize == 2) {
+      uint32_t mm = 0xFF80FF80u;
+#pragma unroll
+      for (int k = 0; k < kSegBlocks; ++k) {
+        const uint32_t t = bmax2(bmax2(w[k].x, w[k].y), bmax2(w[k].z, w[k].w));
+        mm = bmax2(mm, t);
+        if (rs.keys || rs.arg) {
+          const float vm = fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
+          const bool valid = v0 + 32 * k + lane < a.nvec;
+          if (rs.keys) {
+            const uint32_t key = __reduce_max_sync(0xffffffffu, valid ? f2ord(vm) : 0u);
+            if (lane == k) bk = key;
+          }
+          if (rs.arg && valid && (vm > m1 || k1 < 0)) {  // strictly larger: the first vector among equal maxima
+            m1 = fmaxf(m1, vm);
+            k1 = k;
+          }
+        }
+      }
+      if (!rs.arg) m1 = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
+    } else {
+#pragma unroll
+      for (int k = 0; k < kSegBlocks; ++k) {
+        const float vm = vec_max<E>(w[k]);
+        const bool valid = v0 + 32 * k + lane < a.nvec;
+        if (rs.keys) {
+          const uint32_t key = __reduce_max_sync(0xffffffffu, valid ? f2ord(vm) : 0u);
+          if (lane == k) bk = key;
+        }
+        if (valid && (vm > m1 || k1 < 0)) {
+          m1 = fmaxf(m1, vm);
+          k1 = k;
+        }
+      }
+    }
+    const float wm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(m1)));
+    int wa = v0 * E::kVec;  // the segment's first index unless the argmax is tracked
+    if (rs.arg) {
+      int idx = kNone;
+      if (k1 >= 0 && m1 == wm) {
+        uint4 wk = w[0];
+#pragma unroll
+        for (int k = 1; k < kSegBlocks; ++k)
+          if (k == k1) wk = w[k];
+        float f[E::kVec];
+        E::unpack(wk, f);
+#pragma unroll
+        for (int e = E::kVec - 1; e >= 0; --e)
+          if (f[e] == wm) idx = (v0 + 32 * k1 + lane) * E::kVec + e;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+      wa = (idx == kNone) ? v0 * E::kVec : idx;
+    }
+    // pass 2: sums of 2^(z kT - fl(wm kT)), two elements per packed FMA / ADD;
+    // per block the lane's part in the association of lane_sum
+    float ws = 0.f, bsv = 0.f, wt = 0.f;
+    if (!a.greedy && wm != NEG_INF) {
+      const float Mk = __fmul_rn(wm, a.kT);
+      const uint64_t k2 = pack2(a.kT, a.kT), m2 = pack2(-Mk, -Mk);
+      uint64_t acc = pack2(0.f, 0.f);
+      float pr[kSegBlocks];
+#pragma unroll
+      for (int k = 0; k < kSegBlocks; ++k) {
+        uint64_t accj = 0;
+#pragma unroll
+        for (int h = 0; h < E::kPairs; ++h) {
+          float x0, x1;
+          unpack2(fma2(E::pair(w[k], h), k2, m2), x0, x1);
+          const uint64_t e2 = pack2(ex2(x0), ex2(x1));
+          accj = (h == 0) ? e2 : add2(accj, e2);
+        }
+        acc = add2(acc, accj);
+        float lo, hi;
+        unpack2(accj, lo, hi);
+        pr[k] = __fadd_rn(lo, hi);
+      }
+      if (rs.blocks) {
+        bsv = warp_block_sums(pr);
+        // lane k < 8 takes block k's sum; their total by a scan (warp_runs over 8 masses)
+        const float bk8 = __shfl_sync(0xffffffffu, bsv, (lane & 7) * 4);
+        wt = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? bk8 : 0.f), 31);
+      }
+      float lo, hi;
+      unpack2(acc, lo, hi);
+      ws = warp_sum(__fadd_rn(lo, hi));
+    }
+    const size_t si = slot_index(a, b, slot);
+    if (lane == 0)
+      reinterpret_cast<int4 *>(a.seg)[si * a.nseg + sg] =
+          make_int4(__float_as_int(wm), __float_as_int(ws), wa, __float_as_int(wt));
+    if (rs.keys && lane < kSegBlocks) a.bkey[si * a.nblk + sg * kSegBlocks + lane] = bk;
+    if (rs.blocks && (lane & 3) == 0) a.bsum[si * a.nblk + sg * kSegBlocks + (lane >> 2)] = bsv;
+  }
+  if (a.trace && threadIdx.x == 0) {
+    const unsigned long long mk[8] = {0ull, t0, 0ull, 0ull, 0ull, 0ull, 0ull, now_ns()};
+    trace_entry(a, (static_cast<long>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x, 0, b,
+                static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), mk);
   }
 }
 
 // ===========================================================================
-// k_stats: statistics of one staged chunk
+// k_pair: one CTA per row pair
 // ===========================================================================
-// Thread t owns the chunk's vectors t + 256 j (round j); vector nvec, when the
-// row's last chunk ends inside it, is read from global memory (-inf past the
-// end).
-template <class E>
-struct ChunkView {
-  const uint4 *v4;
-  const char *row;
-  int e0, n, nvec, ntail;
-  SSD_DEV bool has(int v) const { return v < nvec || (v == nvec && ntail > 0); }
-  SSD_DEV void get(int v, float *f) const {
-    if (v < nvec) E::unpack(v4[v], f);
-    else ld_vec<E>(row, e0, n, v * E::kVec, -__int_as_float(0x7f800000), f);
-  }
-  // maximum of vector v (-inf if absent)
-  SSD_DEV float vmax(int v) const {
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    if (v < nvec) {
-      const uint4 w = v4[v];
-      if constexpr (E::kSize == 2) {
-        const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-        return fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
-      } else {
-        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
-      }
-    }
-    float m = NEG_INF;
-    if (has(v)) {
-      float f[E::kVec];
-      get(v, f);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e) m = fmaxf(m, f[e]);
-    }
-    return m;
-  }
+struct __align__(16) PairSh {
+  float gm[2], gs[2];  // row maximum and sum of 2^(z kT - fl(gm kT))
+  int ga[2];           // row argmax
+  float sq;            // the draft's normalised mass on S
+  int ncand, nblist;
+  alignas(16) uint32_t hist[2][256];
+  uint64_t S[kMaxF];
+  uint64_t cand[kCandCap];
+  int blist[2 * kCandCap];
+  uint64_t redk[kWarps];
+  unsigned long long mk[8];
 };
+// Dynamic shared memory after PairSh: the target and draft rows' segment
+// records, the draft's block keys, the drawn row's block masses and its
+// segment masses.
+struct PairBufs {
+  SegRec *segT, *segD;
+  uint32_t *keys;
+  float *bm;   // block masses of the drawn row (segment units)
+  float *smm;  // segment masses (row units); scratch of the row merges
+};
+__host__ __device__ inline size_t pair_smem_bytes(int nseg, int nblk) {
+  return sizeof(PairSh) + 2 * static_cast<size_t>(nseg) * sizeof(SegRec) + 2 * static_cast<size_t>(nblk) * 4 +
+         static_cast<size_t>(nseg) * 4;
+}
+SSD_DEV PairBufs pair_bufs(const VocabArgs &a, uint8_t *base) {
+  PairBufs p;
+  uint8_t *o = base;
+  p.segT = reinterpret_cast<SegRec *>(o);
+  o += static_cast<size_t>(a.nseg) * sizeof(SegRec);
+  p.segD = reinterpret_cast<SegRec *>(o);
+  o += static_cast<size_t>(a.nseg) * sizeof(SegRec);
+  p.keys = reinterpret_cast<uint32_t *>(o);
+  o += static_cast<size_t>(a.nblk) * sizeof(uint32_t);
+  p.bm = reinterpret_cast<float *>(o);
+  o += static_cast<size_t>(a.nblk) * sizeof(float);
+  p.smm = reinterpret_cast<float *>(o);
+  return p;
+}
+
+// One warp over a row's segment records (every lane returns the results):
+// the maximum, the lowest index holding it, and the sum in units of
+// fl(max kT) (each lane its segments in order, then a butterfly).
+SSD_DEV void merge_row(const VocabArgs &a, const SegRec *sr, float &M, float &S, int &A) {
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const int lane = threadIdx.x & 31;
+  float m = NEG_INF;
+  int am = kNone;
+  for (int s = lane; s < a.nseg; s += 32) {
+    const float ms = sr[s].m;
+    if (ms > m) {  // a lane's segments in order: a strictly larger maximum keeps the lowest index
+      m = ms;
+      am = sr[s].a;
+    }
+  }
+  M = ord2f(__reduce_max_sync(0xffffffffu, f2ord(m)));
+  const unsigned ai = __reduce_min_sync(0xffffffffu, (m == M) ? static_cast<unsigned>(am) : static_cast<unsigned>(kNone));
+  A = (ai == static_cast<unsigned>(kNone)) ? 0 : static_cast<int>(ai);
+  float sum = 0.f;
+  if (!a.greedy && M != NEG_INF) {
+    const float Mk = __fmul_rn(M, a.kT);
+    for (int s = lane; s < a.nseg; s += 32) {
+      const SegRec r = sr[s];
+      if (r.m != NEG_INF) sum = __fadd_rn(sum, __fmul_rn(r.s, ex2(__fsub_rn(__fmul_rn(r.m, a.kT), Mk))));
+    }
+    sum = warp_sum(sum);
+  }
+  S = sum;
+}
+
+// The elements (key prefix >= t16) of candidate block g of a draft row.
+template <class E>
+SSD_DEV void block_candidates(const VocabArgs &a, const char *row, int g, uint32_t t16, PairSh &sh) {
+  const int lane = threadIdx.x & 31;
+  const int v = g * 32 + lane;
+  if (v >= a.nvec) return;
+  float f[E::kVec];
+  E::unpack(row_vec<E>(a, row, v), f);
+#pragma unroll
+  for (int e = 0; e < E::kVec; ++e) {
+    const int idx = v * E::kVec + e;
+    if (idx < a.V && (f2ord(f[e]) >> 16) >= t16) {
+      const int p = atomicAdd(&sh.ncand, 1);
+      if (p < kCandCap) sh.cand[p] = cand_key(f[e], idx);
+    }
+  }
+}
 
 // Top-F of n distinct nonzero keys by rank (the key with r larger keys goes
-// to dst[r] when r < F); slots past n are set to 0.  No barrier inside.  Up to
-// 64 keys: warp w ranks keys w, w + 8, ..., its lanes comparing keys l and
-// l + 32 against it (two ballots); beyond, a thread per key.
+// to dst[r] when r < F); slots past n are set to 0.  No barrier inside.
 SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
   for (int i = threadIdx.x; i < F; i += kThreads)
     if (i >= n) dst[i] = 0ull;
@@ -541,32 +703,6 @@ SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
     for (int j = 0; j < n && rank < F; ++j) rank += (keys[j] > k) ? 1 : 0;
     if (rank < F) dst[rank] = k;
   }
-}
-
-// The 8 block sums of a warp (kRounds = 8): pr[j] is this lane's part of
-// round j's block.  Recursive halving: at each step a lane keeps half of its
-// rounds and adds its partner's part of them (partners 16, 8, 4 lanes apart),
-// then the last four lanes of a round are summed by a butterfly.  Lane l ends
-// with the sum of round l / 4.
-SSD_DEV float warp_round_sums(const float (&pr)[kRounds]) {
-  static_assert(kRounds == 8, "three halving steps");
-  const int lane = threadIdx.x & 31;
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-  float q4[4], q2[2];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float keep = b4 ? pr[4 + k] : pr[k], send = b4 ? pr[k] : pr[4 + k];
-    q4[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float keep = b3 ? q4[2 + k] : q4[k], send = b3 ? q4[k] : q4[2 + k];
-    q2[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-  float q = __fadd_rn(b2 ? q2[1] : q2[0], __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4));
-  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 2));
-  q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, 1));
-  return q;
 }
 
 // One warp (every lane returns the result): over 256 bucket counts, the
@@ -620,500 +756,30 @@ SSD_DEV void find_bucket(const uint32_t *hist, int need, uint32_t &bucket_out, i
   above_out = static_cast<int>(above);
 }
 
-// The 8 block maximum keys of a warp: vk[j] is this lane's vector key of
-// round j (0: none).  The exchange pattern of warp_round_sums with max; lane
-// l ends with the maximum of round l / 4.
-SSD_DEV uint32_t warp_round_umax(const uint32_t (&vk)[kRounds]) {
-  const int lane = threadIdx.x & 31;
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-  uint32_t q4[4], q2[2];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t keep = b4 ? vk[4 + k] : vk[k], send = b4 ? vk[k] : vk[4 + k];
-    q4[k] = max(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const uint32_t keep = b3 ? q4[2 + k] : q4[k], send = b3 ? q4[k] : q4[2 + k];
-    q2[k] = max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-  uint32_t q = max(b2 ? q2[1] : q2[0], __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4));
-  q = max(q, __shfl_xor_sync(0xffffffffu, q, 2));
-  q = max(q, __shfl_xor_sync(0xffffffffu, q, 1));
-  return q;
-}
-
-// The chunk's record, block sums and (top-F rows) block maximum keys.
-template <class E>
-SSD_DEV void stats_chunk(const VocabArgs &a, int b, int slot, int c, const uint8_t *buf, Smem &sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const RowSlot rs = a.slot[slot];
-  const float kT = a.kT;
-  const bool greedy = a.greedy != 0;
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  ChunkView<E> cv;
-  cv.v4 = reinterpret_cast<const uint4 *>(buf);
-  cv.row = row_ptr(a, rs.tensor, b, rs.row, E::kSize);
-  cv.e0 = c * a.chunk_elems;
-  cv.n = min(a.chunk_elems, a.V - cv.e0);
-  cv.nvec = (cv.n * E::kSize) >> 4;
-  cv.ntail = cv.n - cv.nvec * E::kVec;
-  const bool tail_mine = cv.ntail > 0 && tid == (cv.nvec & (kThreads - 1));  // the partial vector
-
-  // the chunk's argmax is kept where it is used: greedy rows and rows whose
-  // top-1 list is the argmax (F = 1).  Elsewhere the record's index is the
-  // chunk's first element, which is the argmax in the one case a T > 0 draw
-  // can fall back to it (a row without finite logits: every chunk max -inf).
-  const bool need_arg = greedy || rs.F == 1;
-  // rows with a top-F list (F > 1) publish the maximum key of each block
-  // (round, warp); the pair merge selects the row's top-F from them
-  const bool topf = rs.F > 1;
-  uint32_t vk[kRounds];  // topf rows: this lane's vector key of each round (0: no vector)
-  float m1 = NEG_INF;
-  int wi = kNone;
-  if (need_arg) {
-    // pass 1: the thread's maximum and the first of its vectors holding it
-    int j1 = -1;
-#pragma unroll
-    for (int j = 0; j < kRounds; ++j) {
-      const int v = tid + j * kThreads;
-      vk[j] = 0u;
-      if (cv.has(v)) {
-        const float vm = cv.vmax(v);
-        if (topf) vk[j] = f2ord(vm);
-        if (vm > m1 || j1 < 0) {  // strictly larger: the first vector among equal maxima
-          m1 = fmaxf(m1, vm);
-          j1 = j;
-        }
-      }
-    }
-    const float wm1 = warp_max(m1);
-    // the lane holding the warp maximum: its first element there
-    int i1 = kNone;
-    if (m1 == wm1 && j1 >= 0) {
-      const int v = tid + j1 * kThreads;
-      float f[E::kVec];
-      cv.get(v, f);
-#pragma unroll
-      for (int e = E::kVec - 1; e >= 0; --e)
-        if (f[e] == wm1 && v * E::kVec + e < cv.n) i1 = v * E::kVec + e;
-    }
-    wi = i1;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) wi = min(wi, __shfl_xor_sync(0xffffffffu, wi, o));
-  } else {
-    // pass 1: the thread's maximum (bf16 rows: packed maxima of all vectors)
-    if constexpr (E::kSize == 2) {
-      uint32_t mm = 0xFF80FF80u;  // (-inf, -inf)
-#pragma unroll
-      for (int j = 0; j < kRounds; ++j) {
-        const int v = tid + j * kThreads;
-        vk[j] = 0u;
-        if (v < cv.nvec) {
-          const uint4 w = cv.v4[v];
-          const uint32_t t = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-          mm = bmax2(mm, t);
-          if (topf) vk[j] = f2ord(fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u)));
-        }
-      }
-      m1 = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
-    } else {
-#pragma unroll
-      for (int j = 0; j < kRounds; ++j) {
-        const int v = tid + j * kThreads;
-        vk[j] = 0u;
-        if (v < cv.nvec) {
-          const float vm = cv.vmax(v);
-          m1 = fmaxf(m1, vm);
-          if (topf) vk[j] = f2ord(vm);
-        }
-      }
-    }
-    if (tail_mine) {
-      const float vm = cv.vmax(cv.nvec);
-      m1 = fmaxf(m1, vm);
-      if (topf) {
-#pragma unroll
-        for (int j = 0; j < kRounds; ++j)
-          if (j == cv.nvec / kThreads) vk[j] = f2ord(vm);
-      }
-    }
-  }
-  if (topf) {
-    const uint32_t key = warp_round_umax(vk);
-    if ((lane & 3) == 0) a.bmk[chunk_index(a, b, slot, c) * kBlocks + (lane >> 2) * kWarps + warp] = key;
-  }
-  const float wm = warp_max(m1);
-  // pass 2: the warp's sum of 2^(z kT - fl(wm kT)), two elements per packed
-  // FMA / ADD; per round the lane's four pairs first, then into the lane's
-  // total (the same arithmetic whether or not block sums are kept).  Rows
-  // that are drawn from also keep their block sums.
-  float s = 0.f;
-  BlockRec *br = a.blk + chunk_index(a, b, slot, c);
-  if (!greedy && wm != NEG_INF) {
-    const float Mk = __fmul_rn(wm, kT);
-    const uint64_t k2 = pack2(kT, kT), nm2 = pack2(-Mk, -Mk);
-    float tail = 0.f;  // the partial vector's sum, element order
-    if (tail_mine) {
-      float f[E::kVec];
-      cv.get(cv.nvec, f);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e) tail = __fadd_rn(tail, ex2(__fmaf_rn(f[e], kT, -Mk)));
-    }
-    uint64_t acc = pack2(0.f, 0.f);
-    float pr[kRounds];  // block rows: the lane's sum of each round
-#pragma unroll
-    for (int j = 0; j < kRounds; ++j) {
-      const int v = tid + j * kThreads;
-      pr[j] = 0.f;
-      if (v < cv.nvec) {
-        const uint4 w = cv.v4[v];
-        uint64_t accj = 0;
-#pragma unroll
-        for (int h = 0; h < E::kPairs; ++h) {
-          float x0, x1;
-          unpack2(fma2(E::pair(w, h), k2, nm2), x0, x1);
-          const uint64_t e2 = pack2(ex2(x0), ex2(x1));
-          accj = (h == 0) ? e2 : add2(accj, e2);
-        }
-        acc = add2(acc, accj);
-        if (rs.blocks) {
-          float lo, hi;
-          unpack2(accj, lo, hi);
-          pr[j] = __fadd_rn(lo, hi);
-        }
-      } else if (tail_mine && v == cv.nvec) {
-        pr[j] = tail;
-      }
-    }
-    if (rs.blocks) {
-      const float bsum = warp_round_sums(pr);
-      if ((lane & 3) == 0) br->bs[lane >> 2][warp] = bsum;
-    }
-    float lo, hi;
-    unpack2(acc, lo, hi);
-    s = __fadd_rn(__fadd_rn(lo, hi), tail);
-    s = warp_sum(s);
-  } else if (rs.blocks && lane < kRounds) {
-    br->bs[lane][warp] = 0.f;  // every block record of a drawn row is written
-  }
-  if (lane == 0) {
-    if (rs.blocks) br->wm[warp] = wm;
-    sh.wm[warp] = wm;
-    sh.ws[warp] = s;
-    sh.wa[warp] = wi;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // lanes 0..7 hold the warps' records; reduced within groups of 8 lanes
-    const int w = lane & (kWarps - 1);
-    const float wmw = sh.wm[w];
-    float M = wmw;
-#pragma unroll
-    for (int o = kWarps / 2; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    int amax = (wmw == M) ? sh.wa[w] : kNone;
-#pragma unroll
-    for (int o = kWarps / 2; o; o >>= 1) amax = min(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    float S = 0.f;
-    if (!greedy && M != NEG_INF && wmw != NEG_INF)
-      S = __fmul_rn(sh.ws[w], ex2(__fsub_rn(__fmul_rn(wmw, kT), __fmul_rn(M, kT))));
-#pragma unroll
-    for (int o = kWarps / 2; o; o >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
-    if (lane == 0) {
-      if (amax == kNone) amax = 0;  // an all -inf chunk: its first index
-      a.stats[chunk_index(a, b, slot, c)] = ChunkStat{M, S, cv.e0 + amax, 0};
-    }
-  }
-}
-
-// ===========================================================================
-// merges
-// ===========================================================================
-struct RowStat {
-  float m, s;
-  int amax;
-};
-// One warp merges the chunk records of a row (staged in shared memory): the
-// maximum (a strictly larger maximum keeps the lower chunk, hence the lowest
-// index), and the sum rescaled to it (each lane sums its chunks in order, the
-// lanes by a fixed tree).  All 32 lanes call; all return it.
-SSD_DEV RowStat merge_row_warp(const VocabArgs &a, const ChunkStat *rec) {
-  constexpr int L = kMaxChunks / 32;
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  const int lane = threadIdx.x & 31;
-  ChunkStat cs[L];
-#pragma unroll
-  for (int l = 0; l < L; ++l) {
-    const int c = lane + 32 * l;
-    cs[l] = (c < a.nchunks) ? rec[c] : ChunkStat{NEG_INF, 0.f, kNone, 0};
-  }
-  float m = cs[0].m;
-  int am = cs[0].amax;
-#pragma unroll
-  for (int l = 1; l < L; ++l)
-    if (cs[l].m > m) {
-      m = cs[l].m;
-      am = cs[l].amax;
-    }
-  // across lanes: the larger maximum; equal maxima keep the lower index
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
-    if (m2 > m || (m2 == m && a2 < am)) {
-      m = m2;
-      am = a2;
-    }
-  }
-  float sum = 0.f;
-  if (!a.greedy && m != NEG_INF) {
-    const float mk = __fmul_rn(m, a.kT);
-#pragma unroll
-    for (int l = 0; l < L; ++l)
-      if (cs[l].m != NEG_INF) sum = __fadd_rn(sum, __fmul_rn(cs[l].s, ex2(__fsub_rn(__fmul_rn(cs[l].m, a.kT), mk))));
-    sum = warp_sum(sum);
-  }
-  return RowStat{m, sum, am == kNone ? 0 : am};
-}
-
-SSD_DEV float norm_N(float C, float sq) { return __fsub_rn(1.f, __fmul_rn(__fsub_rn(1.f, C), sq)); }
-
-// ===========================================================================
-// draws by the statistics of a row: chunk (chunk masses), block (block sums),
-// then one warp over the block
-// ===========================================================================
-// Chunk masses of 2^(z kT - rk) (rk = fl(row max kT)) from the row's chunk
-// records, into sh.cmass.  Caller synchronises.
-SSD_DEV float chunk_mass(const ChunkStat &cs, float kT, float rk) {
-  return (cs.m == -__int_as_float(0x7f800000)) ? 0.f : __fmul_rn(cs.s, ex2(__fsub_rn(__fmul_rn(cs.m, kT), rk)));
-}
-SSD_DEV void chunk_masses(const VocabArgs &a, int b, int slot, float rk, Smem &sh) {
-  for (int c = threadIdx.x; c < a.nchunks; c += kThreads)
-    sh.cmass[c] = chunk_mass(ldcg_stat(a.stats + chunk_index(a, b, slot, c)), a.kT, rk);
-}
-
-// Draw from row `slot` of sequence b (its elements in `row`) with weights wf =
-// 2^(z kT - rk), scaled by C on the set S (the Fn keys of Slist) when C < 1.
-// sh.cmass holds the chunk masses with the down-weighting applied; `sbr`, when
-// given, the row's block records staged in shared memory (else they are read
-// from global memory).  While warp 0 scans the located block, warp 1 stages
-// its values (zdrawn) and, with `rowZ`, the other row's values there
-// (zother); sh.ival[5] is then the block's first element.  Every thread
-// calls; returns the token (-1 if the masses are all 0).
-template <class E, bool HT, class WF>
-SSD_DEV int stats_draw(const VocabArgs &a, int b, int slot, const char *row, float rk, float u, const WF &wf,
-                       const BlockRec *sbr, const uint64_t *Slist, int Fn, float C, float *zdrawn, const char *rowZ,
-                       float *zother, Smem &sh) {
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (tid == 0) sh.near = 0;
-  if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
-  __syncthreads();
-  const int cs = sh.ival[0];
-  const float local = sh.scal[1];
-  const float Wrow = sh.scal[2];  // the row's total weight
-  if (cs < 0) return -1;
-  // block weights of chunk cs; the elements of S in a block down-weighted in
-  // list order
-  if (tid < kBlocks) {
-    const int j = tid / kWarps, w = tid % kWarps;
-    float wmw, bs;
-    if (sbr) {
-      wmw = sbr[cs].wm[w];
-      bs = sbr[cs].bs[j][w];
-    } else {
-      const BlockRec *br = a.blk + chunk_index(a, b, slot, cs);
-      wmw = __ldcg(&br->wm[w]);
-      bs = __ldcg(&br->bs[j][w]);
-    }
-    float x = (wmw == -__int_as_float(0x7f800000) || !(bs > 0.f))
-                  ? 0.f
-                  : __fmul_rn(bs, ex2(__fsub_rn(__fmul_rn(wmw, a.kT), rk)));
-    if (C < 1.f) {
-      const int e0 = cs * a.chunk_elems;
-      for (int i = 0; i < Fn; ++i) {
-        const uint64_t k = Slist[i];
-        if (!k) continue;
-        const int idx = cand_idx(k) - e0;
-        if (idx < 0 || idx >= a.chunk_elems) continue;
-        const int v = idx / E::kVec;
-        if ((v / kThreads) * kWarps + (v % kThreads) / 32 != tid) continue;
-        const float e = ex2(__fmaf_rn(cand_val(k), a.kT, -rk));
-        x = fmaxf(__fsub_rn(x, __fmul_rn(__fsub_rn(1.f, C), e)), 0.f);
-      }
-    }
-    sh.bw[tid] = x;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    locate(sh.bw, kBlocks, local, true, sh);
-    __syncwarp();
-    if (tid == 0 && sh.ival[0] < 0) {  // no block weight (the masses rounded differently): the last block
-      sh.ival[0] = kBlocks - 1;
-      sh.scal[1] = local;
-      sh.near = 1;
-    }
-  }
-  __syncthreads();
-  const int blk = sh.ival[0];
-  const float local2 = sh.scal[1];
-  int d = -1;
-  float dist = 0.f;
-  if (warp == 0) {
-    d = warp_find<E, HT, !HT>(a, HT ? row : nullptr, HT ? nullptr : row, cs, blk / kWarps, blk % kWarps, local2,
-                              wf, &dist);
-  } else if (warp == 1 && zdrawn) {
-    const int lane = tid & 31;
-    const int e0 = cs * a.chunk_elems;
-    const int n = min(a.chunk_elems, a.V - e0);
-    const int i0 = ((blk / kWarps) * kThreads + (blk % kWarps) * 32 + lane) * E::kVec;
-    float f[E::kVec], g[E::kVec];
-    ld_vec<E>(row, e0, n, i0, 0.f, f);
-    if (rowZ) ld_vec<E>(rowZ, e0, n, i0, 0.f, g);
-#pragma unroll
-    for (int e = 0; e < E::kVec; ++e) zdrawn[lane * E::kVec + e] = f[e];
-    if (rowZ)
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e) zother[lane * E::kVec + e] = g[e];
-  }
-  __syncthreads();  // everyone read sh.ival / sh.scal
-  if (tid == 0) {
-    sh.ival[4] = d;
-    sh.ival[5] = cs * a.chunk_elems + ((blk / kWarps) * kThreads + (blk % kWarps) * 32) * E::kVec;  // zbuf[0]
-    if (!(dist >= __fmul_rn(kNearTie, Wrow))) sh.near = 1;
-  }
-  __syncthreads();
-  return sh.ival[4];
-}
-
-// A draw from a row without usable block sums (rows whose statistics kept
-// none, or Saguaro weights whose down-weighting makes the statistics' masses
-// inexact): exact block sums by one warp per block (the arithmetic of
-// warp_find), chunk masses from them, then the located chunk's block sums
-// again and one warp over the located block.  Every thread calls; returns the
-// token (-1 when the row has no weight).
-template <class E, bool HT, bool HD, class WF>
-SSD_DEV int exact_draw(const VocabArgs &a, const char *rowT, const char *rowD, float u, const WF &wf, Smem &sh) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  auto block_sums = [&](int c) {  // sh.bw[0..kBlocks) of chunk c
-    for (int k = warp; k < kBlocks; k += kWarps) {
-      float x[E::kVec];
-      const float p = lane_weights<E, HT, HD>(a, rowT, rowD, c, k / kWarps, k % kWarps, wf, x);
-      const float incl = warp_incl_scan(p);
-      if (lane == 31) sh.bw[k] = incl;
-    }
-    __syncthreads();
-  };
-  for (int c = 0; c < a.nchunks; ++c) {
-    block_sums(c);
-    if (warp == 0) {
-      const float m = warp_total(sh.bw, kBlocks);
-      if (lane == 0) sh.cmass[c] = m;
-    }
-    __syncthreads();
-  }
-  if (tid == 0) sh.near = 0;
-  if (warp == 0) locate(sh.cmass, a.nchunks, u, false, sh);
-  __syncthreads();
-  const int cs = sh.ival[0];
-  const float local = sh.scal[1];
-  const float Wrow = sh.scal[2];  // the row's total weight
-  if (cs < 0) return -1;
-  __syncthreads();
-  block_sums(cs);
-  if (warp == 0) locate(sh.bw, kBlocks, local, true, sh);
-  __syncthreads();
-  const int blk = sh.ival[0];
-  const float local2 = sh.scal[1];
-  int d = -1;
-  float dist = 0.f;
-  if (warp == 0 && blk >= 0)
-    d = warp_find<E, HT, HD>(a, rowT, rowD, cs, blk / kWarps, blk % kWarps, local2, wf, &dist);
-  __syncthreads();
-  if (tid == 0) {
-    sh.ival[4] = d;
-    if (!(dist >= __fmul_rn(kNearTie, Wrow))) sh.near = 1;
-  }
-  __syncthreads();
-  return sh.ival[4];
-}
-
-// p_{r+1} (target row r) drawn by its statistics; the row's argmax if the
-// masses are all zero.  `st`: the row's chunk (and, up to kStageChunks
-// chunks, block) records staged by stage_chain (target row K only).
-template <class E>
-SSD_DEV int draw_target(const VocabArgs &a, int b, int r, const RowInfo &row, float u, const Stage *st, Smem &sh) {
-  const float mtk = __fmul_rn(row.mt, a.kT);
-  const WTarget wp{mtk, a.kT};
-  const char *rowT = row_ptr(a, 0, b, r, E::kSize);
-  int d;
-  if (a.slot[a.tsl[r]].blocks) {
-    const BlockRec *sbr = nullptr;
-    if (st) {
-      for (int c = threadIdx.x; c < a.nchunks; c += kThreads) sh.cmass[c] = chunk_mass(st->cs[0][c], a.kT, mtk);
-      if (a.nchunks <= kStageChunks) sbr = st->blk;
-    } else {
-      chunk_masses(a, b, a.tsl[r], mtk, sh);
-    }
-    __syncthreads();
-    d = stats_draw<E, true>(a, b, a.tsl[r], rowT, mtk, u, wp, sbr, nullptr, 0, 1.f, nullptr, nullptr, nullptr, sh);
-  } else {
-    d = exact_draw<E, true, false>(a, rowT, nullptr, u, wp, sh);
-  }
-  return (d >= 0) ? d : row.at;
-}
-
-SSD_DEV WResidual residual_weights(const VocabArgs &a, const RowInfo &ri, uint64_t keyF, int F) {
-  WResidual wf;
-  wf.mtk = __fmul_rn(ri.mt, a.kT);
-  wf.kT = a.kT;
-  wf.inv_st = __frcp_rn(ri.st);
-  wf.mdk = __fmul_rn(ri.md, a.kT);
-  const float sN = __fmul_rn(ri.sd, norm_N(a.C, ri.sq));
-  wf.f1 = __frcp_rn(sN);
-  wf.fC = __fdiv_rn(a.C, sN);
-  wf.hasS = F > 0;
-  wf.keyF = keyF;
-  return wf;
-}
-
-// ===========================================================================
-// the row's top-F from its block maximum keys
-// ===========================================================================
-// The elements (value descending, index ascending) of block `blk` (chunk
-// blk / kBlocks, round, warp) that this lane reads: its 16-byte vector.
-template <class E>
-SSD_DEV void block_vec(const VocabArgs &a, const char *row, int blk, float *f, int *i0, int *n) {
-  const int lane = threadIdx.x & 31;
-  const int c = blk / kBlocks, k = blk - c * kBlocks;
-  const int e0 = c * a.chunk_elems;
-  *n = min(a.chunk_elems, a.V - e0) + e0;
-  *i0 = e0 + ((k / kWarps) * kThreads + (k % kWarps) * 32 + lane) * E::kVec;
-  ld_vec<E>(row, e0, *n - e0, *i0 - e0, -__int_as_float(0x7f800000), f);
-}
-
 // The top-F (F > 1) of a draft row into sh.S (descending; zeros past the
 // row's elements).  t16 = the 16-bit key prefix of the F-th largest block
 // maximum (two levels of 256-bucket counts): at least F elements reach it,
 // so the row's top-F all lie in blocks whose maximum does.  Those blocks are
 // read again (one warp per block) and their elements reaching t16 ranked;
-// when ties overflow the buffers, F sweeps of a CTA-wide maximum instead.
-// sh.hist, sh.ncand and sh.ival[7] start at zero.  Every thread calls.
+// when ties overflow the buffers, F sweeps of a CTA maximum instead.  Every
+// thread calls.
 template <class E>
-SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t *bmk, bool staged, Stage &st,
-                      Smem &sh) {
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int nb = a.nchunks * kBlocks;
-  const int lane = tid & 31;
-  auto key_at = [&](int i) -> uint32_t { return staged ? bmk[i] : __ldcg(bmk + i); };
-  // Bucket counts, one add per distinct bucket of a warp's 32 keys (block
-  // maxima of one row crowd into a few buckets; adding key by key would
-  // serialise the shared-memory atomics on them).  The loops run whole warps.
+SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t *keys, PairSh &sh) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = a.nblk;
   auto count = [&](uint32_t *hist, bool v, uint32_t bucket) {
     const uint32_t peers = __match_any_sync(0xffffffffu, v ? bucket : 0xFFFFFFFFu);
     if (v && lane == __ffs(peers) - 1) atomicAdd(&hist[bucket], static_cast<uint32_t>(__popc(peers)));
   };
+  sh.hist[0][tid] = 0u;
+  sh.hist[1][tid] = 0u;
+  if (tid == 0) {
+    sh.ncand = 0;
+    sh.nblist = 0;
+  }
+  __syncthreads();
   for (int i0 = warp * 32; i0 < nb; i0 += kThreads) {
-    const uint32_t k = (i0 + lane < nb) ? key_at(i0 + lane) : 0u;
+    const uint32_t k = (i0 + lane < nb) ? keys[i0 + lane] : 0u;
     count(sh.hist[0], k != 0u, k >> 24);
   }
   __syncthreads();
@@ -1121,42 +787,29 @@ SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t
   int above, above2;
   find_bucket(sh.hist[0], F, b1, above);
   for (int i0 = warp * 32; i0 < nb; i0 += kThreads) {
-    const uint32_t k = (i0 + lane < nb) ? key_at(i0 + lane) : 0u;
+    const uint32_t k = (i0 + lane < nb) ? keys[i0 + lane] : 0u;
     count(sh.hist[1], k != 0u && (k >> 24) == b1, (k >> 16) & 0xFFu);
   }
   __syncthreads();
   find_bucket(sh.hist[1], F - above, b2, above2);
   const uint32_t t16 = (b1 << 8) | b2;
-  // the candidate blocks
-  constexpr int kListCap = kCandCap * 2;
-  int *blist = reinterpret_cast<int *>(sh.cand);
+  constexpr int kListCap = 2 * kCandCap;
   for (int i = tid; i < nb; i += kThreads) {
-    const uint32_t k = key_at(i);
+    const uint32_t k = keys[i];
     if (k && (k >> 16) >= t16) {
-      const int p = atomicAdd(&sh.ival[7], 1);
-      if (p < kListCap) blist[p] = i;
+      const int p = atomicAdd(&sh.nblist, 1);
+      if (p < kListCap) sh.blist[p] = i;
     }
   }
   __syncthreads();
-  const int nbl = sh.ival[7];
+  const int nbl = sh.nblist;
   const bool listed = nbl <= kListCap;
-  if (listed) {
-    for (int q = warp; q < nbl; q += kWarps) {
-      float f[E::kVec];
-      int i0, n;
-      block_vec<E>(a, row, blist[q], f, &i0, &n);
-#pragma unroll
-      for (int e = 0; e < E::kVec; ++e)
-        if (i0 + e < n && (f2ord(f[e]) >> 16) >= t16) {
-          const int p = atomicAdd(&sh.ncand, 1);
-          if (p < kKeyCap) st.ck[p] = cand_key(f[e], i0 + e);
-        }
-    }
-  }
+  if (listed)
+    for (int q = warp; q < nbl; q += kWarps) block_candidates<E>(a, row, sh.blist[q], t16, sh);
   __syncthreads();
   const int nc = sh.ncand;
-  if (listed && nc <= kKeyCap) {
-    rank_select(st.ck, nc, F, sh.S);
+  if (listed && nc <= kCandCap) {
+    rank_select(sh.cand, nc, F, sh.S);
   } else {
     // ties at the threshold: one winner per sweep over the candidate blocks
     // (every block when they overflow the list)
@@ -1165,13 +818,16 @@ SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t
     for (int r = 0; r < F; ++r) {
       uint64_t best = 0ull;
       for (int q = warp; q < nq; q += kWarps) {
+        const int g = listed ? sh.blist[q] : q;
+        const int v = g * 32 + lane;
+        if (v >= a.nvec) continue;
         float f[E::kVec];
-        int i0, n;
-        block_vec<E>(a, row, listed ? blist[q] : q, f, &i0, &n);
+        E::unpack(row_vec<E>(a, row, v), f);
 #pragma unroll
         for (int e = 0; e < E::kVec; ++e) {
-          if (i0 + e >= n || (f2ord(f[e]) >> 16) < t16) continue;
-          const uint64_t key = cand_key(f[e], i0 + e);
+          const int idx = v * E::kVec + e;
+          if (idx >= a.V || (f2ord(f[e]) >> 16) < t16) continue;
+          const uint64_t key = cand_key(f[e], idx);
           if (key < prev && key > best) best = key;
         }
       }
@@ -1183,393 +839,414 @@ SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t
   __syncthreads();
 }
 
-// ===========================================================================
-// pair merge: row statistics, top-F list, Saguaro draw, p(d), q'(d), guesses
-// ===========================================================================
+// One warp: inverse-CDF draw over a row from its segment masses smm (row
+// units), block masses bm (segment units: weights relative to fl(seg max kT))
+// and a warp_find over the located block, which reads both rows' vectors
+// when given.  Returns the element (every lane; -1 when the row has no
+// weight) with its target / draft values and whether it is a near-tie.
+template <class E, class WF>
+SSD_DEV int row_draw(const VocabArgs &a, const SegRec *sr, float rowMk, const float *smm, const float *bm,
+                     const char *rowT, const char *rowD, float u, const WF &wf, bool *near, float *zt, float *zd) {
+  float rem, W;
+  bool fb;
+  const int s = warp_locate(smm, a.nseg, u, false, &rem, &W, &fb);
+  *near = true;
+  if (s < 0) return -1;
+  const float Ms = __fmul_rn(sr[s].m, a.kT);
+  const float f = ex2(__fsub_rn(Ms, rowMk));  // a segment unit in row units
+  float rem2, W2;
+  bool fb2;
+  const int k = warp_locate(bm + s * kSegBlocks, kSegBlocks, __fdiv_rn(rem, f), true, &rem2, &W2, &fb2);
+  if (k < 0) return -1;
+  float dist;
+  const int d = warp_find<E>(a, rowT, rowD, s * kSegBlocks + k, rem2, wf, Ms, &dist, zt, zd);
+  *near = fb || fb2 || d < 0 || !(__fmul_rn(dist, f) >= __fmul_rn(kNearTie, W));
+  return d;
+}
+
 template <class E>
-__device__ __forceinline__ void row_finish(const VocabArgs &a, int b, int r, Stage &st, Smem &sh) {
+__global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ VocabArgs a) {
+  // k_resid (if any) may start launching once every CTA of this grid has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ __align__(16) uint8_t pair_smem[];
+  PairSh &sh = *reinterpret_cast<PairSh *>(pair_smem);
+  const PairBufs pb = pair_bufs(a, pair_smem + sizeof(PairSh));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ts = a.tsl[r], ds = a.dsl[r];
-  const int F = (ds >= 0) ? a.Fs[r] : 0;
-  const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
+  const int b = static_cast<int>(blockIdx.x) / a.npairs;
+  const int j = static_cast<int>(blockIdx.x) - b * a.npairs;
+  const int K = a.K;
   const float NEG_INF = -__int_as_float(0x7f800000);
-  const char *rowT = row_ptr(a, 0, b, r, E::kSize);
-  const char *rowD = row_ptr(a, 1, b, r, E::kSize);
-  const bool draws = r < a.K && a.do_sample && !a.greedy && ds >= 0;
-  const bool stage_blk = draws && a.slot[ds].blocks && a.nchunks <= kStageChunks;
-  const bool given = r < a.K && !a.do_sample && a.do_verify;  // verification of tokens the caller drew
-  const bool stage_bmk = F > 1 && a.nchunks <= kStageChunks;
-  // one round of loads: both rows' chunk records, the draft row's block
-  // maximum keys (top-F), the block records of a row drawn from and (tokens
-  // given) the token with its two logits
-  const uint32_t *gbmk = a.bmk + chunk_index(a, b, ds, 0) * kBlocks;
-  if (stage_bmk)
-    for (int i = tid; i < a.nchunks * (kBlocks / 4); i += kThreads)
-      cp_async16(reinterpret_cast<int4 *>(st.bmk) + i, reinterpret_cast<const int4 *>(gbmk) + i);
-  if (F > 1) {
-    sh.hist[0][tid] = 0u;
-    sh.hist[1][tid] = 0u;
+  if (a.trace && tid == 0) {
+    for (int k = 0; k < 8; ++k) sh.mk[k] = 0ull;
+    sh.mk[1] = now_ns();
   }
-  for (int c = tid; c < a.nchunks; c += kThreads) {
-    if (ts >= 0) cp_async16(&st.cs[0][c], a.stats + chunk_index(a, b, ts, c));
-    if (ds >= 0) cp_async16(&st.cs[1][c], a.stats + chunk_index(a, b, ds, c));
+  const int ts = a.tsl[j], ds = a.dsl[j];
+  const bool hT = ts >= 0, hD = ds >= 0;
+  const int F = hD ? a.Fs[j] : 0;
+  const bool greedy = a.greedy != 0;
+  const bool sampled = a.do_sample && j < K;
+  const bool tested = a.do_verify && j < K;
+  const bool bonus_p = a.do_verify && j == K && !greedy;
+  // C < 1 weights the draft's draw by S: it waits for the top-F list
+  const bool weighted = !greedy && sampled && a.C < 1.f && F > 0;
+  const char *rowT = row_ptr(a, 0, b, j, E::kSize);
+  const char *rowD = row_ptr(a, 1, b, j, E::kSize);
+  // the counters k_resid takes tickets on and the hit count start at zero
+  // (k_resid waits for this grid to complete before it touches them)
+  if (tid == 0) {
+    if (j == 0) a.ctr[2 + b] = 0u;
+    if (j < K && a.do_analytics) a.ctr[2 + a.B + static_cast<size_t>(b) * K + j] = 0u;
+    if (b == 0 && j == 0 && a.do_lookup && a.hits) *a.hits = 0u;
   }
-  if (stage_blk) {
-    constexpr int kW = static_cast<int>(sizeof(BlockRec) / 16);
-    const int4 *src = reinterpret_cast<const int4 *>(a.blk + chunk_index(a, b, ds, 0));
-    int4 *dst = reinterpret_cast<int4 *>(st.blk);
-    for (int i = tid; i < a.nchunks * kW; i += kThreads) cp_async16(dst + i, src + i);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // k_stats has completed
+  if (a.trace && tid == 0) sh.mk[2] = now_ns();
+  // stage the records
+  const int drawn = (sampled && !greedy) ? kDft : (bonus_p ? kTgt : -1);
+  {
+    const int4 *sT = reinterpret_cast<const int4 *>(a.seg + slot_index(a, b, hT ? ts : 0) * a.nseg);
+    const int4 *sD = reinterpret_cast<const int4 *>(a.seg + slot_index(a, b, hD ? ds : 0) * a.nseg);
+    for (int s = tid; s < a.nseg; s += kThreads) {
+      if (hT) cp_async16(pb.segT + s, sT + s);
+      if (hD) cp_async16(pb.segD + s, sD + s);
+    }
+    if (F >= 2) {
+      const uint32_t *k = a.bkey + slot_index(a, b, ds) * a.nblk;
+      for (int i = tid; i < a.nblk / 4; i += kThreads)
+        cp_async16(reinterpret_cast<int4 *>(pb.keys) + i, reinterpret_cast<const int4 *>(k) + i);
+    }
+    if (drawn >= 0) {
+      const float *bs = a.bsum + slot_index(a, b, drawn == kDft ? ds : ts) * a.nblk;
+      for (int i = tid; i < a.nblk / 4; i += kThreads)
+        cp_async16(reinterpret_cast<int4 *>(pb.bm) + i, reinterpret_cast<const int4 *>(bs) + i);
+    }
+    cp_async_wait_all();
   }
   if (tid == 0) {
-    memset(&sh.ri, 0, sizeof(sh.ri));
-    sh.ncand = 0;
-    sh.ival[7] = 0;
-    if (given) {
-      const int d = a.d_in[static_cast<size_t>(b) * a.K + r];
-      sh.ival[2] = d;
-      if (d >= 0 && d < a.V && !a.greedy) {
-        sh.scal[4] = E::ld(rowT, d);
-        sh.scal[5] = E::ld(rowD, d);
-      }
-    }
+    if (!hT) sh.gm[kTgt] = sh.gs[kTgt] = 0.f, sh.ga[kTgt] = 0;
+    if (!hD) sh.gm[kDft] = sh.gs[kDft] = 0.f, sh.ga[kDft] = 0;
   }
-  cp_async_wait_all();
   __syncthreads();
-  // the last two warps merge the target and draft rows' chunk records; all
-  // warps then select the draft row's top-F
-  if (warp == kWarps - 2 && ts >= 0) {
-    const RowStat t = merge_row_warp(a, st.cs[0]);
+  if (a.trace && tid == 0) sh.mk[3] = now_ns();
+  // row statistics: warp 0 the target row, warp 1 the draft row
+  if ((warp == 0 && hT) || (warp == 1 && hD)) {
+    float M, S;
+    int A;
+    merge_row(a, warp == 0 ? pb.segT : pb.segD, M, S, A);
     if (lane == 0) {
-      sh.ri.mt = t.m;
-      sh.ri.st = t.s;
-      sh.ri.at = t.amax;
+      sh.gm[warp] = M;
+      sh.gs[warp] = S;
+      sh.ga[warp] = A;
     }
   }
-  if (warp == kWarps - 1 && ds >= 0) {
-    const RowStat d = merge_row_warp(a, st.cs[1]);
-    if (lane == 0) {
-      sh.ri.md = d.m;
-      sh.ri.sd = d.s;
-      sh.ri.ad = d.amax;
-    }
-  }
-  // the draft row's top-F list: S (and its global copy), Σ_S q and the
-  // guesses of depth r
-  auto list_part = [&]() {
-    if (F > 1) row_topf<E>(a, rowD, F, stage_bmk ? st.bmk : gbmk, stage_bmk, st, sh);
-    __syncthreads();  // the merged statistics and the list
-    const float mdk = __fmul_rn(sh.ri.md, a.kT);
-    if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.ri.md, sh.ri.ad);  // the top-1: the row's argmax
-    if (F == 1) __syncthreads();
-    if (a.do_verify || a.do_lookup || a.do_analytics)
-      for (int i = tid; i < F; i += kThreads) a.S[rr * a.Fcap + i] = sh.S[i];
-    // the draft's normalised mass on S: lane-strided partial sums, a fixed tree
-    if (warp == 0) {
-      float sq = 0.f;
-      if (!a.greedy && sh.ri.md != NEG_INF) {
-        for (int i = lane; i < F; i += 32)
-          if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
-        sq = __fdiv_rn(warp_sum(sq), sh.ri.sd);
-      }
-      if (lane == 0) sh.ri.sq = sq;
+  __syncthreads();
+  if (a.trace && tid == 0) sh.mk[4] = now_ns();
+  const float mtk = __fmul_rn(sh.gm[kTgt], a.kT), mdk = __fmul_rn(sh.gm[kDft], a.kT);
+  const int at = sh.ga[kTgt], ad = sh.ga[kDft];
+  // the drawn row's segment masses in row units (from the segment totals)
+  const SegRec *srd = drawn == kDft ? pb.segD : pb.segT;
+  const float rowMk = drawn == kDft ? mdk : mtk;
+  if (drawn >= 0 && !weighted) {
+    for (int s = tid; s < a.nseg; s += kThreads) {
+      const float m = srd[s].m;
+      pb.smm[s] = (m == NEG_INF) ? 0.f : __fmul_rn(srd[s].t, ex2(__fsub_rn(__fmul_rn(m, a.kT), rowMk)));
     }
     __syncthreads();
-    if (a.do_predict && ds >= 0) {
-      const int sumF = a.foff[a.K + 1];
-      for (int i = tid; i < a.F[r]; i += kThreads) {
-        const uint64_t key = sh.S[i];
-        a.guess[static_cast<size_t>(b) * sumF + a.foff[r] + i] = cand_idx(key);
-        if (a.guess_q) {
-          float q;
-          if (a.greedy) q = (i == 0) ? 1.f : 0.f;
-          else q = __fdiv_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), sh.ri.sd);
-          a.guess_q[static_cast<size_t>(b) * sumF + a.foff[r] + i] = q;
+  }
+  // warp 0 keeps the position's record
+  PairRec r;
+  memset(&r, 0, sizeof(r));
+  r.d = -1;
+  r.bt = -1;
+  r.W = 1.f;
+  r.N = 1.f;
+  // the draw of d_{j+1} (or the given token) with p(d) and q(d) when it does
+  // not depend on S, and the bonus after full acceptance
+  float zt = 0.f, zd = 0.f;
+  bool zknown = false;
+  if (warp == 0) {
+    if (sampled || tested) {
+      int d;
+      bool near = false;
+      if (sampled && greedy) {
+        d = ad;
+      } else if (sampled && !weighted) {
+        const WDraft wd{a.kT, 1.f, 0.f, 0ull, false};
+        d = row_draw<E>(a, pb.segD, mdk, pb.smm, pb.bm, hT ? rowT : nullptr, rowD,
+                        a.u_draft[static_cast<size_t>(b) * K + j], wd, &near, &zt, &zd);
+        zknown = d >= 0;
+        if (d < 0) {
+          d = ad;
+          near = true;
         }
-      }
-    }
-  };
-  // with C = 1 the draw, p(d), q'(d) and the residual weights do not depend
-  // on S: the list comes after the position's verdict, which may start the
-  // residual draw sooner
-  const bool verdict = a.do_verify && !a.greedy && r < a.K;
-  const bool late_list = verdict && !(a.C < 1.f);
-  if (late_list) __syncthreads();  // the merged statistics
-  else list_part();
-  const float mdk = __fmul_rn(sh.ri.md, a.kT);
-  const RowInfo ri = sh.ri;  // late_list: sq = 0 until the list is done (C = 1 makes q' not depend on it)
-  const uint64_t keyF = (F > 0 && !late_list) ? sh.S[F - 1] : 0ull;
-  mark(a, sh.mk, 3);
-  if (r < a.K && (a.do_sample || a.do_verify)) {
-    int d;
-    bool zknown = false;  // zt / zd hold the token's logits
-    float zt = 0.f, zd = 0.f;
-    if (a.do_sample) {
-      float qd;
-      if (a.greedy) {
-        d = ri.ad;
-        qd = 1.f;
+      } else if (sampled) {
+        d = -1;  // drawn once S is known
       } else {
-        const WSaguaro wf{mdk, a.kT, a.C, keyF, F > 0};
-        const float u = a.u_draft[static_cast<size_t>(b) * a.K + r];
-        if (__fmul_rn(__fsub_rn(1.f, a.C), ri.sq) > 0.875f || !a.slot[ds].blocks) {
-          d = exact_draw<E, false, true>(a, nullptr, rowD, u, wf, sh);
-        } else {
-          // chunk masses of q' (unnormalised): s_c 2^(Mk_c - mdk) - (1 - C) sum_{i in S, in c} e_i,
-          // the elements of S in list order
-          for (int c = tid; c < a.nchunks; c += kThreads) {
-            float m = chunk_mass(st.cs[1][c], a.kT, mdk);
-            if (a.C < 1.f) {
-              for (int i = 0; i < F; ++i) {
-                const uint64_t k = sh.S[i];
-                if (!k || cand_idx(k) / a.chunk_elems != c) continue;
-                m = __fsub_rn(m, __fmul_rn(__fsub_rn(1.f, a.C), ex2(__fmaf_rn(cand_val(k), a.kT, -mdk))));
-              }
-              m = fmaxf(m, 0.f);
-            }
-            sh.cmass[c] = m;
-          }
-          __syncthreads();
-          d = stats_draw<E, false>(a, b, ds, rowD, mdk, u, wf, stage_blk ? st.blk : nullptr, sh.S, F, a.C, st.z[1],
-                                   a.do_verify ? rowT : nullptr, st.z[0], sh);
-          if (d >= 0) {
-            const int o = d - sh.ival[5];
-            if (o >= 0 && o < 32 * E::kVec) {
-              zd = st.z[1][o];
-              zt = st.z[0][o];
-              zknown = true;
-            }
-          }
-        }
-        if (tid == 0 && sh.near && a.near_ties) atomicAdd(a.near_ties, 1u);
-        if (d < 0) d = ri.ad;
-        if (!zknown) {
-          zd = E::ld(rowD, d);
-          zt = a.do_verify ? E::ld(rowT, d) : 0.f;
-          zknown = true;
-        }
-        const bool ins = F > 0 && cand_key(zd, d) >= keyF;
-        const float q = __fdiv_rn(ex2(__fmaf_rn(zd, a.kT, -mdk)), ri.sd);
-        qd = __fdiv_rn(ins ? __fmul_rn(q, a.C) : q, norm_N(a.C, ri.sq));
+        d = a.d_in[static_cast<size_t>(b) * K + j];
       }
-      if (tid == 0) {
-        a.d_out[static_cast<size_t>(b) * a.K + r] = d;
-        if (a.qd_out) a.qd_out[static_cast<size_t>(b) * a.K + r] = qd;
-      }
-    } else {
-      d = sh.ival[2];
-      zt = sh.scal[4];
-      zd = sh.scal[5];
-      zknown = true;
+      r.d = d;
+      if (near) r.fl |= kRecDrawNear;
     }
-    if (a.do_verify && tid == 0) {
-      PosInfo pi{d, 0.f, 0.f, 0};
+    if (a.do_verify && j == K) {
+      if (greedy) {
+        r.bt = at;
+      } else {
+        bool near;
+        float z0, z1;
+        int bt = row_draw<E>(a, pb.segT, mtk, pb.smm, pb.bm, rowT, nullptr, a.u_bonus[b], WTarget{a.kT}, &near, &z0,
+                             &z1);
+        if (bt < 0) {
+          bt = at;
+          near = true;
+        }
+        r.bt = bt;
+        if (near) r.fl |= kRecBonusNear;
+      }
+    }
+  }
+  if (a.trace && tid == 0) sh.mk[5] = now_ns();
+  // the draft row's top-F list S, its normalised mass and the guesses of depth j
+  if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.gm[kDft], ad);
+  if (F >= 2) row_topf<E>(a, rowD, F, pb.keys, sh);
+  __syncthreads();
+  if (warp == 1) {
+    float sq = 0.f;
+    if (!greedy && F > 0 && sh.gm[kDft] != NEG_INF) {
+      for (int i = lane; i < F; i += 32)
+        if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
+      sq = __fdiv_rn(warp_sum(sq), sh.gs[kDft]);
+    }
+    if (lane == 0) sh.sq = sq;
+  }
+  if (a.do_predict && hD) {
+    const int sumF = a.foff[K + 1];
+    for (int i = tid; i < a.F[j]; i += kThreads) {
+      const uint64_t key = sh.S[i];
+      a.guess[static_cast<size_t>(b) * sumF + a.foff[j] + i] = cand_idx(key);
+      if (a.guess_q) {
+        float q;
+        if (greedy) q = (i == 0) ? 1.f : 0.f;
+        else q = __fdiv_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), sh.gs[kDft]);
+        a.guess_q[static_cast<size_t>(b) * sumF + a.foff[j] + i] = q;
+      }
+    }
+  }
+  __syncthreads();
+  if (a.trace && tid == 0) sh.mk[6] = now_ns();
+  const uint64_t keyF = F > 0 ? sh.S[F - 1] : 0ull;
+  const float vF = cand_val(keyF);
+  const float N = norm_N(a.C, sh.sq);
+  if (weighted) {
+    // the Saguaro weights: block masses with the elements of S down-weighted
+    // (in list order), segment masses in row units from them
+    for (int i = tid; i < a.nblk; i += kThreads) {
+      float m = pb.bm[i];
+      const float Ms = __fmul_rn(srd[i / kSegBlocks].m, a.kT);
+      for (int t = 0; t < F; ++t) {
+        const uint64_t key = sh.S[t];
+        if (!key || (cand_idx(key) / E::kVec) / 32 != i) continue;
+        m = __fsub_rn(m, __fmul_rn(__fsub_rn(1.f, a.C), ex2(__fmaf_rn(cand_val(key), a.kT, -Ms))));
+      }
+      pb.bm[i] = fmaxf(m, 0.f);
+    }
+    __syncthreads();
+    for (int s = warp; s < a.nseg; s += kWarps) {
+      const float t = warp_total(pb.bm + s * kSegBlocks, kSegBlocks);
+      if (lane == 0) {
+        const float m = srd[s].m;
+        pb.smm[s] = (m == NEG_INF) ? 0.f : __fmul_rn(t, ex2(__fsub_rn(__fmul_rn(m, a.kT), rowMk)));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const WDraft wd{a.kT, a.C, vF, keyF, true};
+      bool near;
+      int d = row_draw<E>(a, pb.segD, mdk, pb.smm, pb.bm, hT ? rowT : nullptr, rowD,
+                          a.u_draft[static_cast<size_t>(b) * K + j], wd, &near, &zt, &zd);
+      zknown = d >= 0;
+      if (d < 0) {
+        d = ad;
+        near = true;
+      }
+      r.d = d;
+      if (near) r.fl |= kRecDrawNear;
+    }
+  }
+  // p(d), q'(d), the verdict, the outputs and the record (warp 0)
+  if (warp == 0) {
+    r.N = N;
+    r.keyF = keyF;
+    r.gm[kTgt] = sh.gm[kTgt];
+    r.gm[kDft] = sh.gm[kDft];
+    r.gs[kTgt] = sh.gs[kTgt];
+    r.gs[kDft] = sh.gs[kDft];
+    if (sampled || tested) {
+      const int d = r.d;
       if (d >= 0 && d < a.V) {
-        if (a.greedy) {
-          pi.p = (d == ri.at) ? 1.f : 0.f;
-          pi.q = (d == ri.ad) ? 1.f : 0.f;
+        if (greedy) {
+          r.p = (d == at) ? 1.f : 0.f;
+          r.q = (d == ad) ? 1.f : 0.f;
         } else {
           if (!zknown) {
-            zt = E::ld(rowT, d);
             zd = E::ld(rowD, d);
+            zt = hT ? E::ld(rowT, d) : 0.f;
           }
           const bool ins = F > 0 && cand_key(zd, d) >= keyF;
-          pi.p = __fdiv_rn(ex2(__fmaf_rn(zt, a.kT, -__fmul_rn(ri.mt, a.kT))), ri.st);
-          const float q = __fdiv_rn(ex2(__fmaf_rn(zd, a.kT, -mdk)), ri.sd);
-          pi.q = __fdiv_rn(ins ? __fmul_rn(q, a.C) : q, norm_N(a.C, ri.sq));
+          const float q = __fdiv_rn(ex2(__fmaf_rn(zd, a.kT, -mdk)), sh.gs[kDft]);
+          r.q = __fdiv_rn(ins ? __fmul_rn(q, a.C) : q, N);
+          if (hT) r.p = __fdiv_rn(ex2(__fmaf_rn(zt, a.kT, -mtk)), sh.gs[kTgt]);
         }
       } else {
-        pi.p = -1.f;
-        atomicOr(a.status, kFlagBadToken);
+        r.p = -1.f;
+        r.q = 0.f;
+        if (lane == 0) atomicOr(a.status, kFlagBadToken);
       }
-      a.pos[static_cast<size_t>(b) * a.K + r] = pi;
-      if (a.accept_prob) {
+      if (tested && r.p >= 0.f && __fmul_rn(a.u_acc[static_cast<size_t>(b) * K + j], r.q) < r.p)
+        r.fl |= kRecAccepted;
+      if (tested) r.bt = at;  // greedy: the bonus; T > 0: the residual draw's fallback
+      if (tested && greedy) {
+        r.W = (at != ad) ? 1.f : 0.f;
+        if (!(r.W > 0.f)) r.fl |= kRecZero;
+      }
+    }
+    if (lane == 0) {
+      if (sampled) {
+        a.d_out[static_cast<size_t>(b) * K + j] = r.d;
+        if (a.qd_out) a.qd_out[static_cast<size_t>(b) * K + j] = r.q;
+      }
+      if (tested && a.accept_prob) {
         float ap;
-        if (pi.p < 0.f) ap = 0.f;
-        else if (pi.q > 0.f) ap = fminf(1.f, __fdiv_rn(pi.p, pi.q));
-        else ap = (pi.p > 0.f) ? 1.f : 0.f;
-        a.accept_prob[static_cast<size_t>(b) * a.K + r] = ap;
+        if (r.p < 0.f) ap = 0.f;
+        else if (r.q > 0.f) ap = fminf(1.f, __fdiv_rn(r.p, r.q));
+        else ap = (r.p > 0.f) ? 1.f : 0.f;
+        a.accept_prob[static_cast<size_t>(b) * K + j] = ap;
+      }
+      if (a.do_verify) a.rec[static_cast<size_t>(b) * (K + 1) + j] = r;
+      if (a.do_analytics) {
+        // the hit partials come from warp 1 (below); the rest of the record here
+        PairRec *dst = a.rec + static_cast<size_t>(b) * (K + 1) + j;
+        dst->N = r.N;
+        dst->keyF = r.keyF;
+        dst->gm[0] = r.gm[0];
+        dst->gm[1] = r.gm[1];
+        dst->gs[0] = r.gs[0];
+        dst->gs[1] = r.gs[1];
       }
     }
   }
-  if (tid == 0) a.rows[rr] = ri;
-  if (verdict) {
-    // the position's verdict (1 accepted, 2 rejected; + 2 once the pair's
-    // list is also written), then the frontier: once the positions before the
-    // first rejection are all accepted, the residual draw may start (ready
-    // word = rejected position + 2) without waiting for the remaining pairs
-    __syncthreads();  // the pair's results are written
-    uint32_t vword = 0;
-    if (tid == 0) {
-      const PosInfo pi = ldcg_pos(a.pos + static_cast<size_t>(b) * a.K + r);
-      const bool ok = pi.p >= 0.f && __fmul_rn(a.u_acc[static_cast<size_t>(b) * a.K + r], pi.q) < pi.p;
-      vword = (ok ? 1u : 2u) + (late_list ? 0u : 2u);
-      st_release(pos_verdict(a, b, r), vword);
-      uint32_t v[kMaxK];  // every verdict load in flight at once
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) v[j] = (j < a.K) ? ld_relaxed(pos_verdict(a, b, j)) : 1u;
-      uint32_t acc_mask = 0, rej_mask = 0;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (v[j] == 1u || v[j] == 3u) acc_mask |= 1u << j;
-        if (v[j] == 2u || v[j] == 4u) rej_mask |= 1u << j;
-      }
-      const uint32_t open = ~acc_mask;  // the first position not known to be accepted
-      if (open) {
-        const int j = __ffs(static_cast<int>(open)) - 1;
-        if ((rej_mask >> j) & 1u) {
-          fence_acq_rel();  // the verdicts (and results) of positions 0..j, then the ready word
-          atomicCAS(ready_word(a, b), 0u, static_cast<uint32_t>(j + 2));
+  // analytics: the guesses' target and residual probability (all of S carries C in q')
+  if (a.do_analytics && warp == 1) {
+    float hp = 0.f, hr = 0.f;
+    if (greedy) {
+      for (int i = lane; i < a.F[j]; i += 32)
+        if (cand_idx(sh.S[i]) == at) hp = 1.f;
+      hp = warp_max(hp);
+      hr = hp;
+    } else {
+      const float inv_st = __frcp_rn(sh.gs[kTgt]);
+      const float fC = __fdiv_rn(a.C, __fmul_rn(sh.gs[kDft], N));
+      for (int i = lane; i < a.F[j]; i += 32) {
+        const uint64_t key = sh.S[i];
+        if (!key) continue;
+        const int d = cand_idx(key);
+        const float p = __fmul_rn(ex2(__fmaf_rn(E::ld(rowT, d), a.kT, -mtk)), inv_st);
+        hp = __fadd_rn(hp, p);
+        if (j < K) {
+          const float q = __fmul_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), fC);
+          hr = __fadd_rn(hr, fmaxf(__fsub_rn(p, q), 0.f));
         }
       }
+      hp = warp_sum(hp);
+      hr = warp_sum(hr);
     }
-    if (late_list) {
-      list_part();
-      if (tid == 0) a.rows[rr] = sh.ri;  // with Σ_S q
-      __syncthreads();                   // the list is written
-      if (tid == 0) st_release(pos_verdict(a, b, r), vword + 2u);
+    if (lane == 0) {
+      PairRec *dst = a.rec + static_cast<size_t>(b) * (K + 1) + j;
+      dst->hp = hp;
+      dst->hr = hr;
+      float al = 0.f, W = 0.f;
+      if (greedy) {
+        al = (j < K && at == ad) ? 1.f : 0.f;
+        W = 1.f - al;
+      }
+      dst->al = al;
+      dst->W = W;
     }
+  }
+  if (a.trace && tid == 0) {
+    sh.mk[7] = now_ns();
+    trace_entry(a, a.trace_pair + blockIdx.x, 1, b, j, sh.mk);
   }
 }
 
 // ===========================================================================
-// sequence finish: acceptance chain, bonus draw, outputs, cache lookup
+// k_resid: residual units, the bonus draw and the sequence finish
 // ===========================================================================
-// The top-F lists of a sequence (cache lookup) fit sh.cand; its payload fits
-// the payload stage.
-SSD_DEV bool lists_staged(const VocabArgs &a) { return a.do_lookup && a.foff[a.K + 1] <= kCandCap; }
-SSD_DEV bool pay_staged(const VocabArgs &a) {
-  return a.do_lookup && a.next_tokens && a.payload && a.foff[a.K + 1] * a.K <= kPayStage;
-}
+constexpr int kLookupStage = 2048;  // guesses + payload words of a sequence staged in shared memory
+constexpr int kBlkStage = 1024;     // residual block sums the last unit stages at once
+struct __align__(16) ResSh {
+  PairRec rec[kMaxK + 1];
+  float u[kMaxK];
+  float seg[kWarps][2];      // this unit's segment masses (residual, p), or its warps' analytics sums
+  float um[2][kMaxUnits];    // the sequence's unit masses (residual, p)
+  float2 bl[kBlkStage];      // residual block sums (residual, p)
+  float bx[kUnitSeg * kSegBlocks];
+  float sm[kUnitSeg];
+  int32_t look[kLookupStage];  // the sequence's guesses, then its payload
+  float scal[4];
+  int ival[4];
+  unsigned long long mk[8];
+};
+// The residual pass's vectors: per warp its segment of both rows (8 blocks of
+// 32 vectors), staged by cp.async so that the block loop need not be unrolled.
+struct __align__(16) ResStage {
+  uint4 v[kWarps][2][kSegBlocks][32];
+};
 
-// Stage in shared memory, in one round of loads, what the final steps of
-// sequence b need whatever the accept count: draft tokens, p(d), q'(d), the
-// uniforms, every row's merged statistics and S threshold key, the top-F
-// lists (sh.cand) and payload (`pay`) of the cache lookup when they fit, the
-// residual unit masses (`umass`) and target row K's chunk and block records
-// for the bonus draw (`st`).  Then the acceptance chain (thread 0).  Every
-// thread returns the accept count.
-SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, bool lists, Smem &sh);
-SSD_DEV void stage_lists(const VocabArgs &a, int b, Smem &sh);
-SSD_DEV int stage_complete(const VocabArgs &a, Smem &sh);
-SSD_DEV int stage_chain(const VocabArgs &a, int b, float *umass, int32_t *pay, Stage *st, Smem &sh) {
-  stage_issue(a, b, pay, st, true, sh);
-  if (umass) {
-    const int nu = a.nchunks * kQuarters;
-    for (int q = threadIdx.x; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
-  }
-  return stage_complete(a, sh);
-}
-// The top-F lists of the cache lookup (when they fit sh.cand), issued
-// (cp.async) without a wait.
-SSD_DEV void stage_lists(const VocabArgs &a, int b, Smem &sh) {
-  if (!lists_staged(a)) return;
-  const size_t r0 = static_cast<size_t>(b) * (a.K + 1);
-  const int nS = a.foff[a.K + 1];
-  for (int i = threadIdx.x; i < nS; i += kThreads) {
-    int r = 0;
-    while (i >= a.foff[r + 1]) ++r;
-    cp_async8(&sh.cand[i], a.S + (r0 + r) * a.Fcap + (i - a.foff[r]));
-  }
-}
-// The loads of stage_chain but the unit masses (and, unless `lists`, the
-// lookup lists), issued (cp.async) without a wait.
-SSD_DEV void stage_issue(const VocabArgs &a, int b, int32_t *pay, Stage *st, bool lists, Smem &sh) {
+// The outputs of sequence b once its bonus token bt is known (sh.rec: its
+// records, sh.u: its acceptance uniforms, sh.look: its lookup lists when
+// `staged`).
+SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, bool near_bonus, bool staged,
+                  ResSh &sh) {
   const int tid = threadIdx.x;
-  const size_t r0 = static_cast<size_t>(b) * (a.K + 1);
-  for (int t = tid; t < a.K; t += kThreads) {
-    cp_async16(&sh.pos[t], a.pos + static_cast<size_t>(b) * a.K + t);
-    cp_async4(&sh.cu[t], a.u_acc + static_cast<size_t>(b) * a.K + t);
-  }
-  for (int i = tid; i < 2 * (a.K + 1); i += kThreads)
-    cp_async16(reinterpret_cast<int4 *>(&sh.rows[i >> 1]) + (i & 1), reinterpret_cast<const int4 *>(a.rows + r0 + (i >> 1)) + (i & 1));
-  for (int r = tid; r <= a.K; r += kThreads) {
-    const int F = a.Fs[r];
-    if (F > 0) cp_async8(&sh.keyF[r], a.S + (r0 + r) * a.Fcap + F - 1);
-    else sh.keyF[r] = 0ull;
-  }
-  if (lists) stage_lists(a, b, sh);
-  if (pay && pay_staged(a)) {
-    const int n = a.foff[a.K + 1] * a.K;
-    const int32_t *src = a.payload + static_cast<size_t>(b) * n;
-    for (int i = tid; i < n; i += kThreads) cp_async4(&pay[i], src + i);
-  }
-  if (st && !a.greedy && a.tsl[a.K] >= 0) {
-    const int ts = a.tsl[a.K];
-    for (int c = tid; c < a.nchunks; c += kThreads) cp_async16(&st->cs[0][c], a.stats + chunk_index(a, b, ts, c));
-    if (a.slot[ts].blocks && a.nchunks <= kStageChunks) {
-      constexpr int kW = static_cast<int>(sizeof(BlockRec) / 16);
-      const int4 *src = reinterpret_cast<const int4 *>(a.blk + chunk_index(a, b, ts, 0));
-      int4 *dst = reinterpret_cast<int4 *>(st->blk);
-      for (int i = tid; i < a.nchunks * kW; i += kThreads) cp_async16(dst + i, src + i);
-    }
-  }
-}
-// Waits for the staged loads, then the acceptance chain; every thread returns
-// the accept count.
-SSD_DEV int stage_complete(const VocabArgs &a, Smem &sh) {
-  const int tid = threadIdx.x;
-  cp_async_wait_all();
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int t = 0; t < a.K; ++t) {
-      const PosInfo pi = sh.pos[t];
-      if (pi.p >= 0.f && __fmul_rn(sh.cu[t], pi.q) < pi.p) ++acc;
-      else break;
-    }
-    sh.ival[1] = acc;
-  }
-  __syncthreads();
-  return sh.ival[1];
-}
-
-// Outputs of sequence b once its bonus token bt is known (sh.cd: draft tokens;
-// the lookup's lists and payload as stage_chain staged them, `pay` its
-// payload stage).
-SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, bool near_bonus, const int32_t *pay,
-                  Smem &sh) {
-  const int tid = threadIdx.x;
-  const int Fa = a.F[acc];
+  const int K = a.K;
+  const int sumF = a.foff[K + 1];
   if (tid == 0) {
     sh.ival[3] = kNone;
     if (a.near_ties && !a.greedy) {
-      // the acceptance tests actually taken (positions 1..acc+1) whose u lies
-      // within kNearTie of p/q', and the bonus draw
+      // the acceptance tests actually taken (positions 1..acc+1) whose u
+      // lies within kNearTie of p/q', the bonus draw and (sampling) the
+      // draws of d_1..d_K
       uint32_t n = near_bonus ? 1u : 0u;
-      for (int t = 0; t <= acc && t < a.K; ++t) {
-        const PosInfo pi = sh.pos[t];
-        if (pi.p >= 0.f && pi.q > 0.f && fabsf(__fsub_rn(sh.cu[t], __fdiv_rn(pi.p, pi.q))) < kNearTie) ++n;
+      for (int t = 0; t <= acc && t < K; ++t) {
+        const PairRec &r = sh.rec[t];
+        if (r.p >= 0.f && r.q > 0.f && fabsf(__fsub_rn(sh.u[t], __fdiv_rn(r.p, r.q))) < kNearTie) ++n;
       }
+      if (a.do_sample)
+        for (int t = 0; t < K; ++t) n += (sh.rec[t].fl & kRecDrawNear) ? 1u : 0u;
       if (n) atomicAdd(a.near_ties, n);
     }
   }
   __syncthreads();
   if (a.do_lookup) {
-    if (lists_staged(a)) {
-      for (int i = tid; i < Fa; i += kThreads)
-        if (cand_idx(sh.cand[a.foff[acc] + i]) == bt) atomicMin(&sh.ival[3], i);
-    } else {
-      const uint64_t *S = a.S + (static_cast<size_t>(b) * (a.K + 1) + acc) * a.Fcap;
-      for (int i = tid; i < Fa; i += kThreads)
-        if (cand_idx(ldcg_key(S + i)) == bt) atomicMin(&sh.ival[3], i);
+    for (int i = tid; i < a.F[acc]; i += kThreads) {
+      const int g = staged ? sh.look[a.foff[acc] + i] : a.guess[static_cast<size_t>(b) * sumF + a.foff[acc] + i];
+      if (g == bt) atomicMin(&sh.ival[3], i);
     }
     __syncthreads();
   }
   const int s_hit = (a.do_lookup && sh.ival[3] != kNone) ? a.foff[acc] + sh.ival[3] : -1;
-  if (tid <= a.K) {
+  for (int t = tid; t <= K; t += kThreads) {
     int v = -1;
-    if (tid < acc) v = sh.pos[tid].d;
-    if (tid == acc) v = bt;
-    a.out_tokens[static_cast<size_t>(b) * (a.K + 1) + tid] = v;
+    if (t < acc) v = sh.rec[t].d;
+    if (t == acc) v = bt;
+    a.out_tokens[static_cast<size_t>(b) * (K + 1) + t] = v;
   }
-  if (a.do_lookup && a.next_tokens && tid < a.K) {
-    int v = -1;
-    if (s_hit >= 0 && a.payload)
-      v = (pay && pay_staged(a)) ? pay[s_hit * a.K + tid]
-                                 : a.payload[(static_cast<size_t>(b) * a.foff[a.K + 1] + s_hit) * a.K + tid];
-    a.next_tokens[static_cast<size_t>(b) * a.K + tid] = v;
-  }
-  __syncthreads();
+  if (a.do_lookup && a.next_tokens)
+    for (int t = tid; t < K; t += kThreads) {
+      int v = -1;
+      if (s_hit >= 0 && a.payload)
+        v = staged ? sh.look[sumF + s_hit * K + t] : a.payload[(static_cast<size_t>(b) * sumF + s_hit) * K + t];
+      a.next_tokens[static_cast<size_t>(b) * K + t] = v;
+    }
   if (tid == 0) {
     if (zero) atomicOr(a.status, kFlagZeroResidual);
     a.accept_len[b] = acc;
@@ -1577,482 +1254,301 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
     if (a.resid_mass) a.resid_mass[b] = W;
     if (a.do_lookup) {
       if (a.slot_out) a.slot_out[b] = s_hit;
-      if (s_hit >= 0) atomicAdd(a.ctr + 1, 1u);
-    }
-    const uint32_t done = atom_add_release(a.ctr, 1u);
-    if (done + 1 == static_cast<uint32_t>(a.B) && a.hits) {
-      fence_acq_rel();
-      *a.hits = ld_relaxed(a.ctr + 1);
+      if (s_hit >= 0 && a.hits) atomicAdd(a.hits, 1u);
     }
   }
-  __syncthreads();
 }
 
-// The last pair of sequence b merged: chain, then (greedy, or every token
-// accepted) the bonus draw and the outputs; a residual draw is left to k_resid.
-template <class E>
-__device__ __forceinline__ void seq_finish(const VocabArgs &a, int b, Stage &st, Smem &sh) {
-  const int acc = stage_chain(a, b, nullptr, st.pay, &st, sh);
-  const bool resid = !a.greedy && acc < a.K;
-  if (threadIdx.x == 0) {
-    // the sequence's k_resid CTAs may go on (unless a pair merge's frontier
-    // already set the word: to the same value); the word carries the accept
-    // count + 2 (1: no residual draw)
-    fence_acq_rel();
-    atomicCAS(ready_word(a, b), 0u, static_cast<uint32_t>((resid ? acc : -1) + 2));
-  }
-  if (resid) return;
-  const RowInfo row = sh.rows[acc];
-  int bt = row.at;
-  float W = 1.f;
-  bool zero = false, near = false;
-  if (a.greedy) {
-    if (acc < a.K) {
-      W = (row.at != row.ad) ? 1.f : 0.f;
-      zero = !(W > 0.f);
-    }
-  } else {
-    bt = draw_target<E>(a, b, acc, row, a.u_bonus[b], acc == a.K ? &st : nullptr, sh);
-    near = threadIdx.x == 0 && sh.near;
-  }
-  emit(a, b, acc, bt, W, zero, near, st.pay, sh);
-}
-
-// The CTA's trace entry: (SM << 48 | kind << 40 | sequence << 20 | index),
-// then its seven marks (0 = not reached).
-SSD_DEV void trace_entry(unsigned long long *tr, int kind, int b, int idx, const unsigned long long *mk) {
-  uint32_t smid;
-  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-  tr[0] = (static_cast<unsigned long long>(smid) << 48) | (static_cast<unsigned long long>(kind) << 40) |
-          (static_cast<unsigned long long>(b & 0xFFFFF) << 20) | static_cast<unsigned long long>(idx & 0xFFFFF);
-#pragma unroll
-  for (int k = 0; k < 7; ++k) tr[1 + k] = mk[k];
-}
-
-// ===========================================================================
-// the kernels
-// ===========================================================================
-template <class E>
-__global__ void __launch_bounds__(kThreads, kStatsCtas) k_stats(const __grid_constant__ VocabArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t *buf = smem_raw;
-  Smem &sh = *reinterpret_cast<Smem *>(smem_raw + kChunkBytes);
-  // k_resid (if any) may start launching once every CTA of this grid has started
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int tid = threadIdx.x;
-  const int c = static_cast<int>(blockIdx.x), slot = static_cast<int>(blockIdx.y);
-  const int b = a.b0 + static_cast<int>(blockIdx.z);
-  const int rem = slot * a.nchunks + c;
-  const RowSlot rs = a.slot[slot];
-  // the chunk's whole vectors: one TMA bulk copy; thread 0 waits (bounded,
-  // sleeping between polls), the other threads at the barrier
-  if (tid == 0) {
-    if (a.trace)
-      for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
-    mark(a, sh.mk, 0);
-    const int e0 = c * a.chunk_elems;
-    const int n = min(a.chunk_elems, a.V - e0);
-    const uint32_t bulk = static_cast<uint32_t>((n * E::kSize) & ~15);
-    mbar_init(&sh.bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(&sh.bar, bulk);
-    if (bulk)
-      bulk_g2s(buf, row_ptr(a, rs.tensor, b, rs.row, E::kSize) + static_cast<int64_t>(e0) * E::kSize, bulk, &sh.bar);
-    // tickets, taken while the copy is in flight: the last CTA of a pair to
-    // start merges the pair, the last pair merger of a sequence to start
-    // finishes the sequence.  Each waits only for CTAs that started before it.
-    int role = 0;
-    if (atomicAdd(pair_tkt(a, b, rs.row), 1u) + 1 == static_cast<uint32_t>(a.pair_chunks[rs.row])) {
-      role = 1;
-      if (a.do_verify && atomicAdd(seq_tkt(a, b), 1u) + 1 == static_cast<uint32_t>(a.npairs)) role = 2;
-    }
-    sh.flag = role;
-    if (!mbar_wait_sleep(&sh.bar, 0)) {
-      atomicOr(a.status, kFlagWaitTimeout);
-      (void)mbar_wait_sleep(&sh.bar, 0);  // the copy still in flight: a second bounded wait before the buffer is read
-    }
-    mark(a, sh.mk, 1);
-  }
-  __syncthreads();
-  const int role = sh.flag;
-  stats_chunk<E>(a, b, slot, c, buf, sh);
-  const int r = rs.row;
-  __syncthreads();  // the chunk's records are written
-  mark(a, sh.mk, 2);
-  if (role == 0) {
-    if (tid == 0) red_add_release(pair_pub(a, b, r), 1u);
-  } else {
-    // merge pair r once its other chunks are published
-    if (tid == 0 && !wait_count(pair_pub(a, b, r), static_cast<uint32_t>(a.pair_chunks[r] - 1)))
-      atomicOr(a.status, kFlagWaitTimeout);
-    __syncthreads();
-    mark(a, sh.mk, 3);
-    Stage &st = *reinterpret_cast<Stage *>(buf);  // the chunk buffer is free again
-    row_finish<E>(a, b, r, st, sh);
-    mark(a, sh.mk, 4);
-    if (a.do_verify) {
-      __syncthreads();  // the pair's results are written
-      if (role == 1) {
-        if (tid == 0) red_add_release(seq_pub(a, b), 1u);
+// Residual pass over unit u (segments 8u .. 8u + 7, one per warp) of row
+// pair j of sequence b: per block the sums of max(0, p - q') and of p (lane
+// sums, then a scan: the arithmetic of warp_find), written to ublk when
+// `store`; the segment masses (warp_runs' arithmetic over the 8 blocks) into
+// sh.seg.  kMins: *mn, *mx (every lane) = the warp's sums of min(p, q') and
+// of max(0, p - q'), each lane in element order.  The warp's vectors are
+// staged in `st` first (all loads in flight at once), then reduced block by
+// block.
+template <class E, bool kMins>
+SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr, bool store, ResSh &sh, ResStage &st,
+                       float *mn_out, float *mx_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sg = u * kUnitSeg + warp;
+  const char *rowT = row_ptr(a, 0, b, j, E::kSize);
+  const char *rowD = row_ptr(a, 1, b, j, E::kSize);
+  float mn = 0.f, mx = 0.f, segr = 0.f, segp = 0.f;
+  if (sg < a.nseg) {
+    for (int k = 0; k < kSegBlocks; ++k) {
+      const int v = sg * kSegVec + 32 * k + lane;
+      if (v < a.nfull) {
+        cp_async16(&st.v[warp][0][k][lane], rowT + static_cast<int64_t>(v) * 16);
+        cp_async16(&st.v[warp][1][k][lane], rowD + static_cast<int64_t>(v) * 16);
       } else {
-        // a rejection the pair merges already resolved (ready word set) leaves
-        // the sequence to the residual draw: nothing is left to finish here
-        if (tid == 0) {
-          sh.flag = (!a.greedy && ld_relaxed(ready_word(a, b)) != 0u) ? 1 : 0;
-          if (!sh.flag && !wait_count(seq_pub(a, b), static_cast<uint32_t>(a.npairs - 1)))
-            atomicOr(a.status, kFlagWaitTimeout);
-        }
-        __syncthreads();
-        if (!sh.flag) seq_finish<E>(a, b, st, sh);
-        mark(a, sh.mk, 5);
+        st.v[warp][0][k][lane] = row_vec<E>(a, rowT, v);
+        st.v[warp][1][k][lane] = row_vec<E>(a, rowD, v);
       }
     }
-  }
-  const int kind = role == 2 ? 3 : role;
-  mark(a, sh.mk, 6);
-  if (a.trace && tid == 0)
-    trace_entry(a.trace + 8 * (static_cast<size_t>(b) * a.nslots * a.nchunks + rem), kind, b, rem, sh.mk);
-}
-
-// Thread 0 of a residual CTA: bounded wait (sleeping between polls) for a
-// sequence's ready word; returns it (0: the wait ran out).  k_resid is a
-// programmatic dependent launch that starts once every k_stats CTA has
-// started, so the word is set unless k_stats failed.
-SSD_DEV uint32_t wait_ready(const uint32_t *w) {
-  for (uint32_t it = 0; it < kMaxPolls; ++it) {
-    const uint32_t v = ld_relaxed(w);
-    if (v) {
-      fence_acq_rel();
-      return v;
+    cp_async_wait_all();
+    __syncwarp();
+    float vr = 0.f, vp = 0.f;  // lane k < 8: block k's sums
+#pragma unroll 1
+    for (int k = 0; k < kSegBlocks; ++k) {
+      const int i0 = (sg * kSegVec + 32 * k + lane) * E::kVec;
+      float ft[E::kVec], fd[E::kVec], xr[E::kVec], xp[E::kVec];
+      E::unpack(st.v[warp][0][k][lane], ft);
+      E::unpack(st.v[warp][1][k][lane], fd);
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e) {
+        if (i0 + e < a.V) {
+          const float p = wr.p(ft[e]), q = wr.q(fd[e], i0 + e);
+          const float r = __fsub_rn(p, q);
+          xr[e] = r > 0.f ? r : 0.f;
+          xp[e] = p;
+          if (kMins) {
+            mn = __fadd_rn(mn, fminf(p, q));
+            mx = __fadd_rn(mx, xr[e]);
+          }
+        } else {
+          xr[e] = xp[e] = 0.f;
+        }
+      }
+      const float br = __shfl_sync(0xffffffffu, warp_incl_scan(lane_sum<E::kVec>(xr)), 31);
+      const float bp = __shfl_sync(0xffffffffu, warp_incl_scan(lane_sum<E::kVec>(xp)), 31);
+      if (lane == k) {
+        vr = br;
+        vp = bp;
+      }
     }
-    __nanosleep(500);
+    segr = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? vr : 0.f), 31);
+    segp = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? vp : 0.f), 31);
+    if (store && lane < kSegBlocks) a.ublk[static_cast<size_t>(b) * a.nblk + sg * kSegBlocks + lane] = make_float2(vr, vp);
+    if (store && lane == 0) a.useg[static_cast<size_t>(b) * a.nseg + sg] = make_float2(segr, segp);
   }
-  return 0u;
+  if (lane == 0) {
+    sh.seg[warp][0] = segr;
+    sh.seg[warp][1] = segp;
+  }
+  if (kMins) {
+    *mn_out = warp_sum(mn);
+    *mx_out = warp_sum(mx);
+  }
 }
 
-// Residual unit (sequence b, chunk c, quarter g = rounds 2g, 2g+1): once the
-// sequence's acceptance chain has run, its block sums of max(0, p - q') over
-// target and draft row a, read straight from global memory.  The unit with the
-// sequence's last ticket draws the bonus once the others are published; it
-// issues its staging loads before its own unit.  `rbst`: the sequence's
-// residual block sums, staged for up to kResidStage chunks.
-constexpr int kResidStage = 16;
+// One warp, the last residual unit of sequence b: the bonus from max(0, p -
+// q') of pair acc (p when the residual has no mass): unit, segment, block,
+// then the element.  sh.um holds the unit masses and, when `staged`, sh.bl
+// every block sum.  Returns (every lane) the token (-1: no weight); sets *W
+// (the residual mass), *zero and *near.
 template <class E>
-SSD_DEV void resid_unit(const VocabArgs &a, float *umass, float *rbst, int32_t *pay, Smem &sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nu = a.nchunks * kQuarters;
-  const int b = static_cast<int>(blockIdx.x / nu);
-  const int u = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * nu);
-  const int c = u / kQuarters, g = u % kQuarters;
-  if (tid == 0) {
-    const uint32_t v = wait_ready(ready_word(a, b));
-    if (!v) atomicOr(a.status, kFlagWaitTimeout);
-    const int acc0 = static_cast<int>(v) - 2;
-    sh.flag = static_cast<int>(v);
-    sh.ival[2] = (v && acc0 >= 0 && acc0 < a.K && atomicAdd(res_tkt(a, b), 1u) + 1 == static_cast<uint32_t>(nu)) ? 1 : 0;
+SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, bool staged, ResSh &sh, float *W_out,
+                       bool *zero, bool *near) {
+  const int lane = threadIdx.x & 31;
+  const int U = a.nunits;
+  const float W0 = warp_total(sh.um[0], U);
+  *W_out = W0;
+  *zero = !(W0 > 0.f);
+  const int X = *zero ? 1 : 0;
+  float rem, W;
+  bool fb;
+  const int q = warp_locate(sh.um[X], U, a.u_bonus[b], false, &rem, &W, &fb);
+  *near = true;
+  if (q < 0) return -1;
+  const float2 *bl = a.ublk + static_cast<size_t>(b) * a.nblk;
+  for (int i = lane; i < kUnitSeg * kSegBlocks; i += 32) {
+    const int g = q * kUnitSeg * kSegBlocks + i;
+    const float2 v = (g < a.nblk) ? (staged ? sh.bl[g] : __ldcg(bl + g)) : make_float2(0.f, 0.f);
+    sh.bx[i] = X ? v.y : v.x;
   }
-  __syncthreads();
-  if (!sh.flag) return;
-  const int acc = sh.flag - 2;
-  if (acc < 0 || acc >= a.K) return;  // sequence finished in k_stats
-  const bool fin = sh.ival[2] != 0;
-  if (fin) stage_issue(a, b, pay, nullptr, false, sh);
-  if (tid == 0 && a.trace)
-    for (int k = 0; k < 7; ++k) sh.mk[k] = 0ull;
-  mark(a, sh.mk, 0);
+  if (lane < kUnitSeg) {  // the unit's segment masses, as the unit pass summed them
+    const int sg = q * kUnitSeg + lane;
+    const float2 v = (sg < a.nseg) ? __ldcg(a.useg + static_cast<size_t>(b) * a.nseg + sg) : make_float2(0.f, 0.f);
+    sh.sm[lane] = X ? v.y : v.x;
+  }
+  __syncwarp();
+  float rem2, W2, rem3, W3;
+  bool fb2, fb3;
+  const int s = warp_locate(sh.sm, kUnitSeg, rem, true, &rem2, &W2, &fb2);
+  if (s < 0) return -1;
+  const int k = warp_locate(sh.bx + s * kSegBlocks, kSegBlocks, rem2, true, &rem3, &W3, &fb3);
+  if (k < 0) return -1;
   const char *rowT = row_ptr(a, 0, b, acc, E::kSize);
   const char *rowD = row_ptr(a, 1, b, acc, E::kSize);
-  {  // this lane's vectors of the unit, on their way into L1 while the row's statistics load
-    const int e0 = c * a.chunk_elems;
-    const int n = min(a.chunk_elems, a.V - e0);
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      const int i0 = ((2 * g + jj) * kThreads + warp * 32 + lane) * E::kVec;
-      if (i0 + E::kVec <= n) {
-        const int64_t off = static_cast<int64_t>(e0 + i0) * E::kSize;
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(rowT + off));
-        asm volatile("prefetch.global.L1 [%0];" ::"l"(rowD + off));
+  const int g = (q * kUnitSeg + s) * kSegBlocks + k;
+  float dist;
+  int bt;
+  if (X) bt = warp_find<E>(a, rowT, nullptr, g, rem3, WProb{a.kT, wr.Mtk, wr.inv_st}, 0.f, &dist);
+  else bt = warp_find<E>(a, rowT, rowD, g, rem3, wr, 0.f, &dist);
+  *near = fb || fb2 || fb3 || bt < 0 || !(dist >= __fmul_rn(kNearTie, W));
+  return bt;
+}
+
+template <class E>
+__global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ VocabArgs a) {
+  __shared__ ResSh sh;
+  extern __shared__ __align__(16) uint8_t res_smem[];
+  ResStage &st = *reinterpret_cast<ResStage *>(res_smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = a.K;
+  const int U = a.nunits;
+  if (a.trace && tid == 0) {
+    for (int k = 0; k < 8; ++k) sh.mk[k] = 0ull;
+    sh.mk[1] = now_ns();
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // k_pair has completed
+  if (a.trace && tid == 0) sh.mk[2] = now_ns();
+  int b = 0, u = 0;
+  if (a.do_analytics) {
+    // unit u of pair j < K (K = 0: one CTA per sequence, finishing it):
+    // the sums of min(p, q') and of max(0, p - q')
+    const int per = K > 0 ? K * U : 1;
+    b = static_cast<int>(blockIdx.x) / per;
+    const int rest = static_cast<int>(blockIdx.x) - b * per;
+    const int j = K > 0 ? rest / U : 0;
+    u = K > 0 ? rest - j * U : 0;
+    int fin = K == 0 ? 1 : 0;
+    if (K > 0) {
+      float mn = 0.f, mx = 0.f;
+      if (!a.greedy) {
+        if (tid == 0) sh.rec[0] = a.rec[static_cast<size_t>(b) * (K + 1) + j];
+        __syncthreads();
+        const WResid wr = resid_weights(a, sh.rec[0], a.Fs[j]);
+        unit_pass<E, true>(a, b, j, u, wr, false, sh, st, &mn, &mx);
+        __syncthreads();  // sh.seg is overwritten below
       }
-    }
-  }
-  const size_t rr = static_cast<size_t>(b) * (a.K + 1) + acc;
-  const RowInfo row = ldcg_row(a.rows + rr);
-  const int F = a.Fs[acc];
-  const uint64_t keyF = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
-  const WResidual wf = residual_weights(a, row, keyF, F);
-  float *rbs = a.rbs + (static_cast<size_t>(b) * a.nchunks + c) * kBlocks;
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const int j = 2 * g + jj;
-    float x[E::kVec];
-    const float p = lane_weights<E, true, true>(a, rowT, rowD, c, j, warp, wf, x);
-    const float incl = warp_incl_scan(p);
-    if (lane == 31) {
-      rbs[j * kWarps + warp] = incl;
-      sh.bw[jj * kWarps + warp] = incl;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const float m = warp_total(sh.bw, 2 * kWarps);
-    if (lane == 0) a.rmass[static_cast<size_t>(b) * nu + u] = m;
-  }
-  mark(a, sh.mk, 2);
-  int kind = 2;
-  __syncthreads();  // the unit's sums are written
-  if (!fin) {
-    if (tid == 0) red_add_release(res_pub(a, b), 1u);
-  } else {
-    kind = 3;
-    if (tid == 0 && !wait_count(res_pub(a, b), static_cast<uint32_t>(nu - 1))) atomicOr(a.status, kFlagWaitTimeout);
-    __syncthreads();
-    mark(a, sh.mk, 3);
-    // the unit masses and (up to kResidStage chunks) every unit's block sums
-    for (int q = tid; q < nu; q += kThreads) cp_async4(&umass[q], a.rmass + static_cast<size_t>(b) * nu + q);
-    const bool rbs_staged = a.nchunks <= kResidStage;
-    if (rbs_staged) {
-      const int4 *src = reinterpret_cast<const int4 *>(a.rbs + static_cast<size_t>(b) * a.nchunks * kBlocks);
-      for (int i = tid; i < a.nchunks * (kBlocks / 4); i += kThreads) cp_async16(reinterpret_cast<int4 *>(rbst) + i, src + i);
-    }
-    const int acc2 = stage_complete(a, sh);  // the same chain: acc2 == acc
-    const RowInfo ra = sh.rows[acc2];
-    const WResidual wa = residual_weights(a, ra, sh.keyF[acc2], a.Fs[acc2]);
-    const float ub = a.u_bonus[b];
-    if (tid == 0) sh.near = 0;
-    if (warp == 0) {
-      locate(umass, nu, ub, false, sh);
-      __syncwarp();
-      const int uq = sh.ival[0];
-      const float local = sh.scal[1];
-      const float W = sh.scal[2];  // the residual's total mass
-      __syncwarp();
       if (lane == 0) {
-        sh.ival[6] = uq;
-        sh.scal[6] = W;
+        sh.seg[warp][0] = mn;
+        sh.seg[warp][1] = mx;
       }
-      if (uq >= 0) {
-        const size_t o = (static_cast<size_t>(uq / kQuarters)) * kBlocks + 2 * (uq % kQuarters) * kWarps;
-        if (lane < 2 * kWarps)
-          sh.bw[lane] = rbs_staged ? rbst[o + lane] : __ldcg(a.rbs + static_cast<size_t>(b) * a.nchunks * kBlocks + o + lane);
-        __syncwarp();
-        locate(sh.bw, 2 * kWarps, local, true, sh);
-        __syncwarp();
-        if (lane == 0 && sh.ival[0] < 0) {  // a unit of positive mass has a positive block; kept for safety
-          sh.ival[0] = 2 * kWarps - 1;
-          sh.scal[1] = local;
-          sh.near = 1;
-        }
-      }
-    }
-    __syncthreads();
-    mark(a, sh.mk, 4);
-    const int uq = sh.ival[6];
-    const float W = sh.scal[6];
-    int bt = -1;
-    bool near = false;  // thread 0
-    if (uq >= 0) {
-      const int k = sh.ival[0];
-      const float local2 = sh.scal[1];
-      int d = -1;
-      float dist = 0.f;
-      if (warp == 0)
-        d = warp_find<E, true, true>(a, rowT, rowD, uq / kQuarters, 2 * (uq % kQuarters) + k / kWarps, k % kWarps,
-                                     local2, wa, &dist);
       __syncthreads();
       if (tid == 0) {
-        sh.ival[4] = d;
-        near = sh.near || !(dist >= __fmul_rn(kNearTie, W));
-      }
-      __syncthreads();
-      bt = sh.ival[4];
-    }
-    const bool zero = uq < 0;  // no residual mass: p_{a+1} instead
-    if (bt < 0) {
-      bt = draw_target<E>(a, b, acc2, ra, ub, nullptr, sh);
-      near = tid == 0 && sh.near;
-    }
-    if (a.do_lookup) {
-      // the lookup lists, once the pair merge of position acc has written its list
-      if (tid == 0 && !wait_count(pos_verdict(a, b, acc), 3u)) atomicOr(a.status, kFlagWaitTimeout);
-      __syncthreads();
-      stage_lists(a, b, sh);
-      cp_async_wait_all();
-      __syncthreads();
-    }
-    mark(a, sh.mk, 5);
-    emit(a, b, acc2, bt, W, zero, near, pay, sh);
-  }
-  mark(a, sh.mk, 6);
-  if (a.trace && tid == 0) {
-    const size_t base = static_cast<size_t>(a.B) * a.nslots * a.nchunks;
-    trace_entry(a.trace + 8 * (base + blockIdx.x), kind, b, u, sh.mk);
-  }
-}
-
-template <class E>
-__global__ void __launch_bounds__(kThreads, 4) k_resid(const __grid_constant__ VocabArgs a) {
-  __shared__ Smem sh;
-  __shared__ float umass[kMaxChunks * kQuarters];  // the sequence's unit masses (final draw)
-  __shared__ int32_t pay[kPayStage];                // the sequence's cache payload (final draw)
-  __shared__ __align__(16) float rbst[kResidStage * kBlocks];  // the sequence's residual block sums (final draw)
-  resid_unit<E>(a, umass, rbst, pay, sh);
-  // the grid completes only after k_stats has: its first CTA waits for it
-  // before exiting
-  if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// ===========================================================================
-// round analytics: alpha_j, W_j, P(a = k), the hit rate, expected tokens
-// ===========================================================================
-// One CTA per (sequence b, position j = r + 1, unit u = chunk u / kQuarters,
-// rounds 2 (u % kQuarters) and the next) of row pair r < K, once the
-// statistics pass has merged the rows: the unit's sums of min(p, q') and of
-// max(0, p - q') (each lane in element order, then the warps by a fixed tree).
-template <class E>
-__global__ void __launch_bounds__(kThreads) k_alpha(const __grid_constant__ VocabArgs a) {
-  __shared__ float red[2][kWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nu = a.nchunks * kQuarters;
-  const long id = blockIdx.x;
-  const int u = static_cast<int>(id % nu);
-  const int r = static_cast<int>((id / nu) % a.K);
-  const int b = static_cast<int>(id / (static_cast<long>(nu) * a.K));
-  const size_t rr = static_cast<size_t>(b) * (a.K + 1) + r;
-  const RowInfo ri = ldcg_row(a.rows + rr);
-  const int F = a.Fs[r];
-  const uint64_t keyF = F > 0 ? ldcg_key(a.S + rr * a.Fcap + F - 1) : 0ull;
-  const WResidual wf = residual_weights(a, ri, keyF, F);  // p and q' factors
-  const char *rowT = row_ptr(a, 0, b, r, E::kSize);
-  const char *rowD = row_ptr(a, 1, b, r, E::kSize);
-  const int c = u / kQuarters, g = u % kQuarters;
-  const int e0 = c * a.chunk_elems;
-  const int n = min(a.chunk_elems, a.V - e0);
-  float smin = 0.f, sres = 0.f;
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const int i0 = ((2 * g + jj) * kThreads + warp * 32 + lane) * E::kVec;
-    float ft[E::kVec], fd[E::kVec];
-    ld_vec<E>(rowT, e0, n, i0, -__int_as_float(0x7f800000), ft);
-    ld_vec<E>(rowD, e0, n, i0, -__int_as_float(0x7f800000), fd);
-#pragma unroll
-    for (int e = 0; e < E::kVec; ++e) {
-      if (i0 + e >= n) continue;
-      const float p = __fmul_rn(ex2(__fmaf_rn(ft[e], wf.kT, -wf.mtk)), wf.inv_st);
-      const float f = (wf.hasS && cand_key(fd[e], e0 + i0 + e) >= wf.keyF) ? wf.fC : wf.f1;
-      const float q = __fmul_rn(ex2(__fmaf_rn(fd[e], wf.kT, -wf.mdk)), f);
-      smin = __fadd_rn(smin, fminf(p, q));
-      sres = __fadd_rn(sres, fmaxf(__fsub_rn(p, q), 0.f));
-    }
-  }
-  smin = warp_sum(smin);
-  sres = warp_sum(sres);
-  if (lane == 0) {
-    red[0][warp] = smin;
-    red[1][warp] = sres;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float m = 0.f, w = 0.f;
-    for (int k = 0; k < kWarps; ++k) {
-      m = __fadd_rn(m, red[0][k]);
-      w = __fadd_rn(w, red[1][k]);
-    }
-    float *o = a.amass + ((static_cast<size_t>(b) * a.K + r) * nu + u) * 2;
-    o[0] = m;
-    o[1] = w;
-  }
-}
-
-// One CTA per sequence, after k_alpha (T > 0) or straight after the
-// statistics pass (T = 0, where p and q' are one-hot at the argmaxes): alpha
-// and W per position, the chance that the bonus lands among the depth-k
-// guesses given a = k, P(a = k), the hit rate and the expected tokens.
-template <class E>
-__global__ void __launch_bounds__(kThreads) k_analytics(const __grid_constant__ VocabArgs a) {
-  __shared__ float s_alpha[kMaxK + 1], s_w[kMaxK + 1], s_hit[kMaxK + 1];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x;
-  const int nu = a.nchunks * kQuarters;
-  const int K = a.K;
-  // alpha_j and W_j: warp r % kWarps sums position r's units in order
-  for (int r = warp; r < K; r += kWarps) {
-    const size_t rr = static_cast<size_t>(b) * (K + 1) + r;
-    float al, w;
-    if (a.greedy) {
-      const RowInfo ri = ldcg_row(a.rows + rr);
-      al = (ri.at == ri.ad) ? 1.f : 0.f;
-      w = 1.f - al;
-    } else {
-      const float *m = a.amass + (static_cast<size_t>(b) * K + r) * nu * 2;
-      float sa = 0.f, sw = 0.f;
-      for (int u = lane; u < nu; u += 32) {
-        sa = __fadd_rn(sa, __ldcg(m + 2 * u));
-        sw = __fadd_rn(sw, __ldcg(m + 2 * u + 1));
-      }
-      al = warp_sum(sa);
-      w = warp_sum(sw);
-    }
-    if (lane == 0) {
-      s_alpha[r] = al;
-      s_w[r] = w;
-    }
-  }
-  __syncthreads();
-  // hit masses: warp k % kWarps over depth k's guesses (S_{k+1}, the top-F_k
-  // of draft row k), each weighted by the bonus distribution given a = k
-  for (int k = warp; k <= K; k += kWarps) {
-    const size_t rr = static_cast<size_t>(b) * (K + 1) + k;
-    const RowInfo ri = ldcg_row(a.rows + rr);
-    const int F = a.Fs[k];
-    const char *rowT = row_ptr(a, 0, b, k, E::kSize);
-    const bool resid = k < K && s_w[k] > 0.f;
-    float h = 0.f;
-    if (a.greedy) {
-      // the bonus is the target argmax (the residual of one-hot rows is that
-      // same one-hot whenever it has mass)
-      for (int i = lane; i < F; i += 32)
-        if (cand_idx(ldcg_key(a.S + rr * a.Fcap + i)) == ri.at) h = 1.f;
-      h = warp_max(h);
-    } else {
-      const float mtk = __fmul_rn(ri.mt, a.kT);
-      const float inv_st = __frcp_rn(ri.st);
-      const float mdk = __fmul_rn(ri.md, a.kT);
-      const float sN = __fmul_rn(ri.sd, norm_N(a.C, ri.sq));
-      const float fC = __fdiv_rn(a.C, sN);
-      for (int i = lane; i < F; i += 32) {
-        const uint64_t key = ldcg_key(a.S + rr * a.Fcap + i);
-        if (!key) continue;
-        const int d = cand_idx(key);
-        const float p = __fmul_rn(ex2(__fmaf_rn(E::ld(rowT, d), a.kT, -mtk)), inv_st);
-        float x = p;
-        if (resid) {  // every guess is in S, so q' carries the factor C
-          const float q = __fmul_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), fC);
-          x = fmaxf(__fsub_rn(p, q), 0.f);
+        float m = 0.f, x = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          m = __fadd_rn(m, sh.seg[w][0]);
+          x = __fadd_rn(x, sh.seg[w][1]);
         }
-        h = __fadd_rn(h, x);
+        a.amass[(static_cast<size_t>(b) * K + j) * U + u] = make_float2(m, x);
+        __threadfence();
+        if (atomicAdd(a.ctr + 2 + a.B + static_cast<size_t>(b) * K + j, 1u) + 1 == static_cast<uint32_t>(U)) {
+          __threadfence();
+          // alpha_j and W_j over the units in order; then this pair's ticket on the sequence
+          if (!a.greedy) {
+            float al = 0.f, W = 0.f;
+            const float2 *src = a.amass + (static_cast<size_t>(b) * K + j) * U;
+            for (int q = 0; q < U; ++q) {
+              const float2 v = __ldcg(src + q);
+              al = __fadd_rn(al, v.x);
+              W = __fadd_rn(W, v.y);
+            }
+            PairRec *dst = a.rec + static_cast<size_t>(b) * (K + 1) + j;
+            dst->al = al;
+            dst->W = W;
+          }
+          __threadfence();
+          fin = (atomicAdd(a.ctr + 2 + b, 1u) + 1 == static_cast<uint32_t>(K)) ? 1 : 0;
+          if (fin) __threadfence();
+        }
       }
-      h = warp_sum(h);
-      if (resid) h = __fdiv_rn(h, s_w[k]);
     }
-    if (lane == 0) s_hit[k] = h;
+    if (tid == 0 && fin) {
+      float run = 1.f, hit = 0.f, etok = 0.f;
+      for (int k = 0; k <= K; ++k) {
+        const PairRec *rp = a.rec + static_cast<size_t>(b) * (K + 1) + k;
+        const float al = __ldcg(&rp->al), W = __ldcg(&rp->W), hp = __ldcg(&rp->hp), hr = __ldcg(&rp->hr);
+        // the bonus given a = k follows r_{k+1} / W_{k+1} (p_{k+1} without residual mass), p_{K+1} for k = K
+        const float h = (k < K && W > 0.f) ? __fdiv_rn(hr, W) : hp;
+        const float pk = (k < K) ? __fmul_rn(run, W) : run;
+        if (k < K) run = __fmul_rn(run, al);
+        hit = __fmaf_rn(pk, h, hit);
+        etok = __fmaf_rn(pk, static_cast<float>(k + 1), etok);
+        a.an_p_accept[static_cast<size_t>(b) * (K + 1) + k] = pk;
+        if (a.an_hit_mass) a.an_hit_mass[static_cast<size_t>(b) * (K + 1) + k] = h;
+        if (k < K) {
+          if (a.an_alpha) a.an_alpha[static_cast<size_t>(b) * K + k] = al;
+          if (a.an_resid_w) a.an_resid_w[static_cast<size_t>(b) * K + k] = W;
+        }
+      }
+      a.an_hit_rate[b] = hit;
+      a.an_exp_tokens[b] = etok;
+    }
+  } else {
+    // verification: the sequence's records and acceptance chain; its lookup
+    // lists staged alongside (a finishing unit needs them)
+    b = static_cast<int>(blockIdx.x) / U;
+    u = static_cast<int>(blockIdx.x) - b * U;
+    const int sumF = a.foff[K + 1];
+    const bool staged = a.do_lookup && sumF * (K + 1) <= kLookupStage;
+    for (int i = tid; i < a.npairs * 4; i += kThreads)
+      cp_async16(reinterpret_cast<int4 *>(sh.rec) + i, reinterpret_cast<const int4 *>(a.rec + static_cast<size_t>(b) * (K + 1)) + i);
+    for (int t = tid; t < K; t += kThreads) sh.u[t] = a.u_acc[static_cast<size_t>(b) * K + t];
+    if (staged) {
+      for (int i = tid; i < sumF; i += kThreads) cp_async4(&sh.look[i], a.guess + static_cast<size_t>(b) * sumF + i);
+      if (a.payload && a.next_tokens)
+        for (int i = tid; i < sumF * K; i += kThreads)
+          cp_async4(&sh.look[sumF + i], a.payload + static_cast<size_t>(b) * sumF * K + i);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (a.trace && tid == 0) sh.mk[3] = now_ns();
+    int acc = 0;
+    while (acc < K && (sh.rec[acc].fl & kRecAccepted)) ++acc;
+    if (a.greedy || acc == K) {
+      if (u == 0) {
+        const PairRec &r = sh.rec[acc];
+        emit(a, b, acc, r.bt, r.W, (r.fl & kRecZero) != 0, (r.fl & kRecBonusNear) != 0, staged, sh);
+      }
+    } else {
+      // the residual of the first rejected position: this unit's block sums
+      const WResid wr = resid_weights(a, sh.rec[acc], a.Fs[acc]);
+      float mn, mx;
+      unit_pass<E, false>(a, b, acc, u, wr, true, sh, st, &mn, &mx);
+      __syncthreads();
+      if (a.trace && tid == 0) sh.mk[4] = now_ns();
+      if (warp == 0) {
+        const float ir = warp_incl_scan(lane < kWarps ? sh.seg[lane][0] : 0.f);
+        const float ip = warp_incl_scan(lane < kWarps ? sh.seg[lane][1] : 0.f);
+        if (lane == 31) {
+          a.umass[static_cast<size_t>(b) * U + u] = make_float2(ir, ip);
+          __threadfence();
+          const uint32_t t = atomicAdd(a.ctr + 2 + b, 1u);
+          sh.ival[0] = (t + 1 == static_cast<uint32_t>(U)) ? 1 : 0;
+          if (sh.ival[0]) __threadfence();
+        }
+      }
+      __syncthreads();
+      if (a.trace && tid == 0) sh.mk[5] = now_ns();
+      if (sh.ival[0]) {
+        // the last unit: the bonus; the unit masses and (when they fit) every
+        // block sum in one round of loads
+        const bool bstaged = a.nblk <= kBlkStage;
+        for (int q = tid; q < U; q += kThreads) {
+          const float2 v = __ldcg(a.umass + static_cast<size_t>(b) * U + q);
+          sh.um[0][q] = v.x;
+          sh.um[1][q] = v.y;
+        }
+        if (bstaged)
+          for (int i = tid; i < a.nblk; i += kThreads) sh.bl[i] = __ldcg(a.ublk + static_cast<size_t>(b) * a.nblk + i);
+        __syncthreads();
+        if (warp == 0) {
+          float W;
+          bool zero, near;
+          int bt = resid_draw<E>(a, b, acc, wr, bstaged, sh, &W, &zero, &near);
+          if (bt < 0) {  // no weight at all: the target argmax
+            bt = sh.rec[acc].bt;
+            near = true;
+          }
+          if (lane == 0) {
+            sh.ival[1] = bt;
+            sh.ival[2] = (near ? 1 : 0) | (zero ? 2 : 0);
+            sh.scal[0] = W;
+          }
+        }
+        __syncthreads();
+        if (a.trace && tid == 0) sh.mk[6] = now_ns();
+        emit(a, b, acc, sh.ival[1], sh.scal[0], (sh.ival[2] & 2) != 0, (sh.ival[2] & 1) != 0, staged, sh);
+      }
+    }
   }
-  __syncthreads();
-  if (tid == 0) {
-    float run = 1.f, hit = 0.f, etok = 0.f;
-    for (int k = 0; k <= K; ++k) {
-      const float pk = (k < K) ? __fmul_rn(run, s_w[k]) : run;
-      if (k < K) run = __fmul_rn(run, s_alpha[k]);
-      hit = __fmaf_rn(pk, s_hit[k], hit);
-      etok = __fmaf_rn(pk, static_cast<float>(k + 1), etok);
-      a.an_p_accept[static_cast<size_t>(b) * (K + 1) + k] = pk;
-      if (a.an_hit_mass) a.an_hit_mass[static_cast<size_t>(b) * (K + 1) + k] = s_hit[k];
-      if (k < K) {
-        if (a.an_alpha) a.an_alpha[static_cast<size_t>(b) * K + k] = s_alpha[k];
-        if (a.an_resid_w) a.an_resid_w[static_cast<size_t>(b) * K + k] = s_w[k];
-      }
-    }
-    a.an_hit_rate[b] = hit;
-    a.an_exp_tokens[b] = etok;
+  if (a.trace && tid == 0) {
+    sh.mk[7] = now_ns();
+    trace_entry(a, a.trace_resid + blockIdx.x, 2, b, u, sh.mk);
   }
 }
 
@@ -2106,9 +1602,8 @@ using namespace ssd;
 namespace {
 
 struct Layout {
-  int nslots, nchunks, chunk_elems, Fcap;
-  size_t ctr_words;
-  size_t ctr_off, stats_off, blk_off, bmk_off, rows_off, S_off, pos_off, rmass_off, rbs_off, amass_off, total;
+  int nvec, nfull, nseg, nblk, nunits;
+  size_t ctr_words, ctr_off, seg_off, bsum_off, bkey_off, rec_off, umass_off, ublk_off, useg_off, amass_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -2117,40 +1612,39 @@ int esize(ssd_dtype_t dt) { return dt == SSD_F32 ? 4 : 2; }
 bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *L) {
   if (B < 0 || K < 0 || K > kMaxK || V < 1 || !F) return false;
   if (dt != SSD_F32 && dt != SSD_BF16) return false;
-  int fmax = 0;
-  for (int k = 0; k <= K; ++k) {
+  for (int k = 0; k <= K; ++k)
     if (F[k] < 0 || F[k] > kMaxF || F[k] > V) return false;
-    fmax = F[k] > fmax ? F[k] : fmax;
-  }
-  L->nslots = 2 * (K + 1);
-  L->chunk_elems = kChunkBytes / esize(dt);
-  L->nchunks = (V + L->chunk_elems - 1) / L->chunk_elems;
-  if (L->nchunks > kMaxChunks) return false;
-  L->Fcap = fmax > 0 ? fmax : 1;
+  const long long bytes = static_cast<long long>(V) * esize(dt);
+  const long long nvec = (bytes + 15) / 16;
+  const long long nseg = (nvec + kSegVec - 1) / kSegVec;
+  if (nseg > kMaxSeg) return false;
+  L->nvec = static_cast<int>(nvec);
+  L->nfull = static_cast<int>(bytes / 16);
+  L->nseg = static_cast<int>(nseg);
+  L->nblk = L->nseg * kSegBlocks;
+  L->nunits = (L->nseg + kUnitSeg - 1) / kUnitSeg;
   const size_t Bn = static_cast<size_t>(B > 0 ? B : 1);
-  const size_t nrec = Bn * L->nslots * L->nchunks;
-  L->ctr_words = ctr_words(Bn, K);
+  const size_t slots = Bn * 2 * (K + 1);
+  L->ctr_words = 2 + Bn + Bn * K;
   size_t o = 0;
   L->ctr_off = o;
   o = align_up(o + L->ctr_words * sizeof(uint32_t), 256);
-  L->stats_off = o;
-  o = align_up(o + nrec * sizeof(ChunkStat), 256);
-  L->blk_off = o;
-  o = align_up(o + nrec * sizeof(BlockRec), 256);
-  L->bmk_off = o;
-  o = align_up(o + nrec * kBlocks * sizeof(uint32_t), 256);
-  L->rows_off = o;
-  o = align_up(o + Bn * (K + 1) * sizeof(RowInfo), 256);
-  L->S_off = o;
-  o = align_up(o + Bn * (K + 1) * L->Fcap * sizeof(uint64_t), 256);
-  L->pos_off = o;
-  o = align_up(o + Bn * (K > 0 ? K : 1) * sizeof(PosInfo), 256);
-  L->rmass_off = o;
-  o = align_up(o + Bn * L->nchunks * kQuarters * sizeof(float), 256);
-  L->rbs_off = o;
-  o = align_up(o + Bn * L->nchunks * kBlocks * sizeof(float), 256);
+  L->seg_off = o;
+  o = align_up(o + slots * L->nseg * sizeof(SegRec), 256);
+  L->bsum_off = o;
+  o = align_up(o + slots * L->nblk * sizeof(float), 256);
+  L->bkey_off = o;
+  o = align_up(o + slots * L->nblk * sizeof(uint32_t), 256);
+  L->rec_off = o;
+  o = align_up(o + Bn * (K + 1) * sizeof(PairRec), 256);
+  L->umass_off = o;
+  o = align_up(o + Bn * L->nunits * sizeof(float2), 256);
+  L->ublk_off = o;
+  o = align_up(o + Bn * L->nblk * sizeof(float2), 256);
+  L->useg_off = o;
+  o = align_up(o + Bn * L->nseg * sizeof(float2), 256);
   L->amass_off = o;
-  o = align_up(o + Bn * (K > 0 ? K : 1) * L->nchunks * kQuarters * 2 * sizeof(float), 256);
+  o = align_up(o + Bn * (K > 0 ? K : 1) * L->nunits * sizeof(float2), 256);
   L->total = o;
   return true;
 }
@@ -2195,9 +1689,11 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.B = B;
   a.K = K;
   a.V = V;
-  a.nchunks = L.nchunks;
-  a.chunk_elems = L.chunk_elems;
-  a.Fcap = L.Fcap;
+  a.nvec = L.nvec;
+  a.nfull = L.nfull;
+  a.nseg = L.nseg;
+  a.nblk = L.nblk;
+  a.nunits = L.nunits;
   a.greedy = (T == 0.f);
   a.kT = a.greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   a.C = C;
@@ -2210,49 +1706,47 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.foff[K + 1] = off;
   char *w = static_cast<char *>(ws);
   a.ctr = reinterpret_cast<uint32_t *>(w + L.ctr_off);
-  a.stats = reinterpret_cast<ChunkStat *>(w + L.stats_off);
-  a.bmk = reinterpret_cast<uint32_t *>(w + L.bmk_off);
-  a.rows = reinterpret_cast<RowInfo *>(w + L.rows_off);
-  a.S = reinterpret_cast<uint64_t *>(w + L.S_off);
-  a.pos = reinterpret_cast<PosInfo *>(w + L.pos_off);
-  a.blk = reinterpret_cast<BlockRec *>(w + L.blk_off);
-  a.rmass = reinterpret_cast<float *>(w + L.rmass_off);
-  a.rbs = reinterpret_cast<float *>(w + L.rbs_off);
-  a.amass = reinterpret_cast<float *>(w + L.amass_off);
+  a.seg = reinterpret_cast<SegRec *>(w + L.seg_off);
+  a.bsum = reinterpret_cast<float *>(w + L.bsum_off);
+  a.bkey = reinterpret_cast<uint32_t *>(w + L.bkey_off);
+  a.rec = reinterpret_cast<PairRec *>(w + L.rec_off);
+  a.umass = reinterpret_cast<float2 *>(w + L.umass_off);
+  a.ublk = reinterpret_cast<float2 *>(w + L.ublk_off);
+  a.useg = reinterpret_cast<float2 *>(w + L.useg_off);
+  a.amass = reinterpret_cast<float2 *>(w + L.amass_off);
   a.status = status;
   return a;
 }
 
-// Rows read by a call: target rows 0..ntarget-1 and draft rows 0..ndraft-1,
-// slots ordered by pair (target r, then draft r).  `topf`: draft rows keep
-// their top-F_r lists.
-void set_slots(VocabArgs &a, int ntarget, int ndraft, bool topf, bool draws) {
-  int n = 0;
+// Rows read per position: target rows 0..ntarget-1 and draft rows 0..ndraft-1
+// (slots ordered by pair: target j, then draft j); `topf`: the draft rows
+// build their top-F_j lists.  Call after the do_* flags are set.
+void set_rows(VocabArgs &a, int ntarget, int ndraft, bool topf) {
   a.npairs = ntarget > ndraft ? ntarget : ndraft;
-  for (int r = 0; r <= a.K; ++r) {
-    a.tsl[r] = a.dsl[r] = -1;
-    a.pair_chunks[r] = 0;
-    a.Fs[r] = (topf && r < ndraft) ? a.F[r] : 0;
+  int n = 0;
+  for (int j = 0; j <= a.K; ++j) {
+    a.tsl[j] = a.dsl[j] = -1;
+    a.Fs[j] = (topf && j < ndraft) ? a.F[j] : 0;
   }
-  for (int r = 0; r < a.npairs; ++r) {
-    int rows = 0;
-    if (r < ntarget) {
-      a.tsl[r] = n;
-      // block sums on the rows a draw may use: target row K (the bonus after
-      // full acceptance) and the draft rows sampled from (d_{r+1})
-      const bool blk = draws && a.do_verify && r == a.K;
-      a.slot[n++] = RowSlot{0, static_cast<int16_t>(r), 0, static_cast<int16_t>(blk)};
-      ++rows;
+  const bool draws = !a.greedy;
+  for (int j = 0; j < a.npairs; ++j) {
+    if (j < ntarget) {
+      a.tsl[j] = n;
+      // block sums on the rows a draw reads: target row K+1 (the bonus after
+      // full acceptance) and the draft rows sampled from
+      const bool blk = draws && a.do_verify && j == a.K;
+      a.slot[n++] = RowSlot{0, static_cast<int16_t>(j), 0, static_cast<uint8_t>(blk), static_cast<uint8_t>(a.greedy),
+                            0};
     }
-    if (r < ndraft) {
-      a.dsl[r] = n;
-      const bool blk = draws && a.do_sample && r < a.K;
-      a.slot[n++] = RowSlot{1, static_cast<int16_t>(r), static_cast<int16_t>(a.Fs[r]), static_cast<int16_t>(blk)};
-      ++rows;
+    if (j < ndraft) {
+      a.dsl[j] = n;
+      const bool blk = draws && a.do_sample && j < a.K;
+      a.slot[n++] = RowSlot{1, static_cast<int16_t>(j), static_cast<uint8_t>(a.Fs[j] >= 2), static_cast<uint8_t>(blk),
+                            static_cast<uint8_t>(a.greedy || a.Fs[j] == 1), 0};
     }
-    a.pair_chunks[r] = rows * a.nchunks;
   }
   a.nslots = n;
+  if (a.greedy) a.nunits = 1;  // no residual pass: one finishing unit per sequence
 }
 
 // Optional timing hook (ssd_set_timing_events): events recorded around the
@@ -2263,84 +1757,79 @@ cudaEvent_t g_ev_after = nullptr;
 void *g_trace = nullptr;
 size_t g_trace_bytes = 0;
 
-constexpr size_t kStatsSmem = kChunkBytes + sizeof(Smem);
-static_assert(kStatsCtas * (kStatsSmem + 1024) <= 228 * 1024, "shared memory of k_stats too large for its CTAs/SM");
-
 ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
 
 constexpr int kMaxDevices = 64;
-std::atomic<uint64_t> g_smem_attr_set[2][kMaxDevices / 64 + 1];
+std::atomic<uint64_t> g_attr_set[2][kMaxDevices / 64 + 1];
 
+// A launch that may begin while the previous kernel on the stream drains
+// (its CTAs wait for that kernel with griddepcontrol.wait).
+template <class Kern>
+cudaError_t launch_dependent(Kern kern, unsigned grid, size_t smem, cudaStream_t s, const VocabArgs &a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// k_stats over every (chunk of 8 segments, row slot, sequence), then k_pair
+// (one CTA per sequence and row pair) and, when verifying or for the
+// analytics, k_resid.
 template <class E>
 cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   constexpr int ti = E::kSize == 4 ? 0 : 1;
+  if (a.B < 1 || a.npairs < 1) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const size_t psmem = pair_smem_bytes(a.nseg, a.nblk);
   const uint64_t bit = 1ull << (dev % 64);
-  if (!(g_smem_attr_set[ti][dev / 64].load() & bit)) {
-    e = cudaFuncSetAttribute(k_stats<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStatsSmem));
+  if (!(g_attr_set[ti][dev / 64].load() & bit)) {
+    e = cudaFuncSetAttribute(k_pair<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pair_smem_bytes(kMaxSeg, kMaxSeg * kSegBlocks)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_resid<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(ResStage)));
     if (e != cudaSuccess) return e;
-    g_smem_attr_set[ti][dev / 64].fetch_or(bit);
+    g_attr_set[ti][dev / 64].fetch_or(bit);
   }
-  const long n1 = static_cast<long>(a.B) * a.nslots * a.nchunks;
-  const long n2 = (a.do_verify && !a.greedy && a.K > 0) ? static_cast<long>(a.B) * a.nchunks * kQuarters : 0;
-  if (n1 < 1) return cudaSuccess;
-  if (n1 > 0x7fffffffL) return cudaErrorInvalidValue;
-  a.nst = n1;
-  a.trace = (g_trace && g_trace_bytes >= static_cast<size_t>(n1 + n2) * 64)
+  const unsigned nchunks = static_cast<unsigned>((a.nseg + kUnitSeg - 1) / kUnitSeg);
+  const long n1 = static_cast<long>(nchunks) * a.nslots * a.B;
+  const long n2 = static_cast<long>(a.B) * a.npairs;
+  const bool resid = a.do_verify || a.do_analytics;
+  const long n3 = !resid ? 0 : (a.do_analytics ? static_cast<long>(a.B) * (a.K > 0 ? a.K * a.nunits : 1)
+                                               : static_cast<long>(a.B) * a.nunits);
+  if (n2 > 0x7fffffffL || n3 > 0x7fffffffL) return cudaErrorInvalidValue;
+  a.trace = (g_trace && a.B <= 65535 && g_trace_bytes >= static_cast<size_t>(n1 + n2 + n3) * 64)
                 ? static_cast<unsigned long long *>(g_trace)
                 : nullptr;
-  // counters start at zero
-  e = cudaMemsetAsync(a.ctr, 0, ctr_words(static_cast<size_t>(a.B), a.K) * sizeof(uint32_t), s);
-  if (e != cudaSuccess) return e;
+  a.trace_pair = n1;
+  a.trace_resid = n1 + n2;
   if (g_ev_before) cudaEventRecord(g_ev_before, s);
   // grid (chunk, row slot, sequence); sequences in launches of at most 65535
   for (int b0 = 0; b0 < a.B; b0 += 65535) {
     a.b0 = b0;
     const unsigned nb = static_cast<unsigned>(a.B - b0 < 65535 ? a.B - b0 : 65535);
-    k_stats<E><<<dim3(static_cast<unsigned>(a.nchunks), static_cast<unsigned>(a.nslots), nb), kThreads, kStatsSmem,
-                 s>>>(a);
+    k_stats<E><<<dim3(nchunks, static_cast<unsigned>(a.nslots), nb), kThreads, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   a.b0 = 0;
   if (g_ev_after) cudaEventRecord(g_ev_after, s);
-  if (n2 > 0) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(n2));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_resid<E>, a);
-  }
-  return e;
+  e = launch_dependent(k_pair<E>, static_cast<unsigned>(n2), psmem, s, a);
+  if (e != cudaSuccess || n3 == 0) return e;
+  return launch_dependent(k_resid<E>, static_cast<unsigned>(n3), sizeof(ResStage), s, a);
 }
 
 cudaError_t launch_any(ssd_dtype_t dt, VocabArgs &a, cudaStream_t s) {
   return dt == SSD_F32 ? launch_vocab<EF32>(a, s) : launch_vocab<EBF16>(a, s);
-}
-
-// The analytics kernels after the statistics pass: the unit sums of every
-// row pair r < K (T > 0), then one CTA per sequence.
-template <class E>
-cudaError_t launch_analytics(const VocabArgs &a, cudaStream_t s) {
-  if (a.B < 1) return cudaSuccess;
-  if (!a.greedy && a.K > 0) {
-    const long n = static_cast<long>(a.B) * a.K * a.nchunks * kQuarters;
-    if (n > 0x7fffffffL) return cudaErrorInvalidValue;
-    k_alpha<E><<<static_cast<unsigned>(n), kThreads, 0, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  k_analytics<E><<<static_cast<unsigned>(a.B), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
 }
 
 // Fixed device scratch for ssd_verify_noalloc: one array per GPU that loads
@@ -2461,7 +1950,7 @@ ssd_status_t ssd_saguaro_sample(const void *draft, ssd_dtype_t dt, int64_t seq_s
   if (!u_draft || !d_out || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(draft, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
   a.do_sample = 1;
-  set_slots(a, 0, K, C < 1.f, !a.greedy);
+  set_rows(a, 0, K, C < 1.f);
   a.u_draft = u_draft;
   a.d_out = d_out;
   a.qd_out = qd_out;
@@ -2486,7 +1975,7 @@ ssd_status_t ssd_verify(const void *target, const void *draft, ssd_dtype_t dt, i
     return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(target, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
   a.do_verify = 1;
-  set_slots(a, K + 1, K, C < 1.f, !a.greedy);
+  set_rows(a, K + 1, K, C < 1.f);
   a.d_in = d;
   a.u_acc = u_acc;
   a.u_bonus = u_bonus;
@@ -2513,7 +2002,7 @@ ssd_status_t ssd_predict_outcomes(const void *draft, ssd_dtype_t dt, int64_t seq
   if (!guess || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(draft, draft, seq_stride, row_stride, B, K, V, F, 1.f, T, L, ws, status);
   a.do_predict = 1;
-  set_slots(a, 0, K + 1, true, false);
+  set_rows(a, 0, K + 1, true);
   a.guess = guess;
   a.guess_q = guess_q;
   return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
@@ -2581,14 +2070,13 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
   a.do_verify = 1;
   a.do_predict = guess != nullptr;
   a.do_lookup = guess != nullptr;
-  set_slots(a, K + 1, a.do_predict ? K + 1 : K, a.do_predict || C < 1.f, !a.greedy);
+  set_rows(a, K + 1, a.do_predict ? K + 1 : K, a.do_predict || C < 1.f);
   a.u_draft = u_draft;
   a.u_acc = u_acc;
   a.u_bonus = u_bonus;
   a.payload = payload;
   a.d_out = d_out;
   a.qd_out = qd_out;
-  a.d_in = d_out;
   a.accept_len = accept_len;
   a.out_tokens = out_tokens;
   a.bonus = bonus;
@@ -2619,17 +2107,14 @@ ssd_status_t ssd_round_analytics(const void *target, const void *draft, ssd_dtyp
   if (!p_accept || !hit_rate || !exp_tokens || !status) return SSD_ERR_INVALID_ARG;
   VocabArgs a = base_args(target, draft, seq_stride, row_stride, B, K, V, F, C, T, L, ws, status);
   a.do_analytics = 1;
-  set_slots(a, K + 1, K + 1, true, false);
+  set_rows(a, K + 1, K + 1, true);
   a.an_alpha = alpha;
   a.an_resid_w = resid_w;
   a.an_p_accept = p_accept;
   a.an_hit_mass = hit_mass;
   a.an_hit_rate = hit_rate;
   a.an_exp_tokens = exp_tokens;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  cudaError_t e = launch_any(dt, a, cs);
-  if (e == cudaSuccess) e = dt == SSD_F32 ? launch_analytics<EF32>(a, cs) : launch_analytics<EBF16>(a, cs);
-  return cuda_status(e);
+  return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
 }
 
 size_t ssd_verify_noalloc_max_bytes(void) { return kStaticScratchBytes; }
