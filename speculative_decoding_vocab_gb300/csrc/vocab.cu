@@ -51,9 +51,10 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSegVec = 256;                   // 16-byte vectors per segment (one warp)
 constexpr int kSegBlocks = 8;                  // blocks of 32 vectors per segment
-constexpr int kUnitSeg = kWarps;               // segments per k_stats CTA and per residual unit
+constexpr int kUnitSeg = kWarps;               // segments per k_stats CTA
+constexpr int kResSeg = kWarps / 2;            // segments per residual unit (two warps per segment)
 constexpr int kMaxSeg = 1024;                  // rows of at most 4 MiB
-constexpr int kMaxUnits = kMaxSeg / kUnitSeg;  // 128
+constexpr int kMaxUnits = kMaxSeg / kResSeg;   // 256
 constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
 constexpr int kMaxF = 256;
@@ -127,7 +128,6 @@ struct VocabArgs {
   uint32_t *bkey;  // [B][nslots][nblk]
   PairRec *rec;    // [B][K+1]
   float2 *umass;   // residual units: [B][nunits] masses of max(0, p - q') and of p
-  float2 *ublk;    // residual block sums: [B][nblk]
   float2 *useg;    // residual segment masses: [B][nseg]
   float2 *amass;   // analytics units: [B][K][nunits] sums of min(p, q') and max(0, p - q')
   // inputs / outputs
@@ -682,22 +682,29 @@ SSD_DEV void block_candidates(const VocabArgs &a, const char *row, int g, uint32
   }
 }
 
+// The warps of k_pair that select the top-F list (warp 0 draws meanwhile):
+// warps 1..7, synchronised by named barrier 1.
+constexpr int kTopWarps = kWarps - 1;
+constexpr int kTopThreads = kTopWarps * 32;
+SSD_DEV void top_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTopThreads) : "memory"); }
+
 // Top-F of n distinct nonzero keys by rank (the key with r larger keys goes
-// to dst[r] when r < F); slots past n are set to 0.  No barrier inside.
+// to dst[r] when r < F); slots past n are set to 0.  The top-F warps; no
+// barrier inside.
 SSD_DEV void rank_select(const uint64_t *keys, int n, int F, uint64_t *dst) {
-  for (int i = threadIdx.x; i < F; i += kThreads)
+  const int gt = threadIdx.x - 32, gw = gt >> 5, lane = threadIdx.x & 31;
+  for (int i = gt; i < F; i += kTopThreads)
     if (i >= n) dst[i] = 0ull;
   if (n <= 64) {
-    const int lane = threadIdx.x & 31;
     const uint64_t a0 = lane < n ? keys[lane] : 0ull, a1 = lane + 32 < n ? keys[lane + 32] : 0ull;
-    for (int i = threadIdx.x >> 5; i < n; i += kWarps) {
+    for (int i = gw; i < n; i += kTopWarps) {
       const uint64_t k = keys[i];
       const int rank = __popc(__ballot_sync(0xffffffffu, a0 > k)) + __popc(__ballot_sync(0xffffffffu, a1 > k));
       if (lane == 0 && rank < F) dst[rank] = k;
     }
     return;
   }
-  for (int i = threadIdx.x; i < n; i += kThreads) {
+  for (int i = gt; i < n; i += kTopThreads) {
     const uint64_t k = keys[i];
     int rank = 0;
     for (int j = 0; j < n && rank < F; ++j) rank += (keys[j] > k) ? 1 : 0;
@@ -757,56 +764,55 @@ SSD_DEV void find_bucket(const uint32_t *hist, int need, uint32_t &bucket_out, i
 }
 
 // The top-F (F > 1) of a draft row into sh.S (descending; zeros past the
-// row's elements).  t16 = the 16-bit key prefix of the F-th largest block
-// maximum (two levels of 256-bucket counts): at least F elements reach it,
-// so the row's top-F all lie in blocks whose maximum does.  Those blocks are
-// read again (one warp per block) and their elements reaching t16 ranked;
-// when ties overflow the buffers, F sweeps of a CTA maximum instead.  Every
-// thread calls.
+// row's elements), by the top-F warps.  t16 = the 16-bit key prefix of the
+// F-th largest block maximum (two levels of 256-bucket counts): at least F
+// elements reach it, so the row's top-F all lie in blocks whose maximum does.
+// Those blocks are read again (one warp per block) and their elements
+// reaching t16 ranked; when ties overflow the buffers, F sweeps of a group
+// maximum instead.
 template <class E>
 SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t *keys, PairSh &sh) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gt = threadIdx.x - 32, gw = gt >> 5, lane = threadIdx.x & 31;
   const int nb = a.nblk;
   auto count = [&](uint32_t *hist, bool v, uint32_t bucket) {
     const uint32_t peers = __match_any_sync(0xffffffffu, v ? bucket : 0xFFFFFFFFu);
     if (v && lane == __ffs(peers) - 1) atomicAdd(&hist[bucket], static_cast<uint32_t>(__popc(peers)));
   };
-  sh.hist[0][tid] = 0u;
-  sh.hist[1][tid] = 0u;
-  if (tid == 0) {
+  for (int i = gt; i < 512; i += kTopThreads) sh.hist[i >> 8][i & 255] = 0u;
+  if (gt == 0) {
     sh.ncand = 0;
     sh.nblist = 0;
   }
-  __syncthreads();
-  for (int i0 = warp * 32; i0 < nb; i0 += kThreads) {
+  top_sync();
+  for (int i0 = gw * 32; i0 < nb; i0 += kTopThreads) {
     const uint32_t k = (i0 + lane < nb) ? keys[i0 + lane] : 0u;
     count(sh.hist[0], k != 0u, k >> 24);
   }
-  __syncthreads();
+  top_sync();
   uint32_t b1, b2;
   int above, above2;
   find_bucket(sh.hist[0], F, b1, above);
-  for (int i0 = warp * 32; i0 < nb; i0 += kThreads) {
+  for (int i0 = gw * 32; i0 < nb; i0 += kTopThreads) {
     const uint32_t k = (i0 + lane < nb) ? keys[i0 + lane] : 0u;
     count(sh.hist[1], k != 0u && (k >> 24) == b1, (k >> 16) & 0xFFu);
   }
-  __syncthreads();
+  top_sync();
   find_bucket(sh.hist[1], F - above, b2, above2);
   const uint32_t t16 = (b1 << 8) | b2;
   constexpr int kListCap = 2 * kCandCap;
-  for (int i = tid; i < nb; i += kThreads) {
+  for (int i = gt; i < nb; i += kTopThreads) {
     const uint32_t k = keys[i];
     if (k && (k >> 16) >= t16) {
       const int p = atomicAdd(&sh.nblist, 1);
       if (p < kListCap) sh.blist[p] = i;
     }
   }
-  __syncthreads();
+  top_sync();
   const int nbl = sh.nblist;
   const bool listed = nbl <= kListCap;
   if (listed)
-    for (int q = warp; q < nbl; q += kWarps) block_candidates<E>(a, row, sh.blist[q], t16, sh);
-  __syncthreads();
+    for (int q = gw; q < nbl; q += kTopWarps) block_candidates<E>(a, row, sh.blist[q], t16, sh);
+  top_sync();
   const int nc = sh.ncand;
   if (listed && nc <= kCandCap) {
     rank_select(sh.cand, nc, F, sh.S);
@@ -817,7 +823,7 @@ SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t
     uint64_t prev = ~0ull;
     for (int r = 0; r < F; ++r) {
       uint64_t best = 0ull;
-      for (int q = warp; q < nq; q += kWarps) {
+      for (int q = gw; q < nq; q += kTopWarps) {
         const int g = listed ? sh.blist[q] : q;
         const int v = g * 32 + lane;
         if (v >= a.nvec) continue;
@@ -831,12 +837,17 @@ SSD_DEV void row_topf(const VocabArgs &a, const char *row, int F, const uint32_t
           if (key < prev && key > best) best = key;
         }
       }
-      best = block_max_u64<kThreads>(best, sh.redk);
-      if (tid == 0) sh.S[r] = best;
+      best = warp_max_u64(best);
+      if (lane == 0) sh.redk[gw] = best;
+      top_sync();
+      best = sh.redk[0];
+      for (int w = 1; w < kTopWarps; ++w) best = sh.redk[w] > best ? sh.redk[w] : best;
+      top_sync();
+      if (gt == 0) sh.S[r] = best;
       prev = best;
     }
   }
-  __syncthreads();
+  top_sync();
 }
 
 // One warp: inverse-CDF draw over a row from its segment masses smm (row
@@ -1004,9 +1015,10 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
     }
   }
   if (a.trace && tid == 0) sh.mk[5] = now_ns();
-  // the draft row's top-F list S, its normalised mass and the guesses of depth j
+  // the draft row's top-F list S (warps 1..7, while warp 0 draws), its
+  // normalised mass and the guesses of depth j
   if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.gm[kDft], ad);
-  if (F >= 2) row_topf<E>(a, rowD, F, pb.keys, sh);
+  if (F >= 2 && warp > 0) row_topf<E>(a, rowD, F, pb.keys, sh);
   __syncthreads();
   if (warp == 1) {
     float sq = 0.f;
@@ -1181,13 +1193,12 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
 // k_resid: residual units, the bonus draw and the sequence finish
 // ===========================================================================
 constexpr int kLookupStage = 2048;  // guesses + payload words of a sequence staged in shared memory
-constexpr int kBlkStage = 1024;     // residual block sums the last unit stages at once
 struct __align__(16) ResSh {
   PairRec rec[kMaxK + 1];
   float u[kMaxK];
-  float seg[kWarps][2];      // this unit's segment masses (residual, p), or its warps' analytics sums
+  float seg[kWarps][2];      // this unit's half-segment masses (residual, p), or its warps' analytics sums
   float um[2][kMaxUnits];    // the sequence's unit masses (residual, p)
-  float2 bl[kBlkStage];      // residual block sums (residual, p)
+  float2 sgm[kMaxSeg];       // the sequence's segment masses (residual, p)
   float bx[kUnitSeg * kSegBlocks];
   float sm[kUnitSeg];
   int32_t look[kLookupStage];  // the sequence's guesses, then its payload
@@ -1198,7 +1209,7 @@ struct __align__(16) ResSh {
 // The residual pass's vectors: per warp its segment of both rows (8 blocks of
 // 32 vectors), staged by cp.async so that the block loop need not be unrolled.
 struct __align__(16) ResStage {
-  uint4 v[kWarps][2][kSegBlocks][32];
+  uint4 v[kWarps][2][kSegBlocks / 2][32];
 };
 
 // The outputs of sequence b once its bonus token bt is known (sh.rec: its
@@ -1259,40 +1270,45 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
   }
 }
 
-// Residual pass over unit u (segments 8u .. 8u + 7, one per warp) of row
-// pair j of sequence b: per block the sums of max(0, p - q') and of p (lane
-// sums, then a scan: the arithmetic of warp_find), written to ublk when
-// `store`; the segment masses (warp_runs' arithmetic over the 8 blocks) into
-// sh.seg.  kMins: *mn, *mx (every lane) = the warp's sums of min(p, q') and
-// of max(0, p - q'), each lane in element order.  The warp's vectors are
-// staged in `st` first (all loads in flight at once), then reduced block by
-// block.
-template <class E, bool kMins>
-SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr, bool store, ResSh &sh, ResStage &st,
-                       float *mn_out, float *mx_out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sg = u * kUnitSeg + warp;
+// Stage nb blocks (32 vectors each) of row pair j of sequence b, from block
+// g0 on, for warp `w` in st: all of the warp's loads in flight at once.
+template <class E>
+SSD_DEV void stage_blocks(const VocabArgs &a, int b, int j, int g0, int nb, int w, ResStage &st) {
+  const int lane = threadIdx.x & 31;
   const char *rowT = row_ptr(a, 0, b, j, E::kSize);
   const char *rowD = row_ptr(a, 1, b, j, E::kSize);
-  float mn = 0.f, mx = 0.f, segr = 0.f, segp = 0.f;
-  if (sg < a.nseg) {
-    for (int k = 0; k < kSegBlocks; ++k) {
-      const int v = sg * kSegVec + 32 * k + lane;
-      if (v < a.nfull) {
-        cp_async16(&st.v[warp][0][k][lane], rowT + static_cast<int64_t>(v) * 16);
-        cp_async16(&st.v[warp][1][k][lane], rowD + static_cast<int64_t>(v) * 16);
-      } else {
-        st.v[warp][0][k][lane] = row_vec<E>(a, rowT, v);
-        st.v[warp][1][k][lane] = row_vec<E>(a, rowD, v);
-      }
+  for (int k = 0; k < nb; ++k) {
+    const int v = (g0 + k) * 32 + lane;
+    if (v < a.nfull) {
+      cp_async16(&st.v[w][0][k][lane], rowT + static_cast<int64_t>(v) * 16);
+      cp_async16(&st.v[w][1][k][lane], rowD + static_cast<int64_t>(v) * 16);
+    } else {
+      st.v[w][0][k][lane] = row_vec<E>(a, rowT, v);
+      st.v[w][1][k][lane] = row_vec<E>(a, rowD, v);
     }
-    cp_async_wait_all();
-    __syncwarp();
-    float vr = 0.f, vp = 0.f;  // lane k < 8: block k's sums
+  }
+  cp_async_wait_all();
+  __syncwarp();
+}
+
+// Residual pass over unit u (segments 4u .. 4u + 3, two warps per segment,
+// four blocks each) of row pair j of sequence b: each lane sums max(0, p -
+// q') and p over its elements in order, the lanes by a butterfly: the
+// half-segment masses, into sh.seg.  kMins: *mn, *mx (every lane) = the
+// warp's sums of min(p, q') and of max(0, p - q').
+template <class E, bool kMins>
+SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr, ResSh &sh, ResStage &st,
+                       float *mn_out, float *mx_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sg = u * kResSeg + (warp >> 1);
+  const int g0 = sg * kSegBlocks + (warp & 1) * (kSegBlocks / 2);
+  float mn = 0.f, rs = 0.f, ps = 0.f;
+  if (sg < a.nseg) {
+    stage_blocks<E>(a, b, j, g0, kSegBlocks / 2, warp, st);
 #pragma unroll 1
-    for (int k = 0; k < kSegBlocks; ++k) {
-      const int i0 = (sg * kSegVec + 32 * k + lane) * E::kVec;
-      float ft[E::kVec], fd[E::kVec], xr[E::kVec], xp[E::kVec];
+    for (int k = 0; k < kSegBlocks / 2; ++k) {
+      const int i0 = ((g0 + k) * 32 + lane) * E::kVec;
+      float ft[E::kVec], fd[E::kVec];
       E::unpack(st.v[warp][0][k][lane], ft);
       E::unpack(st.v[warp][1][k][lane], fd);
 #pragma unroll
@@ -1300,84 +1316,139 @@ SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr
         if (i0 + e < a.V) {
           const float p = wr.p(ft[e]), q = wr.q(fd[e], i0 + e);
           const float r = __fsub_rn(p, q);
-          xr[e] = r > 0.f ? r : 0.f;
-          xp[e] = p;
-          if (kMins) {
-            mn = __fadd_rn(mn, fminf(p, q));
-            mx = __fadd_rn(mx, xr[e]);
-          }
-        } else {
-          xr[e] = xp[e] = 0.f;
+          rs = __fadd_rn(rs, r > 0.f ? r : 0.f);
+          ps = __fadd_rn(ps, p);
+          if (kMins) mn = __fadd_rn(mn, fminf(p, q));
         }
       }
-      const float br = __shfl_sync(0xffffffffu, warp_incl_scan(lane_sum<E::kVec>(xr)), 31);
-      const float bp = __shfl_sync(0xffffffffu, warp_incl_scan(lane_sum<E::kVec>(xp)), 31);
-      if (lane == k) {
-        vr = br;
-        vp = bp;
-      }
     }
-    segr = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? vr : 0.f), 31);
-    segp = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? vp : 0.f), 31);
-    if (store && lane < kSegBlocks) a.ublk[static_cast<size_t>(b) * a.nblk + sg * kSegBlocks + lane] = make_float2(vr, vp);
-    if (store && lane == 0) a.useg[static_cast<size_t>(b) * a.nseg + sg] = make_float2(segr, segp);
+    rs = warp_sum(rs);
+    ps = warp_sum(ps);
   }
   if (lane == 0) {
-    sh.seg[warp][0] = segr;
-    sh.seg[warp][1] = segp;
+    sh.seg[warp][0] = rs;
+    sh.seg[warp][1] = ps;
   }
   if (kMins) {
     *mn_out = warp_sum(mn);
-    *mx_out = warp_sum(mx);
+    *mx_out = rs;
   }
 }
 
-// One warp, the last residual unit of sequence b: the bonus from max(0, p -
-// q') of pair acc (p when the residual has no mass): unit, segment, block,
-// then the element.  sh.um holds the unit masses and, when `staged`, sh.bl
-// every block sum.  Returns (every lane) the token (-1: no weight); sets *W
-// (the residual mass), *zero and *near.
+// The last residual unit of sequence b, every thread: the bonus from max(0,
+// p - q') of pair acc (p when the residual has no mass).  Warp 0 locates the
+// unit (sh.um) and the segment (sh.sgm); the eight warps read the segment's
+// blocks again, one each, for their sums (lane sums, then a scan: the
+// arithmetic of the element search); warp 0 locates the block and the
+// element.  Returns the token (-1: no weight); sets *W (the residual mass),
+// *zero and *near.
 template <class E>
-SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, bool staged, ResSh &sh, float *W_out,
+SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, ResSh &sh, ResStage &st, float *W_out,
                        bool *zero, bool *near) {
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int U = a.nunits;
-  const float W0 = warp_total(sh.um[0], U);
-  *W_out = W0;
-  *zero = !(W0 > 0.f);
-  const int X = *zero ? 1 : 0;
-  float rem, W;
-  bool fb;
-  const int q = warp_locate(sh.um[X], U, a.u_bonus[b], false, &rem, &W, &fb);
+  if (warp == 0) {
+    const float W0 = warp_total(sh.um[0], U);
+    const int X = (W0 > 0.f) ? 0 : 1;
+    float rem, W;
+    bool fb;
+    const int q = warp_locate(sh.um[X], U, a.u_bonus[b], false, &rem, &W, &fb);
+    int sg = -1;
+    float rem2 = 0.f, W2;
+    bool fb2 = false;
+    if (q >= 0) {
+      if (lane < kResSeg) {
+        const int t = q * kResSeg + lane;
+        sh.sm[lane] = (t < a.nseg) ? (X ? sh.sgm[t].y : sh.sgm[t].x) : 0.f;
+      }
+      __syncwarp();
+      const int s = warp_locate(sh.sm, kResSeg, rem, true, &rem2, &W2, &fb2);
+      if (s >= 0) sg = q * kResSeg + s;
+    }
+    if (lane == 0) {
+      sh.ival[0] = sg;
+      sh.ival[1] = X | ((fb || fb2) ? 2 : 0);
+      sh.scal[1] = rem2;
+      sh.scal[2] = W;
+      sh.scal[3] = W0;
+    }
+  }
+  __syncthreads();
+  const int sg = sh.ival[0];
+  const int X = sh.ival[1] & 1;
+  *zero = X != 0;
+  *W_out = sh.scal[3];
   *near = true;
-  if (q < 0) return -1;
-  const float2 *bl = a.ublk + static_cast<size_t>(b) * a.nblk;
-  for (int i = lane; i < kUnitSeg * kSegBlocks; i += 32) {
-    const int g = q * kUnitSeg * kSegBlocks + i;
-    const float2 v = (g < a.nblk) ? (staged ? sh.bl[g] : __ldcg(bl + g)) : make_float2(0.f, 0.f);
-    sh.bx[i] = X ? v.y : v.x;
+  if (sg < 0) return -1;
+  const WProb wp{a.kT, wr.Mtk, wr.inv_st};
+  // block `warp` of the segment: its sum
+  const int g = sg * kSegBlocks + warp;
+  stage_blocks<E>(a, b, acc, g, 1, warp, st);
+  {
+    const int i0 = (g * 32 + lane) * E::kVec;
+    float ft[E::kVec], fd[E::kVec], x[E::kVec];
+    E::unpack(st.v[warp][0][0][lane], ft);
+    E::unpack(st.v[warp][1][0][lane], fd);
+#pragma unroll
+    for (int e = 0; e < E::kVec; ++e)
+      x[e] = (i0 + e < a.V) ? (X ? wp(ft[e], 0.f, 0, 0.f) : wr(ft[e], fd[e], i0 + e, 0.f)) : 0.f;
+    const float t = warp_incl_scan(lane_sum<E::kVec>(x));
+    if (lane == 31) sh.bx[warp] = t;
   }
-  if (lane < kUnitSeg) {  // the unit's segment masses, as the unit pass summed them
-    const int sg = q * kUnitSeg + lane;
-    const float2 v = (sg < a.nseg) ? __ldcg(a.useg + static_cast<size_t>(b) * a.nseg + sg) : make_float2(0.f, 0.f);
-    sh.sm[lane] = X ? v.y : v.x;
+  __syncthreads();
+  int bt = -1;
+  if (warp == 0) {
+    float rem3, W3;
+    bool fb3;
+    const int k = warp_locate(sh.bx, kSegBlocks, sh.scal[1], true, &rem3, &W3, &fb3);
+    if (k >= 0) {
+      const int gk = sg * kSegBlocks + k;
+      const int i0 = (gk * 32 + lane) * E::kVec;
+      float ft[E::kVec], fd[E::kVec], x[E::kVec];
+      E::unpack(st.v[k][0][0][lane], ft);
+      E::unpack(st.v[k][1][0][lane], fd);
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e)
+        x[e] = (i0 + e < a.V) ? (X ? wp(ft[e], 0.f, 0, 0.f) : wr(ft[e], fd[e], i0 + e, 0.f)) : 0.f;
+      const float L = lane_sum<E::kVec>(x);
+      const float incl = warp_incl_scan(L);
+      float ex = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) ex = 0.f;
+      float run = 0.f, edge = 0.f;
+      int hit = -1, lpos = -1;
+#pragma unroll
+      for (int e = 0; e < E::kVec; ++e) {
+        const float before = __fadd_rn(ex, run);
+        run = __fadd_rn(run, x[e]);
+        if (x[e] > 0.f) {
+          lpos = i0 + e;
+          const float after = __fadd_rn(ex, run);
+          if (hit < 0 && after > rem3) {
+            hit = lpos;
+            edge = fminf(__fsub_rn(rem3, before), __fsub_rn(after, rem3));
+          }
+        }
+      }
+      const uint32_t mc = __ballot_sync(0xffffffffu, L > 0.f && __fadd_rn(ex, L) > rem3);
+      float dist = 0.f;
+      if (mc) {
+        const int src = __ffs(mc) - 1;
+        dist = __shfl_sync(0xffffffffu, hit >= 0 ? fmaxf(edge, 0.f) : 0.f, src);
+        bt = __shfl_sync(0xffffffffu, hit >= 0 ? hit : lpos, src);
+      } else {
+        bt = lpos;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) bt = max(bt, __shfl_xor_sync(0xffffffffu, bt, o));
+      }
+      if (lane == 0) sh.ival[2] = ((sh.ival[1] & 2) || fb3 || bt < 0 || !(dist >= __fmul_rn(kNearTie, sh.scal[2]))) ? 1 : 0;
+    } else if (lane == 0) {
+      sh.ival[2] = 1;
+    }
+    if (lane == 0) sh.ival[3] = bt;
   }
-  __syncwarp();
-  float rem2, W2, rem3, W3;
-  bool fb2, fb3;
-  const int s = warp_locate(sh.sm, kUnitSeg, rem, true, &rem2, &W2, &fb2);
-  if (s < 0) return -1;
-  const int k = warp_locate(sh.bx + s * kSegBlocks, kSegBlocks, rem2, true, &rem3, &W3, &fb3);
-  if (k < 0) return -1;
-  const char *rowT = row_ptr(a, 0, b, acc, E::kSize);
-  const char *rowD = row_ptr(a, 1, b, acc, E::kSize);
-  const int g = (q * kUnitSeg + s) * kSegBlocks + k;
-  float dist;
-  int bt;
-  if (X) bt = warp_find<E>(a, rowT, nullptr, g, rem3, WProb{a.kT, wr.Mtk, wr.inv_st}, 0.f, &dist);
-  else bt = warp_find<E>(a, rowT, rowD, g, rem3, wr, 0.f, &dist);
-  *near = fb || fb2 || fb3 || bt < 0 || !(dist >= __fmul_rn(kNearTie, W));
-  return bt;
+  __syncthreads();
+  *near = sh.ival[2] != 0;
+  return sh.ival[3];
 }
 
 template <class E>
@@ -1410,7 +1481,7 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
         if (tid == 0) sh.rec[0] = a.rec[static_cast<size_t>(b) * (K + 1) + j];
         __syncthreads();
         const WResid wr = resid_weights(a, sh.rec[0], a.Fs[j]);
-        unit_pass<E, true>(a, b, j, u, wr, false, sh, st, &mn, &mx);
+        unit_pass<E, true>(a, b, j, u, wr, sh, st, &mn, &mx);
         __syncthreads();  // sh.seg is overwritten below
       }
       if (lane == 0) {
@@ -1498,12 +1569,21 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
       // the residual of the first rejected position: this unit's block sums
       const WResid wr = resid_weights(a, sh.rec[acc], a.Fs[acc]);
       float mn, mx;
-      unit_pass<E, false>(a, b, acc, u, wr, true, sh, st, &mn, &mx);
+      unit_pass<E, false>(a, b, acc, u, wr, sh, st, &mn, &mx);
       __syncthreads();
       if (a.trace && tid == 0) sh.mk[4] = now_ns();
       if (warp == 0) {
-        const float ir = warp_incl_scan(lane < kWarps ? sh.seg[lane][0] : 0.f);
-        const float ip = warp_incl_scan(lane < kWarps ? sh.seg[lane][1] : 0.f);
+        // the segment masses (two halves in order) and the unit's mass by
+        // warp_runs' arithmetic over them
+        float vr = 0.f, vp = 0.f;
+        if (lane < kResSeg) {
+          vr = __fadd_rn(sh.seg[2 * lane][0], sh.seg[2 * lane + 1][0]);
+          vp = __fadd_rn(sh.seg[2 * lane][1], sh.seg[2 * lane + 1][1]);
+        }
+        const int sg = u * kResSeg + lane;
+        if (lane < kResSeg && sg < a.nseg) a.useg[static_cast<size_t>(b) * a.nseg + sg] = make_float2(vr, vp);
+        const float ir = warp_incl_scan(vr);
+        const float ip = warp_incl_scan(vp);
         if (lane == 31) {
           a.umass[static_cast<size_t>(b) * U + u] = make_float2(ir, ip);
           __threadfence();
@@ -1515,34 +1595,23 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
       __syncthreads();
       if (a.trace && tid == 0) sh.mk[5] = now_ns();
       if (sh.ival[0]) {
-        // the last unit: the bonus; the unit masses and (when they fit) every
-        // block sum in one round of loads
-        const bool bstaged = a.nblk <= kBlkStage;
+        // the last unit: the bonus (every unit and segment mass in one round of loads)
         for (int q = tid; q < U; q += kThreads) {
           const float2 v = __ldcg(a.umass + static_cast<size_t>(b) * U + q);
           sh.um[0][q] = v.x;
           sh.um[1][q] = v.y;
         }
-        if (bstaged)
-          for (int i = tid; i < a.nblk; i += kThreads) sh.bl[i] = __ldcg(a.ublk + static_cast<size_t>(b) * a.nblk + i);
+        for (int t = tid; t < a.nseg; t += kThreads) sh.sgm[t] = __ldcg(a.useg + static_cast<size_t>(b) * a.nseg + t);
         __syncthreads();
-        if (warp == 0) {
-          float W;
-          bool zero, near;
-          int bt = resid_draw<E>(a, b, acc, wr, bstaged, sh, &W, &zero, &near);
-          if (bt < 0) {  // no weight at all: the target argmax
-            bt = sh.rec[acc].bt;
-            near = true;
-          }
-          if (lane == 0) {
-            sh.ival[1] = bt;
-            sh.ival[2] = (near ? 1 : 0) | (zero ? 2 : 0);
-            sh.scal[0] = W;
-          }
+        float W;
+        bool zero, near;
+        int bt = resid_draw<E>(a, b, acc, wr, sh, st, &W, &zero, &near);
+        if (bt < 0) {  // no weight at all: the target argmax
+          bt = sh.rec[acc].bt;
+          near = true;
         }
-        __syncthreads();
         if (a.trace && tid == 0) sh.mk[6] = now_ns();
-        emit(a, b, acc, sh.ival[1], sh.scal[0], (sh.ival[2] & 2) != 0, (sh.ival[2] & 1) != 0, staged, sh);
+        emit(a, b, acc, bt, W, zero, near, staged, sh);
       }
     }
   }
@@ -1603,7 +1672,7 @@ namespace {
 
 struct Layout {
   int nvec, nfull, nseg, nblk, nunits;
-  size_t ctr_words, ctr_off, seg_off, bsum_off, bkey_off, rec_off, umass_off, ublk_off, useg_off, amass_off, total;
+  size_t ctr_words, ctr_off, seg_off, bsum_off, bkey_off, rec_off, umass_off, useg_off, amass_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1622,7 +1691,7 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   L->nfull = static_cast<int>(bytes / 16);
   L->nseg = static_cast<int>(nseg);
   L->nblk = L->nseg * kSegBlocks;
-  L->nunits = (L->nseg + kUnitSeg - 1) / kUnitSeg;
+  L->nunits = (L->nseg + kResSeg - 1) / kResSeg;
   const size_t Bn = static_cast<size_t>(B > 0 ? B : 1);
   const size_t slots = Bn * 2 * (K + 1);
   L->ctr_words = 2 + Bn + Bn * K;
@@ -1639,8 +1708,6 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + Bn * (K + 1) * sizeof(PairRec), 256);
   L->umass_off = o;
   o = align_up(o + Bn * L->nunits * sizeof(float2), 256);
-  L->ublk_off = o;
-  o = align_up(o + Bn * L->nblk * sizeof(float2), 256);
   L->useg_off = o;
   o = align_up(o + Bn * L->nseg * sizeof(float2), 256);
   L->amass_off = o;
@@ -1711,7 +1778,6 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.bkey = reinterpret_cast<uint32_t *>(w + L.bkey_off);
   a.rec = reinterpret_cast<PairRec *>(w + L.rec_off);
   a.umass = reinterpret_cast<float2 *>(w + L.umass_off);
-  a.ublk = reinterpret_cast<float2 *>(w + L.ublk_off);
   a.useg = reinterpret_cast<float2 *>(w + L.useg_off);
   a.amass = reinterpret_cast<float2 *>(w + L.amass_off);
   a.status = status;
