@@ -83,6 +83,10 @@ def _declare(lib):
     lib.oracle_branch_attention.argtypes = [_p, _p, _p, _p, _i, _i64, _p, _p, _i, _i, _i, _i, _i,
                                             _i, _d, _p, _p, _p]
     lib.oracle_branch_attention.restype = _i
+    lib.oracle_ngram_backup.argtypes = [_p, _i64, _p, _i, _i, _i, _i, _p, _p, _p, _p]
+    lib.oracle_ngram_backup.restype = _i
+    lib.oracle_fallback_plan.argtypes = [_p, _p, _i, _d, _d, _i, _p, _p, _p, _p, _p, _p]
+    lib.oracle_fallback_plan.restype = _i
 
 
 def _ptr(a):
@@ -273,3 +277,34 @@ def run_round(inp, T=None, C=None):
     v.update(d=d, qd=qd, draft_margin=dm, guess=guess, guess_q=gq, slot=lk["slot"],
              next_tokens=lk["next_tokens"], hits=lk["hits"])
     return v
+
+
+def ngram_backup(history, hist_len, n, K, V, slot, u_rand, next_tokens=None):
+    """Backup tokens for the sequences that missed the cache (slot < 0): the
+    n-gram lookup in each sequence's history, random tokens where it has no
+    continuation.  Returns (next_tokens [B, K], match_pos [B]); hits keep the
+    given next_tokens (zeros when none are given)."""
+    history = _c(history, np.int32)
+    B = history.shape[0]
+    nxt = np.zeros((B, K), np.int32) if next_tokens is None else _c(next_tokens, np.int32).copy()
+    mpos = np.zeros(B, np.int32)
+    _L().oracle_ngram_backup(_ptr(history), history.shape[1], _ptr(_c(hist_len, np.int32)), B, int(n), int(K),
+                             int(V), _ptr(_c(slot, np.int32)), _ptr(_c(u_rand, np.float32)), _ptr(nxt),
+                             _ptr(mpos))
+    return nxt, mpos
+
+
+def fallback_plan(p_hit, e_hit, T_v, T_p, T_b, e_miss):
+    """The batch speedup model per backup option: dict of time, tokens,
+    throughput, speedup (arrays over the options) and best (index)."""
+    p_hit = _c(p_hit, np.float32)
+    e_hit = _c(e_hit, np.float32)
+    T_b = _c(T_b, np.float64)
+    e_miss = _c(e_miss, np.float64)
+    n = len(T_b)
+    out = {k: np.zeros(n) for k in ("time", "tokens", "throughput", "speedup")}
+    best = _L().oracle_fallback_plan(_ptr(p_hit), _ptr(e_hit), len(p_hit), float(T_v), float(T_p), n, _ptr(T_b),
+                                     _ptr(e_miss), *[_ptr(out[k]) for k in ("time", "tokens", "throughput",
+                                                                            "speedup")])
+    out["best"] = int(best)
+    return out

@@ -608,3 +608,88 @@ int oracle_branch_attention(const uint16_t *q, const uint16_t *k_cache, const ui
   }
   return 0;
 }
+
+/* ===========================================================================
+ * Miss fallback (technical summary "超越传统SD：SSD框架全异步解码实现4.7倍平均加速",
+ * "Saguaro 算法" part 3 "大 Batch 下的退避策略", and the speedup statement of
+ * "投机解码的瓶颈与 SSD 的核心机制" in p_hit, T_p and T_b).
+ * ======================================================================== */
+
+/* A uniform token id from a uniform u in [0, 1) with a 24-bit mantissa:
+ * floor(u * V), computed exactly in integers (u * 2^24 is an integer). */
+static int32_t uniform_token(float u, int V) {
+  const uint64_t m = (uint64_t)((double)u * 16777216.0);
+  return (int32_t)((m * (uint64_t)V) >> 24);
+}
+
+/* Low-latency backup speculator for the sequences that missed the
+ * speculation cache (slot[b] < 0): an n-gram lookup in the sequence's own
+ * history.  Reading: with the history h[0..L) (L = hist_len[b]) and its last
+ * n tokens s = h[L-n..L), the latest earlier occurrence m (m + n <= L - 1,
+ * h[m..m+n) = s, searched from m = L-n-1 down to 0) proposes the K tokens
+ * h[m+n], h[m+n+1], ...; positions past L, and every position when s occurs
+ * nowhere earlier (or L < n + 1), take the random backup token
+ * floor(u_rand[b, t] V).  Hits keep their next_tokens.  match_pos[b] = m,
+ * -1 without a match, -2 for a hit. */
+int oracle_ngram_backup(const int32_t *hist, int64_t hist_stride, const int32_t *hist_len, int B, int n, int K,
+                        int V, const int32_t *slot, const float *u_rand, int32_t *next_tokens,
+                        int32_t *match_pos) {
+  for (int b = 0; b < B; ++b) {
+    if (slot[b] >= 0) {
+      match_pos[b] = -2;
+      continue;
+    }
+    const int32_t *h = hist + (int64_t)b * hist_stride;
+    const int L = hist_len[b];
+    int m = -1;
+    if (n >= 1 && L >= n + 1) {
+      for (int c = L - n - 1; c >= 0 && m < 0; --c) {
+        int eq = 1;
+        for (int i = 0; i < n && eq; ++i) eq = (h[c + i] == h[L - n + i]);
+        if (eq) m = c;
+      }
+    }
+    match_pos[b] = m;
+    for (int t = 0; t < K; ++t) {
+      const int p = m + n + t;
+      next_tokens[(int64_t)b * K + t] = (m >= 0 && p < L) ? h[p] : uniform_token(u_rand[(int64_t)b * K + t], V);
+    }
+  }
+  return 0;
+}
+
+/* The batch-level speedup model and the fallback choice.  Reading (the
+ * formula did not survive extraction; restated from the definitions the
+ * pages give): the primary speculator drafts for every predicted outcome
+ * while the target verifies, so a round whose outcome hits the cache costs
+ * max(T_v, T_p); a miss falls back to synchronous speculation with backup o,
+ * and one miss stalls the whole batch for T_b[o].  With independent hits of
+ * probability p_hit[b]:
+ *   time[o]   = max(T_v, T_p) + (1 - prod_b p_hit[b]) T_b[o]
+ *   tokens[o] = sum_b (p_hit[b] e_hit[b] + (1 - p_hit[b]) e_miss[o])
+ *   throughput[o] = tokens[o] / time[o];
+ *   speedup[o] = throughput[o] / (sum_b e_hit[b] / (T_p + T_v)), i.e. against
+ *                synchronous speculative decoding with the primary (draft,
+ *                then verify, every round);
+ *   best = the option of largest throughput (ties: the lower index). */
+int oracle_fallback_plan(const float *p_hit, const float *e_hit, int B, double T_v, double T_p, int nopt,
+                         const double *T_b, const double *e_miss, double *time, double *tokens,
+                         double *throughput, double *speedup) {
+  double pall = 1.0, ph = 0.0, ehit = 0.0, pmiss = 0.0;
+  for (int b = 0; b < B; ++b) {
+    pall *= (double)p_hit[b];
+    ph += (double)p_hit[b] * (double)e_hit[b];
+    pmiss += 1.0 - (double)p_hit[b];
+    ehit += (double)e_hit[b];
+  }
+  const double base = ehit / (T_p + T_v);
+  int best = 0;
+  for (int o = 0; o < nopt; ++o) {
+    time[o] = (T_v > T_p ? T_v : T_p) + (1.0 - pall) * T_b[o];
+    tokens[o] = ph + pmiss * e_miss[o];
+    throughput[o] = tokens[o] / time[o];
+    speedup[o] = throughput[o] / base;
+    if (throughput[o] > throughput[best]) best = o;
+  }
+  return best;
+}

@@ -773,3 +773,106 @@ def test_oracle_is_thread_safe():
                             range(0, spec.B, 6)))
     for k in range(3):
         assert np.array_equal(np.concatenate([p[k] for p in parts]), whole[k])
+
+
+# ---------------------------------------------------------------------------
+# miss fallback: the n-gram backup speculator and the batch speedup model
+# ---------------------------------------------------------------------------
+def test_ngram_backup_worked_examples():
+    """Hand-worked: the suffix (1, 2, 3) last occurs earlier at position 6, so
+    the proposal is h[9..12]; with n = 2 the suffix (2, 3) last occurs at 7."""
+    h = np.array([[5, 1, 2, 3, 9, 9, 1, 2, 3, 7, 1, 2, 3, 0, 0]], np.int32)
+    u = np.full((1, 4), 0.5, np.float32)
+    nxt, m = oracle.ngram_backup(h, [13], 3, 4, 100, [-1], u)
+    assert m[0] == 6 and nxt[0].tolist() == [7, 1, 2, 3]
+    nxt, m = oracle.ngram_backup(h, [13], 2, 4, 100, [-1], u)
+    assert m[0] == 7 and nxt[0].tolist() == [7, 1, 2, 3]
+    # the continuation runs past the history: the rest comes from the random backup
+    h2 = np.array([[4, 4, 8, 4, 4]], np.int32)
+    nxt, m = oracle.ngram_backup(h2, [5], 2, 3, 10, [-1], np.array([[0.0, 0.25, 0.5]], np.float32))
+    assert m[0] == 0 and nxt[0].tolist() == [8, 4, 4]
+    nxt, m = oracle.ngram_backup(h2, [5], 2, 5, 10, [-1], np.array([[0, 0, 0, 0.25, 0.75]], np.float32))
+    assert nxt[0].tolist() == [8, 4, 4, 2, 7]
+    # a hit keeps its tokens; no match and too short a history are all random
+    nxt, m = oracle.ngram_backup(h, [13], 3, 2, 100, [4], np.zeros((1, 2), np.float32),
+                                 next_tokens=np.array([[11, 12]], np.int32))
+    assert m[0] == -2 and nxt[0].tolist() == [11, 12]
+    nxt, m = oracle.ngram_backup(np.array([[1, 2, 3, 4]], np.int32), [4], 2, 2, 1000, [-1],
+                                 np.array([[0.5, 0.125]], np.float32))
+    assert m[0] == -1 and nxt[0].tolist() == [500, 125]
+    # float32(0.9) lies just below 0.9, so the exact floor of u V is 8, not 9
+    nxt, m = oracle.ngram_backup(np.array([[7, 7]], np.int32), [2], 2, 1, 10, [-1], np.array([[0.9]], np.float32))
+    assert m[0] == -1 and nxt[0].tolist() == [8]
+
+
+def test_ngram_backup_properties_random():
+    """On random histories over a small alphabet: the chosen occurrence
+    matches the suffix, none after it does, and the random tokens are
+    floor(u V) in exact rational arithmetic."""
+    from fractions import Fraction
+    rng = np.random.default_rng(7)
+    B, Lmax, K, V = 64, 60, 5, 1000
+    h = rng.integers(0, 4, size=(B, Lmax)).astype(np.int32)
+    lens = rng.integers(0, Lmax + 1, size=B).astype(np.int32)
+    slot = np.where(rng.random(B) < 0.2, 3, -1).astype(np.int32)
+    u = ((rng.integers(0, 1 << 24, size=(B, K))).astype(np.float64) / (1 << 24)).astype(np.float32)
+    for n in (1, 2, 3, 5):
+        nxt, m = oracle.ngram_backup(h, lens, n, K, V, slot, u)
+        for b in range(B):
+            if slot[b] >= 0:
+                assert m[b] == -2
+                continue
+            L = int(lens[b])
+            suf = list(h[b, L - n:L]) if L >= n else None
+            occ = [c for c in range(0, L - n) if suf is not None and list(h[b, c:c + n]) == suf]
+            assert m[b] == (occ[-1] if occ else -1)
+            for t in range(K):
+                p = m[b] + n + t
+                if m[b] >= 0 and p < L:
+                    assert nxt[b, t] == h[b, p]
+                else:
+                    assert nxt[b, t] == int(Fraction(float(u[b, t])) * V)
+
+
+def test_fallback_plan_closed_forms():
+    """Every sequence hits: the batch never waits for a backup, so the round
+    costs max(T_v, T_p) and the speedup over synchronous speculation is
+    (T_p + T_v) / max(T_v, T_p).  A batch of one with a certain miss costs
+    max(T_v, T_p) + T_b and yields e_miss tokens."""
+    out = oracle.fallback_plan(np.ones(8), np.full(8, 3.0), 1.0, 0.4, [0.4, 0.01], [3.0, 1.0])
+    assert np.allclose(out["time"], [1.0, 1.0]) and np.allclose(out["tokens"], [24.0, 24.0])
+    assert np.allclose(out["speedup"], 1.4) and out["best"] == 0
+    out = oracle.fallback_plan([0.0], [3.0], 1.0, 0.4, [0.4, 0.01], [2.5, 1.0])
+    assert np.allclose(out["time"], [1.4, 1.01]) and np.allclose(out["tokens"], [2.5, 1.0])
+    assert out["best"] == 0  # 2.5 / 1.4 > 1 / 1.01
+
+
+def test_fallback_plan_matches_simulation():
+    """Monte Carlo of batch rounds (independent hits; any miss stalls the batch
+    on the backup) against the closed form."""
+    rng = np.random.default_rng(11)
+    B = 6
+    p = rng.uniform(0.5, 0.99, size=B).astype(np.float32)
+    eh = rng.uniform(1.5, 4.0, size=B).astype(np.float32)
+    T_v, T_p, T_b, e_miss = 1.0, 0.7, [0.7, 0.02], [2.0, 1.05]
+    out = oracle.fallback_plan(p, eh, T_v, T_p, T_b, e_miss)
+    R = 400000
+    hits = rng.random((R, B)) < p.astype(np.float64)
+    anymiss = ~hits.all(axis=1)
+    for o in range(2):
+        t = max(T_v, T_p) + anymiss * T_b[o]
+        tok = (hits * eh.astype(np.float64) + (~hits) * e_miss[o]).sum(axis=1)
+        assert abs(t.mean() - out["time"][o]) < 5 * t.std() / np.sqrt(R)
+        assert abs(tok.mean() - out["tokens"][o]) < 5 * tok.std() / np.sqrt(R)
+
+
+def test_fallback_plan_crossover_with_batch_size():
+    """With equal hit rates the chance that some sequence misses grows with the
+    batch, so beyond a critical batch size the fast backup wins (and below it
+    the accurate one); the winner changes exactly once."""
+    T_v, T_p, T_b, e_miss = 1.0, 0.5, [0.5, 0.02], [2.8, 1.0]
+    best = [oracle.fallback_plan(np.full(B, 0.9), np.full(B, 3.0), T_v, T_p, T_b, e_miss)["best"]
+            for B in range(1, 200)]
+    assert best[0] == 0 and best[-1] == 1
+    changes = sum(1 for a, b in zip(best, best[1:]) if a != b)
+    assert changes == 1
