@@ -334,6 +334,8 @@ def bench_ours(args):
         result["branch_attention"] = bench_attention(ssd, device, hbm_peak)
         result["other_rounds"] = bench_other_rounds(ssd, w, device, hbm_peak)
         result["tiny_round"] = bench_tiny_round(ssd, w, device)
+        result["round_analytics"] = bench_analytics(ssd, w, device, hbm_peak)
+        result["miss_fallback"] = bench_fallback(ssd, w, device, hbm_peak)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(spec, inp, args.cpu_seconds)
     if rank == 0:
@@ -485,6 +487,128 @@ def bench_tiny_round(ssd, w, device):
             "note": "back-to-back graph replays of one round each (B = 1): latency, not bandwidth"}
 
 
+def device_round_sets(spec, device, seed):
+    """Zipf-shaped bf16 target/draft logits of ``spec`` generated on the device
+    (bench only), copied into enough input sets that a rotation over them is
+    larger than L2; returns (sets, nsets, bytes per set, uniforms)."""
+    import torch
+    from speculative_decoding_vocab_gb300 import workloads as w
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    shape = (spec.B, spec.K + 1, spec.V)
+    rank = torch.argsort(torch.rand(shape, generator=g, device=device), dim=-1).float() + 1
+    zt = -spec.zipf_slope * torch.log(rank) + spec.target_noise * torch.randn(
+        shape, generator=g, device=device)
+    del rank
+    zd = zt + spec.draft_noise * torch.randn(shape, generator=g, device=device)
+    per = w.round_bytes(spec)
+    nsets = max(2, int(np.ceil(3 * L2_BYTES / per)) + 1) if per < 2 * L2_BYTES else 1
+    sets = [(zt.to(torch.bfloat16), zd.to(torch.bfloat16)) for _ in range(nsets)]
+    del zt, zd
+    u = torch.rand(3, spec.B, spec.K + 1, generator=g, device=device)
+    uni = (u[0, :, :spec.K].contiguous(), u[1, :, :spec.K].contiguous(), u[2, :, 0].contiguous())
+    return sets, nsets, per, uni
+
+
+def bench_analytics(ssd, w, device, hbm_peak):
+    """Exact round analytics (acceptance rates, accept-count distribution, hit
+    rate, expected tokens) on the large-batch Qwen-3 round."""
+    import torch
+    spec = w.qwen3_round(C=0.5)
+    stream = torch.cuda.current_stream(device)
+    sets, nsets, per, _ = device_round_sets(spec, device, 13)
+    B, K = spec.B, spec.K
+    f32 = dict(dtype=torch.float32, device=device)
+    pa, hr, et = torch.empty(B, K + 1, **f32), torch.empty(B, **f32), torch.empty(B, **f32)
+    al, rw, hm = torch.empty(B, K, **f32), torch.empty(B, K, **f32), torch.empty(B, K + 1, **f32)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = ssd.workspace(B, K, spec.V, spec.dtype, spec.F, device)
+
+    def call(i):
+        t, d = sets[i % nsets]
+        ssd.ssd_round_analytics(t, d, spec.V, spec.F, spec.C, spec.T, pa, hr, et, alpha=al,
+                                resid_w=rw, hit_mass=hm, status=st, ws=ws)
+
+    for i in range(3):
+        call(i)
+    graphs = capture_graphs([lambda i=i: call(i) for i in range(nsets)], device)
+    ms = _time_calls(lambda i: graphs[i % nsets].replay(), 50, stream)
+    res = {"workload": spec.name, "ms": round(ms, 4),
+           "seq_rounds_per_s": round(B / (ms * 1e-3), 1), "algorithmic_bytes": per,
+           "frac_of_hbm_peak": round(per / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "mean_hit_rate": round(float(hr.mean().item()), 4),
+           "mean_exp_tokens": round(float(et.mean().item()), 4), "status_flags": int(st.item())}
+    del graphs, sets, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_fallback(ssd, w, device, hbm_peak):
+    """The miss fallback on the large-batch Qwen-3 batch: the n-gram backup over
+    1-8 Ki-token histories (the misses scan their histories; rotating copies
+    larger than L2) and the batch plan."""
+    import torch
+    spec = w.qwen3_histories()
+    stream = torch.cuda.current_stream(device)
+    h = w.make_histories(spec, seed=21)
+    per = h.hist.nbytes
+    nsets = max(2, int(np.ceil(1.5 * L2_BYTES / per)) + 1)
+    hist0 = torch.from_numpy(h.hist).to(device)
+    sets = [hist0.clone() for _ in range(nsets)]
+    del hist0
+    hl = torch.from_numpy(h.hist_len).to(device)
+    slot = torch.from_numpy(h.slot).to(device)
+    u = torch.from_numpy(h.u_rand).to(device)
+    nxt = torch.empty(spec.B, spec.K, dtype=torch.int32, device=device)
+    mp = torch.empty(spec.B, dtype=torch.int32, device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def call(i):
+        ssd.ssd_ngram_backup(sets[i % nsets], hl, spec.n, spec.K, spec.V, u, nxt, slot=slot,
+                             match_pos=mp, status=st)
+
+    for i in range(3):
+        call(i)
+    # one graph holds a call per input copy, so the replays measure the device,
+    # not the host's launch rate (one call is a few microseconds)
+    g = capture_graphs([lambda: [call(i) for i in range(nsets)]], device)[0]
+    g.replay()
+    reps = 20
+    ms = _time_calls(lambda i: g.replay(), reps, stream) / nsets
+    m = mp.cpu().numpy()
+    miss = h.slot < 0
+    # algorithmic bytes: a miss reads its history from the end down to the match
+    # (all of it without one), plus slot, length, uniforms, proposals, positions
+    scanned = np.where(m >= 0, h.hist_len - np.maximum(m, 0), h.hist_len)[miss]
+    alg = int(4 * scanned.sum() + 4 * spec.B * 3 + 8 * spec.K * miss.sum())
+    res = {"workload": spec.name, "ms": round(ms, 4), "misses": int(miss.sum()),
+           "matched": int((m[miss] >= 0).sum()), "algorithmic_bytes": alg,
+           "GB/s": round(alg / (ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm_peak": round(alg / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "status_flags": int(st.item()), "kernel": "k_ngram_backup (one CTA per sequence)",
+           "timing": f"CUDA graph of {nsets} calls over rotating history copies "
+                     f"({nsets * per / 1e6:.0f} MB > L2), replayed {reps} times"}
+    # the plan: one reduction over the batch
+    p = torch.full((spec.B,), 0.9, dtype=torch.float32, device=device)
+    e = torch.full((spec.B,), 3.0, dtype=torch.float32, device=device)
+    best = torch.empty(1, dtype=torch.int32, device=device)
+    thr = torch.empty(2, dtype=torch.float64, device=device)
+
+    def plan(i):
+        ssd.ssd_fallback_plan(p, e, 1.0, 0.5, [0.5, 0.02], [2.8, 1.0], throughput=thr, best=best,
+                              status=st)
+
+    for i in range(3):
+        plan(i)
+    gp = capture_graphs([lambda: [plan(i) for i in range(50)]], device)[0]
+    gp.replay()
+    res["plan_ms"] = round(_time_calls(lambda i: gp.replay(), 20, stream) / 50, 4)
+    res["plan_best"] = int(best.item())
+    del g, gp, sets
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_other_rounds(ssd, w, device, hbm_peak):
     """The large-batch Qwen-3 round for each Saguaro C (with its cache hit rate),
     the at-scale Llama-3 round and the greedy Llama-3 round (seq-rounds/s)."""
@@ -493,22 +617,7 @@ def bench_other_rounds(ssd, w, device, hbm_peak):
     stream = torch.cuda.current_stream(device)
     for spec in (w.qwen3_round(C=1.0), w.qwen3_round(C=0.5), w.qwen3_round(C=0.25),
                  w.llama3_round_at_scale(), w.llama3_round(T=0.0)):
-        g = torch.Generator(device=device)
-        g.manual_seed(11)
-        shape = (spec.B, spec.K + 1, spec.V)
-        rank = torch.argsort(torch.rand(shape, generator=g, device=device), dim=-1).float() + 1
-        zt = -spec.zipf_slope * torch.log(rank) + spec.target_noise * torch.randn(
-            shape, generator=g, device=device)
-        del rank
-        zd = zt + spec.draft_noise * torch.randn(shape, generator=g, device=device)
-        sets = []
-        per = w.round_bytes(spec)
-        nsets = max(2, int(np.ceil(3 * L2_BYTES / per)) + 1) if per < 2 * L2_BYTES else 1
-        for _ in range(nsets):
-            sets.append((zt.to(torch.bfloat16), zd.to(torch.bfloat16)))
-        del zt, zd
-        u = torch.rand(3, spec.B, spec.K + 1, generator=g, device=device)
-        ud, ua, ub = u[0, :, :spec.K].contiguous(), u[1, :, :spec.K].contiguous(), u[2, :, 0].contiguous()
+        sets, nsets, per, (ud, ua, ub) = device_round_sets(spec, device, 11)
         out = make_outputs(spec, device)
         ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
 
@@ -680,6 +789,18 @@ def probe(which):
         torch.cuda.synchronize()
         print(json.dumps({"probe": which, "workload": spec.name, "status": int(out["status"].item())}))
         return
+    if which == "fallback":
+        spec = w.qwen3_histories()
+        h = w.make_histories(spec, seed=21)
+        hist, hl = torch.from_numpy(h.hist).to(device), torch.from_numpy(h.hist_len).to(device)
+        slot, u = torch.from_numpy(h.slot).to(device), torch.from_numpy(h.u_rand).to(device)
+        nxt = torch.empty(spec.B, spec.K, dtype=torch.int32, device=device)
+        st = torch.zeros(1, dtype=torch.int32, device=device)
+        for _ in range(3):
+            ssd.ssd_ngram_backup(hist, hl, spec.n, spec.K, spec.V, u, nxt, slot=slot, status=st)
+        torch.cuda.synchronize()
+        print(json.dumps({"probe": which, "workload": spec.name, "status": int(st.item())}))
+        return
     spec = w.draft_branch_attention() if which == "attn-draft" else w.verify_attention_at_scale()
     q, kc, vc, table, prefix, parent, N, Nq = device_attention_inputs(spec, device, 7)
     out = torch.empty_like(q)
@@ -703,7 +824,7 @@ def main(argv=None):
                     help="reference arm: sequences per host core per step (capped at one batch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e / attention / other rounds")
-    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify"),
+    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify", "fallback"),
                     help="only run a few calls of one workload (for profilers) and exit")
     args = ap.parse_args(argv)
     if args.probe:

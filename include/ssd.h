@@ -7,7 +7,8 @@
  *       section "SSD 如何實現草擬與驗證并行？".
  *   [B] technical summary "超越传统SD：SSD框架全异步解码实现4.7倍平均加速",
  *       sections "投机解码的瓶颈与 SSD 的核心机制", "Saguaro 算法：解决异步推测的三大挑战"
- *       (part 1 "验证结果预测与缓存拓扑优化", part 2 "操纵残差分布") and
+ *       (part 1 "验证结果预测与缓存拓扑优化", part 2 "操纵残差分布", part 3
+ *       "大 Batch 下的退避策略") and
  *       "工程优化与系统表现".
  * The pages' formulas did not survive extraction; where a call fills a gap
  * the reading is stated at the call.
@@ -75,6 +76,9 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
 #define SSD_FLAG_BAD_BLOCK 32u    /* attention: block id outside [0, num_blocks): keys hidden */
 #define SSD_FLAG_BAD_PREFIX 64u   /* attention: prefix_len < 0 or prefix_len + N > 16 maxb:  */
                                   /* keys past the block table are hidden                   */
+#define SSD_FLAG_BAD_HISTORY 128u /* backup: hist_len outside [0, hist_stride]: taken as 0  */
+#define SSD_FLAG_BAD_RATE 256u    /* plan: p_hit outside [0, 1] or e_hit < 0 / not finite:  */
+                                  /* clamped into [0, 1], taken as 0                        */
 
 /* Human-readable name of a status code (static string). */
 const char *ssd_status_string(ssd_status_t st);
@@ -311,6 +315,73 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
                                   int Nq, int Hq, int Hkv, int d, float scale, void *out,
                                   float *lse, uint32_t *status, void *ws, size_t ws_bytes,
                                   ssd_stream_t s);
+
+/*
+ * Miss fallback [B, "Saguaro 算法" part 3 "大 Batch 下的退避策略": a sequence
+ * whose outcome missed the speculation cache falls back to synchronous
+ * speculation with a backup speculator, and one miss holds up the whole batch
+ * for the backup's latency; beyond a batch size set by the hit rate and the
+ * latencies a backup of almost no latency (random tokens or an n-gram model)
+ * is the better choice].
+ *
+ * ssd_ngram_backup: the n-gram backup for the sequences that missed.  Reading
+ * (the pages name the backup only): history row b is hist[b*hist_stride ..
+ * + hist_len[b]) (int32 token ids, positions 0..L-1), s = its last n tokens;
+ * the latest earlier occurrence m (the largest m with m + n <= L - 1 and
+ * h[m..m+n) = s) proposes next_tokens[b, t] = h[m + n + t] for t < K while
+ * m + n + t < L; every other position, and every position when s occurs
+ * nowhere earlier or L < n + 1, takes the random-token backup
+ * floor(u_rand[b, t] * V) (exactly: ((uint64)(u * 2^24) * V) >> 24; u is
+ * clamped into [0, 1)).  n = 0 gives the random-token backup alone.
+ *   slot [B]        the cache lookup's slot: rows with slot[b] >= 0 are hits
+ *                   and are left untouched (NULL: every row missed).
+ *   plan_best       device int32[1] from ssd_fallback_plan, or NULL: when it
+ *                   equals random_option the history is not searched (the
+ *                   random-token backup alone), so the policy runs without a
+ *                   host round trip.
+ *   next_tokens [B, K]  written for missed rows (the cache lookup writes -1
+ *                   there).  match_pos [B] (or NULL) = m, -1 without a match,
+ *                   -2 for a hit.
+ * Supported: 0 <= n <= 32, 0 <= K <= 1024, V >= 1, hist_stride <= 2^30
+ * (hist and hist_len may be NULL when n = 0; u_rand [B, K] fp32).  A copied
+ * token outside [0, V) sets BAD_TOKEN and takes the random token instead;
+ * hist_len[b] outside [0, hist_stride] sets BAD_HISTORY and counts as 0.
+ * One CTA per sequence; a missed sequence scans its history backwards in
+ * chunks of 4096 positions and stops at the first chunk holding a match.
+ */
+ssd_status_t ssd_ngram_backup(const int32_t *hist, int64_t hist_stride, const int32_t *hist_len,
+                              int B, int n, int K, int V, const int32_t *slot,
+                              const float *u_rand, const int32_t *plan_best, int random_option,
+                              int32_t *next_tokens, int32_t *match_pos, uint32_t *status,
+                              ssd_stream_t s);
+
+/*
+ * ssd_fallback_plan: the batch-level speedup model and the backup choice.
+ * Reading (the pages' formula did not survive extraction; restated from [B,
+ * "投机解码的瓶颈与 SSD 的核心机制"]: the primary speculator drafts for the
+ * predicted outcomes while the target verifies, so a round whose outcome hits
+ * costs max(T_v, T_p); a miss falls back to synchronous speculation with
+ * backup o and holds the batch up for T_b[o]).  With independent hits of
+ * probability p_hit[b] (e.g. ssd_round_analytics' hit_rate) and expected
+ * tokens e_hit[b] per round after a hit (e.g. its exp_tokens), for each of the
+ * nopt backups o (T_b[o] its latency, e_miss[o] the expected tokens of a round
+ * after a miss):
+ *   time[o]       = max(T_v, T_p) + (1 - prod_b p_hit[b]) * T_b[o]
+ *   tokens[o]     = sum_b (p_hit[b] e_hit[b] + (1 - p_hit[b]) e_miss[o])
+ *   throughput[o] = tokens[o] / time[o]
+ *   speedup[o]    = throughput[o] / (sum_b e_hit[b] / (T_p + T_v))  (against
+ *                   synchronous speculation with the primary)
+ *   best[0]       = the o of largest throughput (lowest index on ties)
+ * p_hit, e_hit: device fp32 [B]; T_v, T_p, T_b[nopt], e_miss[nopt]: host fp64
+ * (times in any one unit); outputs device fp64 [nopt] and int32[1], each may
+ * be NULL.  Sums and the product are taken in fp64.  Requires B >= 1,
+ * 1 <= nopt <= 8, T_v, T_p >= 0 with T_v + T_p > 0, T_b and e_miss finite and
+ * >= 0 (else SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED).
+ */
+ssd_status_t ssd_fallback_plan(const float *p_hit, const float *e_hit, int B, double T_v,
+                               double T_p, int nopt, const double *T_b, const double *e_miss,
+                               double *time, double *tokens, double *throughput, double *speedup,
+                               int32_t *best, uint32_t *status, ssd_stream_t s);
 
 #ifdef __cplusplus
 }

@@ -24,12 +24,15 @@ FLAG_BAD_OUTCOME = 8
 FLAG_BAD_TREE = 16
 FLAG_BAD_BLOCK = 32
 FLAG_BAD_PREFIX = 64
+FLAG_BAD_HISTORY = 128
+FLAG_BAD_RATE = 256
 
 EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_set_timing_events", "ssd_set_trace",
            "ssd_saguaro_sample",
            "ssd_verify", "ssd_verify_noalloc", "ssd_verify_noalloc_max_bytes",
            "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round", "ssd_round_analytics",
-           "ssd_attention_workspace_size", "ssd_branch_attention")
+           "ssd_attention_workspace_size", "ssd_branch_attention", "ssd_ngram_backup",
+           "ssd_fallback_plan")
 
 _lib = None
 
@@ -106,6 +109,12 @@ def _declare(lib):
     lib.ssd_branch_attention.argtypes = [_vp, _vp, _vp, _vp, _i, _i64, _vp, _vp, _i, _i, _i, _i, _i,
                                          _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.ssd_branch_attention.restype = _i
+    lib.ssd_ngram_backup.argtypes = [_vp, _i64, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp,
+                                     _vp, _vp]
+    lib.ssd_ngram_backup.restype = _i
+    lib.ssd_fallback_plan.argtypes = [_vp, _vp, _i, _d, _d, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp]
+    lib.ssd_fallback_plan.restype = _i
 
 
 # ---------------------------------------------------------------------------
@@ -323,3 +332,35 @@ def ssd_branch_attention(q, k_cache, v_cache, block_table, prefix_len, parent, o
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], nb,
         _ptr(prefix_len), _ptr(parent), B, N, Nq, Hq, Hkv, d, float(scale), _ptr(out), _ptr(lse),
         _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_ngram_backup(hist, hist_len, n, K, V, u_rand, next_tokens, slot=None, match_pos=None,
+                     plan_best=None, random_option=-1, status=None, stream=None):
+    """Fill the missed rows of ``next_tokens`` [B, K] from an n-gram lookup in
+    each sequence's history ``hist`` [B, cap] (int32, ``hist_len`` [B] valid),
+    else random tokens floor(u_rand V)."""
+    B = next_tokens.shape[0] if next_tokens is not None else u_rand.shape[0]
+    stride = 0
+    if hist is not None:
+        if hist.dtype != torch.int32 or hist.dim() != 2 or not hist.is_contiguous():
+            raise ValueError("hist must be a contiguous int32 [B, cap] tensor")
+        stride = hist.shape[1]
+    _check("ssd_ngram_backup", load().ssd_ngram_backup(
+        _ptr(hist), stride, _ptr(hist_len), B, int(n), int(K), int(V), _ptr(slot), _ptr(u_rand),
+        _ptr(plan_best), int(random_option), _ptr(next_tokens), _ptr(match_pos), _ptr(status),
+        _stream(stream)))
+
+
+def ssd_fallback_plan(p_hit, e_hit, T_v, T_p, T_b, e_miss, time=None, tokens=None, throughput=None,
+                      speedup=None, best=None, status=None, stream=None):
+    """Expected round time, tokens, throughput and speedup of each backup option
+    (host lists ``T_b``, ``e_miss``) for the batch's hit probabilities ``p_hit``
+    and tokens ``e_hit`` (device fp32 [B]); ``best`` gets the chosen option."""
+    nopt = len(T_b)
+    if len(e_miss) != nopt:
+        raise ValueError("T_b and e_miss must have one entry per option")
+    tb = (ctypes.c_double * max(nopt, 1))(*[float(x) for x in T_b])
+    em = (ctypes.c_double * max(nopt, 1))(*[float(x) for x in e_miss])
+    _check("ssd_fallback_plan", load().ssd_fallback_plan(
+        _ptr(p_hit), _ptr(e_hit), p_hit.shape[0], float(T_v), float(T_p), nopt, tb, em, _ptr(time),
+        _ptr(tokens), _ptr(throughput), _ptr(speedup), _ptr(best), _ptr(status), _stream(stream)))

@@ -18,6 +18,8 @@ constexpr uint32_t kFlagBadOutcome = 8u;
 constexpr uint32_t kFlagBadTree = 16u;
 constexpr uint32_t kFlagBadBlock = 32u;
 constexpr uint32_t kFlagBadPrefix = 64u;
+constexpr uint32_t kFlagBadHistory = 128u;
+constexpr uint32_t kFlagBadRate = 256u;
 
 // Upper bound on polls of an mbarrier before a wait gives up and reports
 // SSD_FLAG_WAIT_TIMEOUT (each poll may suspend the thread for a short,

@@ -491,19 +491,26 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ V
     float m1 = NEG_INF;
     int k1 = -1;
     if constexpr (E::kSize == 2) {
+      // a segment wholly inside the row needs no validity checks (warp-uniform)
+      const bool full = v0 + kSegVec <= a.nvec;
       uint32_t mm = 0xFF80FF80u;
 #pragma unroll
       for (int k = 0; k < kSegBlocks; ++k) {
         const uint32_t t = bmax2(bmax2(w[k].x, w[k].y), bmax2(w[k].z, w[k].w));
         mm = bmax2(mm, t);
-        if (rs.keys || rs.arg) {
+        if (rs.keys) {
+          // the vector maximum's key from its bf16 bits: the upper half of the
+          // order-preserving key of its float value (the lower half is not needed)
+          const uint32_t h = bmax2(t, __byte_perm(t, 0, 0x1032)) & 0xFFFFu;
+          uint32_t key = ((h & 0x8000u) ? (h ^ 0xFFFFu) : (h | 0x8000u)) << 16;
+          if (!full && v0 + 32 * k + lane >= a.nvec) key = 0u;
+          key = __reduce_max_sync(0xffffffffu, key);
+          if (lane == k) bk = key;
+        }
+        if (rs.arg) {
           const float vm = fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
-          const bool valid = v0 + 32 * k + lane < a.nvec;
-          if (rs.keys) {
-            const uint32_t key = __reduce_max_sync(0xffffffffu, valid ? f2ord(vm) : 0u);
-            if (lane == k) bk = key;
-          }
-          if (rs.arg && valid && (vm > m1 || k1 < 0)) {  // strictly larger: the first vector among equal maxima
+          const bool valid = full || v0 + 32 * k + lane < a.nvec;
+          if (valid && (vm > m1 || k1 < 0)) {  // strictly larger: the first vector among equal maxima
             m1 = fmaxf(m1, vm);
             k1 = k;
           }

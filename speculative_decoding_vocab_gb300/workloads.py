@@ -17,6 +17,9 @@ Contents
   Gaussian logits and Zipf-shaped logits over a seeded permutation, with the
   draft equal to the target plus Gaussian noise.
 * paged KV caches, block tables and branch trees for tree-masked attention.
+* token histories for the miss fallback: Zipf-distributed tokens in which
+  spans repeat earlier spans (the repetition an n-gram backup feeds on), with
+  a seeded set of sequences that missed the speculation cache.
 """
 from __future__ import annotations
 
@@ -38,6 +41,7 @@ _MASK32 = np.uint64(0xFFFFFFFF)
 SLOT_DRAFT = 0   # u_draft[b, j]: the uniform the draft's inverse-CDF draw uses
 SLOT_ACCEPT = 1  # u_acc[b, j]: the uniform of the acceptance test at position j
 SLOT_BONUS = 2   # u_bonus[b]: the uniform of the residual / bonus draw
+SLOT_BACKUP = 3  # u_rand[b, t]: the uniform of the random-token backup at position t
 
 
 def philox4x32_10(counter: np.ndarray, key: tuple[int, int]) -> np.ndarray:
@@ -382,6 +386,97 @@ def round_bytes(spec: RoundSpec) -> int:
     logit read once."""
     elem = 4 if spec.dtype == "f32" else 2
     return 2 * spec.B * (spec.K + 1) * spec.V * elem
+
+
+# ---------------------------------------------------------------------------
+# Token histories for the miss fallback
+# ---------------------------------------------------------------------------
+def backup_uniforms(seed: int, rnd: int, B: int, K: int) -> np.ndarray:
+    """``u_rand[B, K]``: the uniforms of the random-token backup (Philox counter
+    (round, sequence, SLOT_BACKUP, position))."""
+    key = (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    b = np.arange(B, dtype=np.uint32)[:, None]
+    j = np.arange(K, dtype=np.uint32)[None, :]
+    ctr = np.stack(np.broadcast_arrays(np.uint32(rnd & 0xFFFFFFFF), b, np.uint32(SLOT_BACKUP), j),
+                   axis=-1)
+    return uniforms_from_bits(philox4x32_10(ctr, key)[..., 0])
+
+
+@dataclass
+class HistorySpec:
+    """Shape and value recipe of the histories a miss-fallback call reads."""
+    B: int
+    K: int
+    V: int
+    L_min: int                 # history lengths ~ uniform integers in [L_min, L_max]
+    L_max: int
+    cap: int = 0               # row capacity (>= L_max; 0: L_max)
+    n: int = 3                 # n-gram length
+    zipf_slope: float = 1.1    # fresh tokens: P(rank r) ~ r^-slope over a seeded permutation
+    copy_prob: float = 0.3     # a span repeats an earlier span with this chance
+    span_min: int = 4          # span lengths ~ uniform integers in [span_min, span_max]
+    span_max: int = 32
+    miss_rate: float = 0.3     # each sequence missed the cache with this chance
+    name: str = ""
+
+
+@dataclass
+class HistoryInputs:
+    spec: HistorySpec
+    hist: np.ndarray           # [B, cap] int32, zero past hist_len
+    hist_len: np.ndarray       # [B] int32
+    slot: np.ndarray           # [B] int32: -1 for a miss, else a cache slot
+    u_rand: np.ndarray         # [B, K] float32
+
+
+def _zipf_sampler(rng, V: int, slope: float):
+    perm = rng.permutation(V).astype(np.int32)
+    w = np.arange(1, V + 1, dtype=np.float64) ** -slope
+    cdf = np.cumsum(w)
+    cdf /= cdf[-1]
+
+    def draw(n):
+        r = np.minimum(np.searchsorted(cdf, rng.random(n), side="right"), V - 1)
+        return perm[r]
+    return draw
+
+
+def make_histories(spec: HistorySpec, seed: int = 0, rnd: int = 0) -> HistoryInputs:
+    """Seeded histories: fresh Zipf tokens in spans, each span after the first
+    copying an earlier span of the same sequence with chance ``copy_prob``."""
+    rng = np.random.default_rng(seed)
+    cap = spec.cap or spec.L_max
+    draw = _zipf_sampler(rng, spec.V, spec.zipf_slope)
+    lens = rng.integers(spec.L_min, spec.L_max + 1, size=spec.B).astype(np.int32)
+    hist = np.zeros((spec.B, cap), np.int32)
+    for b in range(spec.B):
+        L = int(lens[b])
+        h = draw(L).astype(np.int32)
+        pos = 0
+        while pos < L:
+            s = int(rng.integers(spec.span_min, spec.span_max + 1))
+            s = min(s, L - pos)
+            if pos >= s and rng.random() < spec.copy_prob:
+                src = int(rng.integers(0, pos - s + 1))
+                h[pos:pos + s] = h[src:src + s]
+            pos += s
+        hist[b, :L] = h
+    slot = np.where(rng.random(spec.B) < spec.miss_rate, -1,
+                    rng.integers(0, 64, size=spec.B)).astype(np.int32)
+    return HistoryInputs(spec, hist, lens, slot, backup_uniforms(seed, rnd, spec.B, spec.K))
+
+
+def qwen3_histories(B: int = 256) -> HistorySpec:
+    """The large-batch Qwen-3 round's batch and vocabulary, with prompt+generation
+    histories of 1-8 Ki tokens and the 3-gram backup."""
+    return HistorySpec(B=B, K=4, V=151936, L_min=1024, L_max=8192, n=3,
+                       name=f"qwen3-ngram-backup-B{B}-K4-V151936-L1k-8k-n3")
+
+
+def tiny_histories() -> HistorySpec:
+    return HistorySpec(B=48, K=6, V=50, L_min=0, L_max=700, cap=704, n=2, zipf_slope=0.8,
+                       copy_prob=0.4, span_min=2, span_max=9, miss_rate=0.7,
+                       name="tiny-ngram-backup-B48-K6-V50-L0-700-n2")
 
 
 def ceil_div(a: int, b: int) -> int:
