@@ -87,6 +87,8 @@ def _declare(lib):
     lib.oracle_ngram_backup.restype = _i
     lib.oracle_fallback_plan.argtypes = [_p, _p, _i, _d, _d, _i, _p, _p, _p, _p, _p, _p]
     lib.oracle_fallback_plan.restype = _i
+    lib.oracle_kv_append.argtypes = [_p, _p, _p, _p, _p, _i, _i64, _p, _i, _i, _i, _i, _i, _p]
+    lib.oracle_kv_append.restype = _i
 
 
 def _ptr(a):
@@ -308,3 +310,33 @@ def fallback_plan(p_hit, e_hit, T_v, T_p, T_b, e_miss):
                                                                             "speedup")])
     out["best"] = int(best)
     return out
+
+
+def fill_sample(logits, V, F_t, C, T, u):
+    """One branch-decode draw: every branch row (b, s) of ``logits`` [B, S, V']
+    is sampled with the Saguaro scheme sigma_{F_t, C} (a one-row
+    ``saguaro_sample``).  Returns (tokens [B, S], q' of the token, margin)."""
+    logits = np.ascontiguousarray(logits)
+    B, S, Vp = logits.shape
+    rows = logits.reshape(B * S, 1, Vp)
+    pad = np.zeros((B * S, 1, Vp), logits.dtype)
+    d, qd, mg = saguaro_sample(np.concatenate([rows, pad], axis=1), V, (int(F_t), 0), C, T,
+                               np.asarray(u, np.float32).reshape(B * S, 1))
+    return d.reshape(B, S), qd.reshape(B, S), mg.reshape(B, S)
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_table, prefix_len, node0):
+    """Append rows ``k_new``/``v_new`` [B, S, Hkv, d] (bf16 bits, uint16) to
+    copies of the paged caches [num_blocks, Hkv, 16, d] at logical positions
+    prefix_len[b] + node0 + i.  Returns (k_cache', v_cache', flags [B])."""
+    k_new = np.ascontiguousarray(k_new, np.uint16)
+    v_new = np.ascontiguousarray(v_new, np.uint16)
+    kc = np.array(k_cache, np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, np.uint16, copy=True, order="C")
+    bt = _c(block_table, np.int32)
+    pl = _c(prefix_len, np.int32)
+    B, S, Hkv, d = k_new.shape
+    flags = np.zeros(B, np.uint32)
+    _L().oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                          kc.shape[0], _ptr(pl), int(node0), B, S, Hkv, d, _ptr(flags))
+    return kc, vc, flags

@@ -693,3 +693,51 @@ int oracle_fallback_plan(const float *p_hit, const float *e_hit, int B, double T
   }
   return best;
 }
+
+/* ===========================================================================
+ * Speculation-cache fill by branch decode (technical summary
+ * "超越传统SD：SSD框架全异步解码实现4.7倍平均加速", "投机解码的瓶颈与 SSD 的核心机制":
+ * the draft pre-speculates a continuation for every predicted outcome while
+ * the target verifies; "工程优化与系统表现": all F_k branches are decoded in one
+ * forward pass).  Each decode step feeds one token per branch: its key and
+ * value rows are appended to the paged cache at the branch node's position,
+ * and the next token of every branch is drawn from the draft's logits with
+ * the Saguaro scheme (the draw itself is oracle_saguaro_sample on one row).
+ * ======================================================================== */
+
+/* Append the key/value rows of S new tree nodes per sequence to a paged
+ * cache [num_blocks, Hkv, 16, d] (bf16 bits): row (b, i, h) goes to logical
+ * position pos = prefix_len[b] + node0 + i, i.e. page block_table[b, pos/16],
+ * slot pos % 16.  A position past the block table (pos / 16 >= maxb) or a
+ * negative prefix writes nothing and sets flag 64 for the sequence; a page id
+ * outside [0, num_blocks) writes nothing and sets flag 32. */
+int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache,
+                     const int32_t *block_table, int maxb, int64_t num_blocks, const int32_t *prefix_len,
+                     int node0, int B, int S, int Hkv, int d, uint32_t *flags) {
+  const int page = 16;
+  for (int b = 0; b < B; ++b) {
+    uint32_t fl = 0;
+    for (int i = 0; i < S; ++i) {
+      const int64_t pos = (int64_t)prefix_len[b] + node0 + i;
+      if (prefix_len[b] < 0 || pos / page >= maxb) {
+        fl |= 64u;
+        continue;
+      }
+      const int64_t blk = block_table[(int64_t)b * maxb + pos / page];
+      if (blk < 0 || blk >= num_blocks) {
+        fl |= 32u;
+        continue;
+      }
+      for (int h = 0; h < Hkv; ++h) {
+        const int64_t src = (((int64_t)b * S + i) * Hkv + h) * d;
+        const int64_t dst = ((blk * Hkv + h) * page + pos % page) * d;
+        for (int e = 0; e < d; ++e) {
+          k_cache[dst + e] = k_new[src + e];
+          v_cache[dst + e] = v_new[src + e];
+        }
+      }
+    }
+    if (flags) flags[b] = fl;
+  }
+  return 0;
+}

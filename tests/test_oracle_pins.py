@@ -876,3 +876,79 @@ def test_fallback_plan_crossover_with_batch_size():
     assert best[0] == 0 and best[-1] == 1
     changes = sum(1 for a, b in zip(best, best[1:]) if a != b)
     assert changes == 1
+
+
+# ---------------------------------------------------------------------------
+# cache fill by branch decode: the paged K/V append and the per-branch draw
+# ---------------------------------------------------------------------------
+def _logical(cache, block_table, b, npos):
+    """Positions 0..npos-1 of sequence b gathered through the block table."""
+    pos = np.arange(npos)
+    return cache[block_table[b, pos // 16], :, pos % 16, :]  # [npos, Hkv, d]
+
+
+def test_kv_append_matches_dense_placement():
+    """Gathering the paged caches back in logical order equals a dense history
+    with the new rows assigned at prefix + node0 + i (page boundaries crossed,
+    pages out of order); nothing else changes."""
+    rng = np.random.default_rng(3)
+    B, S, Hkv, d, maxb = 3, 21, 2, 8, 6
+    nb = B * maxb
+    table = rng.permutation(nb).astype(np.int32).reshape(B, maxb)
+    kc = rng.integers(0, 1 << 16, size=(nb, Hkv, 16, d)).astype(np.uint16)
+    vc = rng.integers(0, 1 << 16, size=(nb, Hkv, 16, d)).astype(np.uint16)
+    kn = rng.integers(0, 1 << 16, size=(B, S, Hkv, d)).astype(np.uint16)
+    vn = rng.integers(0, 1 << 16, size=(B, S, Hkv, d)).astype(np.uint16)
+    prefix = np.array([0, 13, 40], np.int32)
+    node0 = 5
+    k2, v2, fl = oracle.kv_append(kn, vn, kc, vc, table, prefix, node0)
+    assert fl.tolist() == [0, 0, 0]
+    npos = 16 * maxb
+    for b in range(B):
+        for new, old, got in ((kn, kc, k2), (vn, vc, v2)):
+            want = _logical(old, table, b, npos).copy()
+            p0 = prefix[b] + node0
+            want[p0:p0 + S] = new[b]
+            np.testing.assert_array_equal(_logical(got, table, b, npos), want)
+    # pages outside every table stay as they were (here: none), and the touched
+    # count is exactly B * S rows per head
+    changed = (k2 != kc).any(axis=3).sum()
+    assert changed <= B * S * Hkv
+
+
+def test_kv_append_flags_and_skips():
+    rng = np.random.default_rng(4)
+    B, S, Hkv, d, maxb = 3, 4, 1, 4, 2
+    kc = np.zeros((4, Hkv, 16, d), np.uint16)
+    table = np.array([[0, 1], [2, 9], [3, 3]], np.int32)   # sequence 1: page id 9 is invalid
+    kn = rng.integers(1, 1 << 16, size=(B, S, Hkv, d)).astype(np.uint16)
+    prefix = np.array([30, 14, -1], np.int32)              # seq 0 runs past the table
+    k2, v2, fl = oracle.kv_append(kn, kn, kc, kc, table, prefix, 0)
+    assert fl.tolist() == [64, 32, 64]
+    # seq 0: positions 30, 31 are written; 32, 33 are past the table
+    np.testing.assert_array_equal(k2[1, 0, 14:16], kn[0, :2, 0])
+    # seq 1: positions 14, 15 on page 2; 16, 17 on the invalid page: skipped
+    np.testing.assert_array_equal(k2[2, 0, 14:16], kn[1, :2, 0])
+    assert not k2[3].any() and not k2[0].any()
+
+
+def test_fill_sample_routing():
+    """Each branch row is drawn with its own uniform and the depth's F_t:
+    equal logits give floor(u V) (u dyadic, so exact), and a dominant token is
+    avoided only when F_t >= 1 and C is small."""
+    B, S, V = 2, 5, 8
+    z = np.zeros((B, S, V), np.float32)
+    u = (np.arange(B * S, dtype=np.float64).reshape(B, S) % 8 + 0.5) / 8
+    tok, q, _ = oracle.fill_sample(z, V, 0, 1.0, 1.0, u.astype(np.float32))
+    np.testing.assert_array_equal(tok, np.floor(u * V).astype(int))
+    np.testing.assert_allclose(q, 1.0 / V, rtol=1e-12)
+    z2 = np.zeros((B, S, V), np.float32)
+    for b in range(B):
+        for s in range(S):
+            z2[b, s, (3 * b + s) % V] = 6.0   # one dominant token per row
+    uu = np.full((B, S), 0.3, np.float32)
+    t0, q0, _ = oracle.fill_sample(z2, V, 0, 1e-4, 1.0, uu)
+    t1, q1, _ = oracle.fill_sample(z2, V, 1, 1e-4, 1.0, uu)
+    dom = (3 * np.arange(B)[:, None] + np.arange(S)[None, :]) % V
+    assert (t0 == dom).all()          # F_t = 0: no down-weighting, the dominant token
+    assert (t1 != dom).all()          # F_t = 1, C = 1e-4: the dominant token is avoided
