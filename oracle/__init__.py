@@ -89,6 +89,9 @@ def _declare(lib):
     lib.oracle_fallback_plan.restype = _i
     lib.oracle_kv_append.argtypes = [_p, _p, _p, _p, _p, _i, _i64, _p, _i, _i, _i, _i, _i, _p]
     lib.oracle_kv_append.restype = _i
+    lib.oracle_tree_verify.argtypes = [_p, _p, _i, _i64, _i64, _i, _i, _i, _d, _p, _p, _p, _p, _p, _p,
+                                       _p, _p, _p, _p, _p]
+    lib.oracle_tree_verify.restype = _i
 
 
 def _ptr(a):
@@ -340,3 +343,35 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_table, prefix_len, node0):
     _L().oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
                           kc.shape[0], _ptr(pl), int(node0), B, S, Hkv, d, _ptr(flags))
     return kc, vc, flags
+
+
+def tree_verify(target, draft, V, T, parent, tokens, u_acc, u_bonus):
+    """Token-tree verification; logits [B, N+1, V'] (row 0: the root, row m+1:
+    after node m; a view broadcast over B with stride 0 is read as is),
+    parent/tokens/u_acc [B, N], u_bonus [B].  Returns a dict of accept_len,
+    path [B, N], bonus, resid_mass, flags, acc_margin [B, N], bonus_margin."""
+    assert target.shape == draft.shape and target.dtype == draft.dtype
+    B, N1, W = target.shape
+    N = N1 - 1
+    es = target.itemsize
+
+    def base(a):
+        if a.strides[0] == 0:  # one set of rows shared by every sequence
+            return np.ascontiguousarray(a[0])[None], 0
+        return np.ascontiguousarray(a), N1 * W
+    t_arr, ss = base(target)
+    d_arr, ss2 = base(draft)
+    assert ss == ss2
+    par = _c(parent, np.int32)
+    tok = _c(tokens, np.int32)
+    ua = _c(u_acc, np.float32)
+    ub = _c(u_bonus, np.float32)
+    out = dict(accept_len=np.zeros(B, np.int32), path=np.zeros((B, N), np.int32),
+               bonus=np.zeros(B, np.int32), resid_mass=np.zeros(B, np.float64),
+               flags=np.zeros(B, np.uint32), acc_margin=np.zeros((B, N), np.float64),
+               bonus_margin=np.zeros(B, np.float64))
+    _L().oracle_tree_verify(_ptr(t_arr), _ptr(d_arr), _dtype_code(t_arr), ss, W, B, N, int(V),
+                            float(T), _ptr(par), _ptr(tok), _ptr(ua), _ptr(ub),
+                            *[_ptr(out[k]) for k in ("accept_len", "path", "bonus", "resid_mass",
+                                                     "flags", "acc_margin", "bonus_margin")])
+    return out

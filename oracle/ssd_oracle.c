@@ -741,3 +741,110 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_c
   }
   return 0;
 }
+
+/* ===========================================================================
+ * Token-tree verification with several candidates per node (the 機器之心
+ * article "全球最強推理引擎還快2倍，斯坦福、普林斯頓破解大模型串行魔咒" names
+ * combining SSD with token-tree speculation as future work; the technical
+ * summary "超越传统SD：SSD框架全异步解码实现4.7倍平均加速" states the single-chain
+ * acceptance rule and the residual p_target - p_draft that this generalises).
+ * Reading: the children of a node were drawn independently from the draft's
+ * distribution q at that node; they are tested one after another against a
+ * target distribution r that starts as p and, after each rejection, becomes
+ * the normalised residual max(0, r - q) / sum max(0, r - q), so that the token
+ * finally emitted at the node follows p (the multi-draft form of the
+ * single-chain rule).
+ * ======================================================================== */
+
+/* Logits [B, N+1, V]: row 0 holds the distributions after the prefix (the
+ * root), row m+1 those after tree node m.  parent [B, N]: parent[m] in
+ * [-1, m-1] (-1 the root); tokens [B, N]; u_acc [B, N] the uniform of node m's
+ * test; u_bonus [B].  Per sequence, from the root:
+ *   p = softmax(target row / T), q = softmax(draft row / T), r = p;
+ *   for each child c of the node in index order (token x):
+ *     x outside [0, V): BAD_TOKEN, the child is skipped;
+ *     accept iff u_acc[c] * q(x) < r(x) -> the walk moves to c;
+ *     else W = sum max(0, r - q); r = max(0, r - q) / W when W > 0, else
+ *          ZERO_RESIDUAL and r stays;
+ *   no child accepted: bonus ~ r by inverse CDF with u_bonus; stop.
+ * A node whose parent lies outside [-1, m-1] is nobody's child (BAD_TREE).
+ * T = 0: one-hot p and q at the argmaxes (lowest index on ties).
+ * Outputs: accept_len[b] = accepted nodes, path[b, 0..] their indices (-1
+ * after), bonus[b]; resid_mass[b] = the W of the last residual taken at the
+ * final node (1 when its r is p); acc_margin[b, c] = |u - r(x)/q(x)| for
+ * tested children (inf otherwise and at T = 0); bonus_margin as in
+ * oracle_inv_cdf (inf at T = 0). */
+int oracle_tree_verify(const void *target, const void *draft, int dtype, int64_t seq_stride,
+                       int64_t row_stride, int B, int N, int V, double T, const int32_t *parent,
+                       const int32_t *tokens, const float *u_acc, const float *u_bonus,
+                       int32_t *accept_len, int32_t *path, int32_t *bonus, double *resid_mass,
+                       uint32_t *flags, double *acc_margin, double *bonus_margin) {
+  double *zt = (double *)malloc(sizeof(double) * (size_t)V);
+  double *zd = (double *)malloc(sizeof(double) * (size_t)V);
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  double *q = (double *)malloc(sizeof(double) * (size_t)V);
+  double *r = (double *)malloc(sizeof(double) * (size_t)V);
+  for (int b = 0; b < B; b++) {
+    const int32_t *par = parent + (int64_t)b * N;
+    const int32_t *tok = tokens + (int64_t)b * N;
+    uint32_t fl = 0;
+    for (int m = 0; m < N; m++) {
+      path[(int64_t)b * N + m] = -1;
+      if (acc_margin) acc_margin[(int64_t)b * N + m] = INFINITY;
+      if (par[m] < -1 || par[m] >= m) fl |= OR_FLAG_BAD_TREE;
+    }
+    int node = -1, L = 0;
+    double Wlast = 1.0;
+    for (;;) {
+      const int64_t off = b * seq_stride + (int64_t)(node + 1) * row_stride;
+      load_row(target, dtype, off, V, zt);
+      load_row(draft, dtype, off, V, zd);
+      oracle_softmax(zt, V, T, p);
+      oracle_softmax(zd, V, T, q);
+      memcpy(r, p, sizeof(double) * (size_t)V);
+      Wlast = 1.0;
+      int next = -1;
+      for (int c = node + 1; c < N && next < 0; c++) {
+        if (par[c] != node) continue;
+        const int x = tok[c];
+        if (x < 0 || x >= V) {
+          fl |= OR_FLAG_BAD_TOKEN;
+          continue;
+        }
+        const double u = (double)u_acc[(int64_t)b * N + c];
+        if (acc_margin && T != 0.0 && q[x] > 0.0) acc_margin[(int64_t)b * N + c] = fabs(u - r[x] / q[x]);
+        if (u * q[x] < r[x]) {
+          next = c;
+          break;
+        }
+        double W = 0.0;
+        for (int i = 0; i < V; i++) W += (r[i] > q[i]) ? r[i] - q[i] : 0.0;
+        if (W > 0.0) {
+          for (int i = 0; i < V; i++) r[i] = (r[i] > q[i]) ? (r[i] - q[i]) / W : 0.0;
+          Wlast = W;
+        } else {
+          fl |= OR_FLAG_ZERO_RESIDUAL;
+        }
+      }
+      if (next >= 0) {
+        path[(int64_t)b * N + L] = next;
+        L++;
+        node = next;
+        continue;
+      }
+      double bm = INFINITY;
+      bonus[b] = oracle_inv_cdf(r, V, (double)u_bonus[b], &bm);
+      if (bonus_margin) bonus_margin[b] = (T == 0.0) ? INFINITY : bm;
+      break;
+    }
+    accept_len[b] = L;
+    if (resid_mass) resid_mass[b] = Wlast;
+    if (flags) flags[b] = fl;
+  }
+  free(zt);
+  free(zd);
+  free(p);
+  free(q);
+  free(r);
+  return 0;
+}

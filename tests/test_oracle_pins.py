@@ -952,3 +952,142 @@ def test_fill_sample_routing():
     dom = (3 * np.arange(B)[:, None] + np.arange(S)[None, :]) % V
     assert (t0 == dom).all()          # F_t = 0: no down-weighting, the dominant token
     assert (t1 != dom).all()          # F_t = 1, C = 1e-4: the dominant token is avoided
+
+
+# ---------------------------------------------------------------------------
+# token-tree verification (several candidates per node)
+# ---------------------------------------------------------------------------
+def _tree_rows(prob_rows):
+    z = np.log(np.asarray(prob_rows, np.float64)).astype(np.float32)
+    return z[None]
+
+
+def _pin_tree_worked_example():
+    """Root: p = (1/2, 1/4, 1/4), q = (1/4, 1/2, 1/4); children 0 (token 1) and
+    1.  Token 1 is tested against r = p: u q = 3/4 * 1/2 > 1/4, rejected, with
+    margin |3/4 - 1/2| = 1/4; the residual is max(0, p - q) = (1/4, 0, 0), W =
+    1/4, r = (1, 0, 0).  (a) child 1 = token 0: u q = 1/8 < 1, accepted
+    (margin |1/2 - 4| = 7/2); node 1 is a leaf, so the bonus comes from its own
+    p = (1/5, 1/5, 3/5): u = 1/2 lands in [2/5, 1) at 1/10 from the lower edge.
+    (b) child 1 = token 2: r(2) = 0, rejected (margin 1/2); W = 3/4, r = (1, 0,
+    0): the bonus is token 0 whatever u (margin 1/2 for u = 1/2)."""
+    rows_t = [(.5, .25, .25), (.2, .2, .6), (.2, .2, .6)]
+    rows_d = [(.25, .5, .25), (1 / 3, 1 / 3, 1 / 3), (1 / 3, 1 / 3, 1 / 3)]
+    zt, zd = _tree_rows(rows_t), _tree_rows(rows_d)
+    par = np.array([[-1, -1]], np.int32)
+    ua = np.array([[0.75, 0.5]], np.float32)
+    ub = np.array([0.5], np.float32)
+    a = oracle.tree_verify(zt, zd, 3, 1.0, par, np.array([[1, 0]], np.int32), ua, ub)
+    assert a["accept_len"][0] == 1 and a["path"][0].tolist() == [1, -1] and a["bonus"][0] == 2
+    assert abs(a["acc_margin"][0, 0] - 0.25) < 1e-6 and abs(a["acc_margin"][0, 1] - 3.5) < 1e-5
+    assert abs(a["bonus_margin"][0] - 0.1) < 1e-6 and a["resid_mass"][0] == 1.0
+    b = oracle.tree_verify(zt, zd, 3, 1.0, par, np.array([[1, 2]], np.int32), ua, ub)
+    assert b["accept_len"][0] == 0 and b["bonus"][0] == 0
+    assert abs(b["acc_margin"][0, 1] - 0.5) < 1e-6
+    assert abs(b["resid_mass"][0] - 0.75) < 1e-6 and abs(b["bonus_margin"][0] - 0.5) < 1e-6
+
+
+def test_tree_verify_worked_example():
+    _pin_tree_worked_example()
+
+
+@pytest.mark.parametrize("T", [0.6, 1.0])
+def test_tree_verify_chain_reduces_to_verify(T):
+    """A chain tree is single-draft verification: the same accept counts and,
+    away from rounding ties, the same bonus as the pinned chain verifier (C = 1)."""
+    rng = np.random.default_rng(21)
+    B, K, V = 300, 4, 50
+    zt = (rng.standard_normal((B, K + 1, V)) * 1.5).astype(np.float32)
+    zd = (zt + rng.standard_normal((B, K + 1, V)) * 0.7).astype(np.float32)
+    ud, ua, ub = w.round_uniforms(5, 1, B, K)
+    F = (1,) * (K + 1)
+    d, _, _ = oracle.saguaro_sample(zd, V, F, 1.0, T, ud)
+    v = oracle.verify(zt, zd, V, F, 1.0, T, d, ua, ub)
+    par = np.broadcast_to(np.arange(-1, K - 1, dtype=np.int32), (B, K)).copy()
+    t = oracle.tree_verify(zt, zd, V, T, par, d, ua, ub)
+    np.testing.assert_array_equal(t["accept_len"], v["accept_len"])
+    ok = t["bonus_margin"] > 1e-9
+    assert ok.mean() > 0.95
+    np.testing.assert_array_equal(t["bonus"][ok], v["bonus"][ok])
+    for b in range(B):
+        a = t["accept_len"][b]
+        assert t["path"][b, :a].tolist() == list(range(a))
+
+
+def test_tree_verify_greedy_walk():
+    """T = 0: the walk takes the first child whose token is the target's argmax
+    at the node and ends with the argmax as the bonus (brute force)."""
+    rng = np.random.default_rng(8)
+    B, V = 100, 6
+    par1 = np.array([-1, -1, -1, 0, 0, 1, 3, 3, 6], np.int32)
+    N = len(par1)
+    zt = rng.integers(-3, 4, size=(B, N + 1, V)).astype(np.float32)
+    zd = rng.integers(-3, 4, size=(B, N + 1, V)).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    am = zt.argmax(axis=2)  # numpy: lowest index on ties
+    for b in range(B):      # make the argmax child likely
+        for m in range(N):
+            if rng.random() < 0.5:
+                tok[b, m] = am[b, par1[m] + 1]
+    par = np.broadcast_to(par1, (B, N)).copy()
+    u = rng.random((B, N)).astype(np.float32)
+    t = oracle.tree_verify(zt, zd, V, 0.0, par, tok, u, rng.random(B).astype(np.float32))
+    for b in range(B):
+        node, walk = -1, []
+        while True:
+            nxt = [c for c in range(N) if par1[c] == node and tok[b, c] == am[b, node + 1]]
+            if not nxt:
+                break
+            node = nxt[0]
+            walk.append(node)
+        assert t["path"][b, :len(walk)].tolist() == walk and t["accept_len"][b] == len(walk)
+        assert t["bonus"][b] == am[b, node + 1]
+
+
+_TREE_PAR = np.array([-1, -1, -1, 0, 0, 1, 1, 2, 2], np.int32)  # 3 children, 2 each
+
+
+def _tree_chi2_counts(T, n=200_000, seed=31):
+    """First emitted token over n independent walks of one tree whose children
+    are drawn i.i.d. from the draft at their parent."""
+    rng = np.random.default_rng(seed)
+    V, N = 6, len(_TREE_PAR)
+    zt = (rng.standard_normal((N + 1, V)) * 1.2).astype(np.float32)
+    zd = (zt + rng.standard_normal((N + 1, V)) * 1.0).astype(np.float32)
+    q = [oracle.softmax(zd[r].astype(np.float64), T) for r in range(N + 1)]
+    tok = np.zeros((n, N), np.int32)
+    for m in range(N):
+        cdf = np.cumsum(q[_TREE_PAR[m] + 1])
+        tok[:, m] = np.minimum(np.searchsorted(cdf, rng.random(n) * cdf[-1], side="right"), V - 1)
+    par = np.broadcast_to(_TREE_PAR, (n, N))
+    t = oracle.tree_verify(np.broadcast_to(zt, (n, N + 1, V)), np.broadcast_to(zd, (n, N + 1, V)),
+                           V, T, par, tok, rng.random((n, N)).astype(np.float32),
+                           rng.random(n).astype(np.float32))
+    first = np.where(t["accept_len"] > 0, tok[np.arange(n), np.maximum(t["path"][:, 0], 0)],
+                     t["bonus"])
+    return np.bincount(first, minlength=V), oracle.softmax(zt[0].astype(np.float64), T)
+
+
+@pytest.mark.parametrize("T", [0.6, 1.0])
+def test_tree_verify_chi2_lossless(T):
+    counts, p = _tree_chi2_counts(T)
+    assert _chi2_pvalue(counts, p) > P_THRESHOLD
+
+
+def test_tree_verify_chi2_detects_stale_residual():
+    """Testing every sibling against p (no residual update) over-emits the
+    draft's favourites: the chi-squared test has power."""
+    with _mutant_oracle("for (int i = 0; i < V; i++) r[i] = (r[i] > q[i]) ? (r[i] - q[i]) / W : 0.0;",
+                        "(void)W;"):
+        counts, p = _tree_chi2_counts(1.0)
+    assert _chi2_pvalue(counts, p) < 1e-12
+
+
+def test_tree_verify_flags():
+    zt = np.zeros((1, 4, 5), np.float32)
+    par = np.array([[-1, 5, 0]], np.int32)        # node 1's parent is past it
+    tok = np.array([[9, 1, 2]], np.int32)         # node 0's token is outside [0, 5)
+    t = oracle.tree_verify(zt, zt, 5, 1.0, par, tok, np.zeros((1, 3), np.float32),
+                           np.zeros(1, np.float32))
+    assert t["flags"][0] == 16 | 1
+    assert t["accept_len"][0] == 0
