@@ -336,6 +336,8 @@ def bench_ours(args):
         result["tiny_round"] = bench_tiny_round(ssd, w, device)
         result["round_analytics"] = bench_analytics(ssd, w, device, hbm_peak)
         result["miss_fallback"] = bench_fallback(ssd, w, device, hbm_peak)
+        result["cache_fill"] = bench_cache_fill(ssd, w, device, hbm_peak)
+        result["tree_verify"] = bench_tree(ssd, w, device, hbm_peak)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(spec, inp, args.cpu_seconds)
     if rank == 0:
@@ -539,6 +541,133 @@ def bench_analytics(ssd, w, device, hbm_peak):
            "mean_hit_rate": round(float(hr.mean().item()), 4),
            "mean_exp_tokens": round(float(et.mean().item()), 4), "status_flags": int(st.item())}
     del graphs, sets, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_cache_fill(ssd, w, device, hbm_peak):
+    """The speculation-cache fill by branch decode on the Llama-3 vocabulary and
+    the draft-attention tree: K decode steps, each a K/V append of the fed
+    nodes, tree attention over the 2 Ki-token prefix and the tree, and the
+    Saguaro draw of every branch's next token into the payload.  One CUDA graph
+    per fill; the draws alone are timed for their HBM roofline."""
+    import torch
+    spec = w.llama3_fill()
+    B, K, S, V, Hq, Hkv, d, L = spec.B, spec.K, spec.S, spec.V, spec.Hq, spec.Hkv, spec.d, spec.L
+    stream = torch.cuda.current_stream(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(23)
+    logits = []
+    for t in range(K):
+        rank = torch.argsort(torch.rand(B, S, V, generator=g, device=device), dim=-1).float() + 1
+        z = -1.1 * torch.log(rank) + torch.randn(B, S, V, generator=g, device=device)
+        logits.append(z.to(torch.bfloat16))
+        del rank, z
+    u = torch.rand(K, B, S, generator=g, device=device)
+    bf = dict(dtype=torch.bfloat16, device=device)
+    kn = [torch.randn(B, S, Hkv, d, generator=g, device=device).to(torch.bfloat16) for _ in range(K)]
+    vn = [torch.randn(B, S, Hkv, d, generator=g, device=device).to(torch.bfloat16) for _ in range(K)]
+    q = [torch.randn(B, S, Hq, d, generator=g, device=device).to(torch.bfloat16) for _ in range(K)]
+    N = K + K * S
+    maxb = (L + N + 15) // 16
+    nb = B * maxb
+    table = torch.randperm(nb, generator=g, device=device).to(torch.int32).view(B, maxb)
+    kc = torch.randn(nb, Hkv, 16, d, generator=g, device=device).to(torch.bfloat16)
+    vc = torch.randn(nb, Hkv, 16, d, generator=g, device=device).to(torch.bfloat16)
+    prefix = torch.full((B,), L, dtype=torch.int32, device=device)
+    parents = [torch.from_numpy(np.broadcast_to(w.fill_tree(K, spec.F, t + 1),
+                                                (B, K + (t + 1) * S)).copy()).to(device)
+               for t in range(K)]
+    out = torch.empty(B, S, Hq, d, **bf)
+    wsn = ssd.ssd_attention_workspace_size(B, S, Hq, Hkv, d, L)
+    wsa = torch.empty(max(wsn, 256), dtype=torch.uint8, device=device)
+    wss = [ssd.fill_workspace(B, S, V, spec.dtype, spec.F[t], device) for t in range(K)]
+    payload = torch.empty(B, S, K, dtype=torch.int32, device=device)
+    tok = torch.empty(B, S, dtype=torch.int32, device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def draw(t):
+        ssd.ssd_fill_sample(logits[t], V, spec.F[t], spec.C, spec.T, u[t], tok, t=t, payload=payload,
+                            status=st, ws=wss[t])
+
+    def fill():
+        for t in range(K):
+            ssd.ssd_kv_append(kn[t], vn[t], kc, vc, table, prefix, K + t * S, status=st)
+            ssd.ssd_branch_attention(q[t], kc, vc, table, prefix, parents[t], out, status=st, ws=wsa)
+            draw(t)
+
+    fill()
+    gf = capture_graphs([fill], device)[0]
+    gd = capture_graphs([lambda: [draw(t) for t in range(K)]], device)[0]
+    for _ in range(3):
+        gf.replay()
+        gd.replay()
+    ms = _time_calls(lambda i: gf.replay(), 20, stream)
+    ms_draw = _time_calls(lambda i: gd.replay(), 20, stream)
+    draw_bytes = K * B * S * V * 2
+    res = {"workload": spec.name, "ms_per_fill": round(ms, 4),
+           "branch_tokens_per_s": round(B * S * K / (ms * 1e-3), 1),
+           "ms_draws": round(ms_draw, 4), "draw_bytes": draw_bytes,
+           "draw_GB/s": round(draw_bytes / (ms_draw * 1e-3) / 1e9, 1),
+           "draw_frac_of_hbm_peak": round(draw_bytes / (ms_draw * 1e-3) / 1e9 / hbm_peak, 4),
+           "launches_per_fill": f"{K} x (1 append + 1-2 attention + 2 draw)", "status_flags": int(st.item()),
+           "steps": f"{K} x (ssd_kv_append, ssd_branch_attention, ssd_fill_sample); "
+                    f"{draw_bytes / 1e6:.0f} MB of draft logits per fill (> L2)"}
+    del gf, gd, logits, kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_tree(ssd, w, device, hbm_peak):
+    """Token-tree verification of the 28-node tree over the Llama-3 vocabulary:
+    children drawn from the draft at their parent (torch.multinomial, setup
+    only); four input copies rotate so the visited rows come from HBM."""
+    import torch
+    spec = w.llama3_tree()
+    B, V, N = spec.B, spec.V, spec.N
+    stream = torch.cuda.current_stream(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(29)
+    shape = (B, N + 1, V)
+    rank = torch.argsort(torch.rand(shape, generator=g, device=device), dim=-1).float() + 1
+    zt = -1.1 * torch.log(rank) + 0.3 * torch.randn(shape, generator=g, device=device)
+    del rank
+    zd = zt + spec.draft_noise * torch.randn(shape, generator=g, device=device)
+    parent1 = w.tree_shape(spec.branching)
+    rows = torch.from_numpy(parent1.astype(np.int64) + 1).to(device)
+    probs = torch.softmax(zd[:, rows, :] / spec.T, dim=-1)  # [B, N, V]: q at each node's parent
+    tok = torch.multinomial(probs.view(B * N, V), 1, generator=g).view(B, N).to(torch.int32)
+    del probs
+    par = torch.from_numpy(np.broadcast_to(parent1, (B, N)).copy()).to(device)
+    ua = torch.rand(B, N, generator=g, device=device)
+    ub = torch.rand(B, generator=g, device=device)
+    nsets = 4
+    sets = [(zt.to(torch.bfloat16), zd.to(torch.bfloat16)) for _ in range(nsets)]
+    del zt, zd
+    i32 = dict(dtype=torch.int32, device=device)
+    acc, path, bon = torch.empty(B, **i32), torch.empty(B, N, **i32), torch.empty(B, **i32)
+    st = torch.zeros(1, **i32)
+
+    def call(i):
+        t, d = sets[i % nsets]
+        ssd.ssd_tree_verify(t, d, V, spec.T, par, tok, ua, ub, acc, path, bon, status=st)
+
+    for i in range(nsets):
+        call(i)
+    gr = capture_graphs([lambda: [call(i) for i in range(nsets)]], device)[0]
+    gr.replay()
+    reps = 25
+    ms = _time_calls(lambda i: gr.replay(), reps, stream) / nsets
+    visited = int(acc.sum().item()) + B  # the rows of every visited node: accepted ones and the root
+    alg = visited * 2 * V * 2
+    res = {"workload": spec.name, "ms": round(ms, 4), "trees_per_s": round(B / (ms * 1e-3), 1),
+           "mean_accept_len": round(visited / B - 1, 3), "algorithmic_bytes": alg,
+           "GB/s": round(alg / (ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm_peak": round(alg / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+           "status_flags": int(st.item()),
+           "kernel": "k_tree_walk (one 4-CTA cluster per sequence)",
+           "timing": f"CUDA graph of {nsets} calls over input copies, replayed {reps} times"}
+    del gr, sets
     torch.cuda.empty_cache()
     return res
 
@@ -789,6 +918,25 @@ def probe(which):
         torch.cuda.synchronize()
         print(json.dumps({"probe": which, "workload": spec.name, "status": int(out["status"].item())}))
         return
+    if which == "tree":
+        spec = w.llama3_tree()
+        tgt, dft = w.tree_logits(spec, 5)
+        parent1 = w.tree_shape(spec.branching)
+        B, N = spec.B, spec.N
+        rng = np.random.default_rng(6)
+        tok = torch.from_numpy(rng.integers(0, 64, size=(B, N)).astype(np.int32)).to(device)
+        par = torch.from_numpy(np.broadcast_to(parent1, (B, N)).copy()).to(device)
+        ua, ub = w.tree_uniforms(5, 0, B, N)
+        i32 = dict(dtype=torch.int32, device=device)
+        acc, path, bon = torch.empty(B, **i32), torch.empty(B, N, **i32), torch.empty(B, **i32)
+        st = torch.zeros(1, **i32)
+        t, d = ssd.tensor(tgt), ssd.tensor(dft)
+        for _ in range(3):
+            ssd.ssd_tree_verify(t, d, spec.V, spec.T, par, tok, ssd.tensor(ua), ssd.tensor(ub), acc,
+                                path, bon, status=st)
+        torch.cuda.synchronize()
+        print(json.dumps({"probe": which, "workload": spec.name, "status": int(st.item())}))
+        return
     if which == "fallback":
         spec = w.qwen3_histories()
         h = w.make_histories(spec, seed=21)
@@ -824,7 +972,7 @@ def main(argv=None):
                     help="reference arm: sequences per host core per step (capped at one batch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e / attention / other rounds")
-    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify", "fallback"),
+    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify", "fallback", "tree"),
                     help="only run a few calls of one workload (for profilers) and exit")
     args = ap.parse_args(argv)
     if args.probe:

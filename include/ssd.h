@@ -279,7 +279,8 @@ ssd_status_t ssd_set_timing_events(void *before, void *after);
  * not reached): start, after the wait for the previous kernel, then per
  * kind -- pair: records staged, rows merged, draw of d done, top-F done,
  * end; residual: records read, unit pass done, ticket taken, bonus drawn,
- * end (statistics CTAs mark only start and end).  Calls whose CTAs do not
+ * end (statistics CTAs mark only their start; the pair kernel's wait mark
+ * shows when the statistics grid has completed).  Calls whose CTAs do not
  * fit in `bytes`, or with more than 65535 sequences, write nothing.
  * Process-wide, not thread-safe; NULL clears.  Diagnostics only.
  */
@@ -315,6 +316,86 @@ ssd_status_t ssd_branch_attention(const void *q, const void *k_cache, const void
                                   int Nq, int Hq, int Hkv, int d, float scale, void *out,
                                   float *lse, uint32_t *status, void *ws, size_t ws_bytes,
                                   ssd_stream_t s);
+
+/*
+ * Speculation-cache fill by branch decode [B, "投机解码的瓶颈与 SSD 的核心机制": while
+ * the target verifies, the draft pre-speculates a continuation for every
+ * predicted outcome (k, guess); "工程优化与系统表现": all F_k branches are
+ * decoded in one forward pass with a custom sparse attention mask].
+ * Reading (the pages give no step loop): a branch is one cache slot s
+ * (0 <= s < S = sum_k F_k, slot-ordered as in ssd_cache_lookup); its chain
+ * starts at the guessed bonus token and grows by one token per decode step
+ * t = 0..Kp-1.  The Kp drawn tokens are the slot's payload: the next round's
+ * draft tokens d_1..d_Kp, so step t draws with sigma_{F_t, C} (draft position
+ * j uses F_{j-1}, as in ssd_saguaro_sample).  One step is
+ *   ssd_kv_append     (the fed tokens' key/value rows into the paged cache),
+ *   ssd_branch_attention (queries: the fed nodes; parent: the branch tree),
+ *   the draft's other layers (not part of this library), then
+ *   ssd_fill_sample   (the next token of every branch, into payload[:, :, t]).
+ *
+ * ssd_fill_sample: logits [B, S, V] (row (b, s) at logits + (b*S + s) *
+ * branch_stride elements; fp32 or bf16; 16-byte aligned base and stride);
+ * every row is drawn as ssd_saguaro_sample draws one draft position, with
+ * F = F_t and the uniform u[b, s]: tokens [B, S] (required), q_out [B, S] =
+ * q'(token) (or NULL), and payload [B, S, Kp] column t (or NULL).  Workspace:
+ * ssd_workspace_size(B*S, 1, V, dt, {F_t, 0}) bytes.  Limits as in
+ * ssd_saguaro_sample; B*S < 2^31.
+ */
+ssd_status_t ssd_fill_sample(const void *logits, ssd_dtype_t dt, int64_t branch_stride, int B, int S,
+                             int V, int F_t, float C, float T, const float *u, int t, int Kp,
+                             int32_t *tokens, float *q_out, int32_t *payload, uint32_t *status,
+                             void *ws, size_t ws_bytes, ssd_stream_t s);
+
+/*
+ * ssd_kv_append: k_new, v_new [B, S, Hkv, d] bf16 (the rows of the S tokens
+ * fed this step) go to the paged caches [num_blocks, Hkv, 16, d] (the layout
+ * of ssd_branch_attention) at logical position pos = prefix_len[b] + node0 + i
+ * of sequence b: page block_table[b, pos / 16], slot pos % 16.  node0 is the
+ * tree index of the step's first node (node m sits at prefix_len + m, as in
+ * ssd_branch_attention).  A negative prefix or a position past the table sets
+ * BAD_PREFIX, a page id outside [0, num_blocks) sets BAD_BLOCK; that row is
+ * not written.  d a multiple of 8, at most 256; 16-byte aligned pointers.
+ * One thread per 16-byte piece.
+ */
+ssd_status_t ssd_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           const int32_t *block_table, int maxb, int64_t num_blocks,
+                           const int32_t *prefix_len, int node0, int B, int S, int Hkv, int d,
+                           uint32_t *status, ssd_stream_t s);
+
+/*
+ * Token-tree verification with several candidates per node [A, closing
+ * paragraph: combining SSD with token-tree speculation is named as future
+ * work; B, "投机解码的瓶颈与 SSD 的核心机制" and "Saguaro 算法" part 2: the
+ * single-chain acceptance rule and the residual p_target - p_draft].
+ * Reading (the pages give no tree rule): the children of a node were drawn
+ * independently from the draft's q at that node; they are tested in index
+ * order against r, which starts as p and becomes the normalised residual
+ * max(0, r - q) / sum max(0, r - q) after each rejection; an accepted child
+ * continues the walk from it; when no child is accepted the bonus is drawn
+ * from r (inverse CDF, u_bonus).  The emitted tokens then follow the target
+ * exactly, as in single-chain verification.
+ *   logits  [B, N+1, V] per tensor (layout and alignment as for ssd_verify):
+ *           row 0 the distributions after the prefix (the root), row m+1 those
+ *           after tree node m;  p = softmax(target / T), q = softmax(draft / T)
+ *           (T = 0: one-hot at the argmax, lowest index on ties).
+ *   parent  [B, N] int32 in [-1, m-1] (-1: the root); tokens [B, N];
+ *   u_acc   [B, N]: the uniform of node m's test (u * q(x) < r(x) accepts);
+ *   u_bonus [B].
+ * Outputs: accept_len [B] (accepted nodes), path [B, N] (their indices in
+ * order, then -1), bonus [B], out_tokens [B, N+1] (the accepted tokens, the
+ * bonus, then -1; or NULL), resid_mass [B] (the W of the last residual taken
+ * at the final node, 1 when its r is p; or NULL).  A parent outside [-1, m-1]
+ * sets BAD_TREE (that node is nobody's child); a token outside [0, V) sets
+ * BAD_TOKEN (that child is skipped); a residual without mass sets
+ * ZERO_RESIDUAL (r stays).  Supported: N <= 256, V * elem <= 512 KiB.
+ * One thread-block cluster of ceil(V*elem / 64 KiB) CTAs per sequence; each
+ * visited node's two rows are read from HBM once.
+ */
+ssd_status_t ssd_tree_verify(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                             int64_t row_stride, int B, int N, int V, float T, const int32_t *parent,
+                             const int32_t *tokens, const float *u_acc, const float *u_bonus,
+                             int32_t *accept_len, int32_t *path, int32_t *bonus, int32_t *out_tokens,
+                             float *resid_mass, uint32_t *status, ssd_stream_t s);
 
 /*
  * Miss fallback [B, "Saguaro 算法" part 3 "大 Batch 下的退避策略": a sequence

@@ -32,7 +32,7 @@ EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_s
            "ssd_verify", "ssd_verify_noalloc", "ssd_verify_noalloc_max_bytes",
            "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round", "ssd_round_analytics",
            "ssd_attention_workspace_size", "ssd_branch_attention", "ssd_ngram_backup",
-           "ssd_fallback_plan")
+           "ssd_fallback_plan", "ssd_fill_sample", "ssd_kv_append", "ssd_tree_verify")
 
 _lib = None
 
@@ -109,6 +109,14 @@ def _declare(lib):
     lib.ssd_branch_attention.argtypes = [_vp, _vp, _vp, _vp, _i, _i64, _vp, _vp, _i, _i, _i, _i, _i,
                                          _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.ssd_branch_attention.restype = _i
+    lib.ssd_fill_sample.argtypes = [_vp, _i, _i64, _i, _i, _i, _i, _f, _f, _vp, _i, _i, _vp, _vp, _vp,
+                                    _vp, _vp, _sz, _vp]
+    lib.ssd_fill_sample.restype = _i
+    lib.ssd_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i64, _vp, _i, _i, _i, _i, _i, _vp, _vp]
+    lib.ssd_kv_append.restype = _i
+    lib.ssd_tree_verify.argtypes = [_vp, _vp, _i, _i64, _i64, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.ssd_tree_verify.restype = _i
     lib.ssd_ngram_backup.argtypes = [_vp, _i64, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp,
                                      _vp, _vp]
     lib.ssd_ngram_backup.restype = _i
@@ -364,3 +372,58 @@ def ssd_fallback_plan(p_hit, e_hit, T_v, T_p, T_b, e_miss, time=None, tokens=Non
     _check("ssd_fallback_plan", load().ssd_fallback_plan(
         _ptr(p_hit), _ptr(e_hit), p_hit.shape[0], float(T_v), float(T_p), nopt, tb, em, _ptr(time),
         _ptr(tokens), _ptr(throughput), _ptr(speedup), _ptr(best), _ptr(status), _stream(stream)))
+
+
+def fill_workspace(B, S, V, dtype, F_t, device="cuda") -> torch.Tensor:
+    """Workspace of one ssd_fill_sample call (B*S one-draw rows at F = F_t)."""
+    return workspace(B * S, 1, V, dtype, (int(F_t), 0), device)
+
+
+def ssd_fill_sample(logits, V, F_t, C, T, u, tokens, t=0, payload=None, q_out=None, status=None,
+                    ws=None, stream=None):
+    """Draw the next token of every branch row of ``logits`` [B, S, V'] with
+    sigma_{F_t, C}; optionally write it into column ``t`` of ``payload`` [B, S, Kp]."""
+    if logits.dim() != 3 or (logits.numel() and logits.stride(2) != 1):
+        raise ValueError("logits must be [B, S, V'] with unit stride on the last dim")
+    B, S = logits.shape[0], logits.shape[1]
+    if logits.numel() and logits.stride(0) != S * logits.stride(1):
+        raise ValueError("branch rows must be evenly spaced (stride(0) == S * stride(1))")
+    dt = _dtype_code(logits.dtype)
+    Kp = 0
+    if payload is not None:
+        if payload.dtype != torch.int32 or not payload.is_contiguous() or tuple(payload.shape[:2]) != (B, S):
+            raise ValueError("payload must be a contiguous int32 [B, S, Kp] tensor")
+        Kp = payload.shape[2]
+    stride = logits.stride(1) if logits.numel() else logits.shape[2]
+    _check("ssd_fill_sample", load().ssd_fill_sample(
+        _ptr(logits), dt, stride, B, S, int(V), int(F_t), float(C), float(T), _ptr(u), int(t), Kp,
+        _ptr(tokens), _ptr(q_out), _ptr(payload), _ptr(status), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def ssd_kv_append(k_new, v_new, k_cache, v_cache, block_table, prefix_len, node0, status=None,
+                  stream=None):
+    """Append the rows ``k_new``/``v_new`` [B, S, Hkv, d] (bf16) at tree nodes
+    node0..node0+S-1 of every sequence's paged cache."""
+    for x in (k_new, v_new, k_cache, v_cache):
+        if x.dtype != torch.bfloat16 or not x.is_contiguous():
+            raise ValueError("k_new, v_new and the caches must be contiguous bfloat16")
+    B, S, Hkv, d = k_new.shape
+    _check("ssd_kv_append", load().ssd_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], k_cache.shape[0], _ptr(prefix_len), int(node0), B, S, Hkv, d,
+        _ptr(status), _stream(stream)))
+
+
+def ssd_tree_verify(target, draft, V, T, parent, tokens, u_acc, u_bonus, accept_len, path, bonus,
+                    out_tokens=None, resid_mass=None, status=None, stream=None):
+    """Verify a token tree per sequence: logits [B, N+1, V'] (row 0 the root,
+    row m+1 after node m), parent/tokens/u_acc [B, N], u_bonus [B]."""
+    dt, ss, rs = _logit_meta(target)
+    if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
+        raise ValueError("target and draft logits must share dtype, shape and strides")
+    B, N1 = target.shape[0], target.shape[1]
+    _check("ssd_tree_verify", load().ssd_tree_verify(
+        _ptr(target), _ptr(draft), dt, ss, rs, B, N1 - 1, int(V), float(T), _ptr(parent),
+        _ptr(tokens), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(path), _ptr(bonus),
+        _ptr(out_tokens), _ptr(resid_mass), _ptr(status), _stream(stream)))

@@ -16,7 +16,7 @@
 //                    in flight per thread), stops at the first chunk with a
 //                    match, and checks the other n - 1 tokens only where the
 //                    first one matches.
-//   k_fallback_plan  one CTA; fp64 reduction over the batch of the hit
+//   k_fallback_plan  one CTA of 128 threads; fp64 reduction over the batch of the hit
 //                    probabilities and expected tokens into the expected round
 //                    time, tokens, throughput and speedup of each backup, and
 //                    the best backup -- on the device, so a chained backup
@@ -38,7 +38,8 @@ constexpr int kNgChunk = kNgThreads * kNgUnroll;     // candidate positions per 
 constexpr int kMaxN = 32;                            // longest n-gram
 constexpr int kMaxBackupK = 1024;                    // longest proposal
 constexpr int64_t kMaxHistory = int64_t(1) << 30;    // longest history row
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 128;  // fp64 is a slow pipe on this part: few threads, little reduction
+constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kMaxOptions = 8;
 
 struct NgramArgs {
@@ -156,7 +157,7 @@ __device__ __forceinline__ double warp_prod_d(double v) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) k_fallback_plan(PlanArgs a) {
-  __shared__ double red[4][kPlanThreads / 32];
+  __shared__ double red[4][kPlanWarps];
   const int tid = threadIdx.x;
   double pall = 1.0, phe = 0.0, pmiss = 0.0, ehit = 0.0;
   uint32_t fl = 0;
@@ -188,10 +189,13 @@ __global__ void __launch_bounds__(kPlanThreads) k_fallback_plan(PlanArgs a) {
   if (fl) atomicOr(a.status, fl);
   __syncthreads();
   if (tid < 32) {
-    pall = warp_prod_d(red[0][tid]);
-    phe = warp_sum_d(red[1][tid]);
-    pmiss = warp_sum_d(red[2][tid]);
-    ehit = warp_sum_d(red[3][tid]);
+    // one warp part per lane; the lanes past the warp count add the identities
+    const bool has = tid < kPlanWarps;
+    const int w = has ? tid : 0;  // every load in bounds
+    pall = warp_prod_d(has ? red[0][w] : 1.0);
+    phe = warp_sum_d(has ? red[1][w] : 0.0);
+    pmiss = warp_sum_d(has ? red[2][w] : 0.0);
+    ehit = warp_sum_d(has ? red[3][w] : 0.0);
     // one option per lane; the best is the largest throughput, lowest index on ties
     const double tmax = a.T_v > a.T_p ? a.T_v : a.T_p;
     const double base = ehit / (a.T_p + a.T_v);

@@ -26,7 +26,7 @@
 //            from L2), draws d_{j+1} from the Saguaro weights (segment, block,
 //            then one block read again), takes p(d), q'(d) and the position's
 //            verdict; at position K+1 it draws the bonus for full acceptance.
-//   k_resid  (verification at T > 0) units of 32 KiB per row: the sequence's
+//   k_resid  (verification at T > 0) units of 16 KiB of each row: the sequence's
 //            first rejected pair read again (from L2) for the block sums of
 //            max(0, p - q'); the unit with the sequence's last ticket draws the
 //            bonus from them and writes the outputs and the cache lookup.  A
@@ -136,6 +136,8 @@ struct VocabArgs {
   const int32_t *payload;
   int32_t *d_out;
   float *qd_out;
+  int32_t *fill_payload;  // cache fill: the draw of sequence b also goes to fill_payload[b * fill_stride + fill_col]
+  int fill_stride, fill_col;
   int32_t *accept_len, *out_tokens, *bonus;
   float *accept_prob, *resid_mass;
   int32_t *guess;
@@ -160,6 +162,17 @@ SSD_DEV unsigned long long now_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
+}
+// A statistics CTA's entry: identity and start mark (the other words stay 0).
+SSD_DEV void trace_start(const VocabArgs &a, long idx, int b, int j) {
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  unsigned long long *tr = a.trace + 8 * idx;
+  tr[0] = (static_cast<unsigned long long>(smid) << 48) | (static_cast<unsigned long long>(b & 0xFFFFF) << 20) |
+          static_cast<unsigned long long>(j & 0xFFFFF);
+  tr[1] = now_ns();
+#pragma unroll
+  for (int k = 2; k < 8; ++k) tr[k] = 0ull;
 }
 SSD_DEV void trace_entry(const VocabArgs &a, long idx, int kind, int b, int j, const unsigned long long *mk) {
   if (!a.trace || threadIdx.x != 0) return;
@@ -461,7 +474,10 @@ template <class E>
 __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ VocabArgs a) {
   // k_pair may start launching once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const unsigned long long t0 = (a.trace && threadIdx.x == 0) ? now_ns() : 0ull;
+  // the start mark only: at 64 registers an end mark makes the statistics pass spill
+  if (a.trace && threadIdx.x == 0)
+    trace_start(a, (static_cast<long>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
+                a.b0 + static_cast<int>(blockIdx.z), static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x));
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sg = static_cast<int>(blockIdx.x) * kWarps + warp;
   const int slot = static_cast<int>(blockIdx.y);
@@ -590,11 +606,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ V
           make_int4(__float_as_int(wm), __float_as_int(ws), wa, __float_as_int(wt));
     if (rs.keys && lane < kSegBlocks) a.bkey[si * a.nblk + sg * kSegBlocks + lane] = bk;
     if (rs.blocks && (lane & 3) == 0) a.bsum[si * a.nblk + sg * kSegBlocks + (lane >> 2)] = bsv;
-  }
-  if (a.trace && threadIdx.x == 0) {
-    const unsigned long long mk[8] = {0ull, t0, 0ull, 0ull, 0ull, 0ull, 0ull, now_ns()};
-    trace_entry(a, (static_cast<long>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x, 0, b,
-                static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), mk);
   }
 }
 
@@ -1131,6 +1142,7 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
       if (sampled) {
         a.d_out[static_cast<size_t>(b) * K + j] = r.d;
         if (a.qd_out) a.qd_out[static_cast<size_t>(b) * K + j] = r.q;
+        if (a.fill_payload) a.fill_payload[static_cast<size_t>(b) * a.fill_stride + a.fill_col] = r.d;
       }
       if (tested && a.accept_prob) {
         float ap;
@@ -2027,6 +2039,37 @@ ssd_status_t ssd_saguaro_sample(const void *draft, ssd_dtype_t dt, int64_t seq_s
   a.u_draft = u_draft;
   a.d_out = d_out;
   a.qd_out = qd_out;
+  return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
+}
+
+ssd_status_t ssd_fill_sample(const void *logits, ssd_dtype_t dt, int64_t branch_stride, int B, int S, int V,
+                             int F_t, float C, float T, const float *u, int t, int Kp, int32_t *tokens,
+                             float *q_out, int32_t *payload, uint32_t *status, void *ws, size_t ws_bytes,
+                             ssd_stream_t s) {
+  // every branch row is a one-draw "sequence": K = 1, F = (F_t, 0)
+  if (B < 0 || S < 0 || (payload && (Kp < 1 || t < 0 || t >= Kp))) return SSD_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * S;
+  if (rows > 0x7fffffffLL) return SSD_ERR_UNSUPPORTED;
+  const int32_t F[2] = {F_t, 0};
+  const int Bp = static_cast<int>(rows);
+  Layout L;
+  ssd_status_t st = layout_or_error(Bp, 1, V, dt, F, &L);
+  if (st != SSD_OK) return st;
+  st = check_logits(logits, dt, branch_stride, branch_stride, Bp, 1, V);
+  if (st != SSD_OK) return st;
+  st = check_common(Bp, C, T, L, ws, ws_bytes, true);
+  if (st != SSD_OK) return st;
+  if (Bp == 0) return SSD_OK;
+  if (!u || !tokens || !status) return SSD_ERR_INVALID_ARG;
+  VocabArgs a = base_args(logits, logits, branch_stride, branch_stride, Bp, 1, V, F, C, T, L, ws, status);
+  a.do_sample = 1;
+  set_rows(a, 0, 1, C < 1.f);
+  a.u_draft = u;
+  a.d_out = tokens;
+  a.qd_out = q_out;
+  a.fill_payload = payload;
+  a.fill_stride = Kp;
+  a.fill_col = t;
   return cuda_status(launch_any(dt, a, reinterpret_cast<cudaStream_t>(s)));
 }
 

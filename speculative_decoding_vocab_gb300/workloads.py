@@ -17,6 +17,11 @@ Contents
   Gaussian logits and Zipf-shaped logits over a seeded permutation, with the
   draft equal to the target plus Gaussian noise.
 * paged KV caches, block tables and branch trees for tree-masked attention.
+* branch-decode (cache fill) steps: per step the draft logits of every
+  branch, the key/value rows of the fed tokens and the step-major branch tree.
+* token trees for multi-candidate verification: a level-order tree of given
+  branching and per-node target / draft logit rows (the children's tokens
+  are drawn by the caller from the draft rows).
 * token histories for the miss fallback: Zipf-distributed tokens in which
   spans repeat earlier spans (the repetition an n-gram backup feeds on), with
   a seeded set of sequences that missed the speculation cache.
@@ -42,6 +47,9 @@ SLOT_DRAFT = 0   # u_draft[b, j]: the uniform the draft's inverse-CDF draw uses
 SLOT_ACCEPT = 1  # u_acc[b, j]: the uniform of the acceptance test at position j
 SLOT_BONUS = 2   # u_bonus[b]: the uniform of the residual / bonus draw
 SLOT_BACKUP = 3  # u_rand[b, t]: the uniform of the random-token backup at position t
+SLOT_FILL = 4    # u_fill[b, t*S + s]: the uniform of branch s's draw at decode step t
+SLOT_TREE = 5    # u_acc[b, m]: the uniform of tree node m's acceptance test
+SLOT_TREE_BONUS = 6  # u_bonus[b]: the uniform of the tree walk's bonus draw
 
 
 def philox4x32_10(counter: np.ndarray, key: tuple[int, int]) -> np.ndarray:
@@ -386,6 +394,173 @@ def round_bytes(spec: RoundSpec) -> int:
     logit read once."""
     elem = 4 if spec.dtype == "f32" else 2
     return 2 * spec.B * (spec.K + 1) * spec.V * elem
+
+
+# ---------------------------------------------------------------------------
+# Cache fill by branch decode
+# ---------------------------------------------------------------------------
+@dataclass
+class FillSpec:
+    """Shape and value recipe of a speculation-cache fill: K decode steps over
+    the S = sum(F) branches of B sequences, with tree attention of shape
+    (Hq, Hkv, d) over a prefix of L tokens."""
+    B: int
+    K: int
+    F: tuple
+    V: int
+    dtype: str
+    T: float
+    C: float
+    Hq: int
+    Hkv: int
+    d: int
+    L: int
+    recipe: str = "zipf"       # draft logits: "zipf" (slope 1.1 + N(0,1)) or "gauss" (N(0, 2^2))
+    name: str = ""
+
+    @property
+    def S(self) -> int:
+        return int(sum(self.F))
+
+
+def fill_tree(K: int, F, steps: int) -> np.ndarray:
+    """Parent indices after ``steps`` decode steps, numbered step-major: nodes
+    0..K-1 are the spine (the round's draft tokens); node K + t*S + s is the
+    token branch s fed at step t.  Step 0 feeds each branch's guessed bonus,
+    hung off spine node a-1 for a slot of depth a (the prefix end for a = 0);
+    step t > 0 feeds the token drawn at step t-1, hung off the branch's
+    previous node.  The nodes fed at a step are the last S nodes."""
+    S = int(sum(F))
+    depth = np.repeat(np.arange(K + 1), F)
+    parent = [-1 if m == 0 else m - 1 for m in range(K)]
+    for t in range(steps):
+        for s in range(S):
+            parent.append(int(depth[s]) - 1 if t == 0 else K + (t - 1) * S + s)
+    return np.asarray(parent, dtype=np.int32)
+
+
+def fill_uniforms(seed: int, rnd: int, t: int, B: int, S: int) -> np.ndarray:
+    """``u[B, S]`` of decode step ``t`` (Philox counter (round, sequence,
+    SLOT_FILL, t*S + s))."""
+    key = (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    b = np.arange(B, dtype=np.uint32)[:, None]
+    j = (t * S + np.arange(S, dtype=np.uint32))[None, :]
+    ctr = np.stack(np.broadcast_arrays(np.uint32(rnd & 0xFFFFFFFF), b, np.uint32(SLOT_FILL),
+                                       j.astype(np.uint32)), axis=-1)
+    return uniforms_from_bits(philox4x32_10(ctr, key)[..., 0])
+
+
+def fill_step_logits(spec: FillSpec, seed: int, t: int, seqs=None) -> np.ndarray:
+    """Draft logits [len(seqs), S, V] of step ``t`` (float32, or bf16 bits),
+    generated per (seed, step, sequence)."""
+    seqs = range(spec.B) if seqs is None else seqs
+    out = []
+    for b in seqs:
+        rng = np.random.default_rng(np.random.SeedSequence([seed, t, b, 0xF111]))
+        if spec.recipe == "zipf":
+            _, zd = _zipf_rows(rng, spec.S, spec.V, 1.1, 0.0, 1.0)
+        else:
+            zd = rng.standard_normal((spec.S, spec.V), dtype=np.float32) * np.float32(2.0)
+        out.append(zd if spec.dtype == "f32" else f32_to_bf16_bits(zd))
+    return np.stack(out)
+
+
+def fill_step_kv(spec: FillSpec, seed: int, t: int):
+    """bf16 bits of the key and value rows [B, S, Hkv, d] of the tokens fed at step ``t``."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, t, 0xF112]))
+    shape = (spec.B, spec.S, spec.Hkv, spec.d)
+    return _bf16_normals(rng, shape), _bf16_normals(rng, shape)
+
+
+def tiny_fill() -> FillSpec:
+    return FillSpec(B=2, K=4, F=(4, 2, 1, 1, 1), V=4096, dtype="f32", T=1.0, C=0.5, Hq=4, Hkv=2,
+                    d=64, L=37, recipe="gauss", name="tiny-cache-fill-B2-K4-S9-V4096-f32")
+
+
+def llama3_fill() -> FillSpec:
+    """The draft-attention tree (K = 4, F = (8,4,2,1,1), chains of 4 nodes) over
+    the Llama-3 vocabulary: 16 sequences, 16 branches each."""
+    return FillSpec(B=16, K=4, F=(8, 4, 2, 1, 1), V=128256, dtype="bf16", T=1.0, C=0.5, Hq=32,
+                    Hkv=8, d=64, L=2048, name="llama3-cache-fill-B16-K4-S16-V128256-bf16-C0.5")
+
+
+# ---------------------------------------------------------------------------
+# Token trees for multi-candidate verification
+# ---------------------------------------------------------------------------
+@dataclass
+class TreeSpec:
+    """A batch of token trees: level-order nodes where each node of depth d has
+    branching[d] children; per node a target and a draft logit row."""
+    B: int
+    V: int
+    dtype: str
+    T: float
+    branching: tuple
+    recipe: str = "zipf"       # "zipf" (-1.1 ln rank + N(0, .3^2)) or "gauss" (N(0, 2^2))
+    draft_noise: float = 1.0   # draft = target + N(0, draft_noise^2)
+    name: str = ""
+
+    @property
+    def N(self) -> int:
+        return len(tree_shape(self.branching))
+
+
+def tree_shape(branching) -> np.ndarray:
+    """Parent indices of a level-order tree: the root (-1) has branching[0]
+    children, each node of depth d has branching[d] children."""
+    parent, level = [], [-1]
+    for nb in branching:
+        nxt = []
+        for u in level:
+            for _ in range(nb):
+                parent.append(u)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.asarray(parent, dtype=np.int32)
+
+
+def tree_logits(spec: TreeSpec, seed: int, seqs=None):
+    """Target and draft logits [len(seqs), N+1, V] (float32, or bf16 bits):
+    row 0 at the root, row m+1 after node m; generated per (seed, sequence)."""
+    seqs = range(spec.B) if seqs is None else seqs
+    N1 = spec.N + 1
+    tgt, dft = [], []
+    for b in seqs:
+        rng = np.random.default_rng(np.random.SeedSequence([seed, b, 0x7733]))
+        if spec.recipe == "zipf":
+            zt, zd = _zipf_rows(rng, N1, spec.V, 1.1, 0.3, spec.draft_noise)
+        else:
+            zt, zd = _gauss_rows(rng, N1, spec.V, 2.0, spec.draft_noise)
+        if spec.dtype != "f32":
+            zt, zd = f32_to_bf16_bits(zt), f32_to_bf16_bits(zd)
+        tgt.append(zt)
+        dft.append(zd)
+    return np.stack(tgt), np.stack(dft)
+
+
+def tree_uniforms(seed: int, rnd: int, B: int, N: int):
+    """``u_acc[B, N]`` and ``u_bonus[B]`` of a tree walk (Philox counters
+    (round, sequence, SLOT_TREE, node) and (round, sequence, SLOT_TREE_BONUS, 0))."""
+    key = (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    b = np.arange(B, dtype=np.uint32)[:, None]
+
+    def draw(kind, n):
+        j = np.arange(n, dtype=np.uint32)[None, :]
+        ctr = np.stack(np.broadcast_arrays(np.uint32(rnd & 0xFFFFFFFF), b, np.uint32(kind), j), axis=-1)
+        return uniforms_from_bits(philox4x32_10(ctr, key)[..., 0])
+    return draw(SLOT_TREE, N), draw(SLOT_TREE_BONUS, 1)[:, 0].copy()
+
+
+def tiny_tree() -> TreeSpec:
+    return TreeSpec(B=3, V=4096, dtype="f32", T=1.0, branching=(3, 2, 1), recipe="gauss",
+                    draft_noise=0.8, name="tiny-tree-B3-N15-V4096-f32")
+
+
+def llama3_tree(B: int = 32) -> TreeSpec:
+    """A 28-node tree (4 candidates at the root, 2 below each, then chains)
+    over the Llama-3 vocabulary."""
+    return TreeSpec(B=B, V=128256, dtype="bf16", T=1.0, branching=(4, 2, 1, 1),
+                    name=f"llama3-tree-B{B}-N28-V128256-bf16")
 
 
 # ---------------------------------------------------------------------------

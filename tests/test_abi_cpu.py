@@ -154,3 +154,39 @@ def test_binding_refuses_host_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         ssd.load(str(tmp_path / "nope.so"))
+
+
+def test_fallback_fill_tree_argument_checks(lib):
+    """Host validation of the miss-fallback, cache-fill and tree calls: every
+    case here is refused (or is an empty batch) before any launch."""
+    E = ssd
+    nul = None
+    fake = ctypes.c_void_p(16)  # never dereferenced: each call returns before a launch
+    # n-gram backup: n or K out of range, negative sizes, empty batch
+    assert lib.ssd_ngram_backup(fake, 8, fake, 1, 33, 4, 10, nul, fake, nul, 0, fake, nul, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_ngram_backup(fake, 8, fake, 1, 3, 1025, 10, nul, fake, nul, 0, fake, nul, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_ngram_backup(fake, 8, fake, -1, 3, 4, 10, nul, fake, nul, 0, fake, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_ngram_backup(fake, 8, fake, 1, 3, 4, 0, nul, fake, nul, 0, fake, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_ngram_backup(nul, 8, nul, 1, 3, 4, 10, nul, fake, nul, 0, fake, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_ngram_backup(nul, 0, nul, 0, 3, 4, 10, nul, nul, nul, 0, nul, nul, nul, nul) == E.SSD_OK
+    # plan: empty batch, too many options, bad timings
+    tb = (ctypes.c_double * 9)(*([0.1] * 9))
+    em = (ctypes.c_double * 9)(*([1.0] * 9))
+    assert lib.ssd_fallback_plan(fake, fake, 0, 1.0, 0.5, 1, tb, em, nul, nul, nul, nul, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_fallback_plan(fake, fake, 4, 1.0, 0.5, 9, tb, em, nul, nul, nul, nul, nul, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_fallback_plan(fake, fake, 4, 0.0, 0.0, 1, tb, em, nul, nul, nul, nul, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_fallback_plan(fake, fake, 4, 1.0, -1.0, 1, tb, em, nul, nul, nul, nul, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    # K/V append: d not a multiple of 8 or above 256, empty batch
+    assert lib.ssd_kv_append(fake, fake, fake, fake, fake, 4, 8, fake, 0, 2, 3, 2, 12, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_kv_append(fake, fake, fake, fake, fake, 4, 8, fake, 0, 2, 3, 2, 264, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_kv_append(fake, fake, fake, fake, fake, 0, 8, fake, 0, 2, 3, 2, 64, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_kv_append(nul, nul, nul, nul, nul, 4, 8, nul, 0, 0, 3, 2, 64, nul, nul) == E.SSD_OK
+    # per-branch draw: column past the payload, C outside (0, 1], workspace missing
+    assert lib.ssd_fill_sample(fake, E.SSD_F32, 16, 1, 2, 16, 2, 0.5, 1.0, fake, 3, 3, fake, nul, fake, fake, nul, 0, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_fill_sample(fake, E.SSD_F32, 16, 1, 2, 16, 2, 0.0, 1.0, fake, 0, 3, fake, nul, fake, fake, nul, 1 << 20, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_fill_sample(fake, E.SSD_F32, 16, 1, 2, 16, 2, 0.5, 1.0, fake, 0, 3, fake, nul, fake, fake, nul, 0, nul) == E.SSD_ERR_WORKSPACE
+    # tree: too many nodes, rows above 512 KiB, bad temperature, empty batch
+    assert lib.ssd_tree_verify(fake, fake, E.SSD_F32, 0, 16, 1, 257, 16, 1.0, fake, fake, fake, fake, fake, fake, fake, nul, nul, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_tree_verify(fake, fake, E.SSD_F32, 0, 131080, 1, 2, 131080, 1.0, fake, fake, fake, fake, fake, fake, fake, nul, nul, fake, nul) == E.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_tree_verify(fake, fake, E.SSD_F32, 0, 16, 1, 2, 16, -1.0, fake, fake, fake, fake, fake, fake, fake, nul, nul, fake, nul) == E.SSD_ERR_INVALID_ARG
+    assert lib.ssd_tree_verify(nul, nul, E.SSD_BF16, 0, 16, 0, 2, 16, 1.0, nul, nul, nul, nul, nul, nul, nul, nul, nul, nul, nul) == E.SSD_OK
