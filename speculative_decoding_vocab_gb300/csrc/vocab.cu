@@ -19,7 +19,8 @@
 //            2^(z log2e/T - fl(max log2e/T)), its argmax where it is used,
 //            and, for rows a draw reads, the eight block sums; for draft rows
 //            with a top-F list, the eight block maximum keys.  No barrier and
-//            no shared memory: a CTA is eight independent warps.
+//            no shared memory: a CTA is four independent warps (eight CTAs per
+//            SM, so the grid's last wave is small).
 //   k_pair   one CTA per row pair (target row j, draft row j) of a sequence:
 //            merges the segment records into row statistics, selects the
 //            top-F from the block maxima (re-reading the few candidate blocks,
@@ -51,7 +52,9 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSegVec = 256;                   // 16-byte vectors per segment (one warp)
 constexpr int kSegBlocks = 8;                  // blocks of 32 vectors per segment
-constexpr int kUnitSeg = kWarps;               // segments per k_stats CTA
+constexpr int kUnitSeg = kWarps;               // segments per residual-unit staging (k_resid)
+constexpr int kStatWarps = 4;                  // segments (one per warp) per k_stats CTA: 128 threads,
+                                               // 8 CTAs per SM, a fine-grained last wave
 constexpr int kResSeg = kWarps / 2;            // segments per residual unit (two warps per segment)
 constexpr int kMaxSeg = 1024;                  // rows of at most 4 MiB
 constexpr int kMaxUnits = kMaxSeg / kResSeg;   // 256
@@ -471,7 +474,7 @@ SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, in
 // k_stats: one warp per segment of a row
 // ===========================================================================
 template <class E>
-__global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ VocabArgs a) {
+__global__ void __launch_bounds__(kStatWarps * 32, 8) k_stats(const __grid_constant__ VocabArgs a) {
   // k_pair may start launching once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the start mark only: at 64 registers an end mark makes the statistics pass spill
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(const __grid_constant__ V
     trace_start(a, (static_cast<long>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
                 a.b0 + static_cast<int>(blockIdx.z), static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x));
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sg = static_cast<int>(blockIdx.x) * kWarps + warp;
+  const int sg = static_cast<int>(blockIdx.x) * kStatWarps + warp;
   const int slot = static_cast<int>(blockIdx.y);
   const int b = a.b0 + static_cast<int>(blockIdx.z);
   const RowSlot rs = a.slot[slot];
@@ -1864,7 +1867,7 @@ cudaError_t launch_dependent(Kern kern, unsigned grid, size_t smem, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// k_stats over every (chunk of 8 segments, row slot, sequence), then k_pair
+// k_stats over every (chunk of 4 segments, row slot, sequence), then k_pair
 // (one CTA per sequence and row pair) and, when verifying or for the
 // analytics, k_resid.
 template <class E>
@@ -1885,7 +1888,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     g_attr_set[ti][dev / 64].fetch_or(bit);
   }
-  const unsigned nchunks = static_cast<unsigned>((a.nseg + kUnitSeg - 1) / kUnitSeg);
+  const unsigned nchunks = static_cast<unsigned>((a.nseg + kStatWarps - 1) / kStatWarps);
   const long n1 = static_cast<long>(nchunks) * a.nslots * a.B;
   const long n2 = static_cast<long>(a.B) * a.npairs;
   const bool resid = a.do_verify || a.do_analytics;
@@ -1902,7 +1905,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   for (int b0 = 0; b0 < a.B; b0 += 65535) {
     a.b0 = b0;
     const unsigned nb = static_cast<unsigned>(a.B - b0 < 65535 ? a.B - b0 : 65535);
-    k_stats<E><<<dim3(nchunks, static_cast<unsigned>(a.nslots), nb), kThreads, 0, s>>>(a);
+    k_stats<E><<<dim3(nchunks, static_cast<unsigned>(a.nslots), nb), kStatWarps * 32, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
