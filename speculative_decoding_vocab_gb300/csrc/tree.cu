@@ -129,10 +129,10 @@ struct Dist {
   float invSp, invSq;  // 1 / the row sums of 2^(z kT - R)
   int ap, aq;          // greedy argmaxes
   SSD_DEV float p(float z, int idx) const {
-    return greedy ? (idx == ap ? 1.f : 0.f) : __fmul_rn(exp2f(__fmaf_rn(z, kT, -Rp)), invSp);
+    return greedy ? (idx == ap ? 1.f : 0.f) : __fmul_rn(ex2(__fmaf_rn(z, kT, -Rp)), invSp);
   }
   SSD_DEV float q(float z, int idx) const {
-    return greedy ? (idx == aq ? 1.f : 0.f) : __fmul_rn(exp2f(__fmaf_rn(z, kT, -Rq)), invSq);
+    return greedy ? (idx == aq ? 1.f : 0.f) : __fmul_rn(ex2(__fmaf_rn(z, kT, -Rq)), invSq);
   }
 };
 
@@ -301,8 +301,8 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
           E::unpack(sD[(warp + kTWarps * k) * 32 + lane], fd);
 #pragma unroll
           for (int e = 0; e < E::kVec; ++e) {
-            if (mt != NEG_INF) st = __fadd_rn(st, exp2f(__fmaf_rn(ft[e], a.kT, -Rt)));
-            if (md != NEG_INF) sd = __fadd_rn(sd, exp2f(__fmaf_rn(fd[e], a.kT, -Rd)));
+            if (mt != NEG_INF) st = __fadd_rn(st, ex2(__fmaf_rn(ft[e], a.kT, -Rt)));
+            if (md != NEG_INF) sd = __fadd_rn(sd, ex2(__fmaf_rn(fd[e], a.kT, -Rd)));
           }
         }
       }
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
             const float R = __fmul_rn(M, a.kT);
             for (int w = 0; w < kTWarps; ++w)
               if (sh.wred[w][2 * h] != NEG_INF)
-                S = __fadd_rn(S, __fmul_rn(sh.wred[w][2 * h + 1], exp2f(__fsub_rn(__fmul_rn(sh.wred[w][2 * h], a.kT), R))));
+                S = __fadd_rn(S, __fmul_rn(sh.wred[w][2 * h + 1], ex2(__fsub_rn(__fmul_rn(sh.wred[w][2 * h], a.kT), R))));
           }
           r[2 * h] = M;
           r[2 * h + 1] = S;
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
           const float R = __fmul_rn(M, kT);
           for (int r = 0; r < n; ++r)
             if (all.a(r, 2 * h) != NEG_INF)
-              S = __fadd_rn(S, __fmul_rn(all.a(r, 2 * h + 1), exp2f(__fsub_rn(__fmul_rn(all.a(r, 2 * h), kT), R))));
+              S = __fadd_rn(S, __fmul_rn(all.a(r, 2 * h + 1), ex2(__fsub_rn(__fmul_rn(all.a(r, 2 * h), kT), R))));
           s.res[2 * h] = R;
           s.res[2 * h + 1] = S;
         }

@@ -70,6 +70,15 @@ constexpr int kTgt = 0, kDft = 1;
 // events are counted (the optional near_ties output).
 constexpr float kNearTie = 1e-6f;
 
+// A pair's record and its guess list are published by writing kReady into
+// the pair's two ready words (release); k_resid polls its sequence's words
+// (acquire) instead of waiting for the whole pair grid.  The sequence's last
+// residual unit sets them back to 0 once the pair grid has completed, so every
+// verification call leaves them 0; a 64-bit value makes a match in a never
+// used workspace practically impossible.
+constexpr unsigned long long kReady = 0x9E3779B97F4A7C15ull;
+constexpr uint32_t kReadyPolls = 1u << 16;  // then the grid's completion is awaited instead
+
 // flag bits of a position's record
 constexpr uint32_t kRecAccepted = 1u;   // the acceptance test passed
 constexpr uint32_t kRecDrawNear = 2u;   // the draw of d was a near-tie
@@ -140,6 +149,7 @@ struct VocabArgs {
   int32_t *d_out;
   float *qd_out;
   int32_t *fill_payload;  // cache fill: the draw of sequence b also goes to fill_payload[b * fill_stride + fill_col]
+  unsigned long long *ready;  // verification: [B][K+1][2] record / guess list published (kReady), else 0; NULL otherwise
   int fill_stride, fill_col;
   int32_t *accept_len, *out_tokens, *bonus;
   float *accept_prob, *resid_mass;
@@ -159,6 +169,20 @@ SSD_DEV const char *row_ptr(const VocabArgs &a, int tensor, int b, int row, int 
   return base + (static_cast<int64_t>(b) * a.seq_stride + static_cast<int64_t>(row) * a.row_stride) * esize;
 }
 SSD_DEV size_t slot_index(const VocabArgs &a, int b, int slot) { return static_cast<size_t>(b) * a.nslots + slot; }
+
+// Publishing a pair's results (release) and waiting for them (acquire, bounded).
+SSD_DEV void publish_ready(unsigned long long *p) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(kReady) : "memory");
+}
+SSD_DEV bool wait_ready(const unsigned long long *p) {
+  for (uint32_t it = 0; it < kReadyPolls; ++it) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    if (v == kReady) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
 
 // Trace marks (ssd_set_trace): %globaltimer.
 SSD_DEV unsigned long long now_ns() {
@@ -481,6 +505,9 @@ __global__ void __launch_bounds__(kStatWarps * 32, 8) k_stats(const __grid_const
   if (a.trace && threadIdx.x == 0)
     trace_start(a, (static_cast<long>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
                 a.b0 + static_cast<int>(blockIdx.z), static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x));
+  if (a.ready && a.hits && a.do_lookup && a.b0 == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+      threadIdx.x == 0)
+    *a.hits = 0u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sg = static_cast<int>(blockIdx.x) * kStatWarps + warp;
   const int slot = static_cast<int>(blockIdx.y);
@@ -921,6 +948,9 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
   const bool bonus_p = a.do_verify && j == K && !greedy;
   // C < 1 weights the draft's draw by S: it waits for the top-F list
   const bool weighted = !greedy && sampled && a.C < 1.f && F > 0;
+  // with C = 1 (or greedy) the record does not depend on S (N = 1, and in or
+  // out of S the draft's weight is the same): it is published before the top-F
+  const bool early = a.ready != nullptr && (greedy || a.C >= 1.f);
   const char *rowT = row_ptr(a, 0, b, j, E::kSize);
   const char *rowD = row_ptr(a, 1, b, j, E::kSize);
   // the counters k_resid takes tickets on and the hit count start at zero
@@ -928,7 +958,7 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
   if (tid == 0) {
     if (j == 0) a.ctr[2 + b] = 0u;
     if (j < K && a.do_analytics) a.ctr[2 + a.B + static_cast<size_t>(b) * K + j] = 0u;
-    if (b == 0 && j == 0 && a.do_lookup && a.hits) *a.hits = 0u;
+    if (!a.ready && b == 0 && j == 0 && a.do_lookup && a.hits) *a.hits = 0u;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");  // k_stats has completed
   if (a.trace && tid == 0) sh.mk[2] = now_ns();
@@ -1036,76 +1066,9 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
     }
   }
   if (a.trace && tid == 0) sh.mk[5] = now_ns();
-  // the draft row's top-F list S (warps 1..7, while warp 0 draws), its
-  // normalised mass and the guesses of depth j
-  if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.gm[kDft], ad);
-  if (F >= 2 && warp > 0) row_topf<E>(a, rowD, F, pb.keys, sh);
-  __syncthreads();
-  if (warp == 1) {
-    float sq = 0.f;
-    if (!greedy && F > 0 && sh.gm[kDft] != NEG_INF) {
-      for (int i = lane; i < F; i += 32)
-        if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
-      sq = __fdiv_rn(warp_sum(sq), sh.gs[kDft]);
-    }
-    if (lane == 0) sh.sq = sq;
-  }
-  if (a.do_predict && hD) {
-    const int sumF = a.foff[K + 1];
-    for (int i = tid; i < a.F[j]; i += kThreads) {
-      const uint64_t key = sh.S[i];
-      a.guess[static_cast<size_t>(b) * sumF + a.foff[j] + i] = cand_idx(key);
-      if (a.guess_q) {
-        float q;
-        if (greedy) q = (i == 0) ? 1.f : 0.f;
-        else q = __fdiv_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), sh.gs[kDft]);
-        a.guess_q[static_cast<size_t>(b) * sumF + a.foff[j] + i] = q;
-      }
-    }
-  }
-  __syncthreads();
-  if (a.trace && tid == 0) sh.mk[6] = now_ns();
-  const uint64_t keyF = F > 0 ? sh.S[F - 1] : 0ull;
-  const float vF = cand_val(keyF);
-  const float N = norm_N(a.C, sh.sq);
-  if (weighted) {
-    // the Saguaro weights: block masses with the elements of S down-weighted
-    // (in list order), segment masses in row units from them
-    for (int i = tid; i < a.nblk; i += kThreads) {
-      float m = pb.bm[i];
-      const float Ms = __fmul_rn(srd[i / kSegBlocks].m, a.kT);
-      for (int t = 0; t < F; ++t) {
-        const uint64_t key = sh.S[t];
-        if (!key || (cand_idx(key) / E::kVec) / 32 != i) continue;
-        m = __fsub_rn(m, __fmul_rn(__fsub_rn(1.f, a.C), ex2(__fmaf_rn(cand_val(key), a.kT, -Ms))));
-      }
-      pb.bm[i] = fmaxf(m, 0.f);
-    }
-    __syncthreads();
-    for (int s = warp; s < a.nseg; s += kWarps) {
-      const float t = warp_total(pb.bm + s * kSegBlocks, kSegBlocks);
-      if (lane == 0) {
-        const float m = srd[s].m;
-        pb.smm[s] = (m == NEG_INF) ? 0.f : __fmul_rn(t, ex2(__fsub_rn(__fmul_rn(m, a.kT), rowMk)));
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const WDraft wd{a.kT, a.C, vF, keyF, true};
-      bool near;
-      int d = row_draw<E>(a, pb.segD, mdk, pb.smm, pb.bm, hT ? rowT : nullptr, rowD,
-                          a.u_draft[static_cast<size_t>(b) * K + j], wd, &near, &zt, &zd);
-      zknown = d >= 0;
-      if (d < 0) {
-        d = ad;
-        near = true;
-      }
-      r.d = d;
-      if (near) r.fl |= kRecDrawNear;
-    }
-  }
-  // p(d), q'(d), the verdict, the outputs and the record (warp 0)
-  if (warp == 0) {
+  // p(d), q'(d), the verdict, the outputs and the record (warp 0); with the
+  // ready words the record is published (release) right after it is written
+  auto finish = [&](float N, uint64_t keyF) {
     r.N = N;
     r.keyF = keyF;
     r.gm[kTgt] = sh.gm[kTgt];
@@ -1155,6 +1118,7 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
         a.accept_prob[static_cast<size_t>(b) * K + j] = ap;
       }
       if (a.do_verify) a.rec[static_cast<size_t>(b) * (K + 1) + j] = r;
+      if (a.ready) publish_ready(&a.ready[(static_cast<size_t>(b) * (K + 1) + j) * 2]);
       if (a.do_analytics) {
         // the hit partials come from warp 1 (below); the rest of the record here
         PairRec *dst = a.rec + static_cast<size_t>(b) * (K + 1) + j;
@@ -1166,7 +1130,82 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
         dst->gs[1] = r.gs[1];
       }
     }
+  };
+  if (early && warp == 0) finish(1.f, 0ull);
+  // the draft row's top-F list S (warps 1..7, while warp 0 draws), its
+  // normalised mass and the guesses of depth j
+  if (F == 1 && tid == 0) sh.S[0] = cand_key(sh.gm[kDft], ad);
+  if (F >= 2 && warp > 0) row_topf<E>(a, rowD, F, pb.keys, sh);
+  __syncthreads();
+  if (warp == 1) {
+    float sq = 0.f;
+    if (!greedy && F > 0 && sh.gm[kDft] != NEG_INF) {
+      for (int i = lane; i < F; i += 32)
+        if (sh.S[i]) sq = __fadd_rn(sq, ex2(__fmaf_rn(cand_val(sh.S[i]), a.kT, -mdk)));
+      sq = __fdiv_rn(warp_sum(sq), sh.gs[kDft]);
+    }
+    if (lane == 0) sh.sq = sq;
   }
+  if (a.do_predict && hD) {
+    const int sumF = a.foff[K + 1];
+    for (int i = tid; i < a.F[j]; i += kThreads) {
+      const uint64_t key = sh.S[i];
+      a.guess[static_cast<size_t>(b) * sumF + a.foff[j] + i] = cand_idx(key);
+      if (a.guess_q) {
+        float q;
+        if (greedy) q = (i == 0) ? 1.f : 0.f;
+        else q = __fdiv_rn(ex2(__fmaf_rn(cand_val(key), a.kT, -mdk)), sh.gs[kDft]);
+        a.guess_q[static_cast<size_t>(b) * sumF + a.foff[j] + i] = q;
+      }
+    }
+  }
+  __syncthreads();
+  if (a.ready && tid == 0) {  // the guess list of depth j is written
+    __threadfence();
+    publish_ready(&a.ready[(static_cast<size_t>(b) * (K + 1) + j) * 2 + 1]);
+  }
+  if (a.trace && tid == 0) sh.mk[6] = now_ns();
+  const uint64_t keyF = F > 0 ? sh.S[F - 1] : 0ull;
+  const float vF = cand_val(keyF);
+  const float N = norm_N(a.C, sh.sq);
+  if (weighted) {
+    // the Saguaro weights: block masses with the elements of S down-weighted
+    // (in list order), segment masses in row units from them
+    for (int i = tid; i < a.nblk; i += kThreads) {
+      float m = pb.bm[i];
+      const float Ms = __fmul_rn(srd[i / kSegBlocks].m, a.kT);
+      for (int t = 0; t < F; ++t) {
+        const uint64_t key = sh.S[t];
+        if (!key || (cand_idx(key) / E::kVec) / 32 != i) continue;
+        m = __fsub_rn(m, __fmul_rn(__fsub_rn(1.f, a.C), ex2(__fmaf_rn(cand_val(key), a.kT, -Ms))));
+      }
+      pb.bm[i] = fmaxf(m, 0.f);
+    }
+    __syncthreads();
+    for (int s = warp; s < a.nseg; s += kWarps) {
+      const float t = warp_total(pb.bm + s * kSegBlocks, kSegBlocks);
+      if (lane == 0) {
+        const float m = srd[s].m;
+        pb.smm[s] = (m == NEG_INF) ? 0.f : __fmul_rn(t, ex2(__fsub_rn(__fmul_rn(m, a.kT), rowMk)));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const WDraft wd{a.kT, a.C, vF, keyF, true};
+      bool near;
+      int d = row_draw<E>(a, pb.segD, mdk, pb.smm, pb.bm, hT ? rowT : nullptr, rowD,
+                          a.u_draft[static_cast<size_t>(b) * K + j], wd, &near, &zt, &zd);
+      zknown = d >= 0;
+      if (d < 0) {
+        d = ad;
+        near = true;
+      }
+      r.d = d;
+      if (near) r.fl |= kRecDrawNear;
+    }
+  }
+  if (!early && warp == 0) finish(N, keyF);
+
   // analytics: the guesses' target and residual probability (all of S carries C in q')
   if (a.do_analytics && warp == 1) {
     float hp = 0.f, hr = 0.f;
@@ -1473,6 +1512,33 @@ SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, Res
   return sh.ival[3];
 }
 
+// Every thread: wait (bounded) for a ready word read by thread 0; when it does
+// not come in time, for the completion of the whole pair grid instead.
+SSD_DEV void await_word(const unsigned long long *w) {
+  bool ok = true;
+  if (threadIdx.x == 0) ok = wait_ready(w);
+  if (__syncthreads_or(!ok)) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// The guess list of depth acc for the lookup, once its pair has written it
+// (into sh.look at its offset when the lists are staged).
+SSD_DEV void ready_lookup(const VocabArgs &a, int b, int acc, bool staged, ResSh &sh) {
+  if (!a.do_lookup) return;
+  await_word(&a.ready[(static_cast<size_t>(b) * (a.K + 1) + acc) * 2 + 1]);
+  if (staged) {
+    const int sumF = a.foff[a.K + 1];
+    for (int i = threadIdx.x; i < a.F[acc]; i += kThreads)
+      sh.look[a.foff[acc] + i] = __ldcg(a.guess + static_cast<size_t>(b) * sumF + a.foff[acc] + i);
+  }
+  __syncthreads();
+}
+// The sequence's last unit (every thread): once the pair grid has completed no
+// pair writes the sequence's ready words again; they go back to 0.
+SSD_DEV void reset_ready(const VocabArgs &a, int b) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int t = threadIdx.x; t < 2 * a.npairs; t += kThreads)
+    a.ready[static_cast<size_t>(b) * (a.K + 1) * 2 + t] = 0ull;
+}
+
 template <class E>
 __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ VocabArgs a) {
   __shared__ ResSh sh;
@@ -1485,8 +1551,10 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
     for (int k = 0; k < 8; ++k) sh.mk[k] = 0ull;
     sh.mk[1] = now_ns();
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // k_pair has completed
-  if (a.trace && tid == 0) sh.mk[2] = now_ns();
+  // verification waits for its own sequence's records (ready words); the
+  // analytics for the whole pair grid
+  const bool proto = a.ready != nullptr;
+  if (!proto) asm volatile("griddepcontrol.wait;" ::: "memory");  // k_pair has completed
   int b = 0, u = 0;
   if (a.do_analytics) {
     // unit u of pair j < K (K = 0: one CTA per sequence, finishing it):
@@ -1566,13 +1634,20 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
     // lists staged alongside (a finishing unit needs them)
     b = static_cast<int>(blockIdx.x) / U;
     u = static_cast<int>(blockIdx.x) - b * U;
+    if (proto) {
+      bool ok = true;
+      if (tid < a.npairs) ok = wait_ready(&a.ready[(static_cast<size_t>(b) * (K + 1) + tid) * 2]);
+      if (__syncthreads_or(!ok)) asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+    if (a.trace && tid == 0) sh.mk[2] = now_ns();
     const int sumF = a.foff[K + 1];
     const bool staged = a.do_lookup && sumF * (K + 1) <= kLookupStage;
     for (int i = tid; i < a.npairs * 4; i += kThreads)
       cp_async16(reinterpret_cast<int4 *>(sh.rec) + i, reinterpret_cast<const int4 *>(a.rec + static_cast<size_t>(b) * (K + 1)) + i);
     for (int t = tid; t < K; t += kThreads) sh.u[t] = a.u_acc[static_cast<size_t>(b) * K + t];
     if (staged) {
-      for (int i = tid; i < sumF; i += kThreads) cp_async4(&sh.look[i], a.guess + static_cast<size_t>(b) * sumF + i);
+      if (!proto)  // with the ready words each list is read once its pair has written it
+        for (int i = tid; i < sumF; i += kThreads) cp_async4(&sh.look[i], a.guess + static_cast<size_t>(b) * sumF + i);
       if (a.payload && a.next_tokens)
         for (int i = tid; i < sumF * K; i += kThreads)
           cp_async4(&sh.look[sumF + i], a.payload + static_cast<size_t>(b) * sumF * K + i);
@@ -1584,8 +1659,17 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
     while (acc < K && (sh.rec[acc].fl & kRecAccepted)) ++acc;
     if (a.greedy || acc == K) {
       if (u == 0) {
+        if (proto) ready_lookup(a, b, acc, staged, sh);
         const PairRec &r = sh.rec[acc];
         emit(a, b, acc, r.bt, r.W, (r.fl & kRecZero) != 0, (r.fl & kRecBonusNear) != 0, staged, sh);
+      }
+      if (proto) {  // every unit takes a ticket; the last one resets the ready words
+        if (tid == 0) {
+          __threadfence();
+          sh.ival[0] = (atomicAdd(a.ctr + 2 + b, 1u) + 1 == static_cast<uint32_t>(U)) ? 1 : 0;
+        }
+        __syncthreads();
+        if (sh.ival[0]) reset_ready(a, b);
       }
     } else {
       // the residual of the first rejected position: this unit's block sums
@@ -1633,7 +1717,9 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
           near = true;
         }
         if (a.trace && tid == 0) sh.mk[6] = now_ns();
+        if (proto) ready_lookup(a, b, acc, staged, sh);
         emit(a, b, acc, bt, W, zero, near, staged, sh);
+        if (proto) reset_ready(a, b);
       }
     }
   }
@@ -1694,7 +1780,7 @@ namespace {
 
 struct Layout {
   int nvec, nfull, nseg, nblk, nunits;
-  size_t ctr_words, ctr_off, seg_off, bsum_off, bkey_off, rec_off, umass_off, useg_off, amass_off, total;
+  size_t ctr_words, ctr_off, seg_off, bsum_off, bkey_off, rec_off, umass_off, useg_off, amass_off, ready_off, total;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1734,6 +1820,8 @@ bool make_layout(int B, int K, int V, ssd_dtype_t dt, const int32_t *F, Layout *
   o = align_up(o + Bn * L->nseg * sizeof(float2), 256);
   L->amass_off = o;
   o = align_up(o + Bn * (K > 0 ? K : 1) * L->nunits * sizeof(float2), 256);
+  L->ready_off = o;
+  o = align_up(o + Bn * (K + 1) * 2 * sizeof(unsigned long long), 256);
   L->total = o;
   return true;
 }
@@ -1802,6 +1890,7 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   a.umass = reinterpret_cast<float2 *>(w + L.umass_off);
   a.useg = reinterpret_cast<float2 *>(w + L.useg_off);
   a.amass = reinterpret_cast<float2 *>(w + L.amass_off);
+  a.ready = reinterpret_cast<unsigned long long *>(w + L.ready_off);
   a.status = status;
   return a;
 }
@@ -1900,6 +1989,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
                 : nullptr;
   a.trace_pair = n1;
   a.trace_resid = n1 + n2;
+  if (!(a.do_verify && !a.do_analytics)) a.ready = nullptr;
   if (g_ev_before) cudaEventRecord(g_ev_before, s);
   // grid (chunk, row slot, sequence); sequences in launches of at most 65535
   for (int b0 = 0; b0 < a.B; b0 += 65535) {

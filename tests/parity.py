@@ -76,8 +76,9 @@ def to_dev(arr, dev="cuda"):
     return ssd.tensor(arr, dev)
 
 
-def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True):
-    """Run one round on the GPU (fused ssd_round, or the four separate calls)."""
+def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True, ws=None):
+    """Run one round on the GPU (fused ssd_round, or the four separate calls);
+    ``ws``: a workspace to use instead of a fresh one."""
     spec = inp.spec
     T = spec.T if T is None else T
     C = spec.C if C is None else C
@@ -93,7 +94,8 @@ def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True):
              guess_q=torch.zeros(B, sumF, **f32), slot=torch.full((B,), -7, **i32),
              next_tokens=torch.full((B, K), -7, **i32), hits=torch.full((1,), 12345, **i32),
              near_ties=torch.zeros(1, **i32), status=torch.zeros(1, **i32))
-    ws = ssd.workspace(B, K, V, spec.dtype, spec.F, dev)
+    if ws is None:
+        ws = ssd.workspace(B, K, V, spec.dtype, spec.F, dev)
     ud, ua, ub = to_dev(inp.u_draft, dev), to_dev(inp.u_acc, dev), to_dev(inp.u_bonus, dev)
     pl = to_dev(inp.payload, dev) if inp.payload is not None else None
     if fused:

@@ -230,3 +230,34 @@ def test_argument_errors():
     assert e.value.code == ssd.SSD_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+
+
+def test_one_workspace_across_calls_of_every_kind():
+    """One workspace (filled with 0xFF bytes first) serves verification calls of
+    several shapes, temperatures and C, with analytics, sampling and
+    separate-call rounds in between: every result equals the oracle's, so no
+    call leaves a stale record or ready word for the next."""
+    import dataclasses
+    a = w.RoundSpec(B=6, K=4, V=4096, dtype="f32", recipe="gauss", T=1.0, C=1.0,
+                    F=(4, 2, 1, 1, 1), draft_noise=0.5, name="reuse-a")
+    b = dataclasses.replace(a, B=3, K=2, F=(3, 2, 1), name="reuse-b")
+    c = dataclasses.replace(a, V=5000, dtype="bf16", recipe="zipf", C=0.5, draft_noise=1.0,
+                            name="reuse-c")
+    n = max(ssd.ssd_workspace_size(s.B, s.K, s.V, s.dtype, s.F) for s in (a, b, c))
+    ws = torch.full((n,), 255, dtype=torch.uint8, device="cuda")
+    rep = Report()
+    ia, ib, ic = w.make_round(a, seed=31), w.make_round(b, seed=32), w.make_round(c, seed=33)
+    for step, (inp, kw) in enumerate([(ia, {}), (ib, {}), (ia, {"fused": False}), (ic, {}),
+                                      (ia, {"T": 0.0}), (ib, {"fused": False}), (ic, {"T": 0.0}),
+                                      (ia, {})]):
+        g = gpu_round(inp, ws=ws, **kw)
+        compare_round(inp, g, T=kw.get("T"), report=rep)
+        if step == 3:  # an analytics call on the same workspace in between
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            f32 = dict(dtype=torch.float32, device="cuda")
+            ssd.ssd_round_analytics(to_dev(ib.target), to_dev(ib.draft), b.V, b.F, b.C, b.T,
+                                    torch.empty(b.B, b.K + 1, **f32), torch.empty(b.B, **f32),
+                                    torch.empty(b.B, **f32), status=st, ws=ws)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+    assert rep.compared == 6 + 3 + 6 + 6 + 6 + 3 + 6 + 6
