@@ -98,7 +98,11 @@ ssd_status_t ssd_fanout_split(int budget, int K, double r, int32_t *F_out);
  * Workspace bytes the vocabulary calls (ssd_saguaro_sample, ssd_verify,
  * ssd_predict_outcomes, ssd_round) need for B sequences of K+1 rows of V
  * logits of type dt with fan-out F (host int32[K+1]).  Returns 0 for
- * unsupported arguments.
+ * unsupported arguments.  The workspace needs no initialisation: a
+ * verification call publishes each pair's record through 64-bit ready words
+ * in it (a fixed 64-bit value, never written by anything else) and sets them
+ * back to 0 before it completes.  Calls that share a workspace must not
+ * overlap on the GPU.
  */
 size_t ssd_workspace_size(int B, int K, int V, ssd_dtype_t dt, const int32_t *F);
 

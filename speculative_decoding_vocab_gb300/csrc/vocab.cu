@@ -1259,25 +1259,33 @@ struct __align__(16) ResSh {
   float u[kMaxK];
   float seg[kWarps][2];      // this unit's half-segment masses (residual, p), or its warps' analytics sums
   float um[2][kMaxUnits];    // the sequence's unit masses (residual, p)
-  float2 sgm[kMaxSeg];       // the sequence's segment masses (residual, p)
   float bx[kUnitSeg * kSegBlocks];
   float sm[kUnitSeg];
-  int32_t look[kLookupStage];  // the sequence's guesses, then its payload
   float scal[4];
   int ival[4];
   unsigned long long mk[8];
 };
-// The residual pass's vectors: per warp its segment of both rows (8 blocks of
-// 32 vectors), staged by cp.async so that the block loop need not be unrolled.
+// The residual pass's vectors: per warp its half segment of both rows (4
+// blocks of 32 vectors), staged by cp.async so that the block loop need not be
+// unrolled.  Once the pass is done the finishing unit reuses the space for the
+// final draw's blocks, the segment masses and the lookup lists, so that a unit
+// CTA stays small and every unit of the grid is resident early.
 struct __align__(16) ResStage {
-  uint4 v[kWarps][2][kSegBlocks / 2][32];
+  union {
+    uint4 v[kWarps][2][kSegBlocks / 2][32];
+    struct {
+      uint4 blk[kWarps][2][32];      // the final draw: one block of both rows per warp
+      float2 sgm[kMaxSeg];           // the sequence's segment masses (residual, p)
+      int32_t look[kLookupStage];    // the sequence's guesses, then its payload
+    } fin;
+  };
 };
 
 // The outputs of sequence b once its bonus token bt is known (sh.rec: its
-// records, sh.u: its acceptance uniforms, sh.look: its lookup lists when
+// records, sh.u: its acceptance uniforms, look: its lookup lists when
 // `staged`).
 SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero, bool near_bonus, bool staged,
-                  ResSh &sh) {
+                  ResSh &sh, const int32_t *look) {
   const int tid = threadIdx.x;
   const int K = a.K;
   const int sumF = a.foff[K + 1];
@@ -1300,7 +1308,7 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
   __syncthreads();
   if (a.do_lookup) {
     for (int i = tid; i < a.F[acc]; i += kThreads) {
-      const int g = staged ? sh.look[a.foff[acc] + i] : a.guess[static_cast<size_t>(b) * sumF + a.foff[acc] + i];
+      const int g = staged ? look[a.foff[acc] + i] : __ldcg(a.guess + static_cast<size_t>(b) * sumF + a.foff[acc] + i);
       if (g == bt) atomicMin(&sh.ival[3], i);
     }
     __syncthreads();
@@ -1316,7 +1324,7 @@ SSD_DEV void emit(const VocabArgs &a, int b, int acc, int bt, float W, bool zero
     for (int t = tid; t < K; t += kThreads) {
       int v = -1;
       if (s_hit >= 0 && a.payload)
-        v = staged ? sh.look[sumF + s_hit * K + t] : a.payload[(static_cast<size_t>(b) * sumF + s_hit) * K + t];
+        v = staged ? look[sumF + s_hit * K + t] : a.payload[(static_cast<size_t>(b) * sumF + s_hit) * K + t];
       a.next_tokens[static_cast<size_t>(b) * K + t] = v;
     }
   if (tid == 0) {
@@ -1347,6 +1355,25 @@ SSD_DEV void stage_blocks(const VocabArgs &a, int b, int j, int g0, int nb, int 
       st.v[w][0][k][lane] = row_vec<E>(a, rowT, v);
       st.v[w][1][k][lane] = row_vec<E>(a, rowD, v);
     }
+  }
+  cp_async_wait_all();
+  __syncwarp();
+}
+
+// Stage block g of row pair j of sequence b for warp w into the final draw's
+// space (every load the thread issued before, e.g. lookup lists, completes too).
+template <class E>
+SSD_DEV void stage_block1(const VocabArgs &a, int b, int j, int g, int w, ResStage &st) {
+  const int lane = threadIdx.x & 31;
+  const char *rowT = row_ptr(a, 0, b, j, E::kSize);
+  const char *rowD = row_ptr(a, 1, b, j, E::kSize);
+  const int v = g * 32 + lane;
+  if (v < a.nfull) {
+    cp_async16(&st.fin.blk[w][0][lane], rowT + static_cast<int64_t>(v) * 16);
+    cp_async16(&st.fin.blk[w][1][lane], rowD + static_cast<int64_t>(v) * 16);
+  } else {
+    st.fin.blk[w][0][lane] = row_vec<E>(a, rowT, v);
+    st.fin.blk[w][1][lane] = row_vec<E>(a, rowD, v);
   }
   cp_async_wait_all();
   __syncwarp();
@@ -1398,7 +1425,7 @@ SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr
 
 // The last residual unit of sequence b, every thread: the bonus from max(0,
 // p - q') of pair acc (p when the residual has no mass).  Warp 0 locates the
-// unit (sh.um) and the segment (sh.sgm); the eight warps read the segment's
+// unit (sh.um) and the segment (st.fin.sgm); the eight warps read the segment's
 // blocks again, one each, for their sums (lane sums, then a scan: the
 // arithmetic of the element search); warp 0 locates the block and the
 // element.  Returns the token (-1: no weight); sets *W (the residual mass),
@@ -1420,7 +1447,7 @@ SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, Res
     if (q >= 0) {
       if (lane < kResSeg) {
         const int t = q * kResSeg + lane;
-        sh.sm[lane] = (t < a.nseg) ? (X ? sh.sgm[t].y : sh.sgm[t].x) : 0.f;
+        sh.sm[lane] = (t < a.nseg) ? (X ? st.fin.sgm[t].y : st.fin.sgm[t].x) : 0.f;
       }
       __syncwarp();
       const int s = warp_locate(sh.sm, kResSeg, rem, true, &rem2, &W2, &fb2);
@@ -1444,12 +1471,12 @@ SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, Res
   const WProb wp{a.kT, wr.Mtk, wr.inv_st};
   // block `warp` of the segment: its sum
   const int g = sg * kSegBlocks + warp;
-  stage_blocks<E>(a, b, acc, g, 1, warp, st);
+  stage_block1<E>(a, b, acc, g, warp, st);
   {
     const int i0 = (g * 32 + lane) * E::kVec;
     float ft[E::kVec], fd[E::kVec], x[E::kVec];
-    E::unpack(st.v[warp][0][0][lane], ft);
-    E::unpack(st.v[warp][1][0][lane], fd);
+    E::unpack(st.fin.blk[warp][0][lane], ft);
+    E::unpack(st.fin.blk[warp][1][lane], fd);
 #pragma unroll
     for (int e = 0; e < E::kVec; ++e)
       x[e] = (i0 + e < a.V) ? (X ? wp(ft[e], 0.f, 0, 0.f) : wr(ft[e], fd[e], i0 + e, 0.f)) : 0.f;
@@ -1466,8 +1493,8 @@ SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, Res
       const int gk = sg * kSegBlocks + k;
       const int i0 = (gk * 32 + lane) * E::kVec;
       float ft[E::kVec], fd[E::kVec], x[E::kVec];
-      E::unpack(st.v[k][0][0][lane], ft);
-      E::unpack(st.v[k][1][0][lane], fd);
+      E::unpack(st.fin.blk[k][0][lane], ft);
+      E::unpack(st.fin.blk[k][1][lane], fd);
 #pragma unroll
       for (int e = 0; e < E::kVec; ++e)
         x[e] = (i0 + e < a.V) ? (X ? wp(ft[e], 0.f, 0, 0.f) : wr(ft[e], fd[e], i0 + e, 0.f)) : 0.f;
@@ -1519,17 +1546,21 @@ SSD_DEV void await_word(const unsigned long long *w) {
   if (threadIdx.x == 0) ok = wait_ready(w);
   if (__syncthreads_or(!ok)) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
-// The guess list of depth acc for the lookup, once its pair has written it
-// (into sh.look at its offset when the lists are staged).
-SSD_DEV void ready_lookup(const VocabArgs &a, int b, int acc, bool staged, ResSh &sh) {
+// The lookup lists: the guess list of depth acc once its pair has written it
+// (its ready word: thread 0 polls while the others load), and the payload,
+// into `look` at their offsets when the lists are staged.
+SSD_DEV void ready_lookup(const VocabArgs &a, int b, int acc, bool staged, int32_t *look) {
   if (!a.do_lookup) return;
-  await_word(&a.ready[(static_cast<size_t>(b) * (a.K + 1) + acc) * 2 + 1]);
-  if (staged) {
-    const int sumF = a.foff[a.K + 1];
+  const int sumF = a.foff[a.K + 1];
+  bool ok = true;
+  if (threadIdx.x == 0) ok = wait_ready(&a.ready[(static_cast<size_t>(b) * (a.K + 1) + acc) * 2 + 1]);
+  if (staged && a.payload && a.next_tokens)
+    for (int i = threadIdx.x; i < sumF * a.K; i += kThreads)
+      cp_async4(&look[sumF + i], a.payload + static_cast<size_t>(b) * sumF * a.K + i);
+  if (__syncthreads_or(!ok)) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (staged)
     for (int i = threadIdx.x; i < a.F[acc]; i += kThreads)
-      sh.look[a.foff[acc] + i] = __ldcg(a.guess + static_cast<size_t>(b) * sumF + a.foff[acc] + i);
-  }
-  __syncthreads();
+      cp_async4(&look[a.foff[acc] + i], a.guess + static_cast<size_t>(b) * sumF + a.foff[acc] + i);
 }
 // The sequence's last unit (every thread): once the pair grid has completed no
 // pair writes the sequence's ready words again; they go back to 0.
@@ -1539,8 +1570,10 @@ SSD_DEV void reset_ready(const VocabArgs &a, int b) {
     a.ready[static_cast<size_t>(b) * (a.K + 1) * 2 + t] = 0ull;
 }
 
+// 48 registers: every unit CTA then fits beside the pair kernel's CTAs, so no
+// sequence's units wait for the pair grid to drain before they start.
 template <class E>
-__global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ VocabArgs a) {
+__global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
   __shared__ ResSh sh;
   extern __shared__ __align__(16) uint8_t res_smem[];
   ResStage &st = *reinterpret_cast<ResStage *>(res_smem);
@@ -1634,7 +1667,7 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
     // lists staged alongside (a finishing unit needs them)
     b = static_cast<int>(blockIdx.x) / U;
     u = static_cast<int>(blockIdx.x) - b * U;
-    if (proto) {
+    {  // verification calls always publish their records (ready words)
       bool ok = true;
       if (tid < a.npairs) ok = wait_ready(&a.ready[(static_cast<size_t>(b) * (K + 1) + tid) * 2]);
       if (__syncthreads_or(!ok)) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1645,13 +1678,6 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
     for (int i = tid; i < a.npairs * 4; i += kThreads)
       cp_async16(reinterpret_cast<int4 *>(sh.rec) + i, reinterpret_cast<const int4 *>(a.rec + static_cast<size_t>(b) * (K + 1)) + i);
     for (int t = tid; t < K; t += kThreads) sh.u[t] = a.u_acc[static_cast<size_t>(b) * K + t];
-    if (staged) {
-      if (!proto)  // with the ready words each list is read once its pair has written it
-        for (int i = tid; i < sumF; i += kThreads) cp_async4(&sh.look[i], a.guess + static_cast<size_t>(b) * sumF + i);
-      if (a.payload && a.next_tokens)
-        for (int i = tid; i < sumF * K; i += kThreads)
-          cp_async4(&sh.look[sumF + i], a.payload + static_cast<size_t>(b) * sumF * K + i);
-    }
     cp_async_wait_all();
     __syncthreads();
     if (a.trace && tid == 0) sh.mk[3] = now_ns();
@@ -1659,18 +1685,20 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
     while (acc < K && (sh.rec[acc].fl & kRecAccepted)) ++acc;
     if (a.greedy || acc == K) {
       if (u == 0) {
-        if (proto) ready_lookup(a, b, acc, staged, sh);
-        const PairRec &r = sh.rec[acc];
-        emit(a, b, acc, r.bt, r.W, (r.fl & kRecZero) != 0, (r.fl & kRecBonusNear) != 0, staged, sh);
-      }
-      if (proto) {  // every unit takes a ticket; the last one resets the ready words
-        if (tid == 0) {
-          __threadfence();
-          sh.ival[0] = (atomicAdd(a.ctr + 2 + b, 1u) + 1 == static_cast<uint32_t>(U)) ? 1 : 0;
-        }
+        ready_lookup(a, b, acc, staged, st.fin.look);
+        cp_async_wait_all();
         __syncthreads();
-        if (sh.ival[0]) reset_ready(a, b);
+        const PairRec &r = sh.rec[acc];
+        emit(a, b, acc, r.bt, r.W, (r.fl & kRecZero) != 0, (r.fl & kRecBonusNear) != 0, staged, sh,
+             st.fin.look);
       }
+      // every unit takes a ticket; the last one resets the ready words
+      if (tid == 0) {
+        __threadfence();
+        sh.ival[0] = (atomicAdd(a.ctr + 2 + b, 1u) + 1 == static_cast<uint32_t>(U)) ? 1 : 0;
+      }
+      __syncthreads();
+      if (sh.ival[0]) reset_ready(a, b);
     } else {
       // the residual of the first rejected position: this unit's block sums
       const WResid wr = resid_weights(a, sh.rec[acc], a.Fs[acc]);
@@ -1701,14 +1729,28 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
       __syncthreads();
       if (a.trace && tid == 0) sh.mk[5] = now_ns();
       if (sh.ival[0]) {
-        // the last unit: the bonus (every unit and segment mass in one round of loads)
-        for (int q = tid; q < U; q += kThreads) {
-          const float2 v = __ldcg(a.umass + static_cast<size_t>(b) * U + q);
-          sh.um[0][q] = v.x;
-          sh.um[1][q] = v.y;
+        // the last unit: the bonus.  Every unit and segment mass in one round
+        // of loads while thread 0 checks that the outcome's guess list is
+        // written; the lookup lists are copied while the draw runs.
+        bool ok = true;
+        if (tid == 0) {
+          if (a.do_lookup) ok = wait_ready(&a.ready[(static_cast<size_t>(b) * (K + 1) + acc) * 2 + 1]);
+        } else {
+          for (int q = tid - 1; q < U; q += kThreads - 1) {
+            const float2 v = __ldcg(a.umass + static_cast<size_t>(b) * U + q);
+            sh.um[0][q] = v.x;
+            sh.um[1][q] = v.y;
+          }
+          for (int t = tid - 1; t < a.nseg; t += kThreads - 1)
+            st.fin.sgm[t] = __ldcg(a.useg + static_cast<size_t>(b) * a.nseg + t);
         }
-        for (int t = tid; t < a.nseg; t += kThreads) sh.sgm[t] = __ldcg(a.useg + static_cast<size_t>(b) * a.nseg + t);
-        __syncthreads();
+        if (staged && a.payload && a.next_tokens)
+          for (int i = tid; i < sumF * K; i += kThreads)
+            cp_async4(&st.fin.look[sumF + i], a.payload + static_cast<size_t>(b) * sumF * K + i);
+        if (__syncthreads_or(!ok)) asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (staged)
+          for (int i = tid; i < a.F[acc]; i += kThreads)
+            cp_async4(&st.fin.look[a.foff[acc] + i], a.guess + static_cast<size_t>(b) * sumF + a.foff[acc] + i);
         float W;
         bool zero, near;
         int bt = resid_draw<E>(a, b, acc, wr, sh, st, &W, &zero, &near);
@@ -1717,9 +1759,10 @@ __global__ void __launch_bounds__(kThreads) k_resid(const __grid_constant__ Voca
           near = true;
         }
         if (a.trace && tid == 0) sh.mk[6] = now_ns();
-        if (proto) ready_lookup(a, b, acc, staged, sh);
-        emit(a, b, acc, bt, W, zero, near, staged, sh);
-        if (proto) reset_ready(a, b);
+        cp_async_wait_all();
+        __syncthreads();
+        emit(a, b, acc, bt, W, zero, near, staged, sh, st.fin.look);
+        reset_ready(a, b);
       }
     }
   }
