@@ -235,6 +235,27 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
                        size_t ws_bytes, ssd_stream_t s);
 
 /*
+ * ssd_round for back-to-back rounds of independent batches: its statistics
+ * pass may start while the kernels of the previous call on the stream are
+ * still finishing (their verification tail is a chain of dependent steps at
+ * low occupancy), so consecutive rounds overlap.  Arguments, outputs and
+ * semantics are those of ssd_round.  The caller guarantees that nothing this
+ * call reads or writes -- logits, uniforms, payload, outputs, status and the
+ * workspace -- is written or read by the kernel launched just before it on
+ * the stream (e.g. the previous round runs on other buffers and the logits
+ * were produced earlier).  A round's own kernels still run in order.
+ */
+ssd_status_t ssd_round_pipelined(const void *target, const void *draft, ssd_dtype_t dt,
+                                 int64_t seq_stride, int64_t row_stride, int B, int K, int V,
+                                 const int32_t *F, float C, float T, const float *u_draft,
+                                 const float *u_acc, const float *u_bonus, const int32_t *payload,
+                                 int32_t *d_out, float *qd_out, int32_t *accept_len,
+                                 int32_t *out_tokens, int32_t *bonus, float *accept_prob,
+                                 float *resid_mass, int32_t *guess, float *guess_q, int32_t *slot,
+                                 int32_t *next_tokens, uint32_t *hits, uint32_t *near_ties,
+                                 uint32_t *status, void *ws, size_t ws_bytes, ssd_stream_t s);
+
+/*
  * Exact analytics of a round, before any uniform is drawn [B,
  * "投机解码的瓶颈与 SSD 的核心机制": the acceptance rate alpha; B, "Saguaro 算法"
  * part 1: the chance that the bonus token lands among the cached guesses is

@@ -32,7 +32,8 @@ EXPORTS = ("ssd_status_string", "ssd_fanout_split", "ssd_workspace_size", "ssd_s
            "ssd_verify", "ssd_verify_noalloc", "ssd_verify_noalloc_max_bytes",
            "ssd_predict_outcomes", "ssd_cache_lookup", "ssd_round", "ssd_round_analytics",
            "ssd_attention_workspace_size", "ssd_branch_attention", "ssd_ngram_backup",
-           "ssd_fallback_plan", "ssd_fill_sample", "ssd_kv_append", "ssd_tree_verify")
+           "ssd_fallback_plan", "ssd_fill_sample", "ssd_kv_append", "ssd_tree_verify",
+           "ssd_round_pipelined")
 
 _lib = None
 
@@ -101,6 +102,8 @@ def _declare(lib):
     lib.ssd_round.argtypes = ([_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp, _vp]
                               + [_vp] * 14 + [_vp, _sz, _vp])
     lib.ssd_round.restype = _i
+    lib.ssd_round_pipelined.argtypes = lib.ssd_round.argtypes
+    lib.ssd_round_pipelined.restype = _i
     lib.ssd_round_analytics.argtypes = ([_vp, _vp, _i, _i64, _i64, _i, _i, _i, _vp, _f, _f]
                                         + [_vp] * 7 + [_vp, _sz, _vp])
     lib.ssd_round_analytics.restype = _i
@@ -291,12 +294,16 @@ def ssd_cache_lookup(guess, payload, K, F, accept_len, bonus, slot, next_tokens=
 def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_len, out_tokens,
               bonus, payload=None, qd_out=None, accept_prob=None, resid_mass=None, guess=None,
               guess_q=None, slot=None, next_tokens=None, hits=None, status=None, ws=None,
-              stream=None, near_ties=None):
+              stream=None, near_ties=None, pipelined=False):
+    """One round (sample, verify, predict, lookup).  ``pipelined``: the call
+    may overlap the previous kernels on the stream (ssd_round_pipelined; no
+    buffer of this call may be in use by the previous call)."""
     dt, ss, rs = _logit_meta(target)
     if draft.dtype != target.dtype or draft.stride() != target.stride() or draft.shape != target.shape:
         raise ValueError("target and draft logits must share dtype, shape and strides")
     B, K1 = target.shape[0], target.shape[1]
-    _check("ssd_round", load().ssd_round(
+    fn = load().ssd_round_pipelined if pipelined else load().ssd_round
+    _check("ssd_round", fn(
         _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
         _ptr(u_draft), _ptr(u_acc), _ptr(u_bonus), _ptr(payload), _ptr(d_out), _ptr(qd_out),
         _ptr(accept_len), _ptr(out_tokens), _ptr(bonus), _ptr(accept_prob), _ptr(resid_mass),

@@ -150,6 +150,7 @@ struct VocabArgs {
   float *qd_out;
   int32_t *fill_payload;  // cache fill: the draw of sequence b also goes to fill_payload[b * fill_stride + fill_col]
   unsigned long long *ready;  // verification: [B][K+1][2] record / guess list published (kReady), else 0; NULL otherwise
+  int pipelined;              // host: k_stats may start while the previous kernel on the stream still runs
   int fill_stride, fill_col;
   int32_t *accept_len, *out_tokens, *bonus;
   float *accept_prob, *resid_mass;
@@ -1586,6 +1587,9 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
   }
   // verification waits for its own sequence's records (ready words); the
   // analytics for the whole pair grid
+  // a statistics pass of the next (pipelined) call may start as soon as every
+  // unit of this grid has started; nothing here waits for it
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const bool proto = a.ready != nullptr;
   if (!proto) asm volatile("griddepcontrol.wait;" ::: "memory");  // k_pair has completed
   int b = 0, u = 0;
@@ -2038,8 +2042,22 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   for (int b0 = 0; b0 < a.B; b0 += 65535) {
     a.b0 = b0;
     const unsigned nb = static_cast<unsigned>(a.B - b0 < 65535 ? a.B - b0 : 65535);
-    k_stats<E><<<dim3(nchunks, static_cast<unsigned>(a.nslots), nb), kStatWarps * 32, 0, s>>>(a);
-    e = cudaGetLastError();
+    const dim3 grid(nchunks, static_cast<unsigned>(a.nslots), nb);
+    if (a.pipelined && b0 == 0) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = grid;
+      cfg.blockDim = dim3(kStatWarps * 32);
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, k_stats<E>, a);
+    } else {
+      k_stats<E><<<grid, kStatWarps * 32, 0, s>>>(a);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
   }
   a.b0 = 0;
@@ -2294,13 +2312,16 @@ ssd_status_t ssd_cache_lookup(const int32_t *guess, const int32_t *payload, int 
   return cuda_status(cudaGetLastError());
 }
 
-ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
-                       int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
-                       const float *u_draft, const float *u_acc, const float *u_bonus, const int32_t *payload,
-                       int32_t *d_out, float *qd_out, int32_t *accept_len, int32_t *out_tokens, int32_t *bonus,
-                       float *accept_prob, float *resid_mass, int32_t *guess, float *guess_q, int32_t *slot,
-                       int32_t *next_tokens, uint32_t *hits, uint32_t *near_ties, uint32_t *status, void *ws,
-                       size_t ws_bytes, ssd_stream_t s) {
+}  // extern "C"
+
+namespace {
+ssd_status_t round_impl(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                        int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                        const float *u_draft, const float *u_acc, const float *u_bonus, const int32_t *payload,
+                        int32_t *d_out, float *qd_out, int32_t *accept_len, int32_t *out_tokens, int32_t *bonus,
+                        float *accept_prob, float *resid_mass, int32_t *guess, float *guess_q, int32_t *slot,
+                        int32_t *next_tokens, uint32_t *hits, uint32_t *near_ties, uint32_t *status, void *ws,
+                        size_t ws_bytes, ssd_stream_t s, bool pipelined) {
   Layout L;
   ssd_status_t st = layout_or_error(B, K, V, dt, F, &L);
   if (st != SSD_OK) return st;
@@ -2340,7 +2361,36 @@ ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, in
   a.next_tokens = next_tokens;
   a.hits = hits;
   a.near_ties = near_ties;
+  a.pipelined = pipelined ? 1 : 0;
   return cuda_status(launch_any(dt, a, cs));
+}
+}  // namespace
+
+extern "C" {
+
+ssd_status_t ssd_round(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                       int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                       const float *u_draft, const float *u_acc, const float *u_bonus, const int32_t *payload,
+                       int32_t *d_out, float *qd_out, int32_t *accept_len, int32_t *out_tokens, int32_t *bonus,
+                       float *accept_prob, float *resid_mass, int32_t *guess, float *guess_q, int32_t *slot,
+                       int32_t *next_tokens, uint32_t *hits, uint32_t *near_ties, uint32_t *status, void *ws,
+                       size_t ws_bytes, ssd_stream_t s) {
+  return round_impl(target, draft, dt, seq_stride, row_stride, B, K, V, F, C, T, u_draft, u_acc, u_bonus, payload,
+                    d_out, qd_out, accept_len, out_tokens, bonus, accept_prob, resid_mass, guess, guess_q, slot,
+                    next_tokens, hits, near_ties, status, ws, ws_bytes, s, false);
+}
+
+ssd_status_t ssd_round_pipelined(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,
+                                 int64_t row_stride, int B, int K, int V, const int32_t *F, float C, float T,
+                                 const float *u_draft, const float *u_acc, const float *u_bonus,
+                                 const int32_t *payload, int32_t *d_out, float *qd_out, int32_t *accept_len,
+                                 int32_t *out_tokens, int32_t *bonus, float *accept_prob, float *resid_mass,
+                                 int32_t *guess, float *guess_q, int32_t *slot, int32_t *next_tokens,
+                                 uint32_t *hits, uint32_t *near_ties, uint32_t *status, void *ws, size_t ws_bytes,
+                                 ssd_stream_t s) {
+  return round_impl(target, draft, dt, seq_stride, row_stride, B, K, V, F, C, T, u_draft, u_acc, u_bonus, payload,
+                    d_out, qd_out, accept_len, out_tokens, bonus, accept_prob, resid_mass, guess, guess_q, slot,
+                    next_tokens, hits, near_ties, status, ws, ws_bytes, s, true);
 }
 
 ssd_status_t ssd_round_analytics(const void *target, const void *draft, ssd_dtype_t dt, int64_t seq_stride,

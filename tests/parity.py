@@ -76,15 +76,12 @@ def to_dev(arr, dev="cuda"):
     return ssd.tensor(arr, dev)
 
 
-def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True, ws=None):
-    """Run one round on the GPU (fused ssd_round, or the four separate calls);
-    ``ws``: a workspace to use instead of a fresh one."""
+def prepare_round(inp: w.RoundInputs, dev="cuda", ws=None):
+    """Device inputs, output buffers (filled with sentinels) and a workspace for
+    one round (the fills and copies are enqueued here)."""
     spec = inp.spec
-    T = spec.T if T is None else T
-    C = spec.C if C is None else C
     B, K, V = spec.B, spec.K, spec.V
     sumF = int(sum(spec.F))
-    tgt, dft = to_dev(inp.target, dev), to_dev(inp.draft, dev)
     i32 = dict(dtype=torch.int32, device=dev)
     f32 = dict(dtype=torch.float32, device=dev)
     o = dict(d=torch.full((B, K), -7, **i32), qd=torch.zeros(B, K, **f32),
@@ -96,14 +93,27 @@ def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True, ws=Non
              near_ties=torch.zeros(1, **i32), status=torch.zeros(1, **i32))
     if ws is None:
         ws = ssd.workspace(B, K, V, spec.dtype, spec.F, dev)
-    ud, ua, ub = to_dev(inp.u_draft, dev), to_dev(inp.u_acc, dev), to_dev(inp.u_bonus, dev)
     pl = to_dev(inp.payload, dev) if inp.payload is not None else None
+    o["_in"] = (to_dev(inp.target, dev), to_dev(inp.draft, dev), to_dev(inp.u_draft, dev),
+                to_dev(inp.u_acc, dev), to_dev(inp.u_bonus, dev), pl, ws)
+    return o
+
+
+def enqueue_round(inp: w.RoundInputs, o, T=None, C=None, fused=True, pipelined=False):
+    """Enqueue a prepared round (fused ssd_round -- or ssd_round_pipelined -- or
+    the four separate calls) without waiting."""
+    spec = inp.spec
+    T = spec.T if T is None else T
+    C = spec.C if C is None else C
+    K, V = spec.K, spec.V
+    tgt, dft, ud, ua, ub, pl, ws = o["_in"]
     if fused:
         ssd.ssd_round(tgt, dft, V, spec.F, C, T, ud, ua, ub, o["d"], o["accept_len"],
                       o["out_tokens"], o["bonus"], payload=pl, qd_out=o["qd"],
                       accept_prob=o["accept_prob"], resid_mass=o["resid_mass"], guess=o["guess"],
                       guess_q=o["guess_q"], slot=o["slot"], next_tokens=o["next_tokens"],
-                      hits=o["hits"], status=o["status"], ws=ws, near_ties=o["near_ties"])
+                      hits=o["hits"], status=o["status"], ws=ws, near_ties=o["near_ties"],
+                      pipelined=pipelined)
     else:
         ssd.ssd_saguaro_sample(dft, V, spec.F, C, T, ud, o["d"], o["qd"], status=o["status"], ws=ws)
         ssd.ssd_verify(tgt, dft, V, spec.F, C, T, o["d"], ua, ub, o["accept_len"], o["out_tokens"],
@@ -113,10 +123,23 @@ def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True, ws=Non
                                  ws=ws)
         ssd.ssd_cache_lookup(o["guess"], pl, K, spec.F, o["accept_len"], o["bonus"], o["slot"],
                              o["next_tokens"], o["hits"], status=o["status"])
-    torch.cuda.synchronize()
-    res = {k: v.cpu().numpy() for k, v in o.items()}
-    res["near_tie_scope"] = "round" if fused else "verify"  # which decisions near_ties counts
+    o["_fused"] = fused
+    return o
+
+
+def collect_round(o):
+    """The outputs of a launched round as numpy arrays (after a synchronize)."""
+    res = {k: v.cpu().numpy() for k, v in o.items() if not k.startswith("_")}
+    res["near_tie_scope"] = "round" if o["_fused"] else "verify"  # which decisions near_ties counts
     return res
+
+
+def gpu_round(inp: w.RoundInputs, T=None, C=None, dev="cuda", fused=True, ws=None):
+    """Run one round on the GPU (fused ssd_round, or the four separate calls);
+    ``ws``: a workspace to use instead of a fresh one."""
+    o = enqueue_round(inp, prepare_round(inp, dev, ws), T, C, fused)
+    torch.cuda.synchronize()
+    return collect_round(o)
 
 
 def _rel_ok(a, b, rtol=PROB_RTOL, floor=1e-30):

@@ -261,3 +261,27 @@ def test_one_workspace_across_calls_of_every_kind():
             torch.cuda.synchronize()
             assert int(st.item()) == 0
     assert rep.compared == 6 + 3 + 6 + 6 + 6 + 3 + 6 + 6
+
+
+def test_pipelined_rounds_back_to_back():
+    """Rounds of independent batches with ssd_round_pipelined, launched back to
+    back without a synchronize so that each statistics pass overlaps the
+    previous round's tail: every round equals the oracle (and so ssd_round)."""
+    from parity import collect_round, enqueue_round, prepare_round
+    spec = w.llama3_round(T=1.0)
+    inps = [w.make_round(spec, seed=40 + i) for i in range(4)]
+    small = w.RoundSpec(B=5, K=3, V=7000, dtype="bf16", recipe="zipf", T=0.7, C=0.5,
+                        F=(3, 2, 1, 1), draft_noise=1.0, name="pipelined-small")
+    inps += [w.make_round(small, seed=50 + i) for i in range(3)]
+    # every buffer is ready before the first round: a pipelined round may start
+    # before the kernel enqueued just before it has finished
+    prepared = [prepare_round(inp) for inp in inps]
+    torch.cuda.synchronize()
+    launched = [enqueue_round(inp, o, pipelined=True) for inp, o in zip(inps, prepared)]
+    torch.cuda.synchronize()
+    rep = Report()
+    for inp, o in zip(inps, launched):
+        g = collect_round(o)
+        assert g["status"][0] == 0
+        compare_round(inp, g, report=rep)
+    assert rep.compared == 4 * 32 + 3 * 5
