@@ -957,6 +957,29 @@ def probe(which):
         torch.cuda.synchronize()
         print(json.dumps({"probe": which, "workload": spec.name, "status": int(out["status"].item())}))
         return
+    if which == "fill":
+        spec = w.llama3_fill()
+        B, K, S, V = spec.B, spec.K, spec.S, spec.V
+        logits = ssd.tensor(w.fill_step_logits(spec, 3, 1))
+        u = torch.from_numpy(w.fill_uniforms(3, 0, 1, B, S)).to(device)
+        kn, vn = (ssd.tensor(x) for x in w.fill_step_kv(spec, 3, 1))
+        N = K + K * S
+        maxb = (spec.L + N + 15) // 16
+        table = torch.arange(B * maxb, dtype=torch.int32, device=device).view(B, maxb)
+        kc = torch.zeros(B * maxb, spec.Hkv, 16, spec.d, dtype=torch.bfloat16, device=device)
+        vc = torch.zeros_like(kc)
+        prefix = torch.full((B,), spec.L, dtype=torch.int32, device=device)
+        tok = torch.empty(B, S, dtype=torch.int32, device=device)
+        payload = torch.empty(B, S, K, dtype=torch.int32, device=device)
+        st = torch.zeros(1, dtype=torch.int32, device=device)
+        ws = ssd.fill_workspace(B, S, V, spec.dtype, spec.F[1], device)
+        for _ in range(3):
+            ssd.ssd_kv_append(kn, vn, kc, vc, table, prefix, K + S, status=st)
+            ssd.ssd_fill_sample(logits, V, spec.F[1], spec.C, spec.T, u, tok, t=1, payload=payload,
+                                status=st, ws=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"probe": which, "workload": spec.name, "status": int(st.item())}))
+        return
     if which == "tree":
         spec = w.llama3_tree()
         tgt, dft = w.tree_logits(spec, 5)
@@ -1011,7 +1034,7 @@ def main(argv=None):
                     help="reference arm: sequences per host core per step (capped at one batch)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e / attention / other rounds")
-    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify", "fallback", "tree"),
+    ap.add_argument("--probe", choices=("round", "attn-draft", "attn-verify", "fallback", "tree", "fill"),
                     help="only run a few calls of one workload (for profilers) and exit")
     args = ap.parse_args(argv)
     if args.probe:
