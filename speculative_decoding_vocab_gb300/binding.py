@@ -131,9 +131,17 @@ def _declare(lib):
 # ---------------------------------------------------------------------------
 # marshalling helpers
 # ---------------------------------------------------------------------------
-def _ptr(t):
+def _ptr(t, dtype=None, strided=False):
+    """Device address of ``t``.  The library reads every array as dense
+    row-major memory of the C type its header names, so a tensor with other
+    strides (unless the call passes them: ``strided``) or of another dtype is
+    refused here rather than read wrongly."""
     if t is None:
         return None
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"expected a {dtype} tensor, got {t.dtype}")
+    if not strided and t.numel() > 1 and not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
     if not t.is_cuda:
         raise ValueError("tensors passed to the library must live on a CUDA device")
     return ctypes.c_void_p(t.data_ptr())
@@ -239,8 +247,8 @@ def ssd_saguaro_sample(draft, V, F, C, T, u_draft, d_out, qd_out=None, status=No
     dt, ss, rs = _logit_meta(draft)
     B, K1 = draft.shape[0], draft.shape[1]
     _check("ssd_saguaro_sample", load().ssd_saguaro_sample(
-        _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T), _ptr(u_draft),
-        _ptr(d_out), _ptr(qd_out), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
+        _ptr(draft, strided=True), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T), _ptr(u_draft, torch.float32),
+        _ptr(d_out, torch.int32), _ptr(qd_out, torch.float32), _ptr(status, torch.int32), _ptr(ws, torch.uint8), 0 if ws is None else ws.numel(),
         _stream(stream)))
 
 
@@ -251,9 +259,9 @@ def ssd_verify(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len, out_tok
         raise ValueError("target and draft logits must share dtype, shape and strides")
     B, K1 = target.shape[0], target.shape[1]
     _check("ssd_verify", load().ssd_verify(
-        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
-        _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
-        _ptr(accept_prob), _ptr(resid_mass), _ptr(near_ties), _ptr(status), _ptr(ws),
+        _ptr(target, strided=True), _ptr(draft, strided=True), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(d, torch.int32), _ptr(u_acc, torch.float32), _ptr(u_bonus, torch.float32), _ptr(accept_len, torch.int32), _ptr(out_tokens, torch.int32), _ptr(bonus, torch.int32),
+        _ptr(accept_prob, torch.float32), _ptr(resid_mass, torch.float32), _ptr(near_ties, torch.int32), _ptr(status, torch.int32), _ptr(ws, torch.uint8),
         0 if ws is None else ws.numel(), _stream(stream)))
 
 
@@ -266,9 +274,9 @@ def ssd_verify_noalloc(target, draft, V, F, C, T, d, u_acc, u_bonus, accept_len,
         raise ValueError("target and draft logits must share dtype, shape and strides")
     B, K1 = target.shape[0], target.shape[1]
     _check("ssd_verify_noalloc", load().ssd_verify_noalloc(
-        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
-        _ptr(d), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(out_tokens), _ptr(bonus),
-        _ptr(accept_prob), _ptr(resid_mass), _ptr(near_ties), _ptr(status), _stream(stream)))
+        _ptr(target, strided=True), _ptr(draft, strided=True), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(d, torch.int32), _ptr(u_acc, torch.float32), _ptr(u_bonus, torch.float32), _ptr(accept_len, torch.int32), _ptr(out_tokens, torch.int32), _ptr(bonus, torch.int32),
+        _ptr(accept_prob, torch.float32), _ptr(resid_mass, torch.float32), _ptr(near_ties, torch.int32), _ptr(status, torch.int32), _stream(stream)))
 
 
 def ssd_verify_noalloc_max_bytes() -> int:
@@ -279,16 +287,16 @@ def ssd_predict_outcomes(draft, V, F, T, guess, guess_q=None, status=None, ws=No
     dt, ss, rs = _logit_meta(draft)
     B, K1 = draft.shape[0], draft.shape[1]
     _check("ssd_predict_outcomes", load().ssd_predict_outcomes(
-        _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(T), _ptr(guess),
-        _ptr(guess_q), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(draft, strided=True), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(T), _ptr(guess, torch.int32),
+        _ptr(guess_q, torch.float32), _ptr(status, torch.int32), _ptr(ws, torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def ssd_cache_lookup(guess, payload, K, F, accept_len, bonus, slot, next_tokens=None, hits=None,
                      status=None, stream=None):
     B = guess.shape[0]
     _check("ssd_cache_lookup", load().ssd_cache_lookup(
-        _ptr(guess), _ptr(payload), B, int(K), _host_F(F), _ptr(accept_len), _ptr(bonus),
-        _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(status), _stream(stream)))
+        _ptr(guess, torch.int32), _ptr(payload, torch.int32), B, int(K), _host_F(F), _ptr(accept_len, torch.int32), _ptr(bonus, torch.int32),
+        _ptr(slot, torch.int32), _ptr(next_tokens, torch.int32), _ptr(hits, torch.int32), _ptr(status, torch.int32), _stream(stream)))
 
 
 def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_len, out_tokens,
@@ -304,11 +312,11 @@ def ssd_round(target, draft, V, F, C, T, u_draft, u_acc, u_bonus, d_out, accept_
     B, K1 = target.shape[0], target.shape[1]
     fn = load().ssd_round_pipelined if pipelined else load().ssd_round
     _check("ssd_round", fn(
-        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
-        _ptr(u_draft), _ptr(u_acc), _ptr(u_bonus), _ptr(payload), _ptr(d_out), _ptr(qd_out),
-        _ptr(accept_len), _ptr(out_tokens), _ptr(bonus), _ptr(accept_prob), _ptr(resid_mass),
-        _ptr(guess), _ptr(guess_q), _ptr(slot), _ptr(next_tokens), _ptr(hits), _ptr(near_ties),
-        _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(target, strided=True), _ptr(draft, strided=True), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(u_draft, torch.float32), _ptr(u_acc, torch.float32), _ptr(u_bonus, torch.float32), _ptr(payload, torch.int32), _ptr(d_out, torch.int32), _ptr(qd_out, torch.float32),
+        _ptr(accept_len, torch.int32), _ptr(out_tokens, torch.int32), _ptr(bonus, torch.int32), _ptr(accept_prob, torch.float32), _ptr(resid_mass, torch.float32),
+        _ptr(guess, torch.int32), _ptr(guess_q, torch.float32), _ptr(slot, torch.int32), _ptr(next_tokens, torch.int32), _ptr(hits, torch.int32), _ptr(near_ties, torch.int32),
+        _ptr(status, torch.int32), _ptr(ws, torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def ssd_round_analytics(target, draft, V, F, C, T, p_accept, hit_rate, exp_tokens, alpha=None,
@@ -318,9 +326,9 @@ def ssd_round_analytics(target, draft, V, F, C, T, p_accept, hit_rate, exp_token
         raise ValueError("target and draft logits must share dtype, shape and strides")
     B, K1 = target.shape[0], target.shape[1]
     _check("ssd_round_analytics", load().ssd_round_analytics(
-        _ptr(target), _ptr(draft), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
-        _ptr(alpha), _ptr(resid_w), _ptr(p_accept), _ptr(hit_mass), _ptr(hit_rate),
-        _ptr(exp_tokens), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
+        _ptr(target, strided=True), _ptr(draft, strided=True), dt, ss, rs, B, K1 - 1, int(V), _host_F(F), float(C), float(T),
+        _ptr(alpha, torch.float32), _ptr(resid_w, torch.float32), _ptr(p_accept, torch.float32), _ptr(hit_mass, torch.float32), _ptr(hit_rate, torch.float32),
+        _ptr(exp_tokens, torch.float32), _ptr(status, torch.int32), _ptr(ws, torch.uint8), 0 if ws is None else ws.numel(),
         _stream(stream)))
 
 
@@ -344,9 +352,9 @@ def ssd_branch_attention(q, k_cache, v_cache, block_table, prefix_len, parent, o
     if scale is None:
         scale = d ** -0.5
     _check("ssd_branch_attention", load().ssd_branch_attention(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], nb,
-        _ptr(prefix_len), _ptr(parent), B, N, Nq, Hq, Hkv, d, float(scale), _ptr(out), _ptr(lse),
-        _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(q, torch.bfloat16), _ptr(k_cache, torch.bfloat16), _ptr(v_cache, torch.bfloat16), _ptr(block_table, torch.int32), block_table.shape[1], nb,
+        _ptr(prefix_len, torch.int32), _ptr(parent, torch.int32), B, N, Nq, Hq, Hkv, d, float(scale), _ptr(out, torch.bfloat16), _ptr(lse, torch.float32),
+        _ptr(status, torch.int32), _ptr(ws, torch.uint8), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def ssd_ngram_backup(hist, hist_len, n, K, V, u_rand, next_tokens, slot=None, match_pos=None,
@@ -361,8 +369,8 @@ def ssd_ngram_backup(hist, hist_len, n, K, V, u_rand, next_tokens, slot=None, ma
             raise ValueError("hist must be a contiguous int32 [B, cap] tensor")
         stride = hist.shape[1]
     _check("ssd_ngram_backup", load().ssd_ngram_backup(
-        _ptr(hist), stride, _ptr(hist_len), B, int(n), int(K), int(V), _ptr(slot), _ptr(u_rand),
-        _ptr(plan_best), int(random_option), _ptr(next_tokens), _ptr(match_pos), _ptr(status),
+        _ptr(hist, torch.int32), stride, _ptr(hist_len, torch.int32), B, int(n), int(K), int(V), _ptr(slot, torch.int32), _ptr(u_rand, torch.float32),
+        _ptr(plan_best, torch.int32), int(random_option), _ptr(next_tokens, torch.int32), _ptr(match_pos, torch.int32), _ptr(status, torch.int32),
         _stream(stream)))
 
 
@@ -377,8 +385,8 @@ def ssd_fallback_plan(p_hit, e_hit, T_v, T_p, T_b, e_miss, time=None, tokens=Non
     tb = (ctypes.c_double * max(nopt, 1))(*[float(x) for x in T_b])
     em = (ctypes.c_double * max(nopt, 1))(*[float(x) for x in e_miss])
     _check("ssd_fallback_plan", load().ssd_fallback_plan(
-        _ptr(p_hit), _ptr(e_hit), p_hit.shape[0], float(T_v), float(T_p), nopt, tb, em, _ptr(time),
-        _ptr(tokens), _ptr(throughput), _ptr(speedup), _ptr(best), _ptr(status), _stream(stream)))
+        _ptr(p_hit, torch.float32), _ptr(e_hit, torch.float32), p_hit.shape[0], float(T_v), float(T_p), nopt, tb, em, _ptr(time, torch.float64),
+        _ptr(tokens, torch.float64), _ptr(throughput, torch.float64), _ptr(speedup, torch.float64), _ptr(best, torch.int32), _ptr(status, torch.int32), _stream(stream)))
 
 
 def fill_workspace(B, S, V, dtype, F_t, device="cuda") -> torch.Tensor:
@@ -403,8 +411,8 @@ def ssd_fill_sample(logits, V, F_t, C, T, u, tokens, t=0, payload=None, q_out=No
         Kp = payload.shape[2]
     stride = logits.stride(1) if logits.numel() else logits.shape[2]
     _check("ssd_fill_sample", load().ssd_fill_sample(
-        _ptr(logits), dt, stride, B, S, int(V), int(F_t), float(C), float(T), _ptr(u), int(t), Kp,
-        _ptr(tokens), _ptr(q_out), _ptr(payload), _ptr(status), _ptr(ws),
+        _ptr(logits, strided=True), dt, stride, B, S, int(V), int(F_t), float(C), float(T), _ptr(u, torch.float32), int(t), Kp,
+        _ptr(tokens, torch.int32), _ptr(q_out, torch.float32), _ptr(payload, torch.int32), _ptr(status, torch.int32), _ptr(ws, torch.uint8),
         0 if ws is None else ws.numel(), _stream(stream)))
 
 
@@ -417,9 +425,9 @@ def ssd_kv_append(k_new, v_new, k_cache, v_cache, block_table, prefix_len, node0
             raise ValueError("k_new, v_new and the caches must be contiguous bfloat16")
     B, S, Hkv, d = k_new.shape
     _check("ssd_kv_append", load().ssd_kv_append(
-        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-        block_table.shape[1], k_cache.shape[0], _ptr(prefix_len), int(node0), B, S, Hkv, d,
-        _ptr(status), _stream(stream)))
+        _ptr(k_new, torch.bfloat16), _ptr(v_new, torch.bfloat16), _ptr(k_cache, torch.bfloat16), _ptr(v_cache, torch.bfloat16), _ptr(block_table, torch.int32),
+        block_table.shape[1], k_cache.shape[0], _ptr(prefix_len, torch.int32), int(node0), B, S, Hkv, d,
+        _ptr(status, torch.int32), _stream(stream)))
 
 
 def ssd_tree_verify(target, draft, V, T, parent, tokens, u_acc, u_bonus, accept_len, path, bonus,
@@ -431,6 +439,6 @@ def ssd_tree_verify(target, draft, V, T, parent, tokens, u_acc, u_bonus, accept_
         raise ValueError("target and draft logits must share dtype, shape and strides")
     B, N1 = target.shape[0], target.shape[1]
     _check("ssd_tree_verify", load().ssd_tree_verify(
-        _ptr(target), _ptr(draft), dt, ss, rs, B, N1 - 1, int(V), float(T), _ptr(parent),
-        _ptr(tokens), _ptr(u_acc), _ptr(u_bonus), _ptr(accept_len), _ptr(path), _ptr(bonus),
-        _ptr(out_tokens), _ptr(resid_mass), _ptr(status), _stream(stream)))
+        _ptr(target, strided=True), _ptr(draft, strided=True), dt, ss, rs, B, N1 - 1, int(V), float(T), _ptr(parent, torch.int32),
+        _ptr(tokens, torch.int32), _ptr(u_acc, torch.float32), _ptr(u_bonus, torch.float32), _ptr(accept_len, torch.int32), _ptr(path, torch.int32), _ptr(bonus, torch.int32),
+        _ptr(out_tokens, torch.int32), _ptr(resid_mass, torch.float32), _ptr(status, torch.int32), _stream(stream)))

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import oracle
@@ -147,8 +148,26 @@ def test_validation_returns_before_any_launch(lib):
 
 def test_binding_refuses_host_tensors(lib):
     import torch
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="CUDA device"):
         ssd._ptr(torch.zeros(4))
+
+
+def test_binding_refuses_other_layouts_and_dtypes():
+    """The library reads arrays as dense row-major memory of the header's C
+    type: a column-major gather (numpy's a[:, idx]) or a float64 uniform
+    array is refused before any pointer is taken."""
+    import torch
+    a = np.arange(12, dtype=np.int32).reshape(3, 4)[:, np.array([0, 2, 1])]
+    assert not a.flags["C_CONTIGUOUS"]
+    with pytest.raises(ValueError, match="contiguous"):
+        ssd._ptr(torch.from_numpy(a), torch.int32)
+    with pytest.raises(ValueError, match="float32"):
+        ssd._ptr(torch.zeros(4, dtype=torch.float64), torch.float32)
+    # strided logits pass the layout check (their strides go to the call)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ssd._ptr(torch.zeros(4, 8)[:, :5], strided=True)
+    # the numpy helper makes any layout dense
+    assert ssd.tensor(a, "cpu").is_contiguous()
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -96,6 +96,26 @@ def test_tree_tiny(T):
     assert (r["accept_len"] > 0).any() and (r["accept_len"] == 0).any()
 
 
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_tree_children_at_target_argmax(T):
+    """Even children carry the target's argmax at their parent, odd ones the
+    token after it: at T = 0 every even child is accepted whatever the draft
+    prefers, so each walk reaches the deepest level."""
+    spec = w.TreeSpec(B=6, V=3000, dtype="f32", T=T, branching=(2, 2), recipe="gauss",
+                      draft_noise=0.8, name="argmax-children")
+    tgt, dft = w.tree_logits(spec, 21)
+    parent1 = w.tree_shape(spec.branching)
+    N = len(parent1)
+    am = tgt.argmax(axis=2)[:, parent1 + 1]
+    tok = np.ascontiguousarray(np.where(np.arange(N)[None, :] % 2 == 0, am, (am + 1) % spec.V),
+                               dtype=np.int32)
+    par = np.broadcast_to(parent1, (spec.B, N)).copy()
+    ua, ub = w.tree_uniforms(21, 0, spec.B, N)
+    g, r, _ = compare(spec, tgt, dft, par, tok, ua, ub)
+    if T == 0.0:
+        assert (r["accept_len"] == 2).all()
+
+
 def test_tree_llama3_full_batch():
     """The 28-node tree over the Llama-3 vocabulary (4 CTAs per sequence), all
     32 sequences."""
