@@ -799,11 +799,36 @@ def bench_other_rounds(ssd, w, device, hbm_peak):
             call(i)
         graphs = capture_graphs([lambda i=i: call(i) for i in range(nsets)], device)
         ms = _time_calls(lambda i: graphs[i % nsets].replay(), 50, stream)
+        hit_rate = int(out["hits"].item()) / spec.B
+        del graphs
+        # the same rounds pipelined (ssd_round_pipelined): consecutive rounds on
+        # different input sets, outputs and workspaces
+        psets = sets if nsets >= 2 else sets + [(sets[0][0].clone(), sets[0][1].clone())]
+        npset = len(psets)
+        pouts = [make_outputs(spec, device) for _ in range(npset)]
+        pws = [ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device) for _ in range(npset)]
+
+        def pchain():
+            for i in range(2 * npset):
+                t, d = psets[i % npset]
+                o = pouts[i % npset]
+                ssd.ssd_round(t, d, spec.V, spec.F, spec.C, spec.T, ud, ua, ub, o["d"], o["accept_len"],
+                              o["out_tokens"], o["bonus"], guess=o["guess"], slot=o["slot"],
+                              hits=o["hits"], status=o["status"], ws=pws[i % npset], pipelined=True)
+
+        pchain()
+        gp = capture_graphs([pchain], device)[0]
+        gp.replay()
+        pms = _time_calls(lambda i: gp.replay(), max(5, 50 // (2 * npset)), stream) / (2 * npset)
         res[spec.name] = {"ms": round(ms, 4), "seq_rounds_per_s": round(spec.B / (ms * 1e-3), 1),
                           "algorithmic_bytes": per, "C": spec.C, "T": spec.T,
                           "frac_of_hbm_peak": round(per / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-                          "hit_rate": round(int(out["hits"].item()) / spec.B, 4)}
-        del graphs, sets, out, ws
+                          "hit_rate": round(hit_rate, 4),
+                          "pipelined_ms": round(pms, 4),
+                          "pipelined_seq_rounds_per_s": round(spec.B / (pms * 1e-3), 1),
+                          "pipelined_frac_of_hbm_peak": round(per / (pms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "status_flags": int(out["status"].item()) + sum(int(o["status"].item()) for o in pouts)}
+        del gp, sets, psets, out, ws, pouts, pws
         torch.cuda.empty_cache()
     return res
 

@@ -34,6 +34,12 @@
 //            sequence that needs no residual is finished by its first unit.
 //            The analytics call runs the units over every pair for the sums of
 //            min(p, q') and max(0, p - q').
+// In a verification call k_pair publishes each pair's record (and its guess
+// list) through ready words in the workspace -- with C = 1 or T = 0 before the
+// top-F selection, which the record then does not depend on -- and k_resid
+// units wait only for their own sequence's records instead of the whole pair
+// grid.  ssd_round_pipelined launches k_stats as a dependent of the previous
+// call's k_resid, so the next batch's HBM pass overlaps this verification tail.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
