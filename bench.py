@@ -204,6 +204,33 @@ def capture_graphs(calls, device):
     return graphs
 
 
+NSTREAMS = 4          # streams that independent rounds are issued on, round-robin
+NBUF = 2 * NSTREAMS   # output/workspace sets: rounds in flight together never share one
+
+
+def stream_chain(launch, device, nstreams=NSTREAMS):
+    """chain(first, n) enqueues rounds first .. first+n-1, round q by launch(q)
+    on stream q % nstreams, forked from and joined back into the current
+    stream (so a CUDA graph captures it whole).  Rounds on one stream follow
+    each other (pipelined: a round's statistics pass overlaps the previous
+    round's tail); rounds on different streams are independent batches and
+    overlap freely."""
+    import torch
+    streams = [torch.cuda.Stream(device) for _ in range(nstreams)]
+
+    def chain(first, n):
+        cur = torch.cuda.current_stream(device)
+        for st in streams:
+            st.wait_stream(cur)
+        for q in range(first, first + n):
+            with torch.cuda.stream(streams[q % nstreams]):
+                launch(q)
+        for st in streams:
+            cur.wait_stream(st)
+
+    return chain
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -225,7 +252,7 @@ def bench_ours(args):
     inp = w.make_round(spec, seed=rank_seed(0, rank))
     # rotating input sets whose total exceeds L2 several times over
     per_set = w.round_bytes(spec)
-    nsets = max(2, int(np.ceil(3 * L2_BYTES / per_set)) + 1)
+    nsets = max(NBUF, int(np.ceil(3 * L2_BYTES / per_set)) + 1)
     sets = [RoundBuffers(spec, inp, device) for _ in range(nsets)]
     out = make_outputs(spec, device)
     ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
@@ -239,37 +266,33 @@ def bench_ours(args):
     for i in range(W):
         graphs[i % nsets].replay()
     torch.cuda.synchronize()
-    # the timed steps: rounds of independent batches (the input sets, each with
-    # its own outputs and workspace) issued back to back with
-    # ssd_round_pipelined, so a round's statistics pass overlaps the previous
-    # round's verification tail; CUDA graphs of 2 * nsets rounds, and single
-    # rounds for a remainder
-    outs = [make_outputs(spec, device) for _ in range(nsets)]
-    wss = [ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device) for _ in range(nsets)]
-    chain_n = 2 * nsets
-
-    def chain(first, n):
-        for q in range(first, first + n):
-            run_round(ssd, spec, sets[q % nsets], outs[q % nsets], wss[q % nsets], pipelined=True)
-
-    for i in range(W):
-        chain(i, 1)
+    # the timed steps: rounds of independent batches (step q reads input set
+    # q % nsets and writes output/workspace set q % NBUF) issued round-robin on
+    # NSTREAMS streams with ssd_round_pipelined: on a stream, a round's
+    # statistics pass overlaps the previous round's verification tail, and the
+    # streams' rounds overlap each other; CUDA graphs of chain_n steps, and one
+    # graph of the remainder
+    outs = [make_outputs(spec, device) for _ in range(NBUF)]
+    wss = [ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device) for _ in range(NBUF)]
+    chain_n = int(np.lcm(nsets, NBUF))
+    chain_n *= max(1, 48 // chain_n)
+    chain = stream_chain(lambda q: run_round(ssd, spec, sets[q % nsets], outs[q % NBUF], wss[q % NBUF],
+                                             pipelined=True), device)
+    chain(0, max(W, NBUF))
     torch.cuda.synchronize()
     g_chain = capture_graphs([lambda: chain(0, chain_n)], device)[0]
-    g_single = capture_graphs([lambda q=q: chain(q, 1) for q in range(nsets)], device)
+    rem = K % chain_n
+    g_rem = capture_graphs([lambda: chain(0, rem)], device)[0] if rem else None
     for _ in range(max(1, W // chain_n + 1)):
         g_chain.replay()
     torch.cuda.synchronize()
 
     def timed_steps(n):
-        """n steps: whole chains, then single rounds for the remainder."""
-        done = 0
-        while n - done >= chain_n:
+        """n steps: whole chains, then the remainder's graph."""
+        for _ in range(n // chain_n):
             g_chain.replay()
-            done += chain_n
-        while done < n:
-            g_single[done % nsets].replay()
-            done += 1
+        if n % chain_n:
+            g_rem.replay()
 
     # the statistics kernel timed on its own stream with CUDA events (direct launches)
     nev = min(K, 256)
@@ -346,9 +369,10 @@ def bench_ours(args):
                 "N(0,0.3^2)), draft = target + N(0,1); Philox4x32-10 uniforms",
         "config": {"workload": spec.name, "B": spec.B, "K": spec.K, "V": spec.V,
                    "input_dtype": "bf16", "T": spec.T, "C": spec.C, "F": list(spec.F),
-                   "call": "ssd_round_pipelined (sample + verify + predict + lookup); consecutive steps are "
-                           "independent batches (rotating input sets, own outputs and workspaces), so a "
-                           "step's statistics pass overlaps the previous step's verification tail; CUDA "
+                   "call": "ssd_round_pipelined (sample + verify + predict + lookup); steps are "
+                           "independent batches (rotating input sets, own outputs and workspaces) issued "
+                           f"round-robin on {NSTREAMS} streams: on a stream a step's statistics pass overlaps "
+                           "the previous step's verification tail, and the streams' steps overlap; CUDA "
                            f"graphs of {chain_n} steps",
                    "l2": f"rotating {nsets} input sets, {nsets * per_set / 1e6:.0f} MB > 129 MB L2",
                    "parallelism": f"replicas x{world} (independent sequences per GPU)"},
@@ -801,32 +825,37 @@ def bench_other_rounds(ssd, w, device, hbm_peak):
         ms = _time_calls(lambda i: graphs[i % nsets].replay(), 50, stream)
         hit_rate = int(out["hits"].item()) / spec.B
         del graphs
-        # the same rounds pipelined (ssd_round_pipelined): consecutive rounds on
-        # different input sets, outputs and workspaces
-        psets = sets if nsets >= 2 else sets + [(sets[0][0].clone(), sets[0][1].clone())]
+        # the same rounds as independent batches on NSTREAMS streams, pipelined
+        # on each (as the headline steps): every round in flight reads its own
+        # input copy and writes its own outputs and workspace
+        psets = [sets[i % nsets] if i < nsets else (sets[0][0].clone(), sets[0][1].clone())
+                 for i in range(max(nsets, NBUF))]
         npset = len(psets)
-        pouts = [make_outputs(spec, device) for _ in range(npset)]
-        pws = [ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device) for _ in range(npset)]
+        pouts = [make_outputs(spec, device) for _ in range(NBUF)]
+        pws = [ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device) for _ in range(NBUF)]
 
-        def pchain():
-            for i in range(2 * npset):
-                t, d = psets[i % npset]
-                o = pouts[i % npset]
-                ssd.ssd_round(t, d, spec.V, spec.F, spec.C, spec.T, ud, ua, ub, o["d"], o["accept_len"],
-                              o["out_tokens"], o["bonus"], guess=o["guess"], slot=o["slot"],
-                              hits=o["hits"], status=o["status"], ws=pws[i % npset], pipelined=True)
+        def plaunch(i):
+            t, d = psets[i % npset]
+            o = pouts[i % NBUF]
+            ssd.ssd_round(t, d, spec.V, spec.F, spec.C, spec.T, ud, ua, ub, o["d"], o["accept_len"],
+                          o["out_tokens"], o["bonus"], guess=o["guess"], slot=o["slot"],
+                          hits=o["hits"], status=o["status"], ws=pws[i % NBUF], pipelined=True)
 
-        pchain()
-        gp = capture_graphs([pchain], device)[0]
+        pchain = stream_chain(plaunch, device)
+        pn = int(np.lcm(npset, NBUF))
+        pn *= max(1, 32 // pn)
+        pchain(0, pn)
+        gp = capture_graphs([lambda: pchain(0, pn)], device)[0]
         gp.replay()
-        pms = _time_calls(lambda i: gp.replay(), max(5, 50 // (2 * npset)), stream) / (2 * npset)
+        pms = _time_calls(lambda i: gp.replay(), max(3, 64 // pn), stream) / pn
         res[spec.name] = {"ms": round(ms, 4), "seq_rounds_per_s": round(spec.B / (ms * 1e-3), 1),
                           "algorithmic_bytes": per, "C": spec.C, "T": spec.T,
                           "frac_of_hbm_peak": round(per / (ms * 1e-3) / 1e9 / hbm_peak, 4),
                           "hit_rate": round(hit_rate, 4),
-                          "pipelined_ms": round(pms, 4),
-                          "pipelined_seq_rounds_per_s": round(spec.B / (pms * 1e-3), 1),
-                          "pipelined_frac_of_hbm_peak": round(per / (pms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "streams_ms": round(pms, 4),
+                          "streams_seq_rounds_per_s": round(spec.B / (pms * 1e-3), 1),
+                          "streams_frac_of_hbm_peak": round(per / (pms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "streams_note": f"independent rounds on {NSTREAMS} streams, pipelined on each",
                           "status_flags": int(out["status"].item()) + sum(int(o["status"].item()) for o in pouts)}
         del gp, sets, psets, out, ws, pouts, pws
         torch.cuda.empty_cache()
