@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
                      const __grid_constant__ AttnArgs a) {
   using CF = AttnCfg<D, MT, PL, RA, NPB>;
   constexpr int NS = CF::kStages;
+  constexpr bool kEarlyExp = PL == 1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t *const smem_all =
@@ -594,65 +595,76 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
       float tmax = row_valid ? t8[0] : NEG_INF;
       tmax = (tmax == NEG_INF) ? NEG_INF : __fmul_rn(tmax, c);
       const bool grow = tmax != NEG_INF && (m_used == NEG_INF || tmax > m_used + 8.f);
-      // the P buffer of tile i is free once P V of tile i - NPB completed
-      if (i >= NPB && !__all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[m][(i - NPB) & 1], ((i - NPB) >> 1) & 1))) {
-        s_abort = 1;
-        break;
-      }
-      // O is rescaled in TMEM (after P V of tile i - 1) when a row's maximum moved
-      if (i >= 1 && __any_sync(0xffffffffu, grow && m_used != NEG_INF)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[m][u ^ 1], ((i - 1) >> 1) & 1))) {
-          s_abort = 1;
-          break;
-        }
-        tc_fence_after();
-        const float f = (grow && m_used != NEG_INF) ? ex2(m_used - tmax) : 1.f;
-        float o[16];
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) {
-          const uint32_t ta = tmem + CF::kOCol + m * D + cc * 16 + lane_off;
-          tmem_ld16(ta, o);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = __fmul_rn(o[j], f);
-          tmem_st16(ta, o);
-        }
-        tc_fence_before();
-      }
+      // a row whose maximum moved rescales its sums now and its O (in TMEM) below
+      const bool rescale = grow && m_used != NEG_INF;
+      const float f = rescale ? ex2(m_used - tmax) : 1.f;
       if (grow) {
-        if (m_used != NEG_INF) {
-          const float f = ex2(m_used - tmax);
+        if (rescale) {
           l2 = fma2(l2, pack2(f, f), pack2(0.f, 0.f));
           lx2 = fma2(lx2, pack2(f, f), pack2(0.f, 0.f));
         }
         m_used = tmax;
       }
-      // P = 2^(s c - m) in bf16, 128 bytes of this row in the swizzled K-major tile
-      uint8_t *prow = smem + CF::kP + (m * NPB + i % NPB) * CF::kPBytes;
+      // the P buffer of tile i is free once P V of tile i - NPB completed; O is
+      // rescaled in TMEM (after P V of tile i - 1) when a row's maximum moved
+      auto wait_p_and_rescale = [&]() -> bool {
+        if (i >= NPB && !__all_sync(0xffffffffu, mbar_wait_sleep(&pv_done[m][(i - NPB) & 1], ((i - NPB) >> 1) & 1)))
+          return false;
+        if (i >= 1 && __any_sync(0xffffffffu, rescale)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[m][u ^ 1], ((i - 1) >> 1) & 1))) return false;
+          tc_fence_after();
+          float o[16];
+#pragma unroll
+          for (int cc = 0; cc < D / 16; ++cc) {
+            const uint32_t ta = tmem + CF::kOCol + m * D + cc * 16 + lane_off;
+            tmem_ld16(ta, o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = __fmul_rn(o[j], f);
+            tmem_st16(ta, o);
+          }
+          tc_fence_before();
+        }
+        return true;
+      };
+      // One pipeline per CTA: the exponentials run before the wait, while P V
+      // of the previous tile does.  Two pipelines per CTA (d = 64) share the
+      // SM's exponential unit and are faster with the wait first.
+      if (!kEarlyExp && !wait_p_and_rescale()) {
+        s_abort = 1;
+        break;
+      }
+      // P = 2^(s c - m) in bf16, in registers
       const uint64_t c2 = pack2(c, c), nm2 = pack2(-m_used, -m_used);
       const bool any = row_valid && m_used != NEG_INF;
       uint64_t la[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)}, lxa[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+      uint32_t pk[kKeys / 2];
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int j = q4 * 8 + 2 * h;
-          float p0 = 0.f, p1 = 0.f;
-          if (any) {
-            float x0, x1;
-            unpack2(fma2(pack2(s[j], s[j + 1]), c2, nm2), x0, x1);
-            p0 = ex2(x0);
-            p1 = ex2(x1);
-          }
-          const uint32_t pb = cvt_bf16x2(p0, p1);
-          lxa[h & 1] = add2(lxa[h & 1], pack2(p0, p1));
-          la[h & 1] = add2(la[h & 1], pack2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
-          pk[h] = pb;
+      for (int h = 0; h < kKeys / 2; ++h) {
+        const int j = 2 * h;
+        float p0 = 0.f, p1 = 0.f;
+        if (any) {
+          float x0, x1;
+          unpack2(fma2(pack2(s[j], s[j + 1]), c2, nm2), x0, x1);
+          p0 = ex2(x0);
+          p1 = ex2(x1);
         }
-        *reinterpret_cast<uint4 *>(prow + sw128(r_own, q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        const uint32_t pb = cvt_bf16x2(p0, p1);
+        lxa[h & 1] = add2(lxa[h & 1], pack2(p0, p1));
+        la[h & 1] = add2(la[h & 1], pack2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
+        pk[h] = pb;
       }
       l2 = add2(l2, add2(la[0], la[1]));
       lx2 = add2(lx2, add2(lxa[0], lxa[1]));
+      if (kEarlyExp && !wait_p_and_rescale()) {
+        s_abort = 1;
+        break;
+      }
+      // 128 bytes of this row in the swizzled K-major P tile
+      uint8_t *prow = smem + CF::kP + (m * NPB + i % NPB) * CF::kPBytes;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<uint4 *>(prow + sw128(r_own, q4)) =
+            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
       fence_proxy_async();  // P (generic writes) -> visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive1(&p_full[m][u]);
