@@ -446,29 +446,32 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
   int issued = 0;  // producer: tiles whose copies were issued
 
   if (warp == CF::kTmaWarp) {
-    // ---------------- producer: K and V pages of each tile into the ring
-    if (lane == 0) {
-      for (int i = 0; i < nt && !s_abort; ++i) {
-        const int st = i % NS;
-        if (i >= NS && !mbar_wait_sleep(&kv_empty[st], ((i / NS) - 1) & 1)) {
+    // ---------------- producer: K and V pages of each tile into the ring; lane 0
+    // takes the stage, one lane per page and operand issues its copy
+    constexpr int kCopies = 2 * kTilePages * (D / 64);
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % NS;
+      int ok = 1;
+      if (lane == 0) {
+        if (s_abort) ok = 0;
+        else if (i >= NS && !mbar_wait_sleep(&kv_empty[st], ((i / NS) - 1) & 1)) {
           s_abort = 1;
-          break;
+          ok = 0;
         }
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTilePages * (D / 64) * (kPage * 128));
-        uint8_t *kdst = smem + CF::kKV + st * 2 * CF::kKVBytes;
-        uint8_t *vdst = kdst + CF::kKVBytes;
-        for (int p = 0; p < kTilePages; ++p) {
-          const int blk = tab[i * kTilePages + p];
-          // pages past the keys or with a bad id load block 0 (finite values, masked out)
-          const int y = ((blk >= 0 ? blk : 0) * a.Hkv + hk) * kPage;
-#pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            tma_load_2d(kdst + h * (kKeys * 128) + p * (kPage * 128), &kmap, h * 64, y, &kv_full[st]);
-            tma_load_2d(vdst + h * (kKeys * 128) + p * (kPage * 128), &vmap, h * 64, y, &kv_full[st]);
-          }
-        }
-        issued = i + 1;
+        if (ok) mbar_arrive_expect_tx(&kv_full[st], 2 * kTilePages * (D / 64) * (kPage * 128));
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane < kCopies) {
+        const int p = lane / (2 * (D / 64)), r = lane % (2 * (D / 64));
+        const int kv = r & 1, h = r >> 1;
+        const int blk = tab[i * kTilePages + p];
+        // pages past the keys or with a bad id load block 0 (finite values, masked out)
+        const int y = ((blk >= 0 ? blk : 0) * a.Hkv + hk) * kPage;
+        uint8_t *dst = smem + CF::kKV + (st * 2 + kv) * CF::kKVBytes + h * (kKeys * 128) + p * (kPage * 128);
+        tma_load_2d(dst, kv ? &vmap : &kmap, h * 64, y, &kv_full[st]);
+      }
+      issued = i + 1;
     }
   } else if (warp == CF::kMmaWarp) {
     // ---------------- MMA issue (one thread): S(t) then O += P(t-1) V(t-1)
