@@ -413,7 +413,10 @@ def bench_e2e(ssd, spec, inp, device, K, W):
     """The same metric through the public call with HOST buffers: every step
     copies that step's logits and uniforms from pinned host memory to the
     device, runs the round and reads the emitted tokens, accept lengths,
-    bonus tokens and cache slots back."""
+    bonus tokens and cache slots back.  Steps are pipelined over two device
+    input buffers: the uploads run on a copy stream and step q + 1's upload
+    overlaps step q's round and readback on the compute stream (the host link
+    bounds the step, not the round)."""
     import torch
     from speculative_decoding_vocab_gb300.binding import pinned
     hin = dict(target=pinned(inp.target), draft=pinned(inp.draft),
@@ -421,35 +424,51 @@ def bench_e2e(ssd, spec, inp, device, K, W):
                u_acc=torch.from_numpy(inp.u_acc).pin_memory(),
                u_bonus=torch.from_numpy(inp.u_bonus).pin_memory(),
                payload=torch.from_numpy(inp.payload).pin_memory())
-    buf = RoundBuffers(spec, inp, device)
-    out = make_outputs(spec, device)
-    ws = ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device)
-    hout = {k: torch.empty_like(out[k], device="cpu").pin_memory()
-            for k in ("out_tokens", "accept_len", "bonus", "slot", "next_tokens")}
+    bufs = [RoundBuffers(spec, inp, device) for _ in range(2)]
+    outs = [make_outputs(spec, device) for _ in range(2)]
+    wss = [ssd.workspace(spec.B, spec.K, spec.V, spec.dtype, spec.F, device) for _ in range(2)]
+    keys = ("out_tokens", "accept_len", "bonus", "slot", "next_tokens")
+    houts = [{k: torch.empty_like(outs[0][k], device="cpu").pin_memory() for k in keys} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in hin.values())
-    d2h = sum(t.numel() * t.element_size() for t in hout.values())
-    stream = torch.cuda.current_stream(device)
+    d2h = sum(t.numel() * t.element_size() for t in houts[0].values())
+    comp = torch.cuda.current_stream(device)
+    copy = torch.cuda.Stream(device)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    for e in uploaded + consumed:  # torch creates the CUDA event on its first record
+        e.record(comp)
 
-    def step():
-        for k in ("target", "draft", "u_draft", "u_acc", "u_bonus", "payload"):
-            getattr(buf, k).copy_(hin[k], non_blocking=True)
-        run_round(ssd, spec, buf, out, ws)
-        for k, t in hout.items():
-            t.copy_(out[k], non_blocking=True)
+    def step(q):
+        i = q % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(consumed[i])  # round q - 2 has read buffer i
+            for k in ("target", "draft", "u_draft", "u_acc", "u_bonus", "payload"):
+                getattr(bufs[i], k).copy_(hin[k], non_blocking=True)
+            uploaded[i].record(copy)
+        comp.wait_event(uploaded[i])
+        run_round(ssd, spec, bufs[i], outs[i], wss[i])
+        consumed[i].record(comp)
+        for k, t in houts[i].items():
+            t.copy_(outs[i][k], non_blocking=True)
 
-    for _ in range(W):
-        step()
+    for q in range(W):
+        step(q)
     torch.cuda.synchronize()
     n = max(K // 4, 20)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n):
-        step()
-    b.record(stream)
+    a.record(comp)
+    copy.wait_stream(comp)  # no upload of the timed steps starts before the start mark
+    for q in range(n):
+        step(q)
+    b.record(comp)  # after the last round, which waited for the last upload, and its readback
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
+    same = all(torch.equal(houts[i][k], outs[i][k].cpu()) for i in range(2) for k in keys)
     return {"value": round(spec.B / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
-            "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "readback_ok": bool(same),
+            "schedule": "uploads on a copy stream into two device input buffers; rounds and readbacks "
+                        "on the compute stream; step q+1's upload overlaps step q's round"}
 
 
 def _time_calls(fn, n, stream):
