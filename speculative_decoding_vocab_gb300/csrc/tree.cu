@@ -19,9 +19,14 @@
 //                vocabulary-wide quantity the node needs -- the softmax
 //                statistics, the residual mass after each rejection, the
 //                block sums of the final draw -- is reduced from there.  Partial results meet through
-//                distributed shared memory and are combined in rank order by
-//                every CTA alike, so the cluster takes the same decisions and
-//                its control flow stays uniform.
+//                distributed shared memory (after each cluster barrier one
+//                lane per CTA copies that CTA's part, all at once) and are
+//                combined in rank order by every CTA alike, so the cluster
+//                takes the same decisions and its control flow stays uniform.
+//                The residual after n rejections is kept in closed form,
+//                max(0, p - A q) / B (see resid_w), so every element costs the
+//                same whatever n is; the next node's rows (the children's)
+//                are prefetched into L2 while a node is evaluated.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -39,6 +44,7 @@ constexpr int kBPW = 8;                      // blocks of 32 vectors per warp an
 constexpr int kCtaBlocks = kTWarps * kBPW;   // 128 blocks per CTA and row
 constexpr int kMaxCW = 8;                    // CTAs per cluster
 constexpr int kMaxNodes = 256;
+constexpr int kPrefetchChildren = 8;         // children whose rows are prefetched at a node
 
 struct TreeArgs {
   const void *target, *draft;
@@ -68,12 +74,13 @@ struct TreeSh {
   float res[4];
   uint64_t rkey[2];
   float bsum[kCtaBlocks];  // block sums of the final draw (this CTA's blocks, in order)
-  float invW[kMaxNodes];   // 1 / W of each residual taken at the current node
+  Part peer[kMaxCW];       // the cluster's parts of the current combination, copied here
   int sel[4];
   int32_t tok[kMaxNodes];
   int16_t first_child[kMaxNodes + 1];
   int16_t next_sib[kMaxNodes];
   int32_t path[kMaxNodes];
+  int32_t par[kMaxNodes];
 };
 
 SSD_DEV unsigned cluster_rank() {
@@ -84,15 +91,9 @@ SSD_DEV unsigned cluster_rank() {
 SSD_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-SSD_DEV float ld_peer_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-SSD_DEV uint64_t ld_peer_u64(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, a multiple of 16).
+SSD_DEV void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 template <class E>
@@ -136,36 +137,80 @@ struct Dist {
   }
 };
 
-// r after n residual steps: r_0 = p, r_{j+1} = max(0, r_j - q) / W_j.
-SSD_DEV float resid_r(float p, float q, int n, const float *invW) {
-  float r = p;
-  for (int j = 0; j < n; ++j) r = __fmul_rn(fmaxf(__fsub_rn(r, q), 0.f), invW[j]);
-  return r;
+// The residual after n rejections at a node, r_{j+1} = max(0, r_j - q) / W_j
+// from r_0 = p, in closed form: r_n = max(0, p - A_n q) / B_n with A_0 = 0,
+// B_0 = 1, A_{n+1} = A_n + B_n and B_{n+1} = B_n W_n = sum_i max(0, p_i -
+// A_{n+1} q_i).  (If p - A_n q > 0 then r_n - q = (p - (A_n + B_n) q) / B_n;
+// otherwise both sides are 0.)  The walk keeps (A, B) and weighs element i by
+// the unnormalised max(0, p_i - A q_i): O(1) per element however many
+// children were rejected.
+SSD_DEV float resid_w(float p, float q, float A) { return fmaxf(__fmaf_rn(-A, q, p), 0.f); }
+// The bonus's weight of element idx: p before any rejection (q is then not
+// computed), else the unnormalised residual.
+SSD_DEV float bonus_w(const Dist &D, float zt, float zd, int idx, int n, float A) {
+  const float p = D.p(zt, idx);
+  return n == 0 ? p : resid_w(p, D.q(zd, idx), A);
 }
 
 // Thread 0 of every CTA publishes sh.part[buf]; after the cluster barrier
 // thread 0 reads the cw parts in rank order, combines them with `comb` and
 // leaves the result in sh.res / sh.rkey for the CTA.
 // The part of CTA `rank` of the cluster.
+// The parts of the cluster's CTAs, copied into this CTA's shared memory.
 struct Peers {
-  uint32_t base0;  // this CTA's sh.part[buf] in the cluster window
-  SSD_DEV uint32_t at(int rank) const {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(base0), "r"(rank));
-    return r;
-  }
-  SSD_DEV float a(int rank, int i) const { return ld_peer_f32(at(rank) + 4 * i); }
-  SSD_DEV uint64_t key(int rank, int i) const { return ld_peer_u64(at(rank) + 16 + 8 * i); }
+  const Part *p;
+  SSD_DEV float a(int rank, int i) const { return p[rank].a[i]; }
+  SSD_DEV uint64_t key(int rank, int i) const { return p[rank].key[i]; }
 };
 
+// After the cluster barrier lane r of warp 0 copies CTA r's part (32 bytes,
+// two remote 16-byte loads, all CTAs at once); thread 0 then combines them.
 template <class Comb>
 SSD_DEV void cluster_combine(TreeSh &sh, int buf, int cw, Comb comb) {
   cluster_sync();
-  if (threadIdx.x == 0) comb(Peers{smem_u32(&sh.part[buf])}, cw, sh);
+  if (threadIdx.x < static_cast<unsigned>(cw)) {
+    uint32_t src;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(src) : "r"(smem_u32(&sh.part[buf])), "r"(threadIdx.x));
+    uint4 lo, hi;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w) : "r"(src) : "memory");
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w) : "r"(src + 16) : "memory");
+    uint4 *dst = reinterpret_cast<uint4 *>(&sh.peer[threadIdx.x]);
+    dst[0] = lo;
+    dst[1] = hi;
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) comb(Peers{sh.peer}, cw, sh);
   __syncthreads();
 }
 
 constexpr size_t kRowStage = static_cast<size_t>(kCtaBlocks) * 32 * sizeof(uint4);  // 64 KB per row
+
+// Running totals of the CTA's block sums in block order, as one warp forms
+// them: lane l sums blocks 4l .. 4l+3 in order, the lanes' totals are scanned,
+// and block 4l + j's running total is the lanes-before part plus the lane's
+// own run up to j.  The CTA's total is lane 31's last running total; the block
+// search repeats exactly this arithmetic.
+static_assert(kCtaBlocks == 4 * 32, "four block sums per lane");
+SSD_DEV void block_runs(const float *bsum, int lane, float (&bs)[4], float (&run)[4], float &excl) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) bs[j] = bsum[4 * lane + j];
+  float r[4];
+  r[0] = bs[0];
+#pragma unroll
+  for (int j = 1; j < 4; ++j) r[j] = __fadd_rn(r[j - 1], bs[j]);
+  float inc = r[3];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc = __fadd_rn(inc, t);
+  }
+  excl = __shfl_up_sync(0xffffffffu, inc, 1);
+  if (lane == 0) excl = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) run[j] = __fadd_rn(excl, r[j]);
+}
 
 template <class E>
 __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
@@ -181,11 +226,13 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
   uint32_t fl = 0;
   const float NEG_INF = -__int_as_float(0x7f800000);
 
-  // children lists in index order (a node's parent must lie in [-1, m-1])
+  // children lists in index order (a node's parent must lie in [-1, m-1]),
+  // built from a copy of the parents in shared memory
+  for (int m = tid; m < N; m += kTT) sh.par[m] = par[m];
   for (int m = tid; m <= N; m += kTT) sh.first_child[m] = -1;
   __syncthreads();
   for (int m = tid; m < N; m += kTT) {
-    const int p = par[m];
+    const int p = sh.par[m];
     sh.tok[m] = a.tokens[static_cast<int64_t>(b) * N + m];
     sh.next_sib[m] = -1;
     if (p < -1 || p >= m) {
@@ -193,19 +240,20 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
       continue;
     }
     for (int c = m + 1; c < N; ++c) {
-      if (par[c] == p) {
+      if (sh.par[c] == p) {
         sh.next_sib[m] = static_cast<int16_t>(c);
         break;
       }
     }
     bool first = true;
-    for (int c = p + 1; c < m && first; ++c) first = (par[c] != p);
+    for (int c = p + 1; c < m && first; ++c) first = (sh.par[c] != p);
     if (first) sh.first_child[p + 1] = static_cast<int16_t>(m);
   }
   __syncthreads();
 
   int buf = 0, node = -1, L = 0, nrej = 0;
   float Wlast = 1.f;
+  float Ar = 0.f, Br = 1.f;  // the residual at this node: max(0, p - Ar q) / Br
   Dist D;
   D.kT = a.kT;
   D.greedy = a.greedy;
@@ -229,6 +277,19 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
     }
     cp_async_wait_all();
     __syncthreads();
+    // the next node is one of this node's children: their rows (this CTA's
+    // slices, the first kPrefetchChildren children) start moving into L2
+    // while the node is evaluated
+    if (tid == 0) {
+      const int64_t v0 = static_cast<int64_t>(rank) * kCtaBlocks * 32;
+      const int64_t v1 = min(v0 + kCtaBlocks * 32, static_cast<int64_t>(a.nfull));
+      int c = sh.first_child[node + 1];
+      for (int n = 0; n < kPrefetchChildren && c >= 0 && v1 > v0; ++n, c = sh.next_sib[c]) {
+        const int64_t coff = (static_cast<int64_t>(b) * a.seq_stride + static_cast<int64_t>(c + 1) * a.row_stride) * E::kSize;
+        prefetch_l2(static_cast<const char *>(a.target) + coff + v0 * 16, static_cast<uint32_t>((v1 - v0) * 16));
+        prefetch_l2(static_cast<const char *>(a.draft) + coff + v0 * 16, static_cast<uint32_t>((v1 - v0) * 16));
+      }
+    }
     // statistics of p and q
     if (a.greedy) {
       uint64_t kp = 0, kq = 0;
@@ -357,6 +418,8 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
     // the children, in index order
     nrej = 0;
     Wlast = 1.f;
+    Ar = 0.f;
+    Br = 1.f;
     int next = -1;
     for (int c = sh.first_child[node + 1]; c >= 0; c = sh.next_sib[c]) {
       const int x = sh.tok[c];
@@ -365,12 +428,14 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
         continue;
       }
       const float px = D.p(E::ld(rowT, x), x), qx = D.q(E::ld(rowD, x), x);
-      const float rx = resid_r(px, qx, nrej, sh.invW);
-      if (__fmul_rn(a.u_acc[static_cast<int64_t>(b) * N + c], qx) < rx) {
+      // accept iff u q < r(x) = max(0, p - A q) / B
+      const float rx = resid_w(px, qx, Ar);
+      if (__fmul_rn(__fmul_rn(a.u_acc[static_cast<int64_t>(b) * N + c], qx), Br) < rx) {
         next = c;
         break;
       }
-      // rejected: W = sum over the row of max(0, r - q)
+      // rejected: B W = sum over the row of max(0, p - (A + B) q)
+      const float An = __fadd_rn(Ar, Br);
       float s = 0.f;
 #pragma unroll 1
       for (int k = 0; k < kBPW; ++k) {
@@ -380,9 +445,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
         const int i0 = (32 * (static_cast<int>(rank) * kCtaBlocks + warp + kTWarps * k) + lane) * E::kVec;
 #pragma unroll
         for (int e = 0; e < E::kVec; ++e) {
-          const float qi = D.q(fd[e], i0 + e);
-          const float ri = resid_r(D.p(ft[e], i0 + e), qi, nrej, sh.invW);
-          s = __fadd_rn(s, fmaxf(__fsub_rn(ri, qi), 0.f));
+          s = __fadd_rn(s, resid_w(D.p(ft[e], i0 + e), D.q(fd[e], i0 + e), An));
         }
       }
       s = warp_sum(s);
@@ -399,13 +462,12 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
         st.res[0] = S;
       });
       buf ^= 1;
-      const float W = sh.res[0];
-      __syncthreads();  // every thread has read sh.res before thread 0 writes invW
-      if (W > 0.f) {
-        if (tid == 0) sh.invW[nrej] = __frcp_rn(W);
+      const float BW = sh.res[0];
+      if (BW > 0.f) {
         ++nrej;
-        Wlast = W;
-        __syncthreads();
+        Wlast = __fdiv_rn(BW, Br);
+        Ar = An;
+        Br = BW;
       } else {
         fl |= kFlagZeroResidual;
       }
@@ -429,7 +491,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
       const int i0 = (32 * (static_cast<int>(rank) * kCtaBlocks + warp + kTWarps * k) + lane) * E::kVec;
       float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < E::kVec; ++e) s = __fadd_rn(s, resid_r(D.p(ft[e], i0 + e), D.q(fd[e], i0 + e), nrej, sh.invW));
+      for (int e = 0; e < E::kVec; ++e) s = __fadd_rn(s, bonus_w(D, ft[e], fd[e], i0 + e, nrej, Ar));
       // the block total by the scan the element search repeats
       float inc = s;
 #pragma unroll
@@ -440,10 +502,10 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
       if (lane == 31) sh.bsum[warp + kTWarps * k] = inc;
     }
     __syncthreads();
-    if (tid == 0) {
-      float S = 0.f;
-      for (int g = 0; g < kCtaBlocks; ++g) S = __fadd_rn(S, sh.bsum[g]);
-      sh.part[buf].a[0] = S;
+    if (warp == 0) {
+      float bs[4], run[4], excl;
+      block_runs(sh.bsum, lane, bs, run, excl);
+      if (lane == 31) sh.part[buf].a[0] = run[3];
     }
     const float ub = a.u_bonus[b];
     cluster_combine(sh, buf, cw, [ub](const Peers &all, int n, TreeSh &st) {
@@ -486,29 +548,35 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
     if (S > 0.f) {
       // the chosen CTA locates the block, its owning warp the lane and element
       if (sh.sel[0] == static_cast<int>(rank)) {
-        if (tid == 0) {
+        if (warp == 0) {
+          // the first block with mass whose running total exceeds t, else the last with mass
           const float t = sh.res[1];
-          float run = 0.f;
+          float bs[4], run[4], excl;
+          block_runs(sh.bsum, lane, bs, run, excl);
           int pick = -1, last = -1;
           float before = 0.f, before_last = 0.f;
-          for (int g = 0; g < kCtaBlocks; ++g) {
-            const float nx = __fadd_rn(run, sh.bsum[g]);
-            if (sh.bsum[g] > 0.f) {
-              if (pick < 0 && nx > t) {
-                pick = g;
-                before = run;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float bef = j == 0 ? excl : run[j - 1];
+            if (bs[j] > 0.f) {
+              if (pick < 0 && run[j] > t) {
+                pick = 4 * lane + j;
+                before = bef;
               }
-              last = g;
-              before_last = run;
+              last = 4 * lane + j;
+              before_last = bef;
             }
-            run = nx;
           }
-          if (pick < 0) {
-            pick = last;
-            before = before_last;
+          const unsigned hitl = __ballot_sync(0xffffffffu, pick >= 0);
+          const unsigned posl = __ballot_sync(0xffffffffu, last >= 0);
+          const int src = hitl ? __ffs(hitl) - 1 : (posl ? 31 - __clz(posl) : -1);
+          if (src >= 0 && lane == src) {
+            sh.sel[1] = hitl ? pick : last;
+            sh.res[2] = __fsub_rn(t, hitl ? before : before_last);
+          } else if (src < 0 && lane == 0) {
+            sh.sel[1] = -1;
+            sh.res[2] = 0.f;
           }
-          sh.sel[1] = pick;
-          sh.res[2] = __fsub_rn(t, before);
         }
         __syncthreads();
         const int g = sh.sel[1];
@@ -520,7 +588,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
           E::unpack(sD[g * 32 + lane], fd);
           float s = 0.f;
 #pragma unroll
-          for (int e = 0; e < E::kVec; ++e) s = __fadd_rn(s, resid_r(D.p(ft[e], i0 + e), D.q(fd[e], i0 + e), nrej, sh.invW));
+          for (int e = 0; e < E::kVec; ++e) s = __fadd_rn(s, bonus_w(D, ft[e], fd[e], i0 + e, nrej, Ar));
           float inc = s;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -539,7 +607,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
             int tokb = -1, lastpos = -1;
 #pragma unroll
             for (int e = 0; e < E::kVec; ++e) {
-              const float we = resid_r(D.p(ft[e], i0 + e), D.q(fd[e], i0 + e), nrej, sh.invW);
+              const float we = bonus_w(D, ft[e], fd[e], i0 + e, nrej, Ar);
               c = __fadd_rn(c, we);
               if (we > 0.f) {
                 if (tokb < 0 && c > tl) tokb = i0 + e;
@@ -558,6 +626,8 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
     fl |= kFlagZeroResidual;
     nrej = 0;
     Wlast = 1.f;
+    Ar = 0.f;
+    Br = 1.f;
   }
 
   if (rank == 0) {
