@@ -70,6 +70,11 @@ def test_workspace_size(lib):
     assert ssd.ssd_workspace_size(32, 5, 8, "bf16", (16, 8, 4, 2, 1, 1)) == 0  # F_k > V
     assert ssd.ssd_workspace_size(2, 17, 1000, "f32", tuple([1] * 18)) == 0   # K > 16
     assert ssd.ssd_workspace_size(2, 1, 1000, "f32", (300, 1)) == 0          # F > 256
+    # rows up to 4 MiB: V = 2^21 in bf16, 2^20 in fp32; one element more is unsupported
+    assert ssd.ssd_workspace_size(2, 2, 1 << 21, "bf16", (16, 4, 1)) > 0
+    assert ssd.ssd_workspace_size(2, 2, (1 << 21) + 8, "bf16", (16, 4, 1)) == 0
+    assert ssd.ssd_workspace_size(2, 2, 1 << 20, "f32", (16, 4, 1)) > 0
+    assert ssd.ssd_workspace_size(2, 2, (1 << 20) + 4, "f32", (16, 4, 1)) == 0
 
 
 def test_attention_workspace_size(lib):

@@ -55,6 +55,15 @@ def test_small_shapes(spec):
     _check(w.make_attention(spec, seed=11))
 
 
+@pytest.mark.parametrize("spec", [
+    w.AttnSpec(B=2, Hq=4, Hkv=2, d=64, L=200, tree="chain", n_chain=128),
+    w.AttnSpec(B=1, Hq=2, Hkv=1, d=128, L=90, tree="chain", n_chain=128, ragged_prefix=True),
+], ids=["chain128-d64", "chain128-d128"])
+def test_largest_trees(spec):
+    """128 tree nodes, the most the attention call takes, all of them queries."""
+    _check(w.make_attention(spec, seed=13))
+
+
 def test_long_unsplit_keys_d128():
     """30,000 keys in one key range (no workspace): the block-table slice leaves
     no room for the six-stage d = 128 kernel, so the four-stage one runs."""

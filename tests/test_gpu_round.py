@@ -116,6 +116,16 @@ def test_shapes(dtype, V, pad, K, F, T):
     compare_round(inp, gpu_round(inp))
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 1 << 21), ("f32", 1 << 20)])
+def test_largest_rows(dtype, V):
+    """Rows of the largest supported size, 4 MiB (1024 segments of 4 KiB): every
+    sequence against the oracle."""
+    spec = w.RoundSpec(B=2, K=2, V=V, dtype=dtype, recipe="gauss", T=0.7, C=0.5, F=(16, 4, 1),
+                       target_sigma=2.0, draft_noise=0.7, row_pad=0)
+    inp = w.make_round(spec, seed=21)
+    compare_round(inp, gpu_round(inp))
+
+
 def test_zero_batch_is_a_noop():
     spec = w.RoundSpec(B=0, K=3, V=100, dtype="f32", recipe="gauss", F=(2, 1, 1, 1))
     inp = w.make_round(spec)

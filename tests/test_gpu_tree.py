@@ -116,6 +116,29 @@ def test_tree_children_at_target_argmax(T):
         assert (r["accept_len"] == 2).all()
 
 
+def test_tree_chain_of_max_nodes_greedy():
+    """A chain of 256 nodes (the largest tree) whose tokens are the target's
+    argmax at T = 0: every walk goes the whole way down, 256 nodes deep."""
+    B, N, V = 2, 256, 640
+    spec = w.TreeSpec(B=B, V=V, dtype="f32", T=0.0, branching=(1,) * N, recipe="gauss",
+                      draft_noise=0.8, name="chain256")
+    tgt, dft = w.tree_logits(spec, 23)
+    parent1 = np.arange(-1, N - 1, dtype=np.int32)
+    assert np.array_equal(parent1, w.tree_shape(spec.branching))
+    tok = np.ascontiguousarray(tgt.argmax(axis=2)[:, :N], dtype=np.int32)
+    par = np.broadcast_to(parent1, (B, N)).copy()
+    ua, ub = w.tree_uniforms(23, 0, B, N)
+    g, r, _ = compare(spec, tgt, dft, par, tok, ua, ub)
+    assert (g["accept_len"] == N).all()
+
+
+def test_tree_binary_254_nodes():
+    """A binary tree seven levels deep (254 nodes), children drawn from the draft."""
+    spec = w.TreeSpec(B=4, V=700, dtype="f32", T=1.0, branching=(2,) * 7, recipe="gauss",
+                      draft_noise=0.6, name="binary254")
+    compare(spec, *inputs(spec, 25))
+
+
 def test_tree_llama3_full_batch():
     """The 28-node tree over the Llama-3 vocabulary (4 CTAs per sequence), all
     32 sequences."""
