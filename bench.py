@@ -392,12 +392,20 @@ def bench_ours(args):
                               "|u - p/q'| < 1e-6 (GPU fp32 count, ssd_round near_ties output)"},
     }
     result["step_roofline_frac"] = round(alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4)
+    # secondary ceilings of a step: the exponentials (one per logit; none at T = 0) on the
+    # special function units, against the HBM time of the logits
+    n_exp = 0 if spec.T == 0 else 2 * (spec.K + 1) * spec.V * spec.B
+    result["secondary_ceilings"] = {
+        "exp_count": n_exp, "sfu_floor_ms": round(sfu_floor_ms(n_exp, device), 5),
+        "hbm_floor_ms": round(alg_bytes / (hbm_peak * 1e9) * 1e3, 5),
+        "note": "16 exponentials per clock per SM at the maximum SM clock; the round is HBM-bound"}
     if not args.no_extras:
         result["e2e"] = bench_e2e(ssd, spec, inp, device, K, W)
         result["branch_attention"] = bench_attention(ssd, device, hbm_peak)
         result["other_rounds"] = bench_other_rounds(ssd, w, device, hbm_peak)
         result["tiny_round"] = bench_tiny_round(ssd, w, device)
         result["round_analytics"] = bench_analytics(ssd, w, device, hbm_peak)
+        result["saguaro_sample"] = bench_saguaro_sample(ssd, w, device, hbm_peak)
         result["miss_fallback"] = bench_fallback(ssd, w, device, hbm_peak)
         result["cache_fill"] = bench_cache_fill(ssd, w, device, hbm_peak)
         result["tree_verify"] = bench_tree(ssd, w, device, hbm_peak)
@@ -469,6 +477,28 @@ def bench_e2e(ssd, spec, inp, device, K, W):
             "readback_ok": bool(same),
             "schedule": "uploads on a copy stream into two device input buffers; rounds and readbacks "
                         "on the compute stream; step q+1's upload overlaps step q's round"}
+
+
+SFU_EXP_PER_CLK_PER_SM = 16  # ex2 results per clock per SM (the special function units)
+
+
+def sfu_floor_ms(n_exp, device):
+    """Time the special function units need for n_exp exponentials at the
+    device's SM count and maximum SM clock (a secondary ceiling)."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    mhz = _max_sm_mhz()
+    return n_exp / (SFU_EXP_PER_CLK_PER_SM * sms * mhz * 1e6) * 1e3
+
+
+def _max_sm_mhz():
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=10).stdout.split()
+        return float(out[0])
+    except Exception:
+        return 2070.0  # the GB300's maximum SM clock
 
 
 def _time_calls(fn, n, stream):
@@ -545,6 +575,8 @@ def bench_attention(ssd, device, hbm_peak):
         res[spec.name] = {"ms": round(ms, 4), "algorithmic_bytes": alg, "GB/s": round(gbs, 1),
                           "frac_of_hbm_peak": round(gbs / hbm_peak, 4),
                           "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 2),
+                          "exp_count": vis_pairs,
+                          "sfu_floor_ms": round(sfu_floor_ms(vis_pairs, device), 4),
                           "kernel": "k_branch_attn_tc (tcgen05/TMEM + TMA)",
                           "status_flags": int(st.item())}
         del g, q, kc, vc, kc2, vc2, out
@@ -592,6 +624,41 @@ def device_round_sets(spec, device, seed):
     u = torch.rand(3, spec.B, spec.K + 1, generator=g, device=device)
     uni = (u[0, :, :spec.K].contiguous(), u[1, :, :spec.K].contiguous(), u[2, :, 0].contiguous())
     return sets, nsets, per, uni
+
+
+def bench_saguaro_sample(ssd, w, device, hbm_peak):
+    """The draft's Saguaro draw alone (ssd_saguaro_sample: the K draft rows of
+    every sequence, K V elem bytes per sequence) on the Llama-3 round (C = 1)
+    and the large-batch Qwen-3 round (C = 0.5)."""
+    import torch
+    res = {}
+    stream = torch.cuda.current_stream(device)
+    for spec in (w.llama3_round(T=1.0, B=32), w.qwen3_round(C=0.5)):
+        sets, nsets, per, (ud, _, _) = device_round_sets(spec, device, 17)
+        B, K = spec.B, spec.K
+        i32 = dict(dtype=torch.int32, device=device)
+        d = torch.empty(B, K, **i32)
+        qd = torch.empty(B, K, dtype=torch.float32, device=device)
+        st = torch.zeros(1, **i32)
+        ws = ssd.workspace(B, K, spec.V, spec.dtype, spec.F, device)
+
+        def call(i):
+            ssd.ssd_saguaro_sample(sets[i % nsets][1], spec.V, spec.F, spec.C, spec.T, ud, d, qd_out=qd,
+                                   status=st, ws=ws)
+
+        for i in range(3):
+            call(i)
+        g = capture_graphs([lambda: [call(i) for i in range(nsets)]], device)[0]
+        g.replay()
+        ms = _time_calls(lambda i: g.replay(), max(3, 60 // nsets), stream) / nsets
+        alg = B * K * spec.V * 2  # the K draft rows of every sequence, bf16
+        res[spec.name] = {"ms": round(ms, 4), "algorithmic_bytes": alg,
+                          "frac_of_hbm_peak": round(alg / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "seq_per_s": round(B / (ms * 1e-3), 1), "C": spec.C,
+                          "status_flags": int(st.item())}
+        del g, sets
+        torch.cuda.empty_cache()
+    return res
 
 
 def bench_analytics(ssd, w, device, hbm_peak):
