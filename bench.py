@@ -577,6 +577,11 @@ def bench_attention(ssd, device, hbm_peak):
                           "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 2),
                           "exp_count": vis_pairs,
                           "sfu_floor_ms": round(sfu_floor_ms(vis_pairs, device), 4),
+                          # the binding floor: HBM bytes, bf16 tensor FLOPs (measured burst
+                          # peak) or the exponentials, whichever takes longest
+                          "frac_of_floor": round(max(alg / (hbm_peak * 1e9),
+                                                     flops / ((load_peaks().get("bf16_tflops") or 1900.0) * 1e12),
+                                                     sfu_floor_ms(vis_pairs, device) * 1e-3) / (ms * 1e-3), 4),
                           "kernel": "k_branch_attn_tc (tcgen05/TMEM + TMA)",
                           "status_flags": int(st.item())}
         del g, q, kc, vc, kc2, vc2, out
