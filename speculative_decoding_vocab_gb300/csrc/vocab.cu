@@ -1702,10 +1702,14 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
         emit(a, b, acc, r.bt, r.W, (r.fl & kRecZero) != 0, (r.fl & kRecBonusNear) != 0, staged, sh,
              st.fin.look);
       }
-      // every unit takes a ticket; the last one resets the ready words
+      // every unit takes a ticket (a sole unit is the last); the last one resets the ready words
       if (tid == 0) {
-        __threadfence();
-        sh.ival[0] = (atomicAdd(a.ctr + 2 + b, 1u) + 1 == static_cast<uint32_t>(U)) ? 1 : 0;
+        if (U == 1) {
+          sh.ival[0] = 1;
+        } else {
+          __threadfence();
+          sh.ival[0] = (atomicAdd(a.ctr + 2 + b, 1u) + 1 == static_cast<uint32_t>(U)) ? 1 : 0;
+        }
       }
       __syncthreads();
       if (sh.ival[0]) reset_ready(a, b);
@@ -1728,7 +1732,16 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
         if (lane < kResSeg && sg < a.nseg) a.useg[static_cast<size_t>(b) * a.nseg + sg] = make_float2(vr, vp);
         const float ir = warp_incl_scan(vr);
         const float ip = warp_incl_scan(vp);
-        if (lane == 31) {
+        if (U == 1) {
+          // the sequence's sole unit is its last: its masses go straight to
+          // where the draw reads them, without the round trip through memory
+          if (lane < kResSeg && sg < a.nseg) st.fin.sgm[sg] = make_float2(vr, vp);
+          if (lane == 31) {
+            sh.um[0][0] = ir;
+            sh.um[1][0] = ip;
+            sh.ival[0] = 1;
+          }
+        } else if (lane == 31) {
           a.umass[static_cast<size_t>(b) * U + u] = make_float2(ir, ip);
           __threadfence();
           const uint32_t t = atomicAdd(a.ctr + 2 + b, 1u);
@@ -1745,7 +1758,7 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
         bool ok = true;
         if (tid == 0) {
           if (a.do_lookup) ok = wait_ready(&a.ready[(static_cast<size_t>(b) * (K + 1) + acc) * 2 + 1]);
-        } else {
+        } else if (U > 1) {
           for (int q = tid - 1; q < U; q += kThreads - 1) {
             const float2 v = __ldcg(a.umass + static_cast<size_t>(b) * U + q);
             sh.um[0][q] = v.x;
