@@ -61,8 +61,9 @@ constexpr int kSegBlocks = 8;                  // blocks of 32 vectors per segme
 constexpr int kUnitSeg = kWarps;               // segments per residual-unit staging (k_resid)
 constexpr int kStatWarps = 4;                  // segments (one per warp) per k_stats CTA: 128 threads,
                                                // 8 CTAs per SM, a fine-grained last wave
-constexpr int kResSeg = kWarps / 2;            // segments per residual unit (two warps per segment)
+constexpr int kResSeg = kWarps / 2;            // segments per group of a residual unit (two warps per segment)
 constexpr int kMaxSeg = 1024;                  // rows of at most 4 MiB
+constexpr int kMaxSub = 8;                     // groups of kResSeg segments per residual unit (<= 32 segments)
 constexpr int kMaxUnits = kMaxSeg / kResSeg;   // 256
 constexpr int kMaxK = 16;
 constexpr int kMaxSlots = 2 * (kMaxK + 1);
@@ -128,6 +129,7 @@ struct VocabArgs {
   int B, K, V;
   int nvec, nfull;  // 16-byte vectors per row (the last may be partial), whole ones
   int nseg, nblk, nunits;
+  int unit_sub;  // groups of kResSeg segments per residual unit (1 .. kMaxSub)
   int nslots, npairs;
   int b0;  // k_stats: first sequence of this launch (grid z = sequence - b0)
   float kT;    // log2(e) / T
@@ -1264,10 +1266,10 @@ constexpr int kLookupStage = 2048;  // guesses + payload words of a sequence sta
 struct __align__(16) ResSh {
   PairRec rec[kMaxK + 1];
   float u[kMaxK];
-  float seg[kWarps][2];      // this unit's half-segment masses (residual, p), or its warps' analytics sums
+  float seg[kMaxSub * kWarps][2];  // this unit's half-segment masses (residual, p) per group, or its warps' analytics sums
   float um[2][kMaxUnits];    // the sequence's unit masses (residual, p)
   float bx[kUnitSeg * kSegBlocks];
-  float sm[kUnitSeg];
+  float sm[kMaxSub * kResSeg];   // the located unit's segment masses
   float scal[4];
   int ival[4];
   unsigned long long mk[8];
@@ -1386,47 +1388,54 @@ SSD_DEV void stage_block1(const VocabArgs &a, int b, int j, int g, int w, ResSta
   __syncwarp();
 }
 
-// Residual pass over unit u (segments 4u .. 4u + 3, two warps per segment,
-// four blocks each) of row pair j of sequence b: each lane sums max(0, p -
+// Residual pass over unit u of row pair j of sequence b: a.unit_sub groups of
+// kResSeg segments (the unit's segments (u unit_sub + g) kResSeg .. + 3 in
+// group g), two warps per segment, four blocks each.  Each lane sums max(0, p -
 // q') and p over its elements in order, the lanes by a butterfly: the
-// half-segment masses, into sh.seg.  kMins: *mn, *mx (every lane) = the
-// warp's sums of min(p, q') and of max(0, p - q').
+// half-segment masses of group g into sh.seg[g kWarps + warp].  kMins: *mn,
+// *mx (every lane) = the warp's sums of min(p, q') and of max(0, p - q') over
+// the unit.
 template <class E, bool kMins>
 SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr, ResSh &sh, ResStage &st,
                        float *mn_out, float *mx_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sg = u * kResSeg + (warp >> 1);
-  const int g0 = sg * kSegBlocks + (warp & 1) * (kSegBlocks / 2);
-  float mn = 0.f, rs = 0.f, ps = 0.f;
-  if (sg < a.nseg) {
-    stage_blocks<E>(a, b, j, g0, kSegBlocks / 2, warp, st);
+  float mn = 0.f, mx = 0.f;
 #pragma unroll 1
-    for (int k = 0; k < kSegBlocks / 2; ++k) {
-      const int i0 = ((g0 + k) * 32 + lane) * E::kVec;
-      float ft[E::kVec], fd[E::kVec];
-      E::unpack(st.v[warp][0][k][lane], ft);
-      E::unpack(st.v[warp][1][k][lane], fd);
+  for (int grp = 0; grp < a.unit_sub; ++grp) {
+    const int sg = (u * a.unit_sub + grp) * kResSeg + (warp >> 1);
+    const int g0 = sg * kSegBlocks + (warp & 1) * (kSegBlocks / 2);
+    float rs = 0.f, ps = 0.f;
+    if (sg < a.nseg) {
+      stage_blocks<E>(a, b, j, g0, kSegBlocks / 2, warp, st);
+#pragma unroll 1
+      for (int k = 0; k < kSegBlocks / 2; ++k) {
+        const int i0 = ((g0 + k) * 32 + lane) * E::kVec;
+        float ft[E::kVec], fd[E::kVec];
+        E::unpack(st.v[warp][0][k][lane], ft);
+        E::unpack(st.v[warp][1][k][lane], fd);
 #pragma unroll
-      for (int e = 0; e < E::kVec; ++e) {
-        if (i0 + e < a.V) {
-          const float p = wr.p(ft[e]), q = wr.q(fd[e], i0 + e);
-          const float r = __fsub_rn(p, q);
-          rs = __fadd_rn(rs, r > 0.f ? r : 0.f);
-          ps = __fadd_rn(ps, p);
-          if (kMins) mn = __fadd_rn(mn, fminf(p, q));
+        for (int e = 0; e < E::kVec; ++e) {
+          if (i0 + e < a.V) {
+            const float p = wr.p(ft[e]), q = wr.q(fd[e], i0 + e);
+            const float r = __fsub_rn(p, q);
+            rs = __fadd_rn(rs, r > 0.f ? r : 0.f);
+            ps = __fadd_rn(ps, p);
+            if (kMins) mn = __fadd_rn(mn, fminf(p, q));
+          }
         }
       }
+      rs = warp_sum(rs);
+      ps = warp_sum(ps);
     }
-    rs = warp_sum(rs);
-    ps = warp_sum(ps);
-  }
-  if (lane == 0) {
-    sh.seg[warp][0] = rs;
-    sh.seg[warp][1] = ps;
+    if (lane == 0) {
+      sh.seg[grp * kWarps + warp][0] = rs;
+      sh.seg[grp * kWarps + warp][1] = ps;
+    }
+    if (kMins) mx = __fadd_rn(mx, rs);
   }
   if (kMins) {
     *mn_out = warp_sum(mn);
-    *mx_out = rs;
+    *mx_out = mx;
   }
 }
 
@@ -1452,13 +1461,14 @@ SSD_DEV int resid_draw(const VocabArgs &a, int b, int acc, const WResid &wr, Res
     float rem2 = 0.f, W2;
     bool fb2 = false;
     if (q >= 0) {
-      if (lane < kResSeg) {
-        const int t = q * kResSeg + lane;
+      const int nus = a.unit_sub * kResSeg;  // the unit's segments (<= 32)
+      if (lane < nus) {
+        const int t = q * nus + lane;
         sh.sm[lane] = (t < a.nseg) ? (X ? st.fin.sgm[t].y : st.fin.sgm[t].x) : 0.f;
       }
       __syncwarp();
-      const int s = warp_locate(sh.sm, kResSeg, rem, true, &rem2, &W2, &fb2);
-      if (s >= 0) sg = q * kResSeg + s;
+      const int s = warp_locate(sh.sm, nus, rem, true, &rem2, &W2, &fb2);
+      if (s >= 0) sg = q * nus + s;
     }
     if (lane == 0) {
       sh.ival[0] = sg;
@@ -1723,19 +1733,21 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
       if (warp == 0) {
         // the segment masses (two halves in order) and the unit's mass by
         // warp_runs' arithmetic over them
+        const int nus = a.unit_sub * kResSeg;  // the unit's segments (<= 32), one per lane
         float vr = 0.f, vp = 0.f;
-        if (lane < kResSeg) {
-          vr = __fadd_rn(sh.seg[2 * lane][0], sh.seg[2 * lane + 1][0]);
-          vp = __fadd_rn(sh.seg[2 * lane][1], sh.seg[2 * lane + 1][1]);
+        if (lane < nus) {
+          const int h = (lane / kResSeg) * kWarps + 2 * (lane % kResSeg);  // its first half in sh.seg
+          vr = __fadd_rn(sh.seg[h][0], sh.seg[h + 1][0]);
+          vp = __fadd_rn(sh.seg[h][1], sh.seg[h + 1][1]);
         }
-        const int sg = u * kResSeg + lane;
-        if (lane < kResSeg && sg < a.nseg) a.useg[static_cast<size_t>(b) * a.nseg + sg] = make_float2(vr, vp);
+        const int sg = u * nus + lane;
+        if (lane < nus && sg < a.nseg) a.useg[static_cast<size_t>(b) * a.nseg + sg] = make_float2(vr, vp);
         const float ir = warp_incl_scan(vr);
         const float ip = warp_incl_scan(vp);
         if (U == 1) {
           // the sequence's sole unit is its last: its masses go straight to
           // where the draw reads them, without the round trip through memory
-          if (lane < kResSeg && sg < a.nseg) st.fin.sgm[sg] = make_float2(vr, vp);
+          if (lane < nus && sg < a.nseg) st.fin.sgm[sg] = make_float2(vr, vp);
           if (lane == 31) {
             sh.um[0][0] = ir;
             sh.um[1][0] = ip;
@@ -1961,6 +1973,19 @@ VocabArgs base_args(const void *target, const void *draft, int64_t seq_stride, i
   return a;
 }
 
+// The device's SM count (queried once per device; 148 when it cannot be read).
+int vocab_num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // Rows read per position: target rows 0..ntarget-1 and draft rows 0..ndraft-1
 // (slots ordered by pair: target j, then draft j); `topf`: the draft rows
 // build their top-F_j lists.  Call after the do_* flags are set.
@@ -1989,7 +2014,29 @@ void set_rows(VocabArgs &a, int ntarget, int ndraft, bool topf) {
     }
   }
   a.nslots = n;
-  if (a.greedy) a.nunits = 1;  // no residual pass: one finishing unit per sequence
+  a.unit_sub = 1;
+  if (a.greedy) {
+    a.nunits = 1;  // no residual pass: one finishing unit per sequence
+  } else {
+    // residual units of as many groups of kResSeg segments as keep the
+    // residual grid near one wave of resident units (five per SM): small
+    // batches keep one group per unit (the pass spread widest), large ones
+    // fewer, fatter units (fewer waves, tickets and waits)
+    const long groups = (a.nseg + kResSeg - 1) / kResSeg;
+    const long per = a.do_analytics ? (a.K > 0 ? a.K : 1) : 1;
+    const long work = static_cast<long>(a.B) * per * groups;
+    // the analytics grid (every pair of every sequence) may take two waves
+    const long slots = (a.do_analytics ? 10L : 5L) * vocab_num_sms();
+    long sub = (work + slots - 1) / slots;
+    if (sub > kMaxSub) sub = kMaxSub;
+    if (sub > groups) sub = groups;
+    if (sub < 1) sub = 1;
+    // the same number of units with their groups spread evenly
+    const long nu = (groups + sub - 1) / sub;
+    sub = (groups + nu - 1) / nu;
+    a.unit_sub = static_cast<int>(sub);
+    a.nunits = static_cast<int>((groups + sub - 1) / sub);
+  }
 }
 
 // Optional timing hook (ssd_set_timing_events): events recorded around the

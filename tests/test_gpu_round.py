@@ -295,3 +295,34 @@ def test_pipelined_rounds_back_to_back():
         assert g["status"][0] == 0
         compare_round(inp, g, report=rep)
     assert rep.compared == 4 * 32 + 3 * 5
+
+
+def test_rounds_on_several_streams():
+    """Independent rounds issued round-robin on four streams, pipelined on each
+    (the bench's schedule), so that rounds of different streams run at once:
+    every round equals the oracle."""
+    from parity import collect_round, enqueue_round, prepare_round
+    spec = w.llama3_round(T=1.0)
+    inps = [w.make_round(spec, seed=60 + i) for i in range(6)]
+    small = w.RoundSpec(B=7, K=4, V=9000, dtype="bf16", recipe="zipf", T=1.0, C=0.25,
+                        F=(4, 2, 1, 1, 1), draft_noise=1.0, name="streams-small")
+    inps += [w.make_round(small, seed=70 + i) for i in range(6)]
+    prepared = [prepare_round(inp) for inp in inps]
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    for st in streams:
+        st.wait_stream(cur)
+    launched = []
+    for q, (inp, o) in enumerate(zip(inps, prepared)):
+        with torch.cuda.stream(streams[q % 4]):
+            launched.append(enqueue_round(inp, o, pipelined=True))
+    for st in streams:
+        cur.wait_stream(st)
+    torch.cuda.synchronize()
+    rep = Report()
+    for inp, o in zip(inps, launched):
+        g = collect_round(o)
+        assert g["status"][0] == 0
+        compare_round(inp, g, report=rep)
+    assert rep.compared == 6 * 32 + 6 * 7
