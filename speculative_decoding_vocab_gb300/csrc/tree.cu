@@ -152,10 +152,10 @@ SSD_DEV float bonus_w(const Dist &D, float zt, float zd, int idx, int n, float A
   return n == 0 ? p : resid_w(p, D.q(zd, idx), A);
 }
 
-// Thread 0 of every CTA publishes sh.part[buf]; after the cluster barrier
-// thread 0 reads the cw parts in rank order, combines them with `comb` and
-// leaves the result in sh.res / sh.rkey for the CTA.
-// The part of CTA `rank` of the cluster.
+// Thread 0 of every CTA publishes sh.part[buf]; after the cluster barrier the
+// CTA copies the cw parts into its own shared memory (cluster_combine) and
+// thread 0 combines them in rank order with `comb`, leaving the result in
+// sh.res / sh.rkey for the CTA.
 // The parts of the cluster's CTAs, copied into this CTA's shared memory.
 struct Peers {
   const Part *p;

@@ -27,8 +27,9 @@
 //            from L2), draws d_{j+1} from the Saguaro weights (segment, block,
 //            then one block read again), takes p(d), q'(d) and the position's
 //            verdict; at position K+1 it draws the bonus for full acceptance.
-//   k_resid  (verification at T > 0) units of 16 KiB of each row: the sequence's
-//            first rejected pair read again (from L2) for the block sums of
+//   k_resid  (verification at T > 0) units of 16 KiB of each row, or of up to
+//            eight times that when the batch is large (one wave of units): the
+//            sequence's first rejected pair read again (from L2) for the block sums of
 //            max(0, p - q'); the unit with the sequence's last ticket draws the
 //            bonus from them and writes the outputs and the cache lookup.  A
 //            sequence that needs no residual is finished by its first unit.
