@@ -135,6 +135,17 @@ struct Dist {
   SSD_DEV float q(float z, int idx) const {
     return greedy ? (idx == aq ? 1.f : 0.f) : __fmul_rn(ex2(__fmaf_rn(z, kT, -Rq)), invSq);
   }
+  // p and q of one element as a packed pair (per lane the roundings of p, q)
+  SSD_DEV void pq(float zt, float zd, int idx, float &pv, float &qv) const {
+    if (greedy) {
+      pv = idx == ap ? 1.f : 0.f;
+      qv = idx == aq ? 1.f : 0.f;
+      return;
+    }
+    float xt, xd;
+    unpack2(fma2(pack2(zt, zd), pack2(kT, kT), pack2(-Rp, -Rq)), xt, xd);
+    unpack2(mul2(pack2(ex2(xt), ex2(xd)), pack2(invSp, invSq)), pv, qv);
+  }
 };
 
 // The residual after n rejections at a node, r_{j+1} = max(0, r_j - q) / W_j
@@ -148,8 +159,10 @@ SSD_DEV float resid_w(float p, float q, float A) { return fmaxf(__fmaf_rn(-A, q,
 // The bonus's weight of element idx: p before any rejection (q is then not
 // computed), else the unnormalised residual.
 SSD_DEV float bonus_w(const Dist &D, float zt, float zd, int idx, int n, float A) {
-  const float p = D.p(zt, idx);
-  return n == 0 ? p : resid_w(p, D.q(zd, idx), A);
+  if (n == 0) return D.p(zt, idx);
+  float p, q;
+  D.pq(zt, zd, idx, p, q);
+  return resid_w(p, q, A);
 }
 
 // Thread 0 of every CTA publishes sh.part[buf]; after the cluster barrier the
@@ -362,8 +375,12 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
           E::unpack(sD[(warp + kTWarps * k) * 32 + lane], fd);
 #pragma unroll
           for (int e = 0; e < E::kVec; ++e) {
-            if (mt != NEG_INF) st = __fadd_rn(st, ex2(__fmaf_rn(ft[e], a.kT, -Rt)));
-            if (md != NEG_INF) sd = __fadd_rn(sd, ex2(__fmaf_rn(fd[e], a.kT, -Rd)));
+            // both rows' terms as one packed pair; a row without a finite
+            // maximum adds +0
+            float xt, xd;
+            unpack2(fma2(pack2(ft[e], fd[e]), pack2(a.kT, a.kT), pack2(-Rt, -Rd)), xt, xd);
+            const float et = mt != NEG_INF ? ex2(xt) : 0.f, ed = md != NEG_INF ? ex2(xd) : 0.f;
+            unpack2(add2(pack2(st, sd), pack2(et, ed)), st, sd);
           }
         }
       }
@@ -445,7 +462,9 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
         const int i0 = (32 * (static_cast<int>(rank) * kCtaBlocks + warp + kTWarps * k) + lane) * E::kVec;
 #pragma unroll
         for (int e = 0; e < E::kVec; ++e) {
-          s = __fadd_rn(s, resid_w(D.p(ft[e], i0 + e), D.q(fd[e], i0 + e), An));
+          float p, q;
+          D.pq(ft[e], fd[e], i0 + e, p, q);
+          s = __fadd_rn(s, resid_w(p, q, An));
         }
       }
       s = warp_sum(s);

@@ -430,7 +430,9 @@ SSD_DEV WResid resid_weights(const VocabArgs &a, const PairRec &r, int F) {
   const float sN = __fmul_rn(r.gs[kDft], r.N);
   w.f1 = __frcp_rn(sN);
   w.fC = __fdiv_rn(a.C, sN);
-  w.S = F > 0;
+  // at C = 1 both weights are the correctly rounded 1 / sN: the membership
+  // test would not change a weight, so it is skipped
+  w.S = F > 0 && a.C < 1.f;
   w.keyF = r.keyF;
   w.vF = cand_val(r.keyF);
   return w;
@@ -1417,10 +1419,13 @@ SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr
 #pragma unroll
         for (int e = 0; e < E::kVec; ++e) {
           if (i0 + e < a.V) {
-            const float p = wr.p(ft[e]), q = wr.q(fd[e], i0 + e);
+            // wr.p and wr.q as one packed pair: per lane the same roundings
+            float xt, xd, p, q;
+            unpack2(fma2(pack2(ft[e], fd[e]), pack2(wr.kT, wr.kT), pack2(-wr.Mtk, -wr.Mdk)), xt, xd);
+            const float fq = (wr.S && in_set(fd[e], i0 + e, wr.vF, wr.keyF)) ? wr.fC : wr.f1;
+            unpack2(mul2(pack2(ex2(xt), ex2(xd)), pack2(wr.inv_st, fq)), p, q);
             const float r = __fsub_rn(p, q);
-            rs = __fadd_rn(rs, r > 0.f ? r : 0.f);
-            ps = __fadd_rn(ps, p);
+            unpack2(add2(pack2(rs, ps), pack2(r > 0.f ? r : 0.f, p)), rs, ps);
             if (kMins) mn = __fadd_rn(mn, fminf(p, q));
           }
         }
