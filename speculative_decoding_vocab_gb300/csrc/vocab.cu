@@ -509,6 +509,138 @@ SSD_DEV int warp_find(const VocabArgs &a, const char *rowT, const char *rowD, in
 // ===========================================================================
 // k_stats: one warp per segment of a row
 // ===========================================================================
+// One warp: the statistics of segment sg of a row, specialised by what the
+// row kind records (KK block maximum keys, KB block sums, KA the argmax):
+// each kind runs code without the other kinds' paths.
+template <class E, bool KK, bool KB, bool KA>
+SSD_DEV void stats_segment(const VocabArgs &a, const RowSlot &rs, int sg, int slot, int b) {
+  const int lane = threadIdx.x & 31;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const char *row = row_ptr(a, rs.tensor, b, rs.row, E::kSize);
+  const int v0 = sg * kSegVec;
+  // every load of the segment in flight at once
+  uint4 w[kSegBlocks];
+#pragma unroll
+  for (int k = 0; k < kSegBlocks; ++k) {
+    const int v = v0 + 32 * k + lane;
+    w[k] = (v < a.nfull) ? ld_stream(row + static_cast<int64_t>(v) * 16) : neg_inf_vec<E>();
+  }
+  if (a.nvec > a.nfull && a.nfull >= v0 && a.nfull < v0 + kSegVec && lane == ((a.nfull - v0) & 31)) {
+    const int kk = (a.nfull - v0) >> 5;  // the row's partial last vector
+    const uint4 t = row_vec<E>(a, row, a.nfull);
+#pragma unroll
+    for (int k = 0; k < kSegBlocks; ++k)
+      if (k == kk) w[k] = t;
+  }
+  // pass 1: maxima (bf16: packed), block maximum keys (lane k < 8 keeps
+  // block k's), the argmax's vector
+  uint32_t bk = 0u;
+  float m1 = NEG_INF;
+  int k1 = -1;
+  if constexpr (E::kSize == 2) {
+    // a segment wholly inside the row needs no validity checks (warp-uniform)
+    const bool full = v0 + kSegVec <= a.nvec;
+    uint32_t mm = 0xFF80FF80u;
+#pragma unroll
+    for (int k = 0; k < kSegBlocks; ++k) {
+      const uint32_t t = bmax2(bmax2(w[k].x, w[k].y), bmax2(w[k].z, w[k].w));
+      mm = bmax2(mm, t);
+      if (KK) {
+        // the vector maximum's key from its bf16 bits: with the maximum in
+        // both halves, negative values flipped and the others' sign bit set
+        // give the upper half of the order-preserving key of its float value
+        // (the lower half follows the upper one and is masked off when stored)
+        const uint32_t m2 = bmax2(t, __byte_perm(t, 0, 0x1032));
+        uint32_t key = m2 ^ (static_cast<uint32_t>(static_cast<int32_t>(m2) >> 31) | 0x80000000u);
+        if (!full && v0 + 32 * k + lane >= a.nvec) key = 0u;
+        key = __reduce_max_sync(0xffffffffu, key);
+        if (lane == k) bk = key;
+      }
+      if (KA) {
+        const float vm = fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
+        const bool valid = full || v0 + 32 * k + lane < a.nvec;
+        if (valid && (vm > m1 || k1 < 0)) {  // strictly larger: the first vector among equal maxima
+          m1 = fmaxf(m1, vm);
+          k1 = k;
+        }
+      }
+    }
+    if (!KA) m1 = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
+  } else {
+#pragma unroll
+    for (int k = 0; k < kSegBlocks; ++k) {
+      const float vm = vec_max<E>(w[k]);
+      const bool valid = v0 + 32 * k + lane < a.nvec;
+      if (KK) {
+        const uint32_t key = __reduce_max_sync(0xffffffffu, valid ? f2ord(vm) : 0u);
+        if (lane == k) bk = key;
+      }
+      if (valid && (vm > m1 || k1 < 0)) {
+        m1 = fmaxf(m1, vm);
+        k1 = k;
+      }
+    }
+  }
+  const float wm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(m1)));
+  int wa = v0 * E::kVec;  // the segment's first index unless the argmax is tracked
+  if (KA) {
+    int idx = kNone;
+    if (k1 >= 0 && m1 == wm) {
+      uint4 wk = w[0];
+#pragma unroll
+      for (int k = 1; k < kSegBlocks; ++k)
+        if (k == k1) wk = w[k];
+      float f[E::kVec];
+      E::unpack(wk, f);
+#pragma unroll
+      for (int e = E::kVec - 1; e >= 0; --e)
+        if (f[e] == wm) idx = (v0 + 32 * k1 + lane) * E::kVec + e;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+    wa = (idx == kNone) ? v0 * E::kVec : idx;
+  }
+  // pass 2: sums of 2^(z kT - fl(wm kT)), two elements per packed FMA / ADD;
+  // per block the lane's part in the association of lane_sum
+  float ws = 0.f, bsv = 0.f, wt = 0.f;
+  if (!a.greedy && wm != NEG_INF) {
+    const float Mk = __fmul_rn(wm, a.kT);
+    const uint64_t k2 = pack2(a.kT, a.kT), m2 = pack2(-Mk, -Mk);
+    uint64_t acc = pack2(0.f, 0.f);
+    float pr[kSegBlocks];
+#pragma unroll
+    for (int k = 0; k < kSegBlocks; ++k) {
+      uint64_t accj = 0;
+#pragma unroll
+      for (int h = 0; h < E::kPairs; ++h) {
+        float x0, x1;
+        unpack2(fma2(E::pair(w[k], h), k2, m2), x0, x1);
+        const uint64_t e2 = pack2(ex2(x0), ex2(x1));
+        accj = (h == 0) ? e2 : add2(accj, e2);
+      }
+      acc = add2(acc, accj);
+      float lo, hi;
+      unpack2(accj, lo, hi);
+      pr[k] = __fadd_rn(lo, hi);
+    }
+    if (KB) {
+      bsv = warp_block_sums(pr);
+      // lane k < 8 takes block k's sum; their total by a scan (warp_runs over 8 masses)
+      const float bk8 = __shfl_sync(0xffffffffu, bsv, (lane & 7) * 4);
+      wt = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? bk8 : 0.f), 31);
+    }
+    float lo, hi;
+    unpack2(acc, lo, hi);
+    ws = warp_sum(__fadd_rn(lo, hi));
+  }
+  const size_t si = slot_index(a, b, slot);
+  if (lane == 0)
+    reinterpret_cast<int4 *>(a.seg)[si * a.nseg + sg] =
+        make_int4(__float_as_int(wm), __float_as_int(ws), wa, __float_as_int(wt));
+  if (KK && lane < kSegBlocks) a.bkey[si * a.nblk + sg * kSegBlocks + lane] = E::kSize == 2 ? bk & 0xFFFF0000u : bk;
+  if (KB && (lane & 3) == 0) a.bsum[si * a.nblk + sg * kSegBlocks + (lane >> 2)] = bsv;
+}
+
 template <class E>
 __global__ void __launch_bounds__(kStatWarps * 32, 8) k_stats(const __grid_constant__ VocabArgs a) {
   // k_pair may start launching once every CTA of this grid has started
@@ -520,134 +652,21 @@ __global__ void __launch_bounds__(kStatWarps * 32, 8) k_stats(const __grid_const
   if (a.ready && a.hits && a.do_lookup && a.b0 == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
       threadIdx.x == 0)
     *a.hits = 0u;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5;
   const int sg = static_cast<int>(blockIdx.x) * kStatWarps + warp;
   const int slot = static_cast<int>(blockIdx.y);
   const int b = a.b0 + static_cast<int>(blockIdx.z);
   const RowSlot rs = a.slot[slot];
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  if (sg < a.nseg) {
-    const char *row = row_ptr(a, rs.tensor, b, rs.row, E::kSize);
-    const int v0 = sg * kSegVec;
-    // every load of the segment in flight at once
-    uint4 w[kSegBlocks];
-#pragma unroll
-    for (int k = 0; k < kSegBlocks; ++k) {
-      const int v = v0 + 32 * k + lane;
-      w[k] = (v < a.nfull) ? ld_stream(row + static_cast<int64_t>(v) * 16) : neg_inf_vec<E>();
-    }
-    if (a.nvec > a.nfull && a.nfull >= v0 && a.nfull < v0 + kSegVec && lane == ((a.nfull - v0) & 31)) {
-      const int kk = (a.nfull - v0) >> 5;  // the row's partial last vector
-      const uint4 t = row_vec<E>(a, row, a.nfull);
-#pragma unroll
-      for (int k = 0; k < kSegBlocks; ++k)
-        if (k == kk) w[k] = t;
-    }
-    // pass 1: maxima (bf16: packed), block maximum keys (lane k < 8 keeps
-    // block k's), the argmax's vector
-    uint32_t bk = 0u;
-    float m1 = NEG_INF;
-    int k1 = -1;
-    if constexpr (E::kSize == 2) {
-      // a segment wholly inside the row needs no validity checks (warp-uniform)
-      const bool full = v0 + kSegVec <= a.nvec;
-      uint32_t mm = 0xFF80FF80u;
-#pragma unroll
-      for (int k = 0; k < kSegBlocks; ++k) {
-        const uint32_t t = bmax2(bmax2(w[k].x, w[k].y), bmax2(w[k].z, w[k].w));
-        mm = bmax2(mm, t);
-        if (rs.keys) {
-          // the vector maximum's key from its bf16 bits: the upper half of the
-          // order-preserving key of its float value (the lower half is not needed)
-          const uint32_t h = bmax2(t, __byte_perm(t, 0, 0x1032)) & 0xFFFFu;
-          uint32_t key = ((h & 0x8000u) ? (h ^ 0xFFFFu) : (h | 0x8000u)) << 16;
-          if (!full && v0 + 32 * k + lane >= a.nvec) key = 0u;
-          key = __reduce_max_sync(0xffffffffu, key);
-          if (lane == k) bk = key;
-        }
-        if (rs.arg) {
-          const float vm = fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xFFFF0000u));
-          const bool valid = full || v0 + 32 * k + lane < a.nvec;
-          if (valid && (vm > m1 || k1 < 0)) {  // strictly larger: the first vector among equal maxima
-            m1 = fmaxf(m1, vm);
-            k1 = k;
-          }
-        }
-      }
-      if (!rs.arg) m1 = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xFFFF0000u));
-    } else {
-#pragma unroll
-      for (int k = 0; k < kSegBlocks; ++k) {
-        const float vm = vec_max<E>(w[k]);
-        const bool valid = v0 + 32 * k + lane < a.nvec;
-        if (rs.keys) {
-          const uint32_t key = __reduce_max_sync(0xffffffffu, valid ? f2ord(vm) : 0u);
-          if (lane == k) bk = key;
-        }
-        if (valid && (vm > m1 || k1 < 0)) {
-          m1 = fmaxf(m1, vm);
-          k1 = k;
-        }
-      }
-    }
-    const float wm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(m1)));
-    int wa = v0 * E::kVec;  // the segment's first index unless the argmax is tracked
-    if (rs.arg) {
-      int idx = kNone;
-      if (k1 >= 0 && m1 == wm) {
-        uint4 wk = w[0];
-#pragma unroll
-        for (int k = 1; k < kSegBlocks; ++k)
-          if (k == k1) wk = w[k];
-        float f[E::kVec];
-        E::unpack(wk, f);
-#pragma unroll
-        for (int e = E::kVec - 1; e >= 0; --e)
-          if (f[e] == wm) idx = (v0 + 32 * k1 + lane) * E::kVec + e;
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-      wa = (idx == kNone) ? v0 * E::kVec : idx;
-    }
-    // pass 2: sums of 2^(z kT - fl(wm kT)), two elements per packed FMA / ADD;
-    // per block the lane's part in the association of lane_sum
-    float ws = 0.f, bsv = 0.f, wt = 0.f;
-    if (!a.greedy && wm != NEG_INF) {
-      const float Mk = __fmul_rn(wm, a.kT);
-      const uint64_t k2 = pack2(a.kT, a.kT), m2 = pack2(-Mk, -Mk);
-      uint64_t acc = pack2(0.f, 0.f);
-      float pr[kSegBlocks];
-#pragma unroll
-      for (int k = 0; k < kSegBlocks; ++k) {
-        uint64_t accj = 0;
-#pragma unroll
-        for (int h = 0; h < E::kPairs; ++h) {
-          float x0, x1;
-          unpack2(fma2(E::pair(w[k], h), k2, m2), x0, x1);
-          const uint64_t e2 = pack2(ex2(x0), ex2(x1));
-          accj = (h == 0) ? e2 : add2(accj, e2);
-        }
-        acc = add2(acc, accj);
-        float lo, hi;
-        unpack2(accj, lo, hi);
-        pr[k] = __fadd_rn(lo, hi);
-      }
-      if (rs.blocks) {
-        bsv = warp_block_sums(pr);
-        // lane k < 8 takes block k's sum; their total by a scan (warp_runs over 8 masses)
-        const float bk8 = __shfl_sync(0xffffffffu, bsv, (lane & 7) * 4);
-        wt = __shfl_sync(0xffffffffu, warp_incl_scan(lane < kSegBlocks ? bk8 : 0.f), 31);
-      }
-      float lo, hi;
-      unpack2(acc, lo, hi);
-      ws = warp_sum(__fadd_rn(lo, hi));
-    }
-    const size_t si = slot_index(a, b, slot);
-    if (lane == 0)
-      reinterpret_cast<int4 *>(a.seg)[si * a.nseg + sg] =
-          make_int4(__float_as_int(wm), __float_as_int(ws), wa, __float_as_int(wt));
-    if (rs.keys && lane < kSegBlocks) a.bkey[si * a.nblk + sg * kSegBlocks + lane] = bk;
-    if (rs.blocks && (lane & 3) == 0) a.bsum[si * a.nblk + sg * kSegBlocks + (lane >> 2)] = bsv;
+  if (sg >= a.nseg) return;
+  switch ((rs.keys ? 1 : 0) | (rs.blocks ? 2 : 0) | (rs.arg ? 4 : 0)) {  // uniform per CTA
+    case 0: stats_segment<E, false, false, false>(a, rs, sg, slot, b); break;
+    case 1: stats_segment<E, true, false, false>(a, rs, sg, slot, b); break;
+    case 2: stats_segment<E, false, true, false>(a, rs, sg, slot, b); break;
+    case 3: stats_segment<E, true, true, false>(a, rs, sg, slot, b); break;
+    case 4: stats_segment<E, false, false, true>(a, rs, sg, slot, b); break;
+    case 5: stats_segment<E, true, false, true>(a, rs, sg, slot, b); break;
+    case 6: stats_segment<E, false, true, true>(a, rs, sg, slot, b); break;
+    default: stats_segment<E, true, true, true>(a, rs, sg, slot, b); break;
   }
 }
 
