@@ -520,10 +520,16 @@ SSD_DEV void stats_segment(const VocabArgs &a, const RowSlot &rs, int sg, int sl
   const int v0 = sg * kSegVec;
   // every load of the segment in flight at once
   uint4 w[kSegBlocks];
+  if (v0 + kSegVec <= a.nfull) {  // warp-uniform: every vector of the segment is whole
+    const char *p = row + static_cast<int64_t>(v0 + lane) * 16;
 #pragma unroll
-  for (int k = 0; k < kSegBlocks; ++k) {
-    const int v = v0 + 32 * k + lane;
-    w[k] = (v < a.nfull) ? ld_stream(row + static_cast<int64_t>(v) * 16) : neg_inf_vec<E>();
+    for (int k = 0; k < kSegBlocks; ++k) w[k] = ld_stream(p + 512 * k);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kSegBlocks; ++k) {
+      const int v = v0 + 32 * k + lane;
+      w[k] = (v < a.nfull) ? ld_stream(row + static_cast<int64_t>(v) * 16) : neg_inf_vec<E>();
+    }
   }
   if (a.nvec > a.nfull && a.nfull >= v0 && a.nfull < v0 + kSegVec && lane == ((a.nfull - v0) & 31)) {
     const int kk = (a.nfull - v0) >> 5;  // the row's partial last vector
