@@ -225,7 +225,9 @@ SSD_DEV void block_runs(const float *bsum, int lane, float (&bs)[4], float (&run
   for (int j = 0; j < 4; ++j) run[j] = __fadd_rn(excl, r[j]);
 }
 
-template <class E>
+// G: T == 0 (one-hot distributions), a template argument so that the
+// per-element weights carry no test of it
+template <class E, bool G>
 __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
   __shared__ TreeSh sh;
   extern __shared__ uint4 stage[];  // [2][kCtaBlocks * 32]: this CTA's vectors of the target, draft row
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
   float Ar = 0.f, Br = 1.f;  // the residual at this node: max(0, p - Ar q) / Br
   Dist D;
   D.kT = a.kT;
-  D.greedy = a.greedy;
+  D.greedy = G;
   for (;;) {
     // the node's rows, into registers
     const int64_t off = static_cast<int64_t>(b) * a.seq_stride + static_cast<int64_t>(node + 1) * a.row_stride;
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kTT, 1) k_tree_walk(TreeArgs a) {
       }
     }
     // statistics of p and q
-    if (a.greedy) {
+    if (G) {
       uint64_t kp = 0, kq = 0;
 #pragma unroll 1
       for (int k = 0; k < kBPW; ++k) {
@@ -671,7 +673,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 template <class E>
 cudaError_t launch_tree(const TreeArgs &a, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(k_tree_walk<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kern)(TreeArgs) = a.greedy ? k_tree_walk<E, true> : k_tree_walk<E, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(2 * kRowStage));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -686,7 +689,7 @@ cudaError_t launch_tree(const TreeArgs &a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_tree_walk<E>, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
