@@ -292,7 +292,9 @@ struct AttnCfg {
 // int entries of one pipeline's block-table slice (16-byte multiple)
 __host__ __device__ inline int attn_tab_stride(int tiles_per_split) { return (tiles_per_split * kTilePages + 3) & ~3; }
 
-template <int D, int MT, int PL, int RA, int NPB>
+// LX: the exact row sums are kept (the log-sum-exp output); without it only
+// the sums of the bf16 P that normalise O are.
+template <int D, int MT, int PL, int RA, int NPB, bool LX>
 __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
     k_branch_attn_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ AttnArgs a) {
@@ -604,7 +606,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
       if (grow) {
         if (rescale) {
           l2 = fma2(l2, pack2(f, f), pack2(0.f, 0.f));
-          lx2 = fma2(lx2, pack2(f, f), pack2(0.f, 0.f));
+          if constexpr (LX) lx2 = fma2(lx2, pack2(f, f), pack2(0.f, 0.f));
         }
         m_used = tmax;
       }
@@ -652,12 +654,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, PL, RA, NPB>::kThreads, 1)
           p1 = ex2(x1);
         }
         const uint32_t pb = cvt_bf16x2(p0, p1);
-        lxa[h & 1] = add2(lxa[h & 1], pack2(p0, p1));
+        if constexpr (LX) lxa[h & 1] = add2(lxa[h & 1], pack2(p0, p1));
         la[h & 1] = add2(la[h & 1], pack2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)));
         pk[h] = pb;
       }
       l2 = add2(l2, add2(la[0], la[1]));
-      lx2 = add2(lx2, add2(lxa[0], lxa[1]));
+      if constexpr (LX) lx2 = add2(lx2, add2(lxa[0], lxa[1]));
       if (kEarlyExp && !wait_p_and_rescale()) {
         s_abort = 1;
         break;
@@ -885,7 +887,7 @@ bool attention_fits(const AttnArgs &a) {
   static const int room = [] {
     cudaFuncAttributes fa;
     int dev = 0, optin = 0;
-    if (cudaFuncGetAttributes(&fa, k_branch_attn_tc<D, MT, PL, RA, NPB>) != cudaSuccess ||
+    if (cudaFuncGetAttributes(&fa, k_branch_attn_tc<D, MT, PL, RA, NPB, true>) != cudaSuccess ||
         cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return 227 * 1024 - 4096;
@@ -897,14 +899,21 @@ bool attention_fits(const AttnArgs &a) {
 template <int D, int MT, int PL, int RA = kRows, int NPB = 2>
 cudaError_t launch_attention(const CUtensorMap &kmap, const CUtensorMap &vmap, const AttnArgs &a,
                              cudaStream_t cs) {
+  // the exact sums only when the log-sum-exp is written (at d = 64 the
+  // two-pipeline kernel keeps them: measured faster with both sums)
+  void (*kern)(const CUtensorMap, const CUtensorMap, const AttnArgs);
+  if constexpr (D == 64)
+    kern = k_branch_attn_tc<D, MT, PL, RA, NPB, true>;
+  else
+    kern = a.lse ? k_branch_attn_tc<D, MT, PL, RA, NPB, true> : k_branch_attn_tc<D, MT, PL, RA, NPB, false>;
   using CF = AttnCfg<D, MT, PL, RA, NPB>;
   const int smem = attention_smem<D, MT, PL, RA, NPB>(a);
   if (!attention_fits<D, MT, PL, RA, NPB>(a)) return cudaErrorInvalidValue;
   cudaError_t e =
-      cudaFuncSetAttribute(k_branch_attn_tc<D, MT, PL, RA, NPB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.items + PL - 1) / PL);
-  k_branch_attn_tc<D, MT, PL, RA, NPB><<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
+  kern<<<grid, CF::kThreads, smem, cs>>>(kmap, vmap, a);
   e = cudaGetLastError();
   if (e == cudaSuccess && a.splits > 1) {
     k_attn_combine<D><<<dim3(a.B * a.Hkv, a.mtiles), 128, 0, cs>>>(a);
