@@ -1422,8 +1422,9 @@ SSD_DEV void stage_block1(const VocabArgs &a, int b, int j, int g, int w, ResSta
 // q') and p over its elements in order, the lanes by a butterfly: the
 // half-segment masses of group g into sh.seg[g kWarps + warp].  kMins: *mn,
 // *mx (every lane) = the warp's sums of min(p, q') and of max(0, p - q') over
-// the unit.
-template <class E, bool kMins>
+// the unit.  kS: the call has C < 1, so the draft's weights may test membership
+// in the top-F set (at C = 1 the unit pass has no code for it).
+template <class E, bool kMins, bool kS>
 SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr, ResSh &sh, ResStage &st,
                        float *mn_out, float *mx_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1447,7 +1448,7 @@ SSD_DEV void unit_pass(const VocabArgs &a, int b, int j, int u, const WResid &wr
             // wr.p and wr.q as one packed pair: per lane the same roundings
             float xt, xd, p, q;
             unpack2(fma2(pack2(ft[e], fd[e]), pack2(wr.kT, wr.kT), pack2(-wr.Mtk, -wr.Mdk)), xt, xd);
-            const float fq = (wr.S && in_set(fd[e], i0 + e, wr.vF, wr.keyF)) ? wr.fC : wr.f1;
+            const float fq = (kS && wr.S && in_set(fd[e], i0 + e, wr.vF, wr.keyF)) ? wr.fC : wr.f1;
             unpack2(mul2(pack2(ex2(xt), ex2(xd)), pack2(wr.inv_st, fq)), p, q);
             const float r = __fsub_rn(p, q);
             unpack2(add2(pack2(rs, ps), pack2(r > 0.f ? r : 0.f, p)), rs, ps);
@@ -1619,8 +1620,8 @@ SSD_DEV void reset_ready(const VocabArgs &a, int b) {
 }
 
 // 48 registers: every unit CTA then fits beside the pair kernel's CTAs, so no
-// sequence's units wait for the pair grid to drain before they start.
-template <class E>
+// sequence's units wait for the pair grid to drain before they start.  CS: C < 1.
+template <class E, bool CS>
 __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
   __shared__ ResSh sh;
   extern __shared__ __align__(16) uint8_t res_smem[];
@@ -1655,7 +1656,7 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
         if (tid == 0) sh.rec[0] = a.rec[static_cast<size_t>(b) * (K + 1) + j];
         __syncthreads();
         const WResid wr = resid_weights(a, sh.rec[0], a.Fs[j]);
-        unit_pass<E, true>(a, b, j, u, wr, sh, st, &mn, &mx);
+        unit_pass<E, true, CS>(a, b, j, u, wr, sh, st, &mn, &mx);
         __syncthreads();  // sh.seg is overwritten below
       }
       if (lane == 0) {
@@ -1758,7 +1759,7 @@ __global__ void __maxnreg__(48) k_resid(const __grid_constant__ VocabArgs a) {
       // the residual of the first rejected position: this unit's block sums
       const WResid wr = resid_weights(a, sh.rec[acc], a.Fs[acc]);
       float mn, mx;
-      unit_pass<E, false>(a, b, acc, u, wr, sh, st, &mn, &mx);
+      unit_pass<E, false, CS>(a, b, acc, u, wr, sh, st, &mn, &mx);
       __syncthreads();
       if (a.trace && tid == 0) sh.mk[4] = now_ns();
       if (warp == 0) {
@@ -2117,7 +2118,9 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(k_pair<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(pair_smem_bytes(kMaxSeg, kMaxSeg * kSegBlocks)));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_resid<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(ResStage)));
+      e = cudaFuncSetAttribute(k_resid<E, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(ResStage)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_resid<E, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(ResStage)));
     if (e != cudaSuccess) return e;
     g_attr_set[ti][dev / 64].fetch_or(bit);
   }
@@ -2161,7 +2164,8 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   if (g_ev_after) cudaEventRecord(g_ev_after, s);
   e = launch_dependent(k_pair<E>, static_cast<unsigned>(n2), psmem, s, a);
   if (e != cudaSuccess || n3 == 0) return e;
-  return launch_dependent(k_resid<E>, static_cast<unsigned>(n3), sizeof(ResStage), s, a);
+  return launch_dependent(a.C < 1.f ? k_resid<E, true> : k_resid<E, false>, static_cast<unsigned>(n3), sizeof(ResStage), s,
+                          a);
 }
 
 cudaError_t launch_any(ssd_dtype_t dt, VocabArgs &a, cudaStream_t s) {
