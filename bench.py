@@ -204,7 +204,7 @@ def capture_graphs(calls, device):
     return graphs
 
 
-NSTREAMS = 4          # streams that independent rounds are issued on, round-robin
+NSTREAMS = 6          # streams that independent rounds are issued on, round-robin
 NBUF = 2 * NSTREAMS   # output/workspace sets: rounds in flight together never share one
 
 

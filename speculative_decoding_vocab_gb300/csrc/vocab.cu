@@ -960,7 +960,9 @@ SSD_DEV int row_draw(const VocabArgs &a, const SegRec *sr, float rowMk, const fl
   return d;
 }
 
-template <class E>
+// CS: C < 1 (the draft's draws weighted by the top-F set); at C = 1 the kernel
+// has no code for the weighted draw.
+template <class E, bool CS>
 __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ VocabArgs a) {
   // k_resid (if any) may start launching once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -984,10 +986,10 @@ __global__ void __launch_bounds__(kThreads) k_pair(const __grid_constant__ Vocab
   const bool tested = a.do_verify && j < K;
   const bool bonus_p = a.do_verify && j == K && !greedy;
   // C < 1 weights the draft's draw by S: it waits for the top-F list
-  const bool weighted = !greedy && sampled && a.C < 1.f && F > 0;
+  const bool weighted = CS && !greedy && sampled && F > 0;
   // with C = 1 (or greedy) the record does not depend on S (N = 1, and in or
   // out of S the draft's weight is the same): it is published before the top-F
-  const bool early = a.ready != nullptr && (greedy || a.C >= 1.f);
+  const bool early = a.ready != nullptr && (greedy || !CS);
   const char *rowT = row_ptr(a, 0, b, j, E::kSize);
   const char *rowD = row_ptr(a, 1, b, j, E::kSize);
   // the counters k_resid takes tickets on and the hit count start at zero
@@ -2115,8 +2117,11 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   const size_t psmem = pair_smem_bytes(a.nseg, a.nblk);
   const uint64_t bit = 1ull << (dev % 64);
   if (!(g_attr_set[ti][dev / 64].load() & bit)) {
-    e = cudaFuncSetAttribute(k_pair<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_pair<E, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(pair_smem_bytes(kMaxSeg, kMaxSeg * kSegBlocks)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_pair<E, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(pair_smem_bytes(kMaxSeg, kMaxSeg * kSegBlocks)));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_resid<E, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sizeof(ResStage)));
     if (e == cudaSuccess)
@@ -2162,7 +2167,7 @@ cudaError_t launch_vocab(VocabArgs &a, cudaStream_t s) {
   }
   a.b0 = 0;
   if (g_ev_after) cudaEventRecord(g_ev_after, s);
-  e = launch_dependent(k_pair<E>, static_cast<unsigned>(n2), psmem, s, a);
+  e = launch_dependent(a.C < 1.f ? k_pair<E, true> : k_pair<E, false>, static_cast<unsigned>(n2), psmem, s, a);
   if (e != cudaSuccess || n3 == 0) return e;
   return launch_dependent(a.C < 1.f ? k_resid<E, true> : k_resid<E, false>, static_cast<unsigned>(n3), sizeof(ResStage), s,
                           a);
