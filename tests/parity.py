@@ -252,8 +252,9 @@ def compare_round(inp: w.RoundInputs, g: dict, T=None, C=None, seqs=None, report
     return rep
 
 
-def gpu_attention(ai: w.AttnInputs, dev="cuda", use_ws=True):
-    """Run ssd_branch_attention; without a workspace the keys are not split."""
+def gpu_attention(ai: w.AttnInputs, dev="cuda", use_ws=True, want_lse=True):
+    """Run ssd_branch_attention; without a workspace the keys are not split;
+    without want_lse no log-sum-exp output is passed (returned lse all NaN)."""
     q = to_dev(ai.q, dev)
     out = torch.full_like(q, float("nan"))
     lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
@@ -263,6 +264,6 @@ def gpu_attention(ai: w.AttnInputs, dev="cuda", use_ws=True):
     ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev) if use_ws else None
     ssd.ssd_branch_attention(q, to_dev(ai.k_cache, dev), to_dev(ai.v_cache, dev),
                              to_dev(ai.block_table, dev), to_dev(ai.prefix_len, dev),
-                             to_dev(ai.parent, dev), out, lse=lse, status=status, ws=ws)
+                             to_dev(ai.parent, dev), out, lse=lse if want_lse else None, status=status, ws=ws)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), lse.cpu().numpy(), int(status.item())

@@ -55,6 +55,28 @@ def test_small_shapes(spec):
     _check(w.make_attention(spec, seed=11))
 
 
+@pytest.mark.parametrize("use_ws", [False, True], ids=["unsplit", "split"])
+@pytest.mark.parametrize("spec", [
+    w.AttnSpec(B=3, Hq=16, Hkv=1, d=128, L=77, tree="chain", n_chain=6, ragged_prefix=True),
+    w.AttnSpec(B=2, Hq=16, Hkv=2, d=128, L=3000, tree="chain", n_chain=8, ragged_prefix=True),
+    w.AttnSpec(B=2, Hq=8, Hkv=1, d=128, L=500, tree="fanout", K=4, F=(20, 4, 2, 1, 1), chain_len=4),
+    w.AttnSpec(B=2, Hq=4, Hkv=2, d=64, L=200, tree="fanout", K=3, F=(3, 2, 1, 1), chain_len=4),
+], ids=["d128-64rows", "d128-64rows-long", "d128-128rows", "d64"])
+def test_without_lse(spec, use_ws):
+    """A call without the log-sum-exp output (the d = 128 kernels then keep only
+    the bf16 row sums): O bit-identical to the call with it, and within the
+    tolerance of the oracle."""
+    ai = w.make_attention(spec, seed=17)
+    out_l, _, st_l = gpu_attention(ai, use_ws=use_ws)
+    out_n, lse_n, st_n = gpu_attention(ai, use_ws=use_ws, want_lse=False)
+    assert st_l == 0 and st_n == 0
+    assert np.isnan(lse_n).all()  # nothing was written to the buffer that was not passed
+    assert np.array_equal(out_n, out_l, equal_nan=True)
+    ref, _, _ = oracle.branch_attention(ai.q, ai.k_cache, ai.v_cache, ai.block_table, ai.prefix_len,
+                                        ai.parent, spec.Hkv)
+    assert np.abs(out_n - ref).max() <= ATOL
+
+
 @pytest.mark.parametrize("spec", [
     w.AttnSpec(B=2, Hq=4, Hkv=2, d=64, L=200, tree="chain", n_chain=128),
     w.AttnSpec(B=1, Hq=2, Hkv=1, d=128, L=90, tree="chain", n_chain=128, ragged_prefix=True),
